@@ -1,0 +1,199 @@
+"""Plain fp64 CPU oracle for one MLA decode step (naive and weight-absorbed).
+
+TEST INFRASTRUCTURE.  Only the tests, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import or run this module.  It shares no code
+with the CUDA library and imports nothing from it.  It is slow on purpose:
+every function is the plain definition written out with NumPy in float64, with
+no blocking, fusion or reordering beyond what the definition states.
+
+Sources (web pages, cited by title and section):
+
+* "Multi-Head Latent Attention" (Lior Sinai), section 2.1 "KV Caching / Theory":
+  decoding with a cache gives exactly the last column of full attention.
+* same page, section 3.1 "C cache": K and V are recovered from the cached
+  latent C^KV by W^UK and W^UV.
+* same page, section 3.3 "Absorption" and eq. 3.3.3: the per-head score
+  C^KV^T (W^UK^T q) and the output W^UV (C^KV z) need no decompressed K or V.
+* same page, section 3.6 "Decoupled RoPE": scores add a RoPE part
+  k^R . q^R, k^R is shared by all heads, and the sum is scaled by
+  1/sqrt(d_h + d_R).
+* same page, section 3.7 "Code": RoPE as a complex multiply of adjacent pairs
+  by cos + i sin of (position * theta_i), theta_i = base^(-2i/dim), positions
+  counted from 0.
+* "Deepseek V2 Lite Inference Engine in C", MLA notes: the fused row order
+  (kv_lora, k_rope) of kv_a_proj, and kv_b_proj's per-head interleaved
+  [k_nope ; v] row blocks, which the naive form below rebuilds.
+* "Transformer and KV Cache Basics", Engineering item 4: masked positions get
+  -inf before the softmax.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against facts
+that the pages and mathematics fix (closed forms, brute force, invariants).
+
+Array conventions (row-major, per sequence b):
+  cache[b, t, :d_c]  = c_kv row of token t;  cache[b, t, d_c:] = k_rope row (already rotated)
+  q_nope[b, h, :d_nope], q_rope[b, h, :d_rope]
+  w_uk[h, d, c]  (W^UK of head h, d_nope x d_c)   w_uv[h, e, c]  (W^UV of head h, d_v x d_c)
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+# ----------------------------------------------------------------------------- RoPE
+def rope_theta(d_rope: int, base: float) -> np.ndarray:
+    """theta_i = base^(-(2i)/d_rope), i = 0 .. d_rope/2 - 1 (Multi-Head Latent Attention, 3.7)."""
+    if d_rope % 2:
+        raise ValueError("RoPE needs an even width")
+    i = np.arange(d_rope // 2, dtype=np.float64)
+    return np.float64(base) ** (-(2.0 * i) / d_rope)
+
+
+def apply_rope(x: np.ndarray, pos, base: float) -> np.ndarray:
+    """Rotate adjacent pairs (x[2i], x[2i+1]) as the complex number x[2i] + i x[2i+1]
+    by exp(i * pos * theta_i) (Multi-Head Latent Attention, 3.7).
+
+    x: [..., d_rope]; pos: scalar or an array broadcastable to x.shape[:-1].
+    """
+    x = np.asarray(x, dtype=np.float64)
+    theta = rope_theta(x.shape[-1], base)
+    ang = np.asarray(pos, dtype=np.float64)[..., None] * theta
+    z = (x[..., 0::2] + 1j * x[..., 1::2]) * (np.cos(ang) + 1j * np.sin(ang))
+    out = np.empty_like(x)
+    out[..., 0::2] = z.real
+    out[..., 1::2] = z.imag
+    return out
+
+
+# ----------------------------------------------------------------------------- absorbed form
+def absorb_q(q_nope: np.ndarray, w_uk: np.ndarray) -> np.ndarray:
+    """q_abs[b,h,c] = sum_d q_nope[b,h,d] * w_uk[h,d,c]: the query contracted with W^UK
+    before it meets the cache (Multi-Head Latent Attention, 3.3; the right-to-left
+    order of the einsum quoted there)."""
+    return np.einsum("bhd,hdc->bhc", q_nope, w_uk)
+
+
+def softmax_stats(s: np.ndarray):
+    """Exact softmax over the last axis: returns (p, lse) with lse = log sum exp(s)."""
+    m = np.max(s, axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    z = np.sum(e, axis=-1, keepdims=True)
+    return e / z, (m + np.log(z))[..., 0]
+
+
+def decode_absorbed(q_nope, q_rope, w_uk, w_uv, cache, lengths, positions,
+                    scale: float, base: float):
+    """One decode step in weight-absorbed form, exact softmax, no splits.
+
+    Returns a dict of fp64 arrays: q_abs [B,H,d_c], q_pe [B,H,d_rope],
+    o_c [B,H,d_c] (latent output), lse [B,H] (natural log of the softmax
+    normaliser of the scaled scores), o [B,H,d_v], and p (list over b of [H,S_b]).
+    """
+    B, H, _ = q_nope.shape
+    d_c = w_uk.shape[2]
+    q_abs = absorb_q(q_nope, w_uk)
+    q_pe = apply_rope(q_rope, np.asarray(positions)[:, None], base)
+    o_c = np.zeros((B, H, d_c))
+    lse = np.full((B, H), -np.inf)
+    o = np.zeros((B, H, w_uv.shape[1]))
+    ps = []
+    for b in range(B):
+        n = int(lengths[b])
+        if n <= 0:
+            raise ValueError("a sequence with no cached rows has no softmax")
+        c = cache[b, :n, :d_c]          # [S_b, d_c]
+        kr = cache[b, :n, d_c:]         # [S_b, d_rope]
+        s = scale * (q_abs[b] @ c.T + q_pe[b] @ kr.T)     # [H, S_b]
+        p, lse[b] = softmax_stats(s)
+        o_c[b] = p @ c                                     # latent output, d_c per head
+        o[b] = np.einsum("hec,hc->he", w_uv, o_c[b])        # W^UV applied after attention
+        ps.append(p)
+    return dict(q_abs=q_abs, q_pe=q_pe, o_c=o_c, lse=lse, o=o, p=ps)
+
+
+# ----------------------------------------------------------------------------- naive form
+def kv_b_proj_from(w_uk: np.ndarray, w_uv: np.ndarray) -> np.ndarray:
+    """Fused up-projection with per-head interleaved row blocks [k_nope(h); v(h)]
+    ("Deepseek V2 Lite Inference Engine in C", MLA notes): shape [H*(d_nope+d_v), d_c]."""
+    H, d_nope, d_c = w_uk.shape
+    d_v = w_uv.shape[1]
+    w = np.empty((H, d_nope + d_v, d_c))
+    w[:, :d_nope] = w_uk
+    w[:, d_nope:] = w_uv
+    return w.reshape(H * (d_nope + d_v), d_c)
+
+
+def decode_naive(q_nope, q_rope, w_uk, w_uv, cache, lengths, positions,
+                 scale: float, base: float):
+    """One decode step without absorption: decompress every cached row into per-head
+    K and V through kv_b_proj, then standard multi-head attention with the decoupled
+    RoPE part concatenated (Multi-Head Latent Attention, 3.1 and 3.7; "Deepseek V2
+    Lite Inference Engine in C", "Use original weights").
+
+    Returns dict(o [B,H,d_v], p list of [H,S_b]).
+    """
+    B, H, d_nope = q_nope.shape
+    d_c = w_uk.shape[2]
+    d_v = w_uv.shape[1]
+    kvb = kv_b_proj_from(w_uk, w_uv)
+    q_pe = apply_rope(q_rope, np.asarray(positions)[:, None], base)
+    o = np.zeros((B, H, d_v))
+    ps = []
+    for b in range(B):
+        n = int(lengths[b])
+        c = cache[b, :n, :d_c]
+        kr = cache[b, :n, d_c:]
+        kv = (c @ kvb.T).reshape(n, H, d_nope + d_v)       # [S, H, 256]
+        k_nope, v = kv[..., :d_nope], kv[..., d_nope:]
+        Q = np.concatenate([q_nope[b], q_pe[b]], axis=-1)   # [H, 192]
+        K = np.concatenate([k_nope, np.broadcast_to(kr[:, None, :], (n, H, kr.shape[1]))],
+                           axis=-1)                          # [S, H, 192], k_rope shared
+        s = scale * np.einsum("hk,thk->ht", Q, K)
+        p, _ = softmax_stats(s)
+        o[b] = np.einsum("ht,the->he", p, v)
+        ps.append(p)
+    return dict(o=o, p=ps)
+
+
+def causal_attention_naive(q_nope_seq, q_rope_seq, w_uk, w_uv, cache_seq, scale, base):
+    """Full causal self-attention over one sequence of S tokens, every query row i
+    rotated at position i, future keys masked with -inf ("Transformer and KV Cache
+    Basics", item 4; Multi-Head Latent Attention, 2.1).  q_*_seq: [S,H,*];
+    cache_seq: [S,row].  Returns outputs [S,H,d_v]."""
+    S, H, d_nope = q_nope_seq.shape
+    d_c = w_uk.shape[2]
+    d_v = w_uv.shape[1]
+    kvb = kv_b_proj_from(w_uk, w_uv)
+    c, kr = cache_seq[:, :d_c], cache_seq[:, d_c:]
+    kv = (c @ kvb.T).reshape(S, H, d_nope + d_v)
+    k_nope, v = kv[..., :d_nope], kv[..., d_nope:]
+    q_pe = apply_rope(q_rope_seq, np.arange(S)[:, None], base)
+    Q = np.concatenate([q_nope_seq, q_pe], axis=-1)                       # [S,H,192]
+    K = np.concatenate([k_nope, np.broadcast_to(kr[:, None, :], (S, H, kr.shape[1]))], -1)
+    s = scale * np.einsum("ihk,jhk->hij", Q, K)                           # [H, S_q, S_k]
+    future = np.arange(S)[:, None] < np.arange(S)[None, :]
+    s = np.where(future[None], -np.inf, s)
+    p, _ = softmax_stats(s)
+    return np.einsum("hij,jhe->ihe", p, v)
+
+
+# ----------------------------------------------------------------------------- split-KV combine
+def split_decode_combine(q_abs, q_pe, cache_b, n: int, scale: float, chunk: int):
+    """Split-KV for one sequence: per chunk j of `chunk` rows compute the chunk's
+    normalised latent output o_j and lse_j, then merge with
+    L = log sum_j exp(lse_j), o_c = sum_j exp(lse_j - L) o_j.  An exact rewrite of
+    the softmax over all rows (used to check the combine arithmetic).
+    q_abs [H,d_c], q_pe [H,d_rope], cache_b [S,row].  Returns (o_c [H,d_c], lse [H])."""
+    d_c = q_abs.shape[1]
+    os_, ls_ = [], []
+    for t0 in range(0, n, chunk):
+        t1 = min(n, t0 + chunk)
+        c, kr = cache_b[t0:t1, :d_c], cache_b[t0:t1, d_c:]
+        s = scale * (q_abs @ c.T + q_pe @ kr.T)
+        p, l = softmax_stats(s)
+        os_.append(p @ c)
+        ls_.append(l)
+    lse = np.stack(ls_)                       # [J, H]
+    L = np.max(lse, axis=0) + np.log(np.sum(np.exp(lse - np.max(lse, axis=0)), axis=0))
+    w = np.exp(lse - L)                       # [J, H]
+    o_c = np.einsum("jh,jhc->hc", w, np.stack(os_))
+    return o_c, L

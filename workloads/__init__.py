@@ -1,0 +1,15 @@
+"""Seeded synthetic MLA decode workloads shared by the tests, the smoke check and the bench.
+
+Holds sizes and random draws only; no arithmetic of the method lives here.
+"""
+from .configs import (ALL_CONFIGS, BY_NAME, MlaConfig, TOL_BF16_MAX_ABS, TOL_BF16_REL_L2,
+                      TOL_F32_MAX_ABS, V2LITE_BF16_B4_S65536_LONG, V2LITE_BF16_B8_S4096,
+                      V2LITE_BF16_B64_RAGGED, V2LITE_F32_B1_S64, V3_BF16_H128_B32_S16384)
+from .generate import MlaInputs, make_inputs
+
+__all__ = [
+    "ALL_CONFIGS", "BY_NAME", "MlaConfig", "MlaInputs", "make_inputs",
+    "TOL_BF16_MAX_ABS", "TOL_BF16_REL_L2", "TOL_F32_MAX_ABS",
+    "V2LITE_F32_B1_S64", "V2LITE_BF16_B8_S4096", "V2LITE_BF16_B64_RAGGED",
+    "V3_BF16_H128_B32_S16384", "V2LITE_BF16_B4_S65536_LONG",
+]

@@ -1,0 +1,97 @@
+"""Seeded synthetic inputs for one MLA decode step.
+
+One CPU ``torch.Generator`` per call, seeded, with a fixed draw order:
+
+1. latent cache ``[B, S_max, d_c + d_rope]`` ~ N(0, 1)  (k_rope taken as already rotated)
+2. ``q_nope [B, H, d_nope]`` ~ N(0, 1)
+3. ``q_rope [B, H, d_rope]`` ~ N(0, 1)
+4. ``W_UK [H, d_nope, d_c]`` ~ N(0, std^2)
+5. ``W_UV [H, d_v, d_c]`` ~ N(0, std^2)
+6. per-sequence lengths (ragged workloads only), uniform in [lo, hi]
+7. the rows to scale (long-context workload only): round(frac * len_b) rows of
+   sequence b chosen by a seeded permutation; whole 576-wide rows are scaled.
+
+Values are drawn in fp32 and then rounded once to the storage type (bf16 by
+round-to-nearest-even), so the CUDA path and the oracle read identical bits.
+Positions are ``len_b - 1``: the cache already holds the current token's row.
+
+This module holds none of the method's arithmetic.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from .configs import MlaConfig
+
+
+@dataclass
+class MlaInputs:
+    cfg: MlaConfig
+    cache: torch.Tensor      # [B, S_max, row], storage dtype, CPU
+    q_nope: torch.Tensor     # [B, H, d_nope]
+    q_rope: torch.Tensor     # [B, H, d_rope]
+    w_uk: torch.Tensor       # [H, d_nope, d_c]
+    w_uv: torch.Tensor       # [H, d_v, d_c]
+    lengths: torch.Tensor    # [B] int32
+    positions: torch.Tensor  # [B] int32
+
+    def as_float64_numpy(self, b: Optional[int] = None):
+        """Exact fp64 copies (bf16 and fp32 values are exactly representable)."""
+        sl = slice(None) if b is None else slice(b, b + 1)
+        f = lambda t: t.to(torch.float64).numpy()
+        return dict(
+            cache=f(self.cache[sl]), q_nope=f(self.q_nope[sl]), q_rope=f(self.q_rope[sl]),
+            w_uk=f(self.w_uk), w_uv=f(self.w_uv),
+            lengths=self.lengths[sl].numpy().astype("int64"),
+            positions=self.positions[sl].numpy().astype("int64"))
+
+
+def _storage(cfg: MlaConfig) -> torch.dtype:
+    return torch.float32 if cfg.dtype == "f32" else torch.bfloat16
+
+
+def make_inputs(cfg: MlaConfig, seed: int = 0, poison_tail: bool = False,
+                lengths: Optional[torch.Tensor] = None) -> MlaInputs:
+    """Draw the inputs of ``cfg`` from ``seed``.
+
+    ``poison_tail`` fills every cache row at or past ``lengths[b]`` with NaN, so
+    that any read of the masked tail that reaches the arithmetic shows up.
+    ``lengths`` overrides the drawn lengths (edge-case tests).
+    """
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    B, H, S = cfg.batch, cfg.heads, cfg.s_max
+    st = _storage(cfg)
+
+    cache = torch.randn((B, S, cfg.row), generator=g, dtype=torch.float32)
+    q_nope = torch.randn((B, H, cfg.d_nope), generator=g, dtype=torch.float32)
+    q_rope = torch.randn((B, H, cfg.d_rope), generator=g, dtype=torch.float32)
+    w_uk = torch.randn((H, cfg.d_nope, cfg.d_c), generator=g, dtype=torch.float32) * cfg.weight_std
+    w_uv = torch.randn((H, cfg.d_v, cfg.d_c), generator=g, dtype=torch.float32) * cfg.weight_std
+
+    if cfg.ragged is not None:
+        lo, hi = cfg.ragged
+        drawn = torch.randint(lo, hi + 1, (B,), generator=g, dtype=torch.int64).to(torch.int32)
+    else:
+        drawn = torch.full((B,), S, dtype=torch.int32)
+    if lengths is not None:
+        drawn = lengths.to(torch.int32).clone()
+
+    if cfg.scaled_row_frac > 0.0:
+        for b in range(B):
+            n = int(drawn[b])
+            k = int(round(cfg.scaled_row_frac * n))
+            rows = torch.randperm(n, generator=g)[:k]
+            cache[b, rows, :] *= cfg.scaled_row_gain
+
+    cache = cache.to(st)
+    if poison_tail:
+        for b in range(B):
+            cache[b, int(drawn[b]):, :] = float("nan")
+
+    positions = (drawn - 1).clamp(min=0).to(torch.int32)
+    return MlaInputs(cfg=cfg, cache=cache, q_nope=q_nope.to(st), q_rope=q_rope.to(st),
+                     w_uk=w_uk.to(st), w_uv=w_uv.to(st), lengths=drawn, positions=positions)
