@@ -1,0 +1,473 @@
+#!/usr/bin/env python
+"""Throughput of one MLA decode step (weight-absorbed, latent cache) on GB300.
+
+A step is the whole hot path for one batch: absorb_q -> decode split ->
+LSE combine -> out_proj, through the C ABI.  The default workload is
+DeepSeek-V2-Lite decode in bf16: B=8 sequences of S=4096 cached rows, H=16.
+Each step reads one "layer": the bench keeps L copies of cache + weights
+(L chosen so that their total exceeds 3x the L2 size) and step k uses layer
+k mod L, so no step finds its cache in L2.
+
+Prints one JSON line.  `value` is latent-cache GB/s of the whole step
+(algorithmic cache bytes B*S*576*2 per step over the device time of the
+timed steps); `tokens_per_s` is B*steps/time.  `roofline` covers the split
+kernel (the dominant kernel), timed with CUDA events around each of its
+launches inside the timed region.
+
+`--impl reference` times the fp64 CPU oracle instead (the reference arm).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA decode latent-cache GB/s (vs ~8 TB/s HBM) and decode tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_bf16_traffic.json")
+KERNEL_SOURCES = ["head_latent_attention_absorbed_gb300/csrc/mla_decode.cu",
+                  "head_latent_attention_absorbed_gb300/csrc/mla_common.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="v2lite_bf16_b8_s4096")
+    ap.add_argument("--splits", type=int, default=0, help="KV chunks per sequence (0 = auto)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- peaks, traffic
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload):
+    try:
+        with open(TRAFFIC_FILE) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("source_sha256") != kernel_sha() or d.get("workload") != workload:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- clocks (NVML)
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML while running."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
+               0x2: "applications_clocks_setting", 0x10: "sync_boost"}
+
+    def __init__(self, bus_id: str | None, period_s: float = 0.002):
+        self.ok = False
+        self.samples = []
+        self.reasons = 0
+        self.period = period_s
+        try:
+            self.nvml = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nvml.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            if bus_id is not None:
+                r = self.nvml.nvmlDeviceGetHandleByPciBusId_v2(bus_id.encode(), ctypes.byref(self.h))
+            else:
+                r = self.nvml.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(self.h))
+            if r != 0:
+                return
+            mx = ctypes.c_uint()
+            self.nvml.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+            self.max_mhz = mx.value
+            self.ok = True
+        except OSError:
+            pass
+
+    def _poll(self):
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        fn = getattr(self.nvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self.nvml.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if fn(self.h, ctypes.byref(rs)) == 0:
+                self.reasons |= rs.value
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._stop = threading.Event()
+            self._t = threading.Thread(target=self._poll, daemon=True)
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        if self.ok:
+            self._stop.set()
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return None
+        names = [n for bit, n in self.REASONS.items() if self.reasons & bit]
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": names, "samples": len(self.samples), "source": "nvml"}
+
+
+# ----------------------------------------------------------------------------- CUDA runtime events
+class ExternalEvents:
+    """CUDA events recorded as graph nodes (cudaEventRecordExternal), so that the
+    launches inside a captured graph can be timed one by one."""
+
+    def __init__(self, n: int):
+        self.rt = ctypes.CDLL("libcudart.so.13")
+        self.rt.cudaEventCreate.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+        self.rt.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+        self.rt.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p,
+                                                 ctypes.c_void_p]
+        self.rt.cudaEventDestroy.argtypes = [ctypes.c_void_p]
+        self.ev = []
+        for _ in range(n):
+            e = ctypes.c_void_p()
+            if self.rt.cudaEventCreate(ctypes.byref(e)) != 0:
+                raise RuntimeError("cudaEventCreate failed")
+            self.ev.append(e)
+
+    def record(self, i: int, stream_handle: int):
+        r = self.rt.cudaEventRecordWithFlags(self.ev[i], ctypes.c_void_p(stream_handle), 1)
+        if r != 0:
+            raise RuntimeError(f"cudaEventRecordWithFlags failed ({r})")
+
+    def elapsed_ms(self, a: int, b: int) -> float:
+        ms = ctypes.c_float()
+        r = self.rt.cudaEventElapsedTime(ctypes.byref(ms), self.ev[a], self.ev[b])
+        if r != 0:
+            raise RuntimeError(f"cudaEventElapsedTime failed ({r})")
+        return ms.value
+
+    def close(self):
+        for e in self.ev:
+            self.rt.cudaEventDestroy(e)
+
+
+def bus_id_of(device_index: int):
+    try:
+        rt = ctypes.CDLL("libcudart.so.13")
+        buf = ctypes.create_string_buffer(64)
+        if rt.cudaDeviceGetPCIBusId(buf, 64, device_index) == 0:
+            return buf.value.decode()
+    except OSError:
+        pass
+    return None
+
+
+# ----------------------------------------------------------------------------- CPU oracle leg
+def oracle_throughput(cfg, budget_s: float, max_steps: int | None = None, warmup: int = 0,
+                      rows_per_step: int | None = None):
+    """Time the fp64 oracle's absorbed path on sequences of `cfg` (inputs converted
+    to fp64 beforehand, outside the timing).  Returns (GB/s, tokens/s, steps, rows, cores)."""
+    import numpy as np
+    from oracle import mla_oracle as O
+    from workloads import make_inputs
+    inp = make_inputs(cfg, seed=0)
+    seqs = [inp.as_float64_numpy(b) for b in range(cfg.batch)]
+    rows = cfg.s_max if rows_per_step is None else max(1, min(cfg.s_max, rows_per_step))
+
+    def one(i):
+        a = seqs[i % cfg.batch]
+        n = rows
+        O.decode_absorbed(a["q_nope"], a["q_rope"], a["w_uk"], a["w_uv"], a["cache"][:, :n],
+                          np.array([n]), np.array([n - 1]), cfg.softmax_scale, cfg.rope_base)
+
+    for i in range(warmup):
+        one(i)
+    t0 = time.perf_counter()
+    steps = 0
+    while True:
+        one(steps)
+        steps += 1
+        el = time.perf_counter() - t0
+        if max_steps is not None and steps >= max_steps:
+            break
+        if max_steps is None and el >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    byts = steps * rows * cfg.row * 2
+    return byts / el / 1e9, steps / el, steps, rows, el
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args, cfg, rank, world):
+    if rank != 0:
+        return 0
+    # Size each step so that warm-up + steps stay within about two minutes.
+    import numpy as np  # noqa: F401
+    probe_gbs, _, _, _, probe_el = oracle_throughput(cfg, 0.0, max_steps=1, rows_per_step=cfg.s_max)
+    per_full = probe_el
+    budget = 120.0
+    rows = cfg.s_max
+    if per_full * (args.steps + args.warmup) > budget:
+        rows = max(32, int(cfg.s_max * budget / (per_full * (args.steps + args.warmup))))
+    gbs, tps, steps, rows, el = oracle_throughput(cfg, 0.0, max_steps=args.steps,
+                                                  warmup=args.warmup, rows_per_step=rows)
+    sample = (f"each step: fp64 NumPy oracle (absorbed form, exact softmax) on one sequence's "
+              f"first {rows} of {cfg.s_max} rows, H={cfg.heads}, cycling over the {cfg.batch} "
+              f"sequences of the workload")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": el / steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "tokens_per_s": tps,
+        "config": workload_config(cfg, None, None),
+        "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(cfg, layers, splits):
+    c = {"workload": cfg.name, "batch": cfg.batch, "heads": cfg.heads, "seq_len": cfg.s_max,
+         "d_c": cfg.d_c, "d_rope": cfg.d_rope, "d_nope": cfg.d_nope, "d_v": cfg.d_v,
+         "cache_dtype": cfg.dtype, "parallelism": "replicas (one batch per GPU, no collective)"}
+    if layers is not None:
+        c["l2"] = (f"inputs larger than L2: {layers} layer copies of cache + W_UK + W_UV rotated, "
+                   f"step k reads layer k mod {layers}")
+    if splits is not None:
+        c["kv_splits"] = splits
+    return c
+
+
+# ----------------------------------------------------------------------------- our arm
+def main():
+    args = parse()
+    from workloads import BY_NAME
+    cfg = BY_NAME[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        return run_reference(args, cfg, rank, world)
+
+    import torch
+    import torch.distributed as dist
+    import head_latent_attention_absorbed_gb300 as mla
+    from workloads import make_inputs
+
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    mla.load()
+
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    inp = make_inputs(cfg, seed=rank)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
+    per_layer = (inp.cache.numel() + inp.w_uk.numel() + inp.w_uv.numel()) * inp.cache.element_size()
+    L = max(2, math.ceil(3 * l2 / per_layer))
+    caches = [inp.cache.to(dev) for _ in range(L)]
+    wuk = [inp.w_uk.to(dev) for _ in range(L)]
+    wuv = [inp.w_uv.to(dev) for _ in range(L)]
+    qn = [inp.q_nope.to(dev) for _ in range(L)]
+    qr = [inp.q_rope.to(dev) for _ in range(L)]
+    lengths = inp.lengths.to(dev)
+    positions = inp.positions.to(dev)
+    step = mla.DecodeStep(cfg.batch, cfg.heads, cfg.s_max, dt, device=dev,
+                          num_splits_requested=args.splits, rope_base=cfg.rope_base,
+                          softmax_scale=cfg.softmax_scale)
+    d = step.dims
+    cache_bytes = int(inp.lengths.to(torch.int64).sum()) * cfg.row * inp.cache.element_size()
+
+    def one_step(k, ev=None, stream_handle=None):
+        l = k % L
+        mla.absorb_q(d, qn[l], qr[l], wuk[l], positions, step.q_abs, step.q_pe, step.rope_base)
+        if ev is not None:
+            ev.record(2 * k, stream_handle)
+        mla.decode_split(d, step.q_abs, step.q_pe, caches[l], lengths, step.workspace, step.scale,
+                         args.splits, step.status)
+        if ev is not None:
+            ev.record(2 * k + 1, stream_handle)
+        mla.decode_combine(d, lengths, step.workspace, step.o_c, args.splits, step.lse)
+        mla.out_proj(d, step.o_c, wuv[l], step.out)
+
+    K, W = args.steps, args.warmup
+    for k in range(W):
+        one_step(k)
+    torch.cuda.synchronize()
+    if int(step.status.item()) != 0:
+        raise RuntimeError(f"device status {int(step.status.item())} after warm-up")
+
+    # Capture the K timed steps in one CUDA graph, with event nodes around every
+    # split launch.
+    ev = ExternalEvents(2 * K)
+    cap = torch.cuda.Stream(device=dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+        sh = torch.cuda.current_stream().cuda_stream
+        for k in range(K):
+            one_step(k, ev, sh)
+    g.replay()                       # one untimed replay (graph upload, warm)
+    torch.cuda.synchronize()
+
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(bus_id_of(dev.index))
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with sampler:
+        t_begin.record()
+        g.replay()
+        t_end.record()
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t_begin.elapsed_time(t_end)
+    split_ms = [ev.elapsed_ms(2 * k, 2 * k + 1) for k in range(K)]
+    ev.close()
+    if int(step.status.item()) != 0:
+        raise RuntimeError(f"device status {int(step.status.item())} after the timed steps")
+
+    if world > 1:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    sec = elapsed_ms / 1e3
+    value = cache_bytes * K * world / sec / 1e9
+    tokens = cfg.batch * K * world / sec
+    split_avg_s = statistics.fmean(split_ms) / 1e3
+
+    # End-to-end through the public call, with host buffers: per step the
+    # queries, lengths and positions go host->device from pinned memory and
+    # the output comes back device->host.
+    e2e = None
+    if not args.no_e2e:
+        h_qn = [t.cpu().pin_memory() for t in qn]
+        h_qr = [t.cpu().pin_memory() for t in qr]
+        h_len = inp.lengths.pin_memory()
+        h_pos = inp.positions.pin_memory()
+        h_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+        d_qn = torch.empty_like(qn[0])
+        d_qr = torch.empty_like(qr[0])
+        d_len = torch.empty_like(lengths)
+        d_pos = torch.empty_like(positions)
+        Ke = min(K, 2000)
+
+        def e2e_step(k):
+            l = k % L
+            d_qn.copy_(h_qn[l], non_blocking=True)
+            d_qr.copy_(h_qr[l], non_blocking=True)
+            d_len.copy_(h_len, non_blocking=True)
+            d_pos.copy_(h_pos, non_blocking=True)
+            o = step.run(d_qn, d_qr, caches[l], d_len, d_pos, wuk[l], wuv[l])
+            h_out.copy_(o, non_blocking=True)
+
+        for k in range(min(W, 20)):
+            e2e_step(k)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for k in range(Ke):
+            e2e_step(k)
+        e1.record()
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1)
+        if world > 1:
+            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        bi = sum(t.numel() * t.element_size() for t in (h_qn[0], h_qr[0], h_len, h_pos))
+        bo = h_out.numel() * h_out.element_size()
+        e2e = {"value": cache_bytes * Ke * world / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+               "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": Ke,
+               "tokens_per_s": cfg.batch * Ke * world / (e_ms / 1e3),
+               "path": "DecodeStep.run (three C-ABI calls, eager launches)"}
+
+    peak, peak_kind = measured_peaks()
+    achieved = cache_bytes / split_avg_s / 1e9
+    roofline = {"bound": "hbm", "kernel": "split_bf16_kernel (mla_decode_split)",
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
+                "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
+                "traffic": recorded_traffic(cfg.name),
+                "bytes_per_launch": cache_bytes,
+                "avg_launch_us": split_avg_s * 1e6,
+                "launches_timed": K}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, tps, nsteps, rows, el = oracle_throughput(cfg, args.cpu_seconds)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
+               "tokens_per_s": tps,
+               "sample": (f"{nsteps} single-sequence decode steps ({rows} rows, H={cfg.heads}) "
+                          f"of this workload through the fp64 NumPy oracle, {el:.1f} s; inputs "
+                          f"converted to fp64 before timing")}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded N(0,1) cache and queries, N(0,0.02^2) weights)",
+        "tokens_per_s": tokens,
+        "config": workload_config(cfg, L, step.splits),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": 4 * K,
+        "clocks": sampler.summary(),
+        "timing": "one CUDA-graph replay of the timed steps, CUDA events on the launch stream",
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

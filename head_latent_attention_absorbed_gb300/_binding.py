@@ -1,0 +1,168 @@
+"""ctypes binding of the C ABI in ``include/mla.h``.
+
+Argument marshalling only: every step of the decode runs in the CUDA library.
+Tensors are torch tensors on a CUDA device (PyTorch provides device memory and
+streams); their data pointers, sizes and the current stream are passed through.
+If the shared library is missing the calls raise: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libmla_gb300.so")
+
+MLA_F32, MLA_BF16 = 0, 1
+MLA_DEV_LENGTH_OUT_OF_RANGE = 1
+MLA_DEV_PIPELINE_TIMEOUT = 2
+STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
+          3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA"}
+EXPORTED = ("mla_absorb_q", "mla_decode_num_splits", "mla_decode_workspace_bytes",
+            "mla_decode_attn", "mla_decode_split", "mla_decode_combine", "mla_out_proj",
+            "mla_status_string", "mla_last_error_message")
+
+
+class MlaDims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("heads", ctypes.c_int32), ("d_c", ctypes.c_int32),
+                ("d_rope", ctypes.c_int32), ("d_nope", ctypes.c_int32), ("d_v", ctypes.c_int32),
+                ("s_max", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+
+
+class MlaError(RuntimeError):
+    def __init__(self, code: int, detail: str):
+        super().__init__(f"{STATUS.get(code, code)}: {detail}")
+        self.code = code
+
+
+_lib = None
+
+
+def load(path: Optional[str] = None):
+    """Load the shared library (once) and declare its signatures."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise RuntimeError(f"CUDA library {p} is not built; run __graft_entry__.build()")
+    lib = ctypes.CDLL(p)
+    P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    D = ctypes.POINTER(MlaDims)
+    lib.mla_absorb_q.argtypes = [D, P, P, P, P, ctypes.c_double, P, P, P]
+    lib.mla_absorb_q.restype = ctypes.c_int
+    lib.mla_decode_num_splits.argtypes = [D, I32]
+    lib.mla_decode_num_splits.restype = I32
+    lib.mla_decode_workspace_bytes.argtypes = [D, I32]
+    lib.mla_decode_workspace_bytes.restype = SZ
+    lib.mla_decode_attn.argtypes = [D, P, P, P, P, ctypes.c_float, I32, P, SZ, P, P, P, P]
+    lib.mla_decode_attn.restype = ctypes.c_int
+    lib.mla_decode_split.argtypes = [D, P, P, P, P, ctypes.c_float, I32, P, SZ, P, P]
+    lib.mla_decode_split.restype = ctypes.c_int
+    lib.mla_decode_combine.argtypes = [D, P, I32, P, SZ, P, P, P]
+    lib.mla_decode_combine.restype = ctypes.c_int
+    lib.mla_out_proj.argtypes = [D, P, P, P, P]
+    lib.mla_out_proj.restype = ctypes.c_int
+    lib.mla_status_string.argtypes = [ctypes.c_int]
+    lib.mla_status_string.restype = ctypes.c_char_p
+    lib.mla_last_error_message.argtypes = []
+    lib.mla_last_error_message.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(code: int):
+    if code != 0:
+        raise MlaError(code, load().mla_last_error_message().decode())
+
+
+def dims(batch: int, heads: int, s_max: int, dtype: int, d_c: int = 512, d_rope: int = 64,
+         d_nope: int = 128, d_v: int = 128) -> MlaDims:
+    return MlaDims(batch, heads, d_c, d_rope, d_nope, d_v, s_max, dtype)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def dtype_code(torch_dtype) -> int:
+    import torch
+    if torch_dtype == torch.bfloat16:
+        return MLA_BF16
+    if torch_dtype == torch.float32:
+        return MLA_F32
+    raise TypeError(f"unsupported dtype {torch_dtype}")
+
+
+def _require(cond: bool, msg: str):
+    if not cond:
+        raise ValueError(msg)
+
+
+def _cuda_contig(*ts):
+    for t in ts:
+        if t is not None:
+            _require(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
+
+
+def num_splits(d: MlaDims, requested: int = 0) -> int:
+    return int(load().mla_decode_num_splits(ctypes.byref(d), int(requested)))
+
+
+def workspace_bytes(d: MlaDims, requested: int = 0) -> int:
+    return int(load().mla_decode_workspace_bytes(ctypes.byref(d), int(requested)))
+
+
+def absorb_q(d: MlaDims, q_nope, q_rope, w_uk, positions, q_abs, q_pe, rope_base: float = 10000.0,
+             stream=None) -> None:
+    """q_abs = q_nope . W_UK per head; q_pe = RoPE(q_rope, positions)."""
+    _cuda_contig(q_nope, q_rope, w_uk, positions, q_abs, q_pe)
+    _check(load().mla_absorb_q(ctypes.byref(d), _ptr(q_nope), _ptr(q_rope), _ptr(w_uk),
+                               _ptr(positions), float(rope_base), _ptr(q_abs), _ptr(q_pe),
+                               _stream(stream)))
+
+
+def decode_attn(d: MlaDims, q_abs, q_pe, cache, lengths, o_c, workspace, softmax_scale: float,
+                num_splits_requested: int = 0, lse=None, dev_status=None, stream=None) -> None:
+    """Split-KV attention over the latent cache followed by the LSE combine."""
+    _cuda_contig(q_abs, q_pe, cache, lengths, o_c, workspace, lse, dev_status)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().mla_decode_attn(ctypes.byref(d), _ptr(q_abs), _ptr(q_pe), _ptr(cache),
+                                  _ptr(lengths), float(softmax_scale), int(num_splits_requested),
+                                  _ptr(workspace), nbytes, _ptr(o_c), _ptr(lse),
+                                  _ptr(dev_status), _stream(stream)))
+
+
+def decode_split(d: MlaDims, q_abs, q_pe, cache, lengths, workspace, softmax_scale: float,
+                 num_splits_requested: int = 0, dev_status=None, stream=None) -> None:
+    """First half of decode_attn: per-chunk partial outputs into the workspace."""
+    _cuda_contig(q_abs, q_pe, cache, lengths, workspace, dev_status)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().mla_decode_split(ctypes.byref(d), _ptr(q_abs), _ptr(q_pe), _ptr(cache),
+                                   _ptr(lengths), float(softmax_scale),
+                                   int(num_splits_requested), _ptr(workspace), nbytes,
+                                   _ptr(dev_status), _stream(stream)))
+
+
+def decode_combine(d: MlaDims, lengths, workspace, o_c, num_splits_requested: int = 0, lse=None,
+                   stream=None) -> None:
+    """Second half of decode_attn: log-sum-exp merge of the chunk partials."""
+    _cuda_contig(lengths, workspace, o_c, lse)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().mla_decode_combine(ctypes.byref(d), _ptr(lengths), int(num_splits_requested),
+                                     _ptr(workspace), nbytes, _ptr(o_c), _ptr(lse),
+                                     _stream(stream)))
+
+
+def out_proj(d: MlaDims, o_c, w_uv, out, stream=None) -> None:
+    """o = W_UV . o_c per head."""
+    _cuda_contig(o_c, w_uv, out)
+    _check(load().mla_out_proj(ctypes.byref(d), _ptr(o_c), _ptr(w_uv), _ptr(out), _stream(stream)))

@@ -1,0 +1,191 @@
+/*
+ * mla.h -- C ABI of the GB300 (sm_103a) MLA decode library.
+ *
+ * One decode step of DeepSeek Multi-Head Latent Attention in weight-absorbed
+ * form over a latent KV cache, as three calls:
+ *
+ *   mla_absorb_q     q_abs = q_nope . W_UK (per head), q_pe = RoPE(q_rope, pos)
+ *   mla_decode_attn  split-KV online-softmax attention of [q_abs || q_pe] against
+ *                    the cached rows [c_kv || k_rope], then a log-sum-exp combine;
+ *                    the output o_c stays in the latent space
+ *   mla_out_proj     o = W_UV . o_c (per head)
+ *
+ * Sources: "Multi-Head Latent Attention" (Lior Sinai) sections 3.1 (C cache),
+ * 3.3 (absorption, eq. 3.3.3), 3.6 (decoupled RoPE: score = nope part + RoPE
+ * part, scaled by 1/sqrt(d_h + d_R), k_rope shared by all heads) and 3.7
+ * (RoPE on adjacent pairs); "Deepseek V2 Lite Inference Engine in C", MLA
+ * notes (absorbing W_UK without materialising it, cache row order
+ * (kv_lora, k_rope)); "Transformer and KV Cache Basics" (decode is bound by
+ * memory bandwidth; overflowing the cache is an error).
+ *
+ * Conventions for every call
+ *  - All tensor pointers are DEVICE pointers, row-major and contiguous, and
+ *    must be 16-byte aligned.  The caller owns every buffer; the library
+ *    allocates no device memory, keeps no per-call state and never
+ *    synchronises the stream.  Work is enqueued on `stream` (a cudaStream_t;
+ *    NULL means the legacy default stream) on the current device.
+ *  - Argument errors are detected on the host before anything is enqueued and
+ *    are returned as a status; nothing is launched then.  A failed launch
+ *    returns MLA_ERR_CUDA.  mla_last_error_message() gives a one-line detail
+ *    for the calling thread's most recent failure.
+ *  - Element types: with dtype MLA_BF16 the cache, q_nope, q_rope and the
+ *    weights are bf16 and all arithmetic accumulates in fp32; with MLA_F32
+ *    they are fp32 and every step runs in fp32 (no TF32).  Every result --
+ *    the absorbed query q_abs, the rotated q_pe, o_c, lse, the output o --
+ *    and the workspace are fp32 in both cases (the bf16 decode kernel feeds
+ *    the fp32 query and the softmax weights to the tensor cores as hi + lo
+ *    bf16 pairs).
+ *  - Supported sizes: d_c = 512, d_rope = 64, d_nope = 128, d_v = 128;
+ *    batch >= 1; s_max >= 1; heads >= 1 (a multiple of 16 for MLA_BF16).
+ *    Anything else returns MLA_ERR_UNSUPPORTED.
+ */
+#ifndef MLA_GB300_H
+#define MLA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,   /* null or misaligned pointer, non-positive size */
+  MLA_ERR_UNSUPPORTED = 2,   /* a size or dtype this build has no kernel for */
+  MLA_ERR_WORKSPACE = 3,     /* workspace smaller than mla_decode_workspace_bytes() */
+  MLA_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed */
+} mla_status;
+
+typedef enum mla_dtype { MLA_F32 = 0, MLA_BF16 = 1 } mla_dtype;
+
+/* Problem sizes shared by the three calls. */
+typedef struct mla_dims {
+  int32_t batch;    /* B: sequences decoded in this step                      */
+  int32_t heads;    /* H: attention heads                                     */
+  int32_t d_c;      /* latent width of c_kv (512)                             */
+  int32_t d_rope;   /* decoupled RoPE width (64)                              */
+  int32_t d_nope;   /* per-head non-rotated query width (128)                 */
+  int32_t d_v;      /* per-head value width (128)                             */
+  int32_t s_max;    /* cache capacity: rows allocated per sequence            */
+  int32_t dtype;    /* mla_dtype                                              */
+} mla_dims;
+
+/* Bits a kernel ORs into the optional device status word (see mla_decode_attn). */
+#define MLA_DEV_LENGTH_OUT_OF_RANGE 1  /* some lengths[b] < 1 or > s_max        */
+#define MLA_DEV_PIPELINE_TIMEOUT 2     /* a bounded wait on a TMA copy gave up  */
+
+/*
+ * mla_absorb_q -- absorbed query and rotated RoPE query for one decode step.
+ *
+ *   q_abs[b,h,c] = sum_{d < d_nope} q_nope[b,h,d] * w_uk[h,d,c]
+ *       (W_UK absorbed into the query side without materialising W_UK^T W_Q:
+ *        Multi-Head Latent Attention 3.3; "Deepseek V2 Lite Inference Engine
+ *        in C", absorption "without materializing WukWq")
+ *   q_pe[b,h,2i:2i+2] = rotation of the pair (q_rope[b,h,2i], q_rope[b,h,2i+1])
+ *       by the angle positions[b] * rope_base^(-2i/d_rope)
+ *       (Multi-Head Latent Attention 3.7: complex multiply of adjacent pairs;
+ *        positions counted from 0; the angle is formed in fp64)
+ *
+ * q_nope   [B, H, d_nope]   dtype           q_rope [B, H, d_rope] dtype
+ * w_uk     [H, d_nope, d_c] dtype           positions [B] int32 (device)
+ * q_abs    [B, H, d_c]      fp32 (out)      q_pe   [B, H, d_rope] fp32 (out)
+ */
+mla_status mla_absorb_q(const mla_dims* dims, const void* q_nope, const void* q_rope,
+                        const void* w_uk, const int32_t* positions, double rope_base,
+                        void* q_abs, void* q_pe, void* stream);
+
+/*
+ * mla_decode_num_splits -- the number of KV chunks per sequence that
+ * mla_decode_attn will use for `requested` (0 = let the library choose from
+ * the current device's SM count).  Chunks hold a multiple of 32 rows, so the
+ * result can be smaller than `requested`.  Returns 0 for invalid dims.
+ */
+int32_t mla_decode_num_splits(const mla_dims* dims, int32_t requested);
+
+/* Bytes of device workspace mla_decode_attn needs for `requested` splits. */
+size_t mla_decode_workspace_bytes(const mla_dims* dims, int32_t requested);
+
+/*
+ * mla_decode_attn -- attention of the absorbed query against the latent cache.
+ *
+ * For sequence b with S_b = lengths[b] cached rows, head h, row t < S_b:
+ *   s[t]   = softmax_scale * (q_abs[b,h,:] . cache[b,t,0:d_c]
+ *                             + q_pe[b,h,:] . cache[b,t,d_c:d_c+d_rope])
+ *   o_c[b,h,:] = sum_t softmax(s)[t] * cache[b,t,0:d_c]
+ *   lse[b,h]   = log(sum_t exp(s[t]))               (natural log)
+ * (Multi-Head Latent Attention 3.3 and 3.6: the nope part of the score is
+ *  the latent row against the absorbed query, k_rope is shared by every head,
+ *  and the output stays latent until W_UV is applied.)  softmax_scale is
+ *  normally 1/sqrt(d_nope + d_rope).
+ *
+ * The rows of a sequence are cut into chunks of equal size; one kernel
+ * computes every chunk's normalised partial output and lse into `workspace`,
+ * a second kernel merges them: L = log sum_j exp(lse_j),
+ * o_c = sum_j exp(lse_j - L) o_j.  Rows t >= S_b are never part of any
+ * result; their contents may be anything, including NaN.
+ *
+ * q_abs   [B, H, d_c]       fp32       q_pe  [B, H, d_rope] fp32
+ * cache   [B, s_max, d_c + d_rope] dtype; row t of sequence b is
+ *         [c_kv (d_c) || k_rope (d_rope)], k_rope already rotated
+ * lengths [B] int32 (device); 1 <= lengths[b] <= s_max
+ * num_splits  chunks per sequence requested (0 = library's choice)
+ * workspace   >= mla_decode_workspace_bytes(dims, num_splits) bytes, device,
+ *             owned by the caller, contents need not be initialised
+ * o_c     [B, H, d_c] fp32 (out)       lse [B, H] fp32 (out, may be NULL)
+ * dev_status  optional device int32 (may be NULL).  Kernels OR
+ *             MLA_DEV_* bits into it and never clear it; the caller zeroes
+ *             it.  A length outside [1, s_max] cannot be checked on the host:
+ *             the kernels clamp it to [0, s_max] (the cache overflow of
+ *             "Transformer and KV Cache Basics" becomes an error bit), and a
+ *             sequence with no rows gets o_c = 0 and lse = -inf.
+ */
+mla_status mla_decode_attn(const mla_dims* dims, const void* q_abs, const void* q_pe,
+                           const void* cache, const int32_t* lengths, float softmax_scale,
+                           int32_t num_splits, void* workspace, size_t workspace_bytes,
+                           float* o_c, float* lse, int32_t* dev_status, void* stream);
+
+/*
+ * mla_decode_split / mla_decode_combine -- the two halves of mla_decode_attn,
+ * for callers that schedule them separately (for example to time or overlap
+ * them).  mla_decode_attn(...) is exactly mla_decode_split(...) followed by
+ * mla_decode_combine(...) on the same stream with the same dims, lengths,
+ * num_splits and workspace.
+ *
+ * mla_decode_split writes, for every chunk j of every sequence b with rows,
+ * the chunk's normalised partial output o_j[b,j,h,:] and lse_j[b,j,h] into
+ * the workspace (layout private to the library); chunks past S_b are not
+ * written.  mla_decode_combine reads them back and writes o_c and lse as
+ * described for mla_decode_attn.  Arguments have the meaning, layout and
+ * error behaviour given above.
+ */
+mla_status mla_decode_split(const mla_dims* dims, const void* q_abs, const void* q_pe,
+                            const void* cache, const int32_t* lengths, float softmax_scale,
+                            int32_t num_splits, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_status, void* stream);
+mla_status mla_decode_combine(const mla_dims* dims, const int32_t* lengths, int32_t num_splits,
+                              const void* workspace, size_t workspace_bytes, float* o_c,
+                              float* lse, void* stream);
+
+/*
+ * mla_out_proj -- per-head value up-projection applied after attention.
+ *
+ *   o[b,h,e] = sum_{c < d_c} w_uv[h,e,c] * o_c[b,h,c]
+ * (Multi-Head Latent Attention eq. 3.3.3, with W^O left to the caller.)
+ *
+ * o_c [B, H, d_c] fp32     w_uv [H, d_v, d_c] dtype     o [B, H, d_v] fp32 (out)
+ */
+mla_status mla_out_proj(const mla_dims* dims, const float* o_c, const void* w_uv, void* out,
+                        void* stream);
+
+/* Static English name of a status code. */
+const char* mla_status_string(mla_status status);
+
+/* Detail of the calling thread's most recent failed call ("" if none). */
+const char* mla_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_GB300_H */

@@ -1,0 +1,138 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle, on the
+same seeded inputs, per call (q_abs, q_pe, o_c, lse) and end to end (o).
+
+Small cases span several 32-row tiles, ragged tails and many chunk counts; the
+five full-size workloads run in the launch configuration the bench uses (the
+library's own chunk choice, or the 128 chunks the long-context workload asks
+for), with the oracle on every sequence or, for the largest, on sampled ones.
+"""
+import numpy as np
+import pytest
+import torch
+
+from _parity import compare, run_cuda, run_oracle
+from workloads import (V2LITE_BF16_B4_S65536_LONG, V2LITE_BF16_B8_S4096, V2LITE_BF16_B64_RAGGED,
+                       V2LITE_F32_B1_S64, V3_BF16_H128_B32_S16384, MlaConfig, make_inputs)
+
+pytestmark = pytest.mark.gpu
+
+
+def small(dtype="bf16", B=3, H=16, S=200, **kw):
+    return MlaConfig(name=f"small_{dtype}_b{B}_h{H}_s{S}", dtype=dtype, batch=B, heads=H, s_max=S,
+                     hidden=2048, **kw)
+
+
+# ------------------------------------------------------------------ small cases
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("splits", [0, 1, 2, 7])
+def test_small_ragged(cuda_lib, dtype, splits):
+    cfg = small(dtype)
+    inp = make_inputs(cfg, seed=splits, poison_tail=True,
+                      lengths=torch.tensor([1, 33, 200], dtype=torch.int32))
+    gpu = run_cuda(inp, num_splits=splits)
+    ref, bs = run_oracle(inp)
+    compare(gpu, ref, bs, dtype)
+    assert gpu["status"] == 0
+
+
+@pytest.mark.parametrize("lengths", [[32, 64, 96], [31, 63, 95], [2, 3, 5], [190, 199, 200]])
+def test_tile_edges(cuda_lib, lengths):
+    cfg = small()
+    inp = make_inputs(cfg, seed=5, poison_tail=True, lengths=torch.tensor(lengths, dtype=torch.int32))
+    gpu = run_cuda(inp, num_splits=3)
+    ref, bs = run_oracle(inp)
+    compare(gpu, ref, bs, "bf16")
+
+
+@pytest.mark.parametrize("H", [32, 128])
+def test_head_groups(cuda_lib, H):
+    cfg = small(H=H, B=2, S=300)
+    inp = make_inputs(cfg, seed=H, lengths=torch.tensor([300, 137], dtype=torch.int32))
+    gpu = run_cuda(inp, num_splits=4)
+    ref, bs = run_oracle(inp)
+    compare(gpu, ref, bs, "bf16")
+
+
+def test_batch_tail_in_projections(cuda_lib):
+    """B=19: the projections' batch tiles of 16 have a ragged second tile."""
+    cfg = small(B=19, S=64)
+    inp = make_inputs(cfg, seed=9)
+    gpu = run_cuda(inp)
+    ref, bs = run_oracle(inp)
+    compare(gpu, ref, bs, "bf16")
+
+
+def test_large_scores_stay_finite(cuda_lib):
+    """Rows scaled x8 push scores far from zero: the online softmax must rescale."""
+    cfg = small(S=512, B=2, scaled_row_frac=0.05, scaled_row_gain=8.0)
+    inp = make_inputs(cfg, seed=3)
+    gpu = run_cuda(inp, num_splits=5)
+    ref, bs = run_oracle(inp)
+    compare(gpu, ref, bs, "bf16")
+
+
+def test_lengths_out_of_range_are_reported(cuda_lib):
+    """A length past the capacity is the cache overflow of the KV-cache page: the
+    kernels clamp it and raise an error bit; an empty sequence gives o_c = 0."""
+    import head_latent_attention_absorbed_gb300 as mla
+    cfg = small(S=96)
+    inp = make_inputs(cfg, seed=1, lengths=torch.tensor([96, 96, 96], dtype=torch.int32))
+    bad = inp.lengths.clone()
+    bad[0] = 500          # overflow -> clamped to 96
+    bad[2] = 0            # empty
+    inp.lengths = bad
+    gpu = run_cuda(inp, num_splits=2)
+    assert gpu["status"] & mla.MLA_DEV_LENGTH_OUT_OF_RANGE
+    inp.lengths = torch.tensor([96, 96, 96], dtype=torch.int32)
+    ref, _ = run_oracle(inp, [0, 1])
+    compare({k: v for k, v in gpu.items() if k != "status"}, ref, [0, 1], "bf16")
+    assert np.all(gpu["o_c"][2] == 0.0) and np.all(np.isneginf(gpu["lse"][2]))
+
+
+def test_repeatable(cuda_lib):
+    cfg = small()
+    inp = make_inputs(cfg, seed=2)
+    a, b = run_cuda(inp, 3), run_cuda(inp, 3)
+    for k in ("q_abs", "o_c", "lse", "o"):
+        np.testing.assert_array_equal(a[k], b[k])
+
+
+# ------------------------------------------------------------------ the five workloads
+def test_v2lite_f32_b1_s64(cuda_lib):
+    inp = make_inputs(V2LITE_F32_B1_S64, seed=0)
+    gpu = run_cuda(inp)
+    ref, bs = run_oracle(inp)
+    compare(gpu, ref, bs, "f32")
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_v2lite_bf16_b8_s4096(cuda_lib, seed):
+    inp = make_inputs(V2LITE_BF16_B8_S4096, seed=seed)
+    gpu = run_cuda(inp)
+    ref, bs = run_oracle(inp)
+    compare(gpu, ref, bs, "bf16")
+
+
+def test_v2lite_bf16_b64_ragged(cuda_lib):
+    inp = make_inputs(V2LITE_BF16_B64_RAGGED, seed=0, poison_tail=True)
+    gpu = run_cuda(inp)
+    assert gpu["status"] == 0
+    ref, bs = run_oracle(inp)
+    compare(gpu, ref, bs, "bf16")
+
+
+def test_v3heads_bf16_h128_b32_s16384(cuda_lib):
+    inp = make_inputs(V3_BF16_H128_B32_S16384, seed=0)
+    gpu = run_cuda(inp)
+    ref, bs = run_oracle(inp, batches=[0, 17, 31])
+    compare(gpu, ref, bs, "bf16")
+    assert np.all(np.isfinite(gpu["o"]))
+
+
+def test_v2lite_long_context_128_splits(cuda_lib):
+    cfg = V2LITE_BF16_B4_S65536_LONG
+    inp = make_inputs(cfg, seed=0)
+    gpu = run_cuda(inp, num_splits=cfg.num_splits)
+    assert gpu["splits"] >= 128
+    ref, bs = run_oracle(inp)
+    compare(gpu, ref, bs, "bf16")

@@ -1,0 +1,106 @@
+"""The C-ABI library builds, loads, exports every symbol its header declares, and
+rejects bad arguments on the host before launching anything (no GPU needed)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from head_latent_attention_absorbed_gb300 import build as b
+    path = b.build()
+    import head_latent_attention_absorbed_gb300 as mla
+    return mla, mla.load(path)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mla_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_three_calls():
+    names = declared_functions()
+    for n in ("mla_absorb_q", "mla_decode_attn", "mla_out_proj"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    mla, so = lib
+    names = declared_functions()
+    out = subprocess.run(["nm", "-D", "--defined-only", mla.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if line.strip())
+    for n in names:
+        assert n in exported, n
+        assert hasattr(so, n)
+    assert set(mla.EXPORTED) <= set(names)
+
+
+def test_status_strings(lib):
+    _, so = lib
+    so.mla_status_string.restype = ctypes.c_char_p
+    assert so.mla_status_string(0) == b"MLA_OK"
+    assert so.mla_status_string(3) == b"MLA_ERR_WORKSPACE"
+
+
+def _d(mla, **kw):
+    base = dict(batch=2, heads=16, s_max=100, dtype=mla.MLA_BF16)
+    base.update(kw)
+    return mla.dims(base["batch"], base["heads"], base["s_max"], base["dtype"])
+
+
+def test_host_validation(lib):
+    mla, so = lib
+    P = ctypes.c_void_p
+    good = 0x10000
+    d = _d(mla)
+    # NULL pointer
+    assert so.mla_decode_attn(ctypes.byref(d), None, P(good), P(good), P(good), 0.1, 0, P(good),
+                              1 << 30, P(good), None, None, None) == 1
+    # misaligned cache
+    assert so.mla_decode_attn(ctypes.byref(d), P(good), P(good), P(good + 2), P(good), 0.1, 0,
+                              P(good), 1 << 30, P(good), None, None, None) == 1
+    # workspace too small
+    assert so.mla_decode_attn(ctypes.byref(d), P(good), P(good), P(good), P(good), 0.1, 0,
+                              P(good), 16, P(good), None, None, None) == 3
+    assert b"workspace" in so.mla_last_error_message()
+    # unsupported sizes
+    bad = _d(mla, heads=15)
+    assert so.mla_decode_attn(ctypes.byref(bad), P(good), P(good), P(good), P(good), 0.1, 0,
+                              P(good), 1 << 30, P(good), None, None, None) == 2
+    bad = mla.dims(2, 16, 100, mla.MLA_BF16, d_c=256)
+    assert so.mla_absorb_q(ctypes.byref(bad), P(good), P(good), P(good), P(good), 1e4, P(good),
+                           P(good), None) == 2
+    bad = mla.dims(0, 16, 100, mla.MLA_BF16)
+    assert so.mla_out_proj(ctypes.byref(bad), P(good), P(good), P(good), None) == 1
+    # negative split request, non-positive scale, bad rope base
+    assert so.mla_decode_attn(ctypes.byref(d), P(good), P(good), P(good), P(good), 0.1, -1,
+                              P(good), 1 << 30, P(good), None, None, None) == 1
+    assert so.mla_decode_attn(ctypes.byref(d), P(good), P(good), P(good), P(good), 0.0, 0,
+                              P(good), 1 << 30, P(good), None, None, None) == 1
+    assert so.mla_absorb_q(ctypes.byref(d), P(good), P(good), P(good), P(good), -1.0, P(good),
+                           P(good), None) == 1
+
+
+def test_split_planning(lib):
+    mla, _ = lib
+    # explicit requests: chunks are multiples of 32 rows
+    d = mla.dims(4, 16, 65536, mla.MLA_BF16)
+    assert mla.num_splits(d, 128) == 128
+    assert mla.num_splits(mla.dims(1, 16, 64, mla.MLA_F32), 7) == 2     # 64 rows -> 2 chunks of 32
+    assert mla.num_splits(mla.dims(1, 16, 1, mla.MLA_F32), 5) == 1
+    # workspace grows with splits: B*splits*H*(512+1) floats (256-byte aligned pieces)
+    n = 4 * 128 * 16
+    ws = mla.workspace_bytes(d, 128)
+    assert ws >= n * 513 * 4 and ws < n * 513 * 4 + 512
+    # automatic choice is a valid split count
+    for (B, H, S) in [(8, 16, 4096), (64, 16, 8192), (32, 128, 16384), (1, 16, 64)]:
+        s = mla.num_splits(mla.dims(B, H, S, mla.MLA_BF16), 0)
+        assert 1 <= s <= (S + 31) // 32
