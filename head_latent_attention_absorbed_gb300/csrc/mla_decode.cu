@@ -33,11 +33,6 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kSubBytes = kTileRows * 128;        // one 32-row x 64-col bf16 box
-constexpr int kStageBytes = 9 * kSubBytes;        // 32 rows x 576 cols
-constexpr int kSStride = 40;                      // floats per head row of a partial-score tile
-constexpr int kSTileFloats = kHeadGroup * kSStride;
-constexpr int kNumStagesBf16 = 4;
 
 struct SplitParams {
   const void* q_abs;
@@ -60,20 +55,125 @@ __device__ __forceinline__ int clamp_length(const SplitParams& p, int b, bool re
   return len;
 }
 
-constexpr size_t bf16_smem_bytes(int nstage) {
-  return 1024 /*alignment slack*/ + size_t(nstage) * kStageBytes +
-         2 * kWarps * kSTileFloats * sizeof(float) + 8 * nstage;
+// ---------------------------------------------------------------------------- bf16 split kernel
+// Shared-memory plan of the tcgen05 split kernel (offsets from a 1024-aligned base).
+constexpr int kTcThreads = 192;                       // warps 0-3 softmax, 4 TMA, 5 MMA
+constexpr int kBoxBytes = kTileRows * 128;            // 128 rows x 64 bf16 columns
+constexpr int kSlots = 10;                            // ring of box slots
+constexpr int kSUnit = 10;                            // positions of a score unit (9 boxes + pad)
+constexpr int kPVUnit = 8;                            // positions of a PV unit (latent boxes)
+constexpr int kQN = 2 * kHeadGroup;                   // hi | lo query rows
+constexpr int kQBoxBytes = kQN * 128;
+constexpr int kPSub = kQN * 128;                      // P^T: 64 tile rows of kQN rows
+constexpr int kPBytes = 2 * kPSub;                    // 128 tile rows
+constexpr int kOffQ = kSlots * kBoxBytes;
+constexpr int kOffP = kOffQ + 9 * kQBoxBytes;         // two P^T buffers
+constexpr int kOffRed = kOffP + 2 * kPBytes;          // [2][16 heads][4 warps] tile maxima
+constexpr int kOffLsum = kOffRed + 2 * kHeadGroup * 4 * 4;
+constexpr int kOffBar = kOffLsum + kHeadGroup * 4 * 4;
+constexpr int BAR_FULL = 0, BAR_EMPTY = kSlots, BAR_SFULL = 2 * kSlots, BAR_SFREE = BAR_SFULL + 2,
+              BAR_PFULL = BAR_SFREE + 2, BAR_ODONE = BAR_PFULL + 2, BAR_ZERO = BAR_ODONE + 2,
+              BAR_DONE = BAR_ZERO + 1, kNumBars = BAR_DONE + 1;
+constexpr int kOffSlot = kOffBar + 8 * kNumBars;
+constexpr int kOffAbort = kOffSlot + 16;
+constexpr size_t kTcSmem = 1024 + kOffAbort + 16;
+constexpr uint32_t kTmemCols = 256;                   // S[2] at 0/32, O^T at 64..191
+// Rescale threshold (log2 units): P may grow to 2^8 before O is rescaled.
+constexpr float kRescaleLog2 = 8.f;
+static_assert(kTcSmem <= 232448, "shared memory plan exceeds 227 KB");
+static_assert(kSlots % 2 == 0 && kSUnit % 2 == 0 && kPVUnit % 2 == 0,
+              "PV box pairs must start on even, non-wrapping slots");
+
+// Waits for a phase; gives up (and raises the CTA's abort flag) after kWaitNs,
+// or at once when another role has already raised it.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > kWaitNs) {
+      *abort = 1;
+      return false;
+    }
+  }
 }
 
-template <int NSTAGE>
-__global__ void __launch_bounds__(kThreads, 1)
-    split_bf16_kernel(const __grid_constant__ CUtensorMap tmap, const SplitParams p) {
+// Per-head max (or sum) over the 32 lanes of a warp of v[0..15]: one exchange
+// across the two half-warps, then a butterfly that halves the values held per
+// lane each round; afterwards lane l holds head l & 15.
+template <bool kMax>
+__device__ __forceinline__ float reduce_heads(float v[16], int lane) {
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const float o = __shfl_xor_sync(0xffffffffu, v[k], 16);
+    v[k] = kMax ? fmaxf(v[k], o) : v[k] + o;
+  }
+#pragma unroll
+  for (int half = 8; half >= 1; half >>= 1) {
+    const bool upper = (lane & half) != 0;
+#pragma unroll
+    for (int k = 0; k < half; ++k) {
+      const float send = upper ? v[k] : v[k + half];
+      const float keep = upper ? v[k + half] : v[k];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, half);
+      v[k] = kMax ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  return v[0];
+}
+
+// Unit u of a chunk with T tiles, in the order the MMA issuer runs them:
+// S(0), S(1), PV(0), S(2), PV(1), ..., S(T-1), PV(T-2), PV(T-1).
+__device__ __forceinline__ void unit_of(int u, int T, bool& is_score, int& tile) {
+  if (u == 0) {
+    is_score = true;
+    tile = 0;
+  } else if (u == 2 * T - 1) {
+    is_score = false;
+    tile = T - 1;
+  } else if (u & 1) {
+    is_score = true;
+    tile = (u + 1) >> 1;
+  } else {
+    is_score = false;
+    tile = (u >> 1) - 1;
+  }
+}
+
+// One CTA per (16-head group g, KV chunk j, sequence b), 192 threads.
+//
+// A 128-row tile is 147 KB, too much to double-buffer, so the cache streams in
+// 16 KB boxes (128 rows x 64 columns, 128-byte swizzle) through a 10-slot
+// ring, in two passes per tile:
+//   score pass : boxes 0..8 from HBM (kept in L2 for the second pass)
+//                S[128 rows x 32] = C[128 x 576] . Q^T[576 x 32]   (36 MMAs, M=128,
+//                N=32: the 16 heads' hi and lo query parts)
+//   PV pass    : latent boxes 0..7 again, now from L2
+//                O^T[512 x 32] += C^T[512 x 128] . P^T[128 x 32]  (4 M=128 blocks,
+//                C read MN-major from box pairs)
+// The issuer runs S(t+1) before PV(t), so the next tile's scores overlap the
+// softmax of the current one.  Roles:
+//   warp 4  : TMEM allocation; one lane runs the TMA ring
+//   warp 5  : one lane issues every tcgen05.mma
+//   warps 0-3: one tile row per thread: softmax across the four warps, P^T
+//             (hi | lo bf16) to shared memory; O^T accumulates in TMEM against a
+//             reference maximum per head that only moves when a tile's maximum
+//             exceeds it by 2^8 (then the warps rescale O^T in TMEM).
+// The fp32 query and P reach the tensor core as bf16 hi + lo pairs (the N=32
+// columns), so their rounding stays near 2^-17 relative.
+__global__ void __launch_bounds__(kTcThreads, 1)
+    split_tc_kernel(const __grid_constant__ CUtensorMap tmap, const SplitParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* stages = smem;
-  float* sbuf = reinterpret_cast<float*>(smem + NSTAGE * kStageBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(sbuf + 2 * kWarps * kSTileFloats);
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bars = sbase + kOffBar;
+  float* red = reinterpret_cast<float*>(smem + kOffRed);
+  float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
+  uint32_t* slot_ptr = reinterpret_cast<uint32_t*>(smem + kOffSlot);
 
   const int g = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -81,230 +181,321 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int r0 = j * p.chunk;
   if (r0 >= len) return;  // chunk past the end of this sequence: nothing to do
   const int r1 = min(r0 + p.chunk, len);
-  const int ntiles = (r1 - r0 + kTileRows - 1) / kTileRows;
+  const int T = (r1 - r0 + kTileRows - 1) / kTileRows;
+  const int last_valid = r1 - (r0 + (T - 1) * kTileRows);   // rows of the last tile
   const int row_base = b * p.s_max + r0;
+  const int h0 = g * kHeadGroup;
+  auto bar = [&](int i) { return bars + 8 * i; };
 
-  const uint32_t full0 = smem_u32(full);
-  const uint32_t stage0 = smem_u32(stages);
-  uint64_t policy = 0;
   if (tid == 0) {
-    for (int s = 0; s < NSTAGE; ++s) mbar_init(full0 + 8 * s, 1);
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(bar(BAR_FULL + i), 1);
+      mbar_init(bar(BAR_EMPTY + i), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(BAR_SFULL + i), 1);
+      mbar_init(bar(BAR_SFREE + i), 4);
+      mbar_init(bar(BAR_PFULL + i), 4);
+      mbar_init(bar(BAR_ODONE + i), 1);
+    }
+    mbar_init(bar(BAR_ZERO), 4);
+    mbar_init(bar(BAR_DONE), 1);
+    *abort_flag = 0;
     fence_mbarrier_init();
   }
+  if (warp == 4) tmem_alloc(smem_u32(slot_ptr), kTmemCols);
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot_ptr;
 
-  auto issue = [&](int tile, int stage) {
-    const uint32_t bar = full0 + 8 * stage;
-    const uint32_t dst = stage0 + stage * kStageBytes;
-    mbar_arrive_expect_tx(bar, kStageBytes);
-#pragma unroll
-    for (int k = 0; k < 9; ++k)
-      tma_load_2d(dst + k * kSubBytes, &tmap, 64 * k, row_base + tile * kTileRows, bar, policy);
-  };
-  if (tid == 0) {
-    prefetch_tmap(&tmap);
-    policy = l2_evict_first_policy();
-    for (int s = 0; s < NSTAGE && s < ntiles; ++s) issue(s, s);
-  }
-
-  // Query fragments for this warp's quarter of the 576 columns (9 k-steps of
-  // 16).  The fp32 query enters the tensor cores as hi + lo bf16 parts, so its
-  // rounding stays near 2^-17 relative (bf16 alone is not enough when a few
-  // large rows dominate the softmax).
-  const int gq = lane >> 2, cq = lane & 3;
-  const int h0 = g * kHeadGroup;
-  const float* qa_base = static_cast<const float*>(p.q_abs);
-  const float* qp_base = static_cast<const float*>(p.q_pe);
-  uint32_t qh[9][4], ql[9][4];
-#pragma unroll
-  for (int ks = 0; ks < 9; ++ks) {
-    const int k0 = 144 * warp + 16 * ks;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int h = h0 + gq + ((e & 1) ? 8 : 0);
-      const int k = k0 + 2 * cq + ((e & 2) ? 8 : 0);
-      const float* src = (k < kDc) ? qa_base + (size_t(b) * p.H + h) * kDc + k
-                                   : qp_base + (size_t(b) * p.H + h) * kDr + (k - kDc);
-      const float2 v = *reinterpret_cast<const float2*>(src);
-      split_bf16(v.x, v.y, qh[ks][e], ql[ks][e]);
-    }
-  }
-
-  float o[16][4];
-#pragma unroll
-  for (int nb = 0; nb < 16; ++nb) o[nb][0] = o[nb][1] = o[nb][2] = o[nb][3] = 0.f;
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-  for (int i = 0; i < ntiles; ++i) {
-    const int s = i % NSTAGE;
-    const uint32_t parity = (i / NSTAGE) & 1;
-    const bool ok = mbar_wait_bounded(full0 + 8 * s, parity);
-    const uint32_t st = stage0 + s * kStageBytes;
-
-    // Partial scores over this warp's 144 columns, all 32 rows (4 n-blocks of 8).
-    float acc[4][4];
-#pragma unroll
-    for (int nb = 0; nb < 4; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < 9; ++ks) {
-      const int k0 = 144 * warp + 16 * ks;
-      const int sub = k0 >> 6, kin = k0 & 63;
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        const int row = np * 16 + ((lane >> 4) << 3) + (lane & 7);
-        const int ch = (kin >> 3) + ((lane >> 3) & 1);
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(st + sub * kSubBytes + sw128(row, ch), b0, b1, b2, b3);
-        mma_bf16(acc[2 * np], qh[ks], b0, b1);
-        mma_bf16(acc[2 * np], ql[ks], b0, b1);
-        mma_bf16(acc[2 * np + 1], qh[ks], b2, b3);
-        mma_bf16(acc[2 * np + 1], ql[ks], b2, b3);
-      }
-    }
-    float* sb = sbuf + ((i & 1) * kWarps + warp) * kSTileFloats;
-#pragma unroll
-    for (int nb = 0; nb < 4; ++nb) {
-      *reinterpret_cast<float2*>(sb + gq * kSStride + nb * 8 + 2 * cq) =
-          make_float2(acc[nb][0], acc[nb][1]);
-      *reinterpret_cast<float2*>(sb + (gq + 8) * kSStride + nb * 8 + 2 * cq) =
-          make_float2(acc[nb][2], acc[nb][3]);
-    }
-
-    const int valid = min(kTileRows, r1 - (r0 + i * kTileRows));
-    if (__syncthreads_or(!ok)) {
-      // A copy did not land in time: report, give in-flight copies a bounded
-      // chance to finish, and leave without touching the outputs.
-      if (tid == 0) {
-        report(p.status, MLA_DEV_PIPELINE_TIMEOUT);
-        for (int t = i; t < ntiles && t < i + NSTAGE; ++t)
-          mbar_wait_bounded(full0 + 8 * (t % NSTAGE), (t / NSTAGE) & 1);
-      }
-      return;
-    }
-    // The previous tile's stage is free (every warp is past its PV product).
-    if (tid == 0 && i >= 1 && i - 1 + NSTAGE < ntiles) {
-      fence_proxy_async_smem();
-      issue(i - 1 + NSTAGE, (i - 1) % NSTAGE);
-    }
-    if (valid < kTileRows) {
-      // Rows past the sequence end may hold anything (NaN included): zero them
-      // so that P = 0 times the row contributes exactly 0 to the PV product.
-      const int nchunks = (kTileRows - valid) * 9 * 8;
-      for (int c = tid; c < nchunks; c += kThreads) {
-        const int sub = c / ((kTileRows - valid) * 8);
-        const int rem = c % ((kTileRows - valid) * 8);
-        const int row = valid + rem / 8, ch = rem % 8;
-        *reinterpret_cast<uint4*>(stages + s * kStageBytes + sub * kSubBytes + row * 128 +
-                                  ch * 16) = make_uint4(0, 0, 0, 0);
-      }
-      __syncthreads();
-    }
-
-    // Full scores for this thread's elements (heads gq, gq+8; rows nb*8+2cq+{0,1}).
-    const float* sb0 = sbuf + (i & 1) * kWarps * kSTileFloats;
-    float sc[4][4];
-#pragma unroll
-    for (int nb = 0; nb < 4; ++nb) {
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        float2 v = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-          const float2 t = *reinterpret_cast<const float2*>(
-              sb0 + w * kSTileFloats + (gq + 8 * hh) * kSStride + nb * 8 + 2 * cq);
-          v.x += t.x;
-          v.y += t.y;
+  // The ring does not depend on the query: the producer starts at once.
+  if (warp == 4) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tmap);
+      const uint64_t keep = l2_evict_last_policy();     // read again by the PV pass
+      const uint64_t stream = l2_evict_first_policy();  // last read
+      int pos = 0;
+      for (int u = 0; u < 2 * T; ++u) {
+        bool is_score;
+        int t;
+        unit_of(u, T, is_score, t);
+        const int n = is_score ? kSUnit : kPVUnit;
+        for (int k = 0; k < n; ++k, ++pos) {
+          const int sl = pos % kSlots, use = pos / kSlots;
+          if (use > 0 && !wait_or_abort(bar(BAR_EMPTY + sl), (use - 1) & 1, abort_flag)) break;
+          if (is_score && k == 9) {
+            mbar_arrive(bar(BAR_FULL + sl));   // padding position: nothing to load
+          } else {
+            mbar_arrive_expect_tx(bar(BAR_FULL + sl), kBoxBytes);
+            tma_load_2d(sbase + sl * kBoxBytes, &tmap, 64 * k, row_base + t * kTileRows,
+                        bar(BAR_FULL + sl), is_score ? keep : stream);
+          }
         }
-        const int row = nb * 8 + 2 * cq;
-        sc[nb][2 * hh] = row < valid ? v.x * p.scale_log2 : -INFINITY;
-        sc[nb][2 * hh + 1] = row + 1 < valid ? v.y * p.scale_log2 : -INFINITY;
-      }
-    }
-    float mx0 = -INFINITY, mx1 = -INFINITY;
-#pragma unroll
-    for (int nb = 0; nb < 4; ++nb) {
-      mx0 = fmaxf(mx0, fmaxf(sc[nb][0], sc[nb][1]));
-      mx1 = fmaxf(mx1, fmaxf(sc[nb][2], sc[nb][3]));
-    }
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float mu0 = mn0 == -INFINITY ? 0.f : mn0;
-    const float mu1 = mn1 == -INFINITY ? 0.f : mn1;
-    const float a0 = ex2(m0 - mu0), a1 = ex2(m1 - mu1);
-    m0 = mn0;
-    m1 = mn1;
-    float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-    for (int nb = 0; nb < 4; ++nb) {
-      sc[nb][0] = ex2(sc[nb][0] - mu0);
-      sc[nb][1] = ex2(sc[nb][1] - mu0);
-      sc[nb][2] = ex2(sc[nb][2] - mu1);
-      sc[nb][3] = ex2(sc[nb][3] - mu1);
-      ps0 += sc[nb][0] + sc[nb][1];
-      ps1 += sc[nb][2] + sc[nb][3];
-    }
-    l0 = l0 * a0 + ps0;
-    l1 = l1 * a1 + ps1;
-    // P as hi + lo bf16 parts (A operand of the PV product).
-    uint32_t ph[2][4], pl[2][4];
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      split_bf16(sc[2 * kk][0], sc[2 * kk][1], ph[kk][0], pl[kk][0]);
-      split_bf16(sc[2 * kk][2], sc[2 * kk][3], ph[kk][1], pl[kk][1]);
-      split_bf16(sc[2 * kk + 1][0], sc[2 * kk + 1][1], ph[kk][2], pl[kk][2]);
-      split_bf16(sc[2 * kk + 1][2], sc[2 * kk + 1][3], ph[kk][3], pl[kk][3]);
-    }
-#pragma unroll
-    for (int nb = 0; nb < 16; ++nb) {
-      o[nb][0] *= a0;
-      o[nb][1] *= a0;
-      o[nb][2] *= a1;
-      o[nb][3] *= a1;
-    }
-    // O[16 x 128 (this warp's columns)] += P[16 x 32] . C[32 x 128]
-#pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-#pragma unroll
-      for (int np = 0; np < 8; ++np) {
-        const int col0 = 128 * warp + 16 * np;
-        const int sub = col0 >> 6, cin = col0 & 63;
-        const int mi = lane >> 3;
-        const int t = kk * 16 + ((mi & 1) << 3) + (lane & 7);
-        const int ch = (cin >> 3) + (mi >> 1);
-        uint32_t r0_, r1_, r2_, r3_;
-        ldsm_x4_t(st + sub * kSubBytes + sw128(t, ch), r0_, r1_, r2_, r3_);
-        mma_bf16(o[2 * np], ph[kk], r0_, r1_);
-        mma_bf16(o[2 * np], pl[kk], r0_, r1_);
-        mma_bf16(o[2 * np + 1], ph[kk], r2_, r3_);
-        mma_bf16(o[2 * np + 1], pl[kk], r2_, r3_);
+        if (*abort_flag) break;
       }
     }
   }
 
-  // Epilogue: normalise by the softmax denominator and write the chunk's partials.
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-  const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f;
-  const float inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
-  const size_t base = (size_t(b) * p.splits + j) * p.H + h0;
-  float* po = p.part_o + base * kDc;
+  // Query rows of the score MMA's B operand (K-major, 128-byte swizzle):
+  // row n < 16 holds bf16(q) of head n, row 16 + n holds bf16(q - bf16(q)).
+  // All loads of a thread are issued before the first store.
+  if (warp != 4) {
+    constexpr int kPairs = kHeadGroup * kRow / 2;
+    constexpr int kFill = 160;                        // warps 0-3 and 5
+    constexpr int kPerThread = (kPairs + kFill - 1) / kFill;
+    const int ft = warp < 4 ? tid : tid - 32;
+    const float* qa = static_cast<const float*>(p.q_abs);
+    const float* qp = static_cast<const float*>(p.q_pe);
+    float2 v[kPerThread];
 #pragma unroll
-  for (int nb = 0; nb < 16; ++nb) {
-    const int col = 128 * warp + nb * 8 + 2 * cq;
-    *reinterpret_cast<float2*>(po + size_t(gq) * kDc + col) =
-        make_float2(o[nb][0] * inv0, o[nb][1] * inv0);
-    *reinterpret_cast<float2*>(po + size_t(gq + 8) * kDc + col) =
-        make_float2(o[nb][2] * inv1, o[nb][3] * inv1);
+    for (int r = 0; r < kPerThread; ++r) {
+      const int idx = ft + kFill * r;
+      if (idx < kPairs) {
+        const int h = idx / (kRow / 2), k = 2 * (idx % (kRow / 2));
+        const size_t bh = size_t(b) * p.H + h0 + h;
+        v[r] = k < kDc ? *reinterpret_cast<const float2*>(qa + bh * kDc + k)
+                       : *reinterpret_cast<const float2*>(qp + bh * kDr + (k - kDc));
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < kPerThread; ++r) {
+      const int idx = ft + kFill * r;
+      if (idx < kPairs) {
+        const int h = idx / (kRow / 2), k = 2 * (idx % (kRow / 2));
+        uint32_t hi, lo;
+        split_bf16(v[r].x, v[r].y, hi, lo);
+        const int box = k >> 6, ch = (k & 63) >> 3, w = k & 7;
+        *reinterpret_cast<uint32_t*>(smem + kOffQ + box * kQBoxBytes + sw128(h, ch) + 2 * w) = hi;
+        *reinterpret_cast<uint32_t*>(smem + kOffQ + box * kQBoxBytes +
+                                     sw128(h + kHeadGroup, ch) + 2 * w) = lo;
+      }
+    }
+    fence_proxy_async_smem();
+    named_bar_sync(2, 160);        // warps 0-3 and 5: the query is in place
   }
-  if (warp == 0 && cq == 0) {
-    p.part_lse[base + gq] = l0 > 0.f ? (m0 + log2f(l0)) * kLn2 : -INFINITY;
-    p.part_lse[base + gq + 8] = l1 > 0.f ? (m1 + log2f(l1)) * kLn2 : -INFINITY;
+
+  if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = umma_idesc_bf16(128, kQN, 0, 0);
+      constexpr uint32_t idesc_o = umma_idesc_bf16(128, kQN, 1, 0);
+      // Base descriptors; a K step only moves the 14-bit start-address field,
+      // so each MMA adds an offset (16-byte units) to a base.
+      const uint64_t dA0 = umma_desc_sw128(sbase, 16, 1024);            // score A: K-major box
+      const uint64_t dQ0 = umma_desc_sw128(sbase + kOffQ, 16, 1024);    // Q hi|lo
+      const uint64_t dC0 = umma_desc_sw128(sbase, kBoxBytes, 1024);     // PV A: MN-major pair
+      const uint64_t dP0 = umma_desc_sw128(sbase + kOffP, 16, 1024);    // P^T
+      int pos = 0;
+      bool ok = true;
+      for (int u = 0; u < 2 * T && ok; ++u) {
+        bool is_score;
+        int t;
+        unit_of(u, T, is_score, t);
+        if (is_score) {
+          const int sb = t & 1;
+          if (t >= 2) ok = wait_or_abort(bar(BAR_SFREE + sb), ((t - 2) >> 1) & 1, abort_flag);
+          for (int k = 0; k < kSUnit && ok; ++k, ++pos) {
+            const int sl = pos % kSlots, use = pos / kSlots;
+            ok = wait_or_abort(bar(BAR_FULL + sl), use & 1, abort_flag);
+            if (!ok) break;
+            if (k == 9) {
+              mbar_arrive(bar(BAR_EMPTY + sl));
+              continue;
+            }
+            tc_fence_after();
+            const uint64_t a = dA0 + static_cast<uint64_t>((sl * kBoxBytes) >> 4);
+            const uint64_t q = dQ0 + static_cast<uint64_t>((k * kQBoxBytes) >> 4);
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4)
+              umma_bf16(tmem + 32 * sb, a + ((s4 * 32) >> 4), q + ((s4 * 32) >> 4), idesc_s,
+                        (k > 0 || s4 > 0) ? 1u : 0u);
+            umma_commit(bar(BAR_EMPTY + sl));
+          }
+          if (ok) umma_commit(bar(BAR_SFULL + sb));
+        } else {
+          const int pb = t & 1;
+          ok = wait_or_abort(bar(BAR_PFULL + pb), (t >> 1) & 1, abort_flag);
+          if (ok && t == T - 1 && last_valid < kTileRows)
+            ok = wait_or_abort(bar(BAR_ZERO), 0, abort_flag);
+          const uint64_t pd = dP0 + static_cast<uint64_t>((pb * kPBytes) >> 4);
+          for (int mb = 0; mb < 4 && ok; ++mb) {
+            const int p0 = pos + 2 * mb;
+            const int s0 = p0 % kSlots;
+            ok = wait_or_abort(bar(BAR_FULL + s0), (p0 / kSlots) & 1, abort_flag) &&
+                 wait_or_abort(bar(BAR_FULL + s0 + 1), ((p0 + 1) / kSlots) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            const uint64_t c = dC0 + static_cast<uint64_t>((s0 * kBoxBytes) >> 4);
+#pragma unroll
+            for (int ks = 0; ks < kTileRows / 16; ++ks)
+              umma_bf16(tmem + 64 + 32 * mb, c + ((ks * 2048) >> 4),
+                        pd + (((ks >> 2) * kPSub + (ks & 3) * 32) >> 4), idesc_o,
+                        (t > 0 || ks > 0) ? 1u : 0u);
+            umma_commit(bar(BAR_EMPTY + s0));
+            umma_commit(bar(BAR_EMPTY + s0 + 1));
+          }
+          pos += kPVUnit;
+          if (ok) umma_commit(bar(BAR_ODONE + pb));
+        }
+      }
+      // Every MMA this thread issued has finished before TMEM is released.
+      umma_commit(bar(BAR_DONE));
+      mbar_wait_bounded(bar(BAR_DONE), 0);
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------------------------ softmax warps
+    const int row = 32 * warp + lane;     // tile row held by this thread
+    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
+    float m[kHeadGroup], l[kHeadGroup];
+#pragma unroll
+    for (int h = 0; h < kHeadGroup; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+    }
+    for (int t = 0; t < T; ++t) {
+      const int sb = t & 1;
+      const int valid = t == T - 1 ? last_valid : kTileRows;
+      wait_or_abort(bar(BAR_SFULL + sb), (t >> 1) & 1, abort_flag);
+      tc_fence_after();
+      float v[32];
+      tmem_ld32(tmem + lane_base + 32 * sb, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_SFREE + sb));
+      const bool rv = row < valid;
+      float sc[kHeadGroup], tt[kHeadGroup];
+#pragma unroll
+      for (int h = 0; h < kHeadGroup; ++h) {
+        sc[h] = rv ? (v[h] + v[kHeadGroup + h]) * p.scale_log2 : -INFINITY;
+        tt[h] = sc[h];
+      }
+      float* rd = red + sb * kHeadGroup * 4;
+      const float wmax = reduce_heads<true>(tt, lane);
+      if (lane < 16) rd[lane * 4 + warp] = wmax;
+      named_bar_sync(1, 128);
+      bool need = false;
+      float tmax[kHeadGroup];
+#pragma unroll
+      for (int h = 0; h < kHeadGroup; ++h) {
+        const float4 q4 = *reinterpret_cast<const float4*>(rd + h * 4);
+        tmax[h] = fmaxf(fmaxf(q4.x, q4.y), fmaxf(q4.z, q4.w));
+        need |= tmax[h] > m[h] + kRescaleLog2;
+      }
+      if (need) {
+        // Move the reference maxima; rescale the row sums and the O^T
+        // accumulated so far (in TMEM, after the previous PV finished).
+        float alpha[kHeadGroup];
+#pragma unroll
+        for (int h = 0; h < kHeadGroup; ++h) {
+          const float mn = fmaxf(m[h], tmax[h]);
+          alpha[h] = m[h] == -INFINITY ? 0.f : ex2(m[h] - mn);
+          m[h] = mn;
+          l[h] *= alpha[h];
+        }
+        if (t > 0) {
+          wait_or_abort(bar(BAR_ODONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag);
+          tc_fence_after();
+#pragma unroll
+          for (int mb = 0; mb < 4; ++mb) {
+            float o[32];
+            tmem_ld32(tmem + lane_base + 64 + 32 * mb, o);
+#pragma unroll
+            for (int h = 0; h < kHeadGroup; ++h) {
+              o[h] *= alpha[h];
+              o[kHeadGroup + h] *= alpha[h];
+            }
+            tmem_st32(tmem + lane_base + 64 + 32 * mb, o);
+          }
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < kHeadGroup; ++h) {
+        const float mu = m[h] == -INFINITY ? 0.f : m[h];
+        sc[h] = ex2(sc[h] - mu);
+        l[h] += sc[h];
+      }
+      // P^T buffer sb was last read by the PV of tile t-2.
+      if (t >= 2) wait_or_abort(bar(BAR_ODONE + sb), ((t - 2) >> 1) & 1, abort_flag);
+      {
+        // P^T (B operand of the PV MMA, K-major 128-byte swizzle, two 64-row
+        // halves): row n < 16 is bf16(p) of head n, row 16 + n is
+        // bf16(p - bf16(p)); the K index is the tile row.
+        uint8_t* pbuf = smem + kOffP + sb * kPBytes + (row >> 6) * kPSub;
+        const int ch = (row & 63) >> 3, w = row & 7;
+#pragma unroll
+        for (int h = 0; h < kHeadGroup; ++h) {
+          const __nv_bfloat16 hi = __float2bfloat16_rn(sc[h]);
+          const __nv_bfloat16 lo = __float2bfloat16_rn(sc[h] - __bfloat162float(hi));
+          *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128(h, ch) + 2 * w) = hi;
+          *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128(h + kHeadGroup, ch) + 2 * w) = lo;
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(BAR_PFULL + sb));
+      if (valid < kTileRows) {
+        // Last tile ends inside the sequence: once its PV boxes have landed,
+        // zero the rows past the end (they may hold anything, NaN included) so
+        // that P = 0 times such a row adds exactly 0.
+        const int base = (kSUnit + kPVUnit) * T - kPVUnit;
+        const int nrow = kTileRows - valid;
+        for (int k = 0; k < kPVUnit; ++k) {
+          const int ps = base + k, sl = ps % kSlots;
+          wait_or_abort(bar(BAR_FULL + sl), (ps / kSlots) & 1, abort_flag);
+          for (int c = tid; c < nrow * 8; c += kThreads)
+            *reinterpret_cast<uint4*>(smem + sl * kBoxBytes + (valid + c / 8) * 128 +
+                                      (c % 8) * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_ZERO));
+      }
+    }
+    // Softmax denominators over the chunk's rows.
+    {
+      float tt[kHeadGroup];
+#pragma unroll
+      for (int h = 0; h < kHeadGroup; ++h) tt[h] = l[h];
+      const float ws = reduce_heads<false>(tt, lane);
+      if (lane < 16) lsum[lane * 4 + warp] = ws;
+    }
+    // O^T after the last PV: this thread's latent row d = 128 mb + 32 warp + lane.
+    wait_or_abort(bar(BAR_ODONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1, abort_flag);
+    tc_fence_after();
+    named_bar_sync(1, 128);
+    if (!*abort_flag) {
+      const size_t base = (size_t(b) * p.splits + j) * p.H + h0;
+      float inv[kHeadGroup];
+#pragma unroll
+      for (int h = 0; h < kHeadGroup; ++h) {
+        const float4 q4 = *reinterpret_cast<const float4*>(lsum + h * 4);
+        const float L = (q4.x + q4.y) + (q4.z + q4.w);
+        inv[h] = L > 0.f ? 1.f / L : 0.f;
+        if (warp == 0 && lane == h)
+          p.part_lse[base + h] = L > 0.f ? (m[h] + log2f(L)) * kLn2 : -INFINITY;
+      }
+#pragma unroll
+      for (int mb = 0; mb < 4; ++mb) {
+        float o[32];
+        tmem_ld32(tmem + lane_base + 64 + 32 * mb, o);
+#pragma unroll
+        for (int h = 0; h < kHeadGroup; ++h)
+          p.part_o[(base + h) * kDc + 128 * mb + 32 * warp + lane] =
+              (o[h] + o[kHeadGroup + h]) * inv[h];
+      }
+    }
   }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 4) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+  if (tid == 0 && *abort_flag) report(p.status, MLA_DEV_PIPELINE_TIMEOUT);
 }
 
 // fp32 path: one CTA per (head, chunk, sequence); each warp runs its own online
@@ -414,13 +605,22 @@ __global__ void __launch_bounds__(128)
   const float inv = 1.f / sum;
   const float* po = p.part_o + (size_t(b) * p.splits * p.H + h) * kDc;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s = 0; s < nsplit; ++s) {
-    const float w = wts[s] * inv;
-    const float4 v = reinterpret_cast<const float4*>(po + size_t(s) * stride * kDc)[tid];
-    acc.x = fmaf(w, v.x, acc.x);
-    acc.y = fmaf(w, v.y, acc.y);
-    acc.z = fmaf(w, v.z, acc.z);
-    acc.w = fmaf(w, v.w, acc.w);
+  // Eight chunk partials in flight per thread before they are accumulated.
+  for (int s0 = 0; s0 < nsplit; s0 += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      v[u] = s0 + u < nsplit
+                 ? reinterpret_cast<const float4*>(po + size_t(s0 + u) * stride * kDc)[tid]
+                 : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float w = s0 + u < nsplit ? wts[s0 + u] * inv : 0.f;
+      acc.x = fmaf(w, v[u].x, acc.x);
+      acc.y = fmaf(w, v[u].y, acc.y);
+      acc.z = fmaf(w, v[u].z, acc.z);
+      acc.w = fmaf(w, v[u].w, acc.w);
+    }
   }
   reinterpret_cast<float4*>(out)[tid] = acc;
   if (tid == 0 && lse_out) lse_out[size_t(b) * p.H + h] = mx + logf(sum);
@@ -584,19 +784,17 @@ extern "C" mla_status mla_decode_split(const mla_dims* dims, const void* q_abs, 
       set_error("%s: cuTensorMapEncodeTiled failed (%d)", who, int(r));
       return MLA_ERR_CUDA;
     }
-    constexpr size_t smem = bf16_smem_bytes(kNumStagesBf16);
     static bool attr_set = false;
     if (!attr_set) {
-      if (cudaFuncSetAttribute(split_bf16_kernel<kNumStagesBf16>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               int(smem)) != cudaSuccess) {
-        set_error("%s: cannot reserve %zu bytes of shared memory", who, smem);
+      if (cudaFuncSetAttribute(split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               int(kTcSmem)) != cudaSuccess) {
+        set_error("%s: cannot reserve %zu bytes of shared memory", who, kTcSmem);
         return MLA_ERR_CUDA;
       }
       attr_set = true;
     }
     dim3 grid(dims->heads / kHeadGroup, p.splits, dims->batch);
-    split_bf16_kernel<kNumStagesBf16><<<grid, kThreads, smem, s>>>(tmap, p);
+    split_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(tmap, p);
   } else {
     dim3 grid(dims->heads, p.splits, dims->batch);
     split_f32_kernel<<<grid, kThreads, 0, s>>>(p);

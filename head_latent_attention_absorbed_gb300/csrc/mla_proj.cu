@@ -8,9 +8,11 @@
 // Multi-Head Latent Attention (Lior Sinai) 3.3 (W^UK is absorbed into the query
 // side, W^UV applied after the latent attention, eq. 3.3.3) and 3.7 (RoPE as a
 // complex rotation of adjacent pairs).  Both products are small batched GEMMs
-// whose time goes into streaming the bf16 weights once; the bf16 kernels stage
-// a weight tile in shared memory (XOR-swizzled 16-byte chunks) and run the
-// batch as the M side of mma.sync m16n8k16 with fp32 accumulation.
+// whose time goes into reading the bf16 weights once; with at most a few
+// hundred FLOPs per weight byte they are latency-bound, so the kernels spread
+// the weights over many small CTAs, issue every global load of a CTA before
+// its first use, and run the batch as the M side of mma.sync m16n8k16 with
+// fp32 accumulation.
 #include <math.h>
 
 #include "mla_common.cuh"
@@ -19,8 +21,14 @@ namespace mla {
 namespace {
 
 // ---------------------------------------------------------------------- RoPE
-// theta_i = base^(-2i/d_rope); the angle pos * theta_i is formed in fp64 so
-// that positions up to 2^31 keep their fractional turns.
+// theta_i = base^(-2i/d_rope) comes from the host in fp64.  The angle
+// pos * theta_i is formed and reduced modulo 2*pi in fp64, so that positions up
+// to 2^31 keep their fractional turns; the reduced angle (|r| <= pi) then goes
+// through single-precision sincosf.
+struct RopeTheta {
+  double theta[kDr / 2];
+};
+
 template <typename T>
 __device__ __forceinline__ float to_f(T v);
 template <>
@@ -29,68 +37,81 @@ template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 template <typename T>
-__device__ void rope_pairs(const T* q_rope, const int32_t* positions, double base, float* q_pe,
-                           int B, int H, int h, int tid, int nthreads) {
-  for (int it = tid; it < B * (kDr / 2); it += nthreads) {
-    const int b = it / (kDr / 2), i = it % (kDr / 2);
-    const double theta = pow(base, -2.0 * i / kDr);
-    const double ang = static_cast<double>(positions[b]) * theta;
-    double sn, cs;
-    sincos(ang, &sn, &cs);
-    const size_t off = (size_t(b) * H + h) * kDr + 2 * i;
-    const double x0 = to_f(q_rope[off]), x1 = to_f(q_rope[off + 1]);
-    q_pe[off] = static_cast<float>(cs * x0 - sn * x1);
-    q_pe[off + 1] = static_cast<float>(sn * x0 + cs * x1);
-  }
+__device__ __forceinline__ void rope_pair(const T* q_rope, const int32_t* positions,
+                                          const RopeTheta& th, float* q_pe, int H, int h, int it) {
+  const int b = it / (kDr / 2), i = it % (kDr / 2);
+  const double two_pi = 6.283185307179586;
+  const double ang = static_cast<double>(positions[b]) * th.theta[i];
+  const double r = ang - two_pi * rint(ang / two_pi);
+  float sn, cs;
+  sincosf(static_cast<float>(r), &sn, &cs);
+  const size_t off = (size_t(b) * H + h) * kDr + 2 * i;
+  const float x0 = to_f(q_rope[off]), x1 = to_f(q_rope[off + 1]);
+  q_pe[off] = cs * x0 - sn * x1;
+  q_pe[off + 1] = sn * x0 + cs * x1;
 }
 
 // ---------------------------------------------------------------------- absorb, bf16
-// grid (H, d_c/64): CTA (h, cb) owns output columns [64cb, 64cb+64) of head h
-// for the whole batch; warp w owns 16 of those columns.
-__global__ void __launch_bounds__(128)
+// grid (H, d_c/16), one warp per CTA: CTA (h, cb) owns output columns
+// [16cb, 16cb+16) of head h for the whole batch.  The 128 x 16 slice of W_UK
+// lands in shared memory through cp.async (all copies in flight at once); the
+// batch rows are the M side of mma.sync m16n8k16.  The CTAs of head h also
+// rotate that head's RoPE pairs, one pair per thread.
+__global__ void __launch_bounds__(32)
     absorb_bf16_kernel(const __nv_bfloat16* __restrict__ q_nope,
                        const __nv_bfloat16* __restrict__ q_rope,
                        const __nv_bfloat16* __restrict__ w_uk, const int32_t* __restrict__ pos,
-                       double base, float* __restrict__ q_abs, float* __restrict__ q_pe, int B,
-                       int H) {
-  __shared__ __align__(128) uint8_t wt[kDn * 128];  // 128 k-rows x 64 bf16 columns
-  const int h = blockIdx.x, cb = blockIdx.y;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int c0 = cb * 64;
-  for (int idx = tid; idx < kDn * 8; idx += 128) {
-    const int k = idx >> 3, ch = idx & 7;
-    const uint4 v = *reinterpret_cast<const uint4*>(w_uk + (size_t(h) * kDn + k) * kDc + c0 + ch * 8);
-    *reinterpret_cast<uint4*>(wt + k * 128 + ((ch ^ (k & 7)) << 4)) = v;
+                       const RopeTheta th, float* __restrict__ q_abs, float* __restrict__ q_pe,
+                       int B, int H) {
+  __shared__ __align__(128) uint8_t wt[kDn * 32];  // 128 k-rows x 16 bf16 columns
+  const int h = blockIdx.x, cb = blockIdx.y, lane = threadIdx.x;
+  const int c0 = cb * 16;
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const int idx = lane + 32 * r;          // 256 chunks of 16 B
+    const int k = idx >> 1, ch = idx & 1;
+    const uint32_t dst = smem_u32(wt + k * 32 + ((ch ^ ((k >> 2) & 1)) << 4));
+    const void* src = w_uk + (size_t(h) * kDn + k) * kDc + c0 + ch * 8;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
   }
-  if (cb == 0) rope_pairs(q_rope, pos, base, q_pe, B, H, h, tid, 128);
-  __syncthreads();
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  for (int it = cb * 32 + lane; it < B * (kDr / 2); it += 32 * gridDim.y)
+    rope_pair(q_rope, pos, th, q_pe, H, h, it);
 
   const int gq = lane >> 2, cq = lane & 3;
   const uint32_t wbase = smem_u32(wt);
   for (int mt = 0; mt * 16 < B; ++mt) {
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     const int bA = mt * 16 + gq, bB = bA + 8;
+    uint32_t a[8][4];
+    const __nv_bfloat16* rA = q_nope + (size_t(bA) * H + h) * kDn + 2 * cq;
+    const __nv_bfloat16* rB = q_nope + (size_t(bB) * H + h) * kDn + 2 * cq;
 #pragma unroll
-    for (int ks = 0; ks < kDn / 16; ++ks) {
-      const int k0 = ks * 16;
-      uint32_t a[4];
-      const __nv_bfloat16* rA = q_nope + (size_t(bA) * H + h) * kDn + k0 + 2 * cq;
-      const __nv_bfloat16* rB = q_nope + (size_t(bB) * H + h) * kDn + k0 + 2 * cq;
-      a[0] = bA < B ? *reinterpret_cast<const uint32_t*>(rA) : 0u;
-      a[1] = bB < B ? *reinterpret_cast<const uint32_t*>(rB) : 0u;
-      a[2] = bA < B ? *reinterpret_cast<const uint32_t*>(rA + 8) : 0u;
-      a[3] = bB < B ? *reinterpret_cast<const uint32_t*>(rB + 8) : 0u;
+    for (int ks = 0; ks < 8; ++ks) {
+      a[ks][0] = bA < B ? *reinterpret_cast<const uint32_t*>(rA + 16 * ks) : 0u;
+      a[ks][1] = bB < B ? *reinterpret_cast<const uint32_t*>(rB + 16 * ks) : 0u;
+      a[ks][2] = bA < B ? *reinterpret_cast<const uint32_t*>(rA + 16 * ks + 8) : 0u;
+      a[ks][3] = bB < B ? *reinterpret_cast<const uint32_t*>(rB + 16 * ks + 8) : 0u;
+    }
+    if (mt == 0) {
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      __syncwarp();
+    }
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      // B fragments of n-blocks 0 and 1 for k in [16ks, 16ks+16): ldmatrix.trans
+      // of the [k][n] slice (32-byte rows, 16-byte chunks swizzled by bit 2 of k).
       const int mi = lane >> 3;
-      const int k = k0 + ((mi & 1) << 3) + (lane & 7);
-      const int ch = 2 * warp + (mi >> 1);
+      const int k = 16 * ks + ((mi & 1) << 3) + (lane & 7);
+      const int ch = mi >> 1;
       uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(wbase + k * 128 + ((ch ^ (k & 7)) << 4), b0, b1, b2, b3);
-      mma_bf16(acc[0], a, b0, b1);
-      mma_bf16(acc[1], a, b2, b3);
+      ldsm_x4_t(wbase + k * 32 + ((ch ^ ((k >> 2) & 1)) << 4), b0, b1, b2, b3);
+      mma_bf16(acc[0], a[ks], b0, b1);
+      mma_bf16(acc[1], a[ks], b2, b3);
     }
 #pragma unroll
     for (int nb = 0; nb < 2; ++nb) {
-      const int c = c0 + 16 * warp + 8 * nb + 2 * cq;
+      const int c = c0 + 8 * nb + 2 * cq;
       if (bA < B)
         *reinterpret_cast<float2*>(q_abs + (size_t(bA) * H + h) * kDc + c) =
             make_float2(acc[nb][0], acc[nb][1]);
@@ -106,15 +127,16 @@ __global__ void __launch_bounds__(128)
 __global__ void __launch_bounds__(128)
     absorb_f32_kernel(const float* __restrict__ q_nope, const float* __restrict__ q_rope,
                       const float* __restrict__ w_uk, const int32_t* __restrict__ pos,
-                      double base, float* __restrict__ q_abs, float* __restrict__ q_pe, int B,
-                      int H) {
+                      const RopeTheta th, float* __restrict__ q_abs, float* __restrict__ q_pe,
+                      int B, int H) {
   __shared__ float q[kDn];
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
   q[tid] = q_nope[(size_t(b) * H + h) * kDn + tid];
-  if (b == 0) rope_pairs(q_rope, pos, base, q_pe, B, H, h, tid, 128);
+  if (tid < kDr / 2) rope_pair(q_rope, pos, th, q_pe, H, h, b * (kDr / 2) + tid);
   __syncthreads();
   const float* w = w_uk + size_t(h) * kDn * kDc;
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
   for (int k = 0; k < kDn; ++k) {
 #pragma unroll
     for (int r = 0; r < 4; ++r) acc[r] = fmaf(q[k], w[size_t(k) * kDc + tid + 128 * r], acc[r]);
@@ -124,59 +146,62 @@ __global__ void __launch_bounds__(128)
 }
 
 // ---------------------------------------------------------------------- out_proj, bf16
-// grid (H, d_v/32): CTA (h, eb) owns outputs e in [32eb, 32eb+32) for the whole
-// batch; warp w owns 8 of them.  o_c (fp32) enters the mma as bf16 hi + lo
-// halves, so its rounding stays below 2^-16 relative.
+// grid (H, d_v/8): CTA (h, eb) owns outputs e in [8eb, 8eb+8) for the whole
+// batch; warp w contracts the 128-wide quarter [128w, 128w+128) of d_c and the
+// four partial sums meet in shared memory.  W_UV's rows are K-contiguous, so
+// its B fragments come straight from global memory; o_c (fp32) enters the mma
+// as bf16 hi + lo parts, keeping its rounding near 2^-17 relative.  Every
+// load of a batch tile is issued before the first mma.
 __global__ void __launch_bounds__(128)
     out_proj_bf16_kernel(const float* __restrict__ o_c, const __nv_bfloat16* __restrict__ w_uv,
                          float* __restrict__ out, int B, int H) {
-  __shared__ __align__(128) uint8_t wt[32 * kDc * 2];  // 32 e-rows x 512 bf16
+  __shared__ float red[4][16][9];
   const int h = blockIdx.x, eb = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int e0 = eb * 32;
-  for (int idx = tid; idx < 32 * 64; idx += 128) {
-    const int e = idx >> 6, ch = idx & 63;
-    const uint4 v = *reinterpret_cast<const uint4*>(w_uv + (size_t(h) * kDv + e0 + e) * kDc + ch * 8);
-    *reinterpret_cast<uint4*>(wt + e * 1024 + ((ch ^ (e & 7)) << 4)) = v;
-  }
-  __syncthreads();
   const int gq = lane >> 2, cq = lane & 3;
-  const uint32_t wbase = smem_u32(wt);
+  const int kw = 128 * warp;
+  uint32_t bf[8][2];
+  const __nv_bfloat16* wrow = w_uv + (size_t(h) * kDv + 8 * eb + gq) * kDc + kw + 2 * cq;
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    bf[ks][0] = *reinterpret_cast<const uint32_t*>(wrow + 16 * ks);
+    bf[ks][1] = *reinterpret_cast<const uint32_t*>(wrow + 16 * ks + 8);
+  }
   for (int mt = 0; mt * 16 < B; ++mt) {
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const int bA = mt * 16 + gq, bB = bA + 8;
-    const float* rA = o_c + (size_t(bA) * H + h) * kDc + 2 * cq;
-    const float* rB = o_c + (size_t(bB) * H + h) * kDc + 2 * cq;
-    for (int ks2 = 0; ks2 < kDc / 32; ++ks2) {
-      const int e = 8 * warp + (lane & 7);
-      const int ch = ks2 * 4 + (lane >> 3);
-      uint32_t bf[4];
-      ldsm_x4(wbase + e * 1024 + ((ch ^ (e & 7)) << 4), bf[0], bf[1], bf[2], bf[3]);
+    const float* rA = o_c + (size_t(bA) * H + h) * kDc + kw + 2 * cq;
+    const float* rB = o_c + (size_t(bB) * H + h) * kDc + kw + 2 * cq;
+    float2 x[8][4];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int k0 = ks2 * 32 + half * 16;
-        float2 x[4];
-        x[0] = bA < B ? *reinterpret_cast<const float2*>(rA + k0) : make_float2(0.f, 0.f);
-        x[1] = bB < B ? *reinterpret_cast<const float2*>(rB + k0) : make_float2(0.f, 0.f);
-        x[2] = bA < B ? *reinterpret_cast<const float2*>(rA + k0 + 8) : make_float2(0.f, 0.f);
-        x[3] = bB < B ? *reinterpret_cast<const float2*>(rB + k0 + 8) : make_float2(0.f, 0.f);
-        uint32_t hi[4], lo[4];
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const __nv_bfloat162 hv = __floats2bfloat162_rn(x[r].x, x[r].y);
-          const float2 hf = __bfloat1622float2(hv);
-          hi[r] = *reinterpret_cast<const uint32_t*>(&hv);
-          lo[r] = pack_bf16(x[r].x - hf.x, x[r].y - hf.y);
-        }
-        mma_bf16(acc, hi, bf[2 * half], bf[2 * half + 1]);
-        mma_bf16(acc, lo, bf[2 * half], bf[2 * half + 1]);
-      }
+    for (int ks = 0; ks < 8; ++ks) {
+      const float2 z = make_float2(0.f, 0.f);
+      x[ks][0] = bA < B ? *reinterpret_cast<const float2*>(rA + 16 * ks) : z;
+      x[ks][1] = bB < B ? *reinterpret_cast<const float2*>(rB + 16 * ks) : z;
+      x[ks][2] = bA < B ? *reinterpret_cast<const float2*>(rA + 16 * ks + 8) : z;
+      x[ks][3] = bB < B ? *reinterpret_cast<const float2*>(rB + 16 * ks + 8) : z;
     }
-    const int e = e0 + 8 * warp + 2 * cq;
-    if (bA < B)
-      *reinterpret_cast<float2*>(out + (size_t(bA) * H + h) * kDv + e) = make_float2(acc[0], acc[1]);
-    if (bB < B)
-      *reinterpret_cast<float2*>(out + (size_t(bB) * H + h) * kDv + e) = make_float2(acc[2], acc[3]);
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      uint32_t hi[4], lo[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) split_bf16(x[ks][r].x, x[ks][r].y, hi[r], lo[r]);
+      mma_bf16(acc, hi, bf[ks][0], bf[ks][1]);
+      mma_bf16(acc, lo, bf[ks][0], bf[ks][1]);
+    }
+    red[warp][gq][2 * cq] = acc[0];
+    red[warp][gq][2 * cq + 1] = acc[1];
+    red[warp][gq + 8][2 * cq] = acc[2];
+    red[warp][gq + 8][2 * cq + 1] = acc[3];
+    __syncthreads();
+    {
+      const int r = tid >> 3, e = tid & 7;  // 16 rows x 8 outputs
+      const int b = mt * 16 + r;
+      if (b < B)
+        out[(size_t(b) * H + h) * kDv + 8 * eb + e] =
+            red[0][r][e] + red[1][r][e] + red[2][r][e] + red[3][r][e];
+    }
+    __syncthreads();
   }
 }
 
@@ -192,6 +217,7 @@ __global__ void __launch_bounds__(128)
   for (int e = warp; e < kDv; e += 4) {
     const float* w = w_uv + (size_t(h) * kDv + e) * kDc;
     float acc = 0.f;
+#pragma unroll 4
     for (int c = lane; c < kDc; c += 32) acc = fmaf(w[c], x[c], acc);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
@@ -225,15 +251,17 @@ extern "C" mla_status mla_absorb_q(const mla_dims* dims, const void* q_nope, con
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int B = dims->batch, H = dims->heads;
+  RopeTheta th;
+  for (int i = 0; i < kDr / 2; ++i) th.theta[i] = pow(rope_base, -2.0 * i / kDr);
   if (dims->dtype == MLA_BF16) {
-    absorb_bf16_kernel<<<dim3(H, kDc / 64), 128, 0, s>>>(
+    absorb_bf16_kernel<<<dim3(H, kDc / 16), 32, 0, s>>>(
         static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(q_rope),
-        static_cast<const __nv_bfloat16*>(w_uk), positions, rope_base,
-        static_cast<float*>(q_abs), static_cast<float*>(q_pe), B, H);
+        static_cast<const __nv_bfloat16*>(w_uk), positions, th, static_cast<float*>(q_abs),
+        static_cast<float*>(q_pe), B, H);
   } else {
     absorb_f32_kernel<<<dim3(H, B), 128, 0, s>>>(
         static_cast<const float*>(q_nope), static_cast<const float*>(q_rope),
-        static_cast<const float*>(w_uk), positions, rope_base, static_cast<float*>(q_abs),
+        static_cast<const float*>(w_uk), positions, th, static_cast<float*>(q_abs),
         static_cast<float*>(q_pe), B, H);
   }
   return launch_status(who);
@@ -255,7 +283,7 @@ extern "C" mla_status mla_out_proj(const mla_dims* dims, const float* o_c, const
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int B = dims->batch, H = dims->heads;
   if (dims->dtype == MLA_BF16) {
-    out_proj_bf16_kernel<<<dim3(H, kDv / 32), 128, 0, s>>>(
+    out_proj_bf16_kernel<<<dim3(H, kDv / 8), 128, 0, s>>>(
         o_c, static_cast<const __nv_bfloat16*>(w_uv), static_cast<float*>(out), B, H);
   } else {
     out_proj_f32_kernel<<<dim3(H, B), 128, 0, s>>>(o_c, static_cast<const float*>(w_uv),
