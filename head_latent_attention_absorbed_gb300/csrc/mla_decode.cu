@@ -6,22 +6,10 @@
 // latent row serves every head (virtual broadcast of C^KV across heads), and
 // the attention output stays in the d_c-wide latent space.
 //
-// bf16 kernel (one CTA per (16-head group, KV chunk, sequence)):
-//   * thread 0 streams 32-row tiles of the cache (32 x 1152 B) through a ring
-//     of shared-memory stages with 2-D TMA loads (nine 64-column boxes per
-//     tile, 128-byte swizzle), each stage completing on its own mbarrier;
-//   * scores S[16 heads x 32 rows] on the tensor cores (mma.sync m16n8k16):
-//     warp w contracts its 144-wide quarter of the 576 columns with the query
-//     held in registers; the four partial score tiles meet in shared memory;
-//   * every warp forms the full scores, runs the online softmax (exp2 domain)
-//     and keeps P in registers as the A operand of the PV product;
-//   * the fp32 query and P enter the bf16 mma as hi + lo parts (two mma per
-//     product), which keeps their rounding near 2^-17 relative;
-//   * warp w accumulates O[16 heads x 128 latent columns] += P . C in fp32
-//     registers, reading the same swizzled stage through ldmatrix.trans;
-//   * one CTA barrier per tile; the stage freed by the previous tile is
-//     refilled right after it.
-// fp32 kernel: plain SIMT, fp32 arithmetic throughout (no TF32).
+// bf16: a tcgen05 kernel run by clusters of two CTAs (see split_tc_kernel);
+// each chunk of rows yields a normalised partial output and its log-sum-exp.
+// fp32: plain SIMT, fp32 arithmetic throughout (no TF32).
+// combine: L = log sum_j exp(lse_j), o_c = sum_j exp(lse_j - L) o_j.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -56,42 +44,65 @@ __device__ __forceinline__ int clamp_length(const SplitParams& p, int b, bool re
 }
 
 // ---------------------------------------------------------------------------- bf16 split kernel
-// Shared-memory plan of the tcgen05 split kernel (offsets from a 1024-aligned base).
-constexpr int kTcThreads = 192;                       // warps 0-3 softmax, 4 TMA, 5 MMA
+// A pair of CTAs (a thread-block cluster of 2, on two SMs) owns one (16-head
+// group, KV chunk, sequence).  The 576 cached columns are split between them,
+// so that each SM streams every byte of its half exactly once while the MMAs
+// still cover 128 rows at a time:
+//   rank 0: latent columns   0..255 (boxes 0-3) and the RoPE columns (box 8)
+//   rank 1: latent columns 256..511 (boxes 4-7)
+// Per 128-row tile each CTA forms partial scores over its columns, the two
+// partials meet through distributed shared memory, both CTAs run the same
+// softmax, and each accumulates O^T for its own 256 latent columns.
+constexpr int kTcThreads = 320;                       // warps 0-7 softmax, 8 TMA, 9 MMA
+constexpr int kSoftThreads = 256;
+constexpr int kHalfHeads = kHeadGroup / 2;            // heads per softmax warp group
 constexpr int kBoxBytes = kTileRows * 128;            // 128 rows x 64 bf16 columns
 constexpr int kSlots = 10;                            // ring of box slots
-constexpr int kSUnit = 10;                            // positions of a score unit (9 boxes + pad)
-constexpr int kPVUnit = 8;                            // positions of a PV unit (latent boxes)
+constexpr int kMaxBoxes = 5;                          // boxes per tile on rank 0
 constexpr int kQN = 2 * kHeadGroup;                   // hi | lo query rows
 constexpr int kQBoxBytes = kQN * 128;
 constexpr int kPSub = kQN * 128;                      // P^T: 64 tile rows of kQN rows
 constexpr int kPBytes = 2 * kPSub;                    // 128 tile rows
+constexpr int kXBytes = kTileRows * kHeadGroup * 4;   // one tile's partial scores
 constexpr int kOffQ = kSlots * kBoxBytes;
-constexpr int kOffP = kOffQ + 9 * kQBoxBytes;         // two P^T buffers
-constexpr int kOffRed = kOffP + 2 * kPBytes;          // [2][16 heads][4 warps] tile maxima
+constexpr int kOffP = kOffQ + kMaxBoxes * kQBoxBytes; // two P^T buffers
+constexpr int kOffOut = kOffP + 2 * kPBytes;          // partial scores sent to the peer
+constexpr int kOffIn = kOffOut + kXBytes;             // two buffers the peer's partials land in
+constexpr int kOffStage = kOffP;                      // fp32 query staging (before P exists)
+constexpr int kOffRed = kOffIn + 2 * kXBytes;         // [2][16 heads][4 warps] tile maxima
 constexpr int kOffLsum = kOffRed + 2 * kHeadGroup * 4 * 4;
 constexpr int kOffBar = kOffLsum + kHeadGroup * 4 * 4;
 constexpr int BAR_FULL = 0, BAR_EMPTY = kSlots, BAR_SFULL = 2 * kSlots, BAR_SFREE = BAR_SFULL + 2,
-              BAR_PFULL = BAR_SFREE + 2, BAR_ODONE = BAR_PFULL + 2, BAR_ZERO = BAR_ODONE + 2,
-              BAR_DONE = BAR_ZERO + 1, kNumBars = BAR_DONE + 1;
+              BAR_PFULL = BAR_SFREE + 2, BAR_ODONE = BAR_PFULL + 2, BAR_XCHG = BAR_ODONE + 2,
+              BAR_Q = BAR_XCHG + 2, BAR_DONE = BAR_Q + 1, kNumBars = BAR_DONE + 1;
 constexpr int kOffSlot = kOffBar + 8 * kNumBars;
 constexpr int kOffAbort = kOffSlot + 16;
 constexpr size_t kTcSmem = 1024 + kOffAbort + 16;
-constexpr uint32_t kTmemCols = 256;                   // S[2] at 0/32, O^T at 64..191
+constexpr uint32_t kTmemCols = 128;                   // S[2] at 0/32, O^T blocks at 64/96
 // Rescale threshold (log2 units): P may grow to 2^8 before O is rescaled.
 constexpr float kRescaleLog2 = 8.f;
 static_assert(kTcSmem <= 232448, "shared memory plan exceeds 227 KB");
-static_assert(kSlots % 2 == 0 && kSUnit % 2 == 0 && kPVUnit % 2 == 0,
-              "PV box pairs must start on even, non-wrapping slots");
+static_assert(kSlots == 10, "PV box pairs (rank 0 slots 0-1,2-3,5-6,7-8; rank 1 even starts) must not wrap");
+static_assert(kHeadGroup * 256 * 4 + kHeadGroup * kDr * 4 <= 2 * kPBytes + kXBytes,
+              "query staging must fit in the P and outbox buffers");
+
+// Columns of the cache (in 64-column boxes) owned by cluster rank r.
+__device__ __forceinline__ int boxes_of(int r) { return r == 0 ? 5 : 4; }
+__device__ __forceinline__ int box_of(int r, int i) { return r == 0 ? (i < 4 ? i : 8) : 4 + i; }
 
 // Waits for a phase; gives up (and raises the CTA's abort flag) after kWaitNs,
-// or at once when another role has already raised it.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort) {
-  if (mbar_try_wait(bar, parity)) return true;
+// or at once when another role has already raised it.  `cluster` selects an
+// acquire at cluster scope (for phases the peer CTA's copies complete).
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort,
+                                              bool cluster = false) {
+  auto poll = [&]() {
+    return cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+  };
+  if (poll()) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
     for (int i = 0; i < 32; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+      if (poll()) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > kWaitNs) {
       *abort = 1;
@@ -100,70 +111,54 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
   }
 }
 
-// Per-head max (or sum) over the 32 lanes of a warp of v[0..15]: one exchange
-// across the two half-warps, then a butterfly that halves the values held per
-// lane each round; afterwards lane l holds head l & 15.
+// Per-head max (or sum) of v[0..7] over the 32 lanes of a warp: one exchange
+// across the half-warps, a butterfly that halves the values held per lane
+// each round, and a last pairwise exchange; afterwards lane l holds head
+// (l >> 1) & 7.
 template <bool kMax>
-__device__ __forceinline__ float reduce_heads(float v[16], int lane) {
+__device__ __forceinline__ float reduce8_heads(float v[8], int lane) {
 #pragma unroll
-  for (int k = 0; k < 16; ++k) {
+  for (int k = 0; k < 8; ++k) {
     const float o = __shfl_xor_sync(0xffffffffu, v[k], 16);
     v[k] = kMax ? fmaxf(v[k], o) : v[k] + o;
   }
 #pragma unroll
-  for (int half = 8; half >= 1; half >>= 1) {
-    const bool upper = (lane & half) != 0;
+  for (int half = 4, bit = 8; half >= 1; half >>= 1, bit >>= 1) {
+    const bool upper = (lane & bit) != 0;
 #pragma unroll
     for (int k = 0; k < half; ++k) {
       const float send = upper ? v[k] : v[k + half];
       const float keep = upper ? v[k + half] : v[k];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, half);
+      const float recv = __shfl_xor_sync(0xffffffffu, send, bit);
       v[k] = kMax ? fmaxf(keep, recv) : keep + recv;
     }
   }
-  return v[0];
+  const float o = __shfl_xor_sync(0xffffffffu, v[0], 1);
+  return kMax ? fmaxf(v[0], o) : v[0] + o;
 }
 
-// Unit u of a chunk with T tiles, in the order the MMA issuer runs them:
-// S(0), S(1), PV(0), S(2), PV(1), ..., S(T-1), PV(T-2), PV(T-1).
-__device__ __forceinline__ void unit_of(int u, int T, bool& is_score, int& tile) {
-  if (u == 0) {
-    is_score = true;
-    tile = 0;
-  } else if (u == 2 * T - 1) {
-    is_score = false;
-    tile = T - 1;
-  } else if (u & 1) {
-    is_score = true;
-    tile = (u + 1) >> 1;
-  } else {
-    is_score = false;
-    tile = (u >> 1) - 1;
-  }
-}
-
-// One CTA per (16-head group g, KV chunk j, sequence b), 192 threads.
-//
-// A 128-row tile is 147 KB, too much to double-buffer, so the cache streams in
-// 16 KB boxes (128 rows x 64 columns, 128-byte swizzle) through a 10-slot
-// ring, in two passes per tile:
-//   score pass : boxes 0..8 from HBM (kept in L2 for the second pass)
-//                S[128 rows x 32] = C[128 x 576] . Q^T[576 x 32]   (36 MMAs, M=128,
-//                N=32: the 16 heads' hi and lo query parts)
-//   PV pass    : latent boxes 0..7 again, now from L2
-//                O^T[512 x 32] += C^T[512 x 128] . P^T[128 x 32]  (4 M=128 blocks,
-//                C read MN-major from box pairs)
-// The issuer runs S(t+1) before PV(t), so the next tile's scores overlap the
-// softmax of the current one.  Roles:
-//   warp 4  : TMEM allocation; one lane runs the TMA ring
-//   warp 5  : one lane issues every tcgen05.mma
-//   warps 0-3: one tile row per thread: softmax across the four warps, P^T
-//             (hi | lo bf16) to shared memory; O^T accumulates in TMEM against a
-//             reference maximum per head that only moves when a tile's maximum
-//             exceeds it by 2^8 (then the warps rescale O^T in TMEM).
-// The fp32 query and P reach the tensor core as bf16 hi + lo pairs (the N=32
-// columns), so their rounding stays near 2^-17 relative.
-__global__ void __launch_bounds__(kTcThreads, 1)
+// Roles inside each CTA (320 threads):
+//   warp 8  : TMEM allocation; one lane first fetches this rank's fp32 query
+//             slice with bulk copies, then streams this rank's boxes of each
+//             128-row tile (TMA, 128-byte swizzle) into a 10-slot ring
+//   warp 9  : one lane issues every tcgen05.mma, each as soon as its inputs
+//             are ready (the PV of a tile first: it frees the tile's slots):
+//               partial scores S_r[128 x 32] = C_r[128 x cols_r] . Q_r^T (M=128,
+//               N=32: the 16 heads' hi and lo query parts), box by box as they
+//               land; S is double-buffered in TMEM so that the next tile's
+//               scores overlap the current tile's softmax
+//               PV  O^T_r[256 x 32] += C_r^T[256 x 128] . P^T[128 x 32]
+//                   (two M=128 blocks; C read MN-major from the same slots)
+//   warps 0-7: one tile row per thread, heads 0-7 in warps 0-3 and heads 8-15
+//             in warps 4-7: the CTA's partial score rows go to the peer in one
+//             bulk copy, the peer's are added, the softmax runs across the
+//             rows, P^T (hi | lo bf16) goes to shared memory; O^T accumulates
+//             in TMEM against a reference maximum per head that moves only
+//             when a tile's maximum exceeds it by 2^8 (then O^T is rescaled in
+//             TMEM).
+// The fp32 query and P reach the tensor core as bf16 hi + lo pairs, so their
+// rounding stays near 2^-17 relative.
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
     split_tc_kernel(const __grid_constant__ CUtensorMap tmap, const SplitParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -175,11 +170,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
   uint32_t* slot_ptr = reinterpret_cast<uint32_t*>(smem + kOffSlot);
 
-  const int g = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int peer = rank ^ 1;
+  const int nb = boxes_of(rank);
+  const int g = blockIdx.x >> 1, j = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int len = clamp_length(p, b, tid == 0 && g == 0 && j == 0);
+  // Both CTAs of a cluster share (j, b): they leave here together or not at all.
+  const int len = clamp_length(p, b, tid == 0 && blockIdx.x == 0 && j == 0);
   const int r0 = j * p.chunk;
-  if (r0 >= len) return;  // chunk past the end of this sequence: nothing to do
+  if (r0 >= len) return;
   const int r1 = min(r0 + p.chunk, len);
   const int T = (r1 - r0 + kTileRows - 1) / kTileRows;
   const int last_valid = r1 - (r0 + (T - 1) * kTileRows);   // rows of the last tile
@@ -194,89 +193,74 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(BAR_SFULL + i), 1);
-      mbar_init(bar(BAR_SFREE + i), 4);
-      mbar_init(bar(BAR_PFULL + i), 4);
+      mbar_init(bar(BAR_SFREE + i), 8);
+      mbar_init(bar(BAR_PFULL + i), 8);
       mbar_init(bar(BAR_ODONE + i), 1);
+      mbar_init(bar(BAR_XCHG + i), 1);
     }
-    mbar_init(bar(BAR_ZERO), 4);
+    mbar_init(bar(BAR_Q), 1);
     mbar_init(bar(BAR_DONE), 1);
     *abort_flag = 0;
     fence_mbarrier_init();
   }
-  if (warp == 4) tmem_alloc(smem_u32(slot_ptr), kTmemCols);
+  if (warp == 8) tmem_alloc(smem_u32(slot_ptr), kTmemCols);
   tc_fence_before();
-  __syncthreads();
+  cluster_sync_all();   // both CTAs' barriers exist before any copy targets them
   tc_fence_after();
   const uint32_t tmem = *slot_ptr;
 
-  // The ring does not depend on the query: the producer starts at once.
-  if (warp == 4) {
+  if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
+      // The query slice first, so that it is not queued behind the cache.
+      const float* qa = static_cast<const float*>(p.q_abs);
+      const float* qp = static_cast<const float*>(p.q_pe);
+      mbar_arrive_expect_tx(bar(BAR_Q), kHeadGroup * 1024 + (rank == 0 ? kHeadGroup * kDr * 4 : 0));
+      for (int h = 0; h < kHeadGroup; ++h)
+        bulk_g2s(sbase + kOffStage + h * 1024, qa + (size_t(b) * p.H + h0 + h) * kDc + 256 * rank,
+                 1024, bar(BAR_Q));
+      if (rank == 0)
+        bulk_g2s(sbase + kOffStage + kHeadGroup * 1024, qp + (size_t(b) * p.H + h0) * kDr,
+                 kHeadGroup * kDr * 4, bar(BAR_Q));
       prefetch_tmap(&tmap);
-      const uint64_t keep = l2_evict_last_policy();     // read again by the PV pass
-      const uint64_t stream = l2_evict_first_policy();  // last read
-      int pos = 0;
-      for (int u = 0; u < 2 * T; ++u) {
-        bool is_score;
-        int t;
-        unit_of(u, T, is_score, t);
-        const int n = is_score ? kSUnit : kPVUnit;
-        for (int k = 0; k < n; ++k, ++pos) {
-          const int sl = pos % kSlots, use = pos / kSlots;
+      const uint64_t policy = l2_evict_first_policy();
+      for (int t = 0; t < T && !*abort_flag; ++t) {
+        for (int i = 0; i < nb; ++i) {
+          const int pos = nb * t + i, sl = pos % kSlots, use = pos / kSlots;
           if (use > 0 && !wait_or_abort(bar(BAR_EMPTY + sl), (use - 1) & 1, abort_flag)) break;
-          if (is_score && k == 9) {
-            mbar_arrive(bar(BAR_FULL + sl));   // padding position: nothing to load
-          } else {
-            mbar_arrive_expect_tx(bar(BAR_FULL + sl), kBoxBytes);
-            tma_load_2d(sbase + sl * kBoxBytes, &tmap, 64 * k, row_base + t * kTileRows,
-                        bar(BAR_FULL + sl), is_score ? keep : stream);
-          }
+          mbar_arrive_expect_tx(bar(BAR_FULL + sl), kBoxBytes);
+          tma_load_2d(sbase + sl * kBoxBytes, &tmap, 64 * box_of(rank, i),
+                      row_base + t * kTileRows, bar(BAR_FULL + sl), policy);
         }
-        if (*abort_flag) break;
       }
     }
-  }
-
-  // Query rows of the score MMA's B operand (K-major, 128-byte swizzle):
-  // row n < 16 holds bf16(q) of head n, row 16 + n holds bf16(q - bf16(q)).
-  // All loads of a thread are issued before the first store.
-  if (warp != 4) {
-    constexpr int kPairs = kHeadGroup * kRow / 2;
-    constexpr int kFill = 160;                        // warps 0-3 and 5
-    constexpr int kPerThread = (kPairs + kFill - 1) / kFill;
-    const int ft = warp < 4 ? tid : tid - 32;
-    const float* qa = static_cast<const float*>(p.q_abs);
-    const float* qp = static_cast<const float*>(p.q_pe);
-    float2 v[kPerThread];
-#pragma unroll
-    for (int r = 0; r < kPerThread; ++r) {
-      const int idx = ft + kFill * r;
-      if (idx < kPairs) {
-        const int h = idx / (kRow / 2), k = 2 * (idx % (kRow / 2));
-        const size_t bh = size_t(b) * p.H + h0 + h;
-        v[r] = k < kDc ? *reinterpret_cast<const float2*>(qa + bh * kDc + k)
-                       : *reinterpret_cast<const float2*>(qp + bh * kDr + (k - kDc));
-      }
-    }
-#pragma unroll
-    for (int r = 0; r < kPerThread; ++r) {
-      const int idx = ft + kFill * r;
-      if (idx < kPairs) {
-        const int h = idx / (kRow / 2), k = 2 * (idx % (kRow / 2));
+  } else {
+    if (warp < 8) {
+      // Query rows of the score MMA's B operand for this rank's columns
+      // (K-major, 128-byte swizzle, one 4 KB box per 64 columns): row n < 16 is
+      // bf16(q) of head n, row 16 + n is bf16(q - bf16(q)).  Staging holds
+      // q_abs[h][256 rank + c] at h*256 + c and (rank 0) q_pe[h][c] after it.
+      wait_or_abort(bar(BAR_Q), 0, abort_flag);
+      const float* stage = reinterpret_cast<const float*>(smem + kOffStage);
+      const int pairs = kHeadGroup * nb * 32;
+      for (int idx = tid; idx < pairs; idx += kSoftThreads) {
+        const int h = idx / (nb * 32), kk = 2 * (idx % (nb * 32));
+        const float2 v = kk < 256 ? *reinterpret_cast<const float2*>(stage + h * 256 + kk)
+                                  : *reinterpret_cast<const float2*>(
+                                        stage + kHeadGroup * 256 + h * kDr + (kk - 256));
         uint32_t hi, lo;
-        split_bf16(v[r].x, v[r].y, hi, lo);
-        const int box = k >> 6, ch = (k & 63) >> 3, w = k & 7;
-        *reinterpret_cast<uint32_t*>(smem + kOffQ + box * kQBoxBytes + sw128(h, ch) + 2 * w) = hi;
-        *reinterpret_cast<uint32_t*>(smem + kOffQ + box * kQBoxBytes +
-                                     sw128(h + kHeadGroup, ch) + 2 * w) = lo;
+        split_bf16(v.x, v.y, hi, lo);
+        const int i = kk >> 6, ch = (kk & 63) >> 3, w = kk & 7;
+        *reinterpret_cast<uint32_t*>(smem + kOffQ + i * kQBoxBytes + sw128(h, ch) + 2 * w) = hi;
+        *reinterpret_cast<uint32_t*>(smem + kOffQ + i * kQBoxBytes + sw128(h + kHeadGroup, ch) +
+                                     2 * w) = lo;
       }
+      fence_proxy_async_smem();
     }
-    fence_proxy_async_smem();
-    named_bar_sync(2, 160);        // warps 0-3 and 5: the query is in place
+    named_bar_sync(2, kSoftThreads + 32);   // warps 0-7 and 9: the query is in place
   }
 
-  if (warp == 5) {
+  if (warp == 9) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc_s = umma_idesc_bf16(128, kQN, 0, 0);
@@ -287,70 +271,82 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t dQ0 = umma_desc_sw128(sbase + kOffQ, 16, 1024);    // Q hi|lo
       const uint64_t dC0 = umma_desc_sw128(sbase, kBoxBytes, 1024);     // PV A: MN-major pair
       const uint64_t dP0 = umma_desc_sw128(sbase + kOffP, 16, 1024);    // P^T
-      int pos = 0;
-      bool ok = true;
-      for (int u = 0; u < 2 * T && ok; ++u) {
-        bool is_score;
-        int t;
-        unit_of(u, T, is_score, t);
-        if (is_score) {
-          const int sb = t & 1;
-          if (t >= 2) ok = wait_or_abort(bar(BAR_SFREE + sb), ((t - 2) >> 1) & 1, abort_flag);
-          for (int k = 0; k < kSUnit && ok; ++k, ++pos) {
-            const int sl = pos % kSlots, use = pos / kSlots;
-            ok = wait_or_abort(bar(BAR_FULL + sl), use & 1, abort_flag);
-            if (!ok) break;
-            if (k == 9) {
-              mbar_arrive(bar(BAR_EMPTY + sl));
-              continue;
-            }
-            tc_fence_after();
-            const uint64_t a = dA0 + static_cast<uint64_t>((sl * kBoxBytes) >> 4);
-            const uint64_t q = dQ0 + static_cast<uint64_t>((k * kQBoxBytes) >> 4);
+      // Event-driven issue: a PV as soon as its P^T is ready (it frees the
+      // tile's slots for the producer), otherwise the next score box as soon
+      // as it lands.
+      int ns = 0, sbx = 0, npv = 0;   // next score tile, next box of it, next PV tile
+      bool sfree = false;             // S buffer of tile ns released by the softmax
+      unsigned long long last = globaltimer_ns();
+      int polls = 0;
+      while (npv < T) {
+        bool progressed = false;
+        if (npv < ns && mbar_try_wait(bar(BAR_PFULL + (npv & 1)), (npv >> 1) & 1)) {
+          const int t = npv, sb = t & 1;
+          tc_fence_after();
+          const uint64_t pd = dP0 + static_cast<uint64_t>((sb * kPBytes) >> 4);
 #pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4)
-              umma_bf16(tmem + 32 * sb, a + ((s4 * 32) >> 4), q + ((s4 * 32) >> 4), idesc_s,
-                        (k > 0 || s4 > 0) ? 1u : 0u);
-            umma_commit(bar(BAR_EMPTY + sl));
-          }
-          if (ok) umma_commit(bar(BAR_SFULL + sb));
-        } else {
-          const int pb = t & 1;
-          ok = wait_or_abort(bar(BAR_PFULL + pb), (t >> 1) & 1, abort_flag);
-          if (ok && t == T - 1 && last_valid < kTileRows)
-            ok = wait_or_abort(bar(BAR_ZERO), 0, abort_flag);
-          const uint64_t pd = dP0 + static_cast<uint64_t>((pb * kPBytes) >> 4);
-          for (int mb = 0; mb < 4 && ok; ++mb) {
-            const int p0 = pos + 2 * mb;
-            const int s0 = p0 % kSlots;
-            ok = wait_or_abort(bar(BAR_FULL + s0), (p0 / kSlots) & 1, abort_flag) &&
-                 wait_or_abort(bar(BAR_FULL + s0 + 1), ((p0 + 1) / kSlots) & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
+          for (int mb = 0; mb < 2; ++mb) {
+            const int s0 = (nb * t + 2 * mb) % kSlots;   // a pair never straddles slot 9 -> 0
             const uint64_t c = dC0 + static_cast<uint64_t>((s0 * kBoxBytes) >> 4);
 #pragma unroll
             for (int ks = 0; ks < kTileRows / 16; ++ks)
               umma_bf16(tmem + 64 + 32 * mb, c + ((ks * 2048) >> 4),
                         pd + (((ks >> 2) * kPSub + (ks & 3) * 32) >> 4), idesc_o,
                         (t > 0 || ks > 0) ? 1u : 0u);
-            umma_commit(bar(BAR_EMPTY + s0));
-            umma_commit(bar(BAR_EMPTY + s0 + 1));
           }
-          pos += kPVUnit;
-          if (ok) umma_commit(bar(BAR_ODONE + pb));
+          for (int i = 0; i < 4; ++i) umma_commit(bar(BAR_EMPTY + (nb * t + i) % kSlots));
+          umma_commit(bar(BAR_ODONE + sb));
+          ++npv;
+          progressed = true;
+        }
+        if (ns < T) {
+          const int sb = ns & 1;
+          if (sbx == 0 && !sfree)
+            sfree = ns < 2 || mbar_try_wait(bar(BAR_SFREE + sb), ((ns - 2) >> 1) & 1);
+          const int pos = nb * ns + sbx, sl = pos % kSlots;
+          if (sfree && mbar_try_wait(bar(BAR_FULL + sl), (pos / kSlots) & 1)) {
+            tc_fence_after();
+            const uint64_t a = dA0 + static_cast<uint64_t>((sl * kBoxBytes) >> 4);
+            const uint64_t q = dQ0 + static_cast<uint64_t>((sbx * kQBoxBytes) >> 4);
+#pragma unroll
+            for (int s4 = 0; s4 < 4; ++s4)
+              umma_bf16(tmem + 32 * sb, a + ((s4 * 32) >> 4), q + ((s4 * 32) >> 4), idesc_s,
+                        (sbx > 0 || s4 > 0) ? 1u : 0u);
+            if (sbx >= 4) umma_commit(bar(BAR_EMPTY + sl));   // RoPE box: not needed by PV
+            if (++sbx == nb) {
+              umma_commit(bar(BAR_SFULL + sb));
+              ++ns;
+              sbx = 0;
+              sfree = false;
+            }
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          polls = 0;
+          last = globaltimer_ns();
+        } else if (++polls >= 64) {
+          polls = 0;
+          if (*abort_flag) break;
+          if (globaltimer_ns() - last > kWaitNs) {
+            *abort_flag = 1;
+            break;
+          }
         }
       }
       // Every MMA this thread issued has finished before TMEM is released.
       umma_commit(bar(BAR_DONE));
       mbar_wait_bounded(bar(BAR_DONE), 0);
     }
-  } else if (warp < 4) {
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax warps
-    const int row = 32 * warp + lane;     // tile row held by this thread
-    const uint32_t lane_base = static_cast<uint32_t>(32 * warp) << 16;
-    float m[kHeadGroup], l[kHeadGroup];
+    const int gp = warp >> 2, wq = warp & 3;
+    const int hb = kHalfHeads * gp;                     // first head of this group
+    const int row = 32 * wq + lane;                     // tile row held by this thread
+    const uint32_t lane_base = static_cast<uint32_t>(32 * wq) << 16;
+    float m[kHalfHeads], l[kHalfHeads];
 #pragma unroll
-    for (int h = 0; h < kHeadGroup; ++h) {
+    for (int h = 0; h < kHalfHeads; ++h) {
       m[h] = -INFINITY;
       l[h] = 0.f;
     }
@@ -359,36 +355,66 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int valid = t == T - 1 ? last_valid : kTileRows;
       wait_or_abort(bar(BAR_SFULL + sb), (t >> 1) & 1, abort_flag);
       tc_fence_after();
-      float v[32];
-      tmem_ld32(tmem + lane_base + 32 * sb, v);
+      float part[kHalfHeads];
+      {
+        uint32_t hi[8], lo[8];
+        tmem_ld8_nowait(tmem + lane_base + 32 * sb + hb, hi);
+        tmem_ld8_nowait(tmem + lane_base + 32 * sb + kHeadGroup + hb, lo);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < kHalfHeads; ++h) part[h] = __uint_as_float(hi[h]) + __uint_as_float(lo[h]);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_SFREE + sb));
+      // This rank's partial score rows travel to the peer in one bulk copy.
+      {
+        float4* out = reinterpret_cast<float4*>(smem + kOffOut + row * 64 + 32 * gp);
+        out[0] = make_float4(part[0], part[1], part[2], part[3]);
+        out[1] = make_float4(part[4], part[5], part[6], part[7]);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, kSoftThreads);
+      if (tid == 0) {
+        mbar_arrive_expect_tx(bar(BAR_XCHG + sb), kXBytes);
+        bulk_s2peer(mapa_shared(sbase + kOffIn + sb * kXBytes, peer), sbase + kOffOut, kXBytes,
+                    mapa_shared(bar(BAR_XCHG + sb), peer));
+        bulk_wait_read();   // the outbox may be rewritten after the next barrier
+      }
+      wait_or_abort(bar(BAR_XCHG + sb), (t >> 1) & 1, abort_flag, true);
       const bool rv = row < valid;
-      float sc[kHeadGroup], tt[kHeadGroup];
+      float sc[kHalfHeads], tt[kHalfHeads];
+      {
+        const float4* in =
+            reinterpret_cast<const float4*>(smem + kOffIn + sb * kXBytes + row * 64 + 32 * gp);
+        const float4 o0 = in[0], o1 = in[1];
+        const float other[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
 #pragma unroll
-      for (int h = 0; h < kHeadGroup; ++h) {
-        sc[h] = rv ? (v[h] + v[kHeadGroup + h]) * p.scale_log2 : -INFINITY;
-        tt[h] = sc[h];
+        for (int h = 0; h < kHalfHeads; ++h) {
+          // Same summation order on both ranks: rank 0's part + rank 1's part.
+          const float s = rank == 0 ? part[h] + other[h] : other[h] + part[h];
+          sc[h] = rv ? s * p.scale_log2 : -INFINITY;
+          tt[h] = sc[h];
+        }
       }
       float* rd = red + sb * kHeadGroup * 4;
-      const float wmax = reduce_heads<true>(tt, lane);
-      if (lane < 16) rd[lane * 4 + warp] = wmax;
-      named_bar_sync(1, 128);
+      const float wmax = reduce8_heads<true>(tt, lane);
+      if (lane < 16 && (lane & 1) == 0) rd[(hb + (lane >> 1)) * 4 + wq] = wmax;
+      named_bar_sync(1, kSoftThreads);
       bool need = false;
-      float tmax[kHeadGroup];
+      float tmax[kHalfHeads];
 #pragma unroll
-      for (int h = 0; h < kHeadGroup; ++h) {
-        const float4 q4 = *reinterpret_cast<const float4*>(rd + h * 4);
+      for (int h = 0; h < kHalfHeads; ++h) {
+        const float4 q4 = *reinterpret_cast<const float4*>(rd + (hb + h) * 4);
         tmax[h] = fmaxf(fmaxf(q4.x, q4.y), fmaxf(q4.z, q4.w));
         need |= tmax[h] > m[h] + kRescaleLog2;
       }
       if (need) {
-        // Move the reference maxima; rescale the row sums and the O^T
-        // accumulated so far (in TMEM, after the previous PV finished).
-        float alpha[kHeadGroup];
+        // Move this group's reference maxima; rescale its row sums and the O^T
+        // columns it owns (in TMEM, after the previous PV finished).
+        float alpha[kHalfHeads];
 #pragma unroll
-        for (int h = 0; h < kHeadGroup; ++h) {
+        for (int h = 0; h < kHalfHeads; ++h) {
           const float mn = fmaxf(m[h], tmax[h]);
           alpha[h] = m[h] == -INFINITY ? 0.f : ex2(m[h] - mn);
           m[h] = mn;
@@ -398,20 +424,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           wait_or_abort(bar(BAR_ODONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag);
           tc_fence_after();
 #pragma unroll
-          for (int mb = 0; mb < 4; ++mb) {
-            float o[32];
-            tmem_ld32(tmem + lane_base + 64 + 32 * mb, o);
+          for (int mb = 0; mb < 2; ++mb) {
 #pragma unroll
-            for (int h = 0; h < kHeadGroup; ++h) {
-              o[h] *= alpha[h];
-              o[kHeadGroup + h] *= alpha[h];
+            for (int half = 0; half < 2; ++half) {
+              const uint32_t col = 64 + 32 * mb + kHeadGroup * half + hb;
+              uint32_t r[8];
+              float o[8];
+              tmem_ld8_nowait(tmem + lane_base + col, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int h = 0; h < kHalfHeads; ++h) o[h] = __uint_as_float(r[h]) * alpha[h];
+              tmem_st8(tmem + lane_base + col, o);
             }
-            tmem_st32(tmem + lane_base + 64 + 32 * mb, o);
           }
+          tmem_wait_st();
         }
       }
 #pragma unroll
-      for (int h = 0; h < kHeadGroup; ++h) {
+      for (int h = 0; h < kHalfHeads; ++h) {
         const float mu = m[h] == -INFINITY ? 0.f : m[h];
         sc[h] = ex2(sc[h] - mu);
         l[h] += sc[h];
@@ -425,73 +455,73 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         uint8_t* pbuf = smem + kOffP + sb * kPBytes + (row >> 6) * kPSub;
         const int ch = (row & 63) >> 3, w = row & 7;
 #pragma unroll
-        for (int h = 0; h < kHeadGroup; ++h) {
+        for (int h = 0; h < kHalfHeads; ++h) {
           const __nv_bfloat16 hi = __float2bfloat16_rn(sc[h]);
           const __nv_bfloat16 lo = __float2bfloat16_rn(sc[h] - __bfloat162float(hi));
-          *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128(h, ch) + 2 * w) = hi;
-          *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128(h + kHeadGroup, ch) + 2 * w) = lo;
+          *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128(hb + h, ch) + 2 * w) = hi;
+          *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128(kHeadGroup + hb + h, ch) + 2 * w) = lo;
+        }
+      }
+      if (valid < kTileRows) {
+        // The last tile ends inside the sequence: zero the rows past the end in
+        // this rank's latent boxes (they may hold anything, NaN included) so
+        // that P = 0 times such a row adds exactly 0.  This tile's score MMA
+        // has finished with them (S was read above).
+        const int nrow = kTileRows - valid;
+        for (int i = 0; i < 4; ++i) {
+          const int sl = (nb * t + i) % kSlots;
+          for (int c = tid; c < nrow * 8; c += kSoftThreads)
+            *reinterpret_cast<uint4*>(smem + sl * kBoxBytes + (valid + c / 8) * 128 +
+                                      (c % 8) * 16) = make_uint4(0, 0, 0, 0);
         }
       }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_PFULL + sb));
-      if (valid < kTileRows) {
-        // Last tile ends inside the sequence: once its PV boxes have landed,
-        // zero the rows past the end (they may hold anything, NaN included) so
-        // that P = 0 times such a row adds exactly 0.
-        const int base = (kSUnit + kPVUnit) * T - kPVUnit;
-        const int nrow = kTileRows - valid;
-        for (int k = 0; k < kPVUnit; ++k) {
-          const int ps = base + k, sl = ps % kSlots;
-          wait_or_abort(bar(BAR_FULL + sl), (ps / kSlots) & 1, abort_flag);
-          for (int c = tid; c < nrow * 8; c += kThreads)
-            *reinterpret_cast<uint4*>(smem + sl * kBoxBytes + (valid + c / 8) * 128 +
-                                      (c % 8) * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(BAR_ZERO));
-      }
     }
     // Softmax denominators over the chunk's rows.
     {
-      float tt[kHeadGroup];
+      float tt[kHalfHeads];
 #pragma unroll
-      for (int h = 0; h < kHeadGroup; ++h) tt[h] = l[h];
-      const float ws = reduce_heads<false>(tt, lane);
-      if (lane < 16) lsum[lane * 4 + warp] = ws;
+      for (int h = 0; h < kHalfHeads; ++h) tt[h] = l[h];
+      const float ws = reduce8_heads<false>(tt, lane);
+      if (lane < 16 && (lane & 1) == 0) lsum[(hb + (lane >> 1)) * 4 + wq] = ws;
     }
-    // O^T after the last PV: this thread's latent row d = 128 mb + 32 warp + lane.
+    // O^T after the last PV: this thread's latent row is
+    // d = 256 rank + 128 mb + 32 wq + lane.
     wait_or_abort(bar(BAR_ODONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1, abort_flag);
     tc_fence_after();
-    named_bar_sync(1, 128);
+    named_bar_sync(1, kSoftThreads);
     if (!*abort_flag) {
       const size_t base = (size_t(b) * p.splits + j) * p.H + h0;
-      float inv[kHeadGroup];
+      float inv[kHalfHeads];
 #pragma unroll
-      for (int h = 0; h < kHeadGroup; ++h) {
-        const float4 q4 = *reinterpret_cast<const float4*>(lsum + h * 4);
+      for (int h = 0; h < kHalfHeads; ++h) {
+        const float4 q4 = *reinterpret_cast<const float4*>(lsum + (hb + h) * 4);
         const float L = (q4.x + q4.y) + (q4.z + q4.w);
         inv[h] = L > 0.f ? 1.f / L : 0.f;
-        if (warp == 0 && lane == h)
-          p.part_lse[base + h] = L > 0.f ? (m[h] + log2f(L)) * kLn2 : -INFINITY;
+        if (rank == 0 && wq == 0 && lane == h)
+          p.part_lse[base + hb + h] = L > 0.f ? (m[h] + log2f(L)) * kLn2 : -INFINITY;
       }
 #pragma unroll
-      for (int mb = 0; mb < 4; ++mb) {
-        float o[32];
-        tmem_ld32(tmem + lane_base + 64 + 32 * mb, o);
+      for (int mb = 0; mb < 2; ++mb) {
+        uint32_t hi[8], lo[8];
+        tmem_ld8_nowait(tmem + lane_base + 64 + 32 * mb + hb, hi);
+        tmem_ld8_nowait(tmem + lane_base + 64 + 32 * mb + kHeadGroup + hb, lo);
+        tmem_wait_ld();
 #pragma unroll
-        for (int h = 0; h < kHeadGroup; ++h)
-          p.part_o[(base + h) * kDc + 128 * mb + 32 * warp + lane] =
-              (o[h] + o[kHeadGroup + h]) * inv[h];
+        for (int h = 0; h < kHalfHeads; ++h)
+          p.part_o[(base + hb + h) * kDc + 256 * rank + 128 * mb + 32 * wq + lane] =
+              (__uint_as_float(hi[h]) + __uint_as_float(lo[h])) * inv[h];
       }
     }
   }
 
+  // Neither CTA leaves while its peer may still copy into its shared memory.
   tc_fence_before();
-  __syncthreads();
-  if (warp == 4) {
+  cluster_sync_all();
+  if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -654,7 +684,7 @@ int chunk_rows(const mla_dims* d, int requested, int* splits_out) {
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const bool bf16 = d->dtype == MLA_BF16;
     const long long per_split = static_cast<long long>(d->batch) * (bf16 ? d->heads / kHeadGroup : d->heads);
-    const long long slots = bf16 ? sms : 4ll * sms;
+    const long long slots = bf16 ? sms / 2 : 4ll * sms;   // bf16: one CTA pair per two SMs
     double best = 1e300;
     splits = 1;
     for (int s = 1; s <= max_splits; ++s) {
@@ -793,7 +823,7 @@ extern "C" mla_status mla_decode_split(const mla_dims* dims, const void* q_abs, 
       }
       attr_set = true;
     }
-    dim3 grid(dims->heads / kHeadGroup, p.splits, dims->batch);
+    dim3 grid(2 * (dims->heads / kHeadGroup), p.splits, dims->batch);   // clusters of 2
     split_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(tmap, p);
   } else {
     dim3 grid(dims->heads, p.splits, dims->batch);
