@@ -6,8 +6,8 @@
 // latent row serves every head (virtual broadcast of C^KV across heads), and
 // the attention output stays in the d_c-wide latent space.
 //
-// bf16: a tcgen05 kernel run by clusters of two CTAs (see split_tc_kernel);
-// each chunk of rows yields a normalised partial output and its log-sum-exp.
+// bf16: a tcgen05 kernel (see split_tc_kernel); each chunk of rows yields a
+// normalised partial output and its log-sum-exp.
 // fp32: plain SIMT, fp32 arithmetic throughout (no TF32).
 // combine: L = log sum_j exp(lse_j), o_c = sum_j exp(lse_j - L) o_j.
 #include <cuda.h>
@@ -44,65 +44,61 @@ __device__ __forceinline__ int clamp_length(const SplitParams& p, int b, bool re
 }
 
 // ---------------------------------------------------------------------------- bf16 split kernel
-// A pair of CTAs (a thread-block cluster of 2, on two SMs) owns one (16-head
-// group, KV chunk, sequence).  The 576 cached columns are split between them,
-// so that each SM streams every byte of its half exactly once while the MMAs
-// still cover 128 rows at a time:
-//   rank 0: latent columns   0..255 (boxes 0-3) and the RoPE columns (box 8)
-//   rank 1: latent columns 256..511 (boxes 4-7)
-// Per 128-row tile each CTA forms partial scores over its columns, the two
-// partials meet through distributed shared memory, both CTAs run the same
-// softmax, and each accumulates O^T for its own 256 latent columns.
-constexpr int kTcThreads = 320;                       // warps 0-7 softmax, 8 TMA, 9 MMA
+// One CTA per (16-head group, KV chunk, sequence).  Every tcgen05.mma covers
+// 128 cache rows (a K=16 step costs the same for M=64 as for M=128 at N=32, so
+// 128-row tiles halve the tensor time per row), but a 128-row tile (147 KB)
+// cannot stay resident from its scores to its PV product.  The cache
+// therefore streams twice per tile, from two decoupled rings:
+//   ring A  score boxes (128 rows x 64 columns, 16 KB) from HBM; a slot is
+//           free again as soon as its four score MMAs finish
+//   ring B  pairs of latent boxes (64 rows x 128 columns, 16 KB) for the PV
+//           product, re-read from L2 (the score pass loads with evict_last);
+//           a tile's pairs are requested once its score MMAs are issued, so
+//           they land about when its P does instead of holding slots early
+// L2 serves the GPU's SMs at close to three times the HBM rate, so the
+// second read costs L2 bandwidth, not HBM time.
+constexpr int kTcThreads = 352;                       // warps 0-7 softmax, 8 TMA A, 9 MMA, 10 TMA B
 constexpr int kSoftThreads = 256;
 constexpr int kHalfHeads = kHeadGroup / 2;            // heads per softmax warp group
 constexpr int kBoxBytes = kTileRows * 128;            // 128 rows x 64 bf16 columns
-constexpr int kSlots = 10;                            // ring of box slots
-constexpr int kMaxBoxes = 5;                          // boxes per tile on rank 0
+constexpr int kSlotsA = 6;
+constexpr int kSlotsB = 4;                            // each slot: two adjacent 64-row boxes
+constexpr int kHalfBox = kBoxBytes / 2;               // 64 rows x 64 bf16 columns
 constexpr int kQN = 2 * kHeadGroup;                   // hi | lo query rows
 constexpr int kQBoxBytes = kQN * 128;
 constexpr int kPSub = kQN * 128;                      // P^T: 64 tile rows of kQN rows
 constexpr int kPBytes = 2 * kPSub;                    // 128 tile rows
-constexpr int kXBytes = kTileRows * kHeadGroup * 4;   // one tile's partial scores
-constexpr int kOffQ = kSlots * kBoxBytes;
-constexpr int kOffP = kOffQ + kMaxBoxes * kQBoxBytes; // two P^T buffers
-constexpr int kOffOut = kOffP + 2 * kPBytes;          // partial scores sent to the peer
-constexpr int kOffIn = kOffOut + kXBytes;             // two buffers the peer's partials land in
-constexpr int kOffStage = kOffP;                      // fp32 query staging (before P exists)
-constexpr int kOffRed = kOffIn + 2 * kXBytes;         // [2][16 heads][4 warps] tile maxima
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kSlotsA * kBoxBytes;
+constexpr int kOffStage = kOffB;                      // fp32 query staging (before ring B runs)
+constexpr int kOffQ = kOffB + kSlotsB * 2 * kHalfBox;
+constexpr int kOffP = kOffQ + 9 * kQBoxBytes;         // two P^T buffers
+constexpr int kOffRed = kOffP + 2 * kPBytes;          // [2][16 heads][4 warps] tile maxima
 constexpr int kOffLsum = kOffRed + 2 * kHeadGroup * 4 * 4;
 constexpr int kOffBar = kOffLsum + kHeadGroup * 4 * 4;
-constexpr int BAR_FULL = 0, BAR_EMPTY = kSlots, BAR_SFULL = 2 * kSlots, BAR_SFREE = BAR_SFULL + 2,
-              BAR_PFULL = BAR_SFREE + 2, BAR_ODONE = BAR_PFULL + 2, BAR_XCHG = BAR_ODONE + 2,
-              BAR_Q = BAR_XCHG + 2, BAR_DONE = BAR_Q + 1, kNumBars = BAR_DONE + 1;
+constexpr int BAR_FULLA = 0, BAR_EMPTYA = kSlotsA, BAR_FULLB = 2 * kSlotsA,
+              BAR_EMPTYB = BAR_FULLB + kSlotsB, BAR_ZEROB = BAR_EMPTYB + kSlotsB,
+              BAR_SFULL = BAR_ZEROB + kSlotsB, BAR_SFREE = BAR_SFULL + 2, BAR_PFULL = BAR_SFREE + 2,
+              BAR_ODONE = BAR_PFULL + 2, BAR_Q = BAR_ODONE + 2, BAR_DONE = BAR_Q + 1,
+              kNumBars = BAR_DONE + 1;
 constexpr int kOffSlot = kOffBar + 8 * kNumBars;
 constexpr int kOffAbort = kOffSlot + 16;
-constexpr size_t kTcSmem = 1024 + kOffAbort + 16;
-constexpr uint32_t kTmemCols = 128;                   // S[2] at 0/32, O^T blocks at 64/96
+constexpr int kOffIssued = kOffAbort + 16;            // score tiles issued so far (ring B gate)
+constexpr size_t kTcSmem = 1024 + kOffIssued + 16;
+constexpr uint32_t kTmemCols = 256;                   // S[2] at 0/32, O^T blocks at 64..191
 // Rescale threshold (log2 units): P may grow to 2^8 before O is rescaled.
 constexpr float kRescaleLog2 = 8.f;
 static_assert(kTcSmem <= 232448, "shared memory plan exceeds 227 KB");
-static_assert(kSlots == 10, "PV box pairs (rank 0 slots 0-1,2-3,5-6,7-8; rank 1 even starts) must not wrap");
-static_assert(kHeadGroup * 256 * 4 + kHeadGroup * kDr * 4 <= 2 * kPBytes + kXBytes,
-              "query staging must fit in the P and outbox buffers");
-
-// Columns of the cache (in 64-column boxes) owned by cluster rank r.
-__device__ __forceinline__ int boxes_of(int r) { return r == 0 ? 5 : 4; }
-__device__ __forceinline__ int box_of(int r, int i) { return r == 0 ? (i < 4 ? i : 8) : 4 + i; }
+static_assert(kHeadGroup * kRow * 4 <= kSlotsB * 2 * kHalfBox, "query staging must fit in ring B");
 
 // Waits for a phase; gives up (and raises the CTA's abort flag) after kWaitNs,
-// or at once when another role has already raised it.  `cluster` selects an
-// acquire at cluster scope (for phases the peer CTA's copies complete).
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort,
-                                              bool cluster = false) {
-  auto poll = [&]() {
-    return cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
-  };
-  if (poll()) return true;
+// or at once when another role has already raised it.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
     for (int i = 0; i < 32; ++i)
-      if (poll()) return true;
+      if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > kWaitNs) {
       *abort = 1;
@@ -137,29 +133,28 @@ __device__ __forceinline__ float reduce8_heads(float v[8], int lane) {
   return kMax ? fmaxf(v[0], o) : v[0] + o;
 }
 
-// Roles inside each CTA (320 threads):
-//   warp 8  : TMEM allocation; one lane first fetches this rank's fp32 query
-//             slice with bulk copies, then streams this rank's boxes of each
-//             128-row tile (TMA, 128-byte swizzle) into a 10-slot ring
-//   warp 9  : one lane issues every tcgen05.mma, each as soon as its inputs
-//             are ready (the PV of a tile first: it frees the tile's slots):
-//               partial scores S_r[128 x 32] = C_r[128 x cols_r] . Q_r^T (M=128,
-//               N=32: the 16 heads' hi and lo query parts), box by box as they
-//               land; S is double-buffered in TMEM so that the next tile's
-//               scores overlap the current tile's softmax
-//               PV  O^T_r[256 x 32] += C_r^T[256 x 128] . P^T[128 x 32]
-//                   (two M=128 blocks; C read MN-major from the same slots)
-//   warps 0-7: one tile row per thread, heads 0-7 in warps 0-3 and heads 8-15
-//             in warps 4-7: the CTA's partial score rows go to the peer in one
-//             bulk copy, the peer's are added, the softmax runs across the
-//             rows, P^T (hi | lo bf16) goes to shared memory; O^T accumulates
-//             in TMEM against a reference maximum per head that moves only
-//             when a tile's maximum exceeds it by 2^8 (then O^T is rescaled in
-//             TMEM).
+// Roles (352 threads):
+//   warp 8  : TMEM allocation; one lane runs ring A (9 score boxes per tile)
+//   warp 10 : one lane fetches the fp32 query slice with bulk copies into the
+//             ring-B area, then runs ring B (8 latent box pairs per tile: four
+//             128-column blocks x two 64-row halves)
+//   warp 9  : one lane issues every tcgen05.mma as soon as its inputs are
+//             ready, a PV block first (it frees a ring-B slot):
+//               scores  S[128 x 32] = C[128 x 576] . Q^T  (M=128, N=32: the 16
+//                       heads' hi and lo query parts; S double-buffered in TMEM)
+//               PV      O^T[512 x 32] += C^T[512 x 128] . P^T[128 x 32]  (four
+//                       M=128 blocks, each in two 64-row halves; C read MN-major
+//                       from a ring-B pair)
+//   warps 0-7: one tile row per thread, heads 0-7 in warps 0-3 and 8-15 in
+//             warps 4-7: softmax across the rows, P^T (hi | lo bf16) to shared
+//             memory; O^T accumulates in TMEM against a reference maximum per
+//             head that moves only when a tile's maximum exceeds it by 2^8
+//             (then O^T is rescaled in TMEM).
 // The fp32 query and P reach the tensor core as bf16 hi + lo pairs, so their
 // rounding stays near 2^-17 relative.
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
-    split_tc_kernel(const __grid_constant__ CUtensorMap tmap, const SplitParams p) {
+__global__ void __launch_bounds__(kTcThreads, 1)
+    split_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_half,
+                    const SplitParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -168,17 +163,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   float* red = reinterpret_cast<float*>(smem + kOffRed);
   float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
+  volatile int* s_issued = reinterpret_cast<volatile int*>(smem + kOffIssued);
   uint32_t* slot_ptr = reinterpret_cast<uint32_t*>(smem + kOffSlot);
 
-  const int rank = static_cast<int>(cluster_ctarank());
-  const int peer = rank ^ 1;
-  const int nb = boxes_of(rank);
-  const int g = blockIdx.x >> 1, j = blockIdx.y, b = blockIdx.z;
+  const int g = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Both CTAs of a cluster share (j, b): they leave here together or not at all.
-  const int len = clamp_length(p, b, tid == 0 && blockIdx.x == 0 && j == 0);
+  const int len = clamp_length(p, b, tid == 0 && g == 0 && j == 0);
   const int r0 = j * p.chunk;
-  if (r0 >= len) return;
+  if (r0 >= len) return;  // chunk past the end of this sequence: nothing to do
   const int r1 = min(r0 + p.chunk, len);
   const int T = (r1 - r0 + kTileRows - 1) / kTileRows;
   const int last_valid = r1 - (r0 + (T - 1) * kTileRows);   // rows of the last tile
@@ -187,77 +179,102 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
   auto bar = [&](int i) { return bars + 8 * i; };
 
   if (tid == 0) {
-    for (int i = 0; i < kSlots; ++i) {
-      mbar_init(bar(BAR_FULL + i), 1);
-      mbar_init(bar(BAR_EMPTY + i), 1);
+    for (int i = 0; i < kSlotsA; ++i) {
+      mbar_init(bar(BAR_FULLA + i), 1);
+      mbar_init(bar(BAR_EMPTYA + i), 1);
+    }
+    for (int i = 0; i < kSlotsB; ++i) {
+      mbar_init(bar(BAR_FULLB + i), 1);
+      mbar_init(bar(BAR_EMPTYB + i), 1);
+      mbar_init(bar(BAR_ZEROB + i), 8);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(BAR_SFULL + i), 1);
       mbar_init(bar(BAR_SFREE + i), 8);
       mbar_init(bar(BAR_PFULL + i), 8);
       mbar_init(bar(BAR_ODONE + i), 1);
-      mbar_init(bar(BAR_XCHG + i), 1);
     }
     mbar_init(bar(BAR_Q), 1);
     mbar_init(bar(BAR_DONE), 1);
     *abort_flag = 0;
+    *s_issued = 0;
     fence_mbarrier_init();
   }
   if (warp == 8) tmem_alloc(smem_u32(slot_ptr), kTmemCols);
   tc_fence_before();
-  cluster_sync_all();   // both CTAs' barriers exist before any copy targets them
+  __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot_ptr;
 
   if (warp == 8) {
-    // ------------------------------------------------------------ TMA producer
+    // ------------------------------------------------------------ ring A (HBM)
     if (lane == 0) {
-      // The query slice first, so that it is not queued behind the cache.
+      prefetch_tmap(&tmap);
+      const uint64_t keep = l2_evict_last_policy();   // read again by ring B
+      for (int t = 0; t < T && !*abort_flag; ++t) {
+        for (int k = 0; k < 9; ++k) {
+          const int pos = 9 * t + k, sl = pos % kSlotsA, use = pos / kSlotsA;
+          if (use > 0 && !wait_or_abort(bar(BAR_EMPTYA + sl), (use - 1) & 1, abort_flag)) break;
+          mbar_arrive_expect_tx(bar(BAR_FULLA + sl), kBoxBytes);
+          tma_load_2d(sbase + kOffA + sl * kBoxBytes, &tmap, 64 * k, row_base + t * kTileRows,
+                      bar(BAR_FULLA + sl), keep);
+        }
+      }
+    }
+  } else if (warp == 10) {
+    // ------------------------------------------------------------ query, then ring B
+    if (lane == 0) {
       const float* qa = static_cast<const float*>(p.q_abs);
       const float* qp = static_cast<const float*>(p.q_pe);
-      mbar_arrive_expect_tx(bar(BAR_Q), kHeadGroup * 1024 + (rank == 0 ? kHeadGroup * kDr * 4 : 0));
-      for (int h = 0; h < kHeadGroup; ++h)
-        bulk_g2s(sbase + kOffStage + h * 1024, qa + (size_t(b) * p.H + h0 + h) * kDc + 256 * rank,
-                 1024, bar(BAR_Q));
-      if (rank == 0)
-        bulk_g2s(sbase + kOffStage + kHeadGroup * 1024, qp + (size_t(b) * p.H + h0) * kDr,
-                 kHeadGroup * kDr * 4, bar(BAR_Q));
-      prefetch_tmap(&tmap);
-      const uint64_t policy = l2_evict_first_policy();
+      mbar_arrive_expect_tx(bar(BAR_Q), kHeadGroup * kRow * 4);
+      bulk_g2s(sbase + kOffStage, qa + (size_t(b) * p.H + h0) * kDc, kHeadGroup * kDc * 4,
+               bar(BAR_Q));
+      bulk_g2s(sbase + kOffStage + kHeadGroup * kDc * 4, qp + (size_t(b) * p.H + h0) * kDr,
+               kHeadGroup * kDr * 4, bar(BAR_Q));
+    }
+    named_bar_sync(2, kSoftThreads + 64);   // the staging area may now be overwritten
+    if (lane == 0) {
+      prefetch_tmap(&tmap_half);
+      const uint64_t stream = l2_evict_first_policy();
       for (int t = 0; t < T && !*abort_flag; ++t) {
-        for (int i = 0; i < nb; ++i) {
-          const int pos = nb * t + i, sl = pos % kSlots, use = pos / kSlots;
-          if (use > 0 && !wait_or_abort(bar(BAR_EMPTY + sl), (use - 1) & 1, abort_flag)) break;
-          mbar_arrive_expect_tx(bar(BAR_FULL + sl), kBoxBytes);
-          tma_load_2d(sbase + sl * kBoxBytes, &tmap, 64 * box_of(rank, i),
-                      row_base + t * kTileRows, bar(BAR_FULL + sl), policy);
+        // Wait until the score MMAs of tile t are issued (its P follows soon).
+        const unsigned long long t0 = globaltimer_ns();
+        while (*s_issued <= t && !*abort_flag)
+          if (globaltimer_ns() - t0 > kWaitNs) *abort_flag = 1;
+        for (int u = 0; u < 8 && !*abort_flag; ++u) {
+          const int mb = u >> 1, kh = u & 1;
+          const int pos = 8 * t + u, sl = pos % kSlotsB, use = pos / kSlotsB;
+          if (use > 0 && !wait_or_abort(bar(BAR_EMPTYB + sl), (use - 1) & 1, abort_flag)) break;
+          mbar_arrive_expect_tx(bar(BAR_FULLB + sl), 2 * kHalfBox);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            tma_load_2d(sbase + kOffB + (2 * sl + h) * kHalfBox, &tmap_half, 64 * (2 * mb + h),
+                        row_base + t * kTileRows + 64 * kh, bar(BAR_FULLB + sl), stream);
         }
       }
     }
   } else {
     if (warp < 8) {
-      // Query rows of the score MMA's B operand for this rank's columns
-      // (K-major, 128-byte swizzle, one 4 KB box per 64 columns): row n < 16 is
-      // bf16(q) of head n, row 16 + n is bf16(q - bf16(q)).  Staging holds
-      // q_abs[h][256 rank + c] at h*256 + c and (rank 0) q_pe[h][c] after it.
+      // Query rows of the score MMA's B operand (K-major, 128-byte swizzle, one
+      // 4 KB box per 64 columns): row n < 16 is bf16(q) of head n, row 16 + n
+      // is bf16(q - bf16(q)).  Staging: q_abs[h0..h0+15][512], then q_pe.
       wait_or_abort(bar(BAR_Q), 0, abort_flag);
-      const float* stage = reinterpret_cast<const float*>(smem + kOffStage);
-      const int pairs = kHeadGroup * nb * 32;
-      for (int idx = tid; idx < pairs; idx += kSoftThreads) {
-        const int h = idx / (nb * 32), kk = 2 * (idx % (nb * 32));
-        const float2 v = kk < 256 ? *reinterpret_cast<const float2*>(stage + h * 256 + kk)
-                                  : *reinterpret_cast<const float2*>(
-                                        stage + kHeadGroup * 256 + h * kDr + (kk - 256));
+      const float* qa_s = reinterpret_cast<const float*>(smem + kOffStage);
+      const float* qp_s = qa_s + kHeadGroup * kDc;
+      for (int idx = tid; idx < kHeadGroup * kRow / 2; idx += kSoftThreads) {
+        const int h = idx / (kRow / 2), k = 2 * (idx % (kRow / 2));
+        const float2 v = k < kDc ? *reinterpret_cast<const float2*>(qa_s + h * kDc + k)
+                                 : *reinterpret_cast<const float2*>(qp_s + h * kDr + (k - kDc));
         uint32_t hi, lo;
         split_bf16(v.x, v.y, hi, lo);
-        const int i = kk >> 6, ch = (kk & 63) >> 3, w = kk & 7;
-        *reinterpret_cast<uint32_t*>(smem + kOffQ + i * kQBoxBytes + sw128(h, ch) + 2 * w) = hi;
-        *reinterpret_cast<uint32_t*>(smem + kOffQ + i * kQBoxBytes + sw128(h + kHeadGroup, ch) +
+        const int box = k >> 6, ch = (k & 63) >> 3, w = k & 7;
+        *reinterpret_cast<uint32_t*>(smem + kOffQ + box * kQBoxBytes + sw128(h, ch) + 2 * w) = hi;
+        *reinterpret_cast<uint32_t*>(smem + kOffQ + box * kQBoxBytes + sw128(h + kHeadGroup, ch) +
                                      2 * w) = lo;
       }
       fence_proxy_async_smem();
     }
-    named_bar_sync(2, kSoftThreads + 32);   // warps 0-7 and 9: the query is in place
+    named_bar_sync(2, kSoftThreads + 64);   // warps 0-7, 9, 10: the query is in place
   }
 
   if (warp == 9) {
@@ -267,44 +284,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       constexpr uint32_t idesc_o = umma_idesc_bf16(128, kQN, 1, 0);
       // Base descriptors; a K step only moves the 14-bit start-address field,
       // so each MMA adds an offset (16-byte units) to a base.
-      const uint64_t dA0 = umma_desc_sw128(sbase, 16, 1024);            // score A: K-major box
-      const uint64_t dQ0 = umma_desc_sw128(sbase + kOffQ, 16, 1024);    // Q hi|lo
-      const uint64_t dC0 = umma_desc_sw128(sbase, kBoxBytes, 1024);     // PV A: MN-major pair
-      const uint64_t dP0 = umma_desc_sw128(sbase + kOffP, 16, 1024);    // P^T
-      // Event-driven issue: a PV as soon as its P^T is ready (it frees the
-      // tile's slots for the producer), otherwise the next score box as soon
-      // as it lands.
-      int ns = 0, sbx = 0, npv = 0;   // next score tile, next box of it, next PV tile
-      bool sfree = false;             // S buffer of tile ns released by the softmax
+      const uint64_t dA0 = umma_desc_sw128(sbase + kOffA, 16, 1024);     // score A: K-major box
+      const uint64_t dQ0 = umma_desc_sw128(sbase + kOffQ, 16, 1024);     // Q hi|lo
+      const uint64_t dC0 = umma_desc_sw128(sbase + kOffB, kHalfBox, 1024);   // PV A: MN-major pair
+      const uint64_t dP0 = umma_desc_sw128(sbase + kOffP, 16, 1024);     // P^T
+      int ns = 0, sbx = 0;            // next score tile and its next box
+      int npv = 0, pmb = 0;           // next PV tile and its next (block, half) unit
+      bool sfree = false, pready = false;
       unsigned long long last = globaltimer_ns();
       int polls = 0;
       while (npv < T) {
         bool progressed = false;
-        if (npv < ns && mbar_try_wait(bar(BAR_PFULL + (npv & 1)), (npv >> 1) & 1)) {
-          const int t = npv, sb = t & 1;
-          tc_fence_after();
-          const uint64_t pd = dP0 + static_cast<uint64_t>((sb * kPBytes) >> 4);
+        if (npv < ns) {
+          if (!pready) pready = mbar_test(bar(BAR_PFULL + (npv & 1)), (npv >> 1) & 1);
+          const int pos = 8 * npv + pmb, sl = pos % kSlotsB, use = pos / kSlotsB;
+          const bool zeroed = npv != T - 1 || last_valid == kTileRows ||
+                              mbar_test(bar(BAR_ZEROB + sl), (pmb >> 2) & 1);
+          if (pready && zeroed && mbar_test(bar(BAR_FULLB + sl), use & 1)) {
+            tc_fence_after();
+            const int mb = pmb >> 1, kh = pmb & 1;
+            const uint64_t c = dC0 + static_cast<uint64_t>((sl * 2 * kHalfBox) >> 4);
+            const uint64_t pd = dP0 + static_cast<uint64_t>(((npv & 1) * kPBytes + kh * kPSub) >> 4);
 #pragma unroll
-          for (int mb = 0; mb < 2; ++mb) {
-            const int s0 = (nb * t + 2 * mb) % kSlots;   // a pair never straddles slot 9 -> 0
-            const uint64_t c = dC0 + static_cast<uint64_t>((s0 * kBoxBytes) >> 4);
-#pragma unroll
-            for (int ks = 0; ks < kTileRows / 16; ++ks)
-              umma_bf16(tmem + 64 + 32 * mb, c + ((ks * 2048) >> 4),
-                        pd + (((ks >> 2) * kPSub + (ks & 3) * 32) >> 4), idesc_o,
-                        (t > 0 || ks > 0) ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks)
+              umma_bf16(tmem + 64 + 32 * mb, c + ((ks * 2048) >> 4), pd + ((ks * 32) >> 4), idesc_o,
+                        (npv > 0 || kh > 0 || ks > 0) ? 1u : 0u);
+            umma_commit(bar(BAR_EMPTYB + sl));
+            if (++pmb == 8) {
+              umma_commit(bar(BAR_ODONE + (npv & 1)));
+              ++npv;
+              pmb = 0;
+              pready = false;
+            }
+            progressed = true;
           }
-          for (int i = 0; i < 4; ++i) umma_commit(bar(BAR_EMPTY + (nb * t + i) % kSlots));
-          umma_commit(bar(BAR_ODONE + sb));
-          ++npv;
-          progressed = true;
         }
         if (ns < T) {
           const int sb = ns & 1;
           if (sbx == 0 && !sfree)
-            sfree = ns < 2 || mbar_try_wait(bar(BAR_SFREE + sb), ((ns - 2) >> 1) & 1);
-          const int pos = nb * ns + sbx, sl = pos % kSlots;
-          if (sfree && mbar_try_wait(bar(BAR_FULL + sl), (pos / kSlots) & 1)) {
+            sfree = ns < 2 || mbar_test(bar(BAR_SFREE + sb), ((ns - 2) >> 1) & 1);
+          const int pos = 9 * ns + sbx, sl = pos % kSlotsA;
+          if (sfree && mbar_test(bar(BAR_FULLA + sl), (pos / kSlotsA) & 1)) {
             tc_fence_after();
             const uint64_t a = dA0 + static_cast<uint64_t>((sl * kBoxBytes) >> 4);
             const uint64_t q = dQ0 + static_cast<uint64_t>((sbx * kQBoxBytes) >> 4);
@@ -312,9 +332,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
             for (int s4 = 0; s4 < 4; ++s4)
               umma_bf16(tmem + 32 * sb, a + ((s4 * 32) >> 4), q + ((s4 * 32) >> 4), idesc_s,
                         (sbx > 0 || s4 > 0) ? 1u : 0u);
-            if (sbx >= 4) umma_commit(bar(BAR_EMPTY + sl));   // RoPE box: not needed by PV
-            if (++sbx == nb) {
+            umma_commit(bar(BAR_EMPTYA + sl));
+            if (++sbx == 9) {
               umma_commit(bar(BAR_SFULL + sb));
+              *s_issued = ns + 1;
               ++ns;
               sbx = 0;
               sfree = false;
@@ -355,48 +376,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       const int valid = t == T - 1 ? last_valid : kTileRows;
       wait_or_abort(bar(BAR_SFULL + sb), (t >> 1) & 1, abort_flag);
       tc_fence_after();
-      float part[kHalfHeads];
+      float sc[kHalfHeads], tt[kHalfHeads];
       {
         uint32_t hi[8], lo[8];
         tmem_ld8_nowait(tmem + lane_base + 32 * sb + hb, hi);
         tmem_ld8_nowait(tmem + lane_base + 32 * sb + kHeadGroup + hb, lo);
         tmem_wait_ld();
+        const bool rv = row < valid;
 #pragma unroll
-        for (int h = 0; h < kHalfHeads; ++h) part[h] = __uint_as_float(hi[h]) + __uint_as_float(lo[h]);
+        for (int h = 0; h < kHalfHeads; ++h) {
+          sc[h] = rv ? (__uint_as_float(hi[h]) + __uint_as_float(lo[h])) * p.scale_log2 : -INFINITY;
+          tt[h] = sc[h];
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_SFREE + sb));
-      // This rank's partial score rows travel to the peer in one bulk copy.
-      {
-        float4* out = reinterpret_cast<float4*>(smem + kOffOut + row * 64 + 32 * gp);
-        out[0] = make_float4(part[0], part[1], part[2], part[3]);
-        out[1] = make_float4(part[4], part[5], part[6], part[7]);
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, kSoftThreads);
-      if (tid == 0) {
-        mbar_arrive_expect_tx(bar(BAR_XCHG + sb), kXBytes);
-        bulk_s2peer(mapa_shared(sbase + kOffIn + sb * kXBytes, peer), sbase + kOffOut, kXBytes,
-                    mapa_shared(bar(BAR_XCHG + sb), peer));
-        bulk_wait_read();   // the outbox may be rewritten after the next barrier
-      }
-      wait_or_abort(bar(BAR_XCHG + sb), (t >> 1) & 1, abort_flag, true);
-      const bool rv = row < valid;
-      float sc[kHalfHeads], tt[kHalfHeads];
-      {
-        const float4* in =
-            reinterpret_cast<const float4*>(smem + kOffIn + sb * kXBytes + row * 64 + 32 * gp);
-        const float4 o0 = in[0], o1 = in[1];
-        const float other[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
-#pragma unroll
-        for (int h = 0; h < kHalfHeads; ++h) {
-          // Same summation order on both ranks: rank 0's part + rank 1's part.
-          const float s = rank == 0 ? part[h] + other[h] : other[h] + part[h];
-          sc[h] = rv ? s * p.scale_log2 : -INFINITY;
-          tt[h] = sc[h];
-        }
-      }
       float* rd = red + sb * kHeadGroup * 4;
       const float wmax = reduce8_heads<true>(tt, lane);
       if (lane < 16 && (lane & 1) == 0) rd[(hb + (lane >> 1)) * 4 + wq] = wmax;
@@ -424,7 +419,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
           wait_or_abort(bar(BAR_ODONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag);
           tc_fence_after();
 #pragma unroll
-          for (int mb = 0; mb < 2; ++mb) {
+          for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
               const uint32_t col = 64 + 32 * mb + kHeadGroup * half + hb;
@@ -462,23 +457,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
           *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128(kHeadGroup + hb + h, ch) + 2 * w) = lo;
         }
       }
-      if (valid < kTileRows) {
-        // The last tile ends inside the sequence: zero the rows past the end in
-        // this rank's latent boxes (they may hold anything, NaN included) so
-        // that P = 0 times such a row adds exactly 0.  This tile's score MMA
-        // has finished with them (S was read above).
-        const int nrow = kTileRows - valid;
-        for (int i = 0; i < 4; ++i) {
-          const int sl = (nb * t + i) % kSlots;
-          for (int c = tid; c < nrow * 8; c += kSoftThreads)
-            *reinterpret_cast<uint4*>(smem + sl * kBoxBytes + (valid + c / 8) * 128 +
-                                      (c % 8) * 16) = make_uint4(0, 0, 0, 0);
-        }
-      }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_PFULL + sb));
+      if (valid < kTileRows) {
+        // The last tile ends inside the sequence.  As each of its latent box
+        // pairs lands in ring B, zero the rows past the end (they may hold
+        // anything, NaN included) so that P = 0 times such a row adds exactly 0.
+        for (int u = 0; u < 8; ++u) {
+          const int kh = u & 1;
+          const int first = max(0, valid - 64 * kh);   // first row of this half to clear
+          const int nrow = 64 - first;
+          const int pos = 8 * t + u, sl = pos % kSlotsB;
+          wait_or_abort(bar(BAR_FULLB + sl), (pos / kSlotsB) & 1, abort_flag);
+          for (int c = tid; c < 2 * nrow * 8; c += kSoftThreads) {
+            const int h = c / (nrow * 8), rem = c % (nrow * 8);
+            *reinterpret_cast<uint4*>(smem + kOffB + (2 * sl + h) * kHalfBox +
+                                      (first + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(BAR_ZEROB + sl));
+        }
+      }
     }
     // Softmax denominators over the chunk's rows.
     {
@@ -488,8 +491,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
       const float ws = reduce8_heads<false>(tt, lane);
       if (lane < 16 && (lane & 1) == 0) lsum[(hb + (lane >> 1)) * 4 + wq] = ws;
     }
-    // O^T after the last PV: this thread's latent row is
-    // d = 256 rank + 128 mb + 32 wq + lane.
+    // O^T after the last PV: this thread's latent row is d = 128 mb + 32 wq + lane.
     wait_or_abort(bar(BAR_ODONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1, abort_flag);
     tc_fence_after();
     named_bar_sync(1, kSoftThreads);
@@ -501,26 +503,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kTcThreads, 1)
         const float4 q4 = *reinterpret_cast<const float4*>(lsum + (hb + h) * 4);
         const float L = (q4.x + q4.y) + (q4.z + q4.w);
         inv[h] = L > 0.f ? 1.f / L : 0.f;
-        if (rank == 0 && wq == 0 && lane == h)
+        if (wq == 0 && lane == h)
           p.part_lse[base + hb + h] = L > 0.f ? (m[h] + log2f(L)) * kLn2 : -INFINITY;
       }
 #pragma unroll
-      for (int mb = 0; mb < 2; ++mb) {
+      for (int mb = 0; mb < 4; ++mb) {
         uint32_t hi[8], lo[8];
         tmem_ld8_nowait(tmem + lane_base + 64 + 32 * mb + hb, hi);
         tmem_ld8_nowait(tmem + lane_base + 64 + 32 * mb + kHeadGroup + hb, lo);
         tmem_wait_ld();
 #pragma unroll
         for (int h = 0; h < kHalfHeads; ++h)
-          p.part_o[(base + hb + h) * kDc + 256 * rank + 128 * mb + 32 * wq + lane] =
+          p.part_o[(base + hb + h) * kDc + 128 * mb + 32 * wq + lane] =
               (__uint_as_float(hi[h]) + __uint_as_float(lo[h])) * inv[h];
       }
     }
   }
 
-  // Neither CTA leaves while its peer may still copy into its shared memory.
   tc_fence_before();
-  cluster_sync_all();
+  __syncthreads();
   if (warp == 8) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -684,7 +685,7 @@ int chunk_rows(const mla_dims* d, int requested, int* splits_out) {
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const bool bf16 = d->dtype == MLA_BF16;
     const long long per_split = static_cast<long long>(d->batch) * (bf16 ? d->heads / kHeadGroup : d->heads);
-    const long long slots = bf16 ? sms / 2 : 4ll * sms;   // bf16: one CTA pair per two SMs
+    const long long slots = bf16 ? sms : 4ll * sms;   // bf16: one CTA per SM
     double best = 1e300;
     splits = 1;
     for (int s = 1; s <= max_splits; ++s) {
@@ -801,18 +802,23 @@ extern "C" mla_status mla_decode_split(const mla_dims* dims, const void* q_abs, 
       set_error("%s: cuTensorMapEncodeTiled is not available from the driver", who);
       return MLA_ERR_CUDA;
     }
-    CUtensorMap tmap;
+    // Two views of the cache [B * s_max rows, 576 columns]: 128-row boxes for
+    // the score pass, 64-row boxes for the PV pass; 64 columns (128 bytes,
+    // 128-byte swizzle) per box in both.
+    CUtensorMap tmap, tmap_half;
     const cuuint64_t gdim[2] = {cuuint64_t(kRow), cuuint64_t(dims->batch) * dims->s_max};
     const cuuint64_t gstride[1] = {cuuint64_t(kRow) * 2};
-    const cuuint32_t box[2] = {64, cuuint32_t(kTileRows)};
     const cuuint32_t estride[2] = {1, 1};
-    CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), gdim,
-                     gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) {
-      set_error("%s: cuTensorMapEncodeTiled failed (%d)", who, int(r));
-      return MLA_ERR_CUDA;
+    for (int v = 0; v < 2; ++v) {
+      const cuuint32_t box[2] = {64, cuuint32_t(v == 0 ? kTileRows : kTileRows / 2)};
+      CUresult r = enc(v == 0 ? &tmap : &tmap_half, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                       const_cast<void*>(cache), gdim, gstride, box, estride,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) {
+        set_error("%s: cuTensorMapEncodeTiled failed (%d)", who, int(r));
+        return MLA_ERR_CUDA;
+      }
     }
     static bool attr_set = false;
     if (!attr_set) {
@@ -823,8 +829,8 @@ extern "C" mla_status mla_decode_split(const mla_dims* dims, const void* q_abs, 
       }
       attr_set = true;
     }
-    dim3 grid(2 * (dims->heads / kHeadGroup), p.splits, dims->batch);   // clusters of 2
-    split_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(tmap, p);
+    dim3 grid(dims->heads / kHeadGroup, p.splits, dims->batch);
+    split_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(tmap, tmap_half, p);
   } else {
     dim3 grid(dims->heads, p.splits, dims->batch);
     split_f32_kernel<<<grid, kThreads, 0, s>>>(p);
