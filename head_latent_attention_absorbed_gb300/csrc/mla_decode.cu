@@ -671,7 +671,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Rows per KV chunk (a multiple of the 32-row tile) and the resulting chunk
+// Rows per KV chunk (a multiple of the 128-row tile) and the resulting chunk
 // count.  With `requested` = 0 the count minimises a makespan estimate: waves
 // of CTAs over the SMs times (rows per chunk + a fixed per-CTA cost), plus the
 // combine's cost per chunk.  The bf16 kernel runs one CTA per SM.

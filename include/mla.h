@@ -98,7 +98,7 @@ mla_status mla_absorb_q(const mla_dims* dims, const void* q_nope, const void* q_
 /*
  * mla_decode_num_splits -- the number of KV chunks per sequence that
  * mla_decode_attn will use for `requested` (0 = let the library choose from
- * the current device's SM count).  Chunks hold a multiple of 32 rows, so the
+ * the current device's SM count).  Chunks hold a multiple of 128 rows, so the
  * result can be smaller than `requested`.  Returns 0 for invalid dims.
  */
 int32_t mla_decode_num_splits(const mla_dims* dims, int32_t requested);
