@@ -40,7 +40,7 @@ KERNEL_SOURCES = ["head_latent_attention_absorbed_gb300/csrc/mla_decode.cu",
                   "head_latent_attention_absorbed_gb300/csrc/mla_common.cuh"]
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=4000)
@@ -51,7 +51,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 # ----------------------------------------------------------------------------- peaks, traffic
@@ -279,14 +279,33 @@ def workload_config(cfg, layers, splits):
     return c
 
 
+# ----------------------------------------------------------------------------- ranks
+def max_over_ranks(x: float, device, world: int) -> float:
+    """The slowest rank's time: every rank contributes its own, all receive the max."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step: float, steps: int, world: int, seconds: float) -> float:
+    """Units all ranks processed (each rank runs its own replica of the workload) per
+    second of the slowest rank."""
+    return units_per_rank_step * steps * world / seconds
+
+
 # ----------------------------------------------------------------------------- our arm
 def main():
-    args = parse()
+    return main_with(parse(), int(os.environ.get("RANK", "0")),
+                     int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def main_with(args, rank: int, world: int, local: int = 0):
     from workloads import BY_NAME
     cfg = BY_NAME[args.workload]
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
 
     if args.impl == "reference":
         return run_reference(args, cfg, rank, world)
@@ -372,13 +391,10 @@ def main():
     if int(step.status.item()) != 0:
         raise RuntimeError(f"device status {int(step.status.item())} after the timed steps")
 
-    if world > 1:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(elapsed_ms, dev, world)
     sec = elapsed_ms / 1e3
-    value = cache_bytes * K * world / sec / 1e9
-    tokens = cfg.batch * K * world / sec
+    value = whole_job_rate(cache_bytes, K, world, sec) / 1e9
+    tokens = whole_job_rate(cfg.batch, K, world, sec)
     split_avg_s = statistics.fmean(split_ms) / 1e3
 
     # End-to-end through the public call, with host buffers: per step the
@@ -419,20 +435,17 @@ def main():
         e1.record()
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1)
-        if world > 1:
-            t = torch.tensor([e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
+        e_ms = max_over_ranks(e_ms, dev, world)
         bi = sum(t.numel() * t.element_size() for t in (h_qn[0], h_qr[0], h_len, h_pos))
         bo = h_out.numel() * h_out.element_size()
-        e2e = {"value": cache_bytes * Ke * world / (e_ms / 1e3) / 1e9, "unit": "GB/s",
+        e2e = {"value": whole_job_rate(cache_bytes, Ke, world, e_ms / 1e3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": Ke,
-               "tokens_per_s": cfg.batch * Ke * world / (e_ms / 1e3),
+               "tokens_per_s": whole_job_rate(cfg.batch, Ke, world, e_ms / 1e3),
                "path": "DecodeStep.run (three C-ABI calls, eager launches)"}
 
     peak, peak_kind = measured_peaks()
     achieved = cache_bytes / split_avg_s / 1e9
-    roofline = {"bound": "hbm", "kernel": "split_bf16_kernel (mla_decode_split)",
+    roofline = {"bound": "hbm", "kernel": "split_tc_kernel (mla_decode_split)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
                 "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
