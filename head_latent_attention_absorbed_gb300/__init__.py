@@ -12,13 +12,13 @@ from typing import Optional
 
 from ._binding import (EXPORTED, LIB_PATH, MLA_BF16, MLA_DEV_LENGTH_OUT_OF_RANGE,
                        MLA_DEV_PIPELINE_TIMEOUT, MLA_F32, MlaDims, MlaError, absorb_q, decode_attn,
-                       decode_combine, decode_split, dims, dtype_code, load, num_splits, out_proj,
-                       workspace_bytes)
+                       decode_attn_noalloc, decode_combine, decode_split, dims, dtype_code, load,
+                       num_splits, out_proj, workspace_bytes)
 
 __all__ = [
     "EXPORTED", "LIB_PATH", "MLA_BF16", "MLA_F32", "MLA_DEV_LENGTH_OUT_OF_RANGE",
     "MLA_DEV_PIPELINE_TIMEOUT", "MlaDims", "MlaError", "absorb_q", "decode_attn",
-    "decode_split", "decode_combine", "dims",
+    "decode_attn_noalloc", "decode_split", "decode_combine", "dims",
     "dtype_code", "load", "num_splits", "out_proj", "workspace_bytes", "DecodeStep",
 ]
 

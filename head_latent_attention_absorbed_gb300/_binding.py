@@ -20,7 +20,8 @@ MLA_DEV_PIPELINE_TIMEOUT = 2
 STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
           3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA"}
 EXPORTED = ("mla_absorb_q", "mla_decode_num_splits", "mla_decode_workspace_bytes",
-            "mla_decode_attn", "mla_decode_split", "mla_decode_combine", "mla_out_proj",
+            "mla_decode_attn", "mla_decode_split", "mla_decode_combine",
+            "mla_decode_attn_noalloc", "mla_out_proj",
             "mla_status_string", "mla_last_error_message")
 
 
@@ -62,6 +63,8 @@ def load(path: Optional[str] = None):
     lib.mla_decode_split.restype = ctypes.c_int
     lib.mla_decode_combine.argtypes = [D, P, I32, P, SZ, P, P, P]
     lib.mla_decode_combine.restype = ctypes.c_int
+    lib.mla_decode_attn_noalloc.argtypes = [D, P, P, P, P, ctypes.c_float, I32, P, P, P, P]
+    lib.mla_decode_attn_noalloc.restype = ctypes.c_int
     lib.mla_out_proj.argtypes = [D, P, P, P, P]
     lib.mla_out_proj.restype = ctypes.c_int
     lib.mla_status_string.argtypes = [ctypes.c_int]
@@ -160,6 +163,21 @@ def decode_combine(d: MlaDims, lengths, workspace, o_c, num_splits_requested: in
     _check(load().mla_decode_combine(ctypes.byref(d), _ptr(lengths), int(num_splits_requested),
                                      _ptr(workspace), nbytes, _ptr(o_c), _ptr(lse),
                                      _stream(stream)))
+
+
+def decode_attn_noalloc(d: MlaDims, q_abs, q_pe, cache, lengths, o_c, softmax_scale: float,
+                        num_splits_requested: int = 0, lse=None, dev_status=None,
+                        stream=None) -> None:
+    """decode_attn with the library's fixed scratch in place of a workspace.
+
+    For hosts that cannot allocate device memory while decoding; the call
+    allocates nothing.  Calls that overlap on the GPU share that scratch and race.
+    """
+    _cuda_contig(q_abs, q_pe, cache, lengths, o_c, lse, dev_status)
+    _check(load().mla_decode_attn_noalloc(ctypes.byref(d), _ptr(q_abs), _ptr(q_pe), _ptr(cache),
+                                          _ptr(lengths), float(softmax_scale),
+                                          int(num_splits_requested), _ptr(o_c), _ptr(lse),
+                                          _ptr(dev_status), _stream(stream)))
 
 
 def out_proj(d: MlaDims, o_c, w_uv, out, stream=None) -> None:

@@ -14,6 +14,8 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "mla_common.cuh"
 
 namespace mla {
@@ -871,4 +873,76 @@ extern "C" mla_status mla_decode_attn(const mla_dims* dims, const void* q_abs, c
     return st;
   }
   return mla_decode_combine(dims, lengths, num_splits, workspace, ws_bytes, o_c, lse, stream);
+}
+
+// ------------------------------------------------------- fixed scratch, no allocation
+// Some hosts cannot allocate device memory when they decode: an inference engine that
+// reserved all device memory for its own pool at start-up (a cudaMalloc would fail or
+// break its accounting), or a latency-critical loop where cudaMalloc and cudaFree would
+// synchronise the device.  mla_decode_attn_noalloc serves them with the chunk partials
+// in this fixed array instead of a caller-supplied workspace.  Every GPU that loads the
+// library reserves MLA_NOALLOC_SCRATCH_BYTES for it until the process exits.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MLA_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};   // device address of the array, per device
+
+// The array's name in host code is only a host-side handle, so the device address
+// is asked from the runtime once per device, with that device current.
+mla_status noalloc_scratch(const char* who, void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    set_error("%s: cudaGetDevice failed", who);
+    return MLA_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    set_error("%s: device ordinal %d is beyond the %d the library tracks", who, dev, kMaxDevices);
+    return MLA_ERR_UNSUPPORTED;
+  }
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* ptr = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (e != cudaSuccess || !ptr) {
+      set_error("%s: cudaGetSymbolAddress of the fixed scratch failed: %s", who,
+                cudaGetErrorString(e));
+      return MLA_ERR_CUDA;
+    }
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MLA_OK;
+}
+}  // namespace
+
+extern "C" mla_status mla_decode_attn_noalloc(const mla_dims* dims, const void* q_abs,
+                                              const void* q_pe, const void* cache,
+                                              const int32_t* lengths, float softmax_scale,
+                                              int32_t num_splits, float* o_c, float* lse,
+                                              int32_t* dev_status, void* stream) {
+  const char* who = "mla_decode_attn_noalloc";
+  mla_status st = check_dims(dims, who);
+  if (st != MLA_OK) return st;
+  if (num_splits < 0) {
+    set_error("%s: num_splits must be >= 0", who);
+    return MLA_ERR_INVALID_ARG;
+  }
+  int splits = 0;
+  chunk_rows(dims, num_splits, &splits);
+  const size_t need = workspace_bytes(dims, splits);
+  if (need > MLA_NOALLOC_SCRATCH_BYTES) {
+    set_error("%s: %d sequences x %d heads x %d chunks need %zu bytes of scratch, more than "
+              "the fixed %zu; use mla_decode_attn with a workspace, or fewer chunks",
+              who, dims->batch, dims->heads, splits, need, size_t(MLA_NOALLOC_SCRATCH_BYTES));
+    return MLA_ERR_WORKSPACE;
+  }
+  void* scratch = nullptr;
+  st = noalloc_scratch(who, &scratch);
+  if (st != MLA_OK) return st;
+  // Every partial the combine reads is written by this call's split kernel, so
+  // nothing left in the array by an earlier call needs clearing.
+  return mla_decode_attn(dims, q_abs, q_pe, cache, lengths, softmax_scale, num_splits, scratch,
+                         size_t(MLA_NOALLOC_SCRATCH_BYTES), o_c, lse, dev_status, stream);
 }

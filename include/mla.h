@@ -168,6 +168,39 @@ mla_status mla_decode_combine(const mla_dims* dims, const int32_t* lengths, int3
                               float* lse, void* stream);
 
 /*
+ * mla_decode_attn_noalloc -- mla_decode_attn for callers that cannot allocate
+ * device memory.  The paper has no counterpart: it is a convenience of this
+ * library.
+ *
+ * Who needs it: a host that reserved all device memory for its own pool at
+ * start-up (a cudaMalloc there fails or breaks the pool's accounting), or a
+ * latency-critical loop in which cudaMalloc and cudaFree would synchronise the
+ * device.  This call allocates nothing: the chunk partials go to one fixed
+ * array of MLA_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library holds until the process exits.  The caller still passes
+ * inputs and outputs, with the meaning, layout and error behaviour given for
+ * mla_decode_attn (which this call runs, with the array as its workspace).
+ *
+ * Limit: a call whose partials need more than MLA_NOALLOC_SCRATCH_BYTES
+ * (mla_decode_workspace_bytes(dims, num_splits) > MLA_NOALLOC_SCRATCH_BYTES)
+ * returns MLA_ERR_WORKSPACE and launches nothing.
+ *
+ * First call on a device: it asks the runtime for the array's device address
+ * with that device current and keeps it; make that first call before any
+ * stream capture begins.
+ *
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents (nothing needs clearing: a call reads only what it wrote).
+ * Calls whose kernels overlap on the GPU (other streams, other host threads)
+ * race on it; order them on one stream or use mla_decode_attn.
+ */
+#define MLA_NOALLOC_SCRATCH_BYTES (16u << 20) /* 16 MiB per device */
+mla_status mla_decode_attn_noalloc(const mla_dims* dims, const void* q_abs, const void* q_pe,
+                                   const void* cache, const int32_t* lengths,
+                                   float softmax_scale, int32_t num_splits, float* o_c,
+                                   float* lse, int32_t* dev_status, void* stream);
+
+/*
  * mla_out_proj -- per-head value up-projection applied after attention.
  *
  *   o[b,h,e] = sum_{c < d_c} w_uv[h,e,c] * o_c[b,h,c]
