@@ -59,7 +59,7 @@ __device__ __forceinline__ int clamp_length(const SplitParams& p, int b, bool re
 //           they land about when its P does instead of holding slots early
 // L2 serves the GPU's SMs at close to three times the HBM rate, so the
 // second read costs L2 bandwidth, not HBM time.
-constexpr int kTcThreads = 352;                       // warps 0-7 softmax, 8 TMA A, 9 MMA, 10 TMA B
+constexpr int kTcThreads = 448;                       // 0-7 softmax, 8 ring A, 10 ring B, 9/11/12/13 MMA
 constexpr int kSoftThreads = 256;
 constexpr int kHalfHeads = kHeadGroup / 2;            // heads per softmax warp group
 constexpr int kBoxBytes = kTileRows * 128;            // 128 rows x 64 bf16 columns
@@ -85,9 +85,11 @@ constexpr int BAR_FULLA = 0, BAR_EMPTYA = kSlotsA, BAR_FULLB = 2 * kSlotsA,
               kNumBars = BAR_DONE + 1;
 constexpr int kOffSlot = kOffBar + 8 * kNumBars;
 constexpr int kOffAbort = kOffSlot + 16;
-constexpr int kOffIssued = kOffAbort + 16;            // score tiles issued so far (ring B gate)
+constexpr int kOffIssued = kOffAbort + 16;            // score tiles issued, per score issuer (ring B gate)
 constexpr size_t kTcSmem = 1024 + kOffIssued + 16;
-constexpr uint32_t kTmemCols = 256;                   // S[2] at 0/32, O^T blocks at 64..191
+constexpr uint32_t kTmemCols = 256;                   // S_0[2] at 0/32, S_1[2] at 64/96, O^T at 128..255
+constexpr uint32_t kS1Col = 64;                       // second score accumulator
+constexpr uint32_t kOCol = 128;                       // O^T blocks, 32 columns each
 // Rescale threshold (log2 units): P may grow to 2^8 before O is rescaled.
 constexpr float kRescaleLog2 = 8.f;
 static_assert(kTcSmem <= 232448, "shared memory plan exceeds 227 KB");
@@ -135,18 +137,20 @@ __device__ __forceinline__ float reduce8_heads(float v[8], int lane) {
   return kMax ? fmaxf(v[0], o) : v[0] + o;
 }
 
-// Roles (352 threads):
+// Roles (448 threads):
 //   warp 8  : TMEM allocation; one lane runs ring A (9 score boxes per tile)
 //   warp 10 : one lane fetches the fp32 query slice with bulk copies into the
 //             ring-B area, then runs ring B (8 latent box pairs per tile: four
 //             128-column blocks x two 64-row halves)
-//   warp 9  : one lane issues every tcgen05.mma as soon as its inputs are
-//             ready, a PV block first (it frees a ring-B slot):
-//               scores  S[128 x 32] = C[128 x 576] . Q^T  (M=128, N=32: the 16
-//                       heads' hi and lo query parts; S double-buffered in TMEM)
-//               PV      O^T[512 x 32] += C^T[512 x 128] . P^T[128 x 32]  (four
-//                       M=128 blocks, each in two 64-row halves; C read MN-major
-//                       from a ring-B pair)
+//   warps 9, 11: score MMAs, each over alternate boxes of the stream, into two
+//               accumulators S_0, S_1 (summed by the softmax):
+//               S[128 x 32] = C[128 x 576] . Q^T  (M=128, N=32: the 16 heads'
+//               hi and lo query parts; S double-buffered in TMEM)
+//   warps 12, 13: PV MMAs, each over two of the four O^T blocks:
+//               O^T[512 x 32] += C^T[512 x 128] . P^T[128 x 32]  (M=128 blocks,
+//               each in two 64-row halves; C read MN-major from a ring-B pair)
+//             A thread issues one tcgen05.mma per ~100 cycles whatever the
+//             shape, so four issuing threads keep the tensor pipe fed.
 //   warps 0-7: one tile row per thread, heads 0-7 in warps 0-3 and 8-15 in
 //             warps 4-7: softmax across the rows, P^T (hi | lo bf16) to shared
 //             memory; O^T accumulates in TMEM against a reference maximum per
@@ -165,7 +169,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   float* red = reinterpret_cast<float*>(smem + kOffRed);
   float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
-  volatile int* s_issued = reinterpret_cast<volatile int*>(smem + kOffIssued);
+  volatile int* s_issued = reinterpret_cast<volatile int*>(smem + kOffIssued);   // [2]
   uint32_t* slot_ptr = reinterpret_cast<uint32_t*>(smem + kOffSlot);
 
   const int g = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
@@ -191,15 +195,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar(BAR_ZEROB + i), 8);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(BAR_SFULL + i), 1);
+      mbar_init(bar(BAR_SFULL + i), 2);   // one commit per score issuer
       mbar_init(bar(BAR_SFREE + i), 8);
       mbar_init(bar(BAR_PFULL + i), 8);
-      mbar_init(bar(BAR_ODONE + i), 1);
+      mbar_init(bar(BAR_ODONE + i), 2);   // one commit per PV issuer
     }
     mbar_init(bar(BAR_Q), 1);
-    mbar_init(bar(BAR_DONE), 1);
+    mbar_init(bar(BAR_DONE), 4);          // every issuer's last commit
     *abort_flag = 0;
-    *s_issued = 0;
+    s_issued[0] = 0;
+    s_issued[1] = 0;
     fence_mbarrier_init();
   }
   if (warp == 8) tmem_alloc(smem_u32(slot_ptr), kTmemCols);
@@ -234,17 +239,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bulk_g2s(sbase + kOffStage + kHeadGroup * kDc * 4, qp + (size_t(b) * p.H + h0) * kDr,
                kHeadGroup * kDr * 4, bar(BAR_Q));
     }
-    named_bar_sync(2, kSoftThreads + 64);   // the staging area may now be overwritten
+    named_bar_sync(2, kSoftThreads + 160);  // the staging area may now be overwritten
     if (lane == 0) {
       prefetch_tmap(&tmap_half);
       const uint64_t stream = l2_evict_first_policy();
       for (int t = 0; t < T && !*abort_flag; ++t) {
         // Wait until the score MMAs of tile t are issued (its P follows soon).
         const unsigned long long t0 = globaltimer_ns();
-        while (*s_issued <= t && !*abort_flag)
+        while ((s_issued[0] <= t || s_issued[1] <= t) && !*abort_flag)
           if (globaltimer_ns() - t0 > kWaitNs) *abort_flag = 1;
+        // Unit u holds O^T block mb = u % 4 (always ring slot mb) for row half u / 4.
         for (int u = 0; u < 8 && !*abort_flag; ++u) {
-          const int mb = u >> 1, kh = u & 1;
+          const int mb = u & 3, kh = u >> 2;
           const int pos = 8 * t + u, sl = pos % kSlotsB, use = pos / kSlotsB;
           if (use > 0 && !wait_or_abort(bar(BAR_EMPTYB + sl), (use - 1) & 1, abort_flag)) break;
           mbar_arrive_expect_tx(bar(BAR_FULLB + sl), 2 * kHalfBox);
@@ -276,88 +282,87 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
       fence_proxy_async_smem();
     }
-    named_bar_sync(2, kSoftThreads + 64);   // warps 0-7, 9, 10: the query is in place
+    named_bar_sync(2, kSoftThreads + 160);  // warps 0-7, 9-13: the query is in place
   }
 
-  if (warp == 9) {
-    // ------------------------------------------------------------ MMA issuer
+  if (warp == 9 || warp == 11) {
+    // ------------------------------------------------------------ score MMA issuers
+    // Issuer i takes the boxes whose stream position 9t + k has parity i, so it
+    // owns ring-A slots i, i + 2, i + 4 and meets each slot's phases in order;
+    // it accumulates them into its own S_i and the softmax adds S_0 + S_1.  One
+    // thread issues a tcgen05.mma only every ~100 cycles, so the work is spread
+    // over threads.
     if (lane == 0) {
+      const int i = warp == 9 ? 0 : 1;
       constexpr uint32_t idesc_s = umma_idesc_bf16(128, kQN, 0, 0);
-      constexpr uint32_t idesc_o = umma_idesc_bf16(128, kQN, 1, 0);
       // Base descriptors; a K step only moves the 14-bit start-address field,
       // so each MMA adds an offset (16-byte units) to a base.
-      const uint64_t dA0 = umma_desc_sw128(sbase + kOffA, 16, 1024);     // score A: K-major box
+      const uint64_t dA0 = umma_desc_sw128(sbase + kOffA, 16, 1024);     // K-major box
       const uint64_t dQ0 = umma_desc_sw128(sbase + kOffQ, 16, 1024);     // Q hi|lo
-      const uint64_t dC0 = umma_desc_sw128(sbase + kOffB, kHalfBox, 1024);   // PV A: MN-major pair
-      const uint64_t dP0 = umma_desc_sw128(sbase + kOffP, 16, 1024);     // P^T
-      int ns = 0, sbx = 0;            // next score tile and its next box
-      int npv = 0, pmb = 0;           // next PV tile and its next (block, half) unit
-      bool sfree = false, pready = false;
-      unsigned long long last = globaltimer_ns();
-      int polls = 0;
-      while (npv < T) {
-        bool progressed = false;
-        if (npv < ns) {
-          if (!pready) pready = mbar_test(bar(BAR_PFULL + (npv & 1)), (npv >> 1) & 1);
-          const int pos = 8 * npv + pmb, sl = pos % kSlotsB, use = pos / kSlotsB;
-          const bool zeroed = npv != T - 1 || last_valid == kTileRows ||
-                              mbar_test(bar(BAR_ZEROB + sl), (pmb >> 2) & 1);
-          if (pready && zeroed && mbar_test(bar(BAR_FULLB + sl), use & 1)) {
-            tc_fence_after();
-            const int mb = pmb >> 1, kh = pmb & 1;
-            const uint64_t c = dC0 + static_cast<uint64_t>((sl * 2 * kHalfBox) >> 4);
-            const uint64_t pd = dP0 + static_cast<uint64_t>(((npv & 1) * kPBytes + kh * kPSub) >> 4);
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              umma_bf16(tmem + 64 + 32 * mb, c + ((ks * 2048) >> 4), pd + ((ks * 32) >> 4), idesc_o,
-                        (npv > 0 || kh > 0 || ks > 0) ? 1u : 0u);
-            umma_commit(bar(BAR_EMPTYB + sl));
-            if (++pmb == 8) {
-              umma_commit(bar(BAR_ODONE + (npv & 1)));
-              ++npv;
-              pmb = 0;
-              pready = false;
-            }
-            progressed = true;
-          }
-        }
-        if (ns < T) {
-          const int sb = ns & 1;
-          if (sbx == 0 && !sfree)
-            sfree = ns < 2 || mbar_test(bar(BAR_SFREE + sb), ((ns - 2) >> 1) & 1);
-          const int pos = 9 * ns + sbx, sl = pos % kSlotsA;
-          if (sfree && mbar_test(bar(BAR_FULLA + sl), (pos / kSlotsA) & 1)) {
-            tc_fence_after();
-            const uint64_t a = dA0 + static_cast<uint64_t>((sl * kBoxBytes) >> 4);
-            const uint64_t q = dQ0 + static_cast<uint64_t>((sbx * kQBoxBytes) >> 4);
-#pragma unroll
-            for (int s4 = 0; s4 < 4; ++s4)
-              umma_bf16(tmem + 32 * sb, a + ((s4 * 32) >> 4), q + ((s4 * 32) >> 4), idesc_s,
-                        (sbx > 0 || s4 > 0) ? 1u : 0u);
-            umma_commit(bar(BAR_EMPTYA + sl));
-            if (++sbx == 9) {
-              umma_commit(bar(BAR_SFULL + sb));
-              *s_issued = ns + 1;
-              ++ns;
-              sbx = 0;
-              sfree = false;
-            }
-            progressed = true;
-          }
-        }
-        if (progressed) {
-          polls = 0;
-          last = globaltimer_ns();
-        } else if (++polls >= 64) {
-          polls = 0;
-          if (*abort_flag) break;
-          if (globaltimer_ns() - last > kWaitNs) {
-            *abort_flag = 1;
+      const uint32_t dS = tmem + kS1Col * i;
+      for (int t = 0; t < T; ++t) {
+        const int sb = t & 1;
+        if (t >= 2 && !wait_or_abort(bar(BAR_SFREE + sb), ((t - 2) >> 1) & 1, abort_flag)) break;
+        bool ok = true, first = true;
+        for (int k = (9 * t + i) & 1; k < 9; k += 2) {
+          const int pos = 9 * t + k, sl = pos % kSlotsA;
+          if (!wait_or_abort(bar(BAR_FULLA + sl), (pos / kSlotsA) & 1, abort_flag)) {
+            ok = false;
             break;
           }
+          tc_fence_after();
+          const uint64_t a = dA0 + static_cast<uint64_t>((sl * kBoxBytes) >> 4);
+          const uint64_t q = dQ0 + static_cast<uint64_t>((k * kQBoxBytes) >> 4);
+#pragma unroll
+          for (int s4 = 0; s4 < 4; ++s4)
+            umma_bf16(dS + 32 * sb, a + ((s4 * 32) >> 4), q + ((s4 * 32) >> 4), idesc_s,
+                      (!first || s4 > 0) ? 1u : 0u);
+          umma_commit(bar(BAR_EMPTYA + sl));
+          first = false;
         }
+        if (!ok) break;
+        umma_commit(bar(BAR_SFULL + sb));
+        s_issued[i] = t + 1;
       }
       // Every MMA this thread issued has finished before TMEM is released.
+      umma_commit(bar(BAR_DONE));
+      mbar_wait_bounded(bar(BAR_DONE), 0);
+    }
+  } else if (warp == 12 || warp == 13) {
+    // ------------------------------------------------------------ PV MMA issuers
+    // Issuer i takes O^T blocks mb = i and i + 2 (ring-B slots i and i + 2).
+    if (lane == 0) {
+      const int i = warp - 12;
+      constexpr uint32_t idesc_o = umma_idesc_bf16(128, kQN, 1, 0);
+      const uint64_t dC0 = umma_desc_sw128(sbase + kOffB, kHalfBox, 1024);   // MN-major pair
+      const uint64_t dP0 = umma_desc_sw128(sbase + kOffP, 16, 1024);         // P^T
+      for (int t = 0; t < T; ++t) {
+        if (!wait_or_abort(bar(BAR_PFULL + (t & 1)), (t >> 1) & 1, abort_flag)) break;
+        bool ok = true;
+        for (int u = i; u < 8; u += 2) {
+          const int mb = u & 3, kh = u >> 2;
+          const int pos = 8 * t + u, sl = pos % kSlotsB;
+          if (t == T - 1 && last_valid < kTileRows &&
+              !wait_or_abort(bar(BAR_ZEROB + sl), kh & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (!wait_or_abort(bar(BAR_FULLB + sl), (pos / kSlotsB) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t c = dC0 + static_cast<uint64_t>((sl * 2 * kHalfBox) >> 4);
+          const uint64_t pd = dP0 + static_cast<uint64_t>(((t & 1) * kPBytes + kh * kPSub) >> 4);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tmem + kOCol + 32 * mb, c + ((ks * 2048) >> 4), pd + ((ks * 32) >> 4), idesc_o,
+                      (t > 0 || kh > 0 || ks > 0) ? 1u : 0u);
+          umma_commit(bar(BAR_EMPTYB + sl));
+        }
+        if (!ok) break;
+        umma_commit(bar(BAR_ODONE + (t & 1)));
+      }
       umma_commit(bar(BAR_DONE));
       mbar_wait_bounded(bar(BAR_DONE), 0);
     }
@@ -380,14 +385,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_after();
       float sc[kHalfHeads], tt[kHalfHeads];
       {
-        uint32_t hi[8], lo[8];
-        tmem_ld8_nowait(tmem + lane_base + 32 * sb + hb, hi);
-        tmem_ld8_nowait(tmem + lane_base + 32 * sb + kHeadGroup + hb, lo);
+        uint32_t hi0[8], lo0[8], hi1[8], lo1[8];
+        tmem_ld8_nowait(tmem + lane_base + 32 * sb + hb, hi0);
+        tmem_ld8_nowait(tmem + lane_base + 32 * sb + kHeadGroup + hb, lo0);
+        tmem_ld8_nowait(tmem + lane_base + kS1Col + 32 * sb + hb, hi1);
+        tmem_ld8_nowait(tmem + lane_base + kS1Col + 32 * sb + kHeadGroup + hb, lo1);
         tmem_wait_ld();
         const bool rv = row < valid;
 #pragma unroll
         for (int h = 0; h < kHalfHeads; ++h) {
-          sc[h] = rv ? (__uint_as_float(hi[h]) + __uint_as_float(lo[h])) * p.scale_log2 : -INFINITY;
+          const float s0 = __uint_as_float(hi0[h]) + __uint_as_float(lo0[h]);
+          const float s1 = __uint_as_float(hi1[h]) + __uint_as_float(lo1[h]);
+          sc[h] = rv ? (s0 + s1) * p.scale_log2 : -INFINITY;
           tt[h] = sc[h];
         }
       }
@@ -424,7 +433,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-              const uint32_t col = 64 + 32 * mb + kHeadGroup * half + hb;
+              const uint32_t col = kOCol + 32 * mb + kHeadGroup * half + hb;
               uint32_t r[8];
               float o[8];
               tmem_ld8_nowait(tmem + lane_base + col, r);
@@ -467,8 +476,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // The last tile ends inside the sequence.  As each of its latent box
         // pairs lands in ring B, zero the rows past the end (they may hold
         // anything, NaN included) so that P = 0 times such a row adds exactly 0.
+        // The PV of tile t-1 must have consumed every slot's previous fill first:
+        // a parity wait on a slot whose previous fill is still in flight would
+        // pass at once.
+        if (t > 0) wait_or_abort(bar(BAR_ODONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag);
         for (int u = 0; u < 8; ++u) {
-          const int kh = u & 1;
+          const int kh = u >> 2;
           const int first = max(0, valid - 64 * kh);   // first row of this half to clear
           const int nrow = 64 - first;
           const int pos = 8 * t + u, sl = pos % kSlotsB;
@@ -511,8 +524,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int mb = 0; mb < 4; ++mb) {
         uint32_t hi[8], lo[8];
-        tmem_ld8_nowait(tmem + lane_base + 64 + 32 * mb + hb, hi);
-        tmem_ld8_nowait(tmem + lane_base + 64 + 32 * mb + kHeadGroup + hb, lo);
+        tmem_ld8_nowait(tmem + lane_base + kOCol + 32 * mb + hb, hi);
+        tmem_ld8_nowait(tmem + lane_base + kOCol + 32 * mb + kHeadGroup + hb, lo);
         tmem_wait_ld();
 #pragma unroll
         for (int h = 0; h < kHalfHeads; ++h)
