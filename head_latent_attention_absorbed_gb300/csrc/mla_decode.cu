@@ -22,6 +22,7 @@ namespace mla {
 namespace {
 
 constexpr int kWarps = 4;
+constexpr int kChunkAlign = 8;   // chunk sizes are multiples of 8 rows
 constexpr int kThreads = kWarps * 32;
 
 struct SplitParams {
@@ -72,7 +73,6 @@ constexpr int kPSub = kQN * 128;                      // P^T: 64 tile rows of kQ
 constexpr int kPBytes = 2 * kPSub;                    // 128 tile rows
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kSlotsA * kBoxBytes;
-constexpr int kOffStage = kOffB;                      // fp32 query staging (before ring B runs)
 constexpr int kOffQ = kOffB + kSlotsB * 2 * kHalfBox;
 constexpr int kOffP = kOffQ + 9 * kQBoxBytes;         // two P^T buffers
 constexpr int kOffRed = kOffP + 2 * kPBytes;          // [2][16 heads][4 warps] tile maxima
@@ -81,8 +81,8 @@ constexpr int kOffBar = kOffLsum + kHeadGroup * 4 * 4;
 constexpr int BAR_FULLA = 0, BAR_EMPTYA = kSlotsA, BAR_FULLB = 2 * kSlotsA,
               BAR_EMPTYB = BAR_FULLB + kSlotsB, BAR_ZEROB = BAR_EMPTYB + kSlotsB,
               BAR_SFULL = BAR_ZEROB + kSlotsB, BAR_SFREE = BAR_SFULL + 2, BAR_PFULL = BAR_SFREE + 2,
-              BAR_ODONE = BAR_PFULL + 2, BAR_Q = BAR_ODONE + 2, BAR_DONE = BAR_Q + 1,
-              kNumBars = BAR_DONE + 1;
+              BAR_ODONE = BAR_PFULL + 2, BAR_LASTA = BAR_ODONE + 2, BAR_FULLX = BAR_LASTA + 1,
+              BAR_ZEROX = BAR_FULLX + 4, BAR_DONE = BAR_ZEROX + 4, kNumBars = BAR_DONE + 1;
 constexpr int kOffSlot = kOffBar + 8 * kNumBars;
 constexpr int kOffAbort = kOffSlot + 16;
 constexpr int kOffIssued = kOffAbort + 16;            // score tiles issued, per score issuer (ring B gate)
@@ -93,7 +93,7 @@ constexpr uint32_t kOCol = 128;                       // O^T blocks, 32 columns 
 // Rescale threshold (log2 units): P may grow to 2^8 before O is rescaled.
 constexpr float kRescaleLog2 = 8.f;
 static_assert(kTcSmem <= 232448, "shared memory plan exceeds 227 KB");
-static_assert(kHeadGroup * kRow * 4 <= kSlotsB * 2 * kHalfBox, "query staging must fit in ring B");
+static_assert(kSlotsA >= 4, "the last tile's second row half borrows four ring-A slots");
 
 // Waits for a phase; gives up (and raises the CTA's abort flag) after kWaitNs,
 // or at once when another role has already raised it.
@@ -174,12 +174,19 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   const int g = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Launched after mla_absorb_q with programmatic serialization: everything up
+  // to the query load (set-up, TMEM, the cache stream) overlaps that kernel.
   const int len = clamp_length(p, b, tid == 0 && g == 0 && j == 0);
   const int r0 = j * p.chunk;
   if (r0 >= len) return;  // chunk past the end of this sequence: nothing to do
   const int r1 = min(r0 + p.chunk, len);
   const int T = (r1 - r0 + kTileRows - 1) / kTileRows;
   const int last_valid = r1 - (r0 + (T - 1) * kTileRows);   // rows of the last tile
+  // The last tile may reach past the chunk into the next chunk's rows (finite
+  // cache data; their scores are masked) and past the sequence's end, where
+  // rows may hold anything (NaN included): those are zeroed before the PV.
+  const int zero_from = len - (r0 + (T - 1) * kTileRows);
+  const bool zero_last = zero_from < kTileRows;
   const int row_base = b * p.s_max + r0;
   const int h0 = g * kHeadGroup;
   auto bar = [&](int i) { return bars + 8 * i; };
@@ -200,7 +207,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar(BAR_PFULL + i), 8);
       mbar_init(bar(BAR_ODONE + i), 2);   // one commit per PV issuer
     }
-    mbar_init(bar(BAR_Q), 1);
+    mbar_init(bar(BAR_LASTA), 2);         // every score MMA has finished
+    for (int i = 0; i < 4; ++i) {
+      mbar_init(bar(BAR_FULLX + i), 1);   // the last tile's pairs in ring A: one use each
+      mbar_init(bar(BAR_ZEROX + i), 8);
+    }
     mbar_init(bar(BAR_DONE), 4);          // every issuer's last commit
     *abort_flag = 0;
     s_issued[0] = 0;
@@ -229,60 +240,80 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   } else if (warp == 10) {
-    // ------------------------------------------------------------ query, then ring B
-    if (lane == 0) {
-      const float* qa = static_cast<const float*>(p.q_abs);
-      const float* qp = static_cast<const float*>(p.q_pe);
-      mbar_arrive_expect_tx(bar(BAR_Q), kHeadGroup * kRow * 4);
-      bulk_g2s(sbase + kOffStage, qa + (size_t(b) * p.H + h0) * kDc, kHeadGroup * kDc * 4,
-               bar(BAR_Q));
-      bulk_g2s(sbase + kOffStage + kHeadGroup * kDc * 4, qp + (size_t(b) * p.H + h0) * kDr,
-               kHeadGroup * kDr * 4, bar(BAR_Q));
-    }
-    named_bar_sync(2, kSoftThreads + 160);  // the staging area may now be overwritten
+    // ------------------------------------------------------------ ring B (L2)
     if (lane == 0) {
       prefetch_tmap(&tmap_half);
       const uint64_t stream = l2_evict_first_policy();
       for (int t = 0; t < T && !*abort_flag; ++t) {
-        // Wait until the score MMAs of tile t are issued (its P follows soon).
-        const unsigned long long t0 = globaltimer_ns();
-        while ((s_issued[0] <= t || s_issued[1] <= t) && !*abort_flag)
-          if (globaltimer_ns() - t0 > kWaitNs) *abort_flag = 1;
-        // Unit u holds O^T block mb = u % 4 (always ring slot mb) for row half u / 4.
+        // From tile 1 on, wait until the score MMAs of tile t are issued (its P
+        // follows soon); tile 0's pairs take the empty ring at once.
+        if (t > 0) {
+          const unsigned long long t0 = globaltimer_ns();
+          while ((s_issued[0] <= t || s_issued[1] <= t) && !*abort_flag)
+            if (globaltimer_ns() - t0 > kWaitNs) *abort_flag = 1;
+        }
+        // Unit u holds O^T block mb = u % 4 (ring slot mb) for row half u / 4.
+        // The last tile's second row half goes to ring-A slots 0-3 instead, free
+        // once every score MMA has finished, so the whole tile is in flight at once.
         for (int u = 0; u < 8 && !*abort_flag; ++u) {
           const int mb = u & 3, kh = u >> 2;
+          const int row = row_base + t * kTileRows + 64 * kh;
+          if (t == T - 1 && u >= 4) {
+            if (u == 4 && !wait_or_abort(bar(BAR_LASTA), 0, abort_flag)) break;
+            const int x = u - 4;
+            mbar_arrive_expect_tx(bar(BAR_FULLX + x), 2 * kHalfBox);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              tma_load_2d(sbase + kOffA + x * kBoxBytes + h * kHalfBox, &tmap_half,
+                          64 * (2 * mb + h), row, bar(BAR_FULLX + x), stream);
+            continue;
+          }
           const int pos = 8 * t + u, sl = pos % kSlotsB, use = pos / kSlotsB;
           if (use > 0 && !wait_or_abort(bar(BAR_EMPTYB + sl), (use - 1) & 1, abort_flag)) break;
           mbar_arrive_expect_tx(bar(BAR_FULLB + sl), 2 * kHalfBox);
 #pragma unroll
           for (int h = 0; h < 2; ++h)
             tma_load_2d(sbase + kOffB + (2 * sl + h) * kHalfBox, &tmap_half, 64 * (2 * mb + h),
-                        row_base + t * kTileRows + 64 * kh, bar(BAR_FULLB + sl), stream);
+                        row, bar(BAR_FULLB + sl), stream);
         }
       }
     }
-  } else {
+  } else if (warp < 8 || warp == 9 || warp == 11) {
     if (warp < 8) {
       // Query rows of the score MMA's B operand (K-major, 128-byte swizzle, one
       // 4 KB box per 64 columns): row n < 16 is bf16(q) of head n, row 16 + n
-      // is bf16(q - bf16(q)).  Staging: q_abs[h0..h0+15][512], then q_pe.
-      wait_or_abort(bar(BAR_Q), 0, abort_flag);
-      const float* qa_s = reinterpret_cast<const float*>(smem + kOffStage);
-      const float* qp_s = qa_s + kHeadGroup * kDc;
-      for (int idx = tid; idx < kHeadGroup * kRow / 2; idx += kSoftThreads) {
-        const int h = idx / (kRow / 2), k = 2 * (idx % (kRow / 2));
-        const float2 v = k < kDc ? *reinterpret_cast<const float2*>(qa_s + h * kDc + k)
-                                 : *reinterpret_cast<const float2*>(qp_s + h * kDr + (k - kDc));
-        uint32_t hi, lo;
-        split_bf16(v.x, v.y, hi, lo);
+      // is bf16(q - bf16(q)).  q_abs[b, h0..h0+15, :] and q_pe[b, h0..h0+15, :]
+      // are contiguous; each thread loads nine float4 before converting them.
+      // They come from the previous kernel of the stream (mla_absorb_q).
+      pdl_wait();
+      const float4* qa = reinterpret_cast<const float4*>(static_cast<const float*>(p.q_abs) +
+                                                         (size_t(b) * p.H + h0) * kDc);
+      const float4* qp = reinterpret_cast<const float4*>(static_cast<const float*>(p.q_pe) +
+                                                         (size_t(b) * p.H + h0) * kDr);
+      constexpr int kNA = kHeadGroup * kDc / 4, kNQ = kNA + kHeadGroup * kDr / 4;
+      static_assert(kNQ == 9 * kSoftThreads, "nine float4 per softmax thread");
+      float4 v[9];
+#pragma unroll
+      for (int i = 0; i < 9; ++i) {
+        const int idx = tid + i * kSoftThreads;
+        v[i] = idx < kNA ? qa[idx] : qp[idx - kNA];
+      }
+#pragma unroll
+      for (int i = 0; i < 9; ++i) {
+        const int idx = tid + i * kSoftThreads;
+        const int h = idx < kNA ? idx / (kDc / 4) : (idx - kNA) / (kDr / 4);
+        const int k = idx < kNA ? 4 * (idx % (kDc / 4)) : kDc + 4 * ((idx - kNA) % (kDr / 4));
+        uint2 hi, lo;
+        split_bf16(v[i].x, v[i].y, hi.x, lo.x);
+        split_bf16(v[i].z, v[i].w, hi.y, lo.y);
         const int box = k >> 6, ch = (k & 63) >> 3, w = k & 7;
-        *reinterpret_cast<uint32_t*>(smem + kOffQ + box * kQBoxBytes + sw128(h, ch) + 2 * w) = hi;
-        *reinterpret_cast<uint32_t*>(smem + kOffQ + box * kQBoxBytes + sw128(h + kHeadGroup, ch) +
-                                     2 * w) = lo;
+        *reinterpret_cast<uint2*>(smem + kOffQ + box * kQBoxBytes + sw128(h, ch) + 2 * w) = hi;
+        *reinterpret_cast<uint2*>(smem + kOffQ + box * kQBoxBytes + sw128(h + kHeadGroup, ch) +
+                                  2 * w) = lo;
       }
       fence_proxy_async_smem();
     }
-    named_bar_sync(2, kSoftThreads + 160);  // warps 0-7, 9-13: the query is in place
+    named_bar_sync(2, kSoftThreads + 64);   // warps 0-7, 9, 11: the query is in place
   }
 
   if (warp == 9 || warp == 11) {
@@ -324,6 +355,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         umma_commit(bar(BAR_SFULL + sb));
         s_issued[i] = t + 1;
       }
+      umma_commit(bar(BAR_LASTA));   // ring A is free for the last tile's PV pairs
       // Every MMA this thread issued has finished before TMEM is released.
       umma_commit(bar(BAR_DONE));
       mbar_wait_bounded(bar(BAR_DONE), 0);
@@ -335,6 +367,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int i = warp - 12;
       constexpr uint32_t idesc_o = umma_idesc_bf16(128, kQN, 1, 0);
       const uint64_t dC0 = umma_desc_sw128(sbase + kOffB, kHalfBox, 1024);   // MN-major pair
+      const uint64_t dX0 = umma_desc_sw128(sbase + kOffA, kHalfBox, 1024);   // pair in ring A
       const uint64_t dP0 = umma_desc_sw128(sbase + kOffP, 16, 1024);         // P^T
       for (int t = 0; t < T; ++t) {
         if (!wait_or_abort(bar(BAR_PFULL + (t & 1)), (t >> 1) & 1, abort_flag)) break;
@@ -342,23 +375,26 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int u = i; u < 8; u += 2) {
           const int mb = u & 3, kh = u >> 2;
           const int pos = 8 * t + u, sl = pos % kSlotsB;
-          if (t == T - 1 && last_valid < kTileRows &&
-              !wait_or_abort(bar(BAR_ZEROB + sl), kh & 1, abort_flag)) {
+          const bool in_a = t == T - 1 && u >= 4;   // borrowed ring-A slot u - 4
+          if (t == T - 1 && zero_last &&
+              !wait_or_abort(in_a ? bar(BAR_ZEROX + (u - 4)) : bar(BAR_ZEROB + sl), 0, abort_flag)) {
             ok = false;
             break;
           }
-          if (!wait_or_abort(bar(BAR_FULLB + sl), (pos / kSlotsB) & 1, abort_flag)) {
+          if (!wait_or_abort(in_a ? bar(BAR_FULLX + (u - 4)) : bar(BAR_FULLB + sl),
+                             in_a ? 0 : (pos / kSlotsB) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint64_t c = dC0 + static_cast<uint64_t>((sl * 2 * kHalfBox) >> 4);
+          const uint64_t c = in_a ? dX0 + static_cast<uint64_t>(((u - 4) * kBoxBytes) >> 4)
+                                  : dC0 + static_cast<uint64_t>((sl * 2 * kHalfBox) >> 4);
           const uint64_t pd = dP0 + static_cast<uint64_t>(((t & 1) * kPBytes + kh * kPSub) >> 4);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             umma_bf16(tmem + kOCol + 32 * mb, c + ((ks * 2048) >> 4), pd + ((ks * 32) >> 4), idesc_o,
                       (t > 0 || kh > 0 || ks > 0) ? 1u : 0u);
-          umma_commit(bar(BAR_EMPTYB + sl));
+          if (!in_a) umma_commit(bar(BAR_EMPTYB + sl));
         }
         if (!ok) break;
         umma_commit(bar(BAR_ODONE + (t & 1)));
@@ -472,9 +508,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_PFULL + sb));
-      if (valid < kTileRows) {
-        // The last tile ends inside the sequence.  As each of its latent box
-        // pairs lands in ring B, zero the rows past the end (they may hold
+      if (t == T - 1 && zero_last) {
+        // The last tile reaches past the sequence's end.  As each of its latent
+        // box pairs lands in ring B, zero the rows past the end (they may hold
         // anything, NaN included) so that P = 0 times such a row adds exactly 0.
         // The PV of tile t-1 must have consumed every slot's previous fill first:
         // a parity wait on a slot whose previous fill is still in flight would
@@ -482,22 +518,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (t > 0) wait_or_abort(bar(BAR_ODONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag);
         for (int u = 0; u < 8; ++u) {
           const int kh = u >> 2;
-          const int first = max(0, valid - 64 * kh);   // first row of this half to clear
+          const int first = max(0, zero_from - 64 * kh);   // first row of this half to clear
           const int nrow = 64 - first;
           const int pos = 8 * t + u, sl = pos % kSlotsB;
-          wait_or_abort(bar(BAR_FULLB + sl), (pos / kSlotsB) & 1, abort_flag);
+          const bool in_a = u >= 4;   // the last tile's second half sits in ring A
+          wait_or_abort(in_a ? bar(BAR_FULLX + (u - 4)) : bar(BAR_FULLB + sl),
+                        in_a ? 0 : (pos / kSlotsB) & 1, abort_flag);
+          uint8_t* pair = smem + (in_a ? kOffA + (u - 4) * kBoxBytes : kOffB + 2 * sl * kHalfBox);
           for (int c = tid; c < 2 * nrow * 8; c += kSoftThreads) {
             const int h = c / (nrow * 8), rem = c % (nrow * 8);
-            *reinterpret_cast<uint4*>(smem + kOffB + (2 * sl + h) * kHalfBox +
-                                      (first + rem / 8) * 128 + (rem % 8) * 16) =
+            *reinterpret_cast<uint4*>(pair + h * kHalfBox + (first + rem / 8) * 128 + (rem % 8) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bar(BAR_ZEROB + sl));
+          if (lane == 0) mbar_arrive(in_a ? bar(BAR_ZEROX + (u - 4)) : bar(BAR_ZEROB + sl));
         }
       }
     }
+    // The combine may start launching: it waits for this grid anyway, and a
+    // dependent that starts much earlier only sleeps longer.
+    if (tid == 0) pdl_launch_dependents();
     // Softmax denominators over the chunk's rows.
     {
       float tt[kHalfHeads];
@@ -614,10 +655,15 @@ __global__ void __launch_bounds__(kThreads)
 
 // Merge of the chunk partials of one (sequence, head):
 //   L = log sum_j exp(lse_j),  o_c = sum_j exp(lse_j - L) o_j.
+// Thread t owns latent columns [4t, 4t+4).  Chunks are taken kCombineChunk at a
+// time with every load of a group in flight at once; a running maximum keeps
+// the weights finite (each thread recomputes the group's weights itself, so
+// there is no shared memory and no block barrier).
+constexpr int kCombineChunk = 20;
 __global__ void __launch_bounds__(128)
     combine_kernel(const SplitParams p, float* o_c, float* lse_out) {
-  extern __shared__ float wts[];  // [splits]
   const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  pdl_wait();   // the partials come from the split kernel just before
   const int len = clamp_length(p, b, false);
   const int nsplit = (len + p.chunk - 1) / p.chunk;
   float* out = o_c + (size_t(b) * p.H + h) * kDc;
@@ -628,48 +674,43 @@ __global__ void __launch_bounds__(128)
   }
   const size_t stride = size_t(p.H);  // between consecutive splits of one (b, h)
   const float* lse_bh = p.part_lse + size_t(b) * p.splits * p.H + h;
-  __shared__ float red[4];
-  float mx = -INFINITY;
-  for (int s = tid; s < nsplit; s += 128) mx = fmaxf(mx, lse_bh[s * stride]);
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-  if ((tid & 31) == 0) red[tid >> 5] = mx;
-  __syncthreads();
-  mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  __syncthreads();
-  float sum = 0.f;
-  for (int s = tid; s < nsplit; s += 128) {
-    const float w = expf(lse_bh[s * stride] - mx);
-    wts[s] = w;
-    sum += w;
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-  if ((tid & 31) == 0) red[tid >> 5] = sum;
-  __syncthreads();
-  sum = red[0] + red[1] + red[2] + red[3];
-  const float inv = 1.f / sum;
-  const float* po = p.part_o + (size_t(b) * p.splits * p.H + h) * kDc;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + (size_t(b) * p.splits * p.H + h) * kDc) + tid;
+  float m = -INFINITY, sum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  // Eight chunk partials in flight per thread before they are accumulated.
-  for (int s0 = 0; s0 < nsplit; s0 += 8) {
-    float4 v[8];
+  for (int s0 = 0; s0 < nsplit; s0 += kCombineChunk) {
+    float ls[kCombineChunk];
+    float4 v[kCombineChunk];
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
-      v[u] = s0 + u < nsplit
-                 ? reinterpret_cast<const float4*>(po + size_t(s0 + u) * stride * kDc)[tid]
-                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < kCombineChunk; ++u) {
+      const bool ok = s0 + u < nsplit;
+      ls[u] = ok ? lse_bh[(s0 + u) * stride] : -INFINITY;
+      v[u] = ok ? po[(s0 + u) * stride * (kDc / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (s0 + kCombineChunk >= nsplit && tid == 0) pdl_launch_dependents();
+    float cm = m;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float w = s0 + u < nsplit ? wts[s0 + u] * inv : 0.f;
+    for (int u = 0; u < kCombineChunk; ++u) cm = fmaxf(cm, ls[u]);
+    // cm is finite: every chunk with rows has a finite lse.
+    const float r = m == -INFINITY ? 0.f : expf(m - cm);
+    sum *= r;
+    acc.x *= r;
+    acc.y *= r;
+    acc.z *= r;
+    acc.w *= r;
+#pragma unroll
+    for (int u = 0; u < kCombineChunk; ++u) {
+      const float w = s0 + u < nsplit ? expf(ls[u] - cm) : 0.f;
+      sum += w;
       acc.x = fmaf(w, v[u].x, acc.x);
       acc.y = fmaf(w, v[u].y, acc.y);
       acc.z = fmaf(w, v[u].z, acc.z);
       acc.w = fmaf(w, v[u].w, acc.w);
     }
+    m = cm;
   }
-  reinterpret_cast<float4*>(out)[tid] = acc;
-  if (tid == 0 && lse_out) lse_out[size_t(b) * p.H + h] = mx + logf(sum);
+  const float inv = 1.f / sum;
+  reinterpret_cast<float4*>(out)[tid] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  if (tid == 0 && lse_out) lse_out[size_t(b) * p.H + h] = m + logf(sum);
 }
 
 // ------------------------------------------------------------------------- host side
@@ -686,13 +727,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// Rows per KV chunk (a multiple of the 128-row tile) and the resulting chunk
+// Rows per KV chunk (a multiple of kChunkAlign rows) and the resulting chunk
 // count.  With `requested` = 0 the count minimises a makespan estimate: waves
 // of CTAs over the SMs times (rows per chunk + a fixed per-CTA cost), plus the
 // combine's cost per chunk.  The bf16 kernel runs one CTA per SM.
 int chunk_rows(const mla_dims* d, int requested, int* splits_out) {
   const int S = d->s_max;
-  const int max_splits = (S + kTileRows - 1) / kTileRows;
+  const int max_splits = (S + kChunkAlign - 1) / kChunkAlign;
   int splits = requested;
   if (splits <= 0) {
     int dev = 0, sms = 148;
@@ -704,7 +745,7 @@ int chunk_rows(const mla_dims* d, int requested, int* splits_out) {
     double best = 1e300;
     splits = 1;
     for (int s = 1; s <= max_splits; ++s) {
-      const int chunk = ((S + s - 1) / s + kTileRows - 1) / kTileRows * kTileRows;
+      const int chunk = ((S + s - 1) / s + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
       const int s_eff = (S + chunk - 1) / chunk;
       if (s_eff != s) continue;
       const long long waves = (per_split * s_eff + slots - 1) / slots;
@@ -718,7 +759,7 @@ int chunk_rows(const mla_dims* d, int requested, int* splits_out) {
   if (splits > max_splits) splits = max_splits;
   if (splits < 1) splits = 1;
   int chunk = (S + splits - 1) / splits;
-  chunk = (chunk + kTileRows - 1) / kTileRows * kTileRows;
+  chunk = (chunk + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
   *splits_out = (S + chunk - 1) / chunk;
   return chunk;
 }
@@ -845,7 +886,7 @@ extern "C" mla_status mla_decode_split(const mla_dims* dims, const void* q_abs, 
       attr_set = true;
     }
     dim3 grid(dims->heads / kHeadGroup, p.splits, dims->batch);
-    split_tc_kernel<<<grid, kTcThreads, kTcSmem, s>>>(tmap, tmap_half, p);
+    launch_pdl(split_tc_kernel, grid, dim3(kTcThreads), kTcSmem, s, tmap, tmap_half, p);
   } else {
     dim3 grid(dims->heads, p.splits, dims->batch);
     split_f32_kernel<<<grid, kThreads, 0, s>>>(p);
@@ -865,8 +906,8 @@ extern "C" mla_status mla_decode_combine(const mla_dims* dims, const int32_t* le
   mla_status st = prepare(who, dims, nullptr, nullptr, nullptr, lengths, 1.f, num_splits,
                           const_cast<void*>(workspace), ws_bytes, nullptr, &p);
   if (st != MLA_OK) return st;
-  combine_kernel<<<dim3(dims->heads, dims->batch), 128, p.splits * sizeof(float),
-                   static_cast<cudaStream_t>(stream)>>>(p, o_c, lse);
+  launch_pdl(combine_kernel, dim3(dims->heads, dims->batch), dim3(128), 0,
+             static_cast<cudaStream_t>(stream), p, o_c, lse);
   return launch_status(who);
 }
 

@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(32)
                        int B, int H) {
   __shared__ __align__(128) uint8_t wt[kDn * 32];  // 128 k-rows x 16 bf16 columns
   const int h = blockIdx.x, cb = blockIdx.y, lane = threadIdx.x;
+  pdl_launch_dependents();   // the decode kernel may start its set-up and cache stream now
   const int c0 = cb * 16;
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
@@ -167,6 +168,9 @@ __global__ void __launch_bounds__(128)
     bf[ks][0] = *reinterpret_cast<const uint32_t*>(wrow + 16 * ks);
     bf[ks][1] = *reinterpret_cast<const uint32_t*>(wrow + 16 * ks + 8);
   }
+  // Launched after the combine with programmatic serialization: the weight
+  // loads above overlap it; o_c is its result.
+  pdl_wait();
   for (int mt = 0; mt * 16 < B; ++mt) {
     const int bA = mt * 16 + gq, bB = bA + 8;
     const float* rA = o_c + (size_t(bA) * H + h) * kDc + kw + 2 * cq;
@@ -283,8 +287,8 @@ extern "C" mla_status mla_out_proj(const mla_dims* dims, const float* o_c, const
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int B = dims->batch, H = dims->heads;
   if (dims->dtype == MLA_BF16) {
-    out_proj_bf16_kernel<<<dim3(H, kDv / 8), 128, 0, s>>>(
-        o_c, static_cast<const __nv_bfloat16*>(w_uv), static_cast<float*>(out), B, H);
+    launch_pdl(out_proj_bf16_kernel, dim3(H, kDv / 8), dim3(128), 0, s, o_c,
+               static_cast<const __nv_bfloat16*>(w_uv), static_cast<float*>(out), B, H);
   } else {
     out_proj_f32_kernel<<<dim3(H, B), 128, 0, s>>>(o_c, static_cast<const float*>(w_uv),
                                                    static_cast<float*>(out), B, H);

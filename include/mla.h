@@ -35,6 +35,16 @@
  *    and the workspace are fp32 in both cases (the bf16 decode kernel feeds
  *    the fp32 query and the softmax weights to the tensor cores as hi + lo
  *    bf16 pairs).
+ *  - Launch overlap: the kernels of mla_decode_attn (and of its halves) and
+ *    the bf16 kernel of mla_out_proj are launched with programmatic stream
+ *    serialization, so each may begin while the kernel before it on the stream
+ *    is still running -- but only if that kernel allows it explicitly
+ *    (griddepcontrol.launch_dependents), as mla_absorb_q and these kernels
+ *    do; after any other kernel, or a copy, they start as usual.  Before
+ *    waiting for their predecessor they read only the cache and lengths
+ *    (mla_decode_attn) or the weights (mla_out_proj); everything the
+ *    predecessor writes is read after the wait.  mla_absorb_q itself starts
+ *    as usual.
  *  - Supported sizes: d_c = 512, d_rope = 64, d_nope = 128, d_v = 128;
  *    batch >= 1; s_max >= 1; heads >= 1 (a multiple of 16 for MLA_BF16).
  *    Anything else returns MLA_ERR_UNSUPPORTED.
@@ -98,7 +108,7 @@ mla_status mla_absorb_q(const mla_dims* dims, const void* q_nope, const void* q_
 /*
  * mla_decode_num_splits -- the number of KV chunks per sequence that
  * mla_decode_attn will use for `requested` (0 = let the library choose from
- * the current device's SM count).  Chunks hold a multiple of 128 rows, so the
+ * the current device's SM count).  Chunks hold a multiple of 8 rows, so the
  * result can be smaller than `requested`.  Returns 0 for invalid dims.
  */
 int32_t mla_decode_num_splits(const mla_dims* dims, int32_t requested);

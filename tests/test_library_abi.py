@@ -91,11 +91,12 @@ def test_host_validation(lib):
 
 def test_split_planning(lib):
     mla, _ = lib
-    # explicit requests: chunks are multiples of 128 rows (the kernel's tile)
+    # explicit requests: chunks are multiples of 8 rows
     d = mla.dims(4, 16, 65536, mla.MLA_BF16)
     assert mla.num_splits(d, 128) == 128
-    assert mla.num_splits(mla.dims(1, 16, 256, mla.MLA_F32), 7) == 2    # 256 rows -> 2 chunks of 128
-    assert mla.num_splits(mla.dims(1, 16, 300, mla.MLA_F32), 3) == 3    # ceil(300/3)=100 -> 128-row chunks
+    assert mla.num_splits(mla.dims(1, 16, 256, mla.MLA_F32), 7) == 7    # 40-row chunks
+    assert mla.num_splits(mla.dims(1, 16, 20, mla.MLA_F32), 7) == 3     # 8-row chunks: 8, 8, 4
+    assert mla.num_splits(mla.dims(1, 16, 300, mla.MLA_F32), 3) == 3    # ceil(300/3)=100 -> 104-row chunks
     assert mla.num_splits(mla.dims(1, 16, 1, mla.MLA_F32), 5) == 1
     # workspace grows with splits: B*splits*H*(512+1) floats (256-byte aligned pieces)
     n = 4 * 128 * 16
@@ -104,4 +105,4 @@ def test_split_planning(lib):
     # automatic choice is a valid split count
     for (B, H, S) in [(8, 16, 4096), (64, 16, 8192), (32, 128, 16384), (1, 16, 64)]:
         s = mla.num_splits(mla.dims(B, H, S, mla.MLA_BF16), 0)
-        assert 1 <= s <= (S + 127) // 128
+        assert 1 <= s <= (S + 7) // 8
