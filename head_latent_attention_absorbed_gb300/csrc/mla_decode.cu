@@ -30,8 +30,8 @@ struct SplitParams {
   const void* q_pe;
   const void* cache;        // used by the fp32 kernel
   const int32_t* lengths;
-  float* part_o;            // [B, splits, H, 512]
-  float* part_lse;          // [B, splits, H]
+  float* part_o;            // [B, H, splits, 512]: one (b, h)'s chunks contiguous
+  float* part_lse;          // [B, H, splits]
   int32_t* status;
   int B, H, s_max, splits, chunk;
   float scale_log2;         // softmax_scale * log2(e)
@@ -82,7 +82,8 @@ constexpr int BAR_FULLA = 0, BAR_EMPTYA = kSlotsA, BAR_FULLB = 2 * kSlotsA,
               BAR_EMPTYB = BAR_FULLB + kSlotsB, BAR_ZEROB = BAR_EMPTYB + kSlotsB,
               BAR_SFULL = BAR_ZEROB + kSlotsB, BAR_SFREE = BAR_SFULL + 2, BAR_PFULL = BAR_SFREE + 2,
               BAR_ODONE = BAR_PFULL + 2, BAR_LASTA = BAR_ODONE + 2, BAR_FULLX = BAR_LASTA + 1,
-              BAR_ZEROX = BAR_FULLX + 4, BAR_DONE = BAR_ZEROX + 4, kNumBars = BAR_DONE + 1;
+              BAR_ZEROX = BAR_FULLX + 8, BAR_ODONE2 = BAR_ZEROX + 8, BAR_PVPREV = BAR_ODONE2 + 1,
+              BAR_DONE = BAR_PVPREV + 1, kNumBars = BAR_DONE + 1;
 constexpr int kOffSlot = kOffBar + 8 * kNumBars;
 constexpr int kOffAbort = kOffSlot + 16;
 constexpr int kOffIssued = kOffAbort + 16;            // score tiles issued, per score issuer (ring B gate)
@@ -93,7 +94,8 @@ constexpr uint32_t kOCol = 128;                       // O^T blocks, 32 columns 
 // Rescale threshold (log2 units): P may grow to 2^8 before O is rescaled.
 constexpr float kRescaleLog2 = 8.f;
 static_assert(kTcSmem <= 232448, "shared memory plan exceeds 227 KB");
-static_assert(kSlotsA >= 4, "the last tile's second row half borrows four ring-A slots");
+static_assert(kSlotsA * kBoxBytes + 9 * kQBoxBytes >= 8 * kBoxBytes,
+              "the last tile's eight latent pairs fit in ring A and the query area");
 
 // Waits for a phase; gives up (and raises the CTA's abort flag) after kWaitNs,
 // or at once when another role has already raised it.
@@ -190,6 +192,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int row_base = b * p.s_max + r0;
   const int h0 = g * kHeadGroup;
   auto bar = [&](int i) { return bars + 8 * i; };
+  // The last tile's latent pairs.  With T >= 2 all eight go to space that is free
+  // once every score MMA has finished (ring-A slots 0-5, then the query area),
+  // so none waits for ring B; with T == 1 pairs 0-3 use ring B from the start
+  // and pairs 4-7 go to ring-A slots 0-3.
+  auto borrowed = [&](int t, int u) { return t == T - 1 && (T >= 2 || u >= 4); };
+  auto borrow_x = [&](int u) { return T >= 2 ? u : u - 4; };
+  auto borrow_off = [&](int x) {
+    return x < kSlotsA ? kOffA + x * kBoxBytes : kOffQ + (x - kSlotsA) * kBoxBytes;
+  };
 
   if (tid == 0) {
     for (int i = 0; i < kSlotsA; ++i) {
@@ -208,10 +219,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       mbar_init(bar(BAR_ODONE + i), 2);   // one commit per PV issuer
     }
     mbar_init(bar(BAR_LASTA), 2);         // every score MMA has finished
-    for (int i = 0; i < 4; ++i) {
-      mbar_init(bar(BAR_FULLX + i), 1);   // the last tile's pairs in ring A: one use each
+    for (int i = 0; i < 8; ++i) {
+      mbar_init(bar(BAR_FULLX + i), 1);   // the last tile's borrowed pairs: one use each
       mbar_init(bar(BAR_ZEROX + i), 8);
     }
+    mbar_init(bar(BAR_ODONE2), 2);        // the score issuers' share of the last PV
+    mbar_init(bar(BAR_PVPREV), 2);        // the PV of tile T-2 has finished
     mbar_init(bar(BAR_DONE), 4);          // every issuer's last commit
     *abort_flag = 0;
     s_issued[0] = 0;
@@ -247,25 +260,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int t = 0; t < T && !*abort_flag; ++t) {
         // From tile 1 on, wait until the score MMAs of tile t are issued (its P
         // follows soon); tile 0's pairs take the empty ring at once.
-        if (t > 0) {
+        if (t > 0 && !(t == T - 1 && T >= 2)) {
           const unsigned long long t0 = globaltimer_ns();
           while ((s_issued[0] <= t || s_issued[1] <= t) && !*abort_flag)
             if (globaltimer_ns() - t0 > kWaitNs) *abort_flag = 1;
         }
         // Unit u holds O^T block mb = u % 4 (ring slot mb) for row half u / 4.
-        // The last tile's second row half goes to ring-A slots 0-3 instead, free
-        // once every score MMA has finished, so the whole tile is in flight at once.
+        bool lasta = false;
         for (int u = 0; u < 8 && !*abort_flag; ++u) {
           const int mb = u & 3, kh = u >> 2;
           const int row = row_base + t * kTileRows + 64 * kh;
-          if (t == T - 1 && u >= 4) {
-            if (u == 4 && !wait_or_abort(bar(BAR_LASTA), 0, abort_flag)) break;
-            const int x = u - 4;
+          if (borrowed(t, u)) {
+            const int x = borrow_x(u);
+            if (!lasta && !wait_or_abort(bar(BAR_LASTA), 0, abort_flag)) break;
+            lasta = true;
             mbar_arrive_expect_tx(bar(BAR_FULLX + x), 2 * kHalfBox);
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-              tma_load_2d(sbase + kOffA + x * kBoxBytes + h * kHalfBox, &tmap_half,
-                          64 * (2 * mb + h), row, bar(BAR_FULLX + x), stream);
+              tma_load_2d(sbase + borrow_off(x) + h * kHalfBox, &tmap_half, 64 * (2 * mb + h), row,
+                          bar(BAR_FULLX + x), stream);
             continue;
           }
           const int pos = 8 * t + u, sl = pos % kSlotsB, use = pos / kSlotsB;
@@ -316,6 +329,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     named_bar_sync(2, kSoftThreads + 64);   // warps 0-7, 9, 11: the query is in place
   }
 
+  // One PV unit: O^T block u % 4 += C^T (pair u of tile t) . P^T (row half u / 4);
+  // four MMAs.  false if a wait gave up.
+  constexpr uint32_t idesc_o = umma_idesc_bf16(128, kQN, 1, 0);
+  auto pv_unit = [&](int t, int u) -> bool {
+    const int mb = u & 3, kh = u >> 2;
+    const int pos = 8 * t + u, sl = pos % kSlotsB;
+    const bool bw = borrowed(t, u);
+    const int x = bw ? borrow_x(u) : 0;
+    if (t == T - 1 && zero_last &&
+        !wait_or_abort(bw ? bar(BAR_ZEROX + x) : bar(BAR_ZEROB + sl), 0, abort_flag))
+      return false;
+    if (!wait_or_abort(bw ? bar(BAR_FULLX + x) : bar(BAR_FULLB + sl), bw ? 0 : (pos / kSlotsB) & 1,
+                       abort_flag))
+      return false;
+    tc_fence_after();
+    // MN-major pair: two 64-column boxes kHalfBox apart; the descriptor's
+    // start address moves by 16-byte units.
+    const uint64_t c = umma_desc_sw128(sbase + kOffA, kHalfBox, 1024) +
+                       static_cast<uint64_t>(((bw ? borrow_off(x) : kOffB + sl * 2 * kHalfBox) - kOffA) >> 4);
+    const uint64_t pd = umma_desc_sw128(sbase + kOffP, 16, 1024) +
+                        static_cast<uint64_t>(((t & 1) * kPBytes + kh * kPSub) >> 4);
+#pragma unroll
+    for (int ks = 0; ks < 4; ++ks)
+      umma_bf16(tmem + kOCol + 32 * mb, c + ((ks * 2048) >> 4), pd + ((ks * 32) >> 4), idesc_o,
+                (t > 0 || kh > 0 || ks > 0) ? 1u : 0u);
+    if (!bw) umma_commit(bar(BAR_EMPTYB + sl));
+    return true;
+  };
+
   if (warp == 9 || warp == 11) {
     // ------------------------------------------------------------ score MMA issuers
     // Issuer i takes the boxes whose stream position 9t + k has parity i, so it
@@ -355,49 +397,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         umma_commit(bar(BAR_SFULL + sb));
         s_issued[i] = t + 1;
       }
-      umma_commit(bar(BAR_LASTA));   // ring A is free for the last tile's PV pairs
+      umma_commit(bar(BAR_LASTA));   // ring A and the query area are free for the last pairs
+      // The last tile's PV is the tail of the kernel: these two threads take O^T
+      // blocks 2 and 3 of it (after the PV issuers have finished tile T-2, the
+      // previous writers of those blocks).
+      {
+        const int t = T - 1;
+        bool ok = !*abort_flag;
+        if (ok && T >= 2 && !wait_or_abort(bar(BAR_PVPREV), 0, abort_flag)) ok = false;
+        if (ok && !wait_or_abort(bar(BAR_PFULL + (t & 1)), (t >> 1) & 1, abort_flag)) ok = false;
+        if (ok && pv_unit(t, 2 + i)) pv_unit(t, 6 + i);
+        umma_commit(bar(BAR_ODONE2));
+      }
       // Every MMA this thread issued has finished before TMEM is released.
       umma_commit(bar(BAR_DONE));
       mbar_wait_bounded(bar(BAR_DONE), 0);
     }
   } else if (warp == 12 || warp == 13) {
     // ------------------------------------------------------------ PV MMA issuers
-    // Issuer i takes O^T blocks mb = i and i + 2 (ring-B slots i and i + 2).
+    // Issuer i takes O^T blocks mb = i and i + 2 (ring-B slots i and i + 2); of
+    // the last tile only block i (the score issuers take blocks 2 and 3).
     if (lane == 0) {
       const int i = warp - 12;
-      constexpr uint32_t idesc_o = umma_idesc_bf16(128, kQN, 1, 0);
-      const uint64_t dC0 = umma_desc_sw128(sbase + kOffB, kHalfBox, 1024);   // MN-major pair
-      const uint64_t dX0 = umma_desc_sw128(sbase + kOffA, kHalfBox, 1024);   // pair in ring A
-      const uint64_t dP0 = umma_desc_sw128(sbase + kOffP, 16, 1024);         // P^T
       for (int t = 0; t < T; ++t) {
         if (!wait_or_abort(bar(BAR_PFULL + (t & 1)), (t >> 1) & 1, abort_flag)) break;
         bool ok = true;
-        for (int u = i; u < 8; u += 2) {
-          const int mb = u & 3, kh = u >> 2;
-          const int pos = 8 * t + u, sl = pos % kSlotsB;
-          const bool in_a = t == T - 1 && u >= 4;   // borrowed ring-A slot u - 4
-          if (t == T - 1 && zero_last &&
-              !wait_or_abort(in_a ? bar(BAR_ZEROX + (u - 4)) : bar(BAR_ZEROB + sl), 0, abort_flag)) {
-            ok = false;
-            break;
-          }
-          if (!wait_or_abort(in_a ? bar(BAR_FULLX + (u - 4)) : bar(BAR_FULLB + sl),
-                             in_a ? 0 : (pos / kSlotsB) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint64_t c = in_a ? dX0 + static_cast<uint64_t>(((u - 4) * kBoxBytes) >> 4)
-                                  : dC0 + static_cast<uint64_t>((sl * 2 * kHalfBox) >> 4);
-          const uint64_t pd = dP0 + static_cast<uint64_t>(((t & 1) * kPBytes + kh * kPSub) >> 4);
-#pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(tmem + kOCol + 32 * mb, c + ((ks * 2048) >> 4), pd + ((ks * 32) >> 4), idesc_o,
-                      (t > 0 || kh > 0 || ks > 0) ? 1u : 0u);
-          if (!in_a) umma_commit(bar(BAR_EMPTYB + sl));
-        }
+        const int step = t == T - 1 ? 4 : 2;
+        for (int u = i; u < 8 && ok; u += step) ok = pv_unit(t, u);
         if (!ok) break;
         umma_commit(bar(BAR_ODONE + (t & 1)));
+        if (t == T - 2) umma_commit(bar(BAR_PVPREV));
       }
       umma_commit(bar(BAR_DONE));
       mbar_wait_bounded(bar(BAR_DONE), 0);
@@ -512,19 +541,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // The last tile reaches past the sequence's end.  As each of its latent
         // box pairs lands in ring B, zero the rows past the end (they may hold
         // anything, NaN included) so that P = 0 times such a row adds exactly 0.
-        // The PV of tile t-1 must have consumed every slot's previous fill first:
-        // a parity wait on a slot whose previous fill is still in flight would
-        // pass at once.
-        if (t > 0) wait_or_abort(bar(BAR_ODONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag);
+        // Borrowed pairs have single-use barriers; ring-B pairs of the last tile
+        // exist only when it is the first tile too (first fills).
         for (int u = 0; u < 8; ++u) {
           const int kh = u >> 2;
           const int first = max(0, zero_from - 64 * kh);   // first row of this half to clear
           const int nrow = 64 - first;
           const int pos = 8 * t + u, sl = pos % kSlotsB;
-          const bool in_a = u >= 4;   // the last tile's second half sits in ring A
-          wait_or_abort(in_a ? bar(BAR_FULLX + (u - 4)) : bar(BAR_FULLB + sl),
-                        in_a ? 0 : (pos / kSlotsB) & 1, abort_flag);
-          uint8_t* pair = smem + (in_a ? kOffA + (u - 4) * kBoxBytes : kOffB + 2 * sl * kHalfBox);
+          const bool bw = borrowed(t, u);
+          const int x = bw ? borrow_x(u) : 0;
+          wait_or_abort(bw ? bar(BAR_FULLX + x) : bar(BAR_FULLB + sl), bw ? 0 : (pos / kSlotsB) & 1,
+                        abort_flag);
+          uint8_t* pair = smem + (bw ? borrow_off(x) : kOffB + 2 * sl * kHalfBox);
           for (int c = tid; c < 2 * nrow * 8; c += kSoftThreads) {
             const int h = c / (nrow * 8), rem = c % (nrow * 8);
             *reinterpret_cast<uint4*>(pair + h * kHalfBox + (first + rem / 8) * 128 + (rem % 8) * 16) =
@@ -532,7 +560,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(in_a ? bar(BAR_ZEROX + (u - 4)) : bar(BAR_ZEROB + sl));
+          if (lane == 0) mbar_arrive(bw ? bar(BAR_ZEROX + x) : bar(BAR_ZEROB + sl));
         }
       }
     }
@@ -549,10 +577,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     // O^T after the last PV: this thread's latent row is d = 128 mb + 32 wq + lane.
     wait_or_abort(bar(BAR_ODONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1, abort_flag);
+    wait_or_abort(bar(BAR_ODONE2), 0, abort_flag);
     tc_fence_after();
     named_bar_sync(1, kSoftThreads);
     if (!*abort_flag) {
-      const size_t base = (size_t(b) * p.splits + j) * p.H + h0;
+      // Row (b, h, j) of the partials; heads h0 + hb + h are p.splits rows apart.
+      const size_t base = (size_t(b) * p.H + h0) * p.splits + j;
       float inv[kHalfHeads];
 #pragma unroll
       for (int h = 0; h < kHalfHeads; ++h) {
@@ -560,17 +590,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const float L = (q4.x + q4.y) + (q4.z + q4.w);
         inv[h] = L > 0.f ? 1.f / L : 0.f;
         if (wq == 0 && lane == h)
-          p.part_lse[base + hb + h] = L > 0.f ? (m[h] + log2f(L)) * kLn2 : -INFINITY;
+          p.part_lse[base + size_t(hb + h) * p.splits] = L > 0.f ? (m[h] + log2f(L)) * kLn2 : -INFINITY;
       }
+      uint32_t hi4[4][8], lo4[4][8];
 #pragma unroll
       for (int mb = 0; mb < 4; ++mb) {
-        uint32_t hi[8], lo[8];
-        tmem_ld8_nowait(tmem + lane_base + kOCol + 32 * mb + hb, hi);
-        tmem_ld8_nowait(tmem + lane_base + kOCol + 32 * mb + kHeadGroup + hb, lo);
-        tmem_wait_ld();
+        tmem_ld8_nowait(tmem + lane_base + kOCol + 32 * mb + hb, hi4[mb]);
+        tmem_ld8_nowait(tmem + lane_base + kOCol + 32 * mb + kHeadGroup + hb, lo4[mb]);
+      }
+      tmem_wait_ld();
+#pragma unroll
+      for (int mb = 0; mb < 4; ++mb) {
+        const uint32_t* hi = hi4[mb];
+        const uint32_t* lo = lo4[mb];
 #pragma unroll
         for (int h = 0; h < kHalfHeads; ++h)
-          p.part_o[(base + hb + h) * kDc + 128 * mb + 32 * wq + lane] =
+          p.part_o[(base + size_t(hb + h) * p.splits) * kDc + 128 * mb + 32 * wq + lane] =
               (__uint_as_float(hi[h]) + __uint_as_float(lo[h])) * inv[h];
       }
     }
@@ -644,7 +679,7 @@ __global__ void __launch_bounds__(kThreads)
     f[w] = wm[w] == -INFINITY ? 0.f : exp2f(wm[w] - M);
     L += f[w] * wl[w];
   }
-  const size_t base = (size_t(b) * p.splits + j) * p.H + h;
+  const size_t base = (size_t(b) * p.H + h) * p.splits + j;
   for (int c = tid; c < kDc; c += kThreads) {
     float v = 0.f;
     for (int w = 0; w < kWarps; ++w) v += f[w] * wo[w][c];
@@ -655,26 +690,29 @@ __global__ void __launch_bounds__(kThreads)
 
 // Merge of the chunk partials of one (sequence, head):
 //   L = log sum_j exp(lse_j),  o_c = sum_j exp(lse_j - L) o_j.
-// Thread t owns latent columns [4t, 4t+4).  Chunks are taken kCombineChunk at a
-// time with every load of a group in flight at once; a running maximum keeps
-// the weights finite (each thread recomputes the group's weights itself, so
-// there is no shared memory and no block barrier).
+// grid (H, B, 4), one warp per CTA: thread t of CTA z owns latent columns
+// [128z + 4t, 128z + 4t + 4).  Chunks are taken kCombineChunk at a time with
+// every load of a group in flight at once; a running maximum keeps the weights
+// finite (each thread recomputes the group's weights itself, so there is no
+// shared memory and no barrier).
 constexpr int kCombineChunk = 20;
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(32)
     combine_kernel(const SplitParams p, float* o_c, float* lse_out) {
-  const int h = blockIdx.x, b = blockIdx.y, tid = threadIdx.x;
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int tid = blockIdx.z * 32 + threadIdx.x;   // float4 column of the 512
+  const int len = clamp_length(p, b, false);   // a caller input, not the split's output
   pdl_wait();   // the partials come from the split kernel just before
-  const int len = clamp_length(p, b, false);
   const int nsplit = (len + p.chunk - 1) / p.chunk;
   float* out = o_c + (size_t(b) * p.H + h) * kDc;
   if (nsplit == 0) {
     reinterpret_cast<float4*>(out)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (tid == 0 && lse_out) lse_out[size_t(b) * p.H + h] = -INFINITY;
+    if (threadIdx.x == 0) pdl_launch_dependents();
     return;
   }
-  const size_t stride = size_t(p.H);  // between consecutive splits of one (b, h)
-  const float* lse_bh = p.part_lse + size_t(b) * p.splits * p.H + h;
-  const float4* po = reinterpret_cast<const float4*>(p.part_o + (size_t(b) * p.splits * p.H + h) * kDc) + tid;
+  const size_t row0 = (size_t(b) * p.H + h) * p.splits;   // this (b, h)'s chunks, contiguous
+  const float* lse_bh = p.part_lse + row0;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + row0 * kDc) + tid;
   float m = -INFINITY, sum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int s0 = 0; s0 < nsplit; s0 += kCombineChunk) {
@@ -683,10 +721,10 @@ __global__ void __launch_bounds__(128)
 #pragma unroll
     for (int u = 0; u < kCombineChunk; ++u) {
       const bool ok = s0 + u < nsplit;
-      ls[u] = ok ? lse_bh[(s0 + u) * stride] : -INFINITY;
-      v[u] = ok ? po[(s0 + u) * stride * (kDc / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+      ls[u] = ok ? lse_bh[s0 + u] : -INFINITY;
+      v[u] = ok ? po[size_t(s0 + u) * (kDc / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (s0 + kCombineChunk >= nsplit && tid == 0) pdl_launch_dependents();
+    if (s0 + kCombineChunk >= nsplit && threadIdx.x == 0) pdl_launch_dependents();
     float cm = m;
 #pragma unroll
     for (int u = 0; u < kCombineChunk; ++u) cm = fmaxf(cm, ls[u]);
@@ -906,7 +944,7 @@ extern "C" mla_status mla_decode_combine(const mla_dims* dims, const int32_t* le
   mla_status st = prepare(who, dims, nullptr, nullptr, nullptr, lengths, 1.f, num_splits,
                           const_cast<void*>(workspace), ws_bytes, nullptr, &p);
   if (st != MLA_OK) return st;
-  launch_pdl(combine_kernel, dim3(dims->heads, dims->batch), dim3(128), 0,
+  launch_pdl(combine_kernel, dim3(dims->heads, dims->batch, kDc / 128), dim3(32), 0,
              static_cast<cudaStream_t>(stream), p, o_c, lse);
   return launch_status(who);
 }
