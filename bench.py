@@ -373,33 +373,21 @@ def main_with(args, rank: int, world: int, local: int = 0):
     if int(step.status.item()) != 0:
         raise RuntimeError(f"device status {int(step.status.item())} after the split-only replay")
 
-    # End-to-end through the public call, with host buffers: per step the
-    # queries, lengths and positions go host->device from pinned memory and
-    # the output comes back device->host.
+    # End-to-end through the public API with host buffers: every step copies the
+    # queries, lengths and positions from pinned host memory and reads o back
+    # into pinned host memory.  Each layer copy's step is captured once with
+    # DecodeStep.capture and replayed.
     e2e = None
     if not args.no_e2e:
-        h_qn = [t.cpu().pin_memory() for t in qn]
-        h_qr = [t.cpu().pin_memory() for t in qr]
-        h_len = inp.lengths.pin_memory()
-        h_pos = inp.positions.pin_memory()
-        h_out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-        d_qn = torch.empty_like(qn[0])
-        d_qr = torch.empty_like(qr[0])
-        d_len = torch.empty_like(lengths)
-        d_pos = torch.empty_like(positions)
+        hosts = [step.capture(caches[l], wuk[l], wuv[l]) for l in range(L)]
+        for l, hs in enumerate(hosts):          # the host side fills each step's inputs
+            hs.q_nope.copy_(inp.q_nope)
+            hs.q_rope.copy_(inp.q_rope)
+            hs.lengths.copy_(inp.lengths)
+            hs.positions.copy_(inp.positions)
         Ke = min(K, 2000)
-
-        def e2e_step(k):
-            l = k % L
-            d_qn.copy_(h_qn[l], non_blocking=True)
-            d_qr.copy_(h_qr[l], non_blocking=True)
-            d_len.copy_(h_len, non_blocking=True)
-            d_pos.copy_(h_pos, non_blocking=True)
-            o = step.run(d_qn, d_qr, caches[l], d_len, d_pos, wuk[l], wuv[l])
-            h_out.copy_(o, non_blocking=True)
-
         for k in range(min(W, 20)):
-            e2e_step(k)
+            hosts[k % L].replay()
         torch.cuda.synchronize()
         if world > 1:
             dist.barrier()
@@ -407,17 +395,20 @@ def main_with(args, rank: int, world: int, local: int = 0):
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record()
         for k in range(Ke):
-            e2e_step(k)
+            hosts[k % L].replay()
         e1.record()
         torch.cuda.synchronize()
         e_ms = e0.elapsed_time(e1)
+        if int(step.status.item()) != 0:
+            raise RuntimeError(f"device status {int(step.status.item())} after the e2e steps")
         e_ms = max_over_ranks(e_ms, dev, world)
-        bi = sum(t.numel() * t.element_size() for t in (h_qn[0], h_qr[0], h_len, h_pos))
-        bo = h_out.numel() * h_out.element_size()
+        bi, bo = hosts[0].h2d_bytes, hosts[0].d2h_bytes
         e2e = {"value": whole_job_rate(cache_bytes, Ke, world, e_ms / 1e3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": Ke,
                "tokens_per_s": whole_job_rate(cfg.batch, Ke, world, e_ms / 1e3),
-               "path": "DecodeStep.run (three C-ABI calls, eager launches)"}
+               "path": "DecodeStep.capture: per step one pinned host->device copy of the "
+                       "queries, lengths and positions, the three C-ABI calls, one "
+                       "device->host copy of o; one CUDA-graph replay per step"}
 
     peak, peak_kind = measured_peaks()
     achieved = cache_bytes / split_avg_s / 1e9

@@ -19,7 +19,7 @@ __all__ = [
     "EXPORTED", "LIB_PATH", "MLA_BF16", "MLA_F32", "MLA_DEV_LENGTH_OUT_OF_RANGE",
     "MLA_DEV_PIPELINE_TIMEOUT", "MlaDims", "MlaError", "absorb_q", "decode_attn",
     "decode_attn_noalloc", "decode_split", "decode_combine", "dims",
-    "dtype_code", "load", "num_splits", "out_proj", "workspace_bytes", "DecodeStep",
+    "dtype_code", "load", "num_splits", "out_proj", "workspace_bytes", "DecodeStep", "HostStep",
 ]
 
 
@@ -58,3 +58,73 @@ class DecodeStep:
                     self.scale, self.splits_requested, self.lse, self.status, stream)
         out_proj(self.dims, self.o_c, w_uv, self.out, stream)
         return self.out
+
+    def capture(self, cache, w_uk, w_uv):
+        """Capture one whole step from host memory as a CUDA graph.
+
+        Returns a ``HostStep``: pinned host tensors ``q_nope``, ``q_rope``,
+        ``lengths``, ``positions`` (the step's inputs, filled by the caller) and
+        ``out`` (o, written by the step), and ``replay()``.  Every replay copies
+        the four inputs to the device in one transfer (they share one pinned
+        block), runs the three library calls against the device-resident cache
+        and weights, and copies o back in one transfer.
+        """
+        return HostStep(self, cache, w_uk, w_uv)
+
+
+class HostStep:
+    """A decode step captured by ``DecodeStep.capture`` (see there)."""
+
+    def __init__(self, step: DecodeStep, cache, w_uk, w_uv):
+        import torch
+        B, H = step.dims.batch, step.dims.heads
+        dt = cache.dtype
+        elt = cache.element_size()
+        pieces = [("q_nope", (B, H, 128), dt, elt), ("q_rope", (B, H, 64), dt, elt),
+                  ("lengths", (B,), torch.int32, 4), ("positions", (B,), torch.int32, 4)]
+        offs, off = [], 0
+        for _, shape, _, e in pieces:
+            n = 1
+            for x in shape:
+                n *= x
+            offs.append(off)
+            off += (n * e + 255) // 256 * 256        # every piece 256-byte aligned
+        dev = step.q_abs.device
+        self._h_block = torch.empty((off,), dtype=torch.uint8).pin_memory()
+        self._d_block = torch.empty((off,), dtype=torch.uint8, device=dev)
+
+        def view(block, i):
+            name, shape, dtype, e = pieces[i]
+            n = 1
+            for x in shape:
+                n *= x
+            return block[offs[i]:offs[i] + n * e].view(dtype).view(shape)
+
+        self.q_nope, self.q_rope, self.lengths, self.positions = (view(self._h_block, i)
+                                                                   for i in range(4))
+        d = [view(self._d_block, i) for i in range(4)]
+        self.out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
+        self.h2d_bytes = off
+        self.d2h_bytes = self.out.numel() * self.out.element_size()
+
+        def body():
+            self._d_block.copy_(self._h_block, non_blocking=True)
+            o = step.run(d[0], d[1], cache, d[2], d[3], w_uk, w_uv)
+            self.out.copy_(o, non_blocking=True)
+
+        # One run outside capture (module loading, kernel attributes); the inputs
+        # are whatever the block holds, so start from valid lengths.
+        self.lengths.fill_(1)
+        self.positions.zero_()
+        self.q_nope.zero_()
+        self.q_rope.zero_()
+        body()
+        torch.cuda.synchronize(dev)
+        self._graph = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=dev)
+        with torch.cuda.graph(self._graph, stream=side):
+            body()
+        self._keep = d
+
+    def replay(self):
+        self._graph.replay()

@@ -136,3 +136,36 @@ def test_v2lite_long_context_128_splits(cuda_lib):
     assert gpu["splits"] >= 128
     ref, bs = run_oracle(inp)
     compare(gpu, ref, bs, "bf16")
+
+
+def test_captured_step_from_host_memory(cuda_lib):
+    """DecodeStep.capture: a CUDA graph that copies the step's inputs from pinned host
+    memory, runs the three calls and copies o back; two replays with different host
+    inputs both match the eager path and the oracle."""
+    mla = cuda_lib
+    cfg = small(B=3, S=300)
+    base = make_inputs(cfg, seed=21, poison_tail=True,
+                       lengths=torch.tensor([300, 45, 129], dtype=torch.int32))
+    step = mla.DecodeStep(cfg.batch, cfg.heads, cfg.s_max, torch.bfloat16,
+                          rope_base=cfg.rope_base, softmax_scale=cfg.softmax_scale)
+    cache, w_uk, w_uv = base.cache.cuda(), base.w_uk.cuda(), base.w_uv.cuda()
+    hs = step.capture(cache, w_uk, w_uv)
+    hs.lengths.copy_(base.lengths)
+    hs.positions.copy_(base.positions)
+    for seed in (22, 23):
+        other = make_inputs(cfg, seed=seed)            # new queries; same cache and weights
+        hs.q_nope.copy_(other.q_nope)
+        hs.q_rope.copy_(other.q_rope)
+        hs.replay()
+        torch.cuda.synchronize()
+        got = hs.out.double().numpy().copy()
+        eager = step.run(other.q_nope.cuda(), other.q_rope.cuda(), cache, base.lengths.cuda(),
+                         base.positions.cuda(), w_uk, w_uv)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(got, eager.double().cpu().numpy())
+        inp = make_inputs(cfg, seed=21, poison_tail=True, lengths=base.lengths)
+        inp.q_nope, inp.q_rope = other.q_nope, other.q_rope
+        ref, bs = run_oracle(inp)
+        from _parity import assert_close
+        assert_close("o", got[bs], ref["o"], "bf16")
+    assert int(step.status.item()) == 0
