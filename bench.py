@@ -1,8 +1,9 @@
 #!/usr/bin/env python
 """Throughput of one MLA decode step (weight-absorbed, latent cache) on GB300.
 
-A step is the whole hot path for one batch: absorb_q -> decode split ->
-LSE combine -> out_proj, through the C ABI.  The default workload is
+A step is the whole hot path for one batch through the C-ABI call
+mla_decode_step: absorb_q -> decode split -> LSE combine -> out_proj (for
+bf16 the combine and out_proj run as one fused kernel).  The default workload is
 DeepSeek-V2-Lite decode in bf16: B=8 sequences of S=4096 cached rows, H=16.
 Each step reads one "layer": the bench keeps L copies of cache + weights
 (L chosen so that their total exceeds 3x the L2 size) and step k uses layer
@@ -306,12 +307,10 @@ def main_with(args, rank: int, world: int, local: int = 0):
     cache_bytes = int(inp.lengths.to(torch.int64).sum()) * cfg.row * inp.cache.element_size()
 
     def one_step(k):
+        # The whole step through the single call mla_decode_step: absorb, split,
+        # and (bf16) the fused combine + W_UV kernel.
         l = k % L
-        mla.absorb_q(d, qn[l], qr[l], wuk[l], positions, step.q_abs, step.q_pe, step.rope_base)
-        mla.decode_split(d, step.q_abs, step.q_pe, caches[l], lengths, step.workspace, step.scale,
-                         args.splits, step.status)
-        mla.decode_combine(d, lengths, step.workspace, step.o_c, args.splits, step.lse)
-        mla.out_proj(d, step.o_c, wuv[l], step.out)
+        step.run(qn[l], qr[l], caches[l], lengths, positions, wuk[l], wuv[l])
 
     K, W = args.steps, args.warmup
     for k in range(W):
@@ -439,7 +438,7 @@ def main_with(args, rank: int, world: int, local: int = 0):
         "tokens_per_s": tokens,
         "config": workload_config(cfg, L, step.splits),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": 4 * K,
+        "gpu_launches": (3 if cfg.dtype == "bf16" else 4) * K,
         "clocks": sampler.summary(),
         "timing": "one CUDA-graph replay of the timed steps (no event nodes inside), CUDA events "
                   "on the replay stream",

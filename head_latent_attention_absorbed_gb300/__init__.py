@@ -12,13 +12,13 @@ from typing import Optional
 
 from ._binding import (EXPORTED, LIB_PATH, MLA_BF16, MLA_DEV_LENGTH_OUT_OF_RANGE,
                        MLA_DEV_PIPELINE_TIMEOUT, MLA_F32, MlaDims, MlaError, absorb_q, decode_attn,
-                       decode_attn_noalloc, decode_combine, decode_split, dims, dtype_code, load,
-                       num_splits, out_proj, workspace_bytes)
+                       decode_attn_noalloc, decode_combine, decode_split, decode_step, dims,
+                       dtype_code, load, num_splits, out_proj, workspace_bytes)
 
 __all__ = [
     "EXPORTED", "LIB_PATH", "MLA_BF16", "MLA_F32", "MLA_DEV_LENGTH_OUT_OF_RANGE",
     "MLA_DEV_PIPELINE_TIMEOUT", "MlaDims", "MlaError", "absorb_q", "decode_attn",
-    "decode_attn_noalloc", "decode_split", "decode_combine", "dims",
+    "decode_attn_noalloc", "decode_split", "decode_combine", "decode_step", "dims",
     "dtype_code", "load", "num_splits", "out_proj", "workspace_bytes", "DecodeStep", "HostStep",
 ]
 
@@ -52,6 +52,14 @@ class DecodeStep:
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
 
     def run(self, q_nope, q_rope, cache, lengths, positions, w_uk, w_uv, stream=None):
+        """The whole step in one library call (mla_decode_step)."""
+        decode_step(self.dims, q_nope, q_rope, w_uk, positions, cache, lengths, w_uv,
+                    self.workspace, self.q_abs, self.q_pe, self.o_c, self.out, self.scale,
+                    self.rope_base, self.splits_requested, self.lse, self.status, stream)
+        return self.out
+
+    def run_calls(self, q_nope, q_rope, cache, lengths, positions, w_uk, w_uv, stream=None):
+        """The same step as the three separate calls absorb_q, decode_attn, out_proj."""
         absorb_q(self.dims, q_nope, q_rope, w_uk, positions, self.q_abs, self.q_pe,
                  self.rope_base, stream)
         decode_attn(self.dims, self.q_abs, self.q_pe, cache, lengths, self.o_c, self.workspace,

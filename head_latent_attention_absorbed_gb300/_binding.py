@@ -21,7 +21,7 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
           3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA"}
 EXPORTED = ("mla_absorb_q", "mla_decode_num_splits", "mla_decode_workspace_bytes",
             "mla_decode_attn", "mla_decode_split", "mla_decode_combine",
-            "mla_decode_attn_noalloc", "mla_out_proj",
+            "mla_decode_attn_noalloc", "mla_decode_step", "mla_out_proj",
             "mla_status_string", "mla_last_error_message")
 
 
@@ -65,6 +65,9 @@ def load(path: Optional[str] = None):
     lib.mla_decode_combine.restype = ctypes.c_int
     lib.mla_decode_attn_noalloc.argtypes = [D, P, P, P, P, ctypes.c_float, I32, P, P, P, P]
     lib.mla_decode_attn_noalloc.restype = ctypes.c_int
+    lib.mla_decode_step.argtypes = [D, P, P, P, P, ctypes.c_double, P, P, ctypes.c_float, I32, P,
+                                    P, SZ, P, P, P, P, P, P, P]
+    lib.mla_decode_step.restype = ctypes.c_int
     lib.mla_out_proj.argtypes = [D, P, P, P, P]
     lib.mla_out_proj.restype = ctypes.c_int
     lib.mla_status_string.argtypes = [ctypes.c_int]
@@ -178,6 +181,20 @@ def decode_attn_noalloc(d: MlaDims, q_abs, q_pe, cache, lengths, o_c, softmax_sc
                                           _ptr(lengths), float(softmax_scale),
                                           int(num_splits_requested), _ptr(o_c), _ptr(lse),
                                           _ptr(dev_status), _stream(stream)))
+
+
+def decode_step(d: MlaDims, q_nope, q_rope, w_uk, positions, cache, lengths, w_uv, workspace,
+                q_abs, q_pe, o_c, out, softmax_scale: float, rope_base: float = 10000.0,
+                num_splits_requested: int = 0, lse=None, dev_status=None, stream=None) -> None:
+    """absorb_q, decode_attn and out_proj in one call (bf16: fused combine + W_UV)."""
+    _cuda_contig(q_nope, q_rope, w_uk, positions, cache, lengths, w_uv, workspace, q_abs, q_pe,
+                 o_c, out, lse, dev_status)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().mla_decode_step(ctypes.byref(d), _ptr(q_nope), _ptr(q_rope), _ptr(w_uk),
+                                  _ptr(positions), float(rope_base), _ptr(cache), _ptr(lengths),
+                                  float(softmax_scale), int(num_splits_requested), _ptr(w_uv),
+                                  _ptr(workspace), nbytes, _ptr(q_abs), _ptr(q_pe), _ptr(o_c),
+                                  _ptr(lse), _ptr(out), _ptr(dev_status), _stream(stream)))
 
 
 def out_proj(d: MlaDims, o_c, w_uv, out, stream=None) -> None:

@@ -751,6 +751,108 @@ __global__ void __launch_bounds__(32)
   if (tid == 0 && lse_out) lse_out[size_t(b) * p.H + h] = m + logf(sum);
 }
 
+// Combine and value up-projection in one launch (bf16 weights), for the whole
+// decode step:
+//   o_c[b,h,:] = sum_j exp(lse_j - L) o_j     (as combine_kernel)
+//   o[b,h,e]   = sum_c W_UV[h,e,c] o_c[b,h,c]   (Multi-Head Latent Attention eq. 3.3.3)
+// grid (H, B, kDv / 32), 128 threads: CTA z produces o rows [32z, 32z + 32).
+// It is small (a few KB of shared memory, moderate registers) so that its
+// CTAs fit beside the split kernel's and launch before that kernel ends;
+// before waiting they ask L2 for their 32 KB slice of W_UV[h].  Each CTA then
+// merges the (b, h) chunk partials itself (each thread four columns, up to
+// kCombineChunk chunks in flight), the one with z = 0 also writes o_c and lse.
+// The slice is read coalesced: load k of thread t is 16-byte chunk 128 k + t,
+// so a warp holds 32 consecutive chunks of one row half and sums its eight
+// products per lane with shuffles.  fp32 arithmetic throughout.
+constexpr int kOutRows = 32;
+__global__ void __launch_bounds__(128)
+    combine_out_kernel(const SplitParams p, const __nv_bfloat16* __restrict__ w_uv,
+                       float* __restrict__ o_c, float* __restrict__ lse_out,
+                       float* __restrict__ out) {
+  __shared__ __align__(16) float oc[kDc];
+  __shared__ float half_dot[kOutRows][2];
+  const int h = blockIdx.x, b = blockIdx.y, z = blockIdx.z, tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const uint4* wslice = reinterpret_cast<const uint4*>(w_uv + (size_t(h) * kDv + kOutRows * z) * kDc);
+#pragma unroll
+  for (int i = 0; i < 2; ++i)   // 256 lines of 128 bytes, two per thread
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(wslice + 8 * (tid + 128 * i)));
+  const int len = clamp_length(p, b, false);   // a caller input, not the split's output
+  pdl_wait();   // the partials come from the split kernel just before
+  const int nsplit = (len + p.chunk - 1) / p.chunk;
+  float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lse_v = -INFINITY;
+  if (nsplit > 0) {
+    const size_t row0 = (size_t(b) * p.H + h) * p.splits;
+    const float* lse_bh = p.part_lse + row0;
+    const float4* po = reinterpret_cast<const float4*>(p.part_o + row0 * kDc) + tid;
+    float m = -INFINITY, sum = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s0 = 0; s0 < nsplit; s0 += kCombineChunk) {
+      float ls[kCombineChunk];
+      float4 v[kCombineChunk];
+#pragma unroll
+      for (int u = 0; u < kCombineChunk; ++u) {
+        const bool ok = s0 + u < nsplit;
+        ls[u] = ok ? lse_bh[s0 + u] : -INFINITY;
+        v[u] = ok ? po[size_t(s0 + u) * (kDc / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      float cm = m;
+#pragma unroll
+      for (int u = 0; u < kCombineChunk; ++u) cm = fmaxf(cm, ls[u]);
+      const float rs = m == -INFINITY ? 0.f : expf(m - cm);
+      sum *= rs;
+      acc.x *= rs;
+      acc.y *= rs;
+      acc.z *= rs;
+      acc.w *= rs;
+#pragma unroll
+      for (int u = 0; u < kCombineChunk; ++u) {
+        const float w = s0 + u < nsplit ? expf(ls[u] - cm) : 0.f;
+        sum += w;
+        acc.x = fmaf(w, v[u].x, acc.x);
+        acc.y = fmaf(w, v[u].y, acc.y);
+        acc.z = fmaf(w, v[u].z, acc.z);
+        acc.w = fmaf(w, v[u].w, acc.w);
+      }
+      m = cm;
+    }
+    const float inv = 1.f / sum;
+    r = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    lse_v = m + logf(sum);
+  }
+  reinterpret_cast<float4*>(oc)[tid] = r;
+  if (z == 0) {
+    reinterpret_cast<float4*>(o_c + (size_t(b) * p.H + h) * kDc)[tid] = r;
+    if (tid == 0 && lse_out) lse_out[size_t(b) * p.H + h] = lse_v;
+  }
+  uint4 wv[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) wv[k] = wslice[128 * k + tid];
+  __syncthreads();
+  // Chunk 128 k + tid: row 2k + warp / 2, columns 8 (tid % 64) .. + 8.
+  const float4* x = reinterpret_cast<const float4*>(oc) + 2 * (tid & 63);
+  const float4 x0 = x[0], x1 = x[1];
+  const float xs[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const uint32_t ww[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
+    float d = 0.f;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 wf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&ww[q]));
+      d = fmaf(wf.x, xs[2 * q], d);
+      d = fmaf(wf.y, xs[2 * q + 1], d);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+    if (lane == 0) half_dot[2 * k + (warp >> 1)][warp & 1] = d;
+  }
+  __syncthreads();
+  if (tid < kOutRows)
+    out[(size_t(b) * p.H + h) * kDv + kOutRows * z + tid] = half_dot[tid][0] + half_dot[tid][1];
+}
+
 // ------------------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -965,6 +1067,45 @@ extern "C" mla_status mla_decode_attn(const mla_dims* dims, const void* q_abs, c
     return st;
   }
   return mla_decode_combine(dims, lengths, num_splits, workspace, ws_bytes, o_c, lse, stream);
+}
+
+extern "C" mla_status mla_decode_step(const mla_dims* dims, const void* q_nope, const void* q_rope,
+                                      const void* w_uk, const int32_t* positions, double rope_base,
+                                      const void* cache, const int32_t* lengths, float softmax_scale,
+                                      int32_t num_splits, const void* w_uv, void* workspace,
+                                      size_t ws_bytes, float* q_abs, float* q_pe, float* o_c,
+                                      float* lse, float* out, int32_t* dev_status, void* stream) {
+  const char* who = "mla_decode_step";
+  mla_status st = check_dims(dims, who);
+  if (st != MLA_OK) return st;
+  if (!o_c || !out || !w_uv || !aligned16(o_c) || !aligned16(out) || !aligned16(w_uv)) {
+    set_error("%s: o_c, out and w_uv must be non-NULL 16-byte aligned pointers", who);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (dims->dtype != MLA_BF16) {
+    // The fp32 path has no fused tail: the three calls in order.
+    st = mla_absorb_q(dims, q_nope, q_rope, w_uk, positions, rope_base, q_abs, q_pe, stream);
+    if (st != MLA_OK) return st;
+    st = mla_decode_attn(dims, q_abs, q_pe, cache, lengths, softmax_scale, num_splits, workspace,
+                         ws_bytes, o_c, lse, dev_status, stream);
+    if (st != MLA_OK) return st;
+    return mla_out_proj(dims, o_c, w_uv, out, stream);
+  }
+  // Validate everything before the first launch, so an argument error leaves
+  // nothing half-enqueued.
+  SplitParams p;
+  st = prepare(who, dims, q_abs, q_pe, cache, lengths, softmax_scale, num_splits, workspace,
+               ws_bytes, dev_status, &p);
+  if (st != MLA_OK) return st;
+  st = mla_absorb_q(dims, q_nope, q_rope, w_uk, positions, rope_base, q_abs, q_pe, stream);
+  if (st != MLA_OK) return st;
+  st = mla_decode_split(dims, q_abs, q_pe, cache, lengths, softmax_scale, num_splits, workspace,
+                        ws_bytes, dev_status, stream);
+  if (st != MLA_OK) return st;
+  launch_pdl(combine_out_kernel, dim3(dims->heads, dims->batch, kDv / kOutRows), dim3(128), 0,
+             static_cast<cudaStream_t>(stream), p, static_cast<const __nv_bfloat16*>(w_uv), o_c,
+             lse, out);
+  return launch_status(who);
 }
 
 // ------------------------------------------------------- fixed scratch, no allocation

@@ -221,6 +221,25 @@ mla_status mla_decode_attn_noalloc(const mla_dims* dims, const void* q_abs, cons
 mla_status mla_out_proj(const mla_dims* dims, const float* o_c, const void* w_uv, void* out,
                         void* stream);
 
+/*
+ * mla_decode_step -- one whole decode step: mla_absorb_q, mla_decode_attn and
+ * mla_out_proj in one call, with the same arguments, meanings and results
+ * (q_abs, q_pe, o_c, lse and out are all written).
+ *
+ * With dtype MLA_BF16 the combine and the value up-projection run as one kernel
+ * (each CTA merges one (sequence, head)'s chunk partials and applies 32 rows of
+ * W_UV[h] to them in fp32), launched with programmatic stream serialization
+ * after the split kernel; before its wait it reads only w_uv and lengths.
+ * With MLA_F32 the three calls run in order.  Every argument is checked before
+ * anything is enqueued.  lse may be NULL.
+ */
+mla_status mla_decode_step(const mla_dims* dims, const void* q_nope, const void* q_rope,
+                           const void* w_uk, const int32_t* positions, double rope_base,
+                           const void* cache, const int32_t* lengths, float softmax_scale,
+                           int32_t num_splits, const void* w_uv, void* workspace,
+                           size_t workspace_bytes, float* q_abs, float* q_pe, float* o_c,
+                           float* lse, float* out, int32_t* dev_status, void* stream);
+
 /* Static English name of a status code. */
 const char* mla_status_string(mla_status status);
 

@@ -9,8 +9,10 @@ from oracle import mla_oracle as O
 from workloads import (TOL_BF16_MAX_ABS, TOL_BF16_REL_L2, TOL_F32_MAX_ABS, MlaInputs)
 
 
-def run_cuda(inp: MlaInputs, num_splits: int = 0, device: str = "cuda"):
-    """One decode step through the three library calls. Returns fp64 numpy arrays."""
+def run_cuda(inp: MlaInputs, num_splits: int = 0, device: str = "cuda", path: str = "step"):
+    """One decode step through the C ABI: ``path`` "step" is mla_decode_step (one call,
+    fused combine + W_UV for bf16), "calls" the three calls mla_absorb_q,
+    mla_decode_attn, mla_out_proj.  Returns fp64 numpy arrays."""
     import head_latent_attention_absorbed_gb300 as mla
     cfg = inp.cfg
     dt = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
@@ -18,8 +20,9 @@ def run_cuda(inp: MlaInputs, num_splits: int = 0, device: str = "cuda"):
                           num_splits_requested=num_splits, rope_base=cfg.rope_base,
                           softmax_scale=cfg.softmax_scale)
     dev = lambda t: t.to(device).contiguous()
-    step.run(dev(inp.q_nope), dev(inp.q_rope), dev(inp.cache), dev(inp.lengths),
-             dev(inp.positions), dev(inp.w_uk), dev(inp.w_uv))
+    run = step.run if path == "step" else step.run_calls
+    run(dev(inp.q_nope), dev(inp.q_rope), dev(inp.cache), dev(inp.lengths),
+        dev(inp.positions), dev(inp.w_uk), dev(inp.w_uv))
     torch.cuda.synchronize()
     f = lambda t: t.detach().to("cpu", torch.float64).numpy()
     return dict(q_abs=f(step.q_abs), q_pe=f(step.q_pe), o_c=f(step.o_c), lse=f(step.lse),

@@ -23,13 +23,14 @@ def small(dtype="bf16", B=3, H=16, S=200, **kw):
 
 
 # ------------------------------------------------------------------ small cases
+@pytest.mark.parametrize("path", ["step", "calls"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("splits", [0, 1, 2, 7])
-def test_small_ragged(cuda_lib, dtype, splits):
+def test_small_ragged(cuda_lib, dtype, splits, path):
     cfg = small(dtype)
     inp = make_inputs(cfg, seed=splits, poison_tail=True,
                       lengths=torch.tensor([1, 33, 200], dtype=torch.int32))
-    gpu = run_cuda(inp, num_splits=splits)
+    gpu = run_cuda(inp, num_splits=splits, path=path)
     ref, bs = run_oracle(inp)
     compare(gpu, ref, bs, dtype)
     assert gpu["status"] == 0
@@ -45,10 +46,11 @@ def test_tile_edges(cuda_lib, lengths):
 
 
 @pytest.mark.parametrize("H", [32, 128])
-def test_head_groups(cuda_lib, H):
+@pytest.mark.parametrize("path", ["step", "calls"])
+def test_head_groups(cuda_lib, H, path):
     cfg = small(H=H, B=2, S=300)
     inp = make_inputs(cfg, seed=H, lengths=torch.tensor([300, 137], dtype=torch.int32))
-    gpu = run_cuda(inp, num_splits=4)
+    gpu = run_cuda(inp, num_splits=4, path=path)
     ref, bs = run_oracle(inp)
     compare(gpu, ref, bs, "bf16")
 
@@ -106,9 +108,10 @@ def test_v2lite_f32_b1_s64(cuda_lib):
 
 
 @pytest.mark.parametrize("seed", [0, 1])
-def test_v2lite_bf16_b8_s4096(cuda_lib, seed):
+@pytest.mark.parametrize("path", ["step", "calls"])
+def test_v2lite_bf16_b8_s4096(cuda_lib, seed, path):
     inp = make_inputs(V2LITE_BF16_B8_S4096, seed=seed)
-    gpu = run_cuda(inp)
+    gpu = run_cuda(inp, path=path)
     ref, bs = run_oracle(inp)
     compare(gpu, ref, bs, "bf16")
 
