@@ -202,11 +202,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     return x < kSlotsA ? kOffA + x * kBoxBytes : kOffQ + (x - kSlotsA) * kBoxBytes;
   };
 
-  if (tid == 0) {
+  // The cache stream starts before anything else: ring A's producer sets up its
+  // own barriers and issues the first fills before the CTA-wide barrier.
+  const uint64_t keep = l2_evict_last_policy();   // read again by ring B
+  if (warp == 8 && lane == 0) {
     for (int i = 0; i < kSlotsA; ++i) {
       mbar_init(bar(BAR_FULLA + i), 1);
       mbar_init(bar(BAR_EMPTYA + i), 1);
     }
+    fence_mbarrier_init();
+    prefetch_tmap(&tmap);
+    for (int pos = 0; pos < kSlotsA && pos < 9 * T; ++pos) {
+      mbar_arrive_expect_tx(bar(BAR_FULLA + pos), kBoxBytes);
+      tma_load_2d(sbase + kOffA + pos * kBoxBytes, &tmap, 64 * (pos % 9),
+                  row_base + (pos / 9) * kTileRows, bar(BAR_FULLA + pos), keep);
+    }
+  }
+  if (tid == 0) {
     for (int i = 0; i < kSlotsB; ++i) {
       mbar_init(bar(BAR_FULLB + i), 1);
       mbar_init(bar(BAR_EMPTYB + i), 1);
@@ -231,7 +243,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     s_issued[1] = 0;
     fence_mbarrier_init();
   }
-  if (warp == 8) tmem_alloc(smem_u32(slot_ptr), kTmemCols);
+  if (warp == 8) {
+    __syncwarp();
+    tmem_alloc(smem_u32(slot_ptr), kTmemCols);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -240,11 +255,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (warp == 8) {
     // ------------------------------------------------------------ ring A (HBM)
     if (lane == 0) {
-      prefetch_tmap(&tmap);
-      const uint64_t keep = l2_evict_last_policy();   // read again by ring B
       for (int t = 0; t < T && !*abort_flag; ++t) {
         for (int k = 0; k < 9; ++k) {
           const int pos = 9 * t + k, sl = pos % kSlotsA, use = pos / kSlotsA;
+          if (pos < kSlotsA) continue;   // issued before the CTA-wide barrier
           if (use > 0 && !wait_or_abort(bar(BAR_EMPTYA + sl), (use - 1) & 1, abort_flag)) break;
           mbar_arrive_expect_tx(bar(BAR_FULLA + sl), kBoxBytes);
           tma_load_2d(sbase + kOffA + sl * kBoxBytes, &tmap, 64 * k, row_base + t * kTileRows,
