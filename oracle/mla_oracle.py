@@ -197,3 +197,33 @@ def split_decode_combine(q_abs, q_pe, cache_b, n: int, scale: float, chunk: int)
     w = np.exp(lse - L)                       # [J, H]
     o_c = np.einsum("jh,jhc->hc", w, np.stack(os_))
     return o_c, L
+
+
+# ----------------------------------------------------------------------------- around the path
+def cache_append_row(x: np.ndarray, w_kva: np.ndarray, pos, d_c: int, base: float) -> np.ndarray:
+    """The cache row of one new token per sequence.
+
+    "Deepseek V2 Lite Inference Engine in C", MLA notes: one fused down-projection
+    kv_a_proj [d_c + d_rope, hidden] maps the token's hidden state to
+    (kv_lora, k_rope).  "Multi-Head Latent Attention" 3.5: the latent part is
+    what the cache stores; 3.7: the RoPE key is rotated at the token's position
+    before it is cached (the decode then uses it as stored).
+
+    x: [B, hidden]; w_kva: [d_c + d_rope, hidden]; pos: [B].  Returns [B, d_c + d_rope]:
+    [x . w_kva[:d_c]^T  ||  RoPE(x . w_kva[d_c:]^T, pos)].
+    """
+    y = np.asarray(x, dtype=np.float64) @ np.asarray(w_kva, dtype=np.float64).T
+    out = y.copy()
+    out[:, d_c:] = apply_rope(y[:, d_c:], np.asarray(pos), base)
+    return out
+
+
+def output_projection(o: np.ndarray, w_o: np.ndarray) -> np.ndarray:
+    """The attention layer's output: the heads' value outputs concatenated and
+    multiplied by W^O ("Multi-Head Latent Attention", eq. 3.3.3: W^O applied to the
+    concatenated per-head outputs).
+
+    o: [B, H, d_v]; w_o: [hidden, H * d_v].  Returns [B, hidden].
+    """
+    o = np.asarray(o, dtype=np.float64)
+    return o.reshape(o.shape[0], -1) @ np.asarray(w_o, dtype=np.float64).T

@@ -306,3 +306,50 @@ def test_pins_catch_a_dropped_rope_term(monkeypatch):
     mutated["cache"][..., 4:] = 0.0
     bad = O.decode_absorbed(**mutated, scale=0.5, base=10000.0)["o"][0]
     assert np.max(np.abs(bad - bo)) > 1e-6
+
+
+# ---------------------------------------------------------------- around the path
+def test_cache_append_brute_force_tiny():
+    """Scalar loops written out: y = W x, the last pair rotated by pos * theta."""
+    rng = np.random.default_rng(3)
+    d_c, d_r, hid = 3, 2, 4
+    x = rng.standard_normal((2, hid))
+    w = rng.standard_normal((d_c + d_r, hid))
+    pos = np.array([0, 5])
+    got = O.cache_append_row(x, w, pos, d_c, 10000.0)
+    for b in range(2):
+        y = [sum(w[o][k] * x[b][k] for k in range(hid)) for o in range(d_c + d_r)]
+        for o in range(d_c):
+            assert got[b, o] == pytest.approx(y[o], abs=1e-12)
+        ang = pos[b] * 1.0          # theta_0 = base^0 = 1 for a single pair
+        c, s = math.cos(ang), math.sin(ang)
+        assert got[b, d_c] == pytest.approx(c * y[d_c] - s * y[d_c + 1], abs=1e-12)
+        assert got[b, d_c + 1] == pytest.approx(s * y[d_c] + c * y[d_c + 1], abs=1e-12)
+
+
+def test_appended_keys_give_relative_scores():
+    """Keys appended at positions m and query rotated at position n score by n - m
+    only: shifting every position by the same amount leaves all scores unchanged."""
+    rng = np.random.default_rng(4)
+    d_c, d_r, hid = 4, 8, 6
+    w = rng.standard_normal((d_c + d_r, hid))
+    xs = rng.standard_normal((5, hid))
+    q = rng.standard_normal(d_r)
+    def scores(shift):
+        rows = np.stack([O.cache_append_row(xs[t:t + 1], w, [t + shift], d_c, 10000.0)[0]
+                         for t in range(5)])
+        qr = O.apply_rope(q, 4 + shift, 10000.0)
+        return rows[:, d_c:] @ qr
+    np.testing.assert_allclose(scores(0), scores(1234), rtol=0, atol=1e-9)
+
+
+def test_output_projection_brute_force_and_identity():
+    rng = np.random.default_rng(5)
+    o = rng.standard_normal((2, 3, 2))
+    w = rng.standard_normal((4, 6))
+    got = O.output_projection(o, w)
+    for b in range(2):
+        flat = [o[b, h, e] for h in range(3) for e in range(2)]
+        for n in range(4):
+            assert got[b, n] == pytest.approx(sum(w[n][k] * flat[k] for k in range(6)), abs=1e-12)
+    np.testing.assert_allclose(O.output_projection(o, np.eye(6)), o.reshape(2, 6), atol=0)

@@ -95,3 +95,40 @@ def make_inputs(cfg: MlaConfig, seed: int = 0, poison_tail: bool = False,
     positions = (drawn - 1).clamp(min=0).to(torch.int32)
     return MlaInputs(cfg=cfg, cache=cache, q_nope=q_nope.to(st), q_rope=q_rope.to(st),
                      w_uk=w_uk.to(st), w_uv=w_uv.to(st), lengths=drawn, positions=positions)
+
+
+@dataclass
+class AppendInputs:
+    cfg: MlaConfig
+    x: torch.Tensor          # [B, hidden] storage dtype: the new token's hidden state
+    w_kva: torch.Tensor      # [d_c + d_rope, hidden] storage dtype
+    positions: torch.Tensor  # [B] int32: the row each token goes to
+
+
+def make_append_inputs(cfg: MlaConfig, seed: int = 0) -> AppendInputs:
+    """Inputs of the cache-append step: x ~ N(0, 1), W_kva ~ N(0, std^2), positions
+    uniform in [0, s_max) -- drawn in that order from one seeded CPU generator."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    st = _storage(cfg)
+    x = torch.randn((cfg.batch, cfg.hidden), generator=g, dtype=torch.float32)
+    w = torch.randn((cfg.row, cfg.hidden), generator=g, dtype=torch.float32) * cfg.weight_std
+    pos = torch.randint(0, cfg.s_max, (cfg.batch,), generator=g, dtype=torch.int64).to(torch.int32)
+    return AppendInputs(cfg=cfg, x=x.to(st), w_kva=w.to(st), positions=pos)
+
+
+@dataclass
+class OutProjInputs:
+    cfg: MlaConfig
+    o: torch.Tensor          # [B, H, d_v] fp32: the heads' value outputs (out_proj's result)
+    w_o: torch.Tensor        # [hidden, H * d_v] storage dtype
+
+
+def make_wo_inputs(cfg: MlaConfig, seed: int = 0) -> OutProjInputs:
+    """Inputs of the W^O projection: o ~ N(0, 1) in fp32, W_O ~ N(0, std^2), in that
+    order from one seeded CPU generator."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(seed)
+    o = torch.randn((cfg.batch, cfg.heads, cfg.d_v), generator=g, dtype=torch.float32)
+    w = torch.randn((cfg.hidden, cfg.heads * cfg.d_v), generator=g, dtype=torch.float32) * cfg.weight_std
+    return OutProjInputs(cfg=cfg, o=o, w_o=w.to(_storage(cfg)))
