@@ -11,7 +11,8 @@ from __future__ import annotations
 from typing import Optional
 
 from ._binding import (EXPORTED, LIB_PATH, MLA_BF16, MLA_DEV_LENGTH_OUT_OF_RANGE,
-                       MLA_DEV_PIPELINE_TIMEOUT, MLA_F32, MlaDims, MlaError, absorb_q, decode_attn,
+                       MLA_DEV_PIPELINE_TIMEOUT, MLA_F32, MlaDims, MlaError, absorb_q, cache_append,
+                       decode_attn, wo_proj,
                        decode_attn_noalloc, decode_combine, decode_split, decode_step, dims,
                        dtype_code, load, num_splits, out_proj, workspace_bytes)
 
@@ -20,6 +21,7 @@ __all__ = [
     "MLA_DEV_PIPELINE_TIMEOUT", "MlaDims", "MlaError", "absorb_q", "decode_attn",
     "decode_attn_noalloc", "decode_split", "decode_combine", "decode_step", "dims",
     "dtype_code", "load", "num_splits", "out_proj", "workspace_bytes", "DecodeStep", "HostStep",
+    "cache_append", "wo_proj",
 ]
 
 

@@ -21,7 +21,8 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
           3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA"}
 EXPORTED = ("mla_absorb_q", "mla_decode_num_splits", "mla_decode_workspace_bytes",
             "mla_decode_attn", "mla_decode_split", "mla_decode_combine",
-            "mla_decode_attn_noalloc", "mla_decode_step", "mla_out_proj",
+            "mla_decode_attn_noalloc", "mla_decode_step", "mla_out_proj", "mla_cache_append",
+            "mla_wo_proj",
             "mla_status_string", "mla_last_error_message")
 
 
@@ -68,6 +69,10 @@ def load(path: Optional[str] = None):
     lib.mla_decode_step.argtypes = [D, P, P, P, P, ctypes.c_double, P, P, ctypes.c_float, I32, P,
                                     P, SZ, P, P, P, P, P, P, P]
     lib.mla_decode_step.restype = ctypes.c_int
+    lib.mla_cache_append.argtypes = [D, I32, P, P, P, ctypes.c_double, P, P, P]
+    lib.mla_cache_append.restype = ctypes.c_int
+    lib.mla_wo_proj.argtypes = [D, I32, P, P, P, P]
+    lib.mla_wo_proj.restype = ctypes.c_int
     lib.mla_out_proj.argtypes = [D, P, P, P, P]
     lib.mla_out_proj.restype = ctypes.c_int
     lib.mla_status_string.argtypes = [ctypes.c_int]
@@ -201,3 +206,19 @@ def out_proj(d: MlaDims, o_c, w_uv, out, stream=None) -> None:
     """o = W_UV . o_c per head."""
     _cuda_contig(o_c, w_uv, out)
     _check(load().mla_out_proj(ctypes.byref(d), _ptr(o_c), _ptr(w_uv), _ptr(out), _stream(stream)))
+
+
+def cache_append(d: MlaDims, x, w_kva, positions, cache, rope_base: float = 10000.0,
+                 dev_status=None, stream=None) -> None:
+    """Write the new token of each sequence into the cache at positions[b]."""
+    _cuda_contig(x, w_kva, positions, cache, dev_status)
+    _check(load().mla_cache_append(ctypes.byref(d), int(x.shape[-1]), _ptr(x), _ptr(w_kva),
+                                   _ptr(positions), float(rope_base), _ptr(cache),
+                                   _ptr(dev_status), _stream(stream)))
+
+
+def wo_proj(d: MlaDims, o, w_o, y, stream=None) -> None:
+    """y = concat_h(o[:, h, :]) . W_O^T."""
+    _cuda_contig(o, w_o, y)
+    _check(load().mla_wo_proj(ctypes.byref(d), int(w_o.shape[0]), _ptr(o), _ptr(w_o), _ptr(y),
+                              _stream(stream)))

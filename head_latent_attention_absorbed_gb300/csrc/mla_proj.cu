@@ -229,6 +229,179 @@ __global__ void __launch_bounds__(128)
   }
 }
 
+// ---------------------------------------------------------------------- row-major skinny GEMM
+// y[b, n] = sum_k x[b, k] * w[n, k] for a bf16 weight stored [N, K] (K contiguous),
+// the shape of both steps around the attention: the cache append's fused
+// down-projection kv_a_proj ("Deepseek V2 Lite Inference Engine in C", MLA
+// notes) and the output projection W^O ("Multi-Head Latent Attention" eq. 3.3.3).
+// grid (N / 8), 256 threads: warp w contracts K range [w K/8, (w+1) K/8) for
+// output columns [8 blockIdx.x, +8); the batch rows are the M side of
+// mma.sync m16n8k16 in tiles of 16, 64 rows per pass.  The weight's B
+// fragments come straight from global memory, eight K steps at a time; an fp32
+// x enters as bf16 hi + lo parts.  The eight warps' sums meet in shared memory
+// and each thread finishes two adjacent columns, so that a RoPE pair stays in
+// one thread.
+enum RowGemmMode { kWriteY = 0, kAppendRow = 1 };
+
+struct RowGemmArgs {
+  const void* x;               // [B, K] fp32 or bf16
+  const __nv_bfloat16* w;      // [N, K]
+  int B, K, N;
+  float* y;                    // kWriteY: [B, N] fp32
+  void* cache;                 // kAppendRow: [B, s_max, N] bf16
+  const int32_t* positions;    // kAppendRow: [B], row written
+  int s_max, d_c;              // kAppendRow: columns >= d_c are rotated
+  int32_t* status;
+};
+
+template <typename XT, int kMode>
+__global__ void __launch_bounds__(256) rowgemm_kernel(const RowGemmArgs a, const RopeTheta th) {
+  __shared__ float red[8][64][9];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gq = lane >> 2, cq = lane & 3;
+  const int n0 = 8 * blockIdx.x;
+  const int kw = warp * (a.K / 8), kn = a.K / 8;
+  const __nv_bfloat16* wrow = a.w + size_t(n0 + gq) * a.K + kw + 2 * cq;
+  for (int b0 = 0; b0 < a.B; b0 += 64) {
+    float acc[4][4];
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[mt][r] = 0.f;
+    const int ntile = min(4, (a.B - b0 + 15) / 16);
+    for (int k0 = 0; k0 < kn; k0 += 128) {
+      uint32_t bf[8][2];
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const bool ok = k0 + 16 * ks < kn;
+        bf[ks][0] = ok ? *reinterpret_cast<const uint32_t*>(wrow + k0 + 16 * ks) : 0u;
+        bf[ks][1] = ok ? *reinterpret_cast<const uint32_t*>(wrow + k0 + 16 * ks + 8) : 0u;
+      }
+      for (int mt = 0; mt < ntile; ++mt) {
+        const int bA = b0 + 16 * mt + gq, bB = bA + 8;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          if (k0 + 16 * ks >= kn) break;
+          const int kk = kw + k0 + 16 * ks + 2 * cq;
+          uint32_t hi[4], lo[4];
+          if constexpr (sizeof(XT) == 4) {
+            const float* x = static_cast<const float*>(a.x);
+            const float2 z = make_float2(0.f, 0.f);
+            const float2 v0 = bA < a.B ? *reinterpret_cast<const float2*>(x + size_t(bA) * a.K + kk) : z;
+            const float2 v1 = bB < a.B ? *reinterpret_cast<const float2*>(x + size_t(bB) * a.K + kk) : z;
+            const float2 v2 = bA < a.B ? *reinterpret_cast<const float2*>(x + size_t(bA) * a.K + kk + 8) : z;
+            const float2 v3 = bB < a.B ? *reinterpret_cast<const float2*>(x + size_t(bB) * a.K + kk + 8) : z;
+            split_bf16(v0.x, v0.y, hi[0], lo[0]);
+            split_bf16(v1.x, v1.y, hi[1], lo[1]);
+            split_bf16(v2.x, v2.y, hi[2], lo[2]);
+            split_bf16(v3.x, v3.y, hi[3], lo[3]);
+            mma_bf16(acc[mt], hi, bf[ks][0], bf[ks][1]);
+            mma_bf16(acc[mt], lo, bf[ks][0], bf[ks][1]);
+          } else {
+            const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
+            hi[0] = bA < a.B ? *reinterpret_cast<const uint32_t*>(x + size_t(bA) * a.K + kk) : 0u;
+            hi[1] = bB < a.B ? *reinterpret_cast<const uint32_t*>(x + size_t(bB) * a.K + kk) : 0u;
+            hi[2] = bA < a.B ? *reinterpret_cast<const uint32_t*>(x + size_t(bA) * a.K + kk + 8) : 0u;
+            hi[3] = bB < a.B ? *reinterpret_cast<const uint32_t*>(x + size_t(bB) * a.K + kk + 8) : 0u;
+            mma_bf16(acc[mt], hi, bf[ks][0], bf[ks][1]);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int mt = 0; mt < 4; ++mt) {
+      red[warp][16 * mt + gq][2 * cq] = acc[mt][0];
+      red[warp][16 * mt + gq][2 * cq + 1] = acc[mt][1];
+      red[warp][16 * mt + gq + 8][2 * cq] = acc[mt][2];
+      red[warp][16 * mt + gq + 8][2 * cq + 1] = acc[mt][3];
+    }
+    __syncthreads();
+    {
+      const int r = tid >> 2, c = 2 * (tid & 3);   // 64 rows x 4 column pairs
+      const int b = b0 + r, n = n0 + c;
+      float v0 = 0.f, v1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        v0 += red[w][r][c];
+        v1 += red[w][r][c + 1];
+      }
+      if (b < a.B) {
+        if constexpr (kMode == kWriteY) {
+          *reinterpret_cast<float2*>(a.y + size_t(b) * a.N + n) = make_float2(v0, v1);
+        } else {
+          const int pos = a.positions[b];
+          if (pos < 0 || pos >= a.s_max) {
+            if (c == 0 && blockIdx.x == 0) report(a.status, MLA_DEV_LENGTH_OUT_OF_RANGE);
+          } else {
+            if (n >= a.d_c) {
+              // RoPE on the key part: the pair (n, n + 1) as one complex number,
+              // rotated by pos * theta_i; the angle in fp64, reduced mod 2 pi.
+              const double two_pi = 6.283185307179586;
+              const double ang = static_cast<double>(pos) * th.theta[(n - a.d_c) / 2];
+              const double rr = ang - two_pi * rint(ang / two_pi);
+              float sn, cs;
+              sincosf(static_cast<float>(rr), &sn, &cs);
+              const float x0 = v0, x1 = v1;
+              v0 = cs * x0 - sn * x1;
+              v1 = sn * x0 + cs * x1;
+            }
+            *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(a.cache) +
+                                               (size_t(b) * a.s_max + pos) * a.N + n) =
+                __floats2bfloat162_rn(v0, v1);
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// fp32 weights and inputs: one warp per output (b, n), fp32 arithmetic throughout.
+template <int kMode>
+__global__ void __launch_bounds__(256) rowgemm_f32_kernel(const RowGemmArgs a, const RopeTheta th,
+                                                          const float* __restrict__ w) {
+  const int warp = (blockIdx.x * 256 + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  const int npairs = a.N / 2;
+  if (warp >= a.B * npairs) return;
+  const int b = warp / npairs, n = 2 * (warp % npairs);
+  const float* x = static_cast<const float*>(a.x) + size_t(b) * a.K;
+  float v0 = 0.f, v1 = 0.f;
+  for (int k = lane; k < a.K; k += 32) {
+    const float xv = x[k];
+    v0 = fmaf(xv, w[size_t(n) * a.K + k], v0);
+    v1 = fmaf(xv, w[size_t(n + 1) * a.K + k], v1);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    v0 += __shfl_xor_sync(0xffffffffu, v0, off);
+    v1 += __shfl_xor_sync(0xffffffffu, v1, off);
+  }
+  if (lane != 0) return;
+  if constexpr (kMode == kWriteY) {
+    a.y[size_t(b) * a.N + n] = v0;
+    a.y[size_t(b) * a.N + n + 1] = v1;
+  } else {
+    const int pos = a.positions[b];
+    if (pos < 0 || pos >= a.s_max) {
+      report(a.status, MLA_DEV_LENGTH_OUT_OF_RANGE);
+      return;
+    }
+    if (n >= a.d_c) {
+      const double two_pi = 6.283185307179586;
+      const double ang = static_cast<double>(pos) * th.theta[(n - a.d_c) / 2];
+      const double rr = ang - two_pi * rint(ang / two_pi);
+      float sn, cs;
+      sincosf(static_cast<float>(rr), &sn, &cs);
+      const float x0 = v0, x1 = v1;
+      v0 = cs * x0 - sn * x1;
+      v1 = sn * x0 + cs * x1;
+    }
+    float* row = static_cast<float*>(a.cache) + (size_t(b) * a.s_max + pos) * a.N;
+    row[n] = v0;
+    row[n + 1] = v1;
+  }
+}
+
 }  // namespace
 }  // namespace mla
 
@@ -292,6 +465,92 @@ extern "C" mla_status mla_out_proj(const mla_dims* dims, const float* o_c, const
   } else {
     out_proj_f32_kernel<<<dim3(H, B), 128, 0, s>>>(o_c, static_cast<const float*>(w_uv),
                                                    static_cast<float*>(out), B, H);
+  }
+  return launch_status(who);
+}
+
+extern "C" mla_status mla_cache_append(const mla_dims* dims, int32_t hidden, const void* x,
+                                       const void* w_kva, const int32_t* positions,
+                                       double rope_base, void* cache, int32_t* dev_status,
+                                       void* stream) {
+  const char* who = "mla_cache_append";
+  mla_status st = check_dims(dims, who);
+  if (st != MLA_OK) return st;
+  if (!x || !w_kva || !positions || !cache) {
+    set_error("%s: a required pointer is NULL", who);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (!aligned16(x) || !aligned16(w_kva) || !aligned16(cache)) {
+    set_error("%s: x, w_kva and cache must be 16-byte aligned", who);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (hidden <= 0 || hidden % 128 != 0) {
+    set_error("%s: hidden = %d must be a positive multiple of 128", who, hidden);
+    return hidden <= 0 ? MLA_ERR_INVALID_ARG : MLA_ERR_UNSUPPORTED;
+  }
+  if (!(rope_base > 0.0) || !isfinite(rope_base)) {
+    set_error("%s: rope_base must be finite and > 0", who);
+    return MLA_ERR_INVALID_ARG;
+  }
+  RopeTheta th;
+  for (int i = 0; i < kDr / 2; ++i) th.theta[i] = pow(rope_base, -2.0 * i / kDr);
+  RowGemmArgs a{};
+  a.x = x;
+  a.w = static_cast<const __nv_bfloat16*>(w_kva);
+  a.B = dims->batch;
+  a.K = hidden;
+  a.N = kRow;
+  a.cache = cache;
+  a.positions = positions;
+  a.s_max = dims->s_max;
+  a.d_c = kDc;
+  a.status = dev_status;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dims->dtype == MLA_BF16) {
+    rowgemm_kernel<__nv_bfloat16, kAppendRow><<<kRow / 8, 256, 0, s>>>(a, th);
+  } else {
+    const int warps = a.B * kRow / 2;
+    rowgemm_f32_kernel<kAppendRow><<<(warps + 7) / 8, 256, 0, s>>>(a, th,
+                                                                   static_cast<const float*>(w_kva));
+  }
+  return launch_status(who);
+}
+
+extern "C" mla_status mla_wo_proj(const mla_dims* dims, int32_t hidden, const float* o,
+                                  const void* w_o, float* y, void* stream) {
+  const char* who = "mla_wo_proj";
+  mla_status st = check_dims(dims, who);
+  if (st != MLA_OK) return st;
+  if (!o || !w_o || !y) {
+    set_error("%s: a required pointer is NULL", who);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (!aligned16(o) || !aligned16(w_o) || !aligned16(y)) {
+    set_error("%s: o, w_o and y must be 16-byte aligned", who);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (hidden <= 0 || hidden % 8 != 0) {
+    set_error("%s: hidden = %d must be a positive multiple of 8", who, hidden);
+    return hidden <= 0 ? MLA_ERR_INVALID_ARG : MLA_ERR_UNSUPPORTED;
+  }
+  RowGemmArgs a{};
+  a.x = o;
+  a.w = static_cast<const __nv_bfloat16*>(w_o);
+  a.B = dims->batch;
+  a.K = dims->heads * kDv;
+  a.N = hidden;
+  a.y = y;
+  RopeTheta th{};
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dims->dtype == MLA_BF16) {
+    if (a.K % 128 != 0) {
+      set_error("%s: heads * d_v = %d must be a multiple of 128", who, a.K);
+      return MLA_ERR_UNSUPPORTED;
+    }
+    rowgemm_kernel<float, kWriteY><<<hidden / 8, 256, 0, s>>>(a, th);
+  } else {
+    const int warps = a.B * hidden / 2;
+    rowgemm_f32_kernel<kWriteY><<<(warps + 7) / 8, 256, 0, s>>>(a, th, static_cast<const float*>(w_o));
   }
   return launch_status(who);
 }

@@ -222,6 +222,44 @@ mla_status mla_out_proj(const mla_dims* dims, const float* o_c, const void* w_uv
                         void* stream);
 
 /*
+ * mla_cache_append -- write each sequence's new token into the latent cache.
+ *
+ *   y[b, :]        = x[b, :] . w_kva^T             (d_c + d_rope outputs)
+ *   cache[b, positions[b], 0:d_c]          = y[b, 0:d_c]
+ *   cache[b, positions[b], d_c:d_c+d_rope] = RoPE(y[b, d_c:], positions[b])
+ * ("Deepseek V2 Lite Inference Engine in C", MLA notes: kv_a_proj fuses the KV
+ *  down-projection and the shared RoPE key; "Multi-Head Latent Attention" 3.5:
+ *  the latent row is what the cache keeps, and 3.7: the key is rotated at its
+ *  position -- adjacent pairs, angle in fp64 -- before it is cached, which is
+ *  the form mla_decode_attn reads.)  The new row is then attended with
+ *  lengths[b] = positions[b] + 1.  fp32 accumulation; the row is rounded once
+ *  to the cache dtype.  No normalisation is applied (none is defined on the
+ *  pages for this step).
+ *
+ * x      [B, hidden] dtype           w_kva [d_c + d_rope, hidden] dtype
+ * positions [B] int32 (device); a position outside [0, s_max) writes nothing
+ *        and sets MLA_DEV_LENGTH_OUT_OF_RANGE in dev_status (may be NULL)
+ * cache  [B, s_max, d_c + d_rope] dtype (in/out: only the new rows change)
+ * hidden must be a multiple of 128.
+ */
+mla_status mla_cache_append(const mla_dims* dims, int32_t hidden, const void* x,
+                            const void* w_kva, const int32_t* positions, double rope_base,
+                            void* cache, int32_t* dev_status, void* stream);
+
+/*
+ * mla_wo_proj -- the attention layer's output projection.
+ *
+ *   y[b, n] = sum_{h, e} w_o[n, h d_v + e] * o[b, h, e]
+ * ("Multi-Head Latent Attention" eq. 3.3.3: W^O applied to the concatenated
+ *  head outputs; o is mla_out_proj's result.)  fp32 accumulation.
+ *
+ * o [B, H, d_v] fp32     w_o [hidden, H d_v] dtype     y [B, hidden] fp32 (out)
+ * hidden must be a multiple of 8 (and H d_v a multiple of 128 for MLA_BF16).
+ */
+mla_status mla_wo_proj(const mla_dims* dims, int32_t hidden, const float* o, const void* w_o,
+                       float* y, void* stream);
+
+/*
  * mla_decode_step -- one whole decode step: mla_absorb_q, mla_decode_attn and
  * mla_out_proj in one call, with the same arguments, meanings and results
  * (q_abs, q_pe, o_c, lse and out are all written).
