@@ -52,6 +52,9 @@ def parse(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="step", choices=["step", "cache_append", "wo_proj"],
+                    help="step: the decode step (default); cache_append / wo_proj: the steps "
+                         "around it, timed alone on the workload's sizes")
     return ap.parse_args(argv)
 
 
@@ -262,6 +265,75 @@ def whole_job_rate(units_per_rank_step: float, steps: int, world: int, seconds: 
     return units_per_rank_step * steps * world / seconds
 
 
+# ----------------------------------------------------------------------------- around the step
+def run_op(args, cfg, rank):
+    """Time mla_cache_append or mla_wo_proj alone on the workload's sizes: K launches
+    in one CUDA graph over L rotating weight copies (more than 3x L2), CUDA events
+    around the replay.  The dominant bytes are the weight's; the line reports them
+    per second against the measured HBM peak."""
+    import torch
+    import head_latent_attention_absorbed_gb300 as mla
+    from workloads import make_append_inputs, make_wo_inputs
+    mla.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    d = mla.dims(cfg.batch, cfg.heads, cfg.s_max, mla.dtype_code(dt))
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 126 * 2 ** 20
+    if args.op == "cache_append":
+        inp = make_append_inputs(cfg, seed=0)
+        wbytes = inp.w_kva.numel() * inp.w_kva.element_size()
+        L = max(2, math.ceil(3 * l2 / wbytes))
+        ws = [inp.w_kva.to(dev) for _ in range(L)]
+        x, pos = inp.x.to(dev), inp.positions.to(dev)
+        cache = torch.zeros((cfg.batch, cfg.s_max, cfg.row), dtype=dt, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        moved = wbytes + x.numel() * x.element_size() + cfg.batch * cfg.row * cache.element_size()
+        launch = lambda k: mla.cache_append(d, x, ws[k % L], pos, cache, cfg.rope_base, status)
+        metric = "cache append: kv_a_proj weight + token + row bytes per second"
+    else:
+        inp = make_wo_inputs(cfg, seed=0)
+        wbytes = inp.w_o.numel() * inp.w_o.element_size()
+        L = max(2, math.ceil(3 * l2 / wbytes))
+        ws = [inp.w_o.to(dev) for _ in range(L)]
+        o = inp.o.to(dev)
+        y = torch.empty((cfg.batch, cfg.hidden), dtype=torch.float32, device=dev)
+        moved = wbytes + o.numel() * 4 + y.numel() * 4
+        launch = lambda k: mla.wo_proj(d, o, ws[k % L], y)
+        metric = "W^O projection: weight + input + output bytes per second"
+    K, W = args.steps, args.warmup
+    for k in range(W):
+        launch(k)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(device=dev)
+    with torch.cuda.graph(g, stream=cap, capture_error_mode="thread_local"):
+        for k in range(K):
+            launch(k)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1e3 / K
+    gbs = moved / (us * 1e-6) / 1e9
+    peak, peak_kind = measured_peaks()
+    line = {"op": args.op, "metric": metric, "value": gbs, "unit": "GB/s", "n_gpus": 1,
+            "steps": K, "warmup": W, "us_per_launch": us, "higher_is_better": True,
+            "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
+            "config": {"workload": cfg.name, "batch": cfg.batch, "heads": cfg.heads,
+                       "hidden": cfg.hidden,
+                       "l2": f"{L} rotating weight copies, more than 3x L2"},
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                         "frac": gbs / peak, "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
+                         "bytes_per_launch": moved}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- our arm
 def main():
     return main_with(parse(), int(os.environ.get("RANK", "0")),
@@ -274,6 +346,8 @@ def main_with(args, rank: int, world: int, local: int = 0):
 
     if args.impl == "reference":
         return run_reference(args, cfg, rank, world)
+    if args.op != "step":
+        return run_op(args, cfg, rank)
 
     import torch
     import torch.distributed as dist

@@ -237,8 +237,8 @@ __global__ void __launch_bounds__(128)
 // grid (N / 8), 256 threads: warp w contracts K range [w K/8, (w+1) K/8) for
 // output columns [8 blockIdx.x, +8); the batch rows are the M side of
 // mma.sync m16n8k16 in tiles of 16, 64 rows per pass.  The weight's B
-// fragments come straight from global memory, eight K steps at a time; an fp32
-// x enters as bf16 hi + lo parts.  The eight warps' sums meet in shared memory
+// fragments come straight from global memory into registers; an fp32 x enters
+// as bf16 hi + lo parts.  The eight warps' sums meet in shared memory
 // and each thread finishes two adjacent columns, so that a RoPE pair stays in
 // one thread.
 enum RowGemmMode { kWriteY = 0, kAppendRow = 1 };
@@ -254,14 +254,25 @@ struct RowGemmArgs {
   int32_t* status;
 };
 
+// K is taken in blocks of 32 with a fixed permutation inside each block, the
+// same for both operands (the sum does not depend on the order): thread
+// (gq, cq) of an MMA pair supplies elements 8 cq .. 8 cq + 7 of the block --
+// (0,1) and (2,3) as the K pairs of the first MMA, (4,5) and (6,7) of the
+// second -- so its weight fragments are one 16-byte load and its inputs two
+// (fp32: four) contiguous loads.  Two 256-wide K chunks of weights are in
+// flight per thread.
 template <typename XT, int kMode>
 __global__ void __launch_bounds__(256) rowgemm_kernel(const RowGemmArgs a, const RopeTheta th) {
   __shared__ float red[8][64][9];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, cq = lane & 3;
   const int n0 = 8 * blockIdx.x;
-  const int kw = warp * (a.K / 8), kn = a.K / 8;
-  const __nv_bfloat16* wrow = a.w + size_t(n0 + gq) * a.K + kw + 2 * cq;
+  const int kw = warp * (a.K / 8), kn = a.K / 8;   // a multiple of 16; blocks of 32 below
+  const uint4* wrow = reinterpret_cast<const uint4*>(a.w + size_t(n0 + gq) * a.K + kw + 8 * cq);
+  const int nblk = (kn + 31) / 32;                 // 32-wide K blocks of this warp
+  // a last block of 16 (K/8 an odd multiple of 16) holds data for cq < 2 only;
+  // the other threads supply zero weights and zero inputs there
+  const int nblk_t = (kn % 32 != 0 && cq >= 2) ? nblk - 1 : nblk;
   for (int b0 = 0; b0 < a.B; b0 += 64) {
     float acc[4][4];
 #pragma unroll
@@ -269,44 +280,66 @@ __global__ void __launch_bounds__(256) rowgemm_kernel(const RowGemmArgs a, const
 #pragma unroll
       for (int r = 0; r < 4; ++r) acc[mt][r] = 0.f;
     const int ntile = min(4, (a.B - b0 + 15) / 16);
-    for (int k0 = 0; k0 < kn; k0 += 128) {
-      uint32_t bf[8][2];
+    constexpr int kC = 8;                          // blocks per chunk (256 of K)
+    uint4 wcur[kC], wnext[kC];
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const bool ok = k0 + 16 * ks < kn;
-        bf[ks][0] = ok ? *reinterpret_cast<const uint32_t*>(wrow + k0 + 16 * ks) : 0u;
-        bf[ks][1] = ok ? *reinterpret_cast<const uint32_t*>(wrow + k0 + 16 * ks + 8) : 0u;
-      }
+    for (int i = 0; i < kC; ++i) wcur[i] = i < nblk_t ? wrow[4 * i] : make_uint4(0, 0, 0, 0);
+    for (int c0 = 0; c0 < nblk; c0 += kC) {
+#pragma unroll
+      for (int i = 0; i < kC; ++i)
+        wnext[i] = c0 + kC + i < nblk_t ? wrow[4 * (c0 + kC + i)] : make_uint4(0, 0, 0, 0);
       for (int mt = 0; mt < ntile; ++mt) {
         const int bA = b0 + 16 * mt + gq, bB = bA + 8;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          if (k0 + 16 * ks >= kn) break;
-          const int kk = kw + k0 + 16 * ks + 2 * cq;
-          uint32_t hi[4], lo[4];
+        for (int i = 0; i < kC; ++i) {
+          const int blk = c0 + i;
+          if (blk >= nblk) break;
+          const bool mine = blk < nblk_t;
+          const int kk = kw + 32 * blk + 8 * cq;
+          uint32_t x0[4], x1[4], x0l[4], x1l[4];   // rows bA, bB: elements 0..7 of this thread
           if constexpr (sizeof(XT) == 4) {
             const float* x = static_cast<const float*>(a.x);
-            const float2 z = make_float2(0.f, 0.f);
-            const float2 v0 = bA < a.B ? *reinterpret_cast<const float2*>(x + size_t(bA) * a.K + kk) : z;
-            const float2 v1 = bB < a.B ? *reinterpret_cast<const float2*>(x + size_t(bB) * a.K + kk) : z;
-            const float2 v2 = bA < a.B ? *reinterpret_cast<const float2*>(x + size_t(bA) * a.K + kk + 8) : z;
-            const float2 v3 = bB < a.B ? *reinterpret_cast<const float2*>(x + size_t(bB) * a.K + kk + 8) : z;
-            split_bf16(v0.x, v0.y, hi[0], lo[0]);
-            split_bf16(v1.x, v1.y, hi[1], lo[1]);
-            split_bf16(v2.x, v2.y, hi[2], lo[2]);
-            split_bf16(v3.x, v3.y, hi[3], lo[3]);
-            mma_bf16(acc[mt], hi, bf[ks][0], bf[ks][1]);
-            mma_bf16(acc[mt], lo, bf[ks][0], bf[ks][1]);
+            float4 va0 = make_float4(0.f, 0.f, 0.f, 0.f), va1 = va0, vb0 = va0, vb1 = va0;
+            if (mine && bA < a.B) {
+              va0 = *reinterpret_cast<const float4*>(x + size_t(bA) * a.K + kk);
+              va1 = *reinterpret_cast<const float4*>(x + size_t(bA) * a.K + kk + 4);
+            }
+            if (mine && bB < a.B) {
+              vb0 = *reinterpret_cast<const float4*>(x + size_t(bB) * a.K + kk);
+              vb1 = *reinterpret_cast<const float4*>(x + size_t(bB) * a.K + kk + 4);
+            }
+            split_bf16(va0.x, va0.y, x0[0], x0l[0]);
+            split_bf16(va0.z, va0.w, x0[1], x0l[1]);
+            split_bf16(va1.x, va1.y, x0[2], x0l[2]);
+            split_bf16(va1.z, va1.w, x0[3], x0l[3]);
+            split_bf16(vb0.x, vb0.y, x1[0], x1l[0]);
+            split_bf16(vb0.z, vb0.w, x1[1], x1l[1]);
+            split_bf16(vb1.x, vb1.y, x1[2], x1l[2]);
+            split_bf16(vb1.z, vb1.w, x1[3], x1l[3]);
           } else {
             const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
-            hi[0] = bA < a.B ? *reinterpret_cast<const uint32_t*>(x + size_t(bA) * a.K + kk) : 0u;
-            hi[1] = bB < a.B ? *reinterpret_cast<const uint32_t*>(x + size_t(bB) * a.K + kk) : 0u;
-            hi[2] = bA < a.B ? *reinterpret_cast<const uint32_t*>(x + size_t(bA) * a.K + kk + 8) : 0u;
-            hi[3] = bB < a.B ? *reinterpret_cast<const uint32_t*>(x + size_t(bB) * a.K + kk + 8) : 0u;
-            mma_bf16(acc[mt], hi, bf[ks][0], bf[ks][1]);
+            uint4 ua = make_uint4(0, 0, 0, 0), ub = ua;
+            if (mine && bA < a.B) ua = *reinterpret_cast<const uint4*>(x + size_t(bA) * a.K + kk);
+            if (mine && bB < a.B) ub = *reinterpret_cast<const uint4*>(x + size_t(bB) * a.K + kk);
+            x0[0] = ua.x; x0[1] = ua.y; x0[2] = ua.z; x0[3] = ua.w;
+            x1[0] = ub.x; x1[1] = ub.y; x1[2] = ub.z; x1[3] = ub.w;
+          }
+          const uint4 wv = wcur[i];
+          // first MMA: K pairs (0,1) and (2,3); second: (4,5) and (6,7)
+          const uint32_t a0[4] = {x0[0], x1[0], x0[1], x1[1]};
+          const uint32_t a1[4] = {x0[2], x1[2], x0[3], x1[3]};
+          mma_bf16(acc[mt], a0, wv.x, wv.y);
+          mma_bf16(acc[mt], a1, wv.z, wv.w);
+          if constexpr (sizeof(XT) == 4) {
+            const uint32_t l0[4] = {x0l[0], x1l[0], x0l[1], x1l[1]};
+            const uint32_t l1[4] = {x0l[2], x1l[2], x0l[3], x1l[3]};
+            mma_bf16(acc[mt], l0, wv.x, wv.y);
+            mma_bf16(acc[mt], l1, wv.z, wv.w);
           }
         }
       }
+#pragma unroll
+      for (int i = 0; i < kC; ++i) wcur[i] = wnext[i];
     }
 #pragma unroll
     for (int mt = 0; mt < 4; ++mt) {

@@ -32,8 +32,10 @@ def _dt(cfg):
     cfg_of(V2LITE_BF16_B8_S4096, s_max=64),
     cfg_of(V3_BF16_H128_B32_S16384, s_max=64),
     cfg_of(V2LITE_BF16_B8_S4096, batch=19, s_max=40),
+    cfg_of(V2LITE_BF16_B8_S4096, batch=5, s_max=24, hidden=1152),
+    cfg_of(V2LITE_BF16_B8_S4096, batch=70, s_max=8),
     cfg_of(V2LITE_F32_B1_S64),
-], ids=["v2lite_bf16", "v3_bf16", "v2lite_bf16_b19", "v2lite_f32"])
+], ids=["v2lite_bf16", "v3_bf16", "v2lite_bf16_b19", "hidden1152_b5", "b70", "v2lite_f32"])
 def test_cache_append_rows(cuda_lib, cfg):
     mla = cuda_lib
     inp = make_append_inputs(cfg, seed=31)
@@ -106,8 +108,9 @@ def test_append_then_decode(cuda_lib):
     cfg_of(V2LITE_BF16_B8_S4096),
     cfg_of(V3_BF16_H128_B32_S16384),
     cfg_of(V2LITE_BF16_B8_S4096, batch=19),
+    cfg_of(V2LITE_BF16_B8_S4096, batch=70, hidden=1160),
     cfg_of(V2LITE_F32_B1_S64),
-], ids=["v2lite_bf16", "v3_bf16", "v2lite_bf16_b19", "v2lite_f32"])
+], ids=["v2lite_bf16", "v3_bf16", "v2lite_bf16_b19", "b70_hidden1160", "v2lite_f32"])
 def test_wo_proj(cuda_lib, cfg):
     mla = cuda_lib
     inp = make_wo_inputs(cfg, seed=35)
