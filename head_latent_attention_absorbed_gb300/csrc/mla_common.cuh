@@ -177,6 +177,16 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t& hi, uin
   lo = pack_bf16(x0 - hf.x, x1 - hf.y);
 }
 
+// RoPE angle pos * theta_i reduced to [-pi, pi] for sincosf.  `turns` is
+// theta_i / (2 pi) in fp64, computed on the host, so the reduction is one fp64
+// product and a rounding (no fp64 division), and positions up to 2^31 keep
+// their fractional turns.
+__device__ __forceinline__ float rope_angle(int pos, double turns) {
+  double t = static_cast<double>(pos) * turns;
+  t -= rint(t);
+  return static_cast<float>(t * 6.283185307179586);
+}
+
 // Byte offset of element (row, col) inside a [rows x 64] bf16 box stored with
 // the 128-byte swizzle: 16-byte chunk index XOR (row mod 8).
 __device__ __forceinline__ uint32_t sw128(int row, int chunk) {

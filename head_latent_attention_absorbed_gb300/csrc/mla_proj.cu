@@ -16,17 +16,18 @@
 #include <math.h>
 
 #include "mla_common.cuh"
+#include "mla_wstream.cuh"
 
 namespace mla {
 namespace {
 
 // ---------------------------------------------------------------------- RoPE
-// theta_i = base^(-2i/d_rope) comes from the host in fp64.  The angle
-// pos * theta_i is formed and reduced modulo 2*pi in fp64, so that positions up
-// to 2^31 keep their fractional turns; the reduced angle (|r| <= pi) then goes
-// through single-precision sincosf.
+// theta_i = base^(-2i/d_rope) comes from the host in fp64 as turns,
+// theta_i / (2 pi).  The angle pos * theta_i is reduced modulo 2 pi in fp64
+// (rope_angle), so that positions up to 2^31 keep their fractional turns; the
+// reduced angle (|r| <= pi) then goes through single-precision sincosf.
 struct RopeTheta {
-  double theta[kDr / 2];
+  double turns[kDr / 2];
 };
 
 template <typename T>
@@ -40,11 +41,8 @@ template <typename T>
 __device__ __forceinline__ void rope_pair(const T* q_rope, const int32_t* positions,
                                           const RopeTheta& th, float* q_pe, int H, int h, int it) {
   const int b = it / (kDr / 2), i = it % (kDr / 2);
-  const double two_pi = 6.283185307179586;
-  const double ang = static_cast<double>(positions[b]) * th.theta[i];
-  const double r = ang - two_pi * rint(ang / two_pi);
   float sn, cs;
-  sincosf(static_cast<float>(r), &sn, &cs);
+  sincosf(rope_angle(positions[b], th.turns[i]), &sn, &cs);
   const size_t off = (size_t(b) * H + h) * kDr + 2 * i;
   const float x0 = to_f(q_rope[off]), x1 = to_f(q_rope[off + 1]);
   q_pe[off] = cs * x0 - sn * x1;
@@ -229,18 +227,12 @@ __global__ void __launch_bounds__(128)
   }
 }
 
-// ---------------------------------------------------------------------- row-major skinny GEMM
-// y[b, n] = sum_k x[b, k] * w[n, k] for a bf16 weight stored [N, K] (K contiguous),
-// the shape of both steps around the attention: the cache append's fused
-// down-projection kv_a_proj ("Deepseek V2 Lite Inference Engine in C", MLA
-// notes) and the output projection W^O ("Multi-Head Latent Attention" eq. 3.3.3).
-// grid (N / 8), 256 threads: warp w contracts K range [w K/8, (w+1) K/8) for
-// output columns [8 blockIdx.x, +8); the batch rows are the M side of
-// mma.sync m16n8k16 in tiles of 16, 64 rows per pass.  The weight's B
-// fragments come straight from global memory into registers; an fp32 x enters
-// as bf16 hi + lo parts.  The eight warps' sums meet in shared memory
-// and each thread finishes two adjacent columns, so that a RoPE pair stays in
-// one thread.
+// ---------------------------------------------------------------------- fp32 row projections
+// y[b, n] = sum_k x[b, k] * w[n, k] with w stored [N, K] (K contiguous): the
+// cache append's fused down-projection kv_a_proj ("Deepseek V2 Lite Inference
+// Engine in C", MLA notes) and the output projection W^O ("Multi-Head Latent
+// Attention" eq. 3.3.3), for fp32 weights.  (bf16 weights go through the
+// tensor-core weight stream of mla_wstream.cu.)
 enum RowGemmMode { kWriteY = 0, kAppendRow = 1 };
 
 struct RowGemmArgs {
@@ -253,141 +245,6 @@ struct RowGemmArgs {
   int s_max, d_c;              // kAppendRow: columns >= d_c are rotated
   int32_t* status;
 };
-
-// K is taken in blocks of 32 with a fixed permutation inside each block, the
-// same for both operands (the sum does not depend on the order): thread
-// (gq, cq) of an MMA pair supplies elements 8 cq .. 8 cq + 7 of the block --
-// (0,1) and (2,3) as the K pairs of the first MMA, (4,5) and (6,7) of the
-// second -- so its weight fragments are one 16-byte load and its inputs two
-// (fp32: four) contiguous loads.  Two 256-wide K chunks of weights are in
-// flight per thread.
-template <typename XT, int kMode>
-__global__ void __launch_bounds__(256) rowgemm_kernel(const RowGemmArgs a, const RopeTheta th) {
-  __shared__ float red[8][64][9];
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int gq = lane >> 2, cq = lane & 3;
-  const int n0 = 8 * blockIdx.x;
-  const int kw = warp * (a.K / 8), kn = a.K / 8;   // a multiple of 16; blocks of 32 below
-  const uint4* wrow = reinterpret_cast<const uint4*>(a.w + size_t(n0 + gq) * a.K + kw + 8 * cq);
-  const int nblk = (kn + 31) / 32;                 // 32-wide K blocks of this warp
-  // a last block of 16 (K/8 an odd multiple of 16) holds data for cq < 2 only;
-  // the other threads supply zero weights and zero inputs there
-  const int nblk_t = (kn % 32 != 0 && cq >= 2) ? nblk - 1 : nblk;
-  for (int b0 = 0; b0 < a.B; b0 += 64) {
-    float acc[4][4];
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) acc[mt][r] = 0.f;
-    const int ntile = min(4, (a.B - b0 + 15) / 16);
-    constexpr int kC = 8;                          // blocks per chunk (256 of K)
-    uint4 wcur[kC], wnext[kC];
-#pragma unroll
-    for (int i = 0; i < kC; ++i) wcur[i] = i < nblk_t ? wrow[4 * i] : make_uint4(0, 0, 0, 0);
-    for (int c0 = 0; c0 < nblk; c0 += kC) {
-#pragma unroll
-      for (int i = 0; i < kC; ++i)
-        wnext[i] = c0 + kC + i < nblk_t ? wrow[4 * (c0 + kC + i)] : make_uint4(0, 0, 0, 0);
-      for (int mt = 0; mt < ntile; ++mt) {
-        const int bA = b0 + 16 * mt + gq, bB = bA + 8;
-#pragma unroll
-        for (int i = 0; i < kC; ++i) {
-          const int blk = c0 + i;
-          if (blk >= nblk) break;
-          const bool mine = blk < nblk_t;
-          const int kk = kw + 32 * blk + 8 * cq;
-          uint32_t x0[4], x1[4], x0l[4], x1l[4];   // rows bA, bB: elements 0..7 of this thread
-          if constexpr (sizeof(XT) == 4) {
-            const float* x = static_cast<const float*>(a.x);
-            float4 va0 = make_float4(0.f, 0.f, 0.f, 0.f), va1 = va0, vb0 = va0, vb1 = va0;
-            if (mine && bA < a.B) {
-              va0 = *reinterpret_cast<const float4*>(x + size_t(bA) * a.K + kk);
-              va1 = *reinterpret_cast<const float4*>(x + size_t(bA) * a.K + kk + 4);
-            }
-            if (mine && bB < a.B) {
-              vb0 = *reinterpret_cast<const float4*>(x + size_t(bB) * a.K + kk);
-              vb1 = *reinterpret_cast<const float4*>(x + size_t(bB) * a.K + kk + 4);
-            }
-            split_bf16(va0.x, va0.y, x0[0], x0l[0]);
-            split_bf16(va0.z, va0.w, x0[1], x0l[1]);
-            split_bf16(va1.x, va1.y, x0[2], x0l[2]);
-            split_bf16(va1.z, va1.w, x0[3], x0l[3]);
-            split_bf16(vb0.x, vb0.y, x1[0], x1l[0]);
-            split_bf16(vb0.z, vb0.w, x1[1], x1l[1]);
-            split_bf16(vb1.x, vb1.y, x1[2], x1l[2]);
-            split_bf16(vb1.z, vb1.w, x1[3], x1l[3]);
-          } else {
-            const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
-            uint4 ua = make_uint4(0, 0, 0, 0), ub = ua;
-            if (mine && bA < a.B) ua = *reinterpret_cast<const uint4*>(x + size_t(bA) * a.K + kk);
-            if (mine && bB < a.B) ub = *reinterpret_cast<const uint4*>(x + size_t(bB) * a.K + kk);
-            x0[0] = ua.x; x0[1] = ua.y; x0[2] = ua.z; x0[3] = ua.w;
-            x1[0] = ub.x; x1[1] = ub.y; x1[2] = ub.z; x1[3] = ub.w;
-          }
-          const uint4 wv = wcur[i];
-          // first MMA: K pairs (0,1) and (2,3); second: (4,5) and (6,7)
-          const uint32_t a0[4] = {x0[0], x1[0], x0[1], x1[1]};
-          const uint32_t a1[4] = {x0[2], x1[2], x0[3], x1[3]};
-          mma_bf16(acc[mt], a0, wv.x, wv.y);
-          mma_bf16(acc[mt], a1, wv.z, wv.w);
-          if constexpr (sizeof(XT) == 4) {
-            const uint32_t l0[4] = {x0l[0], x1l[0], x0l[1], x1l[1]};
-            const uint32_t l1[4] = {x0l[2], x1l[2], x0l[3], x1l[3]};
-            mma_bf16(acc[mt], l0, wv.x, wv.y);
-            mma_bf16(acc[mt], l1, wv.z, wv.w);
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kC; ++i) wcur[i] = wnext[i];
-    }
-#pragma unroll
-    for (int mt = 0; mt < 4; ++mt) {
-      red[warp][16 * mt + gq][2 * cq] = acc[mt][0];
-      red[warp][16 * mt + gq][2 * cq + 1] = acc[mt][1];
-      red[warp][16 * mt + gq + 8][2 * cq] = acc[mt][2];
-      red[warp][16 * mt + gq + 8][2 * cq + 1] = acc[mt][3];
-    }
-    __syncthreads();
-    {
-      const int r = tid >> 2, c = 2 * (tid & 3);   // 64 rows x 4 column pairs
-      const int b = b0 + r, n = n0 + c;
-      float v0 = 0.f, v1 = 0.f;
-#pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        v0 += red[w][r][c];
-        v1 += red[w][r][c + 1];
-      }
-      if (b < a.B) {
-        if constexpr (kMode == kWriteY) {
-          *reinterpret_cast<float2*>(a.y + size_t(b) * a.N + n) = make_float2(v0, v1);
-        } else {
-          const int pos = a.positions[b];
-          if (pos < 0 || pos >= a.s_max) {
-            if (c == 0 && blockIdx.x == 0) report(a.status, MLA_DEV_LENGTH_OUT_OF_RANGE);
-          } else {
-            if (n >= a.d_c) {
-              // RoPE on the key part: the pair (n, n + 1) as one complex number,
-              // rotated by pos * theta_i; the angle in fp64, reduced mod 2 pi.
-              const double two_pi = 6.283185307179586;
-              const double ang = static_cast<double>(pos) * th.theta[(n - a.d_c) / 2];
-              const double rr = ang - two_pi * rint(ang / two_pi);
-              float sn, cs;
-              sincosf(static_cast<float>(rr), &sn, &cs);
-              const float x0 = v0, x1 = v1;
-              v0 = cs * x0 - sn * x1;
-              v1 = sn * x0 + cs * x1;
-            }
-            *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(a.cache) +
-                                               (size_t(b) * a.s_max + pos) * a.N + n) =
-                __floats2bfloat162_rn(v0, v1);
-          }
-        }
-      }
-    }
-    __syncthreads();
-  }
-}
 
 // fp32 weights and inputs: one warp per output (b, n), fp32 arithmetic throughout.
 template <int kMode>
@@ -420,11 +277,8 @@ __global__ void __launch_bounds__(256) rowgemm_f32_kernel(const RowGemmArgs a, c
       return;
     }
     if (n >= a.d_c) {
-      const double two_pi = 6.283185307179586;
-      const double ang = static_cast<double>(pos) * th.theta[(n - a.d_c) / 2];
-      const double rr = ang - two_pi * rint(ang / two_pi);
       float sn, cs;
-      sincosf(static_cast<float>(rr), &sn, &cs);
+      sincosf(rope_angle(pos, th.turns[(n - a.d_c) / 2]), &sn, &cs);
       const float x0 = v0, x1 = v1;
       v0 = cs * x0 - sn * x1;
       v1 = sn * x0 + cs * x1;
@@ -462,7 +316,7 @@ extern "C" mla_status mla_absorb_q(const mla_dims* dims, const void* q_nope, con
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int B = dims->batch, H = dims->heads;
   RopeTheta th;
-  for (int i = 0; i < kDr / 2; ++i) th.theta[i] = pow(rope_base, -2.0 * i / kDr);
+  for (int i = 0; i < kDr / 2; ++i) th.turns[i] = pow(rope_base, -2.0 * i / kDr) / (2.0 * M_PI);
   if (dims->dtype == MLA_BF16) {
     absorb_bf16_kernel<<<dim3(H, kDc / 16), 32, 0, s>>>(
         static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(q_rope),
@@ -526,7 +380,7 @@ extern "C" mla_status mla_cache_append(const mla_dims* dims, int32_t hidden, con
     return MLA_ERR_INVALID_ARG;
   }
   RopeTheta th;
-  for (int i = 0; i < kDr / 2; ++i) th.theta[i] = pow(rope_base, -2.0 * i / kDr);
+  for (int i = 0; i < kDr / 2; ++i) th.turns[i] = pow(rope_base, -2.0 * i / kDr) / (2.0 * M_PI);
   RowGemmArgs a{};
   a.x = x;
   a.w = static_cast<const __nv_bfloat16*>(w_kva);
@@ -540,7 +394,21 @@ extern "C" mla_status mla_cache_append(const mla_dims* dims, int32_t hidden, con
   a.status = dev_status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dims->dtype == MLA_BF16) {
-    rowgemm_kernel<__nv_bfloat16, kAppendRow><<<kRow / 8, 256, 0, s>>>(a, th);
+    WStreamJob j{};
+    j.mode = kWsAppendRow;
+    j.x_f32 = false;
+    j.x = x;
+    j.w = w_kva;
+    j.B = dims->batch;
+    j.K = hidden;
+    j.N = kRow;
+    j.cache = cache;
+    j.positions = positions;
+    j.s_max = dims->s_max;
+    j.d_c = kDc;
+    for (int i = 0; i < kDr / 2; ++i) j.turns[i] = th.turns[i];
+    j.status = dev_status;
+    return wstream_launch(j, s, who);
   } else {
     const int warps = a.B * kRow / 2;
     rowgemm_f32_kernel<kAppendRow><<<(warps + 7) / 8, 256, 0, s>>>(a, th,
@@ -580,7 +448,16 @@ extern "C" mla_status mla_wo_proj(const mla_dims* dims, int32_t hidden, const fl
       set_error("%s: heads * d_v = %d must be a multiple of 128", who, a.K);
       return MLA_ERR_UNSUPPORTED;
     }
-    rowgemm_kernel<float, kWriteY><<<hidden / 8, 256, 0, s>>>(a, th);
+    WStreamJob j{};
+    j.mode = kWsWriteY;
+    j.x_f32 = true;
+    j.x = o;
+    j.w = w_o;
+    j.B = dims->batch;
+    j.K = a.K;
+    j.N = hidden;
+    j.y = y;
+    return wstream_launch(j, s, who);
   } else {
     const int warps = a.B * hidden / 2;
     rowgemm_f32_kernel<kWriteY><<<(warps + 7) / 8, 256, 0, s>>>(a, th, static_cast<const float*>(w_o));
