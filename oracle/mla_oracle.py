@@ -227,3 +227,51 @@ def output_projection(o: np.ndarray, w_o: np.ndarray) -> np.ndarray:
     """
     o = np.asarray(o, dtype=np.float64)
     return o.reshape(o.shape[0], -1) @ np.asarray(w_o, dtype=np.float64).T
+
+
+# ----------------------------------------------------------------------------- FP8 cache elements
+def e4m3_to_float64(codes) -> np.ndarray:
+    """Values of FP8 E4M3 codes ("Multi-Head Latent Attention" 3.1: a cached element
+    takes one to four bytes, FP8 to FP32).
+
+    The E4M3 format used for caches (finite-only): bit 7 the sign, bits 6-3 the
+    exponent with bias 7, bits 2-0 the mantissa.  Exponent field 0 holds the
+    subnormals (m / 8) 2^-6; otherwise the value is (1 + m / 8) 2^(e - 7).  The one
+    pattern with all exponent and mantissa bits set is NaN (there are no
+    infinities), so the largest magnitude is 1.75 * 2^8 = 448.
+    """
+    c = np.asarray(codes).astype(np.int64) & 0xFF
+    sign = np.where((c & 0x80) != 0, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = (c & 7).astype(np.float64)
+    mag = np.where(e == 0, (m / 8.0) * 2.0 ** -6, (1.0 + m / 8.0) * np.exp2(e - 7.0))
+    return np.where((e == 15) & (m == 7), np.nan, sign * mag)
+
+
+def e4m3_round(x) -> np.ndarray:
+    """E4M3 code of the value nearest to x (uint8), ties to the code whose last
+    mantissa bit is 0, magnitudes past 448 saturated to 448, NaN to NaN: the
+    rounding of a value into an FP8 cache.  Written as the definition: the
+    nearest of the 254 finite E4M3 values, by exhaustive comparison.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    codes = np.array([c for c in range(256) if not np.isnan(e4m3_to_float64(c))], dtype=np.int64)
+    vals = e4m3_to_float64(codes)
+    flat = x.reshape(-1)
+    out = np.empty(flat.shape, dtype=np.uint8)
+    for i, v in enumerate(flat):
+        if np.isnan(v):
+            out[i] = 0x7F
+            continue
+        v = min(max(v, -448.0), 448.0)
+        d = np.abs(vals - v)
+        near = codes[d == d.min()]
+        if len(near) > 1:
+            even = near[(near & 1) == 0]
+            near = even if len(even) else near
+        # zero keeps the sign of x
+        if vals[np.searchsorted(codes, near[0])] == 0.0:
+            out[i] = 0x80 if np.signbit(v) else 0x00
+        else:
+            out[i] = near[0]
+    return out.reshape(x.shape)

@@ -6,7 +6,8 @@ import numpy as np
 import torch
 
 from oracle import mla_oracle as O
-from workloads import (TOL_BF16_MAX_ABS, TOL_BF16_REL_L2, TOL_F32_MAX_ABS, MlaInputs)
+from workloads import (TOL_BF16_MAX_ABS, TOL_BF16_REL_L2, TOL_F32_MAX_ABS, MlaInputs,
+                       cache_storage)
 
 
 def run_cuda(inp: MlaInputs, num_splits: int = 0, device: str = "cuda", path: str = "step"):
@@ -15,7 +16,7 @@ def run_cuda(inp: MlaInputs, num_splits: int = 0, device: str = "cuda", path: st
     mla_decode_attn, mla_out_proj.  Returns fp64 numpy arrays."""
     import head_latent_attention_absorbed_gb300 as mla
     cfg = inp.cfg
-    dt = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
+    dt = cache_storage(cfg)   # the cache's type names the library dtype
     step = mla.DecodeStep(cfg.batch, cfg.heads, cfg.s_max, dt, device=device,
                           num_splits_requested=num_splits, rope_base=cfg.rope_base,
                           softmax_scale=cfg.softmax_scale)
@@ -36,6 +37,8 @@ def run_oracle(inp: MlaInputs, batches=None):
     res = {k: [] for k in ("q_abs", "q_pe", "o_c", "lse", "o")}
     for b in batches:
         a = inp.as_float64_numpy(b)
+        if a["cache"] is None:   # FP8 cache: the oracle decodes the E4M3 codes
+            a["cache"] = O.e4m3_to_float64(a["cache_e4m3"])
         n = int(a["lengths"][0])
         a["cache"] = a["cache"][:, :n]
         r = O.decode_absorbed(a["q_nope"], a["q_rope"], a["w_uk"], a["w_uv"], a["cache"],

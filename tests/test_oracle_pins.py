@@ -353,3 +353,48 @@ def test_output_projection_brute_force_and_identity():
         for n in range(4):
             assert got[b, n] == pytest.approx(sum(w[n][k] * flat[k] for k in range(6)), abs=1e-12)
     np.testing.assert_allclose(O.output_projection(o, np.eye(6)), o.reshape(2, 6), atol=0)
+
+
+# ----------------------------------------------------------------------------- FP8 E4M3 elements
+def test_e4m3_decode_matches_library_and_format_landmarks():
+    """Every one of the 256 codes decodes as torch's float8_e4m3fn does (a library
+    routine); the format's landmark values hold (1.0, the largest 448, the
+    smallest normal 2^-6 and subnormal 2^-9, the NaN patterns, signed zero)."""
+    torch = pytest.importorskip("torch")
+    codes = np.arange(256)
+    mine = O.e4m3_to_float64(codes)
+    lib = torch.tensor(codes, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(mine), np.isnan(lib))
+    assert np.array_equal(mine[~np.isnan(mine)], lib[~np.isnan(lib)])
+    v = O.e4m3_to_float64
+    assert v(0x38) == 1.0 and v(0xB8) == -1.0
+    assert v(0x7E) == 448.0 and v(0xFE) == -448.0
+    assert v(0x08) == 2.0 ** -6 and v(0x01) == 2.0 ** -9 and v(0x07) == 7 * 2.0 ** -9
+    assert np.isnan(v(0x7F)) and np.isnan(v(0xFF))
+    assert v(0x00) == 0.0 and v(0x80) == 0.0 and np.signbit(v(0x80))
+    assert int(np.isnan(mine).sum()) == 2
+
+
+def test_e4m3_values_are_ordered_and_symmetric():
+    """Sign-magnitude order: codes 0..126 increase strictly, code c + 128 is -value(c)."""
+    pos = O.e4m3_to_float64(np.arange(127))
+    assert np.all(np.diff(pos) > 0)
+    neg = O.e4m3_to_float64(np.arange(128, 255))
+    np.testing.assert_array_equal(neg, -pos)
+
+
+def test_e4m3_round_is_nearest_even_and_saturating():
+    """Round trip of every finite code; nearest-value rounding agrees with torch's
+    float -> float8_e4m3fn conversion on values across the whole range; exact
+    midpoints go to the even code; magnitudes past 448 saturate."""
+    torch = pytest.importorskip("torch")
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)])
+    np.testing.assert_array_equal(O.e4m3_round(O.e4m3_to_float64(codes)), codes)
+    rng = np.random.default_rng(8)
+    x = rng.standard_normal(3000) * np.exp2(rng.uniform(-11, 8, 3000))
+    x = np.clip(x, -448.0, 448.0).astype(np.float32).astype(np.float64)
+    lib = torch.tensor(x, dtype=torch.float32).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(O.e4m3_round(x), lib)
+    # 1 + 1/16 lies halfway between 1 (0x38, even) and 1.125 (0x39)
+    assert O.e4m3_round(1.0625) == 0x38 and O.e4m3_round(1.1875) == 0x3A
+    assert O.e4m3_round(1e6) == 0x7E and O.e4m3_round(-1e6) == 0xFE

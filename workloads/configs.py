@@ -27,7 +27,8 @@ ROW = D_C + D_ROPE
 @dataclass(frozen=True)
 class MlaConfig:
     name: str
-    dtype: str                 # "f32" or "bf16": storage type of cache, queries, weights
+    dtype: str                 # "f32" or "bf16": storage type of cache, queries, weights;
+                               # "fp8": an FP8 E4M3 cache with bf16 queries and weights
     batch: int
     heads: int
     s_max: int                 # cache capacity in rows per sequence
@@ -51,7 +52,8 @@ class MlaConfig:
 
     @property
     def elt_bytes(self) -> int:
-        return 4 if self.dtype == "f32" else 2
+        """Bytes per cache element."""
+        return {"f32": 4, "bf16": 2, "fp8": 1}[self.dtype]
 
     @property
     def softmax_scale(self) -> float:
@@ -85,7 +87,21 @@ ALL_CONFIGS = (
     V3_BF16_H128_B32_S16384,
     V2LITE_BF16_B4_S65536_LONG,
 )
-BY_NAME = {c.name: c for c in ALL_CONFIGS}
+
+# The same shapes with an FP8 (E4M3) cache: one byte per cached element
+# (Multi-Head Latent Attention, section 3.1).  The cache values are the same
+# N(0, 1) draws rounded to E4M3 instead of bf16.
+V2LITE_FP8_B8_S4096 = V2LITE_BF16_B8_S4096.scaled(name="v2lite_fp8_b8_s4096", dtype="fp8")
+V2LITE_FP8_B64_RAGGED = V2LITE_BF16_B64_RAGGED.scaled(
+    name="v2lite_fp8_b64_ragged512_8192", dtype="fp8")
+V3_FP8_H128_B32_S16384 = V3_BF16_H128_B32_S16384.scaled(
+    name="v3heads_fp8_h128_b32_s16384", dtype="fp8")
+V2LITE_FP8_B4_S65536_LONG = V2LITE_BF16_B4_S65536_LONG.scaled(
+    name="v2lite_fp8_b4_s65536_split128", dtype="fp8")
+FP8_CONFIGS = (V2LITE_FP8_B8_S4096, V2LITE_FP8_B64_RAGGED, V3_FP8_H128_B32_S16384,
+               V2LITE_FP8_B4_S65536_LONG)
+
+BY_NAME = {c.name: c for c in ALL_CONFIGS + FP8_CONFIGS}
 
 # Parity tolerances: bf16 operands with fp32 accumulation, and the fp32 path.
 TOL_BF16_MAX_ABS = 2e-2

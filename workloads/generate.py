@@ -12,7 +12,8 @@ One CPU ``torch.Generator`` per call, seeded, with a fixed draw order:
    sequence b chosen by a seeded permutation; whole 576-wide rows are scaled.
 
 Values are drawn in fp32 and then rounded once to the storage type (bf16 by
-round-to-nearest-even), so the CUDA path and the oracle read identical bits.
+round-to-nearest-even; an FP8 cache to E4M3 by round-to-nearest-even, with
+queries and weights bf16), so the CUDA path and the oracle read identical bits.
 Positions are ``len_b - 1``: the cache already holds the current token's row.
 
 This module holds none of the method's arithmetic.
@@ -39,18 +40,33 @@ class MlaInputs:
     positions: torch.Tensor  # [B] int32
 
     def as_float64_numpy(self, b: Optional[int] = None):
-        """Exact fp64 copies (bf16 and fp32 values are exactly representable)."""
+        """Exact fp64 copies (bf16 and fp32 values are exactly representable).
+
+        An FP8 cache is handed over as its raw E4M3 codes (``cache_e4m3``,
+        uint8) with ``cache`` None: decoding the format is left to the reader.
+        """
         sl = slice(None) if b is None else slice(b, b + 1)
         f = lambda t: t.to(torch.float64).numpy()
+        fp8 = self.cache.dtype == FP8
         return dict(
-            cache=f(self.cache[sl]), q_nope=f(self.q_nope[sl]), q_rope=f(self.q_rope[sl]),
+            cache=None if fp8 else f(self.cache[sl]),
+            cache_e4m3=self.cache[sl].view(torch.uint8).numpy() if fp8 else None,
+            q_nope=f(self.q_nope[sl]), q_rope=f(self.q_rope[sl]),
             w_uk=f(self.w_uk), w_uv=f(self.w_uv),
             lengths=self.lengths[sl].numpy().astype("int64"),
             positions=self.positions[sl].numpy().astype("int64"))
 
 
+FP8 = torch.float8_e4m3fn
+
+
 def _storage(cfg: MlaConfig) -> torch.dtype:
+    """Storage type of queries and weights (bf16 also for an FP8 cache)."""
     return torch.float32 if cfg.dtype == "f32" else torch.bfloat16
+
+
+def cache_storage(cfg: MlaConfig) -> torch.dtype:
+    return FP8 if cfg.dtype == "fp8" else _storage(cfg)
 
 
 def make_inputs(cfg: MlaConfig, seed: int = 0, poison_tail: bool = False,
@@ -87,10 +103,10 @@ def make_inputs(cfg: MlaConfig, seed: int = 0, poison_tail: bool = False,
             rows = torch.randperm(n, generator=g)[:k]
             cache[b, rows, :] *= cfg.scaled_row_gain
 
-    cache = cache.to(st)
     if poison_tail:
         for b in range(B):
             cache[b, int(drawn[b]):, :] = float("nan")
+    cache = cache.to(cache_storage(cfg))
 
     positions = (drawn - 1).clamp(min=0).to(torch.int32)
     return MlaInputs(cfg=cfg, cache=cache, q_nope=q_nope.to(st), q_rope=q_rope.to(st),
