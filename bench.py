@@ -36,9 +36,11 @@ sys.path.insert(0, ROOT)
 METRIC = "MLA decode latent-cache GB/s (vs ~8 TB/s HBM) and decode tokens/s"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_bf16_traffic.json")
-KERNEL_SOURCES = ["head_latent_attention_absorbed_gb300/csrc/mla_decode.cu",
-                  "head_latent_attention_absorbed_gb300/csrc/mla_common.cuh"]
+# DRAM bytes per split launch measured by ncu: a list of records, each naming the
+# kernel, the workload and the sources (with their sha256) it was measured on.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "split_traffic.json")
+SPLIT_KERNEL = {"bf16": "split_tc_kernel", "fp8": "split_fp8_kernel", "f32": "split_f32_kernel"}
+DTYPE_NAME = {"bf16": "bf16", "fp8": "fp8_e4m3 cache, bf16 weights", "f32": "f32"}
 
 
 def parse(argv=None):
@@ -69,23 +71,31 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_sha():
+def sources_sha(sources):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def recorded_traffic(workload):
+def recorded_traffic(kernel, workload):
+    """The recorded DRAM bytes per launch of `kernel` on `workload`, or None when
+    there is no record or its sources have changed since it was taken."""
     try:
         with open(TRAFFIC_FILE) as f:
-            d = json.load(f)
+            records = json.load(f)
     except Exception:
         return None
-    if d.get("source_sha256") != kernel_sha() or d.get("workload") != workload:
-        return None
-    return d.get("dram_bytes_per_launch")
+    for d in records:
+        if d.get("kernel") != kernel or d.get("workload") != workload:
+            continue
+        try:
+            if d.get("source_sha256") == sources_sha(d.get("sources", [])):
+                return d.get("dram_bytes_per_launch")
+        except OSError:
+            return None
+    return None
 
 
 # ----------------------------------------------------------------------------- clocks (NVML)
@@ -172,6 +182,9 @@ def oracle_throughput(cfg, budget_s: float, max_steps: int | None = None, warmup
     from workloads import make_inputs
     inp = make_inputs(cfg, seed=0)
     seqs = [inp.as_float64_numpy(b) for b in range(cfg.batch)]
+    for a in seqs:
+        if a["cache"] is None:   # FP8 cache: the oracle decodes the E4M3 codes
+            a["cache"] = O.e4m3_to_float64(a["cache_e4m3"])
     rows = cfg.s_max if rows_per_step is None else max(1, min(cfg.s_max, rows_per_step))
 
     def one(i):
@@ -193,7 +206,7 @@ def oracle_throughput(cfg, budget_s: float, max_steps: int | None = None, warmup
         if max_steps is None and el >= budget_s:
             break
     el = time.perf_counter() - t0
-    byts = steps * rows * cfg.row * 2
+    byts = steps * rows * cfg.row * cfg.elt_bytes
     return byts / el / 1e9, steps / el, steps, rows, el
 
 
@@ -273,11 +286,11 @@ def run_op(args, cfg, rank):
     per second against the measured HBM peak."""
     import torch
     import head_latent_attention_absorbed_gb300 as mla
-    from workloads import make_append_inputs, make_wo_inputs
+    from workloads import cache_storage, make_append_inputs, make_wo_inputs
     mla.load()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    dt = cache_storage(cfg)   # the cache's type names the library dtype
     d = mla.dims(cfg.batch, cfg.heads, cfg.s_max, mla.dtype_code(dt))
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 126 * 2 ** 20
     if args.op == "cache_append":
@@ -322,7 +335,7 @@ def run_op(args, cfg, rank):
     peak, peak_kind = measured_peaks()
     line = {"op": args.op, "metric": metric, "value": gbs, "unit": "GB/s", "n_gpus": 1,
             "steps": K, "warmup": W, "us_per_launch": us, "higher_is_better": True,
-            "dtype": "bf16" if cfg.dtype == "bf16" else "f32", "data": "synthetic",
+            "dtype": DTYPE_NAME[cfg.dtype], "data": "synthetic",
             "config": {"workload": cfg.name, "batch": cfg.batch, "heads": cfg.heads,
                        "hidden": cfg.hidden,
                        "l2": f"{L} rotating weight copies, more than 3x L2"},
@@ -352,7 +365,7 @@ def main_with(args, rank: int, world: int, local: int = 0):
     import torch
     import torch.distributed as dist
     import head_latent_attention_absorbed_gb300 as mla
-    from workloads import make_inputs
+    from workloads import cache_storage, make_inputs
 
     if world > 1:
         torch.cuda.set_device(local)
@@ -361,11 +374,12 @@ def main_with(args, rank: int, world: int, local: int = 0):
     torch.cuda.set_device(dev)
     mla.load()
 
-    dt = torch.bfloat16 if cfg.dtype == "bf16" else torch.float32
+    dt = cache_storage(cfg)   # the cache's type names the library dtype
     inp = make_inputs(cfg, seed=rank)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
-    per_layer = (inp.cache.numel() + inp.w_uk.numel() + inp.w_uv.numel()) * inp.cache.element_size()
+    per_layer = (inp.cache.numel() * inp.cache.element_size() +
+                 (inp.w_uk.numel() + inp.w_uv.numel()) * inp.w_uk.element_size())
     L = max(2, math.ceil(3 * l2 / per_layer))
     caches = [inp.cache.to(dev) for _ in range(L)]
     wuk = [inp.w_uk.to(dev) for _ in range(L)]
@@ -485,11 +499,12 @@ def main_with(args, rank: int, world: int, local: int = 0):
 
     peak, peak_kind = measured_peaks()
     achieved = cache_bytes / split_avg_s / 1e9
-    roofline = {"bound": "hbm", "kernel": "split_tc_kernel (mla_decode_split)",
+    kname = SPLIT_KERNEL[cfg.dtype]
+    roofline = {"bound": "hbm", "kernel": f"{kname} (mla_decode_split)",
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
                 "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
-                "traffic": recorded_traffic(cfg.name),
+                "traffic": recorded_traffic(kname, cfg.name),
                 "bytes_per_launch": cache_bytes,
                 "avg_launch_us": split_avg_s * 1e6,
                 "launches_timed": Ks,
@@ -507,12 +522,12 @@ def main_with(args, rank: int, world: int, local: int = 0):
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": elapsed_ms / K, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if cfg.dtype == "bf16" else "f32",
+        "vs_baseline": None, "dtype": DTYPE_NAME[cfg.dtype],
         "data": "synthetic (seeded N(0,1) cache and queries, N(0,0.02^2) weights)",
         "tokens_per_s": tokens,
         "config": workload_config(cfg, L, step.splits),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": (3 if cfg.dtype == "bf16" else 4) * K,
+        "gpu_launches": (4 if cfg.dtype == "f32" else 3) * K,
         "clocks": sampler.summary(),
         "timing": "one CUDA-graph replay of the timed steps (no event nodes inside), CUDA events "
                   "on the replay stream",

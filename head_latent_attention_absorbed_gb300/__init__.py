@@ -10,14 +10,14 @@ from __future__ import annotations
 
 from typing import Optional
 
-from ._binding import (EXPORTED, LIB_PATH, MLA_BF16, MLA_DEV_LENGTH_OUT_OF_RANGE,
+from ._binding import (EXPORTED, LIB_PATH, MLA_BF16, MLA_FP8_E4M3, MLA_DEV_LENGTH_OUT_OF_RANGE,
                        MLA_DEV_PIPELINE_TIMEOUT, MLA_F32, MlaDims, MlaError, absorb_q, cache_append,
                        decode_attn, wo_proj,
                        decode_attn_noalloc, decode_combine, decode_split, decode_step, dims,
                        dtype_code, load, num_splits, out_proj, workspace_bytes)
 
 __all__ = [
-    "EXPORTED", "LIB_PATH", "MLA_BF16", "MLA_F32", "MLA_DEV_LENGTH_OUT_OF_RANGE",
+    "EXPORTED", "LIB_PATH", "MLA_BF16", "MLA_F32", "MLA_FP8_E4M3", "MLA_DEV_LENGTH_OUT_OF_RANGE",
     "MLA_DEV_PIPELINE_TIMEOUT", "MlaDims", "MlaError", "absorb_q", "decode_attn",
     "decode_attn_noalloc", "decode_split", "decode_combine", "decode_step", "dims",
     "dtype_code", "load", "num_splits", "out_proj", "workspace_bytes", "DecodeStep", "HostStep",
@@ -27,6 +27,9 @@ __all__ = [
 
 class DecodeStep:
     """One MLA decode step for a fixed (batch, heads, s_max, dtype).
+
+    ``dtype`` is the cache's element type: torch.bfloat16, torch.float32, or
+    torch.float8_e4m3fn (an E4M3 cache with bf16 queries and weights).
 
     ``run`` takes device tensors: q_nope [B,H,128], q_rope [B,H,64],
     cache [B,s_max,576], lengths [B] int32, positions [B] int32,

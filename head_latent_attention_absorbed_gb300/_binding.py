@@ -14,7 +14,7 @@ from typing import Optional
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmla_gb300.so")
 
-MLA_F32, MLA_BF16 = 0, 1
+MLA_F32, MLA_BF16, MLA_FP8_E4M3 = 0, 1, 2
 MLA_DEV_LENGTH_OUT_OF_RANGE = 1
 MLA_DEV_PIPELINE_TIMEOUT = 2
 STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
@@ -110,6 +110,8 @@ def dtype_code(torch_dtype) -> int:
         return MLA_BF16
     if torch_dtype == torch.float32:
         return MLA_F32
+    if torch_dtype == torch.float8_e4m3fn:   # an E4M3 cache; queries and weights bf16
+        return MLA_FP8_E4M3
     raise TypeError(f"unsupported dtype {torch_dtype}")
 
 

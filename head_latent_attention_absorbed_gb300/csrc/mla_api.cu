@@ -33,12 +33,12 @@ mla_status check_dims(const mla_dims* d, const char* who) {
               d->d_c, d->d_rope, d->d_nope, d->d_v);
     return MLA_ERR_UNSUPPORTED;
   }
-  if (d->dtype != MLA_F32 && d->dtype != MLA_BF16) {
-    set_error("%s: dtype %d is neither MLA_F32 nor MLA_BF16", who, d->dtype);
+  if (d->dtype != MLA_F32 && d->dtype != MLA_BF16 && d->dtype != MLA_FP8_E4M3) {
+    set_error("%s: dtype %d is not MLA_F32, MLA_BF16 or MLA_FP8_E4M3", who, d->dtype);
     return MLA_ERR_UNSUPPORTED;
   }
-  if (d->dtype == MLA_BF16 && d->heads % kHeadGroup != 0) {
-    set_error("%s: bf16 kernels need heads to be a multiple of %d (got %d)", who, kHeadGroup,
+  if (d->dtype != MLA_F32 && d->heads % kHeadGroup != 0) {
+    set_error("%s: bf16 and FP8 kernels need heads to be a multiple of %d (got %d)", who, kHeadGroup,
               d->heads);
     return MLA_ERR_UNSUPPORTED;
   }

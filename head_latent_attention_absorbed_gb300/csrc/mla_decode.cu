@@ -17,6 +17,7 @@
 #include <mutex>
 
 #include "mla_common.cuh"
+#include "mla_split.cuh"
 
 namespace mla {
 namespace {
@@ -24,27 +25,6 @@ namespace {
 constexpr int kWarps = 4;
 constexpr int kChunkAlign = 8;   // chunk sizes are multiples of 8 rows
 constexpr int kThreads = kWarps * 32;
-
-struct SplitParams {
-  const void* q_abs;
-  const void* q_pe;
-  const void* cache;        // used by the fp32 kernel
-  const int32_t* lengths;
-  float* part_o;            // [B, H, splits, 512]: one (b, h)'s chunks contiguous
-  float* part_lse;          // [B, H, splits]
-  int32_t* status;
-  int B, H, s_max, splits, chunk;
-  float scale_log2;         // softmax_scale * log2(e)
-};
-
-__device__ __forceinline__ int clamp_length(const SplitParams& p, int b, bool report_it) {
-  int len = p.lengths[b];
-  if (len < 1 || len > p.s_max) {
-    if (report_it) report(p.status, MLA_DEV_LENGTH_OUT_OF_RANGE);
-    len = len < 0 ? 0 : (len > p.s_max ? p.s_max : len);
-  }
-  return len;
-}
 
 // ---------------------------------------------------------------------------- bf16 split kernel
 // One CTA per (16-head group, KV chunk, sequence).  Every tcgen05.mma covers
@@ -893,7 +873,7 @@ int chunk_rows(const mla_dims* d, int requested, int* splits_out) {
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess)
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const bool bf16 = d->dtype == MLA_BF16;
+    const bool bf16 = d->dtype != MLA_F32;   // bf16 and FP8 kernels: one CTA per SM
     const long long per_split = static_cast<long long>(d->batch) * (bf16 ? d->heads / kHeadGroup : d->heads);
     const long long slots = bf16 ? sms : 4ll * sms;   // bf16: one CTA per SM
     double best = 1e300;
@@ -918,10 +898,15 @@ int chunk_rows(const mla_dims* d, int requested, int* splits_out) {
   return chunk;
 }
 
+// Partial outputs, their log-sum-exps, and (FP8 cache) the query images.
 size_t workspace_bytes(const mla_dims* d, int splits) {
   const size_t n = size_t(d->batch) * splits * d->heads;
   const size_t o_bytes = (n * kDc * sizeof(float) + 255) / 256 * 256;
-  return o_bytes + (n * sizeof(float) + 255) / 256 * 256;
+  const size_t lse_bytes = (n * sizeof(float) + 255) / 256 * 256;
+  const size_t img = d->dtype == MLA_FP8_E4M3
+                         ? (size_t(d->batch) * (d->heads / kHeadGroup) * kFp8QImage + 255) / 256 * 256
+                         : 0;
+  return o_bytes + lse_bytes + img;
 }
 
 }  // namespace
@@ -982,6 +967,9 @@ static mla_status prepare(const char* who, const mla_dims* dims, const void* q_a
   const size_t n = size_t(dims->batch) * splits * dims->heads;
   p->part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
                                          (n * kDc * sizeof(float) + 255) / 256 * 256);
+  p->q_img = dims->dtype == MLA_FP8_E4M3
+                 ? reinterpret_cast<uint8_t*>(p->part_lse) + (n * sizeof(float) + 255) / 256 * 256
+                 : nullptr;
   p->status = dev_status;
   p->B = dims->batch;
   p->H = dims->heads;
@@ -1006,6 +994,7 @@ extern "C" mla_status mla_decode_split(const mla_dims* dims, const void* q_abs, 
                           workspace, ws_bytes, dev_status, &p);
   if (st != MLA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dims->dtype == MLA_FP8_E4M3) return launch_split_fp8(p, cache, s, who);
   if (dims->dtype == MLA_BF16) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) {
@@ -1096,7 +1085,7 @@ extern "C" mla_status mla_decode_step(const mla_dims* dims, const void* q_nope, 
     set_error("%s: o_c, out and w_uv must be non-NULL 16-byte aligned pointers", who);
     return MLA_ERR_INVALID_ARG;
   }
-  if (dims->dtype != MLA_BF16) {
+  if (dims->dtype == MLA_F32) {
     // The fp32 path has no fused tail: the three calls in order.
     st = mla_absorb_q(dims, q_nope, q_rope, w_uk, positions, rope_base, q_abs, q_pe, stream);
     if (st != MLA_OK) return st;

@@ -317,7 +317,7 @@ extern "C" mla_status mla_absorb_q(const mla_dims* dims, const void* q_nope, con
   const int B = dims->batch, H = dims->heads;
   RopeTheta th;
   for (int i = 0; i < kDr / 2; ++i) th.turns[i] = pow(rope_base, -2.0 * i / kDr) / (2.0 * M_PI);
-  if (dims->dtype == MLA_BF16) {
+  if (dims->dtype != MLA_F32) {
     absorb_bf16_kernel<<<dim3(H, kDc / 16), 32, 0, s>>>(
         static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(q_rope),
         static_cast<const __nv_bfloat16*>(w_uk), positions, th, static_cast<float*>(q_abs),
@@ -346,7 +346,7 @@ extern "C" mla_status mla_out_proj(const mla_dims* dims, const float* o_c, const
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int B = dims->batch, H = dims->heads;
-  if (dims->dtype == MLA_BF16) {
+  if (dims->dtype != MLA_F32) {
     launch_pdl(out_proj_bf16_kernel, dim3(H, kDv / 8), dim3(128), 0, s, o_c,
                static_cast<const __nv_bfloat16*>(w_uv), static_cast<float*>(out), B, H);
   } else {
@@ -393,7 +393,7 @@ extern "C" mla_status mla_cache_append(const mla_dims* dims, int32_t hidden, con
   a.d_c = kDc;
   a.status = dev_status;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (dims->dtype == MLA_BF16) {
+  if (dims->dtype != MLA_F32) {
     WStreamJob j{};
     j.mode = kWsAppendRow;
     j.x_f32 = false;
@@ -403,6 +403,7 @@ extern "C" mla_status mla_cache_append(const mla_dims* dims, int32_t hidden, con
     j.K = hidden;
     j.N = kRow;
     j.cache = cache;
+    j.cache_fp8 = dims->dtype == MLA_FP8_E4M3;
     j.positions = positions;
     j.s_max = dims->s_max;
     j.d_c = kDc;
@@ -443,7 +444,7 @@ extern "C" mla_status mla_wo_proj(const mla_dims* dims, int32_t hidden, const fl
   a.y = y;
   RopeTheta th{};
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (dims->dtype == MLA_BF16) {
+  if (dims->dtype != MLA_F32) {
     if (a.K % 128 != 0) {
       set_error("%s: heads * d_v = %d must be a multiple of 128", who, a.K);
       return MLA_ERR_UNSUPPORTED;

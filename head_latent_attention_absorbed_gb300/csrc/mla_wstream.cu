@@ -19,6 +19,7 @@
 //   warps 3-6   fp32 x: each stage's staged fp32 box split into the bf16
 //               hi | lo rows of the B operand; then the epilogue (TMEM ->
 //               shared memory, the partial-sum exchange, output)
+#include <cuda_fp8.h>
 #include <cudaTypedefs.h>
 
 #include "mla_wstream.cuh"
@@ -60,7 +61,8 @@ struct WsParams {
   uint32_t tmem_cols;
   int ks;                   // K splits = cluster size
   float* y;
-  __nv_bfloat16* cache;
+  void* cache;              // bf16, or E4M3 with cache_fp8
+  int cache_fp8;
   const int32_t* positions;
   int s_max, d_c;
   double turns[kDr / 2];
@@ -354,8 +356,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             v0 = cs * x0 - sn * x1;
             v1 = sn * x0 + cs * x1;
           }
-          *reinterpret_cast<__nv_bfloat162*>(p.cache + (size_t(b) * p.s_max + pos) * p.N + n) =
-              __floats2bfloat162_rn(v0, v1);
+          const size_t at = (size_t(b) * p.s_max + pos) * p.N + n;
+          if (p.cache_fp8)   // E4M3, round to nearest even, saturating at +-448
+            *reinterpret_cast<__nv_fp8x2_storage_t*>(static_cast<uint8_t*>(p.cache) + at) =
+                __nv_cvt_float2_to_fp8x2(make_float2(v0, v1), __NV_SATFINITE, __NV_E4M3);
+          else
+            *reinterpret_cast<__nv_bfloat162*>(static_cast<__nv_bfloat16*>(p.cache) + at) =
+                __floats2bfloat162_rn(v0, v1);
         }
       }
     }
@@ -519,7 +526,8 @@ mla_status wstream_launch(const WStreamJob& j, cudaStream_t stream, const char* 
   p.Nc = j.x_f32 ? 2 * p.Bc : p.Bc;
   const int mtiles = (j.N + 127) / 128;
   p.y = j.y;
-  p.cache = static_cast<__nv_bfloat16*>(j.cache);
+  p.cache = j.cache;
+  p.cache_fp8 = j.cache_fp8 ? 1 : 0;
   p.positions = j.positions;
   p.s_max = j.s_max;
   p.d_c = j.d_c;

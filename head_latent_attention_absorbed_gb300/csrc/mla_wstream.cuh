@@ -19,7 +19,8 @@ struct WStreamJob {
   const void* w;               // [N, K] bf16, 16-byte aligned
   int B, K, N;                 // K a multiple of 64
   float* y;                    // kWsWriteY: [B, N] fp32
-  void* cache;                 // kWsAppendRow: [B, s_max, N] bf16
+  void* cache;                 // kWsAppendRow: [B, s_max, N] bf16, or E4M3 with cache_fp8
+  bool cache_fp8;              // kWsAppendRow: the cache holds FP8 E4M3 elements
   const int32_t* positions;    // kWsAppendRow: [B], the row written
   int s_max, d_c;              // kWsAppendRow: columns >= d_c are rotated
   double turns[kDr / 2];       // kWsAppendRow: RoPE frequencies / (2 pi)

@@ -30,11 +30,15 @@
  *    for the calling thread's most recent failure.
  *  - Element types: with dtype MLA_BF16 the cache, q_nope, q_rope and the
  *    weights are bf16 and all arithmetic accumulates in fp32; with MLA_F32
- *    they are fp32 and every step runs in fp32 (no TF32).  Every result --
- *    the absorbed query q_abs, the rotated q_pe, o_c, lse, the output o --
- *    and the workspace are fp32 in both cases (the bf16 decode kernel feeds
- *    the fp32 query and the softmax weights to the tensor cores as hi + lo
- *    bf16 pairs).
+ *    they are fp32 and every step runs in fp32 (no TF32).  With
+ *    MLA_FP8_E4M3 the cache elements are one-byte FP8 E4M3 numbers, used as
+ *    they are (no scale; "Multi-Head Latent Attention" 3.1: an element takes
+ *    1-4 bytes, FP8 to FP32), and q_nope, q_rope and the weights are bf16.
+ *    Every result -- the absorbed query q_abs, the rotated q_pe, o_c, lse,
+ *    the output o -- and the workspace are fp32 in every case (the bf16
+ *    decode kernel feeds the fp32 query and the softmax weights to the
+ *    tensor cores as hi + lo bf16 pairs, the FP8 kernel as three and two
+ *    E4M3 parts).
  *  - Launch overlap: the kernels of mla_decode_attn (and of its halves) and
  *    the bf16 kernel of mla_out_proj are launched with programmatic stream
  *    serialization, so each may begin while the kernel before it on the stream
@@ -46,7 +50,8 @@
  *    predecessor writes is read after the wait.  mla_absorb_q itself starts
  *    as usual.
  *  - Supported sizes: d_c = 512, d_rope = 64, d_nope = 128, d_v = 128;
- *    batch >= 1; s_max >= 1; heads >= 1 (a multiple of 16 for MLA_BF16).
+ *    batch >= 1; s_max >= 1; heads >= 1 (a multiple of 16 for MLA_BF16 and
+ *    MLA_FP8_E4M3).
  *    Anything else returns MLA_ERR_UNSUPPORTED.
  */
 #ifndef MLA_GB300_H
@@ -67,7 +72,7 @@ typedef enum mla_status {
   MLA_ERR_CUDA = 4           /* a CUDA runtime call or kernel launch failed */
 } mla_status;
 
-typedef enum mla_dtype { MLA_F32 = 0, MLA_BF16 = 1 } mla_dtype;
+typedef enum mla_dtype { MLA_F32 = 0, MLA_BF16 = 1, MLA_FP8_E4M3 = 2 } mla_dtype;
 
 /* Problem sizes shared by the three calls. */
 typedef struct mla_dims {
@@ -233,7 +238,8 @@ mla_status mla_out_proj(const mla_dims* dims, const float* o_c, const void* w_uv
  *  position -- adjacent pairs, angle in fp64 -- before it is cached, which is
  *  the form mla_decode_attn reads.)  The new row is then attended with
  *  lengths[b] = positions[b] + 1.  fp32 accumulation; the row is rounded once
- *  to the cache dtype.  No normalisation is applied (none is defined on the
+ *  to the cache dtype (MLA_FP8_E4M3: to nearest even, saturating at +-448;
+ *  x and w_kva are then bf16).  No normalisation is applied (none is defined on the
  *  pages for this step).
  *
  * x      [B, hidden] dtype           w_kva [d_c + d_rope, hidden] dtype
