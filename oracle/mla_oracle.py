@@ -176,6 +176,48 @@ def causal_attention_naive(q_nope_seq, q_rope_seq, w_uk, w_uv, cache_seq, scale,
     return np.einsum("hij,jhe->ihe", p, v)
 
 
+# ----------------------------------------------------------------------------- multi-token decode
+def decode_multi_token(q_nope, q_rope, w_uk, w_uv, cache, lengths, q_len: int,
+                       scale: float, base: float):
+    """Decode of q_len new tokens per sequence in one step (speculative or
+    multi-token decoding), weight-absorbed, exact softmax.
+
+    "Transformer and KV Cache Basics", Thinking item 4 (mask design): prefill and
+    decode are treated alike; the cache already holds the new tokens, so with
+    k_len cached rows the q_len queries sit at positions k_len - q_len .. k_len - 1
+    and a key is masked when its position is past the query's (the small upper
+    right triangle of the score matrix).  Each query is rotated at its own
+    position (Multi-Head Latent Attention, 3.7).
+
+    q_nope: [B, q_len, H, d_nope]; q_rope: [B, q_len, H, d_rope]; lengths: [B] (k_len).
+    Returns dict(q_abs, q_pe, o_c, lse, o) with leading dims [B, q_len].
+    """
+    q_nope = np.asarray(q_nope, dtype=np.float64)
+    B, T, H, _ = q_nope.shape
+    if T != q_len:
+        raise ValueError("q_nope's second axis is the token axis of length q_len")
+    d_c = w_uk.shape[2]
+    lengths = np.asarray(lengths)
+    if np.any(lengths < q_len):
+        raise ValueError("every sequence must already cache its q_len new tokens")
+    query_pos = lengths[:, None] - q_len + np.arange(q_len)[None, :]            # [B, T]
+    q_abs = absorb_q(q_nope.reshape(B * T, H, -1), w_uk).reshape(B, T, H, d_c)
+    q_pe = apply_rope(q_rope, query_pos[..., None], base)                       # [B, T, H, d_R]
+    o_c = np.zeros((B, T, H, d_c))
+    lse = np.zeros((B, T, H))
+    o = np.zeros((B, T, H, w_uv.shape[1]))
+    for b in range(B):
+        n = int(lengths[b])
+        c, kr = cache[b, :n, :d_c], cache[b, :n, d_c:]
+        s = scale * (np.einsum("thc,sc->ths", q_abs[b], c) + np.einsum("thr,sr->ths", q_pe[b], kr))
+        future = query_pos[b][:, None] < np.arange(n)[None, :]                  # [T, n]
+        s = np.where(future[:, None, :], -np.inf, s)
+        p, lse[b] = softmax_stats(s)
+        o_c[b] = np.einsum("ths,sc->thc", p, c)
+        o[b] = np.einsum("hec,thc->the", w_uv, o_c[b])
+    return dict(q_abs=q_abs, q_pe=q_pe, o_c=o_c, lse=lse, o=o)
+
+
 # ----------------------------------------------------------------------------- split-KV combine
 def split_decode_combine(q_abs, q_pe, cache_b, n: int, scale: float, chunk: int):
     """Split-KV for one sequence: per chunk j of `chunk` rows compute the chunk's

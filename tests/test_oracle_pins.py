@@ -398,3 +398,46 @@ def test_e4m3_round_is_nearest_even_and_saturating():
     # 1 + 1/16 lies halfway between 1 (0x38, even) and 1.125 (0x39)
     assert O.e4m3_round(1.0625) == 0x38 and O.e4m3_round(1.1875) == 0x3A
     assert O.e4m3_round(1e6) == 0x7E and O.e4m3_round(-1e6) == 0xFE
+
+
+# ----------------------------------------------------------------------------- multi-token decode
+def test_multi_token_decode_is_the_last_rows_of_causal_attention():
+    """q_len new tokens decoded together give exactly the last q_len rows of full
+    causal self-attention over the sequence ("Transformer and KV Cache Basics",
+    Thinking item 4: only the small upper-right triangle is masked), for every
+    q_len up to the whole sequence, through the naive (decompressed K/V) form."""
+    rng = np.random.default_rng(23)
+    S, H, d_c, d_rope, d_nope, d_v = 9, 2, 12, 4, 6, 5
+    qn = rng.standard_normal((S, H, d_nope))
+    qr = rng.standard_normal((S, H, d_rope))
+    c = rng.standard_normal((S, d_c))
+    kr = O.apply_rope(rng.standard_normal((S, d_rope)), np.arange(S), 10000.0)
+    w_uk = 0.3 * rng.standard_normal((H, d_nope, d_c))
+    w_uv = 0.3 * rng.standard_normal((H, d_v, d_c))
+    cache = np.concatenate([c, kr], axis=1)
+    full = O.causal_attention_naive(qn, qr, w_uk, w_uv, cache, 0.3, 10000.0)
+    for T in (1, 2, 4, S):
+        got = O.decode_multi_token(qn[S - T:][None], qr[S - T:][None], w_uk, w_uv, cache[None],
+                                   np.array([S]), T, 0.3, 10000.0)
+        np.testing.assert_allclose(got["o"][0], full[S - T:], atol=1e-12)
+
+
+def test_multi_token_decode_reduces_to_single_token_decode():
+    """Token i of the block equals a single-token decode at cache length
+    k_len - q_len + i + 1 (its own position), per call output; with q_len = 1 the
+    two functions agree on every output."""
+    rng = np.random.default_rng(24)
+    a = _rand_case(rng, B=2, H=3, S=10, lengths=[10, 7])
+    T = 3
+    qn = rng.standard_normal((2, T, 3, a["q_nope"].shape[-1]))
+    qr = rng.standard_normal((2, T, 3, a["q_rope"].shape[-1]))
+    got = O.decode_multi_token(qn, qr, a["w_uk"], a["w_uv"], a["cache"], a["lengths"], T,
+                               0.4, 10000.0)
+    for b in range(2):
+        for i in range(T):
+            n = int(a["lengths"][b]) - T + i + 1
+            one = O.decode_absorbed(qn[b, i][None], qr[b, i][None], a["w_uk"], a["w_uv"],
+                                    a["cache"][b:b + 1], np.array([n]), np.array([n - 1]),
+                                    0.4, 10000.0)
+            for k in ("q_abs", "q_pe", "o_c", "lse", "o"):
+                np.testing.assert_allclose(got[k][b, i], one[k][0], atol=1e-12)

@@ -45,6 +45,9 @@ class MlaConfig:
     d_v: int = D_V
     rope_base: float = 10000.0
     weight_std: float = 0.02
+    # query tokens per sequence in one step (multi-token / speculative decode): the
+    # last q_len cached rows of each sequence are the step's tokens
+    q_len: int = 1
 
     @property
     def row(self) -> int:
@@ -101,7 +104,13 @@ V2LITE_FP8_B4_S65536_LONG = V2LITE_BF16_B4_S65536_LONG.scaled(
 FP8_CONFIGS = (V2LITE_FP8_B8_S4096, V2LITE_FP8_B64_RAGGED, V3_FP8_H128_B32_S16384,
                V2LITE_FP8_B4_S65536_LONG)
 
-BY_NAME = {c.name: c for c in ALL_CONFIGS + FP8_CONFIGS}
+# Multi-token decode ("Transformer and KV Cache Basics", mask design for multi-token
+# decoding): four new tokens per sequence in one step, on the bench shape.
+V2LITE_BF16_B8_S4096_Q4 = V2LITE_BF16_B8_S4096.scaled(name="v2lite_bf16_b8_s4096_q4", q_len=4)
+V2LITE_FP8_B8_S4096_Q4 = V2LITE_FP8_B8_S4096.scaled(name="v2lite_fp8_b8_s4096_q4", q_len=4)
+MULTI_TOKEN_CONFIGS = (V2LITE_BF16_B8_S4096_Q4, V2LITE_FP8_B8_S4096_Q4)
+
+BY_NAME = {c.name: c for c in ALL_CONFIGS + FP8_CONFIGS + MULTI_TOKEN_CONFIGS}
 
 # Parity tolerances: bf16 operands with fp32 accumulation, and the fp32 path.
 TOL_BF16_MAX_ABS = 2e-2

@@ -11,6 +11,9 @@ One CPU ``torch.Generator`` per call, seeded, with a fixed draw order:
 7. the rows to scale (long-context workload only): round(frac * len_b) rows of
    sequence b chosen by a seeded permutation; whole 576-wide rows are scaled.
 
+With ``q_len`` > 1 the queries have B * q_len rows (row b * q_len + i is token i
+of sequence b) and ``positions[b * q_len + i] = len_b - q_len + i``.
+
 Values are drawn in fp32 and then rounded once to the storage type (bf16 by
 round-to-nearest-even; an FP8 cache to E4M3 by round-to-nearest-even, with
 queries and weights bf16), so the CUDA path and the oracle read identical bits.
@@ -32,12 +35,12 @@ from .configs import MlaConfig
 class MlaInputs:
     cfg: MlaConfig
     cache: torch.Tensor      # [B, S_max, row], storage dtype, CPU
-    q_nope: torch.Tensor     # [B, H, d_nope]
-    q_rope: torch.Tensor     # [B, H, d_rope]
+    q_nope: torch.Tensor     # [B * q_len, H, d_nope]
+    q_rope: torch.Tensor     # [B * q_len, H, d_rope]
     w_uk: torch.Tensor       # [H, d_nope, d_c]
     w_uv: torch.Tensor       # [H, d_v, d_c]
     lengths: torch.Tensor    # [B] int32
-    positions: torch.Tensor  # [B] int32
+    positions: torch.Tensor  # [B * q_len] int32
 
     def as_float64_numpy(self, b: Optional[int] = None):
         """Exact fp64 copies (bf16 and fp32 values are exactly representable).
@@ -83,8 +86,8 @@ def make_inputs(cfg: MlaConfig, seed: int = 0, poison_tail: bool = False,
     st = _storage(cfg)
 
     cache = torch.randn((B, S, cfg.row), generator=g, dtype=torch.float32)
-    q_nope = torch.randn((B, H, cfg.d_nope), generator=g, dtype=torch.float32)
-    q_rope = torch.randn((B, H, cfg.d_rope), generator=g, dtype=torch.float32)
+    q_nope = torch.randn((B * cfg.q_len, H, cfg.d_nope), generator=g, dtype=torch.float32)
+    q_rope = torch.randn((B * cfg.q_len, H, cfg.d_rope), generator=g, dtype=torch.float32)
     w_uk = torch.randn((H, cfg.d_nope, cfg.d_c), generator=g, dtype=torch.float32) * cfg.weight_std
     w_uv = torch.randn((H, cfg.d_v, cfg.d_c), generator=g, dtype=torch.float32) * cfg.weight_std
 
@@ -108,7 +111,8 @@ def make_inputs(cfg: MlaConfig, seed: int = 0, poison_tail: bool = False,
             cache[b, int(drawn[b]):, :] = float("nan")
     cache = cache.to(cache_storage(cfg))
 
-    positions = (drawn - 1).clamp(min=0).to(torch.int32)
+    tok = torch.arange(cfg.q_len, dtype=torch.int32)
+    positions = (drawn[:, None] - cfg.q_len + tok[None, :]).clamp(min=0).reshape(-1).to(torch.int32)
     return MlaInputs(cfg=cfg, cache=cache, q_nope=q_nope.to(st), q_rope=q_rope.to(st),
                      w_uk=w_uk.to(st), w_uv=w_uv.to(st), lengths=drawn, positions=positions)
 
