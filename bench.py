@@ -257,6 +257,8 @@ def workload_config(cfg, layers, splits):
                    f"step k reads layer k mod {layers}")
     if splits is not None:
         c["kv_splits"] = splits
+    if cfg.q_len > 1:
+        c["q_len"] = cfg.q_len
     return c
 
 
@@ -347,6 +349,13 @@ def run_op(args, cfg, rank):
     return 0
 
 
+def launches_per_step(cfg) -> int:
+    """Library kernels one step launches: absorb, (FP8: the query image), split,
+    then the fused combine + W_UV (one token, bf16/FP8) or combine and out_proj."""
+    fused = cfg.q_len == 1 and cfg.dtype != "f32"
+    return 1 + (1 if cfg.dtype == "fp8" else 0) + 1 + (1 if fused else 2)
+
+
 # ----------------------------------------------------------------------------- our arm
 def main():
     return main_with(parse(), int(os.environ.get("RANK", "0")),
@@ -390,7 +399,7 @@ def main_with(args, rank: int, world: int, local: int = 0):
     positions = inp.positions.to(dev)
     step = mla.DecodeStep(cfg.batch, cfg.heads, cfg.s_max, dt, device=dev,
                           num_splits_requested=args.splits, rope_base=cfg.rope_base,
-                          softmax_scale=cfg.softmax_scale)
+                          softmax_scale=cfg.softmax_scale, q_len=cfg.q_len)
     d = step.dims
     cache_bytes = int(inp.lengths.to(torch.int64).sum()) * cfg.row * inp.cache.element_size()
 
@@ -436,7 +445,7 @@ def main_with(args, rank: int, world: int, local: int = 0):
     elapsed_ms = max_over_ranks(elapsed_ms, dev, world)
     sec = elapsed_ms / 1e3
     value = whole_job_rate(cache_bytes, K, world, sec) / 1e9
-    tokens = whole_job_rate(cfg.batch, K, world, sec)
+    tokens = whole_job_rate(cfg.batch * cfg.q_len, K, world, sec)
 
     # The dominant kernel alone: Ks back-to-back split launches over the same
     # rotating layer copies, one CUDA graph, CUDA events on the replay stream.
@@ -446,8 +455,13 @@ def main_with(args, rank: int, world: int, local: int = 0):
     gs = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gs, stream=cap, capture_error_mode="thread_local"):
         for k in range(Ks):
-            mla.decode_split(d, step.q_abs, step.q_pe, caches[k % L], lengths, step.workspace,
-                             step.scale, args.splits, step.status)
+            if cfg.q_len == 1:
+                mla.decode_split(d, step.q_abs, step.q_pe, caches[k % L], lengths,
+                                 step.workspace, step.scale, args.splits, step.status)
+            else:   # the split has no separate multi-token entry: split + combine
+                mla.decode_attn_multi(d, cfg.q_len, step.q_abs, step.q_pe, caches[k % L],
+                                      lengths, step.o_c, step.workspace, step.scale, args.splits,
+                                      step.lse, step.status)
     gs.replay()
     torch.cuda.synchronize()
     s_begin = torch.cuda.Event(enable_timing=True)
@@ -492,7 +506,7 @@ def main_with(args, rank: int, world: int, local: int = 0):
         bi, bo = hosts[0].h2d_bytes, hosts[0].d2h_bytes
         e2e = {"value": whole_job_rate(cache_bytes, Ke, world, e_ms / 1e3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": Ke,
-               "tokens_per_s": whole_job_rate(cfg.batch, Ke, world, e_ms / 1e3),
+               "tokens_per_s": whole_job_rate(cfg.batch * cfg.q_len, Ke, world, e_ms / 1e3),
                "path": "DecodeStep.capture: per step one pinned host->device copy of the "
                        "queries, lengths and positions, the three C-ABI calls, one "
                        "device->host copy of o; one CUDA-graph replay per step"}
@@ -500,7 +514,9 @@ def main_with(args, rank: int, world: int, local: int = 0):
     peak, peak_kind = measured_peaks()
     achieved = cache_bytes / split_avg_s / 1e9
     kname = SPLIT_KERNEL[cfg.dtype]
-    roofline = {"bound": "hbm", "kernel": f"{kname} (mla_decode_split)",
+    roofline = {"bound": "hbm",
+                "kernel": (f"{kname} (mla_decode_split)" if cfg.q_len == 1 else
+                           f"{kname} + combine_kernel (mla_decode_attn_multi)"),
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
                 "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
@@ -527,7 +543,7 @@ def main_with(args, rank: int, world: int, local: int = 0):
         "tokens_per_s": tokens,
         "config": workload_config(cfg, L, step.splits),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": (4 if cfg.dtype == "f32" else 3) * K,
+        "gpu_launches": launches_per_step(cfg) * K,
         "clocks": sampler.summary(),
         "timing": "one CUDA-graph replay of the timed steps (no event nodes inside), CUDA events "
                   "on the replay stream",

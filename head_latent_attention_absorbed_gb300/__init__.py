@@ -12,13 +12,14 @@ from typing import Optional
 
 from ._binding import (EXPORTED, LIB_PATH, MLA_BF16, MLA_FP8_E4M3, MLA_DEV_LENGTH_OUT_OF_RANGE,
                        MLA_DEV_PIPELINE_TIMEOUT, MLA_F32, MlaDims, MlaError, absorb_q, cache_append,
-                       decode_attn, wo_proj,
+                       decode_attn, decode_attn_multi, query_dims, wo_proj,
                        decode_attn_noalloc, decode_combine, decode_split, decode_step, dims,
                        dtype_code, load, num_splits, out_proj, workspace_bytes)
 
 __all__ = [
     "EXPORTED", "LIB_PATH", "MLA_BF16", "MLA_F32", "MLA_FP8_E4M3", "MLA_DEV_LENGTH_OUT_OF_RANGE",
     "MLA_DEV_PIPELINE_TIMEOUT", "MlaDims", "MlaError", "absorb_q", "decode_attn",
+    "decode_attn_multi", "query_dims",
     "decode_attn_noalloc", "decode_split", "decode_combine", "decode_step", "dims",
     "dtype_code", "load", "num_splits", "out_proj", "workspace_bytes", "DecodeStep", "HostStep",
     "cache_append", "wo_proj",
@@ -31,45 +32,60 @@ class DecodeStep:
     ``dtype`` is the cache's element type: torch.bfloat16, torch.float32, or
     torch.float8_e4m3fn (an E4M3 cache with bf16 queries and weights).
 
-    ``run`` takes device tensors: q_nope [B,H,128], q_rope [B,H,64],
-    cache [B,s_max,576], lengths [B] int32, positions [B] int32,
-    w_uk [H,128,512], w_uv [H,128,512]; it returns o [B,H,128] fp32 (a buffer
-    reused by the next call).
+    ``run`` takes device tensors: q_nope [R,H,128], q_rope [R,H,64],
+    cache [B,s_max,576], lengths [B] int32, positions [R] int32,
+    w_uk [H,128,512], w_uv [H,128,512]; it returns o [R,H,128] fp32 (a buffer
+    reused by the next call).  R = B * q_len: with ``q_len`` > 1 each sequence
+    decodes q_len new tokens at once (row b * q_len + i is token i of sequence
+    b, at position lengths[b] - q_len + i, causal within the block).
     """
 
     def __init__(self, batch: int, heads: int, s_max: int, dtype, device="cuda",
                  num_splits_requested: int = 0, rope_base: float = 10000.0,
-                 softmax_scale: Optional[float] = None):
+                 softmax_scale: Optional[float] = None, q_len: int = 1):
         import torch
         self.dims = dims(batch, heads, s_max, dtype_code(dtype))
+        self.q_len = q_len
+        self.qdims = query_dims(self.dims, q_len)     # the query side: B * q_len rows
         self.splits_requested = num_splits_requested
-        self.splits = num_splits(self.dims, num_splits_requested)
+        self.splits = num_splits(self.qdims, num_splits_requested)
         self.rope_base = rope_base
         self.scale = softmax_scale if softmax_scale is not None else (128 + 64) ** -0.5
         dev = torch.device(device)
-        self.q_abs = torch.empty((batch, heads, 512), dtype=torch.float32, device=dev)
-        self.q_pe = torch.empty((batch, heads, 64), dtype=torch.float32, device=dev)
-        self.o_c = torch.empty((batch, heads, 512), dtype=torch.float32, device=dev)
-        self.lse = torch.empty((batch, heads), dtype=torch.float32, device=dev)
-        self.out = torch.empty((batch, heads, 128), dtype=torch.float32, device=dev)
-        nbytes = workspace_bytes(self.dims, num_splits_requested)
+        rows = batch * q_len
+        self.q_abs = torch.empty((rows, heads, 512), dtype=torch.float32, device=dev)
+        self.q_pe = torch.empty((rows, heads, 64), dtype=torch.float32, device=dev)
+        self.o_c = torch.empty((rows, heads, 512), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((rows, heads), dtype=torch.float32, device=dev)
+        self.out = torch.empty((rows, heads, 128), dtype=torch.float32, device=dev)
+        nbytes = workspace_bytes(self.qdims, num_splits_requested)
         self.workspace = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
 
     def run(self, q_nope, q_rope, cache, lengths, positions, w_uk, w_uv, stream=None):
-        """The whole step in one library call (mla_decode_step)."""
+        """The whole step: one library call (mla_decode_step) for one token per
+        sequence, the three calls with mla_decode_attn_multi for q_len > 1."""
+        if self.q_len > 1:
+            return self.run_calls(q_nope, q_rope, cache, lengths, positions, w_uk, w_uv, stream)
         decode_step(self.dims, q_nope, q_rope, w_uk, positions, cache, lengths, w_uv,
                     self.workspace, self.q_abs, self.q_pe, self.o_c, self.out, self.scale,
                     self.rope_base, self.splits_requested, self.lse, self.status, stream)
         return self.out
 
     def run_calls(self, q_nope, q_rope, cache, lengths, positions, w_uk, w_uv, stream=None):
-        """The same step as the three separate calls absorb_q, decode_attn, out_proj."""
-        absorb_q(self.dims, q_nope, q_rope, w_uk, positions, self.q_abs, self.q_pe,
+        """The same step as the three separate calls absorb_q, decode_attn (or
+        decode_attn_multi), out_proj."""
+        absorb_q(self.qdims, q_nope, q_rope, w_uk, positions, self.q_abs, self.q_pe,
                  self.rope_base, stream)
-        decode_attn(self.dims, self.q_abs, self.q_pe, cache, lengths, self.o_c, self.workspace,
-                    self.scale, self.splits_requested, self.lse, self.status, stream)
-        out_proj(self.dims, self.o_c, w_uv, self.out, stream)
+        if self.q_len > 1:
+            decode_attn_multi(self.dims, self.q_len, self.q_abs, self.q_pe, cache, lengths,
+                              self.o_c, self.workspace, self.scale, self.splits_requested,
+                              self.lse, self.status, stream)
+        else:
+            decode_attn(self.dims, self.q_abs, self.q_pe, cache, lengths, self.o_c,
+                        self.workspace, self.scale, self.splits_requested, self.lse,
+                        self.status, stream)
+        out_proj(self.qdims, self.o_c, w_uv, self.out, stream)
         return self.out
 
     def capture(self, cache, w_uk, w_uv):
@@ -90,11 +106,11 @@ class HostStep:
 
     def __init__(self, step: DecodeStep, cache, w_uk, w_uv):
         import torch
-        B, H = step.dims.batch, step.dims.heads
-        dt = cache.dtype
-        elt = cache.element_size()
-        pieces = [("q_nope", (B, H, 128), dt, elt), ("q_rope", (B, H, 64), dt, elt),
-                  ("lengths", (B,), torch.int32, 4), ("positions", (B,), torch.int32, 4)]
+        B, H, R = step.dims.batch, step.dims.heads, step.qdims.batch
+        dt = torch.bfloat16 if cache.dtype == torch.float8_e4m3fn else cache.dtype
+        elt = torch.tensor([], dtype=dt).element_size()
+        pieces = [("q_nope", (R, H, 128), dt, elt), ("q_rope", (R, H, 64), dt, elt),
+                  ("lengths", (B,), torch.int32, 4), ("positions", (R,), torch.int32, 4)]
         offs, off = [], 0
         for _, shape, _, e in pieces:
             n = 1
@@ -127,7 +143,7 @@ class HostStep:
 
         # One run outside capture (module loading, kernel attributes); the inputs
         # are whatever the block holds, so start from valid lengths.
-        self.lengths.fill_(1)
+        self.lengths.fill_(step.q_len)
         self.positions.zero_()
         self.q_nope.zero_()
         self.q_rope.zero_()

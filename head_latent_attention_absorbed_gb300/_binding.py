@@ -21,7 +21,7 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
           3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA"}
 EXPORTED = ("mla_absorb_q", "mla_decode_num_splits", "mla_decode_workspace_bytes",
             "mla_decode_attn", "mla_decode_split", "mla_decode_combine",
-            "mla_decode_attn_noalloc", "mla_decode_step", "mla_out_proj", "mla_cache_append",
+            "mla_decode_attn_noalloc", "mla_decode_attn_multi", "mla_decode_step", "mla_out_proj", "mla_cache_append",
             "mla_wo_proj",
             "mla_status_string", "mla_last_error_message")
 
@@ -64,6 +64,9 @@ def load(path: Optional[str] = None):
     lib.mla_decode_split.restype = ctypes.c_int
     lib.mla_decode_combine.argtypes = [D, P, I32, P, SZ, P, P, P]
     lib.mla_decode_combine.restype = ctypes.c_int
+    lib.mla_decode_attn_multi.argtypes = [D, I32, P, P, P, P, ctypes.c_float, I32, P, SZ, P, P, P,
+                                          P]
+    lib.mla_decode_attn_multi.restype = ctypes.c_int
     lib.mla_decode_attn_noalloc.argtypes = [D, P, P, P, P, ctypes.c_float, I32, P, P, P, P]
     lib.mla_decode_attn_noalloc.restype = ctypes.c_int
     lib.mla_decode_step.argtypes = [D, P, P, P, P, ctypes.c_double, P, P, ctypes.c_float, I32, P,
@@ -173,6 +176,28 @@ def decode_combine(d: MlaDims, lengths, workspace, o_c, num_splits_requested: in
     _check(load().mla_decode_combine(ctypes.byref(d), _ptr(lengths), int(num_splits_requested),
                                      _ptr(workspace), nbytes, _ptr(o_c), _ptr(lse),
                                      _stream(stream)))
+
+
+def query_dims(d: MlaDims, q_len: int) -> MlaDims:
+    """The dims of the query side of a q_len-token step: batch B * q_len."""
+    return MlaDims(d.batch * q_len, d.heads, d.d_c, d.d_rope, d.d_nope, d.d_v, d.s_max, d.dtype)
+
+
+def decode_attn_multi(d: MlaDims, q_len: int, q_abs, q_pe, cache, lengths, o_c, workspace,
+                      softmax_scale: float, num_splits_requested: int = 0, lse=None,
+                      dev_status=None, stream=None) -> None:
+    """decode_attn for q_len new tokens per sequence, causal within the block.
+
+    ``d`` describes the cache (B sequences); q_abs, q_pe, o_c and lse have
+    B * q_len rows (row b * q_len + i is token i of sequence b).
+    """
+    _cuda_contig(q_abs, q_pe, cache, lengths, o_c, workspace, lse, dev_status)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().mla_decode_attn_multi(ctypes.byref(d), int(q_len), _ptr(q_abs), _ptr(q_pe),
+                                        _ptr(cache), _ptr(lengths), float(softmax_scale),
+                                        int(num_splits_requested), _ptr(workspace), nbytes,
+                                        _ptr(o_c), _ptr(lse), _ptr(dev_status),
+                                        _stream(stream)))
 
 
 def decode_attn_noalloc(d: MlaDims, q_abs, q_pe, cache, lengths, o_c, softmax_scale: float,

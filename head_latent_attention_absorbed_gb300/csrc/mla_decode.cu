@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // rows may hold anything (NaN included): those are zeroed before the PV.
   const int zero_from = len - (r0 + (T - 1) * kTileRows);
   const bool zero_last = zero_from < kTileRows;
-  const int row_base = b * p.s_max + r0;
+  const int row_base = cache_seq(p, b) * p.s_max + r0;
   const int h0 = g * kHeadGroup;
   auto bar = [&](int i) { return bars + 8 * i; };
   // The last tile's latent pairs.  With T >= 2 all eight go to space that is free
@@ -639,7 +639,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
   for (int i = 0; i < 16; ++i) acc[i] = 0.f;
   for (int t = r0 + warp; t < r1; t += kWarps) {
-    const float* row = cache + (size_t(b) * p.s_max + t) * kRow;
+    const float* row = cache + (size_t(cache_seq(p, b)) * p.s_max + t) * kRow;
     float c[18];
     float dot = 0.f;
 #pragma unroll
@@ -929,13 +929,23 @@ extern "C" size_t mla_decode_workspace_bytes(const mla_dims* dims, int32_t reque
 }
 
 // Validates the arguments shared by the split and combine halves and fills the
-// kernel parameters.  Returns MLA_OK or the status to hand back.
-static mla_status prepare(const char* who, const mla_dims* dims, const void* q_abs,
+// kernel parameters.  `dims` describes the cache (dims->batch sequences); with
+// q_len query tokens per sequence the queries, partials and outputs have
+// dims->batch * q_len rows, and chunks and workspace are planned for that many.
+// Returns MLA_OK or the status to hand back.
+static mla_status prepare(const char* who, const mla_dims* dims, int q_len, const void* q_abs,
                           const void* q_pe, const void* cache, const int32_t* lengths,
                           float softmax_scale, int32_t num_splits, void* workspace,
                           size_t ws_bytes, int32_t* dev_status, SplitParams* p) {
   mla_status st = check_dims(dims, who);
   if (st != MLA_OK) return st;
+  if (q_len < 1 || static_cast<long long>(dims->batch) * q_len > (1ll << 30)) {
+    set_error("%s: q_len=%d must be >= 1 with batch*q_len <= 2^30", who, q_len);
+    return MLA_ERR_INVALID_ARG;
+  }
+  mla_dims qd = *dims;   // one row of queries per (sequence, token)
+  qd.batch = dims->batch * q_len;
+  dims = &qd;
   if (!lengths || !workspace) {
     set_error("%s: a required pointer is NULL", who);
     return MLA_ERR_INVALID_ARG;
@@ -972,6 +982,7 @@ static mla_status prepare(const char* who, const mla_dims* dims, const void* q_a
                  : nullptr;
   p->status = dev_status;
   p->B = dims->batch;
+  p->q_len = q_len;
   p->H = dims->heads;
   p->s_max = dims->s_max;
   p->splits = splits;
@@ -980,18 +991,19 @@ static mla_status prepare(const char* who, const mla_dims* dims, const void* q_a
   return MLA_OK;
 }
 
-extern "C" mla_status mla_decode_split(const mla_dims* dims, const void* q_abs, const void* q_pe,
-                                       const void* cache, const int32_t* lengths,
-                                       float softmax_scale, int32_t num_splits, void* workspace,
-                                       size_t ws_bytes, int32_t* dev_status, void* stream) {
-  const char* who = "mla_decode_split";
+// The split half for q_len query tokens per cache sequence (1: ordinary decode).
+static mla_status decode_split(const char* who, const mla_dims* dims, int q_len,
+                               const void* q_abs, const void* q_pe, const void* cache,
+                               const int32_t* lengths, float softmax_scale, int32_t num_splits,
+                               void* workspace, size_t ws_bytes, int32_t* dev_status,
+                               void* stream) {
   if (!q_abs || !q_pe || !cache) {
     set_error("%s: a required pointer is NULL", who);
     return MLA_ERR_INVALID_ARG;
   }
   SplitParams p;
-  mla_status st = prepare(who, dims, q_abs, q_pe, cache, lengths, softmax_scale, num_splits,
-                          workspace, ws_bytes, dev_status, &p);
+  mla_status st = prepare(who, dims, q_len, q_abs, q_pe, cache, lengths, softmax_scale,
+                          num_splits, workspace, ws_bytes, dev_status, &p);
   if (st != MLA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dims->dtype == MLA_FP8_E4M3) return launch_split_fp8(p, cache, s, who);
@@ -1028,30 +1040,68 @@ extern "C" mla_status mla_decode_split(const mla_dims* dims, const void* q_abs, 
       }
       attr_set = true;
     }
-    dim3 grid(dims->heads / kHeadGroup, p.splits, dims->batch);
+    dim3 grid(dims->heads / kHeadGroup, p.splits, p.B);
     launch_pdl(split_tc_kernel, grid, dim3(kTcThreads), kTcSmem, s, tmap, tmap_half, p);
   } else {
-    dim3 grid(dims->heads, p.splits, dims->batch);
+    dim3 grid(dims->heads, p.splits, p.B);
     split_f32_kernel<<<grid, kThreads, 0, s>>>(p);
   }
   return launch_status(who);
 }
 
-extern "C" mla_status mla_decode_combine(const mla_dims* dims, const int32_t* lengths,
-                                         int32_t num_splits, const void* workspace,
-                                         size_t ws_bytes, float* o_c, float* lse, void* stream) {
-  const char* who = "mla_decode_combine";
+static mla_status decode_combine(const char* who, const mla_dims* dims, int q_len,
+                                 const int32_t* lengths, int32_t num_splits,
+                                 const void* workspace, size_t ws_bytes, float* o_c, float* lse,
+                                 void* stream) {
   if (!o_c || !aligned16(o_c)) {
     set_error("%s: o_c must be a non-NULL 16-byte aligned pointer", who);
     return MLA_ERR_INVALID_ARG;
   }
   SplitParams p;
-  mla_status st = prepare(who, dims, nullptr, nullptr, nullptr, lengths, 1.f, num_splits,
+  mla_status st = prepare(who, dims, q_len, nullptr, nullptr, nullptr, lengths, 1.f, num_splits,
                           const_cast<void*>(workspace), ws_bytes, nullptr, &p);
   if (st != MLA_OK) return st;
-  launch_pdl(combine_kernel, dim3(dims->heads, dims->batch, kDc / 128), dim3(32), 0,
+  launch_pdl(combine_kernel, dim3(dims->heads, p.B, kDc / 128), dim3(32), 0,
              static_cast<cudaStream_t>(stream), p, o_c, lse);
   return launch_status(who);
+}
+
+extern "C" mla_status mla_decode_split(const mla_dims* dims, const void* q_abs, const void* q_pe,
+                                       const void* cache, const int32_t* lengths,
+                                       float softmax_scale, int32_t num_splits, void* workspace,
+                                       size_t ws_bytes, int32_t* dev_status, void* stream) {
+  return decode_split("mla_decode_split", dims, 1, q_abs, q_pe, cache, lengths, softmax_scale,
+                      num_splits, workspace, ws_bytes, dev_status, stream);
+}
+
+extern "C" mla_status mla_decode_combine(const mla_dims* dims, const int32_t* lengths,
+                                         int32_t num_splits, const void* workspace,
+                                         size_t ws_bytes, float* o_c, float* lse, void* stream) {
+  return decode_combine("mla_decode_combine", dims, 1, lengths, num_splits, workspace, ws_bytes,
+                        o_c, lse, stream);
+}
+
+extern "C" mla_status mla_decode_attn_multi(const mla_dims* dims, int32_t q_len,
+                                            const void* q_abs, const void* q_pe,
+                                            const void* cache, const int32_t* lengths,
+                                            float softmax_scale, int32_t num_splits,
+                                            void* workspace, size_t ws_bytes, float* o_c,
+                                            float* lse, int32_t* dev_status, void* stream) {
+  const char* who = "mla_decode_attn_multi";
+  if (!o_c || !aligned16(o_c)) {
+    set_error("%s: o_c must be a non-NULL 16-byte aligned pointer", who);
+    return MLA_ERR_INVALID_ARG;
+  }
+  // Check everything the combine needs before the split is enqueued.
+  SplitParams p;
+  mla_status st = prepare(who, dims, q_len, q_abs, q_pe, cache, lengths, softmax_scale,
+                          num_splits, workspace, ws_bytes, dev_status, &p);
+  if (st != MLA_OK) return st;
+  st = decode_split(who, dims, q_len, q_abs, q_pe, cache, lengths, softmax_scale, num_splits,
+                    workspace, ws_bytes, dev_status, stream);
+  if (st != MLA_OK) return st;
+  return decode_combine(who, dims, q_len, lengths, num_splits, workspace, ws_bytes, o_c, lse,
+                        stream);
 }
 
 extern "C" mla_status mla_decode_attn(const mla_dims* dims, const void* q_abs, const void* q_pe,
@@ -1097,7 +1147,7 @@ extern "C" mla_status mla_decode_step(const mla_dims* dims, const void* q_nope, 
   // Validate everything before the first launch, so an argument error leaves
   // nothing half-enqueued.
   SplitParams p;
-  st = prepare(who, dims, q_abs, q_pe, cache, lengths, softmax_scale, num_splits, workspace,
+  st = prepare(who, dims, 1, q_abs, q_pe, cache, lengths, softmax_scale, num_splits, workspace,
                ws_bytes, dev_status, &p);
   if (st != MLA_OK) return st;
   st = mla_absorb_q(dims, q_nope, q_rope, w_uk, positions, rope_base, q_abs, q_pe, stream);

@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   // the sequence are finite and get P = 0.
   const int zero_from = len - (r0 + (T - 1) * kF8Rows);
   const bool zero_last = zero_from < kF8Rows;
-  const int row_base = b * p.s_max + r0;
+  const int row_base = cache_seq(p, b) * p.s_max + r0;
   const int h0 = g * kHeadGroup;
 
   // The cache stream starts first: the producer sets up the barriers and
@@ -555,7 +555,7 @@ mla_status launch_split_fp8(const SplitParams& p, const void* cache, cudaStream_
   // The cache [B * s_max rows, 576 bytes] in 128-row x 128-byte boxes (128-byte
   // swizzle); the fifth box of a row reaches past column 576 and reads zeros.
   CUtensorMap tmap;
-  const cuuint64_t gdim[2] = {cuuint64_t(kRow), cuuint64_t(p.B) * p.s_max};
+  const cuuint64_t gdim[2] = {cuuint64_t(kRow), cuuint64_t(p.B / p.q_len) * p.s_max};
   const cuuint64_t gstride[1] = {cuuint64_t(kRow)};
   const cuuint32_t box[2] = {128, cuuint32_t(kF8Rows)};
   const cuuint32_t estride[2] = {1, 1};

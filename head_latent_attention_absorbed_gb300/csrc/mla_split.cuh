@@ -14,7 +14,8 @@ struct SplitParams {
   float* part_o;            // [B, H, splits, 512]: one (b, h)'s chunks contiguous
   float* part_lse;          // [B, H, splits]
   int32_t* status;
-  int B, H, s_max, splits, chunk;
+  int B, H, s_max, splits, chunk;  // B counts query groups: cache sequences x q_len
+  int q_len;                // query tokens per cache sequence (1: ordinary decode)
   float scale_log2;         // softmax_scale * log2(e)
   uint8_t* q_img;           // FP8: the query's E4M3 image per (sequence, head group)
 };
@@ -26,13 +27,24 @@ struct SplitParams {
 constexpr size_t kFp8QBoxes = 5 * 64 * 128;
 constexpr size_t kFp8QImage = kFp8QBoxes + 16 * sizeof(float);
 
-__device__ __forceinline__ int clamp_length(const SplitParams& p, int b, bool report_it) {
-  int len = p.lengths[b];
-  if (len < 1 || len > p.s_max) {
+// Query group v (one token of one sequence) reads cache sequence v / q_len.
+__device__ __forceinline__ int cache_seq(const SplitParams& p, int v) { return v / p.q_len; }
+
+// Rows query group v attends.  Token i of a q_len-token step sits at position
+// lengths[b] - q_len + i (the cache already holds all q_len new rows), and a
+// key past the query's own position is masked ("Transformer and KV Cache
+// Basics", mask design for multi-token decoding), so the token sees the first
+// lengths[b] - (q_len - 1 - i) rows.  A length outside [q_len, s_max] is
+// reported and clamped.
+__device__ __forceinline__ int clamp_length(const SplitParams& p, int v, bool report_it) {
+  int full = p.lengths[v / p.q_len];
+  const int back = p.q_len - 1 - v % p.q_len;
+  if (full < p.q_len || full > p.s_max) {
     if (report_it) report(p.status, MLA_DEV_LENGTH_OUT_OF_RANGE);
-    len = len < 0 ? 0 : (len > p.s_max ? p.s_max : len);
+    full = full < 0 ? 0 : (full > p.s_max ? p.s_max : full);
   }
-  return len;
+  const int len = full - back;
+  return len < 0 ? 0 : len;
 }
 
 // The FP8 (E4M3) cache's split kernel (mla_fp8.cu): same grid, partials and

@@ -183,6 +183,42 @@ mla_status mla_decode_combine(const mla_dims* dims, const int32_t* lengths, int3
                               float* lse, void* stream);
 
 /*
+ * mla_decode_attn_multi -- mla_decode_attn for q_len new tokens per sequence
+ * in one step (multi-token or speculative decoding).
+ *
+ * The cache already holds the step's q_len new rows, so for sequence b with
+ * S_b = lengths[b] rows, token i (0 <= i < q_len) sits at position
+ * S_b - q_len + i and attends rows t <= S_b - q_len + i: a key past the
+ * query's own position is masked ("Transformer and KV Cache Basics", mask
+ * design for multi-token decoding: prefill and decode handled alike, the
+ * small upper-right triangle of the score matrix masked).  Each token's
+ * score, softmax and latent output are those of mla_decode_attn with the
+ * sequence cut to its first S_b - q_len + 1 + i rows; with q_len = 1 this is
+ * mla_decode_attn exactly.
+ *
+ * Query-side tensors have one row per (sequence, token): row b*q_len + i.
+ *   q_abs [B*q_len, H, d_c] fp32      q_pe [B*q_len, H, d_rope] fp32
+ *   o_c   [B*q_len, H, d_c] fp32 (out) lse [B*q_len, H] fp32 (out, may be NULL)
+ * (mla_absorb_q and mla_out_proj called with batch B*q_len and positions
+ * S_b - q_len + i produce and consume them.)
+ * dims  describes the cache: dims->batch = B sequences, cache
+ *       [B, s_max, d_c + d_rope]; lengths [B] int32 (device),
+ *       q_len <= lengths[b] <= s_max
+ * q_len >= 1
+ * workspace  >= mla_decode_workspace_bytes(dims', num_splits) bytes, where
+ *       dims' is dims with batch = B*q_len (mla_decode_num_splits(dims',
+ *       num_splits) gives the chunk count used).
+ * A length below q_len or above s_max sets MLA_DEV_LENGTH_OUT_OF_RANGE in
+ * dev_status; a token left with no rows gets o_c = 0 and lse = -inf.
+ * Each token streams its rows separately (the q_len reads of a row meet in L2).
+ */
+mla_status mla_decode_attn_multi(const mla_dims* dims, int32_t q_len, const void* q_abs,
+                                 const void* q_pe, const void* cache, const int32_t* lengths,
+                                 float softmax_scale, int32_t num_splits, void* workspace,
+                                 size_t workspace_bytes, float* o_c, float* lse,
+                                 int32_t* dev_status, void* stream);
+
+/*
  * mla_decode_attn_noalloc -- mla_decode_attn for callers that cannot allocate
  * device memory.  The paper has no counterpart: it is a convenience of this
  * library.
