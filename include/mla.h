@@ -87,7 +87,7 @@ typedef struct mla_dims {
 } mla_dims;
 
 /* Bits a kernel ORs into the optional device status word (see mla_decode_attn). */
-#define MLA_DEV_LENGTH_OUT_OF_RANGE 1  /* some lengths[b] < 1 or > s_max        */
+#define MLA_DEV_LENGTH_OUT_OF_RANGE 1  /* some lengths[b] < 1 (< q_len) or > s_max */
 #define MLA_DEV_PIPELINE_TIMEOUT 2     /* a bounded wait on a TMA copy gave up  */
 
 /*
