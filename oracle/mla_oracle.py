@@ -271,6 +271,75 @@ def output_projection(o: np.ndarray, w_o: np.ndarray) -> np.ndarray:
     return o.reshape(o.shape[0], -1) @ np.asarray(w_o, dtype=np.float64).T
 
 
+# ----------------------------------------------------------------------------- materialised absorption
+def materialize_wkq(w_q_nope: np.ndarray, w_uk: np.ndarray) -> np.ndarray:
+    """W^KQ_h = (W^UK_h)^T W^UQ_h for every head h: the absorption's query-side
+    product written out once as a matrix ("Multi-Head Latent Attention", 3.3: the
+    dimensional analysis gives W^KQ one d_c-row slice per head; 3.5 forms it by a
+    batched product of W^UK transposed with W^UQ; "Deepseek V2 Lite Inference Engine
+    in C", MLA notes: the materialised WukWq of shape (16, 2048, 512)).
+
+    w_q_nope: [H, d_nope, d_in], the rows of the query projection whose output meets
+    the latent keys (q_nope = w_q_nope[h] x); w_uk: [H, d_nope, d_c].
+    Returns [H, d_c, d_in]: q_abs[b, h, :] = W^KQ[h] x_b.
+    """
+    w_q_nope = np.asarray(w_q_nope, dtype=np.float64)
+    w_uk = np.asarray(w_uk, dtype=np.float64)
+    H, d_nope, d_c = w_uk.shape
+    out = np.empty((H, d_c, w_q_nope.shape[2]))
+    for h in range(H):
+        out[h] = w_uk[h].T @ w_q_nope[h]
+    return out
+
+
+def materialize_wov(w_o: np.ndarray, w_uv: np.ndarray) -> np.ndarray:
+    """W^OV = W^O W^UV with the head dimension kept ("Multi-Head Latent Attention",
+    eq. 3.3.3, Y = W^O V Z = W^OV C^KV Z; 3.5 reshapes W^O to (d_out, d_h, H) and
+    multiplies each head's block by W^UV of that head): column block h of W^OV
+    (d_c wide) is W^O's column block h (d_v wide) times W^UV_h.
+
+    w_o: [d_out, H * d_v]; w_uv: [H, d_v, d_c].  Returns [d_out, H * d_c].
+    """
+    w_o = np.asarray(w_o, dtype=np.float64)
+    w_uv = np.asarray(w_uv, dtype=np.float64)
+    H, d_v, d_c = w_uv.shape
+    out = np.empty((w_o.shape[0], H * d_c))
+    for h in range(H):
+        out[:, h * d_c:(h + 1) * d_c] = w_o[:, h * d_v:(h + 1) * d_v] @ w_uv[h]
+    return out
+
+
+def decode_materialized(x, q_rope, w_kq, w_ov, cache, lengths, positions,
+                        scale: float, base: float):
+    """One decode step in the materialised absorbed form: the absorbed query is
+    W^KQ x (no q_nope in between), the latent attention is that of the absorbed
+    form (3.3, 3.6), and the layer output is W^OV applied to the heads' latent
+    outputs concatenated (eq. 3.3.3).
+
+    x: [B, d_in]; q_rope: [B, H, d_rope]; w_kq: [H, d_c, d_in]; w_ov: [d_out, H*d_c].
+    Returns dict(q_abs [B,H,d_c], q_pe [B,H,d_rope], o_c [B,H,d_c], lse [B,H],
+    y [B, d_out]).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    w_kq = np.asarray(w_kq, dtype=np.float64)
+    H, d_c, _ = w_kq.shape
+    B = x.shape[0]
+    q_abs = np.einsum("hci,bi->bhc", w_kq, x)
+    q_pe = apply_rope(q_rope, np.asarray(positions)[:, None], base)
+    o_c = np.zeros((B, H, d_c))
+    lse = np.full((B, H), -np.inf)
+    for b in range(B):
+        n = int(lengths[b])
+        if n <= 0:
+            raise ValueError("a sequence with no cached rows has no softmax")
+        c, kr = cache[b, :n, :d_c], cache[b, :n, d_c:]
+        s = scale * (q_abs[b] @ c.T + q_pe[b] @ kr.T)
+        p, lse[b] = softmax_stats(s)
+        o_c[b] = p @ c
+    y = o_c.reshape(B, H * d_c) @ np.asarray(w_ov, dtype=np.float64).T
+    return dict(q_abs=q_abs, q_pe=q_pe, o_c=o_c, lse=lse, y=y)
+
+
 # ----------------------------------------------------------------------------- FP8 cache elements
 def e4m3_to_float64(codes) -> np.ndarray:
     """Values of FP8 E4M3 codes ("Multi-Head Latent Attention" 3.1: a cached element

@@ -441,3 +441,80 @@ def test_multi_token_decode_reduces_to_single_token_decode():
                                     0.4, 10000.0)
             for k in ("q_abs", "q_pe", "o_c", "lse", "o"):
                 np.testing.assert_allclose(got[k][b, i], one[k][0], atol=1e-12)
+
+
+# ---------------------------------------------------------------- materialised W^KQ and W^OV
+def _materialized_case(rng, B=2, H=3, d_c=6, d_rope=4, d_nope=4, d_v=5, d_in=7, d_out=9, S=6):
+    a = _rand_case(rng, B=B, H=H, d_c=d_c, d_rope=d_rope, d_nope=d_nope, d_v=d_v, S=S)
+    a["x"] = rng.standard_normal((B, d_in))
+    a["w_q_nope"] = 0.4 * rng.standard_normal((H, d_nope, d_in))
+    a["w_o"] = 0.4 * rng.standard_normal((d_out, H * d_v))
+    # the query's nope part as the model computes it: one d_nope block per head
+    a["q_nope"] = np.einsum("hdi,bi->bhd", a["w_q_nope"], a["x"])
+    return a
+
+
+def test_materialized_weights_brute_force_tiny():
+    """W^KQ[h, c, i] = sum_d W^UK[h, d, c] W^UQ[h, d, i] and
+    W^OV[n, h d_c + c] = sum_e W^O[n, h d_v + e] W^UV[h, e, c], by scalar loops
+    ("Multi-Head Latent Attention", 3.3 and eq. 3.3.3)."""
+    rng = np.random.default_rng(31)
+    H, d_nope, d_c, d_in, d_v, d_out = 2, 3, 4, 5, 3, 4
+    w_q = rng.standard_normal((H, d_nope, d_in))
+    w_uk = rng.standard_normal((H, d_nope, d_c))
+    w_o = rng.standard_normal((d_out, H * d_v))
+    w_uv = rng.standard_normal((H, d_v, d_c))
+    kq = O.materialize_wkq(w_q, w_uk)
+    ov = O.materialize_wov(w_o, w_uv)
+    assert kq.shape == (H, d_c, d_in) and ov.shape == (d_out, H * d_c)
+    for h in range(H):
+        for c in range(d_c):
+            for i in range(d_in):
+                v = 0.0
+                for d in range(d_nope):
+                    v += w_uk[h, d, c] * w_q[h, d, i]
+                assert abs(kq[h, c, i] - v) < 1e-12
+    for n in range(d_out):
+        for h in range(H):
+            for c in range(d_c):
+                v = 0.0
+                for e in range(d_v):
+                    v += w_o[n, h * d_v + e] * w_uv[h, e, c]
+                assert abs(ov[n, h * d_c + c] - v) < 1e-12
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_materialized_equals_absorbed_and_naive(seed):
+    """The materialised form (W^KQ x, then W^OV on the latent outputs) gives the
+    absorbed form's q_abs, o_c and lse, and W^O applied to the naive form's head
+    outputs, to 1e-10: the absorption is associativity ("Multi-Head Latent
+    Attention", 3.3 and eq. 3.3.3)."""
+    rng = np.random.default_rng(40 + seed)
+    a = _materialized_case(rng)
+    ab = O.decode_absorbed(a["q_nope"], a["q_rope"], a["w_uk"], a["w_uv"], a["cache"],
+                           a["lengths"], a["positions"], 0.37, 10000.0)
+    nv = O.decode_naive(a["q_nope"], a["q_rope"], a["w_uk"], a["w_uv"], a["cache"],
+                        a["lengths"], a["positions"], 0.37, 10000.0)
+    m = O.decode_materialized(a["x"], a["q_rope"], O.materialize_wkq(a["w_q_nope"], a["w_uk"]),
+                              O.materialize_wov(a["w_o"], a["w_uv"]), a["cache"], a["lengths"],
+                              a["positions"], 0.37, 10000.0)
+    for k in ("q_abs", "q_pe", "o_c", "lse"):
+        np.testing.assert_allclose(m[k], ab[k], atol=1e-10)
+    np.testing.assert_allclose(m["y"], O.output_projection(nv["o"], a["w_o"]), atol=1e-10)
+
+
+def test_pins_catch_a_misplaced_wov_block(monkeypatch):
+    """A W^OV whose head blocks are taken from the wrong head fails the pin above."""
+    real = O.materialize_wov
+
+    def wrong(w_o, w_uv):
+        return real(w_o, np.asarray(w_uv)[::-1])
+    rng = np.random.default_rng(44)
+    a = _materialized_case(rng)
+    monkeypatch.setattr(O, "materialize_wov", wrong)
+    nv = O.decode_naive(a["q_nope"], a["q_rope"], a["w_uk"], a["w_uv"], a["cache"],
+                        a["lengths"], a["positions"], 0.37, 10000.0)
+    m = O.decode_materialized(a["x"], a["q_rope"], O.materialize_wkq(a["w_q_nope"], a["w_uk"]),
+                              O.materialize_wov(a["w_o"], a["w_uv"]), a["cache"], a["lengths"],
+                              a["positions"], 0.37, 10000.0)
+    assert np.max(np.abs(m["y"] - O.output_projection(nv["o"], a["w_o"]))) > 1e-3

@@ -152,3 +152,26 @@ def make_wo_inputs(cfg: MlaConfig, seed: int = 0) -> OutProjInputs:
     o = torch.randn((cfg.batch, cfg.heads, cfg.d_v), generator=g, dtype=torch.float32)
     w = torch.randn((cfg.hidden, cfg.heads * cfg.d_v), generator=g, dtype=torch.float32) * cfg.weight_std
     return OutProjInputs(cfg=cfg, o=o, w_o=w.to(_storage(cfg)))
+
+
+@dataclass
+class MaterializedInputs:
+    base: MlaInputs          # cache, q_rope, w_uk, w_uv, lengths, positions (q_nope unused)
+    x: torch.Tensor          # [B, hidden] storage dtype: the decoded tokens' hidden states
+    w_q_nope: torch.Tensor   # [H, d_nope, hidden] storage dtype: the nope rows of q_proj per head
+    w_o: torch.Tensor        # [hidden, H * d_v] storage dtype
+
+
+def make_materialized_inputs(cfg: MlaConfig, seed: int = 0, **kw) -> MaterializedInputs:
+    """Inputs of the materialised (W^KQ, W^OV) step: ``make_inputs(cfg, seed, **kw)``,
+    then, from a second CPU generator seeded with 10000 + seed, x ~ N(0, 1),
+    W_Q's nope rows ~ N(0, std^2) and W_O ~ N(0, std^2), in that order."""
+    base = make_inputs(cfg, seed, **kw)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(10000 + seed)
+    st = _storage(cfg)
+    B, H = cfg.batch, cfg.heads
+    x = torch.randn((B, cfg.hidden), generator=g, dtype=torch.float32)
+    wq = torch.randn((H, cfg.d_nope, cfg.hidden), generator=g, dtype=torch.float32) * cfg.weight_std
+    wo = torch.randn((cfg.hidden, H * cfg.d_v), generator=g, dtype=torch.float32) * cfg.weight_std
+    return MaterializedInputs(base=base, x=x.to(st), w_q_nope=wq.to(st), w_o=wo.to(st))
