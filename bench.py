@@ -54,7 +54,8 @@ def parse(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="step", choices=["step", "cache_append", "wo_proj"],
+    ap.add_argument("--op", default="step",
+                    choices=["step", "cache_append", "wo_proj", "kq_proj", "ov_proj"],
                     help="step: the decode step (default); cache_append / wo_proj: the steps "
                          "around it, timed alone on the workload's sizes")
     return ap.parse_args(argv)
@@ -282,13 +283,16 @@ def whole_job_rate(units_per_rank_step: float, steps: int, world: int, seconds: 
 
 # ----------------------------------------------------------------------------- around the step
 def run_op(args, cfg, rank):
-    """Time mla_cache_append or mla_wo_proj alone on the workload's sizes: K launches
+    """Time mla_cache_append, mla_wo_proj, or the materialised projections
+    (mla_absorb_q_materialized: x . W^KQ and RoPE; mla_ov_proj: W^OV on o_c) alone
+    on the workload's sizes: K launches
     in one CUDA graph over L rotating weight copies (more than 3x L2), CUDA events
     around the replay.  The dominant bytes are the weight's; the line reports them
     per second against the measured HBM peak."""
     import torch
     import head_latent_attention_absorbed_gb300 as mla
-    from workloads import cache_storage, make_append_inputs, make_wo_inputs
+    from workloads import (cache_storage, make_append_inputs, make_materialized_inputs,
+                           make_wo_inputs)
     mla.load()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -306,6 +310,35 @@ def run_op(args, cfg, rank):
         moved = wbytes + x.numel() * x.element_size() + cfg.batch * cfg.row * cache.element_size()
         launch = lambda k: mla.cache_append(d, x, ws[k % L], pos, cache, cfg.rope_base, status)
         metric = "cache append: kv_a_proj weight + token + row bytes per second"
+    elif args.op in ("kq_proj", "ov_proj"):
+        m = make_materialized_inputs(cfg, seed=0)
+        wdt = m.w_o.dtype
+        H = cfg.heads
+        if args.op == "kq_proj":
+            w0 = torch.empty((H * cfg.d_c, cfg.hidden), dtype=wdt, device=dev)
+            mla.materialize_wkq(d, m.w_q_nope.to(dev), m.base.w_uk.to(dev), w0)
+        else:
+            w0 = torch.empty((cfg.hidden, H * cfg.d_c), dtype=wdt, device=dev)
+            mla.materialize_wov(d, m.w_o.to(dev), m.base.w_uv.to(dev), w0)
+        wbytes = w0.numel() * w0.element_size()
+        L = max(2, math.ceil(3 * l2 / wbytes))
+        ws = [w0.clone() for _ in range(L)]
+        x = m.x.to(dev)
+        q_rope, pos = m.base.q_rope.to(dev), m.base.positions.to(dev)
+        q_abs = torch.empty((cfg.batch, H, cfg.d_c), dtype=torch.float32, device=dev)
+        q_pe = torch.empty((cfg.batch, H, cfg.d_rope), dtype=torch.float32, device=dev)
+        o_c = torch.randn((cfg.batch, H, cfg.d_c), generator=torch.Generator().manual_seed(0)).to(dev)
+        y = torch.empty((cfg.batch, cfg.hidden), dtype=torch.float32, device=dev)
+        if args.op == "kq_proj":
+            moved = (wbytes + x.numel() * x.element_size() + q_abs.numel() * 4 +
+                     q_rope.numel() * q_rope.element_size() + q_pe.numel() * 4)
+            launch = lambda k: mla.absorb_q_materialized(d, x, ws[k % L], q_rope, pos, q_abs, q_pe,
+                                                         cfg.rope_base)
+            metric = "materialised absorb: W^KQ weight + x + q bytes per second"
+        else:
+            moved = wbytes + o_c.numel() * 4 + y.numel() * 4
+            launch = lambda k: mla.ov_proj(d, o_c, ws[k % L], y)
+            metric = "materialised output: W^OV weight + o_c + y bytes per second"
     else:
         inp = make_wo_inputs(cfg, seed=0)
         wbytes = inp.w_o.numel() * inp.w_o.element_size()

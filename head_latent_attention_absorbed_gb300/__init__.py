@@ -13,13 +13,15 @@ from typing import Optional
 from ._binding import (EXPORTED, LIB_PATH, MLA_BF16, MLA_FP8_E4M3, MLA_DEV_LENGTH_OUT_OF_RANGE,
                        MLA_DEV_PIPELINE_TIMEOUT, MLA_F32, MlaDims, MlaError, absorb_q, cache_append,
                        decode_attn, decode_attn_multi, query_dims, wo_proj,
+                       materialize_wkq, materialize_wov, absorb_q_materialized, ov_proj,
                        decode_attn_noalloc, decode_combine, decode_split, decode_step, dims,
                        dtype_code, load, num_splits, out_proj, workspace_bytes)
 
 __all__ = [
     "EXPORTED", "LIB_PATH", "MLA_BF16", "MLA_F32", "MLA_FP8_E4M3", "MLA_DEV_LENGTH_OUT_OF_RANGE",
     "MLA_DEV_PIPELINE_TIMEOUT", "MlaDims", "MlaError", "absorb_q", "decode_attn",
-    "decode_attn_multi", "query_dims",
+    "decode_attn_multi", "query_dims", "materialize_wkq", "materialize_wov",
+    "absorb_q_materialized", "ov_proj",
     "decode_attn_noalloc", "decode_split", "decode_combine", "decode_step", "dims",
     "dtype_code", "load", "num_splits", "out_proj", "workspace_bytes", "DecodeStep", "HostStep",
     "cache_append", "wo_proj",

@@ -22,7 +22,8 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
 EXPORTED = ("mla_absorb_q", "mla_decode_num_splits", "mla_decode_workspace_bytes",
             "mla_decode_attn", "mla_decode_split", "mla_decode_combine",
             "mla_decode_attn_noalloc", "mla_decode_attn_multi", "mla_decode_step", "mla_out_proj", "mla_cache_append",
-            "mla_wo_proj",
+            "mla_wo_proj", "mla_materialize_wkq", "mla_materialize_wov",
+            "mla_absorb_q_materialized", "mla_ov_proj",
             "mla_status_string", "mla_last_error_message")
 
 
@@ -76,6 +77,14 @@ def load(path: Optional[str] = None):
     lib.mla_cache_append.restype = ctypes.c_int
     lib.mla_wo_proj.argtypes = [D, I32, P, P, P, P]
     lib.mla_wo_proj.restype = ctypes.c_int
+    lib.mla_materialize_wkq.argtypes = [D, I32, P, P, P, P]
+    lib.mla_materialize_wkq.restype = ctypes.c_int
+    lib.mla_materialize_wov.argtypes = [D, I32, P, P, P, P]
+    lib.mla_materialize_wov.restype = ctypes.c_int
+    lib.mla_absorb_q_materialized.argtypes = [D, I32, P, P, P, P, ctypes.c_double, P, P, P]
+    lib.mla_absorb_q_materialized.restype = ctypes.c_int
+    lib.mla_ov_proj.argtypes = [D, I32, P, P, P, P]
+    lib.mla_ov_proj.restype = ctypes.c_int
     lib.mla_out_proj.argtypes = [D, P, P, P, P]
     lib.mla_out_proj.restype = ctypes.c_int
     lib.mla_status_string.argtypes = [ctypes.c_int]
@@ -248,4 +257,35 @@ def wo_proj(d: MlaDims, o, w_o, y, stream=None) -> None:
     """y = concat_h(o[:, h, :]) . W_O^T."""
     _cuda_contig(o, w_o, y)
     _check(load().mla_wo_proj(ctypes.byref(d), int(w_o.shape[0]), _ptr(o), _ptr(w_o), _ptr(y),
+                              _stream(stream)))
+
+
+def materialize_wkq(d: MlaDims, w_q_nope, w_uk, w_kq, stream=None) -> None:
+    """W^KQ[h*512 + c, i] = sum_d w_uk[h, d, c] w_q_nope[h, d, i] (once per model)."""
+    _cuda_contig(w_q_nope, w_uk, w_kq)
+    _check(load().mla_materialize_wkq(ctypes.byref(d), int(w_q_nope.shape[-1]), _ptr(w_q_nope),
+                                      _ptr(w_uk), _ptr(w_kq), _stream(stream)))
+
+
+def materialize_wov(d: MlaDims, w_o, w_uv, w_ov, stream=None) -> None:
+    """W^OV[n, h*512 + c] = sum_e w_o[n, h*128 + e] w_uv[h, e, c] (once per model)."""
+    _cuda_contig(w_o, w_uv, w_ov)
+    _check(load().mla_materialize_wov(ctypes.byref(d), int(w_o.shape[0]), _ptr(w_o), _ptr(w_uv),
+                                      _ptr(w_ov), _stream(stream)))
+
+
+def absorb_q_materialized(d: MlaDims, x, w_kq, q_rope, positions, q_abs, q_pe,
+                          rope_base: float = 10000.0, stream=None) -> None:
+    """q_abs = W^KQ x per head; q_pe = RoPE(q_rope, positions)."""
+    _cuda_contig(x, w_kq, q_rope, positions, q_abs, q_pe)
+    _check(load().mla_absorb_q_materialized(ctypes.byref(d), int(x.shape[-1]), _ptr(x),
+                                            _ptr(w_kq), _ptr(q_rope), _ptr(positions),
+                                            float(rope_base), _ptr(q_abs), _ptr(q_pe),
+                                            _stream(stream)))
+
+
+def ov_proj(d: MlaDims, o_c, w_ov, y, stream=None) -> None:
+    """y = W^OV . concat_h(o_c[:, h, :])."""
+    _cuda_contig(o_c, w_ov, y)
+    _check(load().mla_ov_proj(ctypes.byref(d), int(w_ov.shape[0]), _ptr(o_c), _ptr(w_ov), _ptr(y),
                               _stream(stream)))

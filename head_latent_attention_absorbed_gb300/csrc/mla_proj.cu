@@ -289,6 +289,86 @@ __global__ void __launch_bounds__(256) rowgemm_f32_kernel(const RowGemmArgs a, c
   }
 }
 
+// ---------------------------------------------------------------------- materialised weights
+// out(h, m, n) = sum_{k < K} A(h, m, k) B(h, k, n), accumulated in fp32 and rounded
+// once to T: one head's slice of W^KQ = (W^UK)^T W^UQ or of W^OV = W^O W^UV
+// ("Multi-Head Latent Attention" 3.3, eq. 3.3.3 and 3.5).  A is addressed by
+// strides (either its m or its k stride is 1), B and out have unit n stride.
+// A weight transform made once per model, not per step: a plain SIMT tiling,
+// 64 x 64 outputs per CTA, 4 x 4 per thread, K staged 64 at a time.
+struct MatArgs {
+  const void* a;
+  long long a_h, a_m, a_k;
+  const void* b;
+  long long b_h, b_k;
+  void* out;
+  long long o_h, o_m;
+  int M, N, K;
+};
+
+template <typename T>
+__device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+template <typename T>
+__global__ void __launch_bounds__(256) materialize_kernel(const MatArgs p) {
+  __shared__ float As[64][65], Bs[64][64];
+  const int h = blockIdx.z, m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const T* a = static_cast<const T*>(p.a) + h * p.a_h;
+  const T* b = static_cast<const T*>(p.b) + h * p.b_h;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < p.K; k0 += 64) {
+    for (int idx = tid; idx < 64 * 64; idx += 256) {
+      // walk A along its unit stride so that neighbouring threads read neighbouring words
+      const int m = p.a_m == 1 ? idx & 63 : idx >> 6, k = p.a_m == 1 ? idx >> 6 : idx & 63;
+      const bool in = m0 + m < p.M && k0 + k < p.K;
+      As[k][m] = in ? to_f(a[(m0 + m) * p.a_m + (k0 + k) * p.a_k]) : 0.f;
+      const int kb = idx >> 6, nb = idx & 63;
+      const bool inb = k0 + kb < p.K && n0 + nb < p.N;
+      Bs[kb][nb] = inb ? to_f(b[(k0 + kb) * p.b_k + n0 + nb]) : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int k = 0; k < 64; ++k) {
+      float av[4], bv[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        av[i] = As[k][4 * ty + i];
+        bv[i] = Bs[k][4 * tx + i];
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  T* out = static_cast<T*>(p.out) + h * p.o_h;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int m = m0 + 4 * ty + i, n = n0 + 4 * tx + j;
+      if (m < p.M && n < p.N) out[m * p.o_m + n] = from_f<T>(acc[i][j]);
+    }
+}
+
+// q_pe[b, h, :] = RoPE(q_rope[b, h, :], positions[b]): one pair per thread.
+template <typename T>
+__global__ void __launch_bounds__(256) rope_q_kernel(const T* __restrict__ q_rope,
+                                                     const int32_t* __restrict__ pos,
+                                                     const RopeTheta th, float* __restrict__ q_pe,
+                                                     int B, int H) {
+  const int it = blockIdx.x * 256 + threadIdx.x;
+  if (it >= B * H * (kDr / 2)) return;
+  const int i = it % (kDr / 2), h = (it / (kDr / 2)) % H, b = it / (H * (kDr / 2));
+  rope_pair(q_rope, pos, th, q_pe, H, h, b * (kDr / 2) + i);
+}
+
 }  // namespace
 }  // namespace mla
 
@@ -463,5 +543,185 @@ extern "C" mla_status mla_wo_proj(const mla_dims* dims, int32_t hidden, const fl
     const int warps = a.B * hidden / 2;
     rowgemm_f32_kernel<kWriteY><<<(warps + 7) / 8, 256, 0, s>>>(a, th, static_cast<const float*>(w_o));
   }
+  return launch_status(who);
+}
+
+// ------------------------------------------------------------------ materialised absorption
+static mla_status materialize(const char* who, const mla_dims* dims, const MatArgs& a,
+                              cudaStream_t s) {
+  const dim3 grid((a.N + 63) / 64, (a.M + 63) / 64, dims->heads);
+  if (dims->dtype == MLA_F32)
+    materialize_kernel<float><<<grid, 256, 0, s>>>(a);
+  else
+    materialize_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(a);
+  return launch_status(who);
+}
+
+extern "C" mla_status mla_materialize_wkq(const mla_dims* dims, int32_t d_in,
+                                          const void* w_q_nope, const void* w_uk, void* w_kq,
+                                          void* stream) {
+  const char* who = "mla_materialize_wkq";
+  mla_status st = check_dims(dims, who);
+  if (st != MLA_OK) return st;
+  if (!w_q_nope || !w_uk || !w_kq || !aligned16(w_q_nope) || !aligned16(w_uk) ||
+      !aligned16(w_kq)) {
+    set_error("%s: w_q_nope, w_uk and w_kq must be non-NULL 16-byte aligned pointers", who);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (d_in <= 0) {
+    set_error("%s: d_in = %d must be positive", who, d_in);
+    return MLA_ERR_INVALID_ARG;
+  }
+  // W^KQ[h, c, i] = sum_d W^UK[h, d, c] W^UQ[h, d, i]
+  MatArgs a{};
+  a.a = w_uk;
+  a.a_h = static_cast<long long>(kDn) * kDc;
+  a.a_m = 1;
+  a.a_k = kDc;
+  a.b = w_q_nope;
+  a.b_h = static_cast<long long>(kDn) * d_in;
+  a.b_k = d_in;
+  a.out = w_kq;
+  a.o_h = static_cast<long long>(kDc) * d_in;
+  a.o_m = d_in;
+  a.M = kDc;
+  a.N = d_in;
+  a.K = kDn;
+  return materialize(who, dims, a, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" mla_status mla_materialize_wov(const mla_dims* dims, int32_t d_out, const void* w_o,
+                                          const void* w_uv, void* w_ov, void* stream) {
+  const char* who = "mla_materialize_wov";
+  mla_status st = check_dims(dims, who);
+  if (st != MLA_OK) return st;
+  if (!w_o || !w_uv || !w_ov || !aligned16(w_o) || !aligned16(w_uv) || !aligned16(w_ov)) {
+    set_error("%s: w_o, w_uv and w_ov must be non-NULL 16-byte aligned pointers", who);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (d_out <= 0) {
+    set_error("%s: d_out = %d must be positive", who, d_out);
+    return MLA_ERR_INVALID_ARG;
+  }
+  // W^OV[n, h d_c + c] = sum_e W^O[n, h d_v + e] W^UV[h, e, c]
+  const long long H = dims->heads;
+  MatArgs a{};
+  a.a = w_o;
+  a.a_h = kDv;
+  a.a_m = H * kDv;
+  a.a_k = 1;
+  a.b = w_uv;
+  a.b_h = static_cast<long long>(kDv) * kDc;
+  a.b_k = kDc;
+  a.out = w_ov;
+  a.o_h = kDc;
+  a.o_m = H * kDc;
+  a.M = d_out;
+  a.N = kDc;
+  a.K = kDv;
+  return materialize(who, dims, a, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" mla_status mla_absorb_q_materialized(const mla_dims* dims, int32_t d_in, const void* x,
+                                                const void* w_kq, const void* q_rope,
+                                                const int32_t* positions, double rope_base,
+                                                float* q_abs, float* q_pe, void* stream) {
+  const char* who = "mla_absorb_q_materialized";
+  mla_status st = check_dims(dims, who);
+  if (st != MLA_OK) return st;
+  if (!x || !w_kq || !q_rope || !positions || !q_abs || !q_pe) {
+    set_error("%s: a required pointer is NULL", who);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (!aligned16(x) || !aligned16(w_kq) || !aligned16(q_rope) || !aligned16(q_abs) ||
+      !aligned16(q_pe)) {
+    set_error("%s: tensor pointers must be 16-byte aligned", who);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (d_in <= 0 || d_in % 64 != 0) {
+    set_error("%s: d_in = %d must be a positive multiple of 64", who, d_in);
+    return d_in <= 0 ? MLA_ERR_INVALID_ARG : MLA_ERR_UNSUPPORTED;
+  }
+  if (!(rope_base > 0.0) || !isfinite(rope_base)) {
+    set_error("%s: rope_base must be finite and > 0", who);
+    return MLA_ERR_INVALID_ARG;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int B = dims->batch, H = dims->heads;
+  RopeTheta th;
+  for (int i = 0; i < kDr / 2; ++i) th.turns[i] = pow(rope_base, -2.0 * i / kDr) / (2.0 * M_PI);
+  // q_abs [B, H * d_c] = x . W^KQ^T, W^KQ stored [H * d_c, d_in]
+  if (dims->dtype != MLA_F32) {
+    WStreamJob j{};
+    j.mode = kWsWriteY;
+    j.x_f32 = false;
+    j.x = x;
+    j.w = w_kq;
+    j.B = B;
+    j.K = d_in;
+    j.N = H * kDc;
+    j.y = q_abs;
+    st = wstream_launch(j, s, who);
+    if (st != MLA_OK) return st;
+  } else {
+    RowGemmArgs a{};
+    a.x = x;
+    a.B = B;
+    a.K = d_in;
+    a.N = H * kDc;
+    a.y = q_abs;
+    const int warps = a.B * a.N / 2;
+    RopeTheta none{};
+    rowgemm_f32_kernel<kWriteY><<<(warps + 7) / 8, 256, 0, s>>>(a, none,
+                                                               static_cast<const float*>(w_kq));
+    st = launch_status(who);
+    if (st != MLA_OK) return st;
+  }
+  const int pairs = B * H * (kDr / 2);
+  if (dims->dtype == MLA_F32)
+    rope_q_kernel<float><<<(pairs + 255) / 256, 256, 0, s>>>(static_cast<const float*>(q_rope),
+                                                             positions, th, q_pe, B, H);
+  else
+    rope_q_kernel<__nv_bfloat16><<<(pairs + 255) / 256, 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(q_rope), positions, th, q_pe, B, H);
+  return launch_status(who);
+}
+
+extern "C" mla_status mla_ov_proj(const mla_dims* dims, int32_t d_out, const float* o_c,
+                                  const void* w_ov, float* y, void* stream) {
+  const char* who = "mla_ov_proj";
+  mla_status st = check_dims(dims, who);
+  if (st != MLA_OK) return st;
+  if (!o_c || !w_ov || !y || !aligned16(o_c) || !aligned16(w_ov) || !aligned16(y)) {
+    set_error("%s: o_c, w_ov and y must be non-NULL 16-byte aligned pointers", who);
+    return MLA_ERR_INVALID_ARG;
+  }
+  if (d_out <= 0 || d_out % 8 != 0) {
+    set_error("%s: d_out = %d must be a positive multiple of 8", who, d_out);
+    return d_out <= 0 ? MLA_ERR_INVALID_ARG : MLA_ERR_UNSUPPORTED;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // y [B, d_out] = concat_h(o_c[:, h, :]) . W^OV^T, W^OV stored [d_out, H * d_c]
+  if (dims->dtype != MLA_F32) {
+    WStreamJob j{};
+    j.mode = kWsWriteY;
+    j.x_f32 = true;
+    j.x = o_c;
+    j.w = w_ov;
+    j.B = dims->batch;
+    j.K = dims->heads * kDc;
+    j.N = d_out;
+    j.y = y;
+    return wstream_launch(j, s, who);
+  }
+  RowGemmArgs a{};
+  a.x = o_c;
+  a.B = dims->batch;
+  a.K = dims->heads * kDc;
+  a.N = d_out;
+  a.y = y;
+  RopeTheta none{};
+  const int warps = a.B * d_out / 2;
+  rowgemm_f32_kernel<kWriteY><<<(warps + 7) / 8, 256, 0, s>>>(a, none, static_cast<const float*>(w_ov));
   return launch_status(who);
 }

@@ -302,6 +302,50 @@ mla_status mla_wo_proj(const mla_dims* dims, int32_t hidden, const float* o, con
                        float* y, void* stream);
 
 /*
+ * Materialised absorption: the pages' other form of the weight absorption,
+ * where the products of the weights are formed once as matrices instead of
+ * being applied right to left at every step ("Multi-Head Latent Attention"
+ * 3.3, eq. 3.3.3 and 3.5; "Deepseek V2 Lite Inference Engine in C", MLA
+ * notes: the materialised WukWq, per head).  With them a step is
+ *   mla_absorb_q_materialized -> mla_decode_attn -> mla_ov_proj
+ * and needs neither q_nope nor mla_out_proj nor mla_wo_proj.  The materialised
+ * matrices are larger than the factors they come from (W^KQ holds H d_c d_in
+ * values against H d_nope (d_c + d_in)); their rows are streamed once per step.
+ *
+ * mla_materialize_wkq -- W^KQ[h, c, i] = sum_{d < d_nope} w_uk[h, d, c] w_q_nope[h, d, i]
+ *   w_q_nope [H, d_nope, d_in] dtype: the rows of the query projection whose
+ *            output is q_nope (q_nope[b, h, :] = w_q_nope[h] . x[b, :])
+ *   w_uk     [H, d_nope, d_c] dtype
+ *   w_kq     [H * d_c, d_in] dtype (out): row h d_c + c is W^KQ[h, c, :]
+ * mla_materialize_wov -- W^OV[n, h d_c + c] = sum_{e < d_v} w_o[n, h d_v + e] w_uv[h, e, c]
+ *   w_o  [d_out, H * d_v] dtype     w_uv [H, d_v, d_c] dtype
+ *   w_ov [d_out, H * d_c] dtype (out)
+ * Both accumulate in fp32 and round each result once to the weight type
+ * (nearest even for bf16; MLA_FP8_E4M3 means bf16 weights).  They are weight
+ * transforms made once per model.
+ *
+ * mla_absorb_q_materialized -- the absorbed query straight from the hidden state:
+ *   q_abs[b, h, c] = sum_{i < d_in} w_kq[h d_c + c, i] x[b, i]     (fp32 accumulation)
+ *   q_pe = RoPE(q_rope, positions) exactly as mla_absorb_q computes it.
+ *   x [B, d_in] dtype; d_in a multiple of 64.  Other arguments as mla_absorb_q.
+ *
+ * mla_ov_proj -- the layer output straight from the latent attention output:
+ *   y[b, n] = sum_{h, c} w_ov[n, h d_c + c] o_c[b, h, c]            (fp32 accumulation)
+ *   o_c [B, H, d_c] fp32 (mla_decode_attn's result); y [B, d_out] fp32 (out);
+ *   d_out a multiple of 8.
+ */
+mla_status mla_materialize_wkq(const mla_dims* dims, int32_t d_in, const void* w_q_nope,
+                               const void* w_uk, void* w_kq, void* stream);
+mla_status mla_materialize_wov(const mla_dims* dims, int32_t d_out, const void* w_o,
+                               const void* w_uv, void* w_ov, void* stream);
+mla_status mla_absorb_q_materialized(const mla_dims* dims, int32_t d_in, const void* x,
+                                     const void* w_kq, const void* q_rope,
+                                     const int32_t* positions, double rope_base, float* q_abs,
+                                     float* q_pe, void* stream);
+mla_status mla_ov_proj(const mla_dims* dims, int32_t d_out, const float* o_c, const void* w_ov,
+                       float* y, void* stream);
+
+/*
  * mla_decode_step -- one whole decode step: mla_absorb_q, mla_decode_attn and
  * mla_out_proj in one call, with the same arguments, meanings and results
  * (q_abs, q_pe, o_c, lse and out are all written).
