@@ -773,6 +773,9 @@ __global__ void __launch_bounds__(128)
     asm volatile("prefetch.global.L2 [%0];" ::"l"(wslice + 8 * (tid + 128 * i)));
   const int len = clamp_length(p, b, false);   // a caller input, not the split's output
   pdl_wait();   // the partials come from the split kernel just before
+  // The next kernel (the next step's mla_absorb_q) may launch now and fetch its
+  // weights; it waits for this grid before it reads or writes anything else.
+  if (tid == 0) pdl_launch_dependents();
   const int nsplit = (len + p.chunk - 1) / p.chunk;
   float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
   float lse_v = -INFINITY;

@@ -55,6 +55,9 @@ __device__ __forceinline__ void rope_pair(const T* q_rope, const int32_t* positi
 // lands in shared memory through cp.async (all copies in flight at once); the
 // batch rows are the M side of mma.sync m16n8k16.  The CTAs of head h also
 // rotate that head's RoPE pairs, one pair per thread.
+// Launched with programmatic stream serialization: the W_UK copies are issued
+// before the wait for the previous kernel of the stream, so that they overlap
+// its end; everything else (q_nope, q_rope, positions, every write) comes after.
 __global__ void __launch_bounds__(32)
     absorb_bf16_kernel(const __nv_bfloat16* __restrict__ q_nope,
                        const __nv_bfloat16* __restrict__ q_rope,
@@ -74,6 +77,7 @@ __global__ void __launch_bounds__(32)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
+  pdl_wait();
   for (int it = cb * 32 + lane; it < B * (kDr / 2); it += 32 * gridDim.y)
     rope_pair(q_rope, pos, th, q_pe, H, h, it);
 
@@ -398,10 +402,10 @@ extern "C" mla_status mla_absorb_q(const mla_dims* dims, const void* q_nope, con
   RopeTheta th;
   for (int i = 0; i < kDr / 2; ++i) th.turns[i] = pow(rope_base, -2.0 * i / kDr) / (2.0 * M_PI);
   if (dims->dtype != MLA_F32) {
-    absorb_bf16_kernel<<<dim3(H, kDc / 16), 32, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(q_rope),
-        static_cast<const __nv_bfloat16*>(w_uk), positions, th, static_cast<float*>(q_abs),
-        static_cast<float*>(q_pe), B, H);
+    launch_pdl(absorb_bf16_kernel, dim3(H, kDc / 16), dim3(32), 0, s,
+               static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(q_rope),
+               static_cast<const __nv_bfloat16*>(w_uk), positions, th, static_cast<float*>(q_abs),
+               static_cast<float*>(q_pe), B, H);
   } else {
     absorb_f32_kernel<<<dim3(H, B), 128, 0, s>>>(
         static_cast<const float*>(q_nope), static_cast<const float*>(q_rope),
