@@ -6,6 +6,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <utility>
 #include <stdint.h>
 
@@ -394,6 +395,22 @@ __device__ __forceinline__ void named_bar_sync(int id, int count) {
 
 __device__ __forceinline__ void report(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
+}
+
+// One bit per device ordinal (below 64): kernel attributes such as the
+// dynamic shared-memory limit belong to a device, so a set-up made once per
+// process would leave every other device of the process without it.
+struct DeviceFlags {
+  std::atomic<uint64_t> bits{0};
+  bool test(int dev) const { return dev >= 0 && dev < 64 && ((bits.load() >> dev) & 1u); }
+  void set(int dev) {
+    if (dev >= 0 && dev < 64) bits.fetch_or(uint64_t(1) << dev);
+  }
+};
+
+inline int current_device() {
+  int d = 0;
+  return cudaGetDevice(&d) == cudaSuccess ? d : -1;
 }
 
 // Launches `kernel` with programmatic stream serialization (see pdl_wait).

@@ -121,8 +121,7 @@ __device__ __forceinline__ float reduce8_heads(float v[8], int lane) {
 
 // Roles (448 threads):
 //   warp 8  : TMEM allocation; one lane runs ring A (9 score boxes per tile)
-//   warp 10 : one lane fetches the fp32 query slice with bulk copies into the
-//             ring-B area, then runs ring B (8 latent box pairs per tile: four
+//   warp 10 : one lane runs ring B (8 latent box pairs per tile: four
 //             128-column blocks x two 64-row halves)
 //   warps 9, 11: score MMAs, each over alternate boxes of the stream, into two
 //               accumulators S_0, S_1 (summed by the softmax):
@@ -1038,14 +1037,15 @@ static mla_status decode_split(const char* who, const mla_dims* dims, int q_len,
         return MLA_ERR_CUDA;
       }
     }
-    static bool attr_set = false;
-    if (!attr_set) {
+    static DeviceFlags attr_done;
+    const int dev = current_device();
+    if (!attr_done.test(dev)) {
       if (cudaFuncSetAttribute(split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                int(kTcSmem)) != cudaSuccess) {
         set_error("%s: cannot reserve %zu bytes of shared memory", who, kTcSmem);
         return MLA_ERR_CUDA;
       }
-      attr_set = true;
+      attr_done.set(dev);
     }
     dim3 grid(dims->heads / kHeadGroup, p.splits, p.B);
     launch_pdl(split_tc_kernel, grid, dim3(kTcThreads), kTcSmem, s, tmap, tmap_half, p);

@@ -567,14 +567,15 @@ mla_status launch_split_fp8(const SplitParams& p, const void* cache, cudaStream_
     set_error("%s: cuTensorMapEncodeTiled failed (%d)", who, int(r));
     return MLA_ERR_CUDA;
   }
-  static bool attr_set = false;
-  if (!attr_set) {
+  static DeviceFlags attr_done;
+  const int dev = current_device();
+  if (!attr_done.test(dev)) {
     if (cudaFuncSetAttribute(split_fp8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kF8Smem)) != cudaSuccess) {
       set_error("%s: cannot reserve %zu bytes of shared memory", who, kF8Smem);
       return MLA_ERR_CUDA;
     }
-    attr_set = true;
+    attr_done.set(dev);
   }
   launch_pdl(fp8_q_prep_kernel, dim3(p.H, p.B), dim3(160), 0, stream, p);
   dim3 grid(p.H / kHeadGroup, p.splits, p.B);

@@ -442,19 +442,21 @@ struct Kernel {
   static mla_status launch(const CUtensorMap& tw, const CUtensorMap& tx, WsParams& p,
                            int clusters_needed, dim3 grid_yz, cudaStream_t s, const char* who) {
     auto* kern = wstream_kernel<kXf32, kMode>;
-    static int attr_state = 0;   // 1: set up; 2: set up, clusters of 16 allowed
-    if (attr_state == 0) {
+    static DeviceFlags set_up, big_clusters;   // per device: attributes set; clusters of 16 allowed
+    const int dev = current_device();
+    if (!set_up.test(dev)) {
       if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                int(kWsSmemMax)) != cudaSuccess) {
         set_error("%s: cannot reserve %zu bytes of shared memory", who, kWsSmemMax);
         return MLA_ERR_CUDA;
       }
-      attr_state = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-                           cudaSuccess
-                       ? 2
-                       : 1;
+      if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+          cudaSuccess)
+        big_clusters.set(dev);
       cudaGetLastError();
+      set_up.set(dev);
     }
+    const int attr_state = big_clusters.test(dev) ? 2 : 1;
     // K splits: the largest cluster size whose clusters are all resident at
     // once, at least two K boxes per CTA where K allows.
     const int nbt = p.K / kWsBox;

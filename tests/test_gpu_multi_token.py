@@ -111,3 +111,16 @@ def test_bench_shape_four_tokens(cuda_lib, cfg):
     assert gpu["status"] == 0
     ref, bs = run_oracle(inp, batches=[0, 5])
     compare(gpu, ref, bs, cfg.dtype)
+
+
+@pytest.mark.parametrize("H,q_len", [(32, 4), (32, 2), (128, 2)])
+def test_multi_token_head_groups(cuda_lib, H, q_len):
+    """Several 16-head groups with several tokens: the split CTAs of one chunk
+    share the cache stream across head groups and tokens (clusters of up to 8)."""
+    cfg = small("bf16", q_len, B=2, S=300, H=H)
+    inp = make_inputs(cfg, seed=70 + H + q_len, poison_tail=True,
+                      lengths=torch.tensor([130, 300], dtype=torch.int32))
+    gpu = run_cuda(inp, 0)
+    assert gpu["status"] == 0
+    ref, bs = run_oracle(inp)
+    compare(gpu, ref, bs, "bf16")
