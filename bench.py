@@ -55,7 +55,8 @@ def parse(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", default="step",
-                    choices=["step", "cache_append", "wo_proj", "kq_proj", "ov_proj"],
+                    choices=["step", "cache_append", "wo_proj", "kq_proj", "ov_proj", "absorb_q",
+                             "combine", "out_proj"],
                     help="step: the decode step (default); cache_append / wo_proj: the steps "
                          "around it, timed alone on the workload's sizes")
     return ap.parse_args(argv)
@@ -291,8 +292,8 @@ def run_op(args, cfg, rank):
     per second against the measured HBM peak."""
     import torch
     import head_latent_attention_absorbed_gb300 as mla
-    from workloads import (cache_storage, make_append_inputs, make_materialized_inputs,
-                           make_wo_inputs)
+    from workloads import (cache_storage, make_append_inputs, make_inputs,
+                           make_materialized_inputs, make_wo_inputs)
     mla.load()
     dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
@@ -310,6 +311,48 @@ def run_op(args, cfg, rank):
         moved = wbytes + x.numel() * x.element_size() + cfg.batch * cfg.row * cache.element_size()
         launch = lambda k: mla.cache_append(d, x, ws[k % L], pos, cache, cfg.rope_base, status)
         metric = "cache append: kv_a_proj weight + token + row bytes per second"
+    elif args.op in ("absorb_q", "out_proj", "combine"):
+        # The three kernels of the step around the split, each alone: absorb (a1 + a2,
+        # bound by W_UK), combine (a4, the chunk partials), out_proj (a5, bound by W_UV).
+        inp = make_inputs(cfg, seed=0)
+        B, H = cfg.batch, cfg.heads
+        q_abs = torch.empty((B, H, cfg.d_c), dtype=torch.float32, device=dev)
+        q_pe = torch.empty((B, H, cfg.d_rope), dtype=torch.float32, device=dev)
+        o_c = torch.empty((B, H, cfg.d_c), dtype=torch.float32, device=dev)
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+        out = torch.empty((B, H, cfg.d_v), dtype=torch.float32, device=dev)
+        qn, qr = inp.q_nope.to(dev), inp.q_rope.to(dev)
+        pos, lengths = inp.positions.to(dev), inp.lengths.to(dev)
+        wbytes = inp.w_uk.numel() * inp.w_uk.element_size()
+        L = max(2, math.ceil(3 * l2 / wbytes))
+        if args.op == "absorb_q":
+            ws = [inp.w_uk.to(dev) for _ in range(L)]
+            moved = (wbytes + qn.numel() * qn.element_size() + qr.numel() * qr.element_size() +
+                     pos.numel() * 4 + q_abs.numel() * 4 + q_pe.numel() * 4)
+            launch = lambda k: mla.absorb_q(d, qn, qr, ws[k % L], pos, q_abs, q_pe, cfg.rope_base)
+            metric = "absorb: W_UK + queries + q_abs + q_pe bytes per second"
+        elif args.op == "out_proj":
+            ws = [inp.w_uv.to(dev) for _ in range(L)]
+            o_c.normal_()
+            moved = wbytes + o_c.numel() * 4 + out.numel() * 4
+            launch = lambda k: mla.out_proj(d, o_c, ws[k % L], out)
+            metric = "out_proj: W_UV + o_c + o bytes per second"
+        else:
+            L = 1
+            splits = mla.num_splits(d, args.splits)
+            wsp = torch.empty((mla.workspace_bytes(d, args.splits),), dtype=torch.uint8, device=dev)
+            status = torch.zeros(1, dtype=torch.int32, device=dev)
+            mla.absorb_q(d, qn, qr, inp.w_uk.to(dev), pos, q_abs, q_pe, cfg.rope_base)
+            mla.decode_split(d, q_abs, q_pe, inp.cache.to(dev), lengths, wsp, cfg.softmax_scale,
+                             args.splits, status)
+            torch.cuda.synchronize()
+            if int(status.item()) != 0:
+                raise RuntimeError("device status after the split that fills the partials")
+            chunk = (-(-cfg.s_max // splits) + 7) // 8 * 8
+            used = sum(-(-int(n) // chunk) for n in inp.lengths.tolist())   # chunks with rows
+            moved = used * H * (cfg.d_c + 1) * 4 + o_c.numel() * 4 + lse.numel() * 4
+            launch = lambda k: mla.decode_combine(d, lengths, wsp, o_c, args.splits, lse)
+            metric = "combine: chunk partials read + o_c + lse bytes per second (partials in L2)"
     elif args.op in ("kq_proj", "ov_proj"):
         m = make_materialized_inputs(cfg, seed=0)
         wdt = m.w_o.dtype
@@ -373,7 +416,8 @@ def run_op(args, cfg, rank):
             "dtype": DTYPE_NAME[cfg.dtype], "data": "synthetic",
             "config": {"workload": cfg.name, "batch": cfg.batch, "heads": cfg.heads,
                        "hidden": cfg.hidden,
-                       "l2": f"{L} rotating weight copies, more than 3x L2"},
+                       "l2": (f"{L} rotating weight copies, more than 3x L2" if args.op != "combine"
+                              else "the partials, written by the split just before, in L2")},
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
                          "frac": gbs / peak, "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
                          "bytes_per_launch": moved}}
