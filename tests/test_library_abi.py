@@ -106,3 +106,43 @@ def test_split_planning(lib):
     for (B, H, S) in [(8, 16, 4096), (64, 16, 8192), (32, 128, 16384), (1, 16, 64)]:
         s = mla.num_splits(mla.dims(B, H, S, mla.MLA_BF16), 0)
         assert 1 <= s <= (S + 7) // 8
+
+
+def test_host_validation_of_later_calls(lib):
+    """Argument errors of the multi-token and materialised calls come back as a
+    status before anything is launched (no GPU needed)."""
+    mla, so = lib
+    P = ctypes.c_void_p
+    good = 0x10000
+    d = _d(mla)
+    # multi-token: q_len must be >= 1; the workspace is sized for B * q_len query rows
+    assert so.mla_decode_attn_multi(ctypes.byref(d), 0, P(good), P(good), P(good), P(good), 0.1,
+                                    0, P(good), 1 << 30, P(good), None, None, None) == 1
+    qd = mla.query_dims(d, 4)
+    need = mla.workspace_bytes(qd, 0)
+    assert need > mla.workspace_bytes(d, 0)
+    assert so.mla_decode_attn_multi(ctypes.byref(d), 4, P(good), P(good), P(good), P(good), 0.1,
+                                    0, P(good), need - 1, P(good), None, None, None) == 3
+    assert so.mla_decode_attn_multi(ctypes.byref(d), 4, P(good), P(good), P(good), None, 0.1,
+                                    0, P(good), need, P(good), None, None, None) == 1
+    # materialised form: d_in a multiple of 64, d_out a multiple of 8, no NULLs
+    assert so.mla_absorb_q_materialized(ctypes.byref(d), 100, P(good), P(good), P(good), P(good),
+                                        1e4, P(good), P(good), None) == 2
+    assert so.mla_absorb_q_materialized(ctypes.byref(d), 128, None, P(good), P(good), P(good),
+                                        1e4, P(good), P(good), None) == 1
+    assert so.mla_ov_proj(ctypes.byref(d), 2044, P(good), P(good), P(good), None) == 2
+    assert so.mla_ov_proj(ctypes.byref(d), 2048, P(good), None, P(good), None) == 1
+    assert so.mla_materialize_wkq(ctypes.byref(d), 0, P(good), P(good), P(good), None) == 1
+    assert so.mla_materialize_wov(ctypes.byref(d), 2048, P(good), P(good), P(good + 4), None) == 1
+
+
+def test_planner_prefers_whole_tiles(lib):
+    """bf16 and FP8 chunks are costed in whole 128-row tiles: 8 sequences of 4096
+    rows take 16 chunks of 256 rows (one wave on 148 or 152 SMs), not 18-19
+    chunks whose last tile is partial; the fp32 kernel, which has no tiles, is
+    planned on rows."""
+    mla, _ = lib
+    for dt in (mla.MLA_BF16, mla.MLA_FP8_E4M3):
+        assert mla.num_splits(mla.dims(8, 16, 4096, dt), 0) == 16
+    s32 = mla.num_splits(mla.dims(8, 16, 4096, mla.MLA_F32), 0)
+    assert 1 <= s32 <= 512
