@@ -64,15 +64,21 @@ class DecodeStep:
         self.workspace = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
 
-    def run(self, q_nope, q_rope, cache, lengths, positions, w_uk, w_uv, stream=None):
+    def run(self, q_nope, q_rope, cache, lengths, positions, w_uk, w_uv, stream=None, out=None):
         """The whole step: one library call (mla_decode_step) for one token per
-        sequence, the three calls with mla_decode_attn_multi for q_len > 1."""
+        sequence, the three calls with mla_decode_attn_multi for q_len > 1.
+
+        With one token per sequence, q_nope, q_rope, lengths, positions and
+        ``out`` (o, default: this step's device buffer) may be pinned host
+        tensors, read and written by the kernels directly.
+        """
         if self.q_len > 1:
             return self.run_calls(q_nope, q_rope, cache, lengths, positions, w_uk, w_uv, stream)
+        o = self.out if out is None else out
         decode_step(self.dims, q_nope, q_rope, w_uk, positions, cache, lengths, w_uv,
-                    self.workspace, self.q_abs, self.q_pe, self.o_c, self.out, self.scale,
+                    self.workspace, self.q_abs, self.q_pe, self.o_c, o, self.scale,
                     self.rope_base, self.splits_requested, self.lse, self.status, stream)
-        return self.out
+        return o
 
     def run_calls(self, q_nope, q_rope, cache, lengths, positions, w_uk, w_uv, stream=None):
         """The same step as the three separate calls absorb_q, decode_attn (or
@@ -95,10 +101,12 @@ class DecodeStep:
 
         Returns a ``HostStep``: pinned host tensors ``q_nope``, ``q_rope``,
         ``lengths``, ``positions`` (the step's inputs, filled by the caller) and
-        ``out`` (o, written by the step), and ``replay()``.  Every replay copies
-        the four inputs to the device in one transfer (they share one pinned
-        block), runs the three library calls against the device-resident cache
-        and weights, and copies o back in one transfer.
+        ``out`` (o, written by the step), and ``replay()``.  With one token per
+        sequence every replay runs mla_decode_step on the host tensors
+        themselves: its kernels read the inputs and write o over the host link
+        (no copies).  With several tokens per sequence every replay copies the
+        four inputs to the device in one transfer (they share one pinned block),
+        runs the calls, and copies o back in one transfer.
         """
         return HostStep(self, cache, w_uk, w_uv)
 
@@ -135,10 +143,20 @@ class HostStep:
                                                                    for i in range(4))
         d = [view(self._d_block, i) for i in range(4)]
         self.out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-        self.h2d_bytes = off
+        # Bytes that cross the host link each step: the inputs' own bytes when the
+        # kernels read them in place, the whole (padded) block when it is copied.
+        self.h2d_bytes = (sum(t.numel() * t.element_size()
+                              for t in (self.q_nope, self.q_rope, self.lengths, self.positions))
+                          if step.q_len == 1 else off)
         self.d2h_bytes = self.out.numel() * self.out.element_size()
 
+        self.zero_copy = step.q_len == 1
+        h = (self.q_nope, self.q_rope, self.lengths, self.positions)
+
         def body():
+            if self.zero_copy:
+                step.run(h[0], h[1], cache, h[2], h[3], w_uk, w_uv, out=self.out)
+                return
             self._d_block.copy_(self._h_block, non_blocking=True)
             o = step.run(d[0], d[1], cache, d[2], d[3], w_uk, w_uv)
             self.out.copy_(o, non_blocking=True)

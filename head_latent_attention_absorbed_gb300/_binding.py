@@ -138,6 +138,13 @@ def _cuda_contig(*ts):
             _require(t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors")
 
 
+def _cuda_or_pinned(*ts):
+    for t in ts:
+        if t is not None:
+            _require(t.is_contiguous() and (t.is_cuda or t.is_pinned()),
+                     "tensors must be contiguous CUDA tensors or pinned host tensors")
+
+
 def num_splits(d: MlaDims, requested: int = 0) -> int:
     return int(load().mla_decode_num_splits(ctypes.byref(d), int(requested)))
 
@@ -227,9 +234,13 @@ def decode_attn_noalloc(d: MlaDims, q_abs, q_pe, cache, lengths, o_c, softmax_sc
 def decode_step(d: MlaDims, q_nope, q_rope, w_uk, positions, cache, lengths, w_uv, workspace,
                 q_abs, q_pe, o_c, out, softmax_scale: float, rope_base: float = 10000.0,
                 num_splits_requested: int = 0, lse=None, dev_status=None, stream=None) -> None:
-    """absorb_q, decode_attn and out_proj in one call (bf16: fused combine + W_UV)."""
-    _cuda_contig(q_nope, q_rope, w_uk, positions, cache, lengths, w_uv, workspace, q_abs, q_pe,
-                 o_c, out, lse, dev_status)
+    """absorb_q, decode_attn and out_proj in one call (bf16: fused combine + W_UV).
+
+    q_nope, q_rope, positions, lengths and out may be pinned host tensors: the
+    kernels then read and write them over the host link, with no copies.
+    """
+    _cuda_contig(w_uk, cache, w_uv, workspace, q_abs, q_pe, o_c, lse, dev_status)
+    _cuda_or_pinned(q_nope, q_rope, positions, lengths, out)
     nbytes = workspace.numel() * workspace.element_size()
     _check(load().mla_decode_step(ctypes.byref(d), _ptr(q_nope), _ptr(q_rope), _ptr(w_uk),
                                   _ptr(positions), float(rope_base), _ptr(cache), _ptr(lengths),

@@ -1129,6 +1129,19 @@ extern "C" mla_status mla_decode_attn(const mla_dims* dims, const void* q_abs, c
   return mla_decode_combine(dims, lengths, num_splits, workspace, ws_bytes, o_c, lse, stream);
 }
 
+// Whether the device can address `ptr` directly: device or managed memory, or
+// page-locked host memory (mapped into the device's address space).  Pageable
+// host memory is refused: a kernel touching it would fault.
+static bool device_addressable(const void* ptr) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return true;
+  return a.type == cudaMemoryTypeHost && a.devicePointer != nullptr;
+}
+
 extern "C" mla_status mla_decode_step(const mla_dims* dims, const void* q_nope, const void* q_rope,
                                       const void* w_uk, const int32_t* positions, double rope_base,
                                       const void* cache, const int32_t* lengths, float softmax_scale,
@@ -1141,6 +1154,16 @@ extern "C" mla_status mla_decode_step(const mla_dims* dims, const void* q_nope, 
   if (!o_c || !out || !w_uv || !aligned16(o_c) || !aligned16(out) || !aligned16(w_uv)) {
     set_error("%s: o_c, out and w_uv must be non-NULL 16-byte aligned pointers", who);
     return MLA_ERR_INVALID_ARG;
+  }
+  // The per-step inputs and the output may live in page-locked host memory.
+  const void* step_io[5] = {q_nope, q_rope, positions, lengths, out};
+  const char* step_io_name[5] = {"q_nope", "q_rope", "positions", "lengths", "out"};
+  for (int i = 0; i < 5; ++i) {
+    if (step_io[i] && !device_addressable(step_io[i])) {
+      set_error("%s: %s is not memory the device can address (pageable host memory?); use "
+                "device memory or page-locked host memory", who, step_io_name[i]);
+      return MLA_ERR_INVALID_ARG;
+    }
   }
   if (dims->dtype == MLA_F32) {
     // The fp32 path has no fused tail: the three calls in order.

@@ -358,6 +358,18 @@ mla_status mla_ov_proj(const mla_dims* dims, int32_t d_out, const float* o_c, co
  * after the split kernel; before its wait it reads only w_uv and lengths.
  * With MLA_F32 the three calls run in order.  Every argument is checked before
  * anything is enqueued.  lse may be NULL.
+ *
+ * Host buffers for the step's own inputs and output: q_nope, q_rope,
+ * positions, lengths and out may also be page-locked host memory (allocated
+ * with cudaHostAlloc or registered with cudaHostRegister, so that the device
+ * can address it).  The kernels then read the inputs and write o over the
+ * host link themselves, with no copy of their own to enqueue; on a GB300
+ * (NVLink-C2C) this costs about 2 us per step for the inputs and nothing
+ * measurable for o.  The caller must not touch those host buffers until the
+ * stream has passed the step.  Pageable host memory is refused with
+ * MLA_ERR_INVALID_ARG before anything is enqueued.  Every other tensor (the
+ * cache, the weights, q_abs, q_pe, o_c, lse, the workspace) must be device
+ * memory, as for the other calls.
  */
 mla_status mla_decode_step(const mla_dims* dims, const void* q_nope, const void* q_rope,
                            const void* w_uk, const int32_t* positions, double rope_base,

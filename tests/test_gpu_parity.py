@@ -12,7 +12,8 @@ import torch
 
 from _parity import compare, run_cuda, run_oracle
 from workloads import (V2LITE_BF16_B4_S65536_LONG, V2LITE_BF16_B8_S4096, V2LITE_BF16_B64_RAGGED,
-                       V2LITE_F32_B1_S64, V3_BF16_H128_B32_S16384, MlaConfig, make_inputs)
+                       V2LITE_F32_B1_S64, V3_BF16_H128_B32_S16384, MlaConfig, cache_storage,
+                       make_inputs)
 
 pytestmark = pytest.mark.gpu
 
@@ -141,15 +142,17 @@ def test_v2lite_long_context_128_splits(cuda_lib):
     compare(gpu, ref, bs, "bf16")
 
 
-def test_captured_step_from_host_memory(cuda_lib):
-    """DecodeStep.capture: a CUDA graph that copies the step's inputs from pinned host
-    memory, runs the three calls and copies o back; two replays with different host
-    inputs both match the eager path and the oracle."""
+@pytest.mark.parametrize("dtype", ["bf16", "fp8", "f32"])
+def test_captured_step_from_host_memory(cuda_lib, dtype):
+    """DecodeStep.capture: a CUDA graph of mla_decode_step whose kernels read the
+    step's inputs from pinned host memory and write o there; two replays with
+    different host inputs both equal the device-resident eager path bit for bit
+    and match the oracle."""
     mla = cuda_lib
-    cfg = small(B=3, S=300)
+    cfg = small(dtype=dtype, B=3, S=300)
     base = make_inputs(cfg, seed=21, poison_tail=True,
                        lengths=torch.tensor([300, 45, 129], dtype=torch.int32))
-    step = mla.DecodeStep(cfg.batch, cfg.heads, cfg.s_max, torch.bfloat16,
+    step = mla.DecodeStep(cfg.batch, cfg.heads, cfg.s_max, cache_storage(cfg),
                           rope_base=cfg.rope_base, softmax_scale=cfg.softmax_scale)
     cache, w_uk, w_uv = base.cache.cuda(), base.w_uk.cuda(), base.w_uv.cuda()
     hs = step.capture(cache, w_uk, w_uv)
@@ -170,5 +173,34 @@ def test_captured_step_from_host_memory(cuda_lib):
         inp.q_nope, inp.q_rope = other.q_nope, other.q_rope
         ref, bs = run_oracle(inp)
         from _parity import assert_close
-        assert_close("o", got[bs], ref["o"], "bf16")
+        assert_close("o", got[bs], ref["o"], dtype)
     assert int(step.status.item()) == 0
+    assert hs.zero_copy
+
+
+def test_pageable_host_memory_is_refused(cuda_lib):
+    """mla_decode_step accepts page-locked host buffers for its inputs and output
+    but refuses pageable ones before anything is enqueued."""
+    import ctypes
+    mla = cuda_lib
+    cfg = small(B=2, S=64)
+    inp = make_inputs(cfg, seed=24)
+    step = mla.DecodeStep(cfg.batch, cfg.heads, cfg.s_max, torch.bfloat16)
+    pageable = inp.q_nope.clone()                      # ordinary host memory
+    assert not pageable.is_pinned()
+    with pytest.raises(ValueError):
+        step.run(pageable, inp.q_rope.cuda(), inp.cache.cuda(), inp.lengths.cuda(),
+                 inp.positions.cuda(), inp.w_uk.cuda(), inp.w_uv.cuda())
+    lib = mla.load()
+    d = step.dims
+    dev = lambda t: t.cuda()
+    qr, cache, ln, ps = dev(inp.q_rope), dev(inp.cache), dev(inp.lengths), dev(inp.positions)
+    wuk, wuv = dev(inp.w_uk), dev(inp.w_uv)
+    st = lib.mla_decode_step(ctypes.byref(d), pageable.data_ptr(), qr.data_ptr(), wuk.data_ptr(),
+                             ps.data_ptr(), 10000.0, cache.data_ptr(), ln.data_ptr(),
+                             float(step.scale), 0, wuv.data_ptr(), step.workspace.data_ptr(),
+                             step.workspace.numel(), step.q_abs.data_ptr(), step.q_pe.data_ptr(),
+                             step.o_c.data_ptr(), None, step.out.data_ptr(), None,
+                             torch.cuda.current_stream().cuda_stream)
+    assert st == 1                                     # MLA_ERR_INVALID_ARG
+    assert b"q_nope" in lib.mla_last_error_message()
