@@ -397,6 +397,15 @@ __device__ __forceinline__ void report(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
 }
 
+// Rows of the latent cache that mla_decode_step asks L2 to fetch while its
+// absorb kernel runs, so that the cache stream starts before the decode kernel
+// can occupy the SMs.  Each chunk's first `rows` rows (up to its length).
+struct CachePrefetch {
+  const uint8_t* cache;       // [B, s_max, row_bytes]; NULL: no prefetch
+  const int32_t* lengths;     // [B] device
+  int B, s_max, chunk, splits, row_bytes, rows;
+};
+
 // One bit per device ordinal (below 64): kernel attributes such as the
 // dynamic shared-memory limit belong to a device, so a set-up made once per
 // process would leave every other device of the process without it.

@@ -16,6 +16,7 @@
 #include <math.h>
 
 #include "mla_common.cuh"
+#include "mla_split.cuh"
 #include "mla_wstream.cuh"
 
 namespace mla {
@@ -55,15 +56,19 @@ __device__ __forceinline__ void rope_pair(const T* q_rope, const int32_t* positi
 // lands in shared memory through cp.async (all copies in flight at once); the
 // batch rows are the M side of mma.sync m16n8k16.  The CTAs of head h also
 // rotate that head's RoPE pairs, one pair per thread.
-// Launched with programmatic stream serialization: the W_UK copies are issued
-// before the wait for the previous kernel of the stream, so that they overlap
-// its end; everything else (q_nope, q_rope, positions, every write) comes after.
+// Within mla_decode_step it may be launched with programmatic stream
+// serialization: the W_UK copies (and the cache prefetch) are issued before the
+// wait for the previous kernel of the stream, so that they overlap its end;
+// everything else (q_nope, q_rope, positions, every write) comes after.  Launched
+// as usual, the wait returns at once.
+constexpr int kPfPiece = 16384;   // bytes per L2 prefetch instruction
+
 __global__ void __launch_bounds__(32)
     absorb_bf16_kernel(const __nv_bfloat16* __restrict__ q_nope,
                        const __nv_bfloat16* __restrict__ q_rope,
                        const __nv_bfloat16* __restrict__ w_uk, const int32_t* __restrict__ pos,
                        const RopeTheta th, float* __restrict__ q_abs, float* __restrict__ q_pe,
-                       int B, int H) {
+                       int B, int H, const CachePrefetch pf) {
   __shared__ __align__(128) uint8_t wt[kDn * 32];  // 128 k-rows x 16 bf16 columns
   const int h = blockIdx.x, cb = blockIdx.y, lane = threadIdx.x;
   pdl_launch_dependents();   // the decode kernel may start its set-up and cache stream now
@@ -77,6 +82,30 @@ __global__ void __launch_bounds__(32)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
+  if (pf.cache) {
+    // Within mla_decode_step: start the decode kernel's cache stream.  The
+    // pieces of every chunk's first rows are spread over all threads of the
+    // grid, the first piece of every chunk first.  The cache and lengths are
+    // inputs, not results of the previous kernel, so this precedes the wait.
+    const int nchunk = pf.B * pf.splits;
+    const int per_chunk = (pf.rows * pf.row_bytes + kPfPiece - 1) / kPfPiece;
+    const int nthreads = gridDim.x * gridDim.y * 32;
+    const int me = (blockIdx.y * gridDim.x + blockIdx.x) * 32 + lane;
+    for (int id = me; id < nchunk * per_chunk; id += nthreads) {
+      const int k = id / nchunk, c = id % nchunk;
+      const int b = c / pf.splits, r0 = (c % pf.splits) * pf.chunk;
+      const int len = min(max(pf.lengths[b], 0), pf.s_max);
+      const int rows = min(min(pf.chunk, len - r0), pf.rows);
+      if (rows <= 0) continue;
+      const long long first = (static_cast<long long>(b) * pf.s_max + r0) * pf.row_bytes;
+      const long long beg = first + static_cast<long long>(k) * kPfPiece;
+      const long long end = first + static_cast<long long>(rows) * pf.row_bytes;
+      if (beg >= end) continue;
+      const uint32_t size = static_cast<uint32_t>(min(static_cast<long long>(kPfPiece), end - beg));
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(pf.cache + beg), "r"(size)
+                   : "memory");
+    }
+  }
   pdl_wait();
   for (int it = cb * 32 + lane; it < B * (kDr / 2); it += 32 * gridDim.y)
     rope_pair(q_rope, pos, th, q_pe, H, h, it);
@@ -381,7 +410,15 @@ using namespace mla;
 extern "C" mla_status mla_absorb_q(const mla_dims* dims, const void* q_nope, const void* q_rope,
                                    const void* w_uk, const int32_t* positions, double rope_base,
                                    void* q_abs, void* q_pe, void* stream) {
-  const char* who = "mla_absorb_q";
+  CachePrefetch none{};
+  return absorb_q("mla_absorb_q", dims, q_nope, q_rope, w_uk, positions, rope_base, q_abs, q_pe,
+                  stream, none, false);
+}
+
+mla_status mla::absorb_q(const char* who, const mla_dims* dims, const void* q_nope,
+                         const void* q_rope, const void* w_uk, const int32_t* positions,
+                         double rope_base, void* q_abs, void* q_pe, void* stream,
+                         const CachePrefetch& pf, bool early) {
   mla_status st = check_dims(dims, who);
   if (st != MLA_OK) return st;
   if (!q_nope || !q_rope || !w_uk || !positions || !q_abs || !q_pe) {
@@ -402,10 +439,16 @@ extern "C" mla_status mla_absorb_q(const mla_dims* dims, const void* q_nope, con
   RopeTheta th;
   for (int i = 0; i < kDr / 2; ++i) th.turns[i] = pow(rope_base, -2.0 * i / kDr) / (2.0 * M_PI);
   if (dims->dtype != MLA_F32) {
-    launch_pdl(absorb_bf16_kernel, dim3(H, kDc / 16), dim3(32), 0, s,
-               static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(q_rope),
-               static_cast<const __nv_bfloat16*>(w_uk), positions, th, static_cast<float*>(q_abs),
-               static_cast<float*>(q_pe), B, H);
+    if (early)
+      launch_pdl(absorb_bf16_kernel, dim3(H, kDc / 16), dim3(32), 0, s,
+                 static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(q_rope),
+                 static_cast<const __nv_bfloat16*>(w_uk), positions, th, static_cast<float*>(q_abs),
+                 static_cast<float*>(q_pe), B, H, pf);
+    else
+      absorb_bf16_kernel<<<dim3(H, kDc / 16), 32, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(q_rope),
+          static_cast<const __nv_bfloat16*>(w_uk), positions, th, static_cast<float*>(q_abs),
+          static_cast<float*>(q_pe), B, H, pf);
   } else {
     absorb_f32_kernel<<<dim3(H, B), 128, 0, s>>>(
         static_cast<const float*>(q_nope), static_cast<const float*>(q_rope),

@@ -53,4 +53,11 @@ __device__ __forceinline__ int clamp_length(const SplitParams& p, int v, bool re
 mla_status launch_split_fp8(const SplitParams& p, const void* cache, cudaStream_t stream,
                             const char* who);
 
+// mla_absorb_q's work (named `who` in error messages), with the decode kernel's
+// first cache rows prefetched into L2 when pf.cache is set, and (bf16, `early`)
+// launched with programmatic stream serialization (mla_proj.cu).
+mla_status absorb_q(const char* who, const mla_dims* dims, const void* q_nope, const void* q_rope,
+                    const void* w_uk, const int32_t* positions, double rope_base, void* q_abs,
+                    void* q_pe, void* stream, const CachePrefetch& pf, bool early);
+
 }  // namespace mla

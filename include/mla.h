@@ -40,17 +40,19 @@
  *    tensor cores as hi + lo bf16 pairs, the FP8 kernel as three and two
  *    E4M3 parts).
  *  - Launch overlap: the kernels of mla_decode_attn (and of its halves), the
- *    bf16 kernels of mla_absorb_q and mla_out_proj, and the fused tail of
- *    mla_decode_step are launched with programmatic stream serialization, so
- *    each may begin while the kernel before it on the stream is still running
- *    -- but only if that kernel allows it explicitly
- *    (griddepcontrol.launch_dependents), as these kernels do; after any other
- *    kernel, or a copy, they start as usual.  Before waiting for their
- *    predecessor they read only the cache and lengths (mla_decode_attn) or
- *    the weights (mla_absorb_q: w_uk; mla_out_proj and the fused tail: w_uv);
+ *    bf16 kernel of mla_out_proj, and the fused tail of mla_decode_step are
+ *    launched with programmatic stream serialization, so each may begin while
+ *    the kernel before it on the stream is still running -- but only if that
+ *    kernel allows it explicitly (griddepcontrol.launch_dependents), as these
+ *    kernels and mla_absorb_q's do; after any other kernel, or a copy, they
+ *    start as usual.  Within mla_decode_step (bf16 and FP8), when its decode
+ *    grid fits in one wave on the device, the absorb kernel is launched that
+ *    way too.  Before waiting for their predecessor they read only the cache
+ *    and lengths (mla_decode_attn; the absorb inside mla_decode_step) or the
+ *    weights (that absorb: w_uk; mla_out_proj and the fused tail: w_uv);
  *    everything else is read, and everything is written, after the wait.  So
  *    a kernel of the caller that allows early launch must not write those
- *    inputs.
+ *    inputs.  mla_absorb_q on its own starts as usual.
  *  - Supported sizes: d_c = 512, d_rope = 64, d_nope = 128, d_v = 128;
  *    batch >= 1; s_max >= 1; heads >= 1 (a multiple of 16 for MLA_BF16 and
  *    MLA_FP8_E4M3).
