@@ -40,42 +40,56 @@ constexpr int kThreads = kWarps * 32;
 //           they land about when its P does instead of holding slots early
 // L2 serves the GPU's SMs at close to three times the HBM rate, so the
 // second read costs L2 bandwidth, not HBM time.
-constexpr int kTcThreads = 448;                       // 0-7 softmax, 8 ring A, 10 ring B, 9/11/12/13 MMA
-constexpr int kSoftThreads = 256;
-constexpr int kHalfHeads = kHeadGroup / 2;            // heads per softmax warp group
 constexpr int kBoxBytes = kTileRows * 128;            // 128 rows x 64 bf16 columns
-constexpr int kSlotsA = 6;
-constexpr int kSlotsB = 4;                            // each slot: two adjacent 64-row boxes
 constexpr int kHalfBox = kBoxBytes / 2;               // 64 rows x 64 bf16 columns
-constexpr int kQN = 2 * kHeadGroup;                   // hi | lo query rows
-constexpr int kQBoxBytes = kQN * 128;
-constexpr int kPSub = kQN * 128;                      // P^T: 64 tile rows of kQN rows
-constexpr int kPBytes = 2 * kPSub;                    // 128 tile rows
-constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kSlotsA * kBoxBytes;
-constexpr int kOffQ = kOffB + kSlotsB * 2 * kHalfBox;
-constexpr int kOffP = kOffQ + 9 * kQBoxBytes;         // two P^T buffers
-constexpr int kOffRed = kOffP + 2 * kPBytes;          // [2][16 heads][4 warps] tile maxima
-constexpr int kOffLsum = kOffRed + 2 * kHeadGroup * 4 * 4;
-constexpr int kOffBar = kOffLsum + kHeadGroup * 4 * 4;
-constexpr int BAR_FULLA = 0, BAR_EMPTYA = kSlotsA, BAR_FULLB = 2 * kSlotsA,
-              BAR_EMPTYB = BAR_FULLB + kSlotsB, BAR_ZEROB = BAR_EMPTYB + kSlotsB,
-              BAR_SFULL = BAR_ZEROB + kSlotsB, BAR_SFREE = BAR_SFULL + 2, BAR_PFULL = BAR_SFREE + 2,
-              BAR_ODONE = BAR_PFULL + 2, BAR_LASTA = BAR_ODONE + 2, BAR_FULLX = BAR_LASTA + 1,
-              BAR_ZEROX = BAR_FULLX + 8, BAR_ODONE2 = BAR_ZEROX + 8, BAR_PVPREV = BAR_ODONE2 + 1,
-              BAR_DONE = BAR_PVPREV + 1, kNumBars = BAR_DONE + 1;
-constexpr int kOffSlot = kOffBar + 8 * kNumBars;
-constexpr int kOffAbort = kOffSlot + 16;
-constexpr int kOffIssued = kOffAbort + 16;            // score tiles issued, per score issuer (ring B gate)
-constexpr size_t kTcSmem = 1024 + kOffIssued + 16;
-constexpr uint32_t kTmemCols = 256;                   // S_0[2] at 0/32, S_1[2] at 64/96, O^T at 128..255
-constexpr uint32_t kS1Col = 64;                       // second score accumulator
-constexpr uint32_t kOCol = 128;                       // O^T blocks, 32 columns each
 // Rescale threshold (log2 units): P may grow to 2^8 before O is rescaled.
 constexpr float kRescaleLog2 = 8.f;
-static_assert(kTcSmem <= 232448, "shared memory plan exceeds 227 KB");
-static_assert(kSlotsA * kBoxBytes + 9 * kQBoxBytes >= 8 * kBoxBytes,
-              "the last tile's eight latent pairs fit in ring A and the query area");
+
+// The kernel's plan for kG heads per CTA (16 or 32; N = 2 kG query rows, the
+// heads' hi and lo parts).  kG = 32 halves, per head, the MMAs and the tile
+// reads (shared memory and L2); its query and accumulators need more room, so
+// ring A has four slots and P one buffer.
+template <int kG>
+struct TcPlan {
+  static constexpr int kSoftWarps = kG / 2;            // four warps per group of 8 heads
+  static constexpr int kSoftThreads = 32 * kSoftWarps;
+  static constexpr int kThreads = kSoftThreads + 6 * 32;   // + ring A, ring B, 2 score, 2 PV
+  static constexpr int kSlotsA = kG == 16 ? 6 : 4;
+  static constexpr int kSlotsB = 4;                    // each slot: two adjacent 64-row boxes
+  static constexpr int kPBufs = kG == 16 ? 2 : 1;
+  static constexpr int kQN = 2 * kG;                   // hi | lo query rows
+  static constexpr int kQBoxBytes = kQN * 128;
+  static constexpr int kPSub = kQN * 128;              // P^T: 64 tile rows of kQN rows
+  static constexpr int kPBytes = 2 * kPSub;            // 128 tile rows
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + kSlotsA * kBoxBytes;
+  static constexpr int kOffQ = kOffB + kSlotsB * 2 * kHalfBox;
+  static constexpr int kOffP = kOffQ + 9 * kQBoxBytes;
+  static constexpr int kOffRed = kOffP + kPBufs * kPBytes;   // [2][kG heads][4 warps] tile maxima
+  static constexpr int kOffLsum = kOffRed + 2 * kG * 4 * 4;
+  static constexpr int kOffBar = kOffLsum + kG * 4 * 4;
+  static constexpr int BAR_FULLA = 0, BAR_EMPTYA = kSlotsA, BAR_FULLB = 2 * kSlotsA,
+                       BAR_EMPTYB = BAR_FULLB + kSlotsB, BAR_ZEROB = BAR_EMPTYB + kSlotsB,
+                       BAR_SFULL = BAR_ZEROB + kSlotsB, BAR_SFREE = BAR_SFULL + 2,
+                       BAR_PFULL = BAR_SFREE + 2, BAR_ODONE = BAR_PFULL + 2,
+                       BAR_LASTA = BAR_ODONE + 2, BAR_FULLX = BAR_LASTA + 1,
+                       BAR_ZEROX = BAR_FULLX + 8, BAR_ODONE2 = BAR_ZEROX + 8,
+                       BAR_PVPREV = BAR_ODONE2 + 1, BAR_DONE = BAR_PVPREV + 1,
+                       kNumBars = BAR_DONE + 1;
+  static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
+  static constexpr int kOffAbort = kOffSlot + 16;
+  static constexpr int kOffIssued = kOffAbort + 16;   // score tiles issued, per score issuer
+  static constexpr size_t kSmem = 1024 + kOffIssued + 16;
+  // TMEM: S_0[2] at 0 / kQN, S_1[2] at kS1Col / kS1Col + kQN, O^T blocks of kQN
+  // columns from kOCol.
+  static constexpr uint32_t kS1Col = 2 * kQN;
+  static constexpr uint32_t kOCol = 4 * kQN;
+  static constexpr uint32_t kTmemCols = 8 * kQN;       // 256 or 512
+  static_assert(kSmem <= 232448, "shared memory plan exceeds 227 KB");
+  static_assert(kSlotsA * kBoxBytes + 9 * kQBoxBytes >= 8 * kBoxBytes,
+                "the last tile's eight latent pairs fit in ring A and the query area");
+  static_assert(kSlotsA % 2 == 0, "each score issuer owns every other ring-A slot");
+};
 
 // Waits for a phase; gives up (and raises the CTA's abort flag) after kWaitNs,
 // or at once when another role has already raised it.
@@ -139,9 +153,28 @@ __device__ __forceinline__ float reduce8_heads(float v[8], int lane) {
 //             (then O^T is rescaled in TMEM).
 // The fp32 query and P reach the tensor core as bf16 hi + lo pairs, so their
 // rounding stays near 2^-17 relative.
-__global__ void __launch_bounds__(kTcThreads, 1)
+template <int kG>
+__global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
     split_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_half,
                     const SplitParams p) {
+  // The plan's sizes under the names the body uses (kHeadGroup: heads per CTA).
+  using L = TcPlan<kG>;
+  constexpr int kHeadGroup = kG, kHalfHeads = 8, kSoftWarps = L::kSoftWarps;
+  constexpr int kSoftThreads = L::kSoftThreads, kSlotsA = L::kSlotsA, kSlotsB = L::kSlotsB;
+  constexpr int kPBufs = L::kPBufs, kQN = L::kQN, kQBoxBytes = L::kQBoxBytes, kPSub = L::kPSub;
+  constexpr int kPBytes = L::kPBytes, kOffA = L::kOffA, kOffB = L::kOffB, kOffQ = L::kOffQ;
+  constexpr int kOffP = L::kOffP, kOffRed = L::kOffRed, kOffLsum = L::kOffLsum;
+  constexpr int kOffBar = L::kOffBar, kOffSlot = L::kOffSlot, kOffAbort = L::kOffAbort;
+  constexpr int kOffIssued = L::kOffIssued;
+  constexpr uint32_t kS1Col = L::kS1Col, kOCol = L::kOCol, kTmemCols = L::kTmemCols;
+  constexpr int BAR_FULLA = L::BAR_FULLA, BAR_EMPTYA = L::BAR_EMPTYA, BAR_FULLB = L::BAR_FULLB,
+                BAR_EMPTYB = L::BAR_EMPTYB, BAR_ZEROB = L::BAR_ZEROB, BAR_SFULL = L::BAR_SFULL,
+                BAR_SFREE = L::BAR_SFREE, BAR_PFULL = L::BAR_PFULL, BAR_ODONE = L::BAR_ODONE,
+                BAR_LASTA = L::BAR_LASTA, BAR_FULLX = L::BAR_FULLX, BAR_ZEROX = L::BAR_ZEROX,
+                BAR_ODONE2 = L::BAR_ODONE2, BAR_PVPREV = L::BAR_PVPREV, BAR_DONE = L::BAR_DONE;
+  // Role warps after the softmax warps.
+  constexpr int kWarpA = kSoftWarps, kWarpS0 = kSoftWarps + 1, kWarpB = kSoftWarps + 2,
+                kWarpS1 = kSoftWarps + 3, kWarpPV0 = kSoftWarps + 4, kWarpPV1 = kSoftWarps + 5;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -184,7 +217,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // The cache stream starts before anything else: ring A's producer sets up its
   // own barriers and issues the first fills before the CTA-wide barrier.
   const uint64_t keep = l2_evict_last_policy();   // read again by ring B
-  if (warp == 8 && lane == 0) {
+  if (warp == kWarpA && lane == 0) {
     for (int i = 0; i < kSlotsA; ++i) {
       mbar_init(bar(BAR_FULLA + i), 1);
       mbar_init(bar(BAR_EMPTYA + i), 1);
@@ -201,18 +234,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int i = 0; i < kSlotsB; ++i) {
       mbar_init(bar(BAR_FULLB + i), 1);
       mbar_init(bar(BAR_EMPTYB + i), 1);
-      mbar_init(bar(BAR_ZEROB + i), 8);
+      mbar_init(bar(BAR_ZEROB + i), kSoftWarps);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(BAR_SFULL + i), 2);   // one commit per score issuer
-      mbar_init(bar(BAR_SFREE + i), 8);
-      mbar_init(bar(BAR_PFULL + i), 8);
+      mbar_init(bar(BAR_SFREE + i), kSoftWarps);
+      mbar_init(bar(BAR_PFULL + i), kSoftWarps);
       mbar_init(bar(BAR_ODONE + i), 2);   // one commit per PV issuer
     }
     mbar_init(bar(BAR_LASTA), 2);         // every score MMA has finished
     for (int i = 0; i < 8; ++i) {
       mbar_init(bar(BAR_FULLX + i), 1);   // the last tile's borrowed pairs: one use each
-      mbar_init(bar(BAR_ZEROX + i), 8);
+      mbar_init(bar(BAR_ZEROX + i), kSoftWarps);
     }
     mbar_init(bar(BAR_ODONE2), 2);        // the score issuers' share of the last PV
     mbar_init(bar(BAR_PVPREV), 2);        // the PV of tile T-2 has finished
@@ -222,7 +255,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     s_issued[1] = 0;
     fence_mbarrier_init();
   }
-  if (warp == 8) {
+  if (warp == kWarpA) {
     __syncwarp();
     tmem_alloc(smem_u32(slot_ptr), kTmemCols);
   }
@@ -231,7 +264,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *slot_ptr;
 
-  if (warp == 8) {
+  if (warp == kWarpA) {
     // ------------------------------------------------------------ ring A (HBM)
     if (lane == 0) {
       for (int t = 0; t < T && !*abort_flag; ++t) {
@@ -245,7 +278,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     }
-  } else if (warp == 10) {
+  } else if (warp == kWarpB) {
     // ------------------------------------------------------------ ring B (L2)
     if (lane == 0) {
       prefetch_tmap(&tmap_half);
@@ -284,8 +317,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     }
-  } else if (warp < 8 || warp == 9 || warp == 11) {
-    if (warp < 8) {
+  } else if (warp < kSoftWarps || warp == kWarpS0 || warp == kWarpS1) {
+    if (warp < kSoftWarps) {
       // Query rows of the score MMA's B operand (K-major, 128-byte swizzle, one
       // 4 KB box per 64 columns): row n < 16 is bf16(q) of head n, row 16 + n
       // is bf16(q - bf16(q)).  q_abs[b, h0..h0+15, :] and q_pe[b, h0..h0+15, :]
@@ -342,16 +375,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const uint64_t c = umma_desc_sw128(sbase + kOffA, kHalfBox, 1024) +
                        static_cast<uint64_t>(((bw ? borrow_off(x) : kOffB + sl * 2 * kHalfBox) - kOffA) >> 4);
     const uint64_t pd = umma_desc_sw128(sbase + kOffP, 16, 1024) +
-                        static_cast<uint64_t>(((t & 1) * kPBytes + kh * kPSub) >> 4);
+                        static_cast<uint64_t>(((t % kPBufs) * kPBytes + kh * kPSub) >> 4);
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-      umma_bf16(tmem + kOCol + 32 * mb, c + ((ks * 2048) >> 4), pd + ((ks * 32) >> 4), idesc_o,
+      umma_bf16(tmem + kOCol + kQN * mb, c + ((ks * 2048) >> 4), pd + ((ks * 32) >> 4), idesc_o,
                 (t > 0 || kh > 0 || ks > 0) ? 1u : 0u);
     if (!bw) umma_commit(bar(BAR_EMPTYB + sl));
     return true;
   };
 
-  if (warp == 9 || warp == 11) {
+  if (warp == kWarpS0 || warp == kWarpS1) {
     // ------------------------------------------------------------ score MMA issuers
     // Issuer i takes the boxes whose stream position 9t + k has parity i, so it
     // owns ring-A slots i, i + 2, i + 4 and meets each slot's phases in order;
@@ -359,7 +392,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // thread issues a tcgen05.mma only every ~100 cycles, so the work is spread
     // over threads.
     if (lane == 0) {
-      const int i = warp == 9 ? 0 : 1;
+      const int i = warp == kWarpS0 ? 0 : 1;
       constexpr uint32_t idesc_s = umma_idesc_bf16(128, kQN, 0, 0);
       // Base descriptors; a K step only moves the 14-bit start-address field,
       // so each MMA adds an offset (16-byte units) to a base.
@@ -381,7 +414,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const uint64_t q = dQ0 + static_cast<uint64_t>((k * kQBoxBytes) >> 4);
 #pragma unroll
           for (int s4 = 0; s4 < 4; ++s4)
-            umma_bf16(dS + 32 * sb, a + ((s4 * 32) >> 4), q + ((s4 * 32) >> 4), idesc_s,
+            umma_bf16(dS + kQN * sb, a + ((s4 * 32) >> 4), q + ((s4 * 32) >> 4), idesc_s,
                       (!first || s4 > 0) ? 1u : 0u);
           umma_commit(bar(BAR_EMPTYA + sl));
           first = false;
@@ -406,12 +439,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       umma_commit(bar(BAR_DONE));
       mbar_wait_bounded(bar(BAR_DONE), 0);
     }
-  } else if (warp == 12 || warp == 13) {
+  } else if (warp == kWarpPV0 || warp == kWarpPV1) {
     // ------------------------------------------------------------ PV MMA issuers
     // Issuer i takes O^T blocks mb = i and i + 2 (ring-B slots i and i + 2); of
     // the last tile only block i (the score issuers take blocks 2 and 3).
     if (lane == 0) {
-      const int i = warp - 12;
+      const int i = warp - kWarpPV0;
       for (int t = 0; t < T; ++t) {
         if (!wait_or_abort(bar(BAR_PFULL + (t & 1)), (t >> 1) & 1, abort_flag)) break;
         bool ok = true;
@@ -424,7 +457,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       umma_commit(bar(BAR_DONE));
       mbar_wait_bounded(bar(BAR_DONE), 0);
     }
-  } else if (warp < 8) {
+  } else if (warp < kSoftWarps) {
     // ------------------------------------------------------------ softmax warps
     const int gp = warp >> 2, wq = warp & 3;
     const int hb = kHalfHeads * gp;                     // first head of this group
@@ -444,10 +477,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       float sc[kHalfHeads], tt[kHalfHeads];
       {
         uint32_t hi0[8], lo0[8], hi1[8], lo1[8];
-        tmem_ld8_nowait(tmem + lane_base + 32 * sb + hb, hi0);
-        tmem_ld8_nowait(tmem + lane_base + 32 * sb + kHeadGroup + hb, lo0);
-        tmem_ld8_nowait(tmem + lane_base + kS1Col + 32 * sb + hb, hi1);
-        tmem_ld8_nowait(tmem + lane_base + kS1Col + 32 * sb + kHeadGroup + hb, lo1);
+        tmem_ld8_nowait(tmem + lane_base + kQN * sb + hb, hi0);
+        tmem_ld8_nowait(tmem + lane_base + kQN * sb + kHeadGroup + hb, lo0);
+        tmem_ld8_nowait(tmem + lane_base + kS1Col + kQN * sb + hb, hi1);
+        tmem_ld8_nowait(tmem + lane_base + kS1Col + kQN * sb + kHeadGroup + hb, lo1);
         tmem_wait_ld();
         const bool rv = row < valid;
 #pragma unroll
@@ -491,7 +524,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-              const uint32_t col = kOCol + 32 * mb + kHeadGroup * half + hb;
+              const uint32_t col = kOCol + kQN * mb + kHeadGroup * half + hb;
               uint32_t r[8];
               float o[8];
               tmem_ld8_nowait(tmem + lane_base + col, r);
@@ -511,12 +544,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         l[h] += sc[h];
       }
       // P^T buffer sb was last read by the PV of tile t-2.
-      if (t >= 2) wait_or_abort(bar(BAR_ODONE + sb), ((t - 2) >> 1) & 1, abort_flag);
+      if (t >= kPBufs)
+        wait_or_abort(bar(BAR_ODONE + ((t - kPBufs) & 1)), ((t - kPBufs) >> 1) & 1, abort_flag);
       {
         // P^T (B operand of the PV MMA, K-major 128-byte swizzle, two 64-row
         // halves): row n < 16 is bf16(p) of head n, row 16 + n is
         // bf16(p - bf16(p)); the K index is the tile row.
-        uint8_t* pbuf = smem + kOffP + sb * kPBytes + (row >> 6) * kPSub;
+        uint8_t* pbuf = smem + kOffP + (t % kPBufs) * kPBytes + (row >> 6) * kPSub;
         const int ch = (row & 63) >> 3, w = row & 7;
 #pragma unroll
         for (int h = 0; h < kHalfHeads; ++h) {
@@ -588,8 +622,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t hi4[4][8], lo4[4][8];
 #pragma unroll
       for (int mb = 0; mb < 4; ++mb) {
-        tmem_ld8_nowait(tmem + lane_base + kOCol + 32 * mb + hb, hi4[mb]);
-        tmem_ld8_nowait(tmem + lane_base + kOCol + 32 * mb + kHeadGroup + hb, lo4[mb]);
+        tmem_ld8_nowait(tmem + lane_base + kOCol + kQN * mb + hb, hi4[mb]);
+        tmem_ld8_nowait(tmem + lane_base + kOCol + kQN * mb + kHeadGroup + hb, lo4[mb]);
       }
       tmem_wait_ld();
 #pragma unroll
@@ -606,7 +640,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kWarpA) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
@@ -850,6 +884,30 @@ __global__ void __launch_bounds__(128)
 }
 
 // ------------------------------------------------------------------------- host side
+// Heads per CTA of the decode kernel: 32 for a bf16 cache whose head count
+// allows it, else 16 (the FP8 kernel always takes 16).
+int tc_heads_per_cta(const mla_dims* d) {
+  return d->dtype == MLA_BF16 && d->heads % 32 == 0 ? 32 : kHeadGroup;
+}
+
+template <int kG>
+mla_status launch_split_tc(const CUtensorMap& tmap, const CUtensorMap& tmap_half,
+                           const SplitParams& p, int heads, cudaStream_t s, const char* who) {
+  using L = TcPlan<kG>;
+  static DeviceFlags attr_done;
+  const int dev = current_device();
+  if (!attr_done.test(dev)) {
+    if (cudaFuncSetAttribute(split_tc_kernel<kG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(L::kSmem)) != cudaSuccess) {
+      set_error("%s: cannot reserve %zu bytes of shared memory", who, L::kSmem);
+      return MLA_ERR_CUDA;
+    }
+    attr_done.set(dev);
+  }
+  dim3 grid(heads / kG, p.splits, p.B);
+  launch_pdl(split_tc_kernel<kG>, grid, dim3(L::kThreads), L::kSmem, s, tmap, tmap_half, p);
+  return MLA_OK;
+}
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   if (!fn) {
@@ -879,7 +937,8 @@ int chunk_rows(const mla_dims* d, int requested, int* splits_out) {
     if (cudaGetDevice(&dev) == cudaSuccess)
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const bool bf16 = d->dtype != MLA_F32;   // bf16 and FP8 kernels: one CTA per SM
-    const long long per_split = static_cast<long long>(d->batch) * (bf16 ? d->heads / kHeadGroup : d->heads);
+    const long long per_split =
+        static_cast<long long>(d->batch) * (bf16 ? d->heads / tc_heads_per_cta(d) : d->heads);
     const long long slots = bf16 ? sms : 4ll * sms;   // bf16: one CTA per SM
     double best = 1e300;
     splits = 1;
@@ -1037,18 +1096,10 @@ static mla_status decode_split(const char* who, const mla_dims* dims, int q_len,
         return MLA_ERR_CUDA;
       }
     }
-    static DeviceFlags attr_done;
-    const int dev = current_device();
-    if (!attr_done.test(dev)) {
-      if (cudaFuncSetAttribute(split_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               int(kTcSmem)) != cudaSuccess) {
-        set_error("%s: cannot reserve %zu bytes of shared memory", who, kTcSmem);
-        return MLA_ERR_CUDA;
-      }
-      attr_done.set(dev);
-    }
-    dim3 grid(dims->heads / kHeadGroup, p.splits, p.B);
-    launch_pdl(split_tc_kernel, grid, dim3(kTcThreads), kTcSmem, s, tmap, tmap_half, p);
+    st = tc_heads_per_cta(dims) == 32
+             ? launch_split_tc<32>(tmap, tmap_half, p, dims->heads, s, who)
+             : launch_split_tc<16>(tmap, tmap_half, p, dims->heads, s, who);
+    if (st != MLA_OK) return st;
   } else {
     dim3 grid(dims->heads, p.splits, p.B);
     split_f32_kernel<<<grid, kThreads, 0, s>>>(p);
