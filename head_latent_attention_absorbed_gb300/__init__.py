@@ -12,7 +12,8 @@ from typing import Optional
 
 from ._binding import (EXPORTED, LIB_PATH, MLA_BF16, MLA_FP8_E4M3, MLA_DEV_LENGTH_OUT_OF_RANGE,
                        MLA_DEV_PIPELINE_TIMEOUT, MLA_F32, MlaDims, MlaError, absorb_q, cache_append,
-                       decode_attn, decode_attn_multi, query_dims, wo_proj,
+                       decode_attn, decode_attn_multi, multi_num_splits, multi_workspace_bytes,
+                       query_dims, wo_proj,
                        materialize_wkq, materialize_wov, absorb_q_materialized, ov_proj,
                        decode_attn_noalloc, decode_combine, decode_split, decode_step, dims,
                        dtype_code, load, num_splits, out_proj, workspace_bytes)
@@ -20,7 +21,7 @@ from ._binding import (EXPORTED, LIB_PATH, MLA_BF16, MLA_FP8_E4M3, MLA_DEV_LENGT
 __all__ = [
     "EXPORTED", "LIB_PATH", "MLA_BF16", "MLA_F32", "MLA_FP8_E4M3", "MLA_DEV_LENGTH_OUT_OF_RANGE",
     "MLA_DEV_PIPELINE_TIMEOUT", "MlaDims", "MlaError", "absorb_q", "decode_attn",
-    "decode_attn_multi", "query_dims", "materialize_wkq", "materialize_wov",
+    "decode_attn_multi", "multi_num_splits", "multi_workspace_bytes", "query_dims", "materialize_wkq", "materialize_wov",
     "absorb_q_materialized", "ov_proj",
     "decode_attn_noalloc", "decode_split", "decode_combine", "decode_step", "dims",
     "dtype_code", "load", "num_splits", "out_proj", "workspace_bytes", "DecodeStep", "HostStep",
@@ -50,7 +51,8 @@ class DecodeStep:
         self.q_len = q_len
         self.qdims = query_dims(self.dims, q_len)     # the query side: B * q_len rows
         self.splits_requested = num_splits_requested
-        self.splits = num_splits(self.qdims, num_splits_requested)
+        self.splits = (multi_num_splits(self.dims, q_len, num_splits_requested) if q_len > 1
+                       else num_splits(self.dims, num_splits_requested))
         self.rope_base = rope_base
         self.scale = softmax_scale if softmax_scale is not None else (128 + 64) ** -0.5
         dev = torch.device(device)
@@ -60,7 +62,8 @@ class DecodeStep:
         self.o_c = torch.empty((rows, heads, 512), dtype=torch.float32, device=dev)
         self.lse = torch.empty((rows, heads), dtype=torch.float32, device=dev)
         self.out = torch.empty((rows, heads, 128), dtype=torch.float32, device=dev)
-        nbytes = workspace_bytes(self.qdims, num_splits_requested)
+        nbytes = (multi_workspace_bytes(self.dims, q_len, num_splits_requested) if q_len > 1
+                  else workspace_bytes(self.dims, num_splits_requested))
         self.workspace = torch.empty((nbytes,), dtype=torch.uint8, device=dev)
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
 

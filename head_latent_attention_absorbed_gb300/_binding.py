@@ -21,7 +21,8 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
           3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA"}
 EXPORTED = ("mla_absorb_q", "mla_decode_num_splits", "mla_decode_workspace_bytes",
             "mla_decode_attn", "mla_decode_split", "mla_decode_combine",
-            "mla_decode_attn_noalloc", "mla_decode_attn_multi", "mla_decode_step", "mla_out_proj", "mla_cache_append",
+            "mla_decode_attn_noalloc", "mla_decode_attn_multi", "mla_decode_multi_num_splits",
+            "mla_decode_multi_workspace_bytes", "mla_decode_step", "mla_out_proj", "mla_cache_append",
             "mla_wo_proj", "mla_materialize_wkq", "mla_materialize_wov",
             "mla_absorb_q_materialized", "mla_ov_proj",
             "mla_status_string", "mla_last_error_message")
@@ -68,6 +69,10 @@ def load(path: Optional[str] = None):
     lib.mla_decode_attn_multi.argtypes = [D, I32, P, P, P, P, ctypes.c_float, I32, P, SZ, P, P, P,
                                           P]
     lib.mla_decode_attn_multi.restype = ctypes.c_int
+    lib.mla_decode_multi_num_splits.argtypes = [D, I32, I32]
+    lib.mla_decode_multi_num_splits.restype = I32
+    lib.mla_decode_multi_workspace_bytes.argtypes = [D, I32, I32]
+    lib.mla_decode_multi_workspace_bytes.restype = SZ
     lib.mla_decode_attn_noalloc.argtypes = [D, P, P, P, P, ctypes.c_float, I32, P, P, P, P]
     lib.mla_decode_attn_noalloc.restype = ctypes.c_int
     lib.mla_decode_step.argtypes = [D, P, P, P, P, ctypes.c_double, P, P, ctypes.c_float, I32, P,
@@ -197,6 +202,17 @@ def decode_combine(d: MlaDims, lengths, workspace, o_c, num_splits_requested: in
 def query_dims(d: MlaDims, q_len: int) -> MlaDims:
     """The dims of the query side of a q_len-token step: batch B * q_len."""
     return MlaDims(d.batch * q_len, d.heads, d.d_c, d.d_rope, d.d_nope, d.d_v, d.s_max, d.dtype)
+
+
+def multi_num_splits(d: MlaDims, q_len: int, requested: int = 0) -> int:
+    """Chunks per sequence that decode_attn_multi uses (d: the cache's dims)."""
+    return int(load().mla_decode_multi_num_splits(ctypes.byref(d), int(q_len), int(requested)))
+
+
+def multi_workspace_bytes(d: MlaDims, q_len: int, requested: int = 0) -> int:
+    """Workspace bytes decode_attn_multi needs (d: the cache's dims)."""
+    return int(load().mla_decode_multi_workspace_bytes(ctypes.byref(d), int(q_len),
+                                                       int(requested)))
 
 
 def decode_attn_multi(d: MlaDims, q_len: int, q_abs, q_pe, cache, lengths, o_c, workspace,

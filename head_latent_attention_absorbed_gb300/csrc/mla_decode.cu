@@ -186,11 +186,17 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
   volatile int* s_issued = reinterpret_cast<volatile int*>(smem + kOffIssued);   // [2]
   uint32_t* slot_ptr = reinterpret_cast<uint32_t*>(smem + kOffSlot);
 
-  const int g = blockIdx.x, j = blockIdx.y, b = blockIdx.z;
+  // With 32 columns the CTA may hold two tokens of a multi-token step (pair):
+  // columns 0-15 are the 16 heads of query group b, 16-31 those of b + 1, the
+  // next token of the same sequence; the tiles follow the later token's rows
+  // and each 8-head softmax group masks the rows past its own token.
+  const bool pair = kG == 32 && p.tpc == 2;
+  const int g = blockIdx.x, j = blockIdx.y, b = pair ? 2 * blockIdx.z : blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // Launched after mla_absorb_q with programmatic serialization: everything up
   // to the query load (set-up, TMEM, the cache stream) overlaps that kernel.
-  const int len = clamp_length(p, b, tid == 0 && g == 0 && j == 0);
+  const int len = clamp_length(p, pair ? b + 1 : b, tid == 0 && g == 0 && j == 0);
+  const int len_first = pair ? clamp_length(p, b, tid == 0 && g == 0 && j == 0) : len;
   const int r0 = j * p.chunk;
   if (r0 >= len) return;  // chunk past the end of this sequence: nothing to do
   const int r1 = min(r0 + p.chunk, len);
@@ -202,7 +208,7 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
   const int zero_from = len - (r0 + (T - 1) * kTileRows);
   const bool zero_last = zero_from < kTileRows;
   const int row_base = cache_seq(p, b) * p.s_max + r0;
-  const int h0 = g * kHeadGroup;
+  const int h0 = g * (pair ? kHeadGroup / 2 : kHeadGroup);
   auto bar = [&](int i) { return bars + 8 * i; };
   // The last tile's latent pairs.  With T >= 2 all eight go to space that is free
   // once every score MMA has finished (ring-A slots 0-5, then the query area),
@@ -335,7 +341,17 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
 #pragma unroll
       for (int i = 0; i < 9; ++i) {
         const int idx = tid + i * kSoftThreads;
-        v[i] = idx < kNA ? qa[idx] : qp[idx - kNA];
+        if (pair) {
+          // column n: head h0 + n % 16 of query group b + n / 16
+          const int n = idx < kNA ? idx / (kDc / 4) : (idx - kNA) / (kDr / 4);
+          const size_t row = size_t(b + n / 16) * p.H + h0 + n % 16;
+          v[i] = idx < kNA ? reinterpret_cast<const float4*>(static_cast<const float*>(p.q_abs) +
+                                                             row * kDc)[idx % (kDc / 4)]
+                           : reinterpret_cast<const float4*>(static_cast<const float*>(p.q_pe) +
+                                                             row * kDr)[(idx - kNA) % (kDr / 4)];
+        } else {
+          v[i] = idx < kNA ? qa[idx] : qp[idx - kNA];
+        }
       }
 #pragma unroll
       for (int i = 0; i < 9; ++i) {
@@ -471,7 +487,10 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
     }
     for (int t = 0; t < T; ++t) {
       const int sb = t & 1;
-      const int valid = t == T - 1 ? last_valid : kTileRows;
+      int valid = t == T - 1 ? last_valid : kTileRows;
+      if (pair)   // this group's token ends at its own length
+        valid = min(max(min(r0 + p.chunk, gp < 2 ? len_first : len) - (r0 + t * kTileRows), 0),
+                    kTileRows);
       wait_or_abort(bar(BAR_SFULL + sb), (t >> 1) & 1, abort_flag);
       tc_fence_after();
       float sc[kHalfHeads], tt[kHalfHeads];
@@ -608,8 +627,10 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
     tc_fence_after();
     named_bar_sync(1, kSoftThreads);
     if (!*abort_flag) {
-      // Row (b, h, j) of the partials; heads h0 + hb + h are p.splits rows apart.
-      const size_t base = (size_t(b) * p.H + h0) * p.splits + j;
+      // Row (b, h, j) of the partials; heads h0 + hw + h are p.splits rows apart
+      // (paired tokens: groups 2 and 3 belong to query group b + 1).
+      const size_t base = (size_t(pair ? b + (gp >> 1) : b) * p.H + h0) * p.splits + j;
+      const int hw = pair ? kHalfHeads * (gp & 1) : hb;
       float inv[kHalfHeads];
 #pragma unroll
       for (int h = 0; h < kHalfHeads; ++h) {
@@ -617,7 +638,7 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
         const float L = (q4.x + q4.y) + (q4.z + q4.w);
         inv[h] = L > 0.f ? 1.f / L : 0.f;
         if (wq == 0 && lane == h)
-          p.part_lse[base + size_t(hb + h) * p.splits] = L > 0.f ? (m[h] + log2f(L)) * kLn2 : -INFINITY;
+          p.part_lse[base + size_t(hw + h) * p.splits] = L > 0.f ? (m[h] + log2f(L)) * kLn2 : -INFINITY;
       }
       uint32_t hi4[4][8], lo4[4][8];
 #pragma unroll
@@ -632,7 +653,7 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
         const uint32_t* lo = lo4[mb];
 #pragma unroll
         for (int h = 0; h < kHalfHeads; ++h)
-          p.part_o[(base + size_t(hb + h) * p.splits) * kDc + 128 * mb + 32 * wq + lane] =
+          p.part_o[(base + size_t(hw + h) * p.splits) * kDc + 128 * mb + 32 * wq + lane] =
               (__uint_as_float(hi[h]) + __uint_as_float(lo[h])) * inv[h];
       }
     }
@@ -890,6 +911,14 @@ int tc_heads_per_cta(const mla_dims* d) {
   return d->dtype == MLA_BF16 && d->heads % 32 == 0 ? 32 : kHeadGroup;
 }
 
+// Whether the bf16 kernel pairs the tokens of a multi-token step: with fewer
+// than 32 heads per 32-head slice (16, 48, ... heads) and an even q_len, one
+// CTA takes two tokens x 16 heads, so that a chunk's rows are read by half as
+// many CTAs.
+bool pair_tokens(const mla_dims* cache_dims, int q_len) {
+  return cache_dims->dtype == MLA_BF16 && cache_dims->heads % 32 != 0 && q_len % 2 == 0;
+}
+
 template <int kG>
 mla_status launch_split_tc(const CUtensorMap& tmap, const CUtensorMap& tmap_half,
                            const SplitParams& p, int heads, cudaStream_t s, const char* who) {
@@ -904,7 +933,8 @@ mla_status launch_split_tc(const CUtensorMap& tmap, const CUtensorMap& tmap_half
     }
     attr_done.set(dev);
   }
-  dim3 grid(heads / kG, p.splits, p.B);
+  // Paired tokens: 16-head slices, two query groups per CTA.
+  const dim3 grid(p.tpc == 2 ? heads / 16 : heads / kG, p.splits, p.tpc == 2 ? p.B / 2 : p.B);
   launch_pdl(split_tc_kernel<kG>, grid, dim3(L::kThreads), L::kSmem, s, tmap, tmap_half, p);
   return MLA_OK;
 }
@@ -928,7 +958,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // work in 128-row tiles, and a chunk's partial last tile costs about what a
 // full one does (measured: 16 chunks of 256 rows beat 19 of 216 on 8 x 4096
 // rows), so for them a chunk's rows count rounded up to whole tiles.
-int chunk_rows(const mla_dims* d, int requested, int* splits_out) {
+int chunk_rows(const mla_dims* d, int requested, int* splits_out, bool pair = false) {
   const int S = d->s_max;
   const int max_splits = (S + kChunkAlign - 1) / kChunkAlign;
   int splits = requested;
@@ -938,7 +968,8 @@ int chunk_rows(const mla_dims* d, int requested, int* splits_out) {
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const bool bf16 = d->dtype != MLA_F32;   // bf16 and FP8 kernels: one CTA per SM
     const long long per_split =
-        static_cast<long long>(d->batch) * (bf16 ? d->heads / tc_heads_per_cta(d) : d->heads);
+        pair ? static_cast<long long>(d->batch) * d->heads / 32
+             : static_cast<long long>(d->batch) * (bf16 ? d->heads / tc_heads_per_cta(d) : d->heads);
     const long long slots = bf16 ? sms : 4ll * sms;   // bf16: one CTA per SM
     double best = 1e300;
     splits = 1;
@@ -986,6 +1017,26 @@ extern "C" int32_t mla_decode_num_splits(const mla_dims* dims, int32_t requested
   return splits;
 }
 
+extern "C" int32_t mla_decode_multi_num_splits(const mla_dims* dims, int32_t q_len,
+                                               int32_t requested) {
+  if (check_dims(dims, "mla_decode_multi_num_splits") != MLA_OK || q_len < 1) return 0;
+  mla_dims qd = *dims;
+  qd.batch = dims->batch * q_len;
+  int splits = 0;
+  chunk_rows(&qd, requested, &splits, pair_tokens(dims, q_len));
+  return splits;
+}
+
+extern "C" size_t mla_decode_multi_workspace_bytes(const mla_dims* dims, int32_t q_len,
+                                                   int32_t requested) {
+  if (check_dims(dims, "mla_decode_multi_workspace_bytes") != MLA_OK || q_len < 1) return 0;
+  mla_dims qd = *dims;
+  qd.batch = dims->batch * q_len;
+  int splits = 0;
+  chunk_rows(&qd, requested, &splits, pair_tokens(dims, q_len));
+  return workspace_bytes(&qd, splits);
+}
+
 extern "C" size_t mla_decode_workspace_bytes(const mla_dims* dims, int32_t requested) {
   if (check_dims(dims, "mla_decode_workspace_bytes") != MLA_OK) return 0;
   int splits = 0;
@@ -1008,6 +1059,7 @@ static mla_status prepare(const char* who, const mla_dims* dims, int q_len, cons
     set_error("%s: q_len=%d must be >= 1 with batch*q_len <= 2^30", who, q_len);
     return MLA_ERR_INVALID_ARG;
   }
+  const bool pair = pair_tokens(dims, q_len);
   mla_dims qd = *dims;   // one row of queries per (sequence, token)
   qd.batch = dims->batch * q_len;
   dims = &qd;
@@ -1028,7 +1080,7 @@ static mla_status prepare(const char* who, const mla_dims* dims, int q_len, cons
     return MLA_ERR_INVALID_ARG;
   }
   int splits = 0;
-  const int chunk = chunk_rows(dims, num_splits, &splits);
+  const int chunk = chunk_rows(dims, num_splits, &splits, pair);
   const size_t need = workspace_bytes(dims, splits);
   if (ws_bytes < need) {
     set_error("%s: workspace %zu bytes < %zu needed", who, ws_bytes, need);
@@ -1048,6 +1100,7 @@ static mla_status prepare(const char* who, const mla_dims* dims, int q_len, cons
   p->status = dev_status;
   p->B = dims->batch;
   p->q_len = q_len;
+  p->tpc = pair ? 2 : 1;
   p->H = dims->heads;
   p->s_max = dims->s_max;
   p->splits = splits;
@@ -1096,7 +1149,7 @@ static mla_status decode_split(const char* who, const mla_dims* dims, int q_len,
         return MLA_ERR_CUDA;
       }
     }
-    st = tc_heads_per_cta(dims) == 32
+    st = p.tpc == 2 || tc_heads_per_cta(dims) == 32
              ? launch_split_tc<32>(tmap, tmap_half, p, dims->heads, s, who)
              : launch_split_tc<16>(tmap, tmap_half, p, dims->heads, s, who);
     if (st != MLA_OK) return st;

@@ -16,6 +16,8 @@ struct SplitParams {
   int32_t* status;
   int B, H, s_max, splits, chunk;  // B counts query groups: cache sequences x q_len
   int q_len;                // query tokens per cache sequence (1: ordinary decode)
+  int tpc;                  // bf16 kernel, 32 columns: query groups per CTA (2: two tokens
+                            // x 16 heads; 1: 32 heads of one token)
   float scale_log2;         // softmax_scale * log2(e)
   uint8_t* q_img;           // FP8: the query's E4M3 image per (sequence, head group)
 };

@@ -209,13 +209,18 @@ mla_status mla_decode_combine(const mla_dims* dims, const int32_t* lengths, int3
  *       [B, s_max, d_c + d_rope]; lengths [B] int32 (device),
  *       q_len <= lengths[b] <= s_max
  * q_len >= 1
- * workspace  >= mla_decode_workspace_bytes(dims', num_splits) bytes, where
- *       dims' is dims with batch = B*q_len (mla_decode_num_splits(dims',
- *       num_splits) gives the chunk count used).
+ * workspace  >= mla_decode_multi_workspace_bytes(dims, q_len, num_splits)
+ *       bytes (mla_decode_multi_num_splits(dims, q_len, num_splits) gives the
+ *       chunk count used).
  * A length below q_len or above s_max sets MLA_DEV_LENGTH_OUT_OF_RANGE in
  * dev_status; a token left with no rows gets o_c = 0 and lse = -inf.
- * Each token streams its rows separately (the q_len reads of a row meet in L2).
+ * With a bf16 cache, an even q_len and a head count that is not a multiple of
+ * 32, one CTA of the decode kernel takes two tokens x 16 heads, so that a
+ * chunk's rows are read by q_len / 2 CTAs; otherwise each token's CTAs read
+ * them (the reads of a row meet in L2).
  */
+int32_t mla_decode_multi_num_splits(const mla_dims* dims, int32_t q_len, int32_t requested);
+size_t mla_decode_multi_workspace_bytes(const mla_dims* dims, int32_t q_len, int32_t requested);
 mla_status mla_decode_attn_multi(const mla_dims* dims, int32_t q_len, const void* q_abs,
                                  const void* q_pe, const void* cache, const int32_t* lengths,
                                  float softmax_scale, int32_t num_splits, void* workspace,

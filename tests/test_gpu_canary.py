@@ -57,7 +57,7 @@ def test_decode_calls_stay_in_bounds(cuda_lib, dtype, H, q_len, splits):
     o_c, g_oc = guarded((R, H, 512), torch.float32)
     lse, g_lse = guarded((R, H), torch.float32)
     out, g_out = guarded((R, H, 128), torch.float32)
-    ws, g_ws = guarded((mla.workspace_bytes(qd, splits),), torch.uint8)
+    ws, g_ws = guarded((mla.multi_workspace_bytes(d, q_len, splits),), torch.uint8)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     scale = cfg.softmax_scale
     if q_len == 1:

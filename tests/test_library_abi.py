@@ -118,9 +118,10 @@ def test_host_validation_of_later_calls(lib):
     # multi-token: q_len must be >= 1; the workspace is sized for B * q_len query rows
     assert so.mla_decode_attn_multi(ctypes.byref(d), 0, P(good), P(good), P(good), P(good), 0.1,
                                     0, P(good), 1 << 30, P(good), None, None, None) == 1
-    qd = mla.query_dims(d, 4)
-    need = mla.workspace_bytes(qd, 0)
+    need = mla.multi_workspace_bytes(d, 4, 0)
     assert need > mla.workspace_bytes(d, 0)
+    assert mla.multi_workspace_bytes(d, 1, 0) == mla.workspace_bytes(d, 0)
+    assert mla.multi_num_splits(d, 1, 0) == mla.num_splits(d, 0)
     assert so.mla_decode_attn_multi(ctypes.byref(d), 4, P(good), P(good), P(good), P(good), 0.1,
                                     0, P(good), need - 1, P(good), None, None, None) == 3
     assert so.mla_decode_attn_multi(ctypes.byref(d), 4, P(good), P(good), P(good), None, 0.1,
