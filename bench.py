@@ -428,8 +428,9 @@ def run_op(args, cfg, rank):
 
 def launches_per_step(cfg) -> int:
     """Library kernels one step launches: absorb, (FP8: the query image), split,
-    then the fused combine + W_UV (one token, bf16/FP8) or combine and out_proj."""
-    fused = cfg.q_len == 1 and cfg.dtype != "f32"
+    then the fused combine + W_UV (one token, bf16/FP8, batch x heads <= 256) or
+    combine and out_proj."""
+    fused = cfg.q_len == 1 and cfg.dtype != "f32" and cfg.batch * cfg.heads <= 256
     return 1 + (1 if cfg.dtype == "fp8" else 0) + 1 + (1 if fused else 2)
 
 

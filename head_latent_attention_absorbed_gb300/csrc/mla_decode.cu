@@ -1233,6 +1233,9 @@ extern "C" mla_status mla_decode_attn(const mla_dims* dims, const void* q_abs, c
   return mla_decode_combine(dims, lengths, num_splits, workspace, ws_bytes, o_c, lse, stream);
 }
 
+// Largest batch x heads for which mla_decode_step fuses the combine with W_UV.
+constexpr long long kFusedTailMax = 256;
+
 // Bytes of the cache mla_decode_step asks L2 to fetch during its absorb kernel.
 constexpr long long kPrefetchBudget = 16ll << 20;
 
@@ -1328,6 +1331,15 @@ extern "C" mla_status mla_decode_step(const mla_dims* dims, const void* q_nope, 
   st = mla_decode_split(dims, q_abs, q_pe, cache, lengths, softmax_scale, num_splits, workspace,
                         ws_bytes, dev_status, stream);
   if (st != MLA_OK) return st;
+  // The fused tail reads W_UV[h] once per sequence: for small batches that
+  // saves a kernel boundary, for large ones the separate combine and out_proj,
+  // which read W_UV once, win (measured: B*H = 128 fused 20.3 against 22.8 us;
+  // B*H = 1024 102.6 against 99.5 us; B*H = 4096 501 against 446 us).
+  if (static_cast<long long>(dims->batch) * dims->heads > kFusedTailMax) {
+    st = mla_decode_combine(dims, lengths, num_splits, workspace, ws_bytes, o_c, lse, stream);
+    if (st != MLA_OK) return st;
+    return mla_out_proj(dims, o_c, w_uv, out, stream);
+  }
   launch_pdl(combine_out_kernel, dim3(dims->heads, dims->batch, kDv / kOutRows), dim3(128), 0,
              static_cast<cudaStream_t>(stream), p, static_cast<const __nv_bfloat16*>(w_uv), o_c,
              lse, out);

@@ -359,10 +359,12 @@ mla_status mla_ov_proj(const mla_dims* dims, int32_t d_out, const float* o_c, co
  * mla_out_proj in one call, with the same arguments, meanings and results
  * (q_abs, q_pe, o_c, lse and out are all written).
  *
- * With dtype MLA_BF16 the combine and the value up-projection run as one kernel
- * (each CTA merges one (sequence, head)'s chunk partials and applies 32 rows of
- * W_UV[h] to them in fp32), launched with programmatic stream serialization
- * after the split kernel; before its wait it reads only w_uv and lengths.
+ * With dtype MLA_BF16 or MLA_FP8_E4M3 and batch x heads <= 256 the combine and
+ * the value up-projection run as one kernel (each CTA merges one (sequence,
+ * head)'s chunk partials and applies 32 rows of W_UV[h] to them in fp32),
+ * launched with programmatic stream serialization after the split kernel;
+ * before its wait it reads only w_uv and lengths.  Larger batches run
+ * mla_decode_combine and mla_out_proj, which read W_UV once per step.
  * With MLA_F32 the three calls run in order.  Every argument is checked before
  * anything is enqueued.  lse may be NULL.
  *
