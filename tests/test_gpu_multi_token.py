@@ -113,7 +113,7 @@ def test_bench_shape_four_tokens(cuda_lib, cfg):
     compare(gpu, ref, bs, cfg.dtype)
 
 
-@pytest.mark.parametrize("H,q_len", [(32, 4), (32, 2), (128, 2)])
+@pytest.mark.parametrize("H,q_len", [(32, 4), (32, 2), (128, 2), (48, 2), (48, 4)])
 def test_multi_token_head_groups(cuda_lib, H, q_len):
     """Several 16-head groups with several tokens: the split CTAs of one chunk
     share the cache stream across head groups and tokens (clusters of up to 8)."""
