@@ -178,26 +178,35 @@ __global__ void __launch_bounds__(128)
 }
 
 // ---------------------------------------------------------------------- out_proj, bf16
-// grid (H, d_v/8): CTA (h, eb) owns outputs e in [8eb, 8eb+8) for the whole
-// batch; warp w contracts the 128-wide quarter [128w, 128w+128) of d_c and the
-// four partial sums meet in shared memory.  W_UV's rows are K-contiguous, so
-// its B fragments come straight from global memory; o_c (fp32) enters the mma
-// as bf16 hi + lo parts, keeping its rounding near 2^-17 relative.  Every
-// load of a batch tile is issued before the first mma.
+// grid (H, d_v / (8 kNB)): CTA (h, eb) owns outputs e in [8 kNB eb, 8 kNB (eb + 1))
+// for the whole batch, as kNB blocks of 8 that share the o_c fragments; warp w
+// contracts the 128-wide quarter [128w, 128w+128) of d_c and the four partial
+// sums meet in shared memory.  W_UV's rows are K-contiguous, so its B fragments
+// come straight from global memory; o_c (fp32) enters the mma as bf16 hi + lo
+// parts, keeping its rounding near 2^-17 relative.  Every load of a batch tile
+// is issued before the first mma.  kNB = 1 spreads the weights over the most
+// CTAs (small batches); kNB = 4 reads each head's o_c rows 4 times instead of
+// 16 (large batches).
+template <int kNB>
 __global__ void __launch_bounds__(128)
     out_proj_bf16_kernel(const float* __restrict__ o_c, const __nv_bfloat16* __restrict__ w_uv,
                          float* __restrict__ out, int B, int H) {
-  __shared__ float red[4][16][9];
+  constexpr int kE = 8 * kNB;   // outputs per CTA
+  __shared__ float red[4][16][kE + 1];
   const int h = blockIdx.x, eb = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int gq = lane >> 2, cq = lane & 3;
   const int kw = 128 * warp;
-  uint32_t bf[8][2];
-  const __nv_bfloat16* wrow = w_uv + (size_t(h) * kDv + 8 * eb + gq) * kDc + kw + 2 * cq;
+  uint32_t bf[kNB][8][2];
 #pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    bf[ks][0] = *reinterpret_cast<const uint32_t*>(wrow + 16 * ks);
-    bf[ks][1] = *reinterpret_cast<const uint32_t*>(wrow + 16 * ks + 8);
+  for (int nb = 0; nb < kNB; ++nb) {
+    const __nv_bfloat16* wrow =
+        w_uv + (size_t(h) * kDv + kE * eb + 8 * nb + gq) * kDc + kw + 2 * cq;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      bf[nb][ks][0] = *reinterpret_cast<const uint32_t*>(wrow + 16 * ks);
+      bf[nb][ks][1] = *reinterpret_cast<const uint32_t*>(wrow + 16 * ks + 8);
+    }
   }
   // Launched after the combine with programmatic serialization: the weight
   // loads above overlap it; o_c is its result.
@@ -215,25 +224,36 @@ __global__ void __launch_bounds__(128)
       x[ks][2] = bA < B ? *reinterpret_cast<const float2*>(rA + 16 * ks + 8) : z;
       x[ks][3] = bB < B ? *reinterpret_cast<const float2*>(rB + 16 * ks + 8) : z;
     }
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[kNB][4];
+#pragma unroll
+    for (int nb = 0; nb < kNB; ++nb)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[nb][r] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int r = 0; r < 4; ++r) split_bf16(x[ks][r].x, x[ks][r].y, hi[r], lo[r]);
-      mma_bf16(acc, hi, bf[ks][0], bf[ks][1]);
-      mma_bf16(acc, lo, bf[ks][0], bf[ks][1]);
+#pragma unroll
+      for (int nb = 0; nb < kNB; ++nb) {
+        mma_bf16(acc[nb], hi, bf[nb][ks][0], bf[nb][ks][1]);
+        mma_bf16(acc[nb], lo, bf[nb][ks][0], bf[nb][ks][1]);
+      }
     }
-    red[warp][gq][2 * cq] = acc[0];
-    red[warp][gq][2 * cq + 1] = acc[1];
-    red[warp][gq + 8][2 * cq] = acc[2];
-    red[warp][gq + 8][2 * cq + 1] = acc[3];
+#pragma unroll
+    for (int nb = 0; nb < kNB; ++nb) {
+      red[warp][gq][8 * nb + 2 * cq] = acc[nb][0];
+      red[warp][gq][8 * nb + 2 * cq + 1] = acc[nb][1];
+      red[warp][gq + 8][8 * nb + 2 * cq] = acc[nb][2];
+      red[warp][gq + 8][8 * nb + 2 * cq + 1] = acc[nb][3];
+    }
     __syncthreads();
-    {
-      const int r = tid >> 3, e = tid & 7;  // 16 rows x 8 outputs
+#pragma unroll
+    for (int i = tid; i < 16 * kE; i += 128) {   // 16 rows x kE outputs
+      const int r = i / kE, e = i % kE;
       const int b = mt * 16 + r;
       if (b < B)
-        out[(size_t(b) * H + h) * kDv + 8 * eb + e] =
+        out[(size_t(b) * H + h) * kDv + kE * eb + e] =
             red[0][r][e] + red[1][r][e] + red[2][r][e] + red[3][r][e];
     }
     __syncthreads();
@@ -474,8 +494,12 @@ extern "C" mla_status mla_out_proj(const mla_dims* dims, const float* o_c, const
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int B = dims->batch, H = dims->heads;
   if (dims->dtype != MLA_F32) {
-    launch_pdl(out_proj_bf16_kernel, dim3(H, kDv / 8), dim3(128), 0, s, o_c,
-               static_cast<const __nv_bfloat16*>(w_uv), static_cast<float*>(out), B, H);
+    if (B > 16)
+      launch_pdl(out_proj_bf16_kernel<4>, dim3(H, kDv / 32), dim3(128), 0, s, o_c,
+                 static_cast<const __nv_bfloat16*>(w_uv), static_cast<float*>(out), B, H);
+    else
+      launch_pdl(out_proj_bf16_kernel<1>, dim3(H, kDv / 8), dim3(128), 0, s, o_c,
+                 static_cast<const __nv_bfloat16*>(w_uv), static_cast<float*>(out), B, H);
   } else {
     out_proj_f32_kernel<<<dim3(H, B), 128, 0, s>>>(o_c, static_cast<const float*>(w_uv),
                                                    static_cast<float*>(out), B, H);
