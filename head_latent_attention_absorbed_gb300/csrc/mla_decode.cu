@@ -27,7 +27,7 @@ constexpr int kChunkAlign = 8;   // chunk sizes are multiples of 8 rows
 constexpr int kThreads = kWarps * 32;
 
 // ---------------------------------------------------------------------------- bf16 split kernel
-// One CTA per (16-head group, KV chunk, sequence).  Every tcgen05.mma covers
+// One CTA per (head group of 16 or 32, KV chunk, sequence).  Every tcgen05.mma covers
 // 128 cache rows (a K=16 step costs the same for M=64 as for M=128 at N=32, so
 // 128-row tiles halve the tensor time per row), but a 128-row tile (147 KB)
 // cannot stay resident from its scores to its PV product.  The cache
@@ -133,24 +133,26 @@ __device__ __forceinline__ float reduce8_heads(float v[8], int lane) {
   return kMax ? fmaxf(v[0], o) : v[0] + o;
 }
 
-// Roles (448 threads):
-//   warp 8  : TMEM allocation; one lane runs ring A (9 score boxes per tile)
-//   warp 10 : one lane runs ring B (8 latent box pairs per tile: four
-//             128-column blocks x two 64-row halves)
-//   warps 9, 11: score MMAs, each over alternate boxes of the stream, into two
-//               accumulators S_0, S_1 (summed by the softmax):
-//               S[128 x 32] = C[128 x 576] . Q^T  (M=128, N=32: the 16 heads'
-//               hi and lo query parts; S double-buffered in TMEM)
-//   warps 12, 13: PV MMAs, each over two of the four O^T blocks:
-//               O^T[512 x 32] += C^T[512 x 128] . P^T[128 x 32]  (M=128 blocks,
+// Roles, for kG heads per CTA (16: 448 threads; 32: 704), with W = kG / 2
+// softmax warps and N = 2 kG:
+//   warp W    : TMEM allocation; one lane runs ring A (9 score boxes per tile)
+//   warp W+2  : one lane runs ring B (8 latent box pairs per tile: four
+//               128-column blocks x two 64-row halves)
+//   warps W+1, W+3: score MMAs, each over alternate boxes of the stream, into
+//               two accumulators S_0, S_1 (summed by the softmax):
+//               S[128 x N] = C[128 x 576] . Q^T  (M=128, N: the heads' hi and
+//               lo query parts; S double-buffered in TMEM)
+//   warps W+4, W+5: PV MMAs, each over two of the four O^T blocks:
+//               O^T[512 x N] += C^T[512 x 128] . P^T[128 x N]  (M=128 blocks,
 //               each in two 64-row halves; C read MN-major from a ring-B pair)
 //             A thread issues one tcgen05.mma per ~100 cycles whatever the
-//             shape, so four issuing threads keep the tensor pipe fed.
-//   warps 0-7: one tile row per thread, heads 0-7 in warps 0-3 and 8-15 in
-//             warps 4-7: softmax across the rows, P^T (hi | lo bf16) to shared
-//             memory; O^T accumulates in TMEM against a reference maximum per
-//             head that moves only when a tile's maximum exceeds it by 2^8
-//             (then O^T is rescaled in TMEM).
+//             shape (N = 32 or 64), so four issuing threads keep the tensor
+//             pipe fed.
+//   warps 0..W-1: one tile row per thread, a group of four warps per 8 heads
+//             (heads 8i..8i+7 in warps 4i..4i+3): softmax across the rows, P^T
+//             (hi | lo bf16) to shared memory; O^T accumulates in TMEM against a
+//             reference maximum per head that moves only when a tile's maximum
+//             exceeds it by 2^8 (then O^T is rescaled in TMEM).
 // The fp32 query and P reach the tensor core as bf16 hi + lo pairs, so their
 // rounding stays near 2^-17 relative.
 template <int kG>

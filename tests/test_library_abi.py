@@ -147,3 +147,19 @@ def test_planner_prefers_whole_tiles(lib):
         assert mla.num_splits(mla.dims(8, 16, 4096, dt), 0) == 16
     s32 = mla.num_splits(mla.dims(8, 16, 4096, mla.MLA_F32), 0)
     assert 1 <= s32 <= 512
+
+
+def test_multi_token_planning_counts_paired_ctas(lib):
+    """With a bf16 cache, 16 heads and an even q_len, two tokens share a CTA, so
+    the multi-token planner fills the GPU with more chunks than the unpaired one
+    would; its workspace covers every (sequence, token, head, chunk) partial."""
+    mla, _ = lib
+    d = mla.dims(8, 16, 4096, mla.MLA_BF16)
+    paired = mla.multi_num_splits(d, 4, 0)
+    unpaired = mla.num_splits(mla.query_dims(d, 4), 0)
+    assert paired > unpaired
+    assert mla.multi_workspace_bytes(d, 4, 0) == mla.workspace_bytes(mla.query_dims(d, 4), paired)
+    # odd q_len, FP8 and 32-head caches are not paired
+    for dd, q in ((d, 3), (mla.dims(8, 16, 4096, mla.MLA_FP8_E4M3), 4),
+                  (mla.dims(8, 32, 4096, mla.MLA_BF16), 4)):
+        assert mla.multi_num_splits(dd, q, 0) == mla.num_splits(mla.query_dims(dd, q), 0)
