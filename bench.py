@@ -585,13 +585,10 @@ def main_with(args, rank: int, world: int, local: int = 0):
         e2e = {"value": whole_job_rate(cache_bytes, Ke, world, e_ms / 1e3) / 1e9, "unit": "GB/s",
                "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": Ke,
                "tokens_per_s": whole_job_rate(cfg.batch * cfg.q_len, Ke, world, e_ms / 1e3),
-               "path": ("DecodeStep.capture: per step one CUDA-graph replay of mla_decode_step "
-                        "on pinned host buffers -- its kernels read the queries, lengths and "
-                        "positions and write o over the host link, no copy nodes"
-                        if cfg.q_len == 1 else
-                        "DecodeStep.capture: per step one pinned host->device copy of the "
-                        "queries, lengths and positions, the C-ABI calls, one device->host "
-                        "copy of o; one CUDA-graph replay per step")}
+               "path": ("DecodeStep.capture: per step one CUDA-graph replay of mla_decode_step"
+                        + ("" if cfg.q_len == 1 else "_multi") + " on pinned host buffers -- its "
+                        "kernels read the queries, lengths and positions and write o over the "
+                        "host link, no copy nodes")}
 
     peak, peak_kind = measured_peaks()
     achieved = cache_bytes / split_avg_s / 1e9

@@ -12,7 +12,8 @@ from typing import Optional
 
 from ._binding import (EXPORTED, LIB_PATH, MLA_BF16, MLA_FP8_E4M3, MLA_DEV_LENGTH_OUT_OF_RANGE,
                        MLA_DEV_PIPELINE_TIMEOUT, MLA_F32, MlaDims, MlaError, absorb_q, cache_append,
-                       decode_attn, decode_attn_multi, multi_num_splits, multi_workspace_bytes,
+                       decode_attn, decode_attn_multi, decode_step_multi, multi_num_splits,
+                       multi_workspace_bytes,
                        query_dims, wo_proj,
                        materialize_wkq, materialize_wov, absorb_q_materialized, ov_proj,
                        decode_attn_noalloc, decode_combine, decode_split, decode_step, dims,
@@ -21,7 +22,7 @@ from ._binding import (EXPORTED, LIB_PATH, MLA_BF16, MLA_FP8_E4M3, MLA_DEV_LENGT
 __all__ = [
     "EXPORTED", "LIB_PATH", "MLA_BF16", "MLA_F32", "MLA_FP8_E4M3", "MLA_DEV_LENGTH_OUT_OF_RANGE",
     "MLA_DEV_PIPELINE_TIMEOUT", "MlaDims", "MlaError", "absorb_q", "decode_attn",
-    "decode_attn_multi", "multi_num_splits", "multi_workspace_bytes", "query_dims", "materialize_wkq", "materialize_wov",
+    "decode_attn_multi", "decode_step_multi", "multi_num_splits", "multi_workspace_bytes", "query_dims", "materialize_wkq", "materialize_wov",
     "absorb_q_materialized", "ov_proj",
     "decode_attn_noalloc", "decode_split", "decode_combine", "decode_step", "dims",
     "dtype_code", "load", "num_splits", "out_proj", "workspace_bytes", "DecodeStep", "HostStep",
@@ -68,16 +69,20 @@ class DecodeStep:
         self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
 
     def run(self, q_nope, q_rope, cache, lengths, positions, w_uk, w_uv, stream=None, out=None):
-        """The whole step: one library call (mla_decode_step) for one token per
-        sequence, the three calls with mla_decode_attn_multi for q_len > 1.
+        """The whole step in one library call (mla_decode_step, or
+        mla_decode_step_multi for q_len > 1).
 
-        With one token per sequence, q_nope, q_rope, lengths, positions and
-        ``out`` (o, default: this step's device buffer) may be pinned host
-        tensors, read and written by the kernels directly.
+        q_nope, q_rope, lengths, positions and ``out`` (o, default: this step's
+        device buffer) may be pinned host tensors, read and written by the
+        kernels directly.
         """
-        if self.q_len > 1:
-            return self.run_calls(q_nope, q_rope, cache, lengths, positions, w_uk, w_uv, stream)
         o = self.out if out is None else out
+        if self.q_len > 1:
+            decode_step_multi(self.dims, self.q_len, q_nope, q_rope, w_uk, positions, cache,
+                              lengths, w_uv, self.workspace, self.q_abs, self.q_pe, self.o_c, o,
+                              self.scale, self.rope_base, self.splits_requested, self.lse,
+                              self.status, stream)
+            return o
         decode_step(self.dims, q_nope, q_rope, w_uk, positions, cache, lengths, w_uv,
                     self.workspace, self.q_abs, self.q_pe, self.o_c, o, self.scale,
                     self.rope_base, self.splits_requested, self.lse, self.status, stream)
@@ -104,12 +109,10 @@ class DecodeStep:
 
         Returns a ``HostStep``: pinned host tensors ``q_nope``, ``q_rope``,
         ``lengths``, ``positions`` (the step's inputs, filled by the caller) and
-        ``out`` (o, written by the step), and ``replay()``.  With one token per
-        sequence every replay runs mla_decode_step on the host tensors
-        themselves: its kernels read the inputs and write o over the host link
-        (no copies).  With several tokens per sequence every replay copies the
-        four inputs to the device in one transfer (they share one pinned block),
-        runs the calls, and copies o back in one transfer.
+        ``out`` (o, written by the step), and ``replay()``.  Every replay runs
+        mla_decode_step (mla_decode_step_multi for several tokens per sequence)
+        on the host tensors themselves: its kernels read the inputs and write o
+        over the host link, with no copies.
         """
         return HostStep(self, cache, w_uk, w_uv)
 
@@ -133,7 +136,6 @@ class HostStep:
             off += (n * e + 255) // 256 * 256        # every piece 256-byte aligned
         dev = step.q_abs.device
         self._h_block = torch.empty((off,), dtype=torch.uint8).pin_memory()
-        self._d_block = torch.empty((off,), dtype=torch.uint8, device=dev)
 
         def view(block, i):
             name, shape, dtype, e = pieces[i]
@@ -144,25 +146,18 @@ class HostStep:
 
         self.q_nope, self.q_rope, self.lengths, self.positions = (view(self._h_block, i)
                                                                    for i in range(4))
-        d = [view(self._d_block, i) for i in range(4)]
         self.out = torch.empty(step.out.shape, dtype=step.out.dtype).pin_memory()
-        # Bytes that cross the host link each step: the inputs' own bytes when the
-        # kernels read them in place, the whole (padded) block when it is copied.
-        self.h2d_bytes = (sum(t.numel() * t.element_size()
-                              for t in (self.q_nope, self.q_rope, self.lengths, self.positions))
-                          if step.q_len == 1 else off)
+        # Bytes that cross the host link each step: the kernels read the inputs
+        # and write o in place (mla_decode_step and mla_decode_step_multi accept
+        # page-locked host buffers).
+        self.h2d_bytes = sum(t.numel() * t.element_size()
+                             for t in (self.q_nope, self.q_rope, self.lengths, self.positions))
         self.d2h_bytes = self.out.numel() * self.out.element_size()
 
-        self.zero_copy = step.q_len == 1
         h = (self.q_nope, self.q_rope, self.lengths, self.positions)
 
         def body():
-            if self.zero_copy:
-                step.run(h[0], h[1], cache, h[2], h[3], w_uk, w_uv, out=self.out)
-                return
-            self._d_block.copy_(self._h_block, non_blocking=True)
-            o = step.run(d[0], d[1], cache, d[2], d[3], w_uk, w_uv)
-            self.out.copy_(o, non_blocking=True)
+            step.run(h[0], h[1], cache, h[2], h[3], w_uk, w_uv, out=self.out)
 
         # One run outside capture (module loading, kernel attributes); the inputs
         # are whatever the block holds, so start from valid lengths.
@@ -176,7 +171,6 @@ class HostStep:
         side = torch.cuda.Stream(device=dev)
         with torch.cuda.graph(self._graph, stream=side):
             body()
-        self._keep = d
 
     def replay(self):
         self._graph.replay()

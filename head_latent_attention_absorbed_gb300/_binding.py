@@ -22,7 +22,7 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
 EXPORTED = ("mla_absorb_q", "mla_decode_num_splits", "mla_decode_workspace_bytes",
             "mla_decode_attn", "mla_decode_split", "mla_decode_combine",
             "mla_decode_attn_noalloc", "mla_decode_attn_multi", "mla_decode_multi_num_splits",
-            "mla_decode_multi_workspace_bytes", "mla_decode_step", "mla_out_proj", "mla_cache_append",
+            "mla_decode_multi_workspace_bytes", "mla_decode_step", "mla_decode_step_multi", "mla_out_proj", "mla_cache_append",
             "mla_wo_proj", "mla_materialize_wkq", "mla_materialize_wov",
             "mla_absorb_q_materialized", "mla_ov_proj",
             "mla_status_string", "mla_last_error_message")
@@ -78,6 +78,9 @@ def load(path: Optional[str] = None):
     lib.mla_decode_step.argtypes = [D, P, P, P, P, ctypes.c_double, P, P, ctypes.c_float, I32, P,
                                     P, SZ, P, P, P, P, P, P, P]
     lib.mla_decode_step.restype = ctypes.c_int
+    lib.mla_decode_step_multi.argtypes = [D, I32, P, P, P, P, ctypes.c_double, P, P, ctypes.c_float,
+                                          I32, P, P, SZ, P, P, P, P, P, P, P]
+    lib.mla_decode_step_multi.restype = ctypes.c_int
     lib.mla_cache_append.argtypes = [D, I32, P, P, P, ctypes.c_double, P, P, P]
     lib.mla_cache_append.restype = ctypes.c_int
     lib.mla_wo_proj.argtypes = [D, I32, P, P, P, P]
@@ -263,6 +266,23 @@ def decode_step(d: MlaDims, q_nope, q_rope, w_uk, positions, cache, lengths, w_u
                                   float(softmax_scale), int(num_splits_requested), _ptr(w_uv),
                                   _ptr(workspace), nbytes, _ptr(q_abs), _ptr(q_pe), _ptr(o_c),
                                   _ptr(lse), _ptr(out), _ptr(dev_status), _stream(stream)))
+
+
+def decode_step_multi(d: MlaDims, q_len: int, q_nope, q_rope, w_uk, positions, cache, lengths,
+                      w_uv, workspace, q_abs, q_pe, o_c, out, softmax_scale: float,
+                      rope_base: float = 10000.0, num_splits_requested: int = 0, lse=None,
+                      dev_status=None, stream=None) -> None:
+    """decode_step for q_len tokens per sequence (d: the cache's dims; the query
+    side has B * q_len rows).  The step's inputs and out may be pinned host tensors."""
+    _cuda_contig(w_uk, cache, w_uv, workspace, q_abs, q_pe, o_c, lse, dev_status)
+    _cuda_or_pinned(q_nope, q_rope, positions, lengths, out)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(load().mla_decode_step_multi(ctypes.byref(d), int(q_len), _ptr(q_nope), _ptr(q_rope),
+                                        _ptr(w_uk), _ptr(positions), float(rope_base),
+                                        _ptr(cache), _ptr(lengths), float(softmax_scale),
+                                        int(num_splits_requested), _ptr(w_uv), _ptr(workspace),
+                                        nbytes, _ptr(q_abs), _ptr(q_pe), _ptr(o_c), _ptr(lse),
+                                        _ptr(out), _ptr(dev_status), _stream(stream)))
 
 
 def out_proj(d: MlaDims, o_c, w_uv, out, stream=None) -> None:

@@ -1254,15 +1254,22 @@ static bool device_addressable(const void* ptr) {
   return a.type == cudaMemoryTypeHost && a.devicePointer != nullptr;
 }
 
-extern "C" mla_status mla_decode_step(const mla_dims* dims, const void* q_nope, const void* q_rope,
-                                      const void* w_uk, const int32_t* positions, double rope_base,
-                                      const void* cache, const int32_t* lengths, float softmax_scale,
-                                      int32_t num_splits, const void* w_uv, void* workspace,
-                                      size_t ws_bytes, float* q_abs, float* q_pe, float* o_c,
-                                      float* lse, float* out, int32_t* dev_status, void* stream) {
-  const char* who = "mla_decode_step";
+// The whole step for q_len tokens per sequence (mla_decode_step: q_len = 1).
+static mla_status decode_step(const char* who, const mla_dims* dims, int q_len,
+                              const void* q_nope, const void* q_rope, const void* w_uk,
+                              const int32_t* positions, double rope_base, const void* cache,
+                              const int32_t* lengths, float softmax_scale, int32_t num_splits,
+                              const void* w_uv, void* workspace, size_t ws_bytes, float* q_abs,
+                              float* q_pe, float* o_c, float* lse, float* out,
+                              int32_t* dev_status, void* stream) {
   mla_status st = check_dims(dims, who);
   if (st != MLA_OK) return st;
+  if (q_len < 1 || static_cast<long long>(dims->batch) * q_len > (1ll << 30)) {
+    set_error("%s: q_len=%d must be >= 1 with batch*q_len <= 2^30", who, q_len);
+    return MLA_ERR_INVALID_ARG;
+  }
+  mla_dims qd = *dims;   // the query side: one row per (sequence, token)
+  qd.batch = dims->batch * q_len;
   if (!o_c || !out || !w_uv || !aligned16(o_c) || !aligned16(out) || !aligned16(w_uv)) {
     set_error("%s: o_c, out and w_uv must be non-NULL 16-byte aligned pointers", who);
     return MLA_ERR_INVALID_ARG;
@@ -1279,18 +1286,22 @@ extern "C" mla_status mla_decode_step(const mla_dims* dims, const void* q_nope, 
   }
   if (dims->dtype == MLA_F32) {
     // The fp32 path has no fused tail: the three calls in order.
-    st = mla_absorb_q(dims, q_nope, q_rope, w_uk, positions, rope_base, q_abs, q_pe, stream);
+    st = mla_absorb_q(&qd, q_nope, q_rope, w_uk, positions, rope_base, q_abs, q_pe, stream);
     if (st != MLA_OK) return st;
-    st = mla_decode_attn(dims, q_abs, q_pe, cache, lengths, softmax_scale, num_splits, workspace,
-                         ws_bytes, o_c, lse, dev_status, stream);
+    st = q_len == 1 ? mla_decode_attn(dims, q_abs, q_pe, cache, lengths, softmax_scale,
+                                      num_splits, workspace, ws_bytes, o_c, lse, dev_status,
+                                      stream)
+                    : mla_decode_attn_multi(dims, q_len, q_abs, q_pe, cache, lengths,
+                                            softmax_scale, num_splits, workspace, ws_bytes, o_c,
+                                            lse, dev_status, stream);
     if (st != MLA_OK) return st;
-    return mla_out_proj(dims, o_c, w_uv, out, stream);
+    return mla_out_proj(&qd, o_c, w_uv, out, stream);
   }
   // Validate everything before the first launch, so an argument error leaves
   // nothing half-enqueued.
   SplitParams p;
-  st = prepare(who, dims, 1, q_abs, q_pe, cache, lengths, softmax_scale, num_splits, workspace,
-               ws_bytes, dev_status, &p);
+  st = prepare(who, dims, q_len, q_abs, q_pe, cache, lengths, softmax_scale, num_splits,
+               workspace, ws_bytes, dev_status, &p);
   if (st != MLA_OK) return st;
   CachePrefetch pf{};
   bool single_wave = false;
@@ -1321,31 +1332,61 @@ extern "C" mla_status mla_decode_step(const mla_dims* dims, const void* q_nope, 
       cudaGetLastError();
       sms = 0;
     }
-    single_wave = nchunk * (dims->heads / kHeadGroup) <= sms;
+    const long long ctas =
+        static_cast<long long>(p.splits) *
+        (p.tpc == 2 ? static_cast<long long>(p.B / 2) * (dims->heads / 16)
+                    : static_cast<long long>(p.B) * (dims->heads / tc_heads_per_cta(dims)));
+    single_wave = ctas <= sms;
     if (pf.rows <= 0 || !single_wave) pf.cache = nullptr;
   }
   // The early launch of the absorb pays only with a one-wave decode grid: with
   // several waves the early decode CTAs crowd out the previous step's tail
   // (measured: 64 ragged sequences, step 103 -> 122 us with it).
-  st = absorb_q(who, dims, q_nope, q_rope, w_uk, positions, rope_base, q_abs, q_pe, stream, pf,
+  st = absorb_q(who, &qd, q_nope, q_rope, w_uk, positions, rope_base, q_abs, q_pe, stream, pf,
                 single_wave);
   if (st != MLA_OK) return st;
-  st = mla_decode_split(dims, q_abs, q_pe, cache, lengths, softmax_scale, num_splits, workspace,
-                        ws_bytes, dev_status, stream);
+  st = decode_split(who, dims, q_len, q_abs, q_pe, cache, lengths, softmax_scale, num_splits,
+                    workspace, ws_bytes, dev_status, stream);
   if (st != MLA_OK) return st;
   // The fused tail reads W_UV[h] once per sequence: for small batches that
   // saves a kernel boundary, for large ones the separate combine and out_proj,
   // which read W_UV once, win (measured: B*H = 128 fused 20.3 against 22.8 us;
   // B*H = 1024 102.6 against 99.5 us; B*H = 4096 501 against 446 us).
-  if (static_cast<long long>(dims->batch) * dims->heads > kFusedTailMax) {
-    st = mla_decode_combine(dims, lengths, num_splits, workspace, ws_bytes, o_c, lse, stream);
+  if (static_cast<long long>(qd.batch) * dims->heads > kFusedTailMax) {
+    st = decode_combine(who, dims, q_len, lengths, num_splits, workspace, ws_bytes, o_c, lse,
+                        stream);
     if (st != MLA_OK) return st;
-    return mla_out_proj(dims, o_c, w_uv, out, stream);
+    return mla_out_proj(&qd, o_c, w_uv, out, stream);
   }
-  launch_pdl(combine_out_kernel, dim3(dims->heads, dims->batch, kDv / kOutRows), dim3(128), 0,
+  launch_pdl(combine_out_kernel, dim3(dims->heads, qd.batch, kDv / kOutRows), dim3(128), 0,
              static_cast<cudaStream_t>(stream), p, static_cast<const __nv_bfloat16*>(w_uv), o_c,
              lse, out);
   return launch_status(who);
+}
+
+extern "C" mla_status mla_decode_step(const mla_dims* dims, const void* q_nope, const void* q_rope,
+                                      const void* w_uk, const int32_t* positions, double rope_base,
+                                      const void* cache, const int32_t* lengths, float softmax_scale,
+                                      int32_t num_splits, const void* w_uv, void* workspace,
+                                      size_t ws_bytes, float* q_abs, float* q_pe, float* o_c,
+                                      float* lse, float* out, int32_t* dev_status, void* stream) {
+  return decode_step("mla_decode_step", dims, 1, q_nope, q_rope, w_uk, positions, rope_base,
+                     cache, lengths, softmax_scale, num_splits, w_uv, workspace, ws_bytes, q_abs,
+                     q_pe, o_c, lse, out, dev_status, stream);
+}
+
+extern "C" mla_status mla_decode_step_multi(const mla_dims* dims, int32_t q_len,
+                                            const void* q_nope, const void* q_rope,
+                                            const void* w_uk, const int32_t* positions,
+                                            double rope_base, const void* cache,
+                                            const int32_t* lengths, float softmax_scale,
+                                            int32_t num_splits, const void* w_uv,
+                                            void* workspace, size_t ws_bytes, float* q_abs,
+                                            float* q_pe, float* o_c, float* lse, float* out,
+                                            int32_t* dev_status, void* stream) {
+  return decode_step("mla_decode_step_multi", dims, q_len, q_nope, q_rope, w_uk, positions,
+                     rope_base, cache, lengths, softmax_scale, num_splits, w_uv, workspace,
+                     ws_bytes, q_abs, q_pe, o_c, lse, out, dev_status, stream);
 }
 
 // ------------------------------------------------------- fixed scratch, no allocation

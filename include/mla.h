@@ -387,6 +387,24 @@ mla_status mla_decode_step(const mla_dims* dims, const void* q_nope, const void*
                            size_t workspace_bytes, float* q_abs, float* q_pe, float* o_c,
                            float* lse, float* out, int32_t* dev_status, void* stream);
 
+/*
+ * mla_decode_step_multi -- mla_decode_step for q_len new tokens per sequence:
+ * mla_absorb_q and mla_out_proj over the B*q_len query rows around
+ * mla_decode_attn_multi (causal within the block), with the same launch
+ * overlap, cache prefetch and host-buffer rules as mla_decode_step.
+ * q_nope, q_rope [B*q_len, H, .], positions [B*q_len]; lengths [B];
+ * q_abs, q_pe, o_c, lse, out have B*q_len rows; workspace >=
+ * mla_decode_multi_workspace_bytes(dims, q_len, num_splits).  q_len = 1 is
+ * mla_decode_step.
+ */
+mla_status mla_decode_step_multi(const mla_dims* dims, int32_t q_len, const void* q_nope,
+                                 const void* q_rope, const void* w_uk, const int32_t* positions,
+                                 double rope_base, const void* cache, const int32_t* lengths,
+                                 float softmax_scale, int32_t num_splits, const void* w_uv,
+                                 void* workspace, size_t workspace_bytes, float* q_abs,
+                                 float* q_pe, float* o_c, float* lse, float* out,
+                                 int32_t* dev_status, void* stream);
+
 /* Static English name of a status code. */
 const char* mla_status_string(mla_status status);
 

@@ -124,3 +124,50 @@ def test_multi_token_head_groups(cuda_lib, H, q_len):
     assert gpu["status"] == 0
     ref, bs = run_oracle(inp)
     compare(gpu, ref, bs, "bf16")
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_separate_calls_multi_token(cuda_lib, dtype):
+    """The three calls (absorb over B*q_len rows, mla_decode_attn_multi, out_proj)
+    match the oracle as the one-call step does."""
+    import head_latent_attention_absorbed_gb300 as mla
+    cfg = small(dtype, 4)
+    inp = make_inputs(cfg, seed=90, poison_tail=True,
+                      lengths=torch.tensor([4, 129, 300], dtype=torch.int32))
+    step = mla.DecodeStep(cfg.batch, cfg.heads, cfg.s_max, cache_storage(cfg), q_len=4)
+    d = lambda t: t.cuda().contiguous()
+    step.run_calls(d(inp.q_nope), d(inp.q_rope), d(inp.cache), d(inp.lengths), d(inp.positions),
+                   d(inp.w_uk), d(inp.w_uv))
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    f = lambda t: t.detach().cpu().double().numpy().reshape((cfg.batch, 4) + tuple(t.shape[1:]))
+    gpu = dict(q_abs=f(step.q_abs), q_pe=f(step.q_pe), o_c=f(step.o_c), lse=f(step.lse),
+               o=f(step.out))
+    ref, bs = run_oracle(inp)
+    compare(gpu, ref, bs, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_captured_multi_token_step_from_host_memory(cuda_lib, dtype):
+    """DecodeStep.capture with four tokens: the kernels read the pinned host inputs
+    and write o in place; a replay equals the device-resident eager step bit for bit."""
+    import numpy as np
+    import head_latent_attention_absorbed_gb300 as mla
+    cfg = small(dtype, 4)
+    inp = make_inputs(cfg, seed=91, poison_tail=True,
+                      lengths=torch.tensor([4, 129, 300], dtype=torch.int32))
+    step = mla.DecodeStep(cfg.batch, cfg.heads, cfg.s_max, cache_storage(cfg), q_len=4)
+    cache, w_uk, w_uv = inp.cache.cuda(), inp.w_uk.cuda(), inp.w_uv.cuda()
+    hs = step.capture(cache, w_uk, w_uv)
+    hs.q_nope.copy_(inp.q_nope)
+    hs.q_rope.copy_(inp.q_rope)
+    hs.lengths.copy_(inp.lengths)
+    hs.positions.copy_(inp.positions)
+    hs.replay()
+    torch.cuda.synchronize()
+    got = hs.out.double().numpy().copy()
+    eager = step.run(inp.q_nope.cuda(), inp.q_rope.cuda(), cache, inp.lengths.cuda(),
+                     inp.positions.cuda(), w_uk, w_uv)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(got, eager.double().cpu().numpy())
+    assert int(step.status.item()) == 0
