@@ -22,7 +22,8 @@ from ._binding import (EXPORTED, LIB_PATH, MLA_BF16, MLA_FP8_E4M3, MLA_DEV_LENGT
 __all__ = [
     "EXPORTED", "LIB_PATH", "MLA_BF16", "MLA_F32", "MLA_FP8_E4M3", "MLA_DEV_LENGTH_OUT_OF_RANGE",
     "MLA_DEV_PIPELINE_TIMEOUT", "MlaDims", "MlaError", "absorb_q", "decode_attn",
-    "decode_attn_multi", "decode_step_multi", "multi_num_splits", "multi_workspace_bytes", "query_dims", "materialize_wkq", "materialize_wov",
+    "decode_attn_multi", "decode_step_multi", "multi_num_splits", "multi_workspace_bytes",
+    "query_dims", "materialize_wkq", "materialize_wov",
     "absorb_q_materialized", "ov_proj",
     "decode_attn_noalloc", "decode_split", "decode_combine", "decode_step", "dims",
     "dtype_code", "load", "num_splits", "out_proj", "workspace_bytes", "DecodeStep", "HostStep",

@@ -22,7 +22,8 @@ STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
 EXPORTED = ("mla_absorb_q", "mla_decode_num_splits", "mla_decode_workspace_bytes",
             "mla_decode_attn", "mla_decode_split", "mla_decode_combine",
             "mla_decode_attn_noalloc", "mla_decode_attn_multi", "mla_decode_multi_num_splits",
-            "mla_decode_multi_workspace_bytes", "mla_decode_step", "mla_decode_step_multi", "mla_out_proj", "mla_cache_append",
+            "mla_decode_multi_workspace_bytes", "mla_decode_step", "mla_decode_step_multi",
+            "mla_out_proj", "mla_cache_append",
             "mla_wo_proj", "mla_materialize_wkq", "mla_materialize_wov",
             "mla_absorb_q_materialized", "mla_ov_proj",
             "mla_status_string", "mla_last_error_message")
