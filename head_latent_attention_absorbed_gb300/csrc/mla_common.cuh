@@ -4,6 +4,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <atomic>
@@ -327,6 +328,10 @@ struct CachePrefetch {
   const int32_t* lengths;     // [B] device
   int B, s_max, chunk, splits, row_bytes, rows;
 };
+
+// The driver's tensor-map encoder (cuTensorMapEncodeTiled), looked up once per
+// process, thread-safely; NULL if the driver does not provide it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // One bit per device ordinal (below 64): kernel attributes such as the
 // dynamic shared-memory limit belong to a device, so a set-up made once per

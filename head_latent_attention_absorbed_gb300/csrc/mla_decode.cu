@@ -940,19 +940,6 @@ mla_status launch_split_tc(const CUtensorMap& tmap, const CUtensorMap& tmap_half
   launch_pdl(split_tc_kernel<kG>, grid, dim3(L::kThreads), L::kSmem, s, tmap, tmap_half, p);
   return MLA_OK;
 }
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
-  return fn;
-}
-
 // Rows per KV chunk (a multiple of kChunkAlign rows) and the resulting chunk
 // count.  With `requested` = 0 the count minimises a makespan estimate: waves
 // of CTAs over the SMs times (rows per chunk + a fixed per-CTA cost), plus the
@@ -1128,7 +1115,7 @@ static mla_status decode_split(const char* who, const mla_dims* dims, int q_len,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dims->dtype == MLA_FP8_E4M3) return launch_split_fp8(p, cache, s, who);
   if (dims->dtype == MLA_BF16) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) {
       set_error("%s: cuTensorMapEncodeTiled is not available from the driver", who);
       return MLA_ERR_CUDA;

@@ -530,24 +530,11 @@ __global__ void __launch_bounds__(kF8Threads, 1)
   if (tid == 0 && *abort_flag) report(p.status, MLA_DEV_PIPELINE_TIMEOUT);
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 fp8_tmap_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
-  return fn;
-}
-
 }  // namespace
 
 mla_status launch_split_fp8(const SplitParams& p, const void* cache, cudaStream_t stream,
                             const char* who) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = fp8_tmap_encoder();
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) {
     set_error("%s: cuTensorMapEncodeTiled is not available from the driver", who);
     return MLA_ERR_CUDA;

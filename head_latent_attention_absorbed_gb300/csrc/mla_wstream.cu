@@ -22,24 +22,12 @@
 #include <cuda_fp8.h>
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include "mla_wstream.cuh"
 
 namespace mla {
 namespace {
-
-// The driver's tensor-map encoder, looked up once.
-PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  if (!fn) {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-  }
-  return fn;
-}
 
 constexpr int kWsThreads = 224;
 constexpr int kWsBox = 64;                           // K elements per box
@@ -411,6 +399,8 @@ struct Kernel {
   static int max_clusters(int ks, size_t smem) {
     static int cache_ks[8] = {0}, cache_val[8] = {0};
     static size_t cache_smem[8] = {0};
+    static std::mutex cache_mutex;   // the cache is shared by every host thread
+    std::lock_guard<std::mutex> lock(cache_mutex);
     for (int i = 0; i < 8; ++i)
       if (cache_ks[i] == ks && cache_smem[i] == smem) return cache_val[i];
     cudaLaunchConfig_t cfg = {};
@@ -511,7 +501,7 @@ mla_status wstream_launch(const WStreamJob& j, cudaStream_t stream, const char* 
               kWsBox);
     return MLA_ERR_UNSUPPORTED;
   }
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tmap_encoder();
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
   if (!enc) {
     set_error("%s: cuTensorMapEncodeTiled is not available from the driver", who);
     return MLA_ERR_CUDA;
