@@ -221,6 +221,15 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
   auto borrow_off = [&](int x) {
     return x < kSlotsA ? kOffA + x * kBoxBytes : kOffQ + (x - kSlotsA) * kBoxBytes;
   };
+  // With six ring-A slots the stream ends with the last tile's boxes 3-8 still
+  // in ring A, and its latent boxes 4, 5 and 6, 7 sit in adjacent slots whatever
+  // T is.  So the last tile's O^T blocks 2 and 3 take their PV operand from ring
+  // A in place, and only boxes 0-3 are read again -- as whole 128-row boxes, into
+  // the ring-B space -- instead of all eight pairs.
+  constexpr bool kResidentTail = kSlotsA == 6;
+  auto tail_box_off = [&](int k) {   // the last tile's latent box k (0-7)
+    return k < 4 ? kOffB + k * kBoxBytes : kOffA + ((9 * (T - 1) + k) % kSlotsA) * kBoxBytes;
+  };
 
   // The cache stream starts before anything else: ring A's producer sets up its
   // own barriers and issues the first fills before the CTA-wide barrier.
@@ -292,6 +301,18 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
       prefetch_tmap(&tmap_half);
       const uint64_t stream = l2_evict_first_policy();
       for (int t = 0; t < T && !*abort_flag; ++t) {
+        if (kResidentTail && t == T - 1) {
+          // Boxes 0-3 of the last tile into the ring-B space, once ring B is free
+          // (the PV of tile T-2 has finished) and every score MMA has finished.
+          if (T >= 2 && !wait_or_abort(bar(BAR_PVPREV), 0, abort_flag)) break;
+          if (!wait_or_abort(bar(BAR_LASTA), 0, abort_flag)) break;
+          for (int k = 0; k < 4; ++k) {
+            mbar_arrive_expect_tx(bar(BAR_FULLX + k), kBoxBytes);
+            tma_load_2d(sbase + kOffB + k * kBoxBytes, &tmap, 64 * k, row_base + t * kTileRows,
+                        bar(BAR_FULLX + k), stream);
+          }
+          break;
+        }
         // From tile 1 on, wait until the score MMAs of tile t are issued (its P
         // follows soon); tile 0's pairs take the empty ring at once.
         if (t > 0 && !(t == T - 1 && T >= 2)) {
@@ -378,6 +399,27 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
   constexpr uint32_t idesc_o = umma_idesc_bf16(128, kQN, 1, 0);
   auto pv_unit = [&](int t, int u) -> bool {
     const int mb = u & 3, kh = u >> 2;
+    if (kResidentTail && t == T - 1) {
+      // Block mb's two 64-column boxes 2mb, 2mb + 1 (128 rows each, kBoxBytes
+      // apart): read again into ring B (mb 0, 1) or still in ring A (mb 2, 3).
+      const int k0 = 2 * mb;
+      if (zero_last && (!wait_or_abort(bar(BAR_ZEROX + k0), 0, abort_flag) ||
+                        !wait_or_abort(bar(BAR_ZEROX + k0 + 1), 0, abort_flag)))
+        return false;
+      if (mb < 2 && (!wait_or_abort(bar(BAR_FULLX + k0), 0, abort_flag) ||
+                     !wait_or_abort(bar(BAR_FULLX + k0 + 1), 0, abort_flag)))
+        return false;
+      tc_fence_after();
+      const uint64_t c = umma_desc_sw128(sbase + kOffA, kBoxBytes, 1024) +
+                         static_cast<uint64_t>((tail_box_off(k0) + kh * kHalfBox - kOffA) >> 4);
+      const uint64_t pd = umma_desc_sw128(sbase + kOffP, 16, 1024) +
+                          static_cast<uint64_t>(((t % kPBufs) * kPBytes + kh * kPSub) >> 4);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(tmem + kOCol + kQN * mb, c + ((ks * 2048) >> 4), pd + ((ks * 32) >> 4), idesc_o,
+                  (t > 0 || kh > 0 || ks > 0) ? 1u : 0u);
+      return true;
+    }
     const int pos = 8 * t + u, sl = pos % kSlotsB;
     const bool bw = borrowed(t, u);
     const int x = bw ? borrow_x(u) : 0;
@@ -591,7 +633,21 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
         // anything, NaN included) so that P = 0 times such a row adds exactly 0.
         // Borrowed pairs have single-use barriers; ring-B pairs of the last tile
         // exist only when it is the first tile too (first fills).
-        for (int u = 0; u < 8; ++u) {
+        if (kResidentTail) {
+          // Whole 128-row boxes: 0-3 once read again, 4-7 in ring A (landed
+          // before the scores this thread has read).
+          const int nrow = kTileRows - zero_from;
+          for (int k = 0; k < 8; ++k) {
+            if (k < 4) wait_or_abort(bar(BAR_FULLX + k), 0, abort_flag);
+            uint8_t* box = smem + tail_box_off(k) + zero_from * 128;
+            for (int c = tid; c < nrow * 8; c += kSoftThreads)
+              *reinterpret_cast<uint4*>(box + c * 16) = make_uint4(0, 0, 0, 0);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar(BAR_ZEROX + k));
+          }
+        }
+        for (int u = 0; u < 8 && !kResidentTail; ++u) {
           const int kh = u >> 2;
           const int first = max(0, zero_from - 64 * kh);   // first row of this half to clear
           const int nrow = 64 - first;
