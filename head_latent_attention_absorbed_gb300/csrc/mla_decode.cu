@@ -221,14 +221,21 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
   auto borrow_off = [&](int x) {
     return x < kSlotsA ? kOffA + x * kBoxBytes : kOffQ + (x - kSlotsA) * kBoxBytes;
   };
-  // With six ring-A slots the stream ends with the last tile's boxes 3-8 still
-  // in ring A, and its latent boxes 4, 5 and 6, 7 sit in adjacent slots whatever
-  // T is.  So the last tile's O^T blocks 2 and 3 take their PV operand from ring
-  // A in place, and only boxes 0-3 are read again -- as whole 128-row boxes, into
-  // the ring-B space -- instead of all eight pairs.
+  // With six ring-A slots the last tile streams its RoPE box first, so the
+  // stream ends with its latent boxes 2-7 still in ring A (stream positions 3-8
+  // of the tile; 9 (T-1) is 0 or 3 modulo 6).  O^T block mb (boxes 2mb, 2mb + 1)
+  // takes its PV operand from ring A in place when the two boxes sit in adjacent
+  // slots: blocks 1 and 3 always, block 2 when T is even.  The other blocks' boxes
+  // are read again, as whole 128-row boxes, into the ring-B space.
   constexpr bool kResidentTail = kSlotsA == 6;
+  auto box_at = [&](int t, int j) {   // latent/RoPE box at position j of tile t
+    return kResidentTail && t == T - 1 ? (j + 8) % 9 : j;
+  };
+  auto tail_slot = [&](int k) { return (9 * (T - 1) + k + 1) % kSlotsA; };
+  auto tail_res = [&](int mb) { return mb >= 1 && tail_slot(2 * mb) != kSlotsA - 1; };
   auto tail_box_off = [&](int k) {   // the last tile's latent box k (0-7)
-    return k < 4 ? kOffB + k * kBoxBytes : kOffA + ((9 * (T - 1) + k) % kSlotsA) * kBoxBytes;
+    return tail_res(k >> 1) ? kOffA + tail_slot(k) * kBoxBytes
+                            : kOffB + (k < 2 ? k : k - 2) * kBoxBytes;
   };
 
   // The cache stream starts before anything else: ring A's producer sets up its
@@ -243,7 +250,7 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
     prefetch_tmap(&tmap);
     for (int pos = 0; pos < kSlotsA && pos < 9 * T; ++pos) {
       mbar_arrive_expect_tx(bar(BAR_FULLA + pos), kBoxBytes);
-      tma_load_2d(sbase + kOffA + pos * kBoxBytes, &tmap, 64 * (pos % 9),
+      tma_load_2d(sbase + kOffA + pos * kBoxBytes, &tmap, 64 * box_at(pos / 9, pos % 9),
                   row_base + (pos / 9) * kTileRows, bar(BAR_FULLA + pos), keep);
     }
   }
@@ -290,8 +297,8 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
           if (pos < kSlotsA) continue;   // issued before the CTA-wide barrier
           if (use > 0 && !wait_or_abort(bar(BAR_EMPTYA + sl), (use - 1) & 1, abort_flag)) break;
           mbar_arrive_expect_tx(bar(BAR_FULLA + sl), kBoxBytes);
-          tma_load_2d(sbase + kOffA + sl * kBoxBytes, &tmap, 64 * k, row_base + t * kTileRows,
-                      bar(BAR_FULLA + sl), keep);
+          tma_load_2d(sbase + kOffA + sl * kBoxBytes, &tmap, 64 * box_at(t, k),
+                      row_base + t * kTileRows, bar(BAR_FULLA + sl), keep);
         }
       }
     }
@@ -302,13 +309,15 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
       const uint64_t stream = l2_evict_first_policy();
       for (int t = 0; t < T && !*abort_flag; ++t) {
         if (kResidentTail && t == T - 1) {
-          // Boxes 0-3 of the last tile into the ring-B space, once ring B is free
-          // (the PV of tile T-2 has finished) and every score MMA has finished.
+          // The last tile's boxes that left ring A, into the ring-B space, once
+          // ring B is free (the PV of tile T-2 has finished) and every score MMA
+          // has finished.
           if (T >= 2 && !wait_or_abort(bar(BAR_PVPREV), 0, abort_flag)) break;
           if (!wait_or_abort(bar(BAR_LASTA), 0, abort_flag)) break;
-          for (int k = 0; k < 4; ++k) {
+          for (int k = 0; k < 8; ++k) {
+            if (tail_res(k >> 1)) continue;
             mbar_arrive_expect_tx(bar(BAR_FULLX + k), kBoxBytes);
-            tma_load_2d(sbase + kOffB + k * kBoxBytes, &tmap, 64 * k, row_base + t * kTileRows,
+            tma_load_2d(sbase + tail_box_off(k), &tmap, 64 * k, row_base + t * kTileRows,
                         bar(BAR_FULLX + k), stream);
           }
           break;
@@ -401,12 +410,12 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
     const int mb = u & 3, kh = u >> 2;
     if (kResidentTail && t == T - 1) {
       // Block mb's two 64-column boxes 2mb, 2mb + 1 (128 rows each, kBoxBytes
-      // apart): read again into ring B (mb 0, 1) or still in ring A (mb 2, 3).
+      // apart): still in ring A or read again into the ring-B space.
       const int k0 = 2 * mb;
       if (zero_last && (!wait_or_abort(bar(BAR_ZEROX + k0), 0, abort_flag) ||
                         !wait_or_abort(bar(BAR_ZEROX + k0 + 1), 0, abort_flag)))
         return false;
-      if (mb < 2 && (!wait_or_abort(bar(BAR_FULLX + k0), 0, abort_flag) ||
+      if (!tail_res(mb) && (!wait_or_abort(bar(BAR_FULLX + k0), 0, abort_flag) ||
                      !wait_or_abort(bar(BAR_FULLX + k0 + 1), 0, abort_flag)))
         return false;
       tc_fence_after();
@@ -471,7 +480,7 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
           }
           tc_fence_after();
           const uint64_t a = dA0 + static_cast<uint64_t>((sl * kBoxBytes) >> 4);
-          const uint64_t q = dQ0 + static_cast<uint64_t>((k * kQBoxBytes) >> 4);
+          const uint64_t q = dQ0 + static_cast<uint64_t>((box_at(t, k) * kQBoxBytes) >> 4);
 #pragma unroll
           for (int s4 = 0; s4 < 4; ++s4)
             umma_bf16(dS + kQN * sb, a + ((s4 * 32) >> 4), q + ((s4 * 32) >> 4), idesc_s,
@@ -634,11 +643,11 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
         // Borrowed pairs have single-use barriers; ring-B pairs of the last tile
         // exist only when it is the first tile too (first fills).
         if (kResidentTail) {
-          // Whole 128-row boxes: 0-3 once read again, 4-7 in ring A (landed
-          // before the scores this thread has read).
+          // Whole 128-row boxes: in ring A (landed before the scores this thread
+          // has read) or once read again.
           const int nrow = kTileRows - zero_from;
           for (int k = 0; k < 8; ++k) {
-            if (k < 4) wait_or_abort(bar(BAR_FULLX + k), 0, abort_flag);
+            if (!tail_res(k >> 1)) wait_or_abort(bar(BAR_FULLX + k), 0, abort_flag);
             uint8_t* box = smem + tail_box_off(k) + zero_from * 128;
             for (int c = tid; c < nrow * 8; c += kSoftThreads)
               *reinterpret_cast<uint4*>(box + c * 16) = make_uint4(0, 0, 0, 0);
