@@ -495,15 +495,23 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     named_bar_sync(1, kF8Soft);
     if (!*abort_flag) {
       const size_t base = (size_t(b) * p.H + h0) * p.splits + j;
-      float inv[kHalf];
+      // 1/L by the approximate reciprocal (within 2 ulp for the L > 0 reached
+      // here, 1 <= L <= 2^8 x rows), branch-free; lane h of the first warp of
+      // each group writes head h's log-sum-exp.
+      float inv[kHalf], Lme = 0.f, mme = 0.f;
 #pragma unroll
       for (int h = 0; h < kHalf; ++h) {
         const float4 q4 = *reinterpret_cast<const float4*>(lsum + (hb + h) * 4);
         const float L = (q4.x + q4.y) + (q4.z + q4.w);
-        inv[h] = L > 0.f ? 1.f / L : 0.f;
-        if (wq == 0 && lane == h)
-          p.part_lse[base + size_t(hb + h) * p.splits] = L > 0.f ? (m[h] + log2f(L)) * kLn2 : -INFINITY;
+        inv[h] = L > 0.f ? __fdividef(1.f, L) : 0.f;
+        Lme = lane == h ? L : Lme;
+        mme = lane == h ? m[h] : mme;
       }
+      if (wq == 0 && lane < kHalf)
+        p.part_lse[base + size_t(hb + lane) * p.splits] =
+            Lme > 0.f ? (mme + log2f(Lme)) * kLn2 : -INFINITY;
+      float* row0 = p.part_o + (base + size_t(hb) * p.splits) * kDc + 32 * wq + lane;
+      const size_t head_stride = size_t(p.splits) * kDc;
 #pragma unroll
       for (int mb = 0; mb < 4; ++mb) {
         uint32_t o1[8], o2[8], o3[8];
@@ -511,12 +519,12 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         tmem_ld8_nowait(tmem + lane_base + kOCol + kPN * mb + kHeadGroup + hb, o2);
         tmem_ld8_nowait(tmem + lane_base + kOCol + kPN * mb + 2 * kHeadGroup + hb, o3);
         tmem_wait_ld();
+        float* row = row0 + 128 * mb;
 #pragma unroll
-        for (int h = 0; h < kHalf; ++h)
-          p.part_o[(base + size_t(hb + h) * p.splits) * kDc + 128 * mb + 32 * wq + lane] =
-              (__uint_as_float(o1[h]) +
-               (__uint_as_float(o2[h]) * 0.0625f + __uint_as_float(o3[h]) * 0.00390625f)) *
-              inv[h];
+        for (int h = 0; h < kHalf; ++h, row += head_stride)
+          *row = (__uint_as_float(o1[h]) +
+                  (__uint_as_float(o2[h]) * 0.0625f + __uint_as_float(o3[h]) * 0.00390625f)) *
+                 inv[h];
       }
     }
   }
