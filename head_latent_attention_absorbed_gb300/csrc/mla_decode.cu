@@ -195,12 +195,43 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
   const bool pair = kG == 32 && p.tpc == 2;
   const int g = blockIdx.x, j = blockIdx.y, b = pair ? 2 * blockIdx.z : blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r0 = j * p.chunk;
+  const int row_base = cache_seq(p, b) * p.s_max + r0;
+  auto bar = [&](int i) { return bars + 8 * i; };
+
+  // The cache stream starts before anything else: ring A's producer sets up its
+  // own barriers and issues tile 0's first six boxes (stream positions 0-5 hold
+  // boxes 0-5; the RoPE-first order below applies only to a last tile after
+  // another) before the CTA-wide barrier.  They need only the chunk's first
+  // row, so in a one-wave grid they go out before the sequence length is known.
+  const uint64_t keep = l2_evict_last_policy();   // read again by ring B
+  auto first_fills = [&]() {
+    for (int i = 0; i < kSlotsA; ++i) {
+      mbar_init(bar(BAR_FULLA + i), 1);
+      mbar_init(bar(BAR_EMPTYA + i), 1);
+    }
+    fence_mbarrier_init();
+    prefetch_tmap(&tmap);
+    for (int pos = 0; pos < kSlotsA; ++pos) {
+      mbar_arrive_expect_tx(bar(BAR_FULLA + pos), kBoxBytes);
+      tma_load_2d(sbase + kOffA + pos * kBoxBytes, &tmap, 64 * pos, row_base,
+                  bar(BAR_FULLA + pos), keep);
+    }
+  };
+  const bool ring_a = warp == kWarpA && lane == 0;
+  if (ring_a && p.fill_early) first_fills();
   // Launched after mla_absorb_q with programmatic serialization: everything up
   // to the query load (set-up, TMEM, the cache stream) overlaps that kernel.
   const int len = clamp_length(p, pair ? b + 1 : b, tid == 0 && g == 0 && j == 0);
   const int len_first = pair ? clamp_length(p, b, tid == 0 && g == 0 && j == 0) : len;
-  const int r0 = j * p.chunk;
-  if (r0 >= len) return;  // chunk past the end of this sequence: nothing to do
+  if (r0 >= len) {
+    // Chunk past the end of this sequence: nothing to do once early copies
+    // (into this CTA's shared memory) have landed.
+    if (ring_a && p.fill_early)
+      for (int pos = 0; pos < kSlotsA; ++pos) mbar_wait_bounded(bar(BAR_FULLA + pos), 0);
+    return;
+  }
+  if (ring_a && !p.fill_early) first_fills();
   const int r1 = min(r0 + p.chunk, len);
   const int T = (r1 - r0 + kTileRows - 1) / kTileRows;
   const int last_valid = r1 - (r0 + (T - 1) * kTileRows);   // rows of the last tile
@@ -209,9 +240,7 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
   // rows may hold anything (NaN included): those are zeroed before the PV.
   const int zero_from = len - (r0 + (T - 1) * kTileRows);
   const bool zero_last = zero_from < kTileRows;
-  const int row_base = cache_seq(p, b) * p.s_max + r0;
   const int h0 = g * (pair ? kHeadGroup / 2 : kHeadGroup);
-  auto bar = [&](int i) { return bars + 8 * i; };
   // The last tile's latent pairs.  With T >= 2 all eight go to space that is free
   // once every score MMA has finished (ring-A slots 0-5, then the query area),
   // so none waits for ring B; with T == 1 pairs 0-3 use ring B from the start
@@ -221,39 +250,30 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
   auto borrow_off = [&](int x) {
     return x < kSlotsA ? kOffA + x * kBoxBytes : kOffQ + (x - kSlotsA) * kBoxBytes;
   };
-  // With six ring-A slots the last tile streams its RoPE box first, so the
-  // stream ends with its latent boxes 2-7 still in ring A (stream positions 3-8
-  // of the tile; 9 (T-1) is 0 or 3 modulo 6).  O^T block mb (boxes 2mb, 2mb + 1)
-  // takes its PV operand from ring A in place when the two boxes sit in adjacent
-  // slots: blocks 1 and 3 always, block 2 when T is even.  The other blocks' boxes
-  // are read again, as whole 128-row boxes, into the ring-B space.
+  // With six ring-A slots the stream ends with the last tile's positions 3-8
+  // still in ring A (positions 0-2 share slots with 6-8).  After at least one
+  // other tile the last tile streams its RoPE box first, so those positions hold
+  // latent boxes 2-7; a single tile keeps the order 0-8 (its first boxes were
+  // issued before T was known), leaving boxes 3-7.  O^T block mb (boxes 2mb,
+  // 2mb + 1) takes its PV operand from ring A in place when both boxes are there
+  // and sit in adjacent slots (9 (T-1) is 0 or 3 modulo 6): blocks 1 and 3, and
+  // block 2 when T is even, after another tile; blocks 2 and 3 of a single tile.
+  // The other blocks' boxes are read again, as whole 128-row boxes, into the
+  // ring-B space.
   constexpr bool kResidentTail = kSlotsA == 6;
+  const bool rope_first = kResidentTail && T >= 2;
   auto box_at = [&](int t, int j) {   // latent/RoPE box at position j of tile t
-    return kResidentTail && t == T - 1 ? (j + 8) % 9 : j;
+    return rope_first && t == T - 1 ? (j + 8) % 9 : j;
   };
-  auto tail_slot = [&](int k) { return (9 * (T - 1) + k + 1) % kSlotsA; };
-  auto tail_res = [&](int mb) { return mb >= 1 && tail_slot(2 * mb) != kSlotsA - 1; };
+  auto tail_pos = [&](int k) { return rope_first ? k + 1 : k; };   // of latent box k
+  auto tail_slot = [&](int k) { return (9 * (T - 1) + tail_pos(k)) % kSlotsA; };
+  auto tail_res = [&](int mb) {
+    return tail_pos(2 * mb) >= 3 && tail_slot(2 * mb) != kSlotsA - 1;
+  };
   auto tail_box_off = [&](int k) {   // the last tile's latent box k (0-7)
     return tail_res(k >> 1) ? kOffA + tail_slot(k) * kBoxBytes
-                            : kOffB + (k < 2 ? k : k - 2) * kBoxBytes;
+                            : kOffB + (k < 2 ? k : 2 + (k & 1)) * kBoxBytes;
   };
-
-  // The cache stream starts before anything else: ring A's producer sets up its
-  // own barriers and issues the first fills before the CTA-wide barrier.
-  const uint64_t keep = l2_evict_last_policy();   // read again by ring B
-  if (warp == kWarpA && lane == 0) {
-    for (int i = 0; i < kSlotsA; ++i) {
-      mbar_init(bar(BAR_FULLA + i), 1);
-      mbar_init(bar(BAR_EMPTYA + i), 1);
-    }
-    fence_mbarrier_init();
-    prefetch_tmap(&tmap);
-    for (int pos = 0; pos < kSlotsA && pos < 9 * T; ++pos) {
-      mbar_arrive_expect_tx(bar(BAR_FULLA + pos), kBoxBytes);
-      tma_load_2d(sbase + kOffA + pos * kBoxBytes, &tmap, 64 * box_at(pos / 9, pos % 9),
-                  row_base + (pos / 9) * kTileRows, bar(BAR_FULLA + pos), keep);
-    }
-  }
   if (tid == 0) {
     for (int i = 0; i < kSlotsB; ++i) {
       mbar_init(bar(BAR_FULLB + i), 1);
@@ -1007,7 +1027,18 @@ mla_status launch_split_tc(const CUtensorMap& tmap, const CUtensorMap& tmap_half
   }
   // Paired tokens: 16-head slices, two query groups per CTA.
   const dim3 grid(p.tpc == 2 ? heads / 16 : heads / kG, p.splits, p.tpc == 2 ? p.B / 2 : p.B);
-  launch_pdl(split_tc_kernel<kG>, grid, dim3(L::kThreads), L::kSmem, s, tmap, tmap_half, p);
+  // A CTA whose chunk lies past its sequence's end would fetch its first boxes
+  // for nothing; that costs little in a one-wave grid, but in several waves it
+  // delays the CTAs behind it (measured: 64 ragged sequences, split 67.9 ->
+  // 70.4 us with the early fetch everywhere).
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    sms = 0;
+  }
+  SplitParams q = p;
+  q.fill_early = static_cast<long long>(grid.x) * grid.y * grid.z <= sms;
+  launch_pdl(split_tc_kernel<kG>, grid, dim3(L::kThreads), L::kSmem, s, tmap, tmap_half, q);
   return MLA_OK;
 }
 // Rows per KV chunk (a multiple of kChunkAlign rows) and the resulting chunk

@@ -20,6 +20,8 @@ struct SplitParams {
                             // x 16 heads; 1: 32 heads of one token)
   float scale_log2;         // softmax_scale * log2(e)
   uint8_t* q_img;           // FP8: the query's E4M3 image per (sequence, head group)
+  int fill_early;           // bf16 kernel: issue tile 0's first boxes before the length
+                            // is known (a one-wave grid)
 };
 
 // FP8 cache: the query of one (sequence, 16-head group) as the split kernel's
