@@ -46,6 +46,20 @@ def test_tile_edges(cuda_lib, lengths):
     compare(gpu, ref, bs, "bf16")
 
 
+@pytest.mark.parametrize("path", ["step", "calls"])
+@pytest.mark.parametrize("S,lengths", [(384, [384, 300]), (512, [512, 400]), (640, [640, 555])])
+def test_tile_count_parity(cuda_lib, S, lengths, path):
+    """One chunk of 3, 4 or 5 tiles: the 16-head kernel reads the last tile's O^T
+    blocks in place from its stream ring or again from L2 depending on whether
+    the tile count is odd or even; the second sequence's last tile is partial."""
+    cfg = small(B=2, S=S)
+    inp = make_inputs(cfg, seed=S, poison_tail=True, lengths=torch.tensor(lengths, dtype=torch.int32))
+    gpu = run_cuda(inp, num_splits=1, path=path)
+    ref, bs = run_oracle(inp)
+    compare(gpu, ref, bs, "bf16")
+    assert gpu["status"] == 0
+
+
 @pytest.mark.parametrize("H", [32, 128])
 @pytest.mark.parametrize("path", ["step", "calls"])
 def test_head_groups(cuda_lib, H, path):
