@@ -62,7 +62,16 @@ __device__ __forceinline__ void rope_pair(const T* q_rope, const int32_t* positi
 // everything else (q_nope, q_rope, positions, every write) comes after.  Launched
 // as usual, the wait returns at once.
 constexpr int kPfPiece = 16384;   // bytes per L2 prefetch instruction
+// Bytes between two staged query rows (128 bf16 = 256 B of data): the pad of
+// 16 B puts the eight rows of an ldmatrix in eight different bank quads.
+constexpr int kQsRow = 2 * kDn + 16;
 
+// kStage (queries in host memory): each 16-row tile of q_nope is first copied
+// into shared memory with coalesced 16-byte loads (8 per lane, whole 128-byte
+// lines over the host link) and the A fragments come from ldmatrix; otherwise
+// each lane loads its fragments directly (32 four-byte loads, which from
+// device memory cost one round trip less).
+template <bool kStage>
 __global__ void __launch_bounds__(32)
     absorb_bf16_kernel(const __nv_bfloat16* __restrict__ q_nope,
                        const __nv_bfloat16* __restrict__ q_rope,
@@ -70,6 +79,7 @@ __global__ void __launch_bounds__(32)
                        const RopeTheta th, float* __restrict__ q_abs, float* __restrict__ q_pe,
                        int B, int H, const CachePrefetch pf) {
   __shared__ __align__(128) uint8_t wt[kDn * 32];  // 128 k-rows x 16 bf16 columns
+  __shared__ __align__(16) uint8_t qs[kStage ? 16 * kQsRow : 16];  // one tile's 16 query rows
   const int h = blockIdx.x, cb = blockIdx.y, lane = threadIdx.x;
   pdl_launch_dependents();   // the decode kernel may start its set-up and cache stream now
   const int c0 = cb * 16;
@@ -111,26 +121,47 @@ __global__ void __launch_bounds__(32)
     rope_pair(q_rope, pos, th, q_pe, H, h, it);
 
   const int gq = lane >> 2, cq = lane & 3;
-  const uint32_t wbase = smem_u32(wt);
+  const uint32_t wbase = smem_u32(wt), qbase = smem_u32(qs);
   for (int mt = 0; mt * 16 < B; ++mt) {
     const int bA = mt * 16 + gq, bB = bA + 8;
     uint32_t a[8][4];
-    const __nv_bfloat16* rA = q_nope + (size_t(bA) * H + h) * kDn + 2 * cq;
-    const __nv_bfloat16* rB = q_nope + (size_t(bB) * H + h) * kDn + 2 * cq;
+    if constexpr (kStage) {
+      // The tile's 16 query rows q_nope[b, h, :] (256 B each) into shared
+      // memory: load r of lane l is 16-byte chunk (l + 32 r) % 16 of row
+      // (l + 32 r) / 16 (rows past B read as zeros).
+      if (mt > 0) __syncwarp();   // the previous tile's rows have been read
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      a[ks][0] = bA < B ? *reinterpret_cast<const uint32_t*>(rA + 16 * ks) : 0u;
-      a[ks][1] = bB < B ? *reinterpret_cast<const uint32_t*>(rB + 16 * ks) : 0u;
-      a[ks][2] = bA < B ? *reinterpret_cast<const uint32_t*>(rA + 16 * ks + 8) : 0u;
-      a[ks][3] = bB < B ? *reinterpret_cast<const uint32_t*>(rB + 16 * ks + 8) : 0u;
+      for (int r = 0; r < 8; ++r) {
+        const int i = lane + 32 * r, row = i >> 4, ch = i & 15;
+        const int bq = mt * 16 + row;
+        const uint4 v = bq < B ? reinterpret_cast<const uint4*>(
+                                     q_nope + (size_t(bq) * H + h) * kDn)[ch]
+                               : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(qs + row * kQsRow + ch * 16) = v;
+      }
+    } else {
+      const __nv_bfloat16* rA = q_nope + (size_t(bA) * H + h) * kDn + 2 * cq;
+      const __nv_bfloat16* rB = q_nope + (size_t(bB) * H + h) * kDn + 2 * cq;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        a[ks][0] = bA < B ? *reinterpret_cast<const uint32_t*>(rA + 16 * ks) : 0u;
+        a[ks][1] = bB < B ? *reinterpret_cast<const uint32_t*>(rB + 16 * ks) : 0u;
+        a[ks][2] = bA < B ? *reinterpret_cast<const uint32_t*>(rA + 16 * ks + 8) : 0u;
+        a[ks][3] = bB < B ? *reinterpret_cast<const uint32_t*>(rB + 16 * ks + 8) : 0u;
+      }
     }
-    if (mt == 0) {
-      asm volatile("cp.async.wait_all;" ::: "memory");
-      __syncwarp();
-    }
+    if (mt == 0) asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
+      // A fragment of k in [16ks, 16ks+16): lanes 0-7 / 8-15 / 16-23 / 24-31
+      // address rows 0-7 / 8-15 / 0-7 / 8-15 at columns 16ks / 16ks / 16ks+8 /
+      // 16ks+8, the order of the mma's four A registers.
+      if constexpr (kStage)
+        ldsm_x4(qbase + ((lane & 7) + 8 * ((lane >> 3) & 1)) * kQsRow +
+                    (16 * ks + 8 * (lane >> 4)) * 2,
+                a[ks][0], a[ks][1], a[ks][2], a[ks][3]);
       // B fragments of n-blocks 0 and 1 for k in [16ks, 16ks+16): ldmatrix.trans
       // of the [k][n] slice (32-byte rows, 16-byte chunks swizzled by bit 2 of k).
       const int mi = lane >> 3;
@@ -427,9 +458,25 @@ __global__ void __launch_bounds__(256) rope_q_kernel(const T* __restrict__ q_rop
 
 using namespace mla;
 
-// Dynamic shared memory (unused) of the early-launched absorb: with its 4 KB of
-// static shared memory, at most four CTAs fit on an SM.
-constexpr size_t kAbsorbSpreadSmem = 44u << 10;
+// Dynamic shared memory (unused) of the early-launched absorb: with its static
+// shared memory (4 KB, or 8.25 KB when it stages the queries) and the 1 KB the
+// SM reserves per CTA, a CTA takes 48-49 KB, so at most four fit on an SM; the
+// total stays within the 48 KB a launch may use without opting in.
+constexpr size_t kAbsorbSpreadSmem = (44u << 10) - 16;
+constexpr size_t kAbsorbSpreadSmemStaged = 39u << 10;
+static_assert(kAbsorbSpreadSmem + kDn * 32 + 16 <= (48u << 10) &&
+                  kAbsorbSpreadSmemStaged + kDn * 32 + 16 * kQsRow <= (48u << 10),
+              "the early absorb's shared memory needs no opt-in");
+
+// Whether `p` is page-locked host memory (read by the kernels over the host link).
+static bool host_resident(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeHost;
+}
 
 extern "C" mla_status mla_absorb_q(const mla_dims* dims, const void* q_nope, const void* q_rope,
                                    const void* w_uk, const int32_t* positions, double rope_base,
@@ -463,6 +510,14 @@ mla_status mla::absorb_q(const char* who, const mla_dims* dims, const void* q_no
   RopeTheta th;
   for (int i = 0; i < kDr / 2; ++i) th.turns[i] = pow(rope_base, -2.0 * i / kDr) / (2.0 * M_PI);
   if (dims->dtype != MLA_F32) {
+    // Queries in host memory: stage each tile with whole-line reads (measured on
+    // 8 sequences x 16 heads, one step per graph launch: 1.26 -> 1.29-1.31 TB/s
+    // end to end; from device memory the direct loads are faster).
+    const bool stage = host_resident(q_nope);
+    auto kern = stage ? absorb_bf16_kernel<true> : absorb_bf16_kernel<false>;
+    const auto* qn = static_cast<const __nv_bfloat16*>(q_nope);
+    const auto* qr = static_cast<const __nv_bfloat16*>(q_rope);
+    const auto* wk = static_cast<const __nv_bfloat16*>(w_uk);
     if (early)
       // Launched while the previous step's fused tail fills most SMs' register
       // files, the grid's small CTAs would all land on the few SMs left free
@@ -470,15 +525,12 @@ mla_status mla::absorb_q(const char* who, const mla_dims* dims, const void* q_no
       // 3.3 us from the wait to the last exit).  Unused shared memory caps
       // them at four per SM, so the rest start on the SMs the tail leaves:
       // 128 SMs, 1.7 us, and the step 19.5 -> 18.5 us.
-      launch_pdl(absorb_bf16_kernel, dim3(H, kDc / 16), dim3(32), kAbsorbSpreadSmem, s,
-                 static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(q_rope),
-                 static_cast<const __nv_bfloat16*>(w_uk), positions, th, static_cast<float*>(q_abs),
-                 static_cast<float*>(q_pe), B, H, pf);
+      launch_pdl(kern, dim3(H, kDc / 16), dim3(32),
+                 stage ? kAbsorbSpreadSmemStaged : kAbsorbSpreadSmem, s, qn, qr, wk, positions,
+                 th, static_cast<float*>(q_abs), static_cast<float*>(q_pe), B, H, pf);
     else
-      absorb_bf16_kernel<<<dim3(H, kDc / 16), 32, 0, s>>>(
-          static_cast<const __nv_bfloat16*>(q_nope), static_cast<const __nv_bfloat16*>(q_rope),
-          static_cast<const __nv_bfloat16*>(w_uk), positions, th, static_cast<float*>(q_abs),
-          static_cast<float*>(q_pe), B, H, pf);
+      kern<<<dim3(H, kDc / 16), 32, 0, s>>>(qn, qr, wk, positions, th, static_cast<float*>(q_abs),
+                                           static_cast<float*>(q_pe), B, H, pf);
   } else {
     absorb_f32_kernel<<<dim3(H, B), 128, 0, s>>>(
         static_cast<const float*>(q_nope), static_cast<const float*>(q_rope),
