@@ -66,6 +66,15 @@ constexpr int kPfPiece = 16384;   // bytes per L2 prefetch instruction
 // 16 B puts the eight rows of an ldmatrix in eight different bank quads.
 constexpr int kQsRow = 2 * kDn + 16;
 
+// Four 8x8 bf16 matrices from shared memory (lanes 8i..8i+7 address the rows
+// of matrix i), one register each, untransposed.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
 // kStage (queries in host memory): each 16-row tile of q_nope is first copied
 // into shared memory with coalesced 16-byte loads (8 per lane, whole 128-byte
 // lines over the host link) and the A fragments come from ldmatrix; otherwise
