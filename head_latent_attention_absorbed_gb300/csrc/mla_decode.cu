@@ -270,9 +270,14 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
   auto tail_res = [&](int mb) {
     return tail_pos(2 * mb) >= 3 && tail_slot(2 * mb) != kSlotsA - 1;
   };
+  // Block 0 is never in ring A at the end: its two boxes are read again into
+  // the query area, free once every score MMA has finished; a second block read
+  // again (a single tile, or T odd) goes to the ring-B space.
+  static_assert(!kResidentTail || 2 * kBoxBytes <= 9 * kQBoxBytes,
+                "block 0's boxes fit in the query area");
   auto tail_box_off = [&](int k) {   // the last tile's latent box k (0-7)
     return tail_res(k >> 1) ? kOffA + tail_slot(k) * kBoxBytes
-                            : kOffB + (k < 2 ? k : 2 + (k & 1)) * kBoxBytes;
+                            : (k < 2 ? kOffQ : kOffB) + (k & 1) * kBoxBytes;
   };
   if (tid == 0) {
     for (int i = 0; i < kSlotsB; ++i) {
@@ -329,13 +334,17 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
       const uint64_t stream = l2_evict_first_policy();
       for (int t = 0; t < T && !*abort_flag; ++t) {
         if (kResidentTail && t == T - 1) {
-          // The last tile's boxes that left ring A, into the ring-B space, once
-          // ring B is free (the PV of tile T-2 has finished) and every score MMA
-          // has finished.
-          if (T >= 2 && !wait_or_abort(bar(BAR_PVPREV), 0, abort_flag)) break;
+          // The last tile's boxes that left ring A: block 0's into the query
+          // area once every score MMA has finished, a second block's into the
+          // ring-B space once the PV of tile T-2 has finished too.
           if (!wait_or_abort(bar(BAR_LASTA), 0, abort_flag)) break;
+          bool second = false;
           for (int k = 0; k < 8; ++k) {
             if (tail_res(k >> 1)) continue;
+            if (k >= 2 && !second) {
+              if (T >= 2 && !wait_or_abort(bar(BAR_PVPREV), 0, abort_flag)) break;
+              second = true;
+            }
             mbar_arrive_expect_tx(bar(BAR_FULLX + k), kBoxBytes);
             tma_load_2d(sbase + tail_box_off(k), &tmap, 64 * k, row_base + t * kTileRows,
                         bar(BAR_FULLX + k), stream);
