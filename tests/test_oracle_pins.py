@@ -103,11 +103,14 @@ def _brute(q_nope, q_rope, w_uk, w_uv, cache, n, pos, scale, base):
     return np.array(out_o), np.array(out_oc), np.array(out_lse)
 
 
+@pytest.mark.parametrize("d_rope", [2, 4])
 @pytest.mark.parametrize("H", [1, 2])
 @pytest.mark.parametrize("S", [1, 2, 3])
-def test_brute_force_tiny(H, S):
-    rng = np.random.default_rng(100 + 10 * H + S)
-    case = _rand_case(rng, B=1, H=H, d_c=4, d_rope=2, d_nope=2, d_v=3, S=S, lengths=[S])
+def test_brute_force_tiny(H, S, d_rope):
+    """With d_rope = 4 two frequencies meet two pairs, so the brute force also
+    sees which frequency rotates which pair."""
+    rng = np.random.default_rng(100 + 10 * H + S + 1000 * d_rope)
+    case = _rand_case(rng, B=1, H=H, d_c=4, d_rope=d_rope, d_nope=2, d_v=3, S=S, lengths=[S])
     case["positions"] = np.array([5])
     scale = 0.5
     a = O.decode_absorbed(**case, scale=scale, base=10000.0)
@@ -178,6 +181,45 @@ def test_rope_width_two_is_plane_rotation():
         x = np.array([0.3, -1.7])
         R = np.array([[math.cos(pos), -math.sin(pos)], [math.sin(pos), math.cos(pos)]])
         np.testing.assert_allclose(O.apply_rope(x, pos, 10000.0), R @ x, atol=1e-15)
+
+
+def _rope_scalar(x, pos, base):
+    """RoPE by scalar loops: pair i = (x[2i], x[2i+1]) is the complex number
+    x[2i] + i x[2i+1] turned by the angle pos * base^(-2i/d) (Multi-Head Latent
+    Attention, 3.7: frequencies from the even indices 0, 2, ..., d-2 over d, and
+    the vector read as consecutive complex pairs in order)."""
+    d = len(x)
+    out = [0.0] * d
+    for i in range(d // 2):
+        ang = pos * base ** (-(2.0 * i) / d)
+        out[2 * i] = math.cos(ang) * x[2 * i] - math.sin(ang) * x[2 * i + 1]
+        out[2 * i + 1] = math.sin(ang) * x[2 * i] + math.cos(ang) * x[2 * i + 1]
+    return np.array(out)
+
+
+@pytest.mark.parametrize("d_rope,pos,base", [(6, 7, 10000.0), (8, 3, 10000.0),
+                                             (64, 4095, 10000.0), (10, 11, 50.0)])
+def test_rope_brute_force_pair_frequencies(d_rope, pos, base):
+    """Several pairs at a position other than 0: every pair turns by its own
+    frequency, so a frequency given to the wrong pair shows."""
+    x = np.random.default_rng(17 + d_rope).standard_normal((3, d_rope))
+    got = O.apply_rope(x, pos, base)
+    for r in range(3):
+        np.testing.assert_allclose(got[r], _rope_scalar(x[r].tolist(), pos, base),
+                                   rtol=0, atol=1e-12)
+
+
+def test_rope_each_pair_turns_by_its_own_angle():
+    """A vector with a single nonzero pair i = (1, 0) comes back as
+    (cos a, sin a) with a = pos * base^(-2i/d): the angle of pair i alone."""
+    d, pos, base = 8, 3, 100.0
+    for i in range(d // 2):
+        x = np.zeros(d)
+        x[2 * i] = 1.0
+        y = O.apply_rope(x, pos, base)
+        a = pos * base ** (-2.0 * i / d)       # 3, 0.95, 0.3, 0.095 radians
+        assert abs(math.atan2(y[2 * i + 1], y[2 * i]) - a) <= 1e-14
+        assert np.count_nonzero(np.delete(y, [2 * i, 2 * i + 1])) == 0
 
 
 def test_rope_frequencies_closed_form():
@@ -291,6 +333,23 @@ def test_pins_catch_a_wrong_rope_sign(monkeypatch):
     x = np.array([0.3, -1.7])
     R = np.array([[math.cos(3), -math.sin(3)], [math.sin(3), math.cos(3)]])
     assert np.max(np.abs(O.apply_rope(x, 3, 10000.0) - R @ x)) > 1e-3
+
+
+def test_pins_catch_reversed_rope_frequencies(monkeypatch):
+    """Plant the frequencies in reverse pair order (pair 0 turning slowest): the
+    scalar RoPE pin and the d_rope = 4 brute force must both fail."""
+    orig = O.rope_theta
+    monkeypatch.setattr(O, "rope_theta", lambda d, b: orig(d, b)[::-1].copy())
+    x = np.random.default_rng(23).standard_normal(6)
+    assert np.max(np.abs(O.apply_rope(x, 7, 10000.0) - _rope_scalar(x.tolist(), 7, 10000.0))) > 1e-3
+    rng = np.random.default_rng(100 + 10 * 2 + 3 + 4000)
+    case = _rand_case(rng, B=1, H=2, d_c=4, d_rope=4, d_nope=2, d_v=3, S=3, lengths=[3])
+    case["positions"] = np.array([5])
+    bo, _, _ = _brute(case["q_nope"][0].tolist(), case["q_rope"][0].tolist(),
+                      case["w_uk"].tolist(), case["w_uv"].tolist(),
+                      case["cache"][0].tolist(), 3, 5, 0.5, 10000.0)
+    bad = O.decode_absorbed(**case, scale=0.5, base=10000.0)["o"][0]
+    assert np.max(np.abs(bad - bo)) > 1e-6
 
 
 def test_pins_catch_a_dropped_rope_term(monkeypatch):
