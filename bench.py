@@ -12,8 +12,14 @@ k mod L, so no step finds its cache in L2.
 Prints one JSON line.  `value` is latent-cache GB/s of the whole step
 (algorithmic cache bytes B*S*576*2 per step over the device time of the
 timed steps); `tokens_per_s` is B*steps/time.  `roofline` covers the split
-kernel (the dominant kernel), timed with CUDA events around each of its
-launches inside the timed region.
+kernel (the dominant kernel) and, under `decode_attn`, mla_decode_attn
+(split + LSE combine), each timed as a CUDA graph of back-to-back plain
+launches (each starting after the previous one ended) with the overlapped
+figure beside it; `roofline_workloads` gives the same two for the ragged,
+128-head and long-context workloads; `steady` replays a long graph of steps
+with the SM clock sampled throughout.  The CPU leg (`cpu_baseline`) times the
+fp64 oracle on all cores and on one thread, and compares the last timed
+step's outputs with the oracle (`check`); the run fails if they disagree.
 
 `--impl reference` times the fp64 CPU oracle instead (the reference arm).
 """
@@ -54,6 +60,11 @@ def parse(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the split / decode_attn rooflines of the other workloads")
+    ap.add_argument("--steady-steps", type=int, default=2000,
+                    help="steps per replay of the long steady-state graph (0: skip)")
+    ap.add_argument("--cpu-single-thread", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--op", default="step",
                     choices=["step", "cache_append", "wo_proj", "kq_proj", "ov_proj", "absorb_q",
                              "combine", "out_proj"],
@@ -155,12 +166,19 @@ class ClockSampler:
             self._stop.set()
             self._t.join()
 
-    def summary(self):
+    def summary(self, bins: bool = False):
         if not self.ok or not self.samples:
             return None
         names = [n for bit, n in self.REASONS.items() if self.reasons & bit]
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": names, "samples": len(self.samples), "source": "nvml"}
+        out = {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+               "reasons": names, "samples": len(self.samples), "source": "nvml"}
+        if bins:   # samples per 15 MHz clock step
+            hist = {}
+            for v in self.samples:
+                k = str(int(v // 15 * 15))
+                hist[k] = hist.get(k, 0) + 1
+            out["sm_mhz_bins"] = dict(sorted(hist.items(), key=lambda kv: -int(kv[0])))
+        return out
 
 
 def bus_id_of(device_index: int):
@@ -217,6 +235,96 @@ def cpu_cores():
         return len(os.sched_getaffinity(0))
     except AttributeError:
         return os.cpu_count()
+
+
+def blas_threads():
+    """(library, threads) of NumPy's BLAS, read from the loaded OpenBLAS itself
+    (no extra package needed); (None, None) if it cannot be read."""
+    import numpy as np
+    np.ones(2) @ np.ones(2)               # make sure the BLAS library is loaded
+    try:
+        paths = sorted({ln.split()[-1] for ln in open("/proc/self/maps")
+                        if "openblas" in ln.lower() and ln.strip().endswith(".so") or
+                        ("openblas" in ln.lower() and ".so" in ln.split()[-1])})
+    except OSError:
+        return None, None
+    for path in paths:
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for name in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                     "openblas_get_num_threads"):
+            fn = getattr(lib, name, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                return os.path.basename(path), int(fn())
+    return None, None
+
+
+def single_thread_oracle(cfg, seconds: float):
+    """The same oracle leg in a child process whose BLAS and OpenMP pools have
+    one thread.  Returns its JSON dict or None."""
+    import subprocess
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-single-thread", "--workload",
+           cfg.name, "--cpu-seconds", str(seconds)]
+    try:
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=seconds + 120)
+        return json.loads(r.stdout.strip().splitlines()[-1]) if r.returncode == 0 else None
+    except Exception:
+        return None
+
+
+def oracle_check(cfg, gpu_out, seed: int):
+    """The last timed step's outputs (o, o_c, lse; every step of the timed graph
+    reads identical copies of the same inputs) against the fp64 oracle on up to
+    eight sequences of the workload, with the parity tolerances."""
+    import numpy as np
+    from oracle import mla_oracle as O
+    from workloads import (TOL_BF16_MAX_ABS, TOL_BF16_REL_L2, TOL_F32_MAX_ABS, make_inputs)
+    inp = make_inputs(cfg, seed=seed)
+    nb = min(cfg.batch, 8)
+    seqs = sorted({round(i * (cfg.batch - 1) / max(nb - 1, 1)) for i in range(nb)})
+    res, ok = {"sequences": seqs, "step": "last timed step"}, True
+    refs = {k: [] for k in ("o", "o_c", "lse")}
+    rows = []
+    for b in seqs:
+        for i in range(cfg.q_len):
+            rows.append(b * cfg.q_len + i)
+        a = inp.as_float64_numpy(b)
+        if a["cache"] is None:
+            a["cache"] = O.e4m3_to_float64(a["cache_e4m3"])
+        if cfg.q_len == 1:
+            n = int(a["lengths"][0])
+            r = O.decode_absorbed(a["q_nope"], a["q_rope"], a["w_uk"], a["w_uv"],
+                                  a["cache"][:, :n], a["lengths"], a["positions"],
+                                  cfg.softmax_scale, cfg.rope_base)
+            for k in refs:
+                refs[k].append(r[k][0])
+        else:   # rows b * q_len .. + q_len - 1 are sequence b's tokens
+            T = cfg.q_len
+            n = int(a["lengths"][0])
+            qn = inp.q_nope[b * T:(b + 1) * T].double().numpy()[None]
+            qr = inp.q_rope[b * T:(b + 1) * T].double().numpy()[None]
+            r = O.decode_multi_token(qn, qr, a["w_uk"], a["w_uv"], a["cache"][:, :n],
+                                     np.array([n]), T, cfg.softmax_scale, cfg.rope_base)
+            for k in refs:
+                refs[k].extend(list(r[k][0]))
+    for k in ("o", "o_c", "lse"):
+        ref = np.stack(refs[k])
+        got = gpu_out[k][rows]
+        ma = float(np.max(np.abs(got - ref)))
+        rl = float(np.linalg.norm((got - ref).ravel()) / max(np.linalg.norm(ref.ravel()), 1e-300))
+        fin = bool(np.all(np.isfinite(got)))
+        good = fin and (ma <= TOL_F32_MAX_ABS if cfg.dtype == "f32"
+                        else ma <= TOL_BF16_MAX_ABS and rl <= TOL_BF16_REL_L2)
+        res[k] = {"max_abs": ma, "rel_l2": rl}
+        ok = ok and good
+    res["tolerance"] = ({"max_abs": TOL_F32_MAX_ABS} if cfg.dtype == "f32" else
+                        {"max_abs": TOL_BF16_MAX_ABS, "rel_l2": TOL_BF16_REL_L2})
+    res["ok"] = ok
+    return res
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -434,6 +542,104 @@ def launches_per_step(cfg) -> int:
     return 1 + (1 if cfg.dtype == "fp8" else 0) + 1 + (1 if fused else 2)
 
 
+# ----------------------------------------------------------------------------- timing helpers
+def graph_time(mla, stream, launch, n: int, reps: int, overlap: bool = True, bus=None):
+    """Capture n calls launch(0..n-1) as one CUDA graph on `stream`, with the
+    library's programmatic launches on or off; replay it once untimed, then
+    `reps` times with CUDA events around each replay on the replaying stream.
+    Returns (microseconds per launch of each replay, clock summary or None);
+    the SM clock is sampled only when `bus` is given."""
+    import torch
+    mla.set_launch_overlap(overlap)
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="thread_local"):
+            for k in range(n):
+                launch(k)
+    finally:
+        mla.set_launch_overlap(True)
+    g.replay()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(bus) if bus is not None else None
+    out = []
+    with (sampler if sampler is not None else _Nothing()):
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            out.append(e0.elapsed_time(e1) * 1e3 / n)
+    del g
+    return out, (sampler.summary(bins=True) if sampler is not None else None)
+
+
+class _Nothing:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+# The other workloads whose split and mla_decode_attn rooflines the default run
+# reports beside the bench workload's: the ragged batch, the 128-head batch and
+# the long context at its 128 chunks per sequence.
+OTHER_WORKLOADS = ("v2lite_bf16_b64_ragged512_8192", "v3heads_bf16_h128_b32_s16384",
+                   "v2lite_bf16_b4_s65536_split128")
+
+
+def workload_rooflines(mla, dev, stream, peak, bus):
+    """Split-only and mla_decode_attn rooflines of OTHER_WORKLOADS: plain launches
+    (programmatic launch off) over two or more cache copies larger than L2 in all,
+    median of three replays; bytes are the valid rows' (ragged tails excluded)."""
+    import torch
+    from workloads import BY_NAME, cache_storage, make_inputs
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or 126 * 2 ** 20
+    res = []
+    for name in OTHER_WORKLOADS:
+        c = BY_NAME[name]
+        inp = make_inputs(c, seed=0)
+        per = inp.cache.numel() * inp.cache.element_size()
+        L = max(2, math.ceil(3 * l2 / per))
+        caches = [inp.cache.to(dev) for _ in range(L)]
+        lengths, pos = inp.lengths.to(dev), inp.positions.to(dev)
+        d = mla.dims(c.batch, c.heads, c.s_max, mla.dtype_code(cache_storage(c)))
+        B, H = c.batch, c.heads
+        q_abs = torch.empty((B, H, c.d_c), dtype=torch.float32, device=dev)
+        q_pe = torch.empty((B, H, c.d_rope), dtype=torch.float32, device=dev)
+        o_c = torch.empty((B, H, c.d_c), dtype=torch.float32, device=dev)
+        lse = torch.empty((B, H), dtype=torch.float32, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        mla.absorb_q(d, inp.q_nope.to(dev), inp.q_rope.to(dev), inp.w_uk.to(dev), pos, q_abs,
+                     q_pe, c.rope_base)
+        ws = torch.empty((mla.workspace_bytes(d, c.num_splits),), dtype=torch.uint8, device=dev)
+        nbytes = int(inp.lengths.to(torch.int64).sum()) * c.row * c.elt_bytes
+        n = max(8, min(200, int(20e-3 / (nbytes / 5e12))))    # about 20 ms per replay
+        split = lambda k: mla.decode_split(d, q_abs, q_pe, caches[k % L], lengths, ws,
+                                           c.softmax_scale, c.num_splits, status)
+        attn = lambda k: mla.decode_attn(d, q_abs, q_pe, caches[k % L], lengths, o_c, ws,
+                                         c.softmax_scale, c.num_splits, lse, status)
+        sp, clk = graph_time(mla, stream, split, n, 3, overlap=False, bus=bus)
+        at, _ = graph_time(mla, stream, attn, n, 3, overlap=False)
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item())} on {name}")
+        entry = {"workload": name, "batch": B, "heads": H, "s_max": c.s_max,
+                 "kv_splits": mla.num_splits(d, c.num_splits), "bytes_per_launch": nbytes,
+                 "launches_timed": n, "replays": 3, "clocks": clk}
+        for key, us_list in (("split", sp), ("decode_attn", at)):
+            us = statistics.median(us_list)
+            gbs = nbytes / (us * 1e-6) / 1e9
+            entry[key] = {"avg_launch_us": us, "achieved": gbs, "frac": gbs / peak,
+                          "spread_us": [min(us_list), max(us_list)]}
+        res.append(entry)
+        del caches, ws, inp
+        torch.cuda.empty_cache()
+    return res
+
+
 # ----------------------------------------------------------------------------- our arm
 def main():
     return main_with(parse(), int(os.environ.get("RANK", "0")),
@@ -444,6 +650,12 @@ def main_with(args, rank: int, world: int, local: int = 0):
     from workloads import BY_NAME
     cfg = BY_NAME[args.workload]
 
+    if args.cpu_single_thread:   # child of the CPU leg, BLAS limited to one thread
+        gbs, tps, nsteps, rows, el = oracle_throughput(cfg, args.cpu_seconds)
+        print(json.dumps({"value": gbs, "unit": "GB/s", "cores": 1, "steps": nsteps,
+                          "rows": rows, "seconds": el, "tokens_per_s": tps,
+                          "env": "OPENBLAS_NUM_THREADS=OMP_NUM_THREADS=MKL_NUM_THREADS=1"}))
+        return 0
     if args.impl == "reference":
         return run_reference(args, cfg, rank, world)
     if args.op != "step":
@@ -475,8 +687,10 @@ def main_with(args, rank: int, world: int, local: int = 0):
     qr = [inp.q_rope.to(dev) for _ in range(L)]
     lengths = inp.lengths.to(dev)
     positions = inp.positions.to(dev)
+    splits_req = args.splits or cfg.num_splits   # the workload's own chunk count, if any
+    bus = bus_id_of(dev.index)
     step = mla.DecodeStep(cfg.batch, cfg.heads, cfg.s_max, dt, device=dev,
-                          num_splits_requested=args.splits, rope_base=cfg.rope_base,
+                          num_splits_requested=splits_req, rope_base=cfg.rope_base,
                           softmax_scale=cfg.softmax_scale, q_len=cfg.q_len)
     d = step.dims
     cache_bytes = int(inp.lengths.to(torch.int64).sum()) * cfg.row * inp.cache.element_size()
@@ -505,7 +719,7 @@ def main_with(args, rank: int, world: int, local: int = 0):
 
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(bus_id_of(dev.index))
+    sampler = ClockSampler(bus)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -525,32 +739,59 @@ def main_with(args, rank: int, world: int, local: int = 0):
     value = whole_job_rate(cache_bytes, K, world, sec) / 1e9
     tokens = whole_job_rate(cfg.batch * cfg.q_len, K, world, sec)
 
-    # The dominant kernel alone: Ks back-to-back split launches over the same
-    # rotating layer copies, one CUDA graph, CUDA events on the replay stream.
-    # (Event nodes between the launches of the step graph would themselves add
-    # microseconds per launch.)
-    Ks = min(K, 400)
-    gs = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gs, stream=cap, capture_error_mode="thread_local"):
-        for k in range(Ks):
-            if cfg.q_len == 1:
-                mla.decode_split(d, step.q_abs, step.q_pe, caches[k % L], lengths,
-                                 step.workspace, step.scale, args.splits, step.status)
-            else:   # the split has no separate multi-token entry: split + combine
-                mla.decode_attn_multi(d, cfg.q_len, step.q_abs, step.q_pe, caches[k % L],
-                                      lengths, step.o_c, step.workspace, step.scale, args.splits,
-                                      step.lse, step.status)
-    gs.replay()
-    torch.cuda.synchronize()
-    s_begin = torch.cuda.Event(enable_timing=True)
-    s_end = torch.cuda.Event(enable_timing=True)
-    s_begin.record()
-    gs.replay()
-    s_end.record()
-    torch.cuda.synchronize()
-    split_avg_s = s_begin.elapsed_time(s_end) / 1e3 / Ks
+    # Outputs of the last timed step, kept for the oracle check of the CPU leg
+    # before the graphs below overwrite them.
+    last_out = {"o": step.out.double().cpu().numpy(), "o_c": step.o_c.double().cpu().numpy(),
+                "lse": step.lse.double().cpu().numpy()}
+
+    # The dominant kernel and mla_decode_attn (split + combine) alone: graphs of Ks
+    # back-to-back launches over the rotating layer copies, timed with CUDA events
+    # around each of `reps` replays (median reported).  "plain": programmatic launch
+    # off, so each launch starts after the previous one ended and the average is one
+    # launch's whole duration; "overlapped": the library's default launches, where
+    # a launch's set-up and first cache boxes overlap the previous launch's tail.
+    Ks, reps = 400, 5
+
+    def split_launch(k):
+        mla.decode_split(d, step.q_abs, step.q_pe, caches[k % L], lengths, step.workspace,
+                         step.scale, splits_req, step.status)
+
+    def attn_launch(k):
+        if cfg.q_len == 1:
+            mla.decode_attn(d, step.q_abs, step.q_pe, caches[k % L], lengths, step.o_c,
+                            step.workspace, step.scale, splits_req, step.lse, step.status)
+        else:
+            mla.decode_attn_multi(d, cfg.q_len, step.q_abs, step.q_pe, caches[k % L], lengths,
+                                  step.o_c, step.workspace, step.scale, splits_req, step.lse,
+                                  step.status)
+
+    if cfg.q_len > 1:    # no separate multi-token split entry: split + combine
+        split_launch = attn_launch
+    split_plain, clk_split = graph_time(mla, cap, split_launch, Ks, reps, overlap=False,
+                                        bus=bus)
+    split_ovl, _ = graph_time(mla, cap, split_launch, Ks, reps, overlap=True)
+    attn_plain, clk_attn = graph_time(mla, cap, attn_launch, Ks, reps, overlap=False, bus=bus)
+    attn_ovl, _ = graph_time(mla, cap, attn_launch, Ks, reps, overlap=True)
     if int(step.status.item()) != 0:
         raise RuntimeError(f"device status {int(step.status.item())} after the split-only replay")
+
+    # The same step graph, long: `--steady-steps` steps per replay, five replays,
+    # with the SM clock sampled throughout (a timed region long enough for many
+    # samples), so that the step time can be read against the clock.
+    steady = None
+    if args.steady_steps > 0:
+        st_us, st_clk = graph_time(mla, cap, one_step, args.steady_steps, 5, overlap=True,
+                                   bus=bus)
+        if int(step.status.item()) != 0:
+            raise RuntimeError(f"device status {int(step.status.item())} after the steady replays")
+        med = statistics.median(st_us)
+        steady = {"steps_per_replay": args.steady_steps, "replays": len(st_us),
+                  "us_per_step": med, "us_per_step_min": min(st_us),
+                  "us_per_step_max": max(st_us),
+                  "value": cache_bytes / (med * 1e-6) / 1e9, "unit": "GB/s",
+                  "tokens_per_s": cfg.batch * cfg.q_len / (med * 1e-6),
+                  "clocks": st_clk,
+                  "us_x_sm_mhz": med * st_clk["sm_mhz"] if st_clk else None}
 
     # End-to-end through the public API with host buffers: every step copies the
     # queries, lengths and positions from pinned host memory and reads o back
@@ -591,28 +832,57 @@ def main_with(args, rank: int, world: int, local: int = 0):
                         "host link, no copy nodes")}
 
     peak, peak_kind = measured_peaks()
-    achieved = cache_bytes / split_avg_s / 1e9
     kname = SPLIT_KERNEL[cfg.dtype]
+
+    def rate(us_list):
+        us = statistics.median(us_list)
+        gbs = cache_bytes / (us * 1e-6) / 1e9
+        return {"achieved": gbs, "frac": gbs / peak, "avg_launch_us": us,
+                "spread_us": [min(us_list), max(us_list)]}
+
+    sp, so, ap, ao = rate(split_plain), rate(split_ovl), rate(attn_plain), rate(attn_ovl)
+    attn_name = "mla_decode_attn" if cfg.q_len == 1 else "mla_decode_attn_multi"
     roofline = {"bound": "hbm",
                 "kernel": (f"{kname} (mla_decode_split)" if cfg.q_len == 1 else
-                           f"{kname} + combine_kernel (mla_decode_attn_multi)"),
-                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                           f"{kname} + combine_kernel ({attn_name})"),
+                "achieved": sp["achieved"], "peak": peak, "unit": "GB/s", "frac": sp["frac"],
                 "peak_kind": f"{peak_kind} (copy bandwidth, burst)",
-                "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
+                "frac_of_nominal_8TBs": sp["achieved"] / NOMINAL_HBM_GBS,
                 "traffic": recorded_traffic(kname, cfg.name),
                 "bytes_per_launch": cache_bytes,
-                "avg_launch_us": split_avg_s * 1e6,
-                "launches_timed": Ks,
-                "timing": "graph of back-to-back split launches, CUDA events around its replay"}
+                "avg_launch_us": sp["avg_launch_us"], "spread_us": sp["spread_us"],
+                "launches_timed": Ks, "replays": reps,
+                "timing": (f"plain launches (programmatic launch off): a CUDA graph of {Ks} "
+                           f"back-to-back launches over the rotating layer copies, each starting "
+                           f"after the previous one ended; CUDA events around each replay, "
+                           f"median of {reps} replays"),
+                "clocks": clk_split,
+                "us_x_sm_mhz": sp["avg_launch_us"] * clk_split["sm_mhz"] if clk_split else None,
+                "overlapped": dict(so, timing="the library's default programmatic launches: "
+                                   "each launch's set-up and first cache boxes overlap the "
+                                   "previous launch's tail (a pipelined throughput)"),
+                "decode_attn": dict(ap, call=attn_name, kernels="split + LSE combine",
+                                    bytes_per_launch=cache_bytes, target_frac=0.70,
+                                    timing="plain launches, as above", clocks=clk_attn,
+                                    overlapped=ao)}
 
-    cpu = None
+    others = None
+    if not args.no_workloads and world == 1 and cfg.name == "v2lite_bf16_b8_s4096":
+        others = workload_rooflines(mla, dev, cap, peak, bus)
+
+    cpu, check = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        blas_lib, blas_n = blas_threads()
         gbs, tps, nsteps, rows, el = oracle_throughput(cfg, args.cpu_seconds)
+        single = single_thread_oracle(cfg, min(args.cpu_seconds, 5.0))
         cpu = {"value": gbs, "unit": "GB/s", "cores": cpu_cores(), "kind": "oracle",
-               "tokens_per_s": tps,
+               "tokens_per_s": tps, "blas": blas_lib, "blas_threads": blas_n,
                "sample": (f"{nsteps} single-sequence decode steps ({rows} rows, H={cfg.heads}) "
                           f"of this workload through the fp64 NumPy oracle, {el:.1f} s; inputs "
-                          f"converted to fp64 before timing")}
+                          f"converted to fp64 before timing"),
+               "single_thread": single}
+        # The oracle leg also checks the GPU's last timed step against the oracle.
+        check = oracle_check(cfg, last_out, seed=rank)
 
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -621,7 +891,8 @@ def main_with(args, rank: int, world: int, local: int = 0):
         "data": "synthetic (seeded N(0,1) cache and queries, N(0,0.02^2) weights)",
         "tokens_per_s": tokens,
         "config": workload_config(cfg, L, step.splits),
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "roofline": roofline, "roofline_workloads": others, "steady": steady,
+        "cpu_baseline": cpu, "check": check, "e2e": e2e,
         "gpu_launches": launches_per_step(cfg) * K,
         "clocks": sampler.summary(),
         "timing": "one CUDA-graph replay of the timed steps (no event nodes inside), CUDA events "
@@ -631,6 +902,9 @@ def main_with(args, rank: int, world: int, local: int = 0):
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
+    if check is not None and not check["ok"]:
+        print("bench: the last timed step does not match the oracle", file=sys.stderr)
+        return 1
     return 0
 
 

@@ -17,7 +17,8 @@ from ._binding import (EXPORTED, LIB_PATH, MLA_BF16, MLA_FP8_E4M3, MLA_DEV_LENGT
                        query_dims, wo_proj,
                        materialize_wkq, materialize_wov, absorb_q_materialized, ov_proj,
                        decode_attn_noalloc, decode_combine, decode_split, decode_step, dims,
-                       dtype_code, load, num_splits, out_proj, workspace_bytes)
+                       dtype_code, load, num_splits, out_proj, set_launch_overlap,
+                       workspace_bytes)
 
 __all__ = [
     "EXPORTED", "LIB_PATH", "MLA_BF16", "MLA_F32", "MLA_FP8_E4M3", "MLA_DEV_LENGTH_OUT_OF_RANGE",
@@ -27,7 +28,7 @@ __all__ = [
     "absorb_q_materialized", "ov_proj",
     "decode_attn_noalloc", "decode_split", "decode_combine", "decode_step", "dims",
     "dtype_code", "load", "num_splits", "out_proj", "workspace_bytes", "DecodeStep", "HostStep",
-    "cache_append", "wo_proj",
+    "cache_append", "wo_proj", "set_launch_overlap",
 ]
 
 
@@ -108,6 +109,9 @@ class DecodeStep:
     def capture(self, cache, w_uk, w_uv):
         """Capture one whole step from host memory as a CUDA graph.
 
+        The returned ``HostStep`` keeps ``cache``, ``w_uk``, ``w_uv`` and this
+        step alive for as long as it exists.
+
         Returns a ``HostStep``: pinned host tensors ``q_nope``, ``q_rope``,
         ``lengths``, ``positions`` (the step's inputs, filled by the caller) and
         ``out`` (o, written by the step), and ``replay()``.  Every replay runs
@@ -156,6 +160,9 @@ class HostStep:
         self.d2h_bytes = self.out.numel() * self.out.element_size()
 
         h = (self.q_nope, self.q_rope, self.lengths, self.positions)
+        # The graph holds raw addresses: keep every tensor it reads or writes (and
+        # the step that owns the intermediates) alive as long as this object.
+        self._keep = (step, cache, w_uk, w_uv)
 
         def body():
             step.run(h[0], h[1], cache, h[2], h[3], w_uk, w_uv, out=self.out)

@@ -26,7 +26,8 @@ EXPORTED = ("mla_absorb_q", "mla_decode_num_splits", "mla_decode_workspace_bytes
             "mla_out_proj", "mla_cache_append",
             "mla_wo_proj", "mla_materialize_wkq", "mla_materialize_wov",
             "mla_absorb_q_materialized", "mla_ov_proj",
-            "mla_status_string", "mla_last_error_message")
+            "mla_status_string", "mla_last_error_message", "mla_test_set_split_hooks",
+            "mla_set_launch_overlap")
 
 
 class MlaDims(ctypes.Structure):
@@ -100,9 +101,18 @@ def load(path: Optional[str] = None):
     lib.mla_status_string.restype = ctypes.c_char_p
     lib.mla_last_error_message.argtypes = []
     lib.mla_last_error_message.restype = ctypes.c_char_p
+    lib.mla_test_set_split_hooks.argtypes = [ctypes.c_uint64, I32]
+    lib.mla_test_set_split_hooks.restype = None
+    lib.mla_set_launch_overlap.argtypes = [I32]
+    lib.mla_set_launch_overlap.restype = None
     if path is None:
         _lib = lib
     return lib
+
+
+def set_launch_overlap(enable: bool) -> None:
+    """Programmatic dependent launch on (default) or off for later launches."""
+    load().mla_set_launch_overlap(1 if enable else 0)
 
 
 def _check(code: int):

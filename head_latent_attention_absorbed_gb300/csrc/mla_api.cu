@@ -65,6 +65,34 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// A driver function by name and ABI version through the runtime's entry-point
+// query; NULL if the driver does not provide it.
+static void* driver_entry(const char* name, unsigned int version) {
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, version, cudaEnableDefault, &q) == cudaSuccess &&
+      q == cudaDriverEntryPointSuccess)
+    return f;
+  cudaGetLastError();
+  return nullptr;
+}
+
+unsigned long long current_context_id() {
+  static const auto get_current =
+      reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(driver_entry("cuCtxGetCurrent", 4000));
+  static const auto get_id =
+      reinterpret_cast<PFN_cuCtxGetId_v12000>(driver_entry("cuCtxGetId", 12000));
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+static std::atomic<int> g_launch_overlap{1};
+
+bool launch_overlap_enabled() { return g_launch_overlap.load(std::memory_order_relaxed) != 0; }
+
 mla_status launch_status(const char* who) {
   cudaError_t e = cudaPeekAtLastError();
   if (e != cudaSuccess) {
@@ -89,3 +117,7 @@ extern "C" const char* mla_status_string(mla_status s) {
 }
 
 extern "C" const char* mla_last_error_message(void) { return mla::g_last_error; }
+
+extern "C" void mla_set_launch_overlap(int32_t enable) {
+  mla::g_launch_overlap.store(enable != 0 ? 1 : 0);
+}

@@ -333,6 +333,11 @@ struct CachePrefetch {
 // process, thread-safely; NULL if the driver does not provide it.
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
+// The calling thread's current CUDA context as the driver's process-unique ID
+// (cuCtxGetId, never reused by a later context); 0 if there is no current
+// context or the driver lacks the call.
+unsigned long long current_context_id();
+
 // One bit per device ordinal (below 64): kernel attributes such as the
 // dynamic shared-memory limit belong to a device, so a set-up made once per
 // process would leave every other device of the process without it.
@@ -349,7 +354,12 @@ inline int current_device() {
   return cudaGetDevice(&d) == cudaSuccess ? d : -1;
 }
 
-// Launches `kernel` with programmatic stream serialization (see pdl_wait).
+// Whether launches may overlap their predecessor (mla_set_launch_overlap; on
+// by default).
+bool launch_overlap_enabled();
+
+// Launches `kernel` with programmatic stream serialization (see pdl_wait), or
+// as a plain launch when overlap is switched off.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t stream, Args&&... args) {
@@ -362,7 +372,7 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = launch_overlap_enabled() ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 

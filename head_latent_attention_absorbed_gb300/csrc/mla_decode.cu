@@ -91,20 +91,31 @@ struct TcPlan {
   static_assert(kSlotsA % 2 == 0, "each score issuer owns every other ring-A slot");
 };
 
-// Waits for a phase; gives up (and raises the CTA's abort flag) after kWaitNs,
+// Waits for a phase; gives up (and raises the CTA's abort flag) after limit_ns,
 // or at once when another role has already raised it.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort,
+                                              unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       *abort = 1;
       return false;
     }
   }
+}
+
+// After an abort: waits (bounded) until the copy armed on `bar` for the phase
+// with this parity has landed, so that no copy into shared memory is still in
+// flight when the CTA leaves.  A phase that completed before returns at once.
+__device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity,
+                                            unsigned long long limit_ns) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > limit_ns) return;
 }
 
 // Per-head max (or sum) of v[0..7] over the 32 lanes of a warp: one exchange
@@ -187,6 +198,8 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
   volatile int* s_issued = reinterpret_cast<volatile int*>(smem + kOffIssued);   // [2]
   uint32_t* slot_ptr = reinterpret_cast<uint32_t*>(smem + kOffSlot);
+  // Limit of every bounded wait below (a test hook may shorten it).
+  const unsigned long long wait_ns = p.wait_ns ? p.wait_ns : kWaitNs;
 
   // With 32 columns the CTA may hold two tokens of a multi-token step (pair):
   // columns 0-15 are the 16 heads of query group b, 16-31 those of b + 1, the
@@ -316,38 +329,49 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
   if (warp == kWarpA) {
     // ------------------------------------------------------------ ring A (HBM)
     if (lane == 0) {
+      int issued = kSlotsA;   // stream positions issued so far (the first fills included)
       for (int t = 0; t < T && !*abort_flag; ++t) {
+        if (p.stop_after_tiles > 0 && t >= p.stop_after_tiles) break;   // test hook
         for (int k = 0; k < 9; ++k) {
           const int pos = 9 * t + k, sl = pos % kSlotsA, use = pos / kSlotsA;
           if (pos < kSlotsA) continue;   // issued before the CTA-wide barrier
-          if (use > 0 && !wait_or_abort(bar(BAR_EMPTYA + sl), (use - 1) & 1, abort_flag)) break;
+          if (use > 0 && !wait_or_abort(bar(BAR_EMPTYA + sl), (use - 1) & 1, abort_flag, wait_ns)) break;
           mbar_arrive_expect_tx(bar(BAR_FULLA + sl), kBoxBytes);
           tma_load_2d(sbase + kOffA + sl * kBoxBytes, &tmap, 64 * box_at(t, k),
                       row_base + t * kTileRows, bar(BAR_FULLA + sl), keep);
+          issued = pos + 1;
         }
       }
+      // After an abort, the boxes still in flight (at most the last use of each
+      // slot) land before the CTA leaves.
+      if (*abort_flag)
+        for (int pos = issued > kSlotsA ? issued - kSlotsA : 0; pos < issued; ++pos)
+          drain_phase(bar(BAR_FULLA + pos % kSlotsA), (pos / kSlotsA) & 1, wait_ns);
     }
   } else if (warp == kWarpB) {
     // ------------------------------------------------------------ ring B (L2)
     if (lane == 0) {
       prefetch_tmap(&tmap_half);
       const uint64_t stream = l2_evict_first_policy();
+      int issued = 0;          // ring-B positions issued (8 per tile)
+      uint32_t armed_x = 0;    // single-use barriers BAR_FULLX + k armed
       for (int t = 0; t < T && !*abort_flag; ++t) {
         if (kResidentTail && t == T - 1) {
           // The last tile's boxes that left ring A: block 0's into the query
           // area once every score MMA has finished, a second block's into the
           // ring-B space once the PV of tile T-2 has finished too.
-          if (!wait_or_abort(bar(BAR_LASTA), 0, abort_flag)) break;
+          if (!wait_or_abort(bar(BAR_LASTA), 0, abort_flag, wait_ns)) break;
           bool second = false;
           for (int k = 0; k < 8; ++k) {
             if (tail_res(k >> 1)) continue;
             if (k >= 2 && !second) {
-              if (T >= 2 && !wait_or_abort(bar(BAR_PVPREV), 0, abort_flag)) break;
+              if (T >= 2 && !wait_or_abort(bar(BAR_PVPREV), 0, abort_flag, wait_ns)) break;
               second = true;
             }
             mbar_arrive_expect_tx(bar(BAR_FULLX + k), kBoxBytes);
             tma_load_2d(sbase + tail_box_off(k), &tmap, 64 * k, row_base + t * kTileRows,
                         bar(BAR_FULLX + k), stream);
+            armed_x |= 1u << k;
           }
           break;
         }
@@ -356,7 +380,7 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
         if (t > 0 && !(t == T - 1 && T >= 2)) {
           const unsigned long long t0 = globaltimer_ns();
           while ((s_issued[0] <= t || s_issued[1] <= t) && !*abort_flag)
-            if (globaltimer_ns() - t0 > kWaitNs) *abort_flag = 1;
+            if (globaltimer_ns() - t0 > wait_ns) *abort_flag = 1;
         }
         // Unit u holds O^T block mb = u % 4 (ring slot mb) for row half u / 4.
         bool lasta = false;
@@ -365,23 +389,33 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
           const int row = row_base + t * kTileRows + 64 * kh;
           if (borrowed(t, u)) {
             const int x = borrow_x(u);
-            if (!lasta && !wait_or_abort(bar(BAR_LASTA), 0, abort_flag)) break;
+            if (!lasta && !wait_or_abort(bar(BAR_LASTA), 0, abort_flag, wait_ns)) break;
             lasta = true;
             mbar_arrive_expect_tx(bar(BAR_FULLX + x), 2 * kHalfBox);
 #pragma unroll
             for (int h = 0; h < 2; ++h)
               tma_load_2d(sbase + borrow_off(x) + h * kHalfBox, &tmap_half, 64 * (2 * mb + h), row,
                           bar(BAR_FULLX + x), stream);
+            armed_x |= 1u << x;
             continue;
           }
           const int pos = 8 * t + u, sl = pos % kSlotsB, use = pos / kSlotsB;
-          if (use > 0 && !wait_or_abort(bar(BAR_EMPTYB + sl), (use - 1) & 1, abort_flag)) break;
+          if (use > 0 && !wait_or_abort(bar(BAR_EMPTYB + sl), (use - 1) & 1, abort_flag, wait_ns)) break;
           mbar_arrive_expect_tx(bar(BAR_FULLB + sl), 2 * kHalfBox);
 #pragma unroll
           for (int h = 0; h < 2; ++h)
             tma_load_2d(sbase + kOffB + (2 * sl + h) * kHalfBox, &tmap_half, 64 * (2 * mb + h),
                         row, bar(BAR_FULLB + sl), stream);
+          issued = pos + 1;
         }
+      }
+      // After an abort, the pairs still in flight land before the CTA leaves:
+      // the last use of each ring slot, and every single-use barrier armed.
+      if (*abort_flag) {
+        for (int pos = issued > kSlotsB ? issued - kSlotsB : 0; pos < issued; ++pos)
+          drain_phase(bar(BAR_FULLB + pos % kSlotsB), (pos / kSlotsB) & 1, wait_ns);
+        for (int k = 0; k < 8; ++k)
+          if (armed_x >> k & 1u) drain_phase(bar(BAR_FULLX + k), 0, wait_ns);
       }
     }
   } else if (warp < kSoftWarps || warp == kWarpS0 || warp == kWarpS1) {
@@ -441,11 +475,11 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
       // Block mb's two 64-column boxes 2mb, 2mb + 1 (128 rows each, kBoxBytes
       // apart): still in ring A or read again into the ring-B space.
       const int k0 = 2 * mb;
-      if (zero_last && (!wait_or_abort(bar(BAR_ZEROX + k0), 0, abort_flag) ||
-                        !wait_or_abort(bar(BAR_ZEROX + k0 + 1), 0, abort_flag)))
+      if (zero_last && (!wait_or_abort(bar(BAR_ZEROX + k0), 0, abort_flag, wait_ns) ||
+                        !wait_or_abort(bar(BAR_ZEROX + k0 + 1), 0, abort_flag, wait_ns)))
         return false;
-      if (!tail_res(mb) && (!wait_or_abort(bar(BAR_FULLX + k0), 0, abort_flag) ||
-                     !wait_or_abort(bar(BAR_FULLX + k0 + 1), 0, abort_flag)))
+      if (!tail_res(mb) && (!wait_or_abort(bar(BAR_FULLX + k0), 0, abort_flag, wait_ns) ||
+                     !wait_or_abort(bar(BAR_FULLX + k0 + 1), 0, abort_flag, wait_ns)))
         return false;
       tc_fence_after();
       const uint64_t c = umma_desc_sw128(sbase + kOffA, kBoxBytes, 1024) +
@@ -462,10 +496,10 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
     const bool bw = borrowed(t, u);
     const int x = bw ? borrow_x(u) : 0;
     if (t == T - 1 && zero_last &&
-        !wait_or_abort(bw ? bar(BAR_ZEROX + x) : bar(BAR_ZEROB + sl), 0, abort_flag))
+        !wait_or_abort(bw ? bar(BAR_ZEROX + x) : bar(BAR_ZEROB + sl), 0, abort_flag, wait_ns))
       return false;
     if (!wait_or_abort(bw ? bar(BAR_FULLX + x) : bar(BAR_FULLB + sl), bw ? 0 : (pos / kSlotsB) & 1,
-                       abort_flag))
+                       abort_flag, wait_ns))
       return false;
     tc_fence_after();
     // MN-major pair: two 64-column boxes kHalfBox apart; the descriptor's
@@ -499,11 +533,11 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
       const uint32_t dS = tmem + kS1Col * i;
       for (int t = 0; t < T; ++t) {
         const int sb = t & 1;
-        if (t >= 2 && !wait_or_abort(bar(BAR_SFREE + sb), ((t - 2) >> 1) & 1, abort_flag)) break;
+        if (t >= 2 && !wait_or_abort(bar(BAR_SFREE + sb), ((t - 2) >> 1) & 1, abort_flag, wait_ns)) break;
         bool ok = true, first = true;
         for (int k = (9 * t + i) & 1; k < 9; k += 2) {
           const int pos = 9 * t + k, sl = pos % kSlotsA;
-          if (!wait_or_abort(bar(BAR_FULLA + sl), (pos / kSlotsA) & 1, abort_flag)) {
+          if (!wait_or_abort(bar(BAR_FULLA + sl), (pos / kSlotsA) & 1, abort_flag, wait_ns)) {
             ok = false;
             break;
           }
@@ -528,8 +562,8 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
       {
         const int t = T - 1;
         bool ok = !*abort_flag;
-        if (ok && T >= 2 && !wait_or_abort(bar(BAR_PVPREV), 0, abort_flag)) ok = false;
-        if (ok && !wait_or_abort(bar(BAR_PFULL + (t & 1)), (t >> 1) & 1, abort_flag)) ok = false;
+        if (ok && T >= 2 && !wait_or_abort(bar(BAR_PVPREV), 0, abort_flag, wait_ns)) ok = false;
+        if (ok && !wait_or_abort(bar(BAR_PFULL + (t & 1)), (t >> 1) & 1, abort_flag, wait_ns)) ok = false;
         if (ok && pv_unit(t, 2 + i)) pv_unit(t, 6 + i);
         umma_commit(bar(BAR_ODONE2));
       }
@@ -544,7 +578,7 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
     if (lane == 0) {
       const int i = warp - kWarpPV0;
       for (int t = 0; t < T; ++t) {
-        if (!wait_or_abort(bar(BAR_PFULL + (t & 1)), (t >> 1) & 1, abort_flag)) break;
+        if (!wait_or_abort(bar(BAR_PFULL + (t & 1)), (t >> 1) & 1, abort_flag, wait_ns)) break;
         bool ok = true;
         const int step = t == T - 1 ? 4 : 2;
         for (int u = i; u < 8 && ok; u += step) ok = pv_unit(t, u);
@@ -573,7 +607,7 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
       if (pair)   // this group's token ends at its own length
         valid = min(max(min(r0 + p.chunk, gp < 2 ? len_first : len) - (r0 + t * kTileRows), 0),
                     kTileRows);
-      wait_or_abort(bar(BAR_SFULL + sb), (t >> 1) & 1, abort_flag);
+      wait_or_abort(bar(BAR_SFULL + sb), (t >> 1) & 1, abort_flag, wait_ns);
       tc_fence_after();
       float sc[kHalfHeads], tt[kHalfHeads];
       {
@@ -619,7 +653,7 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
           l[h] *= alpha[h];
         }
         if (t > 0) {
-          wait_or_abort(bar(BAR_ODONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag);
+          wait_or_abort(bar(BAR_ODONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag, wait_ns);
           tc_fence_after();
 #pragma unroll
           for (int mb = 0; mb < 4; ++mb) {
@@ -646,7 +680,8 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
       }
       // P^T buffer sb was last read by the PV of tile t-2.
       if (t >= kPBufs)
-        wait_or_abort(bar(BAR_ODONE + ((t - kPBufs) & 1)), ((t - kPBufs) >> 1) & 1, abort_flag);
+        wait_or_abort(bar(BAR_ODONE + ((t - kPBufs) & 1)), ((t - kPBufs) >> 1) & 1, abort_flag,
+                      wait_ns);
       {
         // P^T (B operand of the PV MMA, K-major 128-byte swizzle, two 64-row
         // halves): row n < 16 is bf16(p) of head n, row 16 + n is
@@ -676,7 +711,7 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
           // has read) or once read again.
           const int nrow = kTileRows - zero_from;
           for (int k = 0; k < 8; ++k) {
-            if (!tail_res(k >> 1)) wait_or_abort(bar(BAR_FULLX + k), 0, abort_flag);
+            if (!tail_res(k >> 1)) wait_or_abort(bar(BAR_FULLX + k), 0, abort_flag, wait_ns);
             uint8_t* box = smem + tail_box_off(k) + zero_from * 128;
             for (int c = tid; c < nrow * 8; c += kSoftThreads)
               *reinterpret_cast<uint4*>(box + c * 16) = make_uint4(0, 0, 0, 0);
@@ -693,7 +728,7 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
           const bool bw = borrowed(t, u);
           const int x = bw ? borrow_x(u) : 0;
           wait_or_abort(bw ? bar(BAR_FULLX + x) : bar(BAR_FULLB + sl), bw ? 0 : (pos / kSlotsB) & 1,
-                        abort_flag);
+                        abort_flag, wait_ns);
           uint8_t* pair = smem + (bw ? borrow_off(x) : kOffB + 2 * sl * kHalfBox);
           for (int c = tid; c < 2 * nrow * 8; c += kSoftThreads) {
             const int h = c / (nrow * 8), rem = c % (nrow * 8);
@@ -718,8 +753,8 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
       if (lane < 16 && (lane & 1) == 0) lsum[(hb + (lane >> 1)) * 4 + wq] = ws;
     }
     // O^T after the last PV: this thread's latent row is d = 128 mb + 32 wq + lane.
-    wait_or_abort(bar(BAR_ODONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1, abort_flag);
-    wait_or_abort(bar(BAR_ODONE2), 0, abort_flag);
+    wait_or_abort(bar(BAR_ODONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1, abort_flag, wait_ns);
+    wait_or_abort(bar(BAR_ODONE2), 0, abort_flag, wait_ns);
     tc_fence_after();
     named_bar_sync(1, kSoftThreads);
     if (!*abort_flag) {
@@ -1143,6 +1178,15 @@ extern "C" size_t mla_decode_workspace_bytes(const mla_dims* dims, int32_t reque
   return workspace_bytes(dims, splits);
 }
 
+// Test hooks of the bf16 split kernel (mla_test_set_split_hooks); 0 in normal use.
+static std::atomic<unsigned long long> g_hook_wait_ns{0};
+static std::atomic<int> g_hook_stop_tiles{0};
+
+extern "C" void mla_test_set_split_hooks(uint64_t wait_ns, int32_t stop_after_tiles) {
+  g_hook_wait_ns.store(wait_ns);
+  g_hook_stop_tiles.store(stop_after_tiles > 0 ? stop_after_tiles : 0);
+}
+
 // Validates the arguments shared by the split and combine halves and fills the
 // kernel parameters.  `dims` describes the cache (dims->batch sequences); with
 // q_len query tokens per sequence the queries, partials and outputs have
@@ -1205,6 +1249,9 @@ static mla_status prepare(const char* who, const mla_dims* dims, int q_len, cons
   p->splits = splits;
   p->chunk = chunk;
   p->scale_log2 = softmax_scale * kLog2e;
+  p->fill_early = 0;
+  p->wait_ns = g_hook_wait_ns.load();
+  p->stop_after_tiles = g_hook_stop_tiles.load();
   return MLA_OK;
 }
 
@@ -1498,10 +1545,19 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[MLA_NOALLOC_SCRATCH_B
 namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
-void* g_noalloc_ptr[kMaxDevices] = {};   // device address of the array, per device
+// Device address of the array per device ordinal, and the context it belongs to.
+struct NoallocAddr {
+  unsigned long long ctx_id;
+  void* ptr;
+};
+NoallocAddr g_noalloc_addr[kMaxDevices] = {};
 
 // The array's name in host code is only a host-side handle, so the device address
-// is asked from the runtime once per device, with that device current.
+// is asked from the runtime with the device current.  The address belongs to the
+// library's module as loaded in one context: after cudaDeviceReset, or with another
+// context current on the same device, the module is loaded again and the array may
+// move.  So the address is kept together with the context's process-unique ID and
+// asked again whenever the current context differs (or its ID is unknown).
 mla_status noalloc_scratch(const char* who, void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -1513,7 +1569,9 @@ mla_status noalloc_scratch(const char* who, void** out) {
     return MLA_ERR_UNSUPPORTED;
   }
   std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-  if (!g_noalloc_ptr[dev]) {
+  NoallocAddr& a = g_noalloc_addr[dev];
+  const unsigned long long ctx = current_context_id();
+  if (ctx == 0 || a.ctx_id != ctx || !a.ptr) {
     void* ptr = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
     if (e != cudaSuccess || !ptr) {
@@ -1521,9 +1579,11 @@ mla_status noalloc_scratch(const char* who, void** out) {
                 cudaGetErrorString(e));
       return MLA_ERR_CUDA;
     }
-    g_noalloc_ptr[dev] = ptr;
+    // The lookup may have created the device's primary context: take its ID now.
+    a.ctx_id = current_context_id();
+    a.ptr = ptr;
   }
-  *out = g_noalloc_ptr[dev];
+  *out = a.ptr;
   return MLA_OK;
 }
 }  // namespace

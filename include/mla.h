@@ -37,7 +37,7 @@
  *    Every result -- the absorbed query q_abs, the rotated q_pe, o_c, lse,
  *    the output o -- and the workspace are fp32 in every case (the bf16
  *    decode kernel feeds the fp32 query and the softmax weights to the
- *    tensor cores as hi + lo bf16 pairs, the FP8 kernel as three and two
+ *    tensor cores as hi + lo bf16 pairs, the FP8 kernel as four and three
  *    E4M3 parts).
  *  - Launch overlap: the kernels of mla_decode_attn (and of its halves), the
  *    bf16 kernel of mla_out_proj, and the fused tail of mla_decode_step are
@@ -92,7 +92,7 @@ typedef struct mla_dims {
 
 /* Bits a kernel ORs into the optional device status word (see mla_decode_attn). */
 #define MLA_DEV_LENGTH_OUT_OF_RANGE 1  /* some lengths[b] < 1 (< q_len) or > s_max */
-#define MLA_DEV_PIPELINE_TIMEOUT 2     /* a bounded wait on a TMA copy gave up  */
+#define MLA_DEV_PIPELINE_TIMEOUT 2     /* a bounded wait in a kernel's pipeline gave up */
 
 /*
  * mla_absorb_q -- absorbed query and rotated RoPE query for one decode step.
@@ -245,9 +245,12 @@ mla_status mla_decode_attn_multi(const mla_dims* dims, int32_t q_len, const void
  * (mla_decode_workspace_bytes(dims, num_splits) > MLA_NOALLOC_SCRATCH_BYTES)
  * returns MLA_ERR_WORKSPACE and launches nothing.
  *
- * First call on a device: it asks the runtime for the array's device address
- * with that device current and keeps it; make that first call before any
- * stream capture begins.
+ * First call on a device (and in each CUDA context): it asks the runtime for
+ * the array's device address with that device current and keeps it together
+ * with the context's unique ID; make that first call before any stream capture
+ * begins.  A later call from another context (after cudaDeviceReset, or with
+ * another context current on the same device) asks again before it launches
+ * anything, since the library's module and the array are loaded anew there.
  *
  * Sharing: every call on a device uses the same array, which keeps the last
  * call's contents (nothing needs clearing: a call reads only what it wrote).
@@ -410,6 +413,42 @@ const char* mla_status_string(mla_status status);
 
 /* Detail of the calling thread's most recent failed call ("" if none). */
 const char* mla_last_error_message(void);
+
+/*
+ * mla_set_launch_overlap -- whether the library's kernels are launched with
+ * programmatic dependent launch (1, the default) or as plain launches (0).
+ *
+ * With overlap, a kernel may start while its predecessor on the stream is
+ * still running: it prepares (tensor memory, barriers, weight and cache
+ * prefetches) and waits on the device before it reads that predecessor's
+ * results.  Without it, every launch starts only after the previous one has
+ * finished, so a graph of back-to-back launches times each launch whole.
+ * Results are the same either way.  Process-wide; read when a kernel is
+ * enqueued (a graph keeps the launch form of its capture).  Not an operation
+ * of the pages: a measurement switch of this library.
+ */
+void mla_set_launch_overlap(int32_t enable);
+
+/*
+ * mla_test_set_split_hooks -- test hooks of the bf16 split kernel; not for
+ * production use.  The pages have no counterpart: this exists so that a test
+ * can make the kernel's bounded waits run out without faulting or hanging the
+ * GPU (the overflow-returns-an-error rule of "Transformer and KV Cache Basics",
+ * applied to the kernel's own pipeline).
+ *
+ * wait_ns           limit of every bounded wait of the bf16 split kernel in ns
+ *                   (0: the default of 2 s).
+ * stop_after_tiles  > 0: the kernel's HBM ring issues only the first
+ *                   stop_after_tiles 128-row tiles of each chunk, so a chunk
+ *                   with more tiles leaves its consumers waiting; they give up
+ *                   after wait_ns, set MLA_DEV_PIPELINE_TIMEOUT in dev_status,
+ *                   write no partial, let the copies still in flight land, free
+ *                   their tensor memory and return.  0: normal operation.
+ *
+ * Process-wide; read when a split is enqueued (launches captured in a graph
+ * keep the values of their capture).  Reset with (0, 0) after the test.
+ */
+void mla_test_set_split_hooks(uint64_t wait_ns, int32_t stop_after_tiles);
 
 #ifdef __cplusplus
 }

@@ -5,15 +5,19 @@ the library instead of a caller-supplied workspace.
 
 Checked through the C ABI against mla_decode_attn on the same inputs, on two calls
 in a row with different inputs and chunk counts, so a second call that saw the first
-call's leftovers in the shared array would show.  This file is collected last.
+call's leftovers in the shared array would show.  Both calls run the same kernels
+with the same chunking on the same inputs, so their results must be equal bit for
+bit.  With an FP8 cache the scratch also holds the query's E4M3 image after the
+partials, which the size check counts.  This file is collected last.
 """
 import ctypes
 
+import numpy as np
 import pytest
 import torch
 
-from _parity import assert_close
-from workloads import V2LITE_BF16_B8_S4096, MlaConfig, make_inputs
+from workloads import (V2LITE_BF16_B8_S4096, V2LITE_FP8_B8_S4096, MlaConfig, cache_storage,
+                       make_inputs)
 
 pytestmark = pytest.mark.gpu
 
@@ -21,7 +25,7 @@ pytestmark = pytest.mark.gpu
 def _decode_both(mla, inp, num_splits):
     """o_c and lse from mla_decode_attn (caller workspace) and from the fixed-scratch call."""
     cfg = inp.cfg
-    dt = torch.float32 if cfg.dtype == "f32" else torch.bfloat16
+    dt = cache_storage(cfg)   # the cache's type names the library dtype
     dev = "cuda"
     B, H = cfg.batch, cfg.heads
     d = mla.dims(B, H, cfg.s_max, mla.dtype_code(dt))
@@ -48,20 +52,25 @@ def _decode_both(mla, inp, num_splits):
     return out
 
 
-def test_noalloc_matches_workspace_call_twice(cuda_lib):
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
+def test_noalloc_matches_workspace_call_twice(cuda_lib, dtype):
     mla = cuda_lib
     # first call: the 8 x 4096-row decode workload, library's chunk choice
-    first = make_inputs(V2LITE_BF16_B8_S4096, seed=11)
+    first = make_inputs(V2LITE_BF16_B8_S4096 if dtype == "bf16" else V2LITE_FP8_B8_S4096,
+                        seed=11)
     # second call: other inputs, a ragged batch and fewer chunks, so a partial that
     # the second call failed to write would still hold the first call's value
-    cfg2 = MlaConfig(name="noalloc_ragged_b5_s1000", dtype="bf16", batch=5, heads=16,
+    cfg2 = MlaConfig(name=f"noalloc_ragged_{dtype}_b5_s1000", dtype=dtype, batch=5, heads=16,
                      s_max=1000, hidden=2048)
     second = make_inputs(cfg2, seed=12, poison_tail=True,
                          lengths=torch.tensor([1, 129, 1000, 640, 77], dtype=torch.int32))
     for inp, splits in ((first, 0), (second, 3)):
         r = _decode_both(mla, inp, splits)
-        assert_close("o_c", r["noalloc"][0], r["workspace"][0], "bf16")
-        assert_close("lse", r["noalloc"][1], r["workspace"][1], "bf16")
+        for k, name in ((0, "o_c"), (1, "lse")):
+            got, want = r["noalloc"][k], r["workspace"][k]
+            assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+            assert np.array_equal(got, want), \
+                f"{name}: max abs difference {np.max(np.abs(got - want)):.3e}, equality expected"
 
 
 def test_noalloc_rejects_partials_beyond_the_fixed_size(cuda_lib):
