@@ -27,7 +27,8 @@ EXPORTED = ("mla_absorb_q", "mla_decode_num_splits", "mla_decode_workspace_bytes
             "mla_wo_proj", "mla_materialize_wkq", "mla_materialize_wov",
             "mla_absorb_q_materialized", "mla_ov_proj",
             "mla_status_string", "mla_last_error_message", "mla_test_set_split_hooks",
-            "mla_set_launch_overlap")
+            "mla_set_launch_overlap", "mla_decode_plan", "mla_test_set_split_debug",
+            "mla_test_set_split_form")
 
 
 class MlaDims(ctypes.Structure):
@@ -105,6 +106,13 @@ def load(path: Optional[str] = None):
     lib.mla_test_set_split_hooks.restype = None
     lib.mla_set_launch_overlap.argtypes = [I32]
     lib.mla_set_launch_overlap.restype = None
+    lib.mla_test_set_split_debug.argtypes = [P]
+    lib.mla_test_set_split_debug.restype = None
+    lib.mla_test_set_split_form.argtypes = [I32]
+    lib.mla_test_set_split_form.restype = None
+    lib.mla_decode_plan.argtypes = [D, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
+                                    ctypes.POINTER(I32)]
+    lib.mla_decode_plan.restype = ctypes.c_int
     if path is None:
         _lib = lib
     return lib
@@ -166,6 +174,14 @@ def _cuda_or_pinned(*ts):
 
 def num_splits(d: MlaDims, requested: int = 0) -> int:
     return int(load().mla_decode_num_splits(ctypes.byref(d), int(requested)))
+
+
+def plan(d: MlaDims, requested: int = 0):
+    """(splits, chunk rows, persistent) of the split for `requested` chunks."""
+    sp, ch, pe = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    _check(load().mla_decode_plan(ctypes.byref(d), int(requested), ctypes.byref(sp),
+                                  ctypes.byref(ch), ctypes.byref(pe)))
+    return sp.value, ch.value, bool(pe.value)
 
 
 def workspace_bytes(d: MlaDims, requested: int = 0) -> int:

@@ -45,11 +45,35 @@ constexpr int kHalfBox = kBoxBytes / 2;               // 64 rows x 64 bf16 colum
 // Rescale threshold (log2 units): P may grow to 2^8 before O is rescaled.
 constexpr float kRescaleLog2 = 8.f;
 
+// One work item of a split CTA: one chunk of one query group's rows for one
+// head group.  A CTA of an ordinary grid has one item (its blockIdx); a
+// persistent CTA has the items plan_items gives it, streamed back to back.
+struct SplitItem {
+  int row0;        // cache row (of the [B*s_max, 576] view) of the item's first row
+  int tiles;       // 128-row tiles
+  int t0;          // index of its first tile in the CTA's tile stream
+  int valid_last;  // rows of its last tile that belong to the item
+  int zero_from;   // rows of its last tile before the sequence's end; from there on
+                   // (< 128) rows may hold anything and are zeroed before the PV
+  int part;        // partial row of its first head: (v * H + h0) * splits + j
+  int qv;          // query group (row block of q_abs and q_pe)
+  int h0;          // first head
+};
+// Items a persistent CTA can hold (the planner keeps within it).
+constexpr int kMaxItems = 128;
+// Test hook (mla_test_set_split_form): 0 the planner chooses the split's form,
+// 1 persistent wherever the kernel allows it, 2 never persistent.
+std::atomic<int> g_split_form{0};
+
 // The kernel's plan for kG heads per CTA (16 or 32; N = 2 kG query rows, the
 // heads' hi and lo parts).  kG = 32 halves, per head, the MMAs and the tile
 // reads (shared memory and L2); its query and accumulators need more room, so
-// ring A has four slots and P one buffer.
-template <int kG>
+// ring A has four slots, P one buffer and O^T one buffer.  kPersist: the
+// persistent instance (16 heads per CTA) holds a table of work items and
+// double-buffers O^T in tensor memory, so that a CTA's next item accumulates
+// while the previous one's epilogue reads its result; the ordinary instance
+// has one item and none of that code.
+template <int kG, bool kPersist = false>
 struct TcPlan {
   static constexpr int kSoftWarps = kG / 2;            // four warps per group of 8 heads
   static constexpr int kSoftThreads = 32 * kSoftWarps;
@@ -57,6 +81,8 @@ struct TcPlan {
   static constexpr int kSlotsA = kG == 16 ? 6 : 4;
   static constexpr int kSlotsB = 4;                    // each slot: two adjacent 64-row boxes
   static constexpr int kPBufs = kG == 16 ? 2 : 1;
+  static constexpr int kOBufs = kPersist ? 2 : 1;      // O^T accumulators in tensor memory
+  static constexpr int kItems = kPersist ? kMaxItems : 1;
   static constexpr int kQN = 2 * kG;                   // hi | lo query rows
   static constexpr int kQBoxBytes = kQN * 128;
   static constexpr int kPSub = kQN * 128;              // P^T: 64 tile rows of kQN rows
@@ -67,7 +93,8 @@ struct TcPlan {
   static constexpr int kOffP = kOffQ + 9 * kQBoxBytes;
   static constexpr int kOffRed = kOffP + kPBufs * kPBytes;   // [2][kG heads][4 warps] tile maxima
   static constexpr int kOffLsum = kOffRed + 2 * kG * 4 * 4;
-  static constexpr int kOffBar = kOffLsum + kG * 4 * 4;
+  static constexpr int kOffItems = kOffLsum + kG * 4 * 4;
+  static constexpr int kOffBar = kOffItems + kItems * static_cast<int>(sizeof(SplitItem));
   static constexpr int BAR_FULLA = 0, BAR_EMPTYA = kSlotsA, BAR_FULLB = 2 * kSlotsA,
                        BAR_EMPTYB = BAR_FULLB + kSlotsB, BAR_ZEROB = BAR_EMPTYB + kSlotsB,
                        BAR_SFULL = BAR_ZEROB + kSlotsB, BAR_SFREE = BAR_SFULL + 2,
@@ -75,16 +102,20 @@ struct TcPlan {
                        BAR_LASTA = BAR_ODONE + 2, BAR_FULLX = BAR_LASTA + 1,
                        BAR_ZEROX = BAR_FULLX + 8, BAR_ODONE2 = BAR_ZEROX + 8,
                        BAR_PVPREV = BAR_ODONE2 + 1, BAR_DONE = BAR_PVPREV + 1,
-                       kNumBars = BAR_DONE + 1;
+                       BAR_QFREE = BAR_DONE + 1, BAR_QREADY = BAR_QFREE + 1,
+                       BAR_ODRAIN = BAR_QREADY + 1, kNumBars = BAR_ODRAIN + 2;
   static constexpr int kOffSlot = kOffBar + 8 * kNumBars;
   static constexpr int kOffAbort = kOffSlot + 16;
   static constexpr int kOffIssued = kOffAbort + 16;   // score tiles issued, per score issuer
-  static constexpr size_t kSmem = 1024 + kOffIssued + 16;
+  static constexpr int kOffCount = kOffIssued + 16;   // [items, tiles] of this CTA
+  static constexpr size_t kSmem = 1024 + kOffCount + 16;
   // TMEM: S_0[2] at 0 / kQN, S_1[2] at kS1Col / kS1Col + kQN, O^T blocks of kQN
-  // columns from kOCol.
+  // columns from kOCol (buffer x at kOCol + x kOBufCols).
   static constexpr uint32_t kS1Col = 2 * kQN;
   static constexpr uint32_t kOCol = 4 * kQN;
-  static constexpr uint32_t kTmemCols = 8 * kQN;       // 256 or 512
+  static constexpr uint32_t kOBufCols = 4 * kQN;
+  static constexpr uint32_t kTmemCols = kG == 16 && !kPersist ? 256 : 512;
+  static_assert(kOCol + kOBufs * kOBufCols <= kTmemCols, "tensor memory plan");
   static_assert(kSmem <= 232448, "shared memory plan exceeds 227 KB");
   static_assert(kSlotsA * kBoxBytes + 9 * kQBoxBytes >= 8 * kBoxBytes,
                 "the last tile's eight latent pairs fit in ring A and the query area");
@@ -102,6 +133,10 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort) return false;
     if (globaltimer_ns() - t0 > limit_ns) {
+      // The words after the flag keep where the CTA's first wait gave up (the
+      // barrier's address, its parity and the waiting thread), for a test hook.
+      abort[1] = static_cast<int>(bar);
+      abort[2] = static_cast<int>(parity | (threadIdx.x << 8));
       *abort = 1;
       return false;
     }
@@ -116,6 +151,97 @@ __device__ __forceinline__ void drain_phase(uint32_t bar, uint32_t parity,
   const unsigned long long t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity))
     if (globaltimer_ns() - t0 > limit_ns) return;
+}
+
+// Exclusive prefix sum of x over the warp's lanes, and the warp's total.
+__device__ __forceinline__ int warp_exclusive_scan(int x, int lane, int* total) {
+  int incl = x;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += y;
+  }
+  *total = __shfl_sync(0xffffffffu, incl, 31);
+  return incl - x;
+}
+
+// Persistent grid: the items of CTA c of G, computed by one whole warp.  Every
+// (head group, query group, chunk) with rows is an item; items are ordered by
+// head group, then query group, then chunk, which numbers every tile of every
+// item consecutively (TT tiles in all).  CTA c takes the items whose first tile
+// falls in [c TT / G, (c + 1) TT / G): an equal share of the tiles, give or take
+// one chunk, and mostly consecutive chunks of one sequence (one query load).
+// Chunks are whole tiles here (chunk % 128 == 0), so a tile never straddles two
+// items.  Writes items[0..n) with their first tile in the CTA's stream and
+// counts[0] = n, counts[1] = tiles; n > kMaxItems (never planned) raises
+// MLA_DEV_PIPELINE_TIMEOUT and keeps the first kMaxItems.
+__device__ void plan_items(const SplitParams& p, SplitItem* items, volatile int* counts,
+                           int lane) {
+  const int groups = p.H / 16, ct = p.chunk / kTileRows;
+  const long long G = gridDim.x, c = blockIdx.x;
+  // Tiles of one head group: the sum over query groups of ceil(len / 128).
+  long long tg = 0;
+  for (int v0 = 0; v0 < p.B; v0 += 32) {
+    const int v = v0 + lane;
+    const int len = v < p.B ? clamp_length(p, v, c == 0) : 0;
+    int tot;
+    warp_exclusive_scan((len + kTileRows - 1) / kTileRows, lane, &tot);
+    tg += tot;
+  }
+  const long long TT = groups * tg, lo = c * TT / G, hi = (c + 1) * TT / G;
+  int n = 0;
+  long long base = 0;   // first tile of the current block of query groups
+  for (int g = 0; g < groups && base < hi; ++g) {
+    for (int v0 = 0; v0 < p.B && base < hi; v0 += 32) {
+      const int v = v0 + lane;
+      const int len = v < p.B ? clamp_length(p, v, false) : 0;
+      const int tiles = (len + kTileRows - 1) / kTileRows;
+      int tot;
+      const long long s = base + warp_exclusive_scan(tiles, lane, &tot);   // its first tile
+      // chunks j of this query group whose first tile s + j ct is in [lo, hi)
+      const int nch = (tiles + ct - 1) / ct;
+      long long jlo = lo > s ? (lo - s + ct - 1) / ct : 0;
+      long long jhi = hi > s ? (hi - s + ct - 1) / ct : 0;
+      jlo = jlo < nch ? jlo : nch;
+      jhi = jhi < nch ? jhi : nch;
+      const int cnt = jhi > jlo ? static_cast<int>(jhi - jlo) : 0;
+      int ctot;
+      int pos = n + warp_exclusive_scan(cnt, lane, &ctot);
+      for (long long jj = jlo; jj < jhi; ++jj, ++pos) {
+        if (pos >= kMaxItems) break;
+        const int j = static_cast<int>(jj);
+        const int r0 = j * p.chunk, r1 = min(r0 + p.chunk, len);
+        const int it = (r1 - r0 + kTileRows - 1) / kTileRows;
+        SplitItem m;
+        m.row0 = cache_seq(p, v) * p.s_max + r0;
+        m.tiles = it;
+        m.t0 = 0;
+        m.valid_last = r1 - (r0 + (it - 1) * kTileRows);
+        m.zero_from = len - (r0 + (it - 1) * kTileRows);
+        m.part = (v * p.H + 16 * g) * p.splits + j;
+        m.qv = v;
+        m.h0 = 16 * g;
+        items[pos] = m;
+      }
+      n += ctot;
+      base += tot;
+    }
+  }
+  __syncwarp();
+  if (lane == 0) {
+    if (n > kMaxItems) {
+      report(p.status, MLA_DEV_PIPELINE_TIMEOUT);
+      n = kMaxItems;
+    }
+    int t = 0;
+    for (int i = 0; i < n; ++i) {
+      items[i].t0 = t;
+      t += items[i].tiles;
+    }
+    counts[0] = n;
+    counts[1] = t;
+  }
+  __syncwarp();
 }
 
 // Per-head max (or sum) of v[0..7] over the 32 lanes of a warp: one exchange
@@ -166,25 +292,38 @@ __device__ __forceinline__ float reduce8_heads(float v[8], int lane) {
 //             exceeds it by 2^8 (then O^T is rescaled in TMEM).
 // The fp32 query and P reach the tensor core as bf16 hi + lo pairs, so their
 // rounding stays near 2^-17 relative.
-template <int kG>
-__global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
+//
+// The CTA works through its items (SplitItem) as one stream of T tiles: the
+// rings and MMA issuers run across item boundaries without a pause.  At the end
+// of an item the softmax warps write its partial one tile later (its O^T buffer
+// is done by then, and the next item accumulates into the other buffer), and
+// when the next item belongs to another query group or head group they load
+// that query into the query area once the score MMAs of the item are done (the
+// score issuers wait for it).  Only the CTA's last tile takes the special tail
+// path (its boxes read in place from ring A).
+template <int kG, bool kPersist>
+__global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
     split_tc_kernel(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap tmap_half,
                     const SplitParams p) {
   // The plan's sizes under the names the body uses (kHeadGroup: heads per CTA).
-  using L = TcPlan<kG>;
+  using L = TcPlan<kG, kPersist>;
+  static_assert(!kPersist || kG == 16, "the persistent instance takes 16 heads per CTA");
   constexpr int kHeadGroup = kG, kHalfHeads = 8, kSoftWarps = L::kSoftWarps;
   constexpr int kSoftThreads = L::kSoftThreads, kSlotsA = L::kSlotsA, kSlotsB = L::kSlotsB;
   constexpr int kPBufs = L::kPBufs, kQN = L::kQN, kQBoxBytes = L::kQBoxBytes, kPSub = L::kPSub;
   constexpr int kPBytes = L::kPBytes, kOffA = L::kOffA, kOffB = L::kOffB, kOffQ = L::kOffQ;
   constexpr int kOffP = L::kOffP, kOffRed = L::kOffRed, kOffLsum = L::kOffLsum;
   constexpr int kOffBar = L::kOffBar, kOffSlot = L::kOffSlot, kOffAbort = L::kOffAbort;
-  constexpr int kOffIssued = L::kOffIssued;
+  constexpr int kOffIssued = L::kOffIssued, kOffItems = L::kOffItems, kOffCount = L::kOffCount;
+
   constexpr uint32_t kS1Col = L::kS1Col, kOCol = L::kOCol, kTmemCols = L::kTmemCols;
+  constexpr uint32_t kOBufCols = L::kOBufCols;
   constexpr int BAR_FULLA = L::BAR_FULLA, BAR_EMPTYA = L::BAR_EMPTYA, BAR_FULLB = L::BAR_FULLB,
                 BAR_EMPTYB = L::BAR_EMPTYB, BAR_ZEROB = L::BAR_ZEROB, BAR_SFULL = L::BAR_SFULL,
                 BAR_SFREE = L::BAR_SFREE, BAR_PFULL = L::BAR_PFULL, BAR_ODONE = L::BAR_ODONE,
                 BAR_LASTA = L::BAR_LASTA, BAR_FULLX = L::BAR_FULLX, BAR_ZEROX = L::BAR_ZEROX,
-                BAR_ODONE2 = L::BAR_ODONE2, BAR_PVPREV = L::BAR_PVPREV, BAR_DONE = L::BAR_DONE;
+                BAR_ODONE2 = L::BAR_ODONE2, BAR_PVPREV = L::BAR_PVPREV, BAR_DONE = L::BAR_DONE,
+                BAR_QFREE = L::BAR_QFREE, BAR_QREADY = L::BAR_QREADY, BAR_ODRAIN = L::BAR_ODRAIN;
   // Role warps after the softmax warps.
   constexpr int kWarpA = kSoftWarps, kWarpS0 = kSoftWarps + 1, kWarpB = kSoftWarps + 2,
                 kWarpS1 = kSoftWarps + 3, kWarpPV0 = kSoftWarps + 4, kWarpPV1 = kSoftWarps + 5;
@@ -195,6 +334,8 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
   const uint32_t bars = sbase + kOffBar;
   float* red = reinterpret_cast<float*>(smem + kOffRed);
   float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
+  SplitItem* items = reinterpret_cast<SplitItem*>(smem + kOffItems);
+  volatile int* counts = reinterpret_cast<volatile int*>(smem + kOffCount);   // [items, tiles]
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffAbort);
   volatile int* s_issued = reinterpret_cast<volatile int*>(smem + kOffIssued);   // [2]
   uint32_t* slot_ptr = reinterpret_cast<uint32_t*>(smem + kOffSlot);
@@ -206,19 +347,17 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
   // next token of the same sequence; the tiles follow the later token's rows
   // and each 8-head softmax group masks the rows past its own token.
   const bool pair = kG == 32 && p.tpc == 2;
-  const int g = blockIdx.x, j = blockIdx.y, b = pair ? 2 * blockIdx.z : blockIdx.z;
+  constexpr bool persist = kPersist;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int r0 = j * p.chunk;
-  const int row_base = cache_seq(p, b) * p.s_max + r0;
   auto bar = [&](int i) { return bars + 8 * i; };
 
   // The cache stream starts before anything else: ring A's producer sets up its
   // own barriers and issues tile 0's first six boxes (stream positions 0-5 hold
   // boxes 0-5; the RoPE-first order below applies only to a last tile after
-  // another) before the CTA-wide barrier.  They need only the chunk's first
-  // row, so in a one-wave grid they go out before the sequence length is known.
+  // another) before the CTA-wide barrier.  In a one-wave grid they need only the
+  // chunk's first row and go out before the sequence length is known.
   const uint64_t keep = l2_evict_last_policy();   // read again by ring B
-  auto first_fills = [&]() {
+  auto first_fills = [&](int row) {
     for (int i = 0; i < kSlotsA; ++i) {
       mbar_init(bar(BAR_FULLA + i), 1);
       mbar_init(bar(BAR_EMPTYA + i), 1);
@@ -227,33 +366,130 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
     prefetch_tmap(&tmap);
     for (int pos = 0; pos < kSlotsA; ++pos) {
       mbar_arrive_expect_tx(bar(BAR_FULLA + pos), kBoxBytes);
-      tma_load_2d(sbase + kOffA + pos * kBoxBytes, &tmap, 64 * pos, row_base,
+      tma_load_2d(sbase + kOffA + pos * kBoxBytes, &tmap, 64 * pos, row,
                   bar(BAR_FULLA + pos), keep);
     }
   };
   const bool ring_a = warp == kWarpA && lane == 0;
-  if (ring_a && p.fill_early) first_fills();
-  // Launched after mla_absorb_q with programmatic serialization: everything up
-  // to the query load (set-up, TMEM, the cache stream) overlaps that kernel.
-  const int len = clamp_length(p, pair ? b + 1 : b, tid == 0 && g == 0 && j == 0);
-  const int len_first = pair ? clamp_length(p, b, tid == 0 && g == 0 && j == 0) : len;
-  if (r0 >= len) {
-    // Chunk past the end of this sequence: nothing to do once early copies
-    // (into this CTA's shared memory) have landed.
-    if (ring_a && p.fill_early)
-      for (int pos = 0; pos < kSlotsA; ++pos) mbar_wait_bounded(bar(BAR_FULLA + pos), 0);
-    return;
+  int len_first = 0, len_pair = 0;   // paired tokens: rows of the earlier and later token
+  int r0_one = 0;                    // one-item CTA: the chunk's first row in its sequence
+  if (persist) {
+    if (warp == kWarpA) plan_items(p, items, counts, lane);
+    __syncthreads();
+    if (counts[0] == 0) return;   // no tile for this CTA
+    if (ring_a) first_fills(items[0].row0);
+  } else {
+    const int g = blockIdx.x, j = blockIdx.y, b = pair ? 2 * blockIdx.z : blockIdx.z;
+    const int r0 = j * p.chunk;
+    r0_one = r0;
+    const int row_base = cache_seq(p, b) * p.s_max + r0;
+    if (ring_a && p.fill_early) first_fills(row_base);
+    // Launched after mla_absorb_q with programmatic serialization: everything up
+    // to the query load (set-up, TMEM, the cache stream) overlaps that kernel.
+    const int len = clamp_length(p, pair ? b + 1 : b, tid == 0 && g == 0 && j == 0);
+    len_pair = len;
+    len_first = pair ? clamp_length(p, b, tid == 0 && g == 0 && j == 0) : len;
+    if (r0 >= len) {
+      // Chunk past the end of this sequence: nothing to do once early copies
+      // (into this CTA's shared memory) have landed.
+      if (ring_a && p.fill_early)
+        for (int pos = 0; pos < kSlotsA; ++pos) mbar_wait_bounded(bar(BAR_FULLA + pos), 0);
+      return;
+    }
+    if (ring_a && !p.fill_early) first_fills(row_base);
+    if (tid == 0) {
+      // The last tile may reach past the chunk into the next chunk's rows (finite
+      // cache data; their scores are masked) and past the sequence's end, where
+      // rows may hold anything (NaN included): those are zeroed before the PV.
+      const int r1 = min(r0 + p.chunk, len);
+      const int nt = (r1 - r0 + kTileRows - 1) / kTileRows;
+      SplitItem m;
+      m.row0 = row_base;
+      m.tiles = nt;
+      m.t0 = 0;
+      m.valid_last = r1 - (r0 + (nt - 1) * kTileRows);
+      m.zero_from = len - (r0 + (nt - 1) * kTileRows);
+      m.h0 = g * (pair ? kHeadGroup / 2 : kHeadGroup);
+      m.part = (b * p.H + m.h0) * p.splits + j;
+      m.qv = b;
+      items[0] = m;
+      counts[0] = 1;
+      counts[1] = nt;
+    }
   }
-  if (ring_a && !p.fill_early) first_fills();
-  const int r1 = min(r0 + p.chunk, len);
-  const int T = (r1 - r0 + kTileRows - 1) / kTileRows;
-  const int last_valid = r1 - (r0 + (T - 1) * kTileRows);   // rows of the last tile
-  // The last tile may reach past the chunk into the next chunk's rows (finite
-  // cache data; their scores are masked) and past the sequence's end, where
-  // rows may hold anything (NaN included): those are zeroed before the PV.
-  const int zero_from = len - (r0 + (T - 1) * kTileRows);
+  if (tid == 0) {
+    for (int i = 0; i < kSlotsB; ++i) {
+      mbar_init(bar(BAR_FULLB + i), 1);
+      mbar_init(bar(BAR_EMPTYB + i), 1);
+      mbar_init(bar(BAR_ZEROB + i), kSoftWarps);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(BAR_SFULL + i), 2);   // one commit per score issuer
+      mbar_init(bar(BAR_SFREE + i), kSoftWarps);
+      mbar_init(bar(BAR_PFULL + i), kSoftWarps);
+      mbar_init(bar(BAR_ODONE + i), 2);   // one commit per PV issuer
+      mbar_init(bar(BAR_ODRAIN + i), kSoftWarps);   // an O^T buffer's result has been read
+    }
+    mbar_init(bar(BAR_LASTA), 2);         // every score MMA has finished
+    for (int i = 0; i < 8; ++i) {
+      mbar_init(bar(BAR_FULLX + i), 1);   // the last tile's borrowed pairs: one use each
+      mbar_init(bar(BAR_ZEROX + i), kSoftWarps);
+    }
+    mbar_init(bar(BAR_ODONE2), 2);        // the score issuers' share of the last PV
+    mbar_init(bar(BAR_PVPREV), 2);        // the PV of tile T-2 has finished
+    mbar_init(bar(BAR_DONE), 4);          // every issuer's last commit
+    mbar_init(bar(BAR_QFREE), 2);         // an item's score MMAs are done with the query
+    mbar_init(bar(BAR_QREADY), kSoftWarps);   // the next item's query is in place
+    abort_flag[0] = 0;
+    abort_flag[1] = 0;
+    abort_flag[2] = 0;
+    s_issued[0] = 0;
+    s_issued[1] = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == kWarpA) {
+    __syncwarp();
+    tmem_alloc(smem_u32(slot_ptr), kTmemCols);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot_ptr;
+  const int n_items = counts[0];
+  const int T = counts[1];
+  const SplitItem fin = items[n_items - 1];   // the item of the CTA's last tile
+  const int fin_item = n_items - 1;
+  const int last_row = fin.row0 + (fin.tiles - 1) * kTileRows;
+  const int last_valid = fin.valid_last;
+  const int zero_from = fin.zero_from;
   const bool zero_last = zero_from < kTileRows;
-  const int h0 = g * (pair ? kHeadGroup / 2 : kHeadGroup);
+  const bool fin_first = T - 1 == fin.t0;     // the last tile is its item's first
+  // Item i accumulates into O^T buffer i % kOBufs.
+  auto obuf_col = [&](int i) { return kOCol + static_cast<uint32_t>(i % L::kOBufs) * kOBufCols; };
+  // Walks the items along the tile stream: item index, and its tiles' end.
+  struct Cursor {
+    int i, end;
+  };
+  constexpr bool kMulti = kPersist;   // the ordinary instance has one item per CTA
+  auto seek = [&](Cursor& c, int t) {
+    while (kMulti && t >= c.end) {
+      ++c.i;
+      c.end = items[c.i].t0 + items[c.i].tiles;
+    }
+  };
+  auto row_of = [&](const Cursor& c, int t) {
+    return items[c.i].row0 + (t - items[c.i].t0) * kTileRows;
+  };
+  // Whether item i (> 0) needs another query than item i - 1.
+  auto new_query = [&](int i) {
+    return items[i].qv != items[i - 1].qv || items[i].h0 != items[i - 1].h0;
+  };
+  // A tile before the last one that ends an item at its sequence's end: its
+  // ring-B pairs are zeroed past the end before the PV.
+  auto zero_mid = [&](const Cursor& c, int t) {
+    const SplitItem& it = items[c.i];
+    return kMulti && t != T - 1 && t == it.t0 + it.tiles - 1 && it.zero_from < kTileRows;
+  };
   // The last tile's latent pairs.  With T >= 2 all eight go to space that is free
   // once every score MMA has finished (ring-A slots 0-5, then the query area),
   // so none waits for ring B; with T == 1 pairs 0-3 use ring B from the start
@@ -292,53 +528,66 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
     return tail_res(k >> 1) ? kOffA + tail_slot(k) * kBoxBytes
                             : (k < 2 ? kOffQ : kOffB) + (k & 1) * kBoxBytes;
   };
-  if (tid == 0) {
-    for (int i = 0; i < kSlotsB; ++i) {
-      mbar_init(bar(BAR_FULLB + i), 1);
-      mbar_init(bar(BAR_EMPTYB + i), 1);
-      mbar_init(bar(BAR_ZEROB + i), kSoftWarps);
+
+  // Query rows of the score MMA's B operand (K-major, 128-byte swizzle, one 4 KB
+  // box per 64 columns): row n < kG is bf16(q) of head n, row kG + n is
+  // bf16(q - bf16(q)).  q_abs[v, h0..h0+kG-1, :] and q_pe[v, h0.., :] are
+  // contiguous; each softmax thread loads nine float4 before converting them.
+  auto load_query = [&](int v, int h0) {
+    const float4* qa = reinterpret_cast<const float4*>(static_cast<const float*>(p.q_abs) +
+                                                       (size_t(v) * p.H + h0) * kDc);
+    const float4* qp = reinterpret_cast<const float4*>(static_cast<const float*>(p.q_pe) +
+                                                       (size_t(v) * p.H + h0) * kDr);
+    constexpr int kNA = kHeadGroup * kDc / 4, kNQ = kNA + kHeadGroup * kDr / 4;
+    static_assert(kNQ == 9 * kSoftThreads, "nine float4 per softmax thread");
+    float4 q4[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      const int idx = tid + i * kSoftThreads;
+      if (pair) {
+        // column n: head h0 + n % 16 of query group v + n / 16
+        const int n = idx < kNA ? idx / (kDc / 4) : (idx - kNA) / (kDr / 4);
+        const size_t row = size_t(v + n / 16) * p.H + h0 + n % 16;
+        q4[i] = idx < kNA ? reinterpret_cast<const float4*>(static_cast<const float*>(p.q_abs) +
+                                                            row * kDc)[idx % (kDc / 4)]
+                          : reinterpret_cast<const float4*>(static_cast<const float*>(p.q_pe) +
+                                                            row * kDr)[(idx - kNA) % (kDr / 4)];
+      } else {
+        q4[i] = idx < kNA ? qa[idx] : qp[idx - kNA];
+      }
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar(BAR_SFULL + i), 2);   // one commit per score issuer
-      mbar_init(bar(BAR_SFREE + i), kSoftWarps);
-      mbar_init(bar(BAR_PFULL + i), kSoftWarps);
-      mbar_init(bar(BAR_ODONE + i), 2);   // one commit per PV issuer
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      const int idx = tid + i * kSoftThreads;
+      const int h = idx < kNA ? idx / (kDc / 4) : (idx - kNA) / (kDr / 4);
+      const int k = idx < kNA ? 4 * (idx % (kDc / 4)) : kDc + 4 * ((idx - kNA) % (kDr / 4));
+      uint2 hi, lo;
+      split_bf16(q4[i].x, q4[i].y, hi.x, lo.x);
+      split_bf16(q4[i].z, q4[i].w, hi.y, lo.y);
+      const int box = k >> 6, ch = (k & 63) >> 3, w = k & 7;
+      *reinterpret_cast<uint2*>(smem + kOffQ + box * kQBoxBytes + sw128(h, ch) + 2 * w) = hi;
+      *reinterpret_cast<uint2*>(smem + kOffQ + box * kQBoxBytes + sw128(h + kHeadGroup, ch) +
+                                2 * w) = lo;
     }
-    mbar_init(bar(BAR_LASTA), 2);         // every score MMA has finished
-    for (int i = 0; i < 8; ++i) {
-      mbar_init(bar(BAR_FULLX + i), 1);   // the last tile's borrowed pairs: one use each
-      mbar_init(bar(BAR_ZEROX + i), kSoftWarps);
-    }
-    mbar_init(bar(BAR_ODONE2), 2);        // the score issuers' share of the last PV
-    mbar_init(bar(BAR_PVPREV), 2);        // the PV of tile T-2 has finished
-    mbar_init(bar(BAR_DONE), 4);          // every issuer's last commit
-    *abort_flag = 0;
-    s_issued[0] = 0;
-    s_issued[1] = 0;
-    fence_mbarrier_init();
-  }
-  if (warp == kWarpA) {
-    __syncwarp();
-    tmem_alloc(smem_u32(slot_ptr), kTmemCols);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *slot_ptr;
+    fence_proxy_async_smem();
+  };
 
   if (warp == kWarpA) {
     // ------------------------------------------------------------ ring A (HBM)
     if (lane == 0) {
       int issued = kSlotsA;   // stream positions issued so far (the first fills included)
+      Cursor c{0, items[0].tiles};
       for (int t = 0; t < T && !*abort_flag; ++t) {
         if (p.stop_after_tiles > 0 && t >= p.stop_after_tiles) break;   // test hook
+        seek(c, t);
+        const int row = row_of(c, t);
         for (int k = 0; k < 9; ++k) {
           const int pos = 9 * t + k, sl = pos % kSlotsA, use = pos / kSlotsA;
           if (pos < kSlotsA) continue;   // issued before the CTA-wide barrier
           if (use > 0 && !wait_or_abort(bar(BAR_EMPTYA + sl), (use - 1) & 1, abort_flag, wait_ns)) break;
           mbar_arrive_expect_tx(bar(BAR_FULLA + sl), kBoxBytes);
-          tma_load_2d(sbase + kOffA + sl * kBoxBytes, &tmap, 64 * box_at(t, k),
-                      row_base + t * kTileRows, bar(BAR_FULLA + sl), keep);
+          tma_load_2d(sbase + kOffA + sl * kBoxBytes, &tmap, 64 * box_at(t, k), row,
+                      bar(BAR_FULLA + sl), keep);
           issued = pos + 1;
         }
       }
@@ -355,7 +604,9 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
       const uint64_t stream = l2_evict_first_policy();
       int issued = 0;          // ring-B positions issued (8 per tile)
       uint32_t armed_x = 0;    // single-use barriers BAR_FULLX + k armed
+      Cursor c{0, items[0].tiles};
       for (int t = 0; t < T && !*abort_flag; ++t) {
+        seek(c, t);
         if (kResidentTail && t == T - 1) {
           // The last tile's boxes that left ring A: block 0's into the query
           // area once every score MMA has finished, a second block's into the
@@ -369,8 +620,8 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
               second = true;
             }
             mbar_arrive_expect_tx(bar(BAR_FULLX + k), kBoxBytes);
-            tma_load_2d(sbase + tail_box_off(k), &tmap, 64 * k, row_base + t * kTileRows,
-                        bar(BAR_FULLX + k), stream);
+            tma_load_2d(sbase + tail_box_off(k), &tmap, 64 * k, last_row, bar(BAR_FULLX + k),
+                        stream);
             armed_x |= 1u << k;
           }
           break;
@@ -380,13 +631,18 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
         if (t > 0 && !(t == T - 1 && T >= 2)) {
           const unsigned long long t0 = globaltimer_ns();
           while ((s_issued[0] <= t || s_issued[1] <= t) && !*abort_flag)
-            if (globaltimer_ns() - t0 > wait_ns) *abort_flag = 1;
+            if (globaltimer_ns() - t0 > wait_ns) {
+              abort_flag[1] = static_cast<int>(bars) - 8;   // no barrier: index -1
+              abort_flag[2] = (t & 0xFF) | (tid << 8);
+              *abort_flag = 1;
+            }
         }
         // Unit u holds O^T block mb = u % 4 (ring slot mb) for row half u / 4.
         bool lasta = false;
+        const int trow = row_of(c, t);
         for (int u = 0; u < 8 && !*abort_flag; ++u) {
           const int mb = u & 3, kh = u >> 2;
-          const int row = row_base + t * kTileRows + 64 * kh;
+          const int row = trow + 64 * kh;
           if (borrowed(t, u)) {
             const int x = borrow_x(u);
             if (!lasta && !wait_or_abort(bar(BAR_LASTA), 0, abort_flag, wait_ns)) break;
@@ -419,57 +675,21 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
       }
     }
   } else if (warp < kSoftWarps || warp == kWarpS0 || warp == kWarpS1) {
+    // The first item's query.  It comes from the previous kernel of the stream
+    // (mla_absorb_q).
     if (warp < kSoftWarps) {
-      // Query rows of the score MMA's B operand (K-major, 128-byte swizzle, one
-      // 4 KB box per 64 columns): row n < 16 is bf16(q) of head n, row 16 + n
-      // is bf16(q - bf16(q)).  q_abs[b, h0..h0+15, :] and q_pe[b, h0..h0+15, :]
-      // are contiguous; each thread loads nine float4 before converting them.
-      // They come from the previous kernel of the stream (mla_absorb_q).
       pdl_wait();
-      const float4* qa = reinterpret_cast<const float4*>(static_cast<const float*>(p.q_abs) +
-                                                         (size_t(b) * p.H + h0) * kDc);
-      const float4* qp = reinterpret_cast<const float4*>(static_cast<const float*>(p.q_pe) +
-                                                         (size_t(b) * p.H + h0) * kDr);
-      constexpr int kNA = kHeadGroup * kDc / 4, kNQ = kNA + kHeadGroup * kDr / 4;
-      static_assert(kNQ == 9 * kSoftThreads, "nine float4 per softmax thread");
-      float4 v[9];
-#pragma unroll
-      for (int i = 0; i < 9; ++i) {
-        const int idx = tid + i * kSoftThreads;
-        if (pair) {
-          // column n: head h0 + n % 16 of query group b + n / 16
-          const int n = idx < kNA ? idx / (kDc / 4) : (idx - kNA) / (kDr / 4);
-          const size_t row = size_t(b + n / 16) * p.H + h0 + n % 16;
-          v[i] = idx < kNA ? reinterpret_cast<const float4*>(static_cast<const float*>(p.q_abs) +
-                                                             row * kDc)[idx % (kDc / 4)]
-                           : reinterpret_cast<const float4*>(static_cast<const float*>(p.q_pe) +
-                                                             row * kDr)[(idx - kNA) % (kDr / 4)];
-        } else {
-          v[i] = idx < kNA ? qa[idx] : qp[idx - kNA];
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < 9; ++i) {
-        const int idx = tid + i * kSoftThreads;
-        const int h = idx < kNA ? idx / (kDc / 4) : (idx - kNA) / (kDr / 4);
-        const int k = idx < kNA ? 4 * (idx % (kDc / 4)) : kDc + 4 * ((idx - kNA) % (kDr / 4));
-        uint2 hi, lo;
-        split_bf16(v[i].x, v[i].y, hi.x, lo.x);
-        split_bf16(v[i].z, v[i].w, hi.y, lo.y);
-        const int box = k >> 6, ch = (k & 63) >> 3, w = k & 7;
-        *reinterpret_cast<uint2*>(smem + kOffQ + box * kQBoxBytes + sw128(h, ch) + 2 * w) = hi;
-        *reinterpret_cast<uint2*>(smem + kOffQ + box * kQBoxBytes + sw128(h + kHeadGroup, ch) +
-                                  2 * w) = lo;
-      }
-      fence_proxy_async_smem();
+      load_query(items[0].qv, items[0].h0);
     }
-    named_bar_sync(2, kSoftThreads + 64);   // warps 0-7, 9, 11: the query is in place
+    named_bar_sync(2, kSoftThreads + 64);   // softmax warps and score issuers: query in place
   }
 
-  // One PV unit: O^T block u % 4 += C^T (pair u of tile t) . P^T (row half u / 4);
-  // four MMAs.  false if a wait gave up.
+  // One PV unit: O^T block u % 4 (of the O^T buffer at column ocol) += C^T (pair
+  // u of tile t) . P^T (row half u / 4); four MMAs; `fresh`: the tile is its
+  // item's first (the block starts from zero); `zmid`: a tile before the last
+  // whose pairs are zeroed past the sequence's end first.  false if a wait gave up.
   constexpr uint32_t idesc_o = umma_idesc_bf16(128, kQN, 1, 0);
-  auto pv_unit = [&](int t, int u) -> bool {
+  auto pv_unit = [&](int t, int u, bool fresh, uint32_t ocol, bool zmid) -> bool {
     const int mb = u & 3, kh = u >> 2;
     if (kResidentTail && t == T - 1) {
       // Block mb's two 64-column boxes 2mb, 2mb + 1 (128 rows each, kBoxBytes
@@ -488,8 +708,8 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
                           static_cast<uint64_t>(((t % kPBufs) * kPBytes + kh * kPSub) >> 4);
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(tmem + kOCol + kQN * mb, c + ((ks * 2048) >> 4), pd + ((ks * 32) >> 4), idesc_o,
-                  (t > 0 || kh > 0 || ks > 0) ? 1u : 0u);
+        umma_bf16(tmem + ocol + kQN * mb, c + ((ks * 2048) >> 4), pd + ((ks * 32) >> 4), idesc_o,
+                  (!fresh || kh > 0 || ks > 0) ? 1u : 0u);
       return true;
     }
     const int pos = 8 * t + u, sl = pos % kSlotsB;
@@ -498,6 +718,9 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
     if (t == T - 1 && zero_last &&
         !wait_or_abort(bw ? bar(BAR_ZEROX + x) : bar(BAR_ZEROB + sl), 0, abort_flag, wait_ns))
       return false;
+    // A zeroed tile before the last zeroes each slot twice (units u and u + 4),
+    // so the zeroing of unit u completes the phase of parity u / 4.
+    if (zmid && !wait_or_abort(bar(BAR_ZEROB + sl), kh, abort_flag, wait_ns)) return false;
     if (!wait_or_abort(bw ? bar(BAR_FULLX + x) : bar(BAR_FULLB + sl), bw ? 0 : (pos / kSlotsB) & 1,
                        abort_flag, wait_ns))
       return false;
@@ -510,10 +733,16 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
                         static_cast<uint64_t>(((t % kPBufs) * kPBytes + kh * kPSub) >> 4);
 #pragma unroll
     for (int ks = 0; ks < 4; ++ks)
-      umma_bf16(tmem + kOCol + kQN * mb, c + ((ks * 2048) >> 4), pd + ((ks * 32) >> 4), idesc_o,
-                (t > 0 || kh > 0 || ks > 0) ? 1u : 0u);
+      umma_bf16(tmem + ocol + kQN * mb, c + ((ks * 2048) >> 4), pd + ((ks * 32) >> 4), idesc_o,
+                (!fresh || kh > 0 || ks > 0) ? 1u : 0u);
     if (!bw) umma_commit(bar(BAR_EMPTYB + sl));
     return true;
+  };
+  // Before item i's first PV: the epilogue of item i - kOBufs has read the O^T
+  // buffer item i accumulates into.
+  auto wait_drain = [&](int i) {
+    return i < L::kOBufs || wait_or_abort(bar(BAR_ODRAIN + i % L::kOBufs),
+                                          ((i - L::kOBufs) / L::kOBufs) & 1, abort_flag, wait_ns);
   };
 
   if (warp == kWarpS0 || warp == kWarpS1) {
@@ -531,7 +760,17 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
       const uint64_t dA0 = umma_desc_sw128(sbase + kOffA, 16, 1024);     // K-major box
       const uint64_t dQ0 = umma_desc_sw128(sbase + kOffQ, 16, 1024);     // Q hi|lo
       const uint32_t dS = tmem + kS1Col * i;
+      Cursor c{0, items[0].tiles};
+      int qk = 0;   // query changes so far
       for (int t = 0; t < T; ++t) {
+        seek(c, t);
+        if (kMulti && __builtin_expect(c.i > 0 && t == items[c.i].t0 && new_query(c.i), 0)) {
+          // The previous item's score MMAs release the query area; the softmax
+          // warps fill it with this item's query.
+          umma_commit(bar(BAR_QFREE));
+          if (!wait_or_abort(bar(BAR_QREADY), qk & 1, abort_flag, wait_ns)) break;
+          ++qk;
+        }
         const int sb = t & 1;
         if (t >= 2 && !wait_or_abort(bar(BAR_SFREE + sb), ((t - 2) >> 1) & 1, abort_flag, wait_ns)) break;
         bool ok = true, first = true;
@@ -563,8 +802,10 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
         const int t = T - 1;
         bool ok = !*abort_flag;
         if (ok && T >= 2 && !wait_or_abort(bar(BAR_PVPREV), 0, abort_flag, wait_ns)) ok = false;
+        if (ok && fin_first && !wait_drain(fin_item)) ok = false;
         if (ok && !wait_or_abort(bar(BAR_PFULL + (t & 1)), (t >> 1) & 1, abort_flag, wait_ns)) ok = false;
-        if (ok && pv_unit(t, 2 + i)) pv_unit(t, 6 + i);
+        if (ok && pv_unit(t, 2 + i, fin_first, obuf_col(fin_item), false))
+          pv_unit(t, 6 + i, fin_first, obuf_col(fin_item), false);
         umma_commit(bar(BAR_ODONE2));
       }
       // Every MMA this thread issued has finished before TMEM is released.
@@ -577,11 +818,16 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
     // the last tile only block i (the score issuers take blocks 2 and 3).
     if (lane == 0) {
       const int i = warp - kWarpPV0;
+      Cursor c{0, items[0].tiles};
       for (int t = 0; t < T; ++t) {
+        seek(c, t);
+        const bool fresh = t == items[c.i].t0;
+        if (fresh && !wait_drain(c.i)) break;
         if (!wait_or_abort(bar(BAR_PFULL + (t & 1)), (t >> 1) & 1, abort_flag, wait_ns)) break;
         bool ok = true;
         const int step = t == T - 1 ? 4 : 2;
-        for (int u = i; u < 8 && ok; u += step) ok = pv_unit(t, u);
+        const bool zmid = zero_mid(c, t);
+        for (int u = i; u < 8 && ok; u += step) ok = pv_unit(t, u, fresh, obuf_col(c.i), zmid);
         if (!ok) break;
         umma_commit(bar(BAR_ODONE + (t & 1)));
         if (t == T - 2) umma_commit(bar(BAR_PVPREV));
@@ -601,12 +847,87 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
       m[h] = -INFINITY;
       l[h] = 0.f;
     }
+    // An item's result: its row sums and maxima (m, l), once its last PV
+    // (tile t_end) has finished; O^T buffer at column ocol.
+    auto finish_item = [&](int idx, int t_end, const float* mm, const float* ll, bool last) {
+      const SplitItem it = items[idx];
+      const uint32_t ocol = obuf_col(idx);
+      {
+        float tt[kHalfHeads];
+#pragma unroll
+        for (int h = 0; h < kHalfHeads; ++h) tt[h] = ll[h];
+        const float ws = reduce8_heads<false>(tt, lane);
+        if (lane < 16 && (lane & 1) == 0) lsum[(hb + (lane >> 1)) * 4 + wq] = ws;
+      }
+      // O^T after the item's last PV: this thread's latent row is d = 128 mb + 32 wq + lane.
+      wait_or_abort(bar(BAR_ODONE + (t_end & 1)), (t_end >> 1) & 1, abort_flag, wait_ns);
+      if (last) wait_or_abort(bar(BAR_ODONE2), 0, abort_flag, wait_ns);
+      tc_fence_after();
+      named_bar_sync(1, kSoftThreads);
+      if (!*abort_flag) {
+        // Row (v, h, j) of the partials; heads h0 + hw + h are p.splits rows apart
+        // (paired tokens: groups 2 and 3 belong to query group v + 1).
+        const size_t base = size_t(it.part) + (pair ? size_t(gp >> 1) * p.H * p.splits : 0);
+        const int hw = pair ? kHalfHeads * (gp & 1) : hb;
+        // 1/L by the approximate reciprocal (within 2 ulp for the L > 0 reached
+        // here, 1 <= L <= 2^8 x rows): a branch-free instruction, where eight
+        // IEEE divisions in a row cost about 0.4 us of the CTA's critical path.
+        // Lane h of the first warp of each group writes head h's log-sum-exp.
+        float inv[kHalfHeads], Lme = 0.f, mme = 0.f;
+#pragma unroll
+        for (int h = 0; h < kHalfHeads; ++h) {
+          const float4 q4 = *reinterpret_cast<const float4*>(lsum + (hb + h) * 4);
+          const float Ls = (q4.x + q4.y) + (q4.z + q4.w);
+          inv[h] = Ls > 0.f ? __fdividef(1.f, Ls) : 0.f;
+          Lme = lane == h ? Ls : Lme;
+          mme = lane == h ? mm[h] : mme;
+        }
+        if (wq == 0 && lane < kHalfHeads)
+          p.part_lse[base + size_t(hw + lane) * p.splits] =
+              Lme > 0.f ? (mme + log2f(Lme)) * kLn2 : -INFINITY;
+        uint32_t hi4[4][8], lo4[4][8];
+#pragma unroll
+        for (int mb = 0; mb < 4; ++mb) {
+          tmem_ld8_nowait(tmem + lane_base + ocol + kQN * mb + hb, hi4[mb]);
+          tmem_ld8_nowait(tmem + lane_base + ocol + kQN * mb + kHeadGroup + hb, lo4[mb]);
+        }
+        tmem_wait_ld();
+        float* orow = p.part_o + (base + size_t(hw) * p.splits) * kDc + 32 * wq + lane;
+        const size_t head_stride = size_t(p.splits) * kDc;
+#pragma unroll
+        for (int h = 0; h < kHalfHeads; ++h, orow += head_stride)
+#pragma unroll
+          for (int mb = 0; mb < 4; ++mb)
+            orow[128 * mb] = (__uint_as_float(hi4[mb][h]) + __uint_as_float(lo4[mb][h])) * inv[h];
+      }
+      if (!last) {
+        // The O^T buffer may take a later item now.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(BAR_ODRAIN + idx % L::kOBufs));
+      }
+    };
+    Cursor c{0, items[0].tiles};
+    int qk = 0;                  // query changes so far
+    int pend = -1, pend_t = 0;   // item whose partial is still to be written, its last tile
+    float mp[kHalfHeads], lp[kHalfHeads];
     for (int t = 0; t < T; ++t) {
+      seek(c, t);
+      const SplitItem it = items[c.i];
+      const bool first_t = t == it.t0, last_t = t == it.t0 + it.tiles - 1;
       const int sb = t & 1;
-      int valid = t == T - 1 ? last_valid : kTileRows;
-      if (pair)   // this group's token ends at its own length
-        valid = min(max(min(r0 + p.chunk, gp < 2 ? len_first : len) - (r0 + t * kTileRows), 0),
+      int valid = last_t ? it.valid_last : kTileRows;
+      if (pair)   // this group's token ends at its own length (one item: tile t of chunk r0)
+        valid = min(max(min(r0_one + p.chunk, gp < 2 ? len_first : len_pair) -
+                            (r0_one + t * kTileRows), 0),
                     kTileRows);
+      if (kMulti && first_t && t > 0) {
+#pragma unroll
+        for (int h = 0; h < kHalfHeads; ++h) {
+          m[h] = -INFINITY;
+          l[h] = 0.f;
+        }
+      }
       wait_or_abort(bar(BAR_SFULL + sb), (t >> 1) & 1, abort_flag, wait_ns);
       tc_fence_after();
       float sc[kHalfHeads], tt[kHalfHeads];
@@ -643,7 +964,8 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
       }
       if (need) {
         // Move this group's reference maxima; rescale its row sums and the O^T
-        // columns it owns (in TMEM, after the previous PV finished).
+        // columns it owns (in TMEM, after the previous PV finished).  The first
+        // tile of an item starts from nothing (its first PV overwrites).
         float alpha[kHalfHeads];
 #pragma unroll
         for (int h = 0; h < kHalfHeads; ++h) {
@@ -652,14 +974,15 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
           m[h] = mn;
           l[h] *= alpha[h];
         }
-        if (t > 0) {
+        if (!first_t) {
           wait_or_abort(bar(BAR_ODONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag, wait_ns);
           tc_fence_after();
+          const uint32_t ocol = obuf_col(c.i);
 #pragma unroll
           for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-              const uint32_t col = kOCol + kQN * mb + kHeadGroup * half + hb;
+              const uint32_t col = ocol + kQN * mb + kHeadGroup * half + hb;
               uint32_t r[8];
               float o[8];
               tmem_ld8_nowait(tmem + lane_base + col, r);
@@ -713,8 +1036,8 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
           for (int k = 0; k < 8; ++k) {
             if (!tail_res(k >> 1)) wait_or_abort(bar(BAR_FULLX + k), 0, abort_flag, wait_ns);
             uint8_t* box = smem + tail_box_off(k) + zero_from * 128;
-            for (int c = tid; c < nrow * 8; c += kSoftThreads)
-              *reinterpret_cast<uint4*>(box + c * 16) = make_uint4(0, 0, 0, 0);
+            for (int q = tid; q < nrow * 8; q += kSoftThreads)
+              *reinterpret_cast<uint4*>(box + q * 16) = make_uint4(0, 0, 0, 0);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(BAR_ZEROX + k));
@@ -729,70 +1052,73 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
           const int x = bw ? borrow_x(u) : 0;
           wait_or_abort(bw ? bar(BAR_FULLX + x) : bar(BAR_FULLB + sl), bw ? 0 : (pos / kSlotsB) & 1,
                         abort_flag, wait_ns);
-          uint8_t* pair = smem + (bw ? borrow_off(x) : kOffB + 2 * sl * kHalfBox);
-          for (int c = tid; c < 2 * nrow * 8; c += kSoftThreads) {
-            const int h = c / (nrow * 8), rem = c % (nrow * 8);
-            *reinterpret_cast<uint4*>(pair + h * kHalfBox + (first + rem / 8) * 128 + (rem % 8) * 16) =
+          uint8_t* pr = smem + (bw ? borrow_off(x) : kOffB + 2 * sl * kHalfBox);
+          for (int q = tid; q < 2 * nrow * 8; q += kSoftThreads) {
+            const int h = q / (nrow * 8), rem = q % (nrow * 8);
+            *reinterpret_cast<uint4*>(pr + h * kHalfBox + (first + rem / 8) * 128 + (rem % 8) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(bw ? bar(BAR_ZEROX + x) : bar(BAR_ZEROB + sl));
         }
+      } else if (__builtin_expect(zero_mid(c, t), 0)) {
+        // A tile before the last that ends its item at the sequence's end: the
+        // same zeroing on its ring-B pairs (one phase of the slot's barrier per
+        // pair, two pairs per slot).
+        // Its slots' previous uses belong to tile t - 1: once that tile's PV has
+        // finished, each slot's full barrier is at most one phase short of
+        // this tile's pair, so the parity waits below cannot pass on an older
+        // phase (the PV issuers, not this role, consume the ring in order).
+        const int zf = it.zero_from;
+        if (t > 0)
+          wait_or_abort(bar(BAR_ODONE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag, wait_ns);
+        for (int u = 0; u < 8; ++u) {
+          const int kh = u >> 2;
+          const int first = max(0, zf - 64 * kh);
+          const int nrow = 64 - first;
+          const int pos = 8 * t + u, sl = pos % kSlotsB;
+          wait_or_abort(bar(BAR_FULLB + sl), (pos / kSlotsB) & 1, abort_flag, wait_ns);
+          uint8_t* pr = smem + kOffB + 2 * sl * kHalfBox;
+          for (int q = tid; q < 2 * nrow * 8; q += kSoftThreads) {
+            const int h = q / (nrow * 8), rem = q % (nrow * 8);
+            *reinterpret_cast<uint4*>(pr + h * kHalfBox + (first + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(BAR_ZEROB + sl));
+        }
+      }
+      // The previous item's partial, one tile late: its last PV has had this
+      // tile's softmax to finish.
+      if (kMulti && pend >= 0) {
+        finish_item(pend, pend_t, mp, lp, false);
+        pend = -1;
+      }
+      if (kMulti && last_t && t != T - 1) {
+        // The next item's query, once this item's score MMAs are done with the
+        // query area (the score issuers wait for it).
+        if (__builtin_expect(new_query(c.i + 1), 0)) {
+          wait_or_abort(bar(BAR_QFREE), qk & 1, abort_flag, wait_ns);
+          load_query(items[c.i + 1].qv, items[c.i + 1].h0);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar(BAR_QREADY));
+          ++qk;
+        }
+        pend = c.i;
+        pend_t = t;
+#pragma unroll
+        for (int h = 0; h < kHalfHeads; ++h) {
+          mp[h] = m[h];
+          lp[h] = l[h];
+        }
       }
     }
     // The combine may start launching: it waits for this grid anyway, and a
     // dependent that starts much earlier only sleeps longer.
     if (tid == 0) pdl_launch_dependents();
-    // Softmax denominators over the chunk's rows.
-    {
-      float tt[kHalfHeads];
-#pragma unroll
-      for (int h = 0; h < kHalfHeads; ++h) tt[h] = l[h];
-      const float ws = reduce8_heads<false>(tt, lane);
-      if (lane < 16 && (lane & 1) == 0) lsum[(hb + (lane >> 1)) * 4 + wq] = ws;
-    }
-    // O^T after the last PV: this thread's latent row is d = 128 mb + 32 wq + lane.
-    wait_or_abort(bar(BAR_ODONE + ((T - 1) & 1)), ((T - 1) >> 1) & 1, abort_flag, wait_ns);
-    wait_or_abort(bar(BAR_ODONE2), 0, abort_flag, wait_ns);
-    tc_fence_after();
-    named_bar_sync(1, kSoftThreads);
-    if (!*abort_flag) {
-      // Row (b, h, j) of the partials; heads h0 + hw + h are p.splits rows apart
-      // (paired tokens: groups 2 and 3 belong to query group b + 1).
-      const size_t base = (size_t(pair ? b + (gp >> 1) : b) * p.H + h0) * p.splits + j;
-      const int hw = pair ? kHalfHeads * (gp & 1) : hb;
-      // 1/L by the approximate reciprocal (within 2 ulp for the L > 0 reached
-      // here, 1 <= L <= 2^8 x rows): a branch-free instruction, where eight
-      // IEEE divisions in a row cost about 0.4 us of the CTA's critical path.
-      // Lane h of the first warp of each group writes head h's log-sum-exp.
-      float inv[kHalfHeads], Lme = 0.f, mme = 0.f;
-#pragma unroll
-      for (int h = 0; h < kHalfHeads; ++h) {
-        const float4 q4 = *reinterpret_cast<const float4*>(lsum + (hb + h) * 4);
-        const float L = (q4.x + q4.y) + (q4.z + q4.w);
-        inv[h] = L > 0.f ? __fdividef(1.f, L) : 0.f;
-        Lme = lane == h ? L : Lme;
-        mme = lane == h ? m[h] : mme;
-      }
-      if (wq == 0 && lane < kHalfHeads)
-        p.part_lse[base + size_t(hw + lane) * p.splits] =
-            Lme > 0.f ? (mme + log2f(Lme)) * kLn2 : -INFINITY;
-      uint32_t hi4[4][8], lo4[4][8];
-#pragma unroll
-      for (int mb = 0; mb < 4; ++mb) {
-        tmem_ld8_nowait(tmem + lane_base + kOCol + kQN * mb + hb, hi4[mb]);
-        tmem_ld8_nowait(tmem + lane_base + kOCol + kQN * mb + kHeadGroup + hb, lo4[mb]);
-      }
-      tmem_wait_ld();
-      float* row = p.part_o + (base + size_t(hw) * p.splits) * kDc + 32 * wq + lane;
-      const size_t head_stride = size_t(p.splits) * kDc;
-#pragma unroll
-      for (int h = 0; h < kHalfHeads; ++h, row += head_stride)
-#pragma unroll
-        for (int mb = 0; mb < 4; ++mb)
-          row[128 * mb] = (__uint_as_float(hi4[mb][h]) + __uint_as_float(lo4[mb][h])) * inv[h];
-    }
+    finish_item(fin_item, T - 1, m, l, true);
   }
 
   tc_fence_before();
@@ -801,7 +1127,23 @@ __global__ void __launch_bounds__(TcPlan<kG>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
-  if (tid == 0 && *abort_flag) report(p.status, MLA_DEV_PIPELINE_TIMEOUT);
+  if (tid == 0 && *abort_flag) {
+    report(p.status, MLA_DEV_PIPELINE_TIMEOUT);
+    if (p.debug) {   // test hook: where this CTA's first wait gave up
+      const int k = atomicAdd(p.debug, 1);
+      if (k < 256) {
+        int* r = p.debug + 1 + 8 * k;
+        r[0] = static_cast<int>(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+        r[1] = (abort_flag[1] - static_cast<int>(bars)) / 8;   // barrier index
+        r[2] = abort_flag[2] & 0xFF;                            // parity
+        r[3] = abort_flag[2] >> 8;                              // thread
+        r[4] = n_items;
+        r[5] = T;
+        r[6] = s_issued[0];
+        r[7] = s_issued[1];
+      }
+    }
+  }
 }
 
 // fp32 path: one CTA per (head, chunk, sequence); each warp runs its own online
@@ -935,6 +1277,113 @@ __global__ void __launch_bounds__(32)
   if (tid == 0 && lse_out) lse_out[size_t(b) * p.H + h] = m + logf(sum);
 }
 
+// The same merge for many chunks (more than 16): grid (H, B, 4), CTA z owns
+// latent columns [128z, 128z + 128), lane t the float4 at 128z + 4t.  The CTA's
+// W warps share the chunks (warp w takes chunks
+// w, w + W, ...); each keeps up to kCombineChunk chunks' loads in flight and a
+// running maximum that keeps the weights finite, and the W warp states are then
+// merged through shared memory.  W grows with the chunk count (combine_warps),
+// so that many chunks are not read one group after another by a single warp.
+constexpr int kCombineMaxWarps = 8;
+// The warp states are merged in dynamic shared memory (W > 1 only), so that a
+// one-warp CTA needs none and fits beside a split CTA, launching early.
+__global__ void __launch_bounds__(32 * kCombineMaxWarps)
+    combine_warps_kernel(const SplitParams p, float* o_c, float* lse_out) {
+  extern __shared__ float4 s_acc[];   // [W][32], then s_m[W], s_sum[W]
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int W = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col = blockIdx.z * 32 + lane;      // float4 column of the 512
+  const int len = clamp_length(p, b, false);   // a caller input, not the split's output
+  pdl_wait();   // the partials come from the split kernel just before
+  const int nsplit = (len + p.chunk - 1) / p.chunk;
+  float* out = o_c + (size_t(b) * p.H + h) * kDc;
+  if (nsplit == 0) {
+    if (warp == 0) {
+      reinterpret_cast<float4*>(out)[col] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (col == 0 && lse_out) lse_out[size_t(b) * p.H + h] = -INFINITY;
+    }
+    if (threadIdx.x == 0) pdl_launch_dependents();
+    return;
+  }
+  const size_t row0 = (size_t(b) * p.H + h) * p.splits;   // this (b, h)'s chunks, contiguous
+  const float* lse_bh = p.part_lse + row0;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + row0 * kDc) + col;
+  float m = -INFINITY, sum = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = warp; s0 < nsplit; s0 += W * kCombineChunk) {
+    float ls[kCombineChunk];
+    float4 v[kCombineChunk];
+#pragma unroll
+    for (int u = 0; u < kCombineChunk; ++u) {
+      const int sj = s0 + W * u;
+      const bool ok = sj < nsplit;
+      ls[u] = ok ? lse_bh[sj] : -INFINITY;
+      v[u] = ok ? po[size_t(sj) * (kDc / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (s0 + W * kCombineChunk >= nsplit && threadIdx.x == 0) pdl_launch_dependents();
+    float cm = m;
+#pragma unroll
+    for (int u = 0; u < kCombineChunk; ++u) cm = fmaxf(cm, ls[u]);
+    // cm is finite: every chunk with rows has a finite lse, and s0 < nsplit.
+    const float r = m == -INFINITY ? 0.f : expf(m - cm);
+    sum *= r;
+    acc.x *= r;
+    acc.y *= r;
+    acc.z *= r;
+    acc.w *= r;
+#pragma unroll
+    for (int u = 0; u < kCombineChunk; ++u) {
+      const float w = s0 + W * u < nsplit ? expf(ls[u] - cm) : 0.f;
+      sum += w;
+      acc.x = fmaf(w, v[u].x, acc.x);
+      acc.y = fmaf(w, v[u].y, acc.y);
+      acc.z = fmaf(w, v[u].z, acc.z);
+      acc.w = fmaf(w, v[u].w, acc.w);
+    }
+    m = cm;
+  }
+  if (W > 1) {
+    // Merge the warps' states (a warp without chunks has m = -inf, sum = 0).
+    float* s_m = reinterpret_cast<float*>(s_acc + 32 * W);
+    float* s_sum = s_m + W;
+    s_acc[32 * warp + lane] = acc;
+    if (lane == 0) {
+      s_m[warp] = m;
+      s_sum[warp] = sum;
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    float M = -INFINITY;
+    for (int w = 0; w < W; ++w) M = fmaxf(M, s_m[w]);
+    sum = 0.f;
+    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int w = 0; w < W; ++w) {
+      const float f = s_m[w] == -INFINITY ? 0.f : expf(s_m[w] - M);
+      const float4 a4 = s_acc[32 * w + lane];
+      sum = fmaf(f, s_sum[w], sum);
+      acc.x = fmaf(f, a4.x, acc.x);
+      acc.y = fmaf(f, a4.y, acc.y);
+      acc.z = fmaf(f, a4.z, acc.z);
+      acc.w = fmaf(f, a4.w, acc.w);
+    }
+    m = M;
+  }
+  const float inv = 1.f / sum;
+  reinterpret_cast<float4*>(out)[col] = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+  if (col == 0 && lse_out) lse_out[size_t(b) * p.H + h] = m + logf(sum);
+}
+
+// Warps per combine CTA for `splits` chunks: one up to 64 chunks (combine_kernel:
+// few enough registers that many of its CTAs run at once, and launch beside the
+// split's), then more (combine_warps_kernel), so that a warp takes at most about
+// 16 chunks (128 chunks: 6.8 us against 7.9 for one warp per CTA).
+int combine_warps(int splits) {
+  if (splits <= 64) return 1;   // measured: 22 chunks over two warps 12.7 us against 5.8
+  int w = 1;
+  while (w < kCombineMaxWarps && splits > 16 * w) w *= 2;
+  return w;
+}
+
 // Combine and value up-projection in one launch (bf16 weights), for the whole
 // decode step:
 //   o_c[b,h,:] = sum_j exp(lse_j - L) o_j     (as combine_kernel)
@@ -1055,77 +1504,153 @@ bool pair_tokens(const mla_dims* cache_dims, int q_len) {
   return cache_dims->dtype == MLA_BF16 && cache_dims->heads % 32 != 0 && q_len % 2 == 0;
 }
 
-template <int kG>
+template <int kG, bool kPersist>
 mla_status launch_split_tc(const CUtensorMap& tmap, const CUtensorMap& tmap_half,
                            const SplitParams& p, int heads, cudaStream_t s, const char* who) {
-  using L = TcPlan<kG>;
+  using L = TcPlan<kG, kPersist>;
   static DeviceFlags attr_done;
   const int dev = current_device();
   if (!attr_done.test(dev)) {
-    if (cudaFuncSetAttribute(split_tc_kernel<kG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(split_tc_kernel<kG, kPersist>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(L::kSmem)) != cudaSuccess) {
       set_error("%s: cannot reserve %zu bytes of shared memory", who, L::kSmem);
       return MLA_ERR_CUDA;
     }
     attr_done.set(dev);
   }
-  // Paired tokens: 16-head slices, two query groups per CTA.
-  const dim3 grid(p.tpc == 2 ? heads / 16 : heads / kG, p.splits, p.tpc == 2 ? p.B / 2 : p.B);
-  // A CTA whose chunk lies past its sequence's end would fetch its first boxes
-  // for nothing; that costs little in a one-wave grid, but in several waves it
-  // delays the CTAs behind it (measured: 64 ragged sequences, split 67.9 ->
-  // 70.4 us with the early fetch everywhere).
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
     cudaGetLastError();
     sms = 0;
   }
+  // Paired tokens: 16-head slices, two query groups per CTA.  A persistent grid
+  // has one CTA per SM.
+  const dim3 grid = p.persist ? dim3(sms > 0 ? sms : 1)
+                              : dim3(p.tpc == 2 ? heads / 16 : heads / kG, p.splits,
+                                     p.tpc == 2 ? p.B / 2 : p.B);
+  // A CTA whose chunk lies past its sequence's end would fetch its first boxes
+  // for nothing; that costs little in a one-wave grid, but in several waves it
+  // delays the CTAs behind it (measured: 64 ragged sequences, split 67.9 ->
+  // 70.4 us with the early fetch everywhere).
   SplitParams q = p;
-  q.fill_early = static_cast<long long>(grid.x) * grid.y * grid.z <= sms;
-  launch_pdl(split_tc_kernel<kG>, grid, dim3(L::kThreads), L::kSmem, s, tmap, tmap_half, q);
+  q.fill_early = !p.persist && static_cast<long long>(grid.x) * grid.y * grid.z <= sms;
+  launch_pdl(split_tc_kernel<kG, kPersist>, grid, dim3(L::kThreads), L::kSmem, s, tmap, tmap_half, q);
   return MLA_OK;
 }
-// Rows per KV chunk (a multiple of kChunkAlign rows) and the resulting chunk
-// count.  With `requested` = 0 the count minimises a makespan estimate: waves
-// of CTAs over the SMs times (rows per chunk + a fixed per-CTA cost), plus the
-// combine's cost per chunk.  The bf16 and FP8 kernels run one CTA per SM and
-// work in 128-row tiles, and a chunk's partial last tile costs about what a
-// full one does (measured: 16 chunks of 256 rows beat 19 of 216 on 8 x 4096
-// rows), so for them a chunk's rows count rounded up to whole tiles.
-int chunk_rows(const mla_dims* d, int requested, int* splits_out, bool pair = false) {
+// How the split kernel cuts the rows: chunk rows, chunks per sequence, and
+// whether the grid is persistent.
+struct SplitPlan {
+  int chunk, splits;
+  bool persist;
+};
+
+int device_sms() {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    sms = 148;
+  }
+  return sms;
+}
+
+// Rows per KV chunk and the resulting chunk count, and the launch form.
+//  - One CTA per chunk.  With `requested` = 0 the count minimises a makespan
+//    estimate (in units of cache rows): waves of CTAs over the SMs times (rows
+//    per chunk + a fixed per-CTA cost), plus the combine's cost per chunk.  The
+//    bf16 and FP8 kernels run one CTA per SM and work in 128-row tiles, and a
+//    chunk's partial last tile costs about what a full one does (measured: 16
+//    chunks of 256 rows beat 19 of 216 on 8 x 4096 rows), so for them a chunk's
+//    rows count rounded up to whole tiles.  Chunks are multiples of
+//    kChunkAlign rows.
+//  - Persistent (the bf16 kernel with 16 heads per CTA), whenever that grid
+//    would take more than one wave, or, with the count left to the library, when
+//    its estimate is within 15 % of the best one-wave plan's (which balances only
+//    if every sequence is full): one CTA per SM works through the chunks whose
+//    first tile falls in its share of all tiles, so a CTA's start-up and
+//    last-tile chain are paid once and its stream runs across chunk boundaries
+//    (measured on 4 x 65536 rows at 128 chunks: 72.6 us in 3.4 waves).  Chunks
+//    are whole tiles.  With `requested` = 0 the chunk minimises: the largest
+//    share (all tiles over the SMs, counted for full-length sequences since the
+//    lengths live on the device) plus one chunk less a tile (a share ends
+//    mid-chunk), one start-up, each chunk's partial (32 KB written and read
+//    again, about 56 rows' worth of traffic and epilogue; measured on 64 ragged
+//    sequences: 16 chunks of 512 rows beat 22 of 384), and the combine's cost
+//    per chunk.
+SplitPlan plan_split(const mla_dims* d, int requested, bool pair = false) {
   const int S = d->s_max;
   const int max_splits = (S + kChunkAlign - 1) / kChunkAlign;
-  int splits = requested;
-  if (splits <= 0) {
-    int dev = 0, sms = 148;
-    if (cudaGetDevice(&dev) == cudaSuccess)
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const bool bf16 = d->dtype != MLA_F32;   // bf16 and FP8 kernels: one CTA per SM
-    const long long per_split =
-        pair ? static_cast<long long>(d->batch) * d->heads / 32
-             : static_cast<long long>(d->batch) * (bf16 ? d->heads / tc_heads_per_cta(d) : d->heads);
-    const long long slots = bf16 ? sms : 4ll * sms;   // bf16: one CTA per SM
-    double best = 1e300;
-    splits = 1;
-    for (int s = 1; s <= max_splits; ++s) {
-      const int chunk = ((S + s - 1) / s + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
+  const bool tiled = d->dtype != MLA_F32;   // bf16 and FP8 kernels: one CTA per SM
+  const long long groups = d->dtype == MLA_F32 ? d->heads : d->heads / tc_heads_per_cta(d);
+  const long long per_split = pair ? static_cast<long long>(d->batch) * d->heads / 32
+                                   : static_cast<long long>(d->batch) * groups;
+  const bool can_persist = d->dtype == MLA_BF16 && !pair && tc_heads_per_cta(d) == 16;
+  const long long sms = device_sms();
+  const long long slots = tiled ? sms : 4ll * sms;
+  auto chunk_of = [&](int s, int align) {
+    return ((S + s - 1) / s + align - 1) / align * align;
+  };
+  // One CTA per chunk.
+  int np_chunk = 0, np_splits = 0;
+  double np_cost = 1e300;
+  {
+    double& best = np_cost;
+    const int lo = requested > 0 ? requested : 1, hi = requested > 0 ? requested : max_splits;
+    for (int s = lo; s <= hi && s <= max_splits; ++s) {
+      const int chunk = chunk_of(s, kChunkAlign);
       const int s_eff = (S + chunk - 1) / chunk;
-      if (s_eff != s) continue;
+      if (requested <= 0 && s_eff != s) continue;
       const long long waves = (per_split * s_eff + slots - 1) / slots;
-      const int rows = bf16 ? (chunk + kTileRows - 1) / kTileRows * kTileRows : chunk;
+      const int rows = tiled ? (chunk + kTileRows - 1) / kTileRows * kTileRows : chunk;
       const double cost = double(waves) * (rows + 96) + 4.0 * s_eff;
       if (cost < best) {
         best = cost;
-        splits = s;
+        np_chunk = chunk;
+        np_splits = s_eff;
       }
     }
+    if (np_chunk == 0) {   // more chunks requested than row groups: one per 8 rows
+      np_chunk = kChunkAlign;
+      np_splits = (S + np_chunk - 1) / np_chunk;
+    }
   }
-  if (splits > max_splits) splits = max_splits;
-  if (splits < 1) splits = 1;
-  int chunk = (S + splits - 1) / splits;
-  chunk = (chunk + kChunkAlign - 1) / kChunkAlign * kChunkAlign;
-  *splits_out = (S + chunk - 1) / chunk;
-  return chunk;
+  const bool np_one_wave = per_split * np_splits <= slots;
+  const int form = g_split_form.load();
+  if (!can_persist || form == 2 || (form == 0 && requested > 0 && np_one_wave))
+    return {np_chunk, np_splits, false};
+  // Persistent.
+  const long long tt = groups * d->batch * ((S + kTileRows - 1) / kTileRows);   // tiles, at most
+  const long long share = (tt + sms - 1) / sms;
+  if (share + 1 > kMaxItems) return {np_chunk, np_splits, false};   // more chunks than a CTA holds
+  int p_chunk = 0, p_splits = 0;
+  double best = 1e300;
+  const int lo = requested > 0 ? requested : 1, hi = requested > 0 ? requested : max_splits;
+  for (int s = lo; s <= hi && s <= max_splits; ++s) {
+    const int chunk = chunk_of(s, kTileRows);
+    const int s_eff = (S + chunk - 1) / chunk;
+    if (requested <= 0 && s_eff != s) continue;
+    const long long ct = chunk / kTileRows;
+    const long long max_tiles = share + ct - 1;
+    const double cost = double(max_tiles) * kTileRows + 96 + 56.0 * ((max_tiles + ct - 1) / ct) +
+                        4.0 * s_eff;
+    if (cost < best) {
+      best = cost;
+      p_chunk = chunk;
+      p_splits = s_eff;
+    }
+  }
+  // The persistent estimate already counts its worst case (a share ending one
+  // chunk short of a tile), and one CTA per chunk balances only when every
+  // sequence is full, so near-ties (within 15 %) go to the persistent grid.
+  if (p_chunk == 0 || (form == 0 && np_one_wave && best > 1.15 * np_cost))
+    return {np_chunk, np_splits, false};
+  return {p_chunk, p_splits, true};
+}
+
+int chunk_rows(const mla_dims* d, int requested, int* splits_out, bool pair = false) {
+  const SplitPlan pl = plan_split(d, requested, pair);
+  *splits_out = pl.splits;
+  return pl.chunk;
 }
 
 // Partial outputs, their log-sum-exps, and (FP8 cache) the query images.
@@ -1149,6 +1674,17 @@ extern "C" int32_t mla_decode_num_splits(const mla_dims* dims, int32_t requested
   int splits = 0;
   chunk_rows(dims, requested, &splits);
   return splits;
+}
+
+extern "C" mla_status mla_decode_plan(const mla_dims* dims, int32_t requested, int32_t* splits,
+                                      int32_t* chunk, int32_t* persistent) {
+  mla_status st = check_dims(dims, "mla_decode_plan");
+  if (st != MLA_OK) return st;
+  const SplitPlan pl = plan_split(dims, requested);
+  if (splits) *splits = pl.splits;
+  if (chunk) *chunk = pl.chunk;
+  if (persistent) *persistent = pl.persist ? 1 : 0;
+  return MLA_OK;
 }
 
 extern "C" int32_t mla_decode_multi_num_splits(const mla_dims* dims, int32_t q_len,
@@ -1181,6 +1717,10 @@ extern "C" size_t mla_decode_workspace_bytes(const mla_dims* dims, int32_t reque
 // Test hooks of the bf16 split kernel (mla_test_set_split_hooks); 0 in normal use.
 static std::atomic<unsigned long long> g_hook_wait_ns{0};
 static std::atomic<int> g_hook_stop_tiles{0};
+static std::atomic<int32_t*> g_hook_debug{nullptr};
+extern "C" void mla_test_set_split_form(int32_t form) { g_split_form.store(form); }
+
+extern "C" void mla_test_set_split_debug(int32_t* records) { g_hook_debug.store(records); }
 
 extern "C" void mla_test_set_split_hooks(uint64_t wait_ns, int32_t stop_after_tiles) {
   g_hook_wait_ns.store(wait_ns);
@@ -1222,8 +1762,8 @@ static mla_status prepare(const char* who, const mla_dims* dims, int q_len, cons
     set_error("%s: num_splits must be >= 0", who);
     return MLA_ERR_INVALID_ARG;
   }
-  int splits = 0;
-  const int chunk = chunk_rows(dims, num_splits, &splits, pair);
+  const SplitPlan plan = plan_split(dims, num_splits, pair);
+  const int splits = plan.splits, chunk = plan.chunk;
   const size_t need = workspace_bytes(dims, splits);
   if (ws_bytes < need) {
     set_error("%s: workspace %zu bytes < %zu needed", who, ws_bytes, need);
@@ -1250,7 +1790,9 @@ static mla_status prepare(const char* who, const mla_dims* dims, int q_len, cons
   p->chunk = chunk;
   p->scale_log2 = softmax_scale * kLog2e;
   p->fill_early = 0;
+  p->persist = plan.persist ? 1 : 0;
   p->wait_ns = g_hook_wait_ns.load();
+  p->debug = g_hook_debug.load();
   p->stop_after_tiles = g_hook_stop_tiles.load();
   return MLA_OK;
 }
@@ -1296,8 +1838,9 @@ static mla_status decode_split(const char* who, const mla_dims* dims, int q_len,
       }
     }
     st = p.tpc == 2 || tc_heads_per_cta(dims) == 32
-             ? launch_split_tc<32>(tmap, tmap_half, p, dims->heads, s, who)
-             : launch_split_tc<16>(tmap, tmap_half, p, dims->heads, s, who);
+             ? launch_split_tc<32, false>(tmap, tmap_half, p, dims->heads, s, who)
+             : p.persist ? launch_split_tc<16, true>(tmap, tmap_half, p, dims->heads, s, who)
+                         : launch_split_tc<16, false>(tmap, tmap_half, p, dims->heads, s, who);
     if (st != MLA_OK) return st;
   } else {
     dim3 grid(dims->heads, p.splits, p.B);
@@ -1318,8 +1861,14 @@ static mla_status decode_combine(const char* who, const mla_dims* dims, int q_le
   mla_status st = prepare(who, dims, q_len, nullptr, nullptr, nullptr, lengths, 1.f, num_splits,
                           const_cast<void*>(workspace), ws_bytes, nullptr, &p);
   if (st != MLA_OK) return st;
-  launch_pdl(combine_kernel, dim3(dims->heads, p.B, kDc / 128), dim3(32), 0,
-             static_cast<cudaStream_t>(stream), p, o_c, lse);
+  const int cw = combine_warps(p.splits);
+  if (cw == 1)
+    launch_pdl(combine_kernel, dim3(dims->heads, p.B, kDc / 128), dim3(32), 0,
+               static_cast<cudaStream_t>(stream), p, o_c, lse);
+  else
+    launch_pdl(combine_warps_kernel, dim3(dims->heads, p.B, kDc / 128), dim3(32 * cw),
+               size_t(cw) * (32 * sizeof(float4) + 2 * sizeof(float)),
+               static_cast<cudaStream_t>(stream), p, o_c, lse);
   return launch_status(who);
 }
 
@@ -1480,7 +2029,7 @@ static mla_status decode_step(const char* who, const mla_dims* dims, int q_len,
         static_cast<long long>(p.splits) *
         (p.tpc == 2 ? static_cast<long long>(p.B / 2) * (dims->heads / 16)
                     : static_cast<long long>(p.B) * (dims->heads / tc_heads_per_cta(dims)));
-    single_wave = ctas <= sms;
+    single_wave = !p.persist && ctas <= sms;
     if (pf.rows <= 0 || !single_wave) pf.cache = nullptr;
   }
   // The early launch of the absorb pays only with a one-wave decode grid: with

@@ -22,9 +22,12 @@ struct SplitParams {
   uint8_t* q_img;           // FP8: the query's E4M3 image per (sequence, head group)
   int fill_early;           // bf16 kernel: issue tile 0's first boxes before the length
                             // is known (a one-wave grid)
+  int persist;              // bf16 kernel, 16 heads per CTA: a persistent grid whose CTAs
+                            // take several chunks each (chunk % 128 == 0)
   // Test hooks of the bf16 kernel (see mla_test_set_split_hooks), 0 in normal use:
   unsigned long long wait_ns;   // limit of each bounded wait (0: kWaitNs)
   int stop_after_tiles;         // ring A issues only this many tiles of a chunk (0: all)
+  int32_t* debug;               // where timed-out CTAs record their first failed wait
 };
 
 // FP8 cache: the query of one (sequence, 16-head group) as the split kernel's

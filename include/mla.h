@@ -117,10 +117,33 @@ mla_status mla_absorb_q(const mla_dims* dims, const void* q_nope, const void* q_
 /*
  * mla_decode_num_splits -- the number of KV chunks per sequence that
  * mla_decode_attn will use for `requested` (0 = let the library choose from
- * the current device's SM count).  Chunks hold a multiple of 8 rows, so the
- * result can be smaller than `requested`.  Returns 0 for invalid dims.
+ * the current device's SM count).  Chunks hold a multiple of 8 rows (of 128
+ * rows when the split kernel runs persistent, see mla_decode_plan), so the
+ * result can differ from `requested`.  Returns 0 for invalid dims.
  */
 int32_t mla_decode_num_splits(const mla_dims* dims, int32_t requested);
+
+/*
+ * mla_decode_plan -- how mla_decode_attn (and mla_decode_split, the step calls
+ * and mla_decode_attn_noalloc) cut the rows for `requested` chunks on the
+ * current device.  Any output pointer may be NULL.
+ *
+ * splits      chunks per sequence (as mla_decode_num_splits); a sequence of
+ *             length S_b has ceil(S_b / chunk) partials
+ * chunk       rows per chunk (a multiple of 8; of 128 when persistent)
+ * persistent  1: the bf16 split kernel (16 heads per CTA) runs as one CTA per
+ *             SM, each CTA working through the chunks whose first 128-row tile
+ *             falls in its equal share of all tiles, back to back; chosen when
+ *             one CTA per chunk would need several waves and the library's
+ *             estimate favours it.  0: one CTA per (head group, chunk, sequence).
+ *             Results do not depend on it beyond rounding order.
+ *
+ * A chunk's partial is the exact softmax-normalised output of its rows and its
+ * log-sum-exp (Multi-Head Latent Attention, 3.6 restated per chunk); the
+ * combine merges them.  Returns MLA_OK or the dims' error status.
+ */
+mla_status mla_decode_plan(const mla_dims* dims, int32_t requested, int32_t* splits,
+                           int32_t* chunk, int32_t* persistent);
 
 /* Bytes of device workspace mla_decode_attn needs for `requested` splits. */
 size_t mla_decode_workspace_bytes(const mla_dims* dims, int32_t requested);
@@ -449,6 +472,27 @@ void mla_set_launch_overlap(int32_t enable);
  * keep the values of their capture).  Reset with (0, 0) after the test.
  */
 void mla_test_set_split_hooks(uint64_t wait_ns, int32_t stop_after_tiles);
+
+/*
+ * mla_test_set_split_debug -- test hook of the bf16 split kernel; not for
+ * production use.  records: NULL (off) or a zeroed device array of 1 + 8 * 256
+ * int32.  Every CTA whose bounded wait ran out appends one record of eight
+ * words after atomically counting itself in records[0]: its block index, the
+ * index of the barrier its first failed wait was on (-1: ring B's wait for the
+ * score issuers), that wait's parity, the waiting thread, the CTA's work items
+ * and tiles, and the tiles each score issuer had issued.  Process-wide; read
+ * when a split is enqueued.
+ */
+void mla_test_set_split_debug(int32_t* records);
+
+/*
+ * mla_test_set_split_form -- test hook; not for production use.  0: the
+ * library chooses the split's launch form (mla_decode_plan); 1: the persistent
+ * grid wherever the kernel supports it (bf16, 16 heads per CTA); 2: never the
+ * persistent grid.  Process-wide; read by every later planning call, so set it
+ * before sizing a workspace and keep it until the calls that use it are done.
+ */
+void mla_test_set_split_form(int32_t form);
 
 #ifdef __cplusplus
 }

@@ -37,14 +37,17 @@ def small(dtype, B=3, S=300, H=16, hidden=2048, q_len=1):
                      hidden=hidden, q_len=q_len)
 
 
-@pytest.mark.parametrize("dtype,H,q_len", [("bf16", 16, 1), ("fp8", 16, 1), ("f32", 16, 1),
-                                           ("bf16", 32, 1), ("bf16", 16, 4), ("fp8", 16, 2)])
+@pytest.mark.parametrize("dtype,H,q_len,B", [("bf16", 16, 1, 3), ("fp8", 16, 1, 3),
+                                             ("f32", 16, 1, 3), ("bf16", 32, 1, 3),
+                                             ("bf16", 16, 4, 3), ("fp8", 16, 2, 3),
+                                             ("bf16", 16, 1, 60), ("bf16", 16, 3, 20)])
 @pytest.mark.parametrize("splits", [0, 3])
-def test_decode_calls_stay_in_bounds(cuda_lib, dtype, H, q_len, splits):
+def test_decode_calls_stay_in_bounds(cuda_lib, dtype, H, q_len, B, splits):
+    """B = 60 (three chunks) and 20 x 3 tokens run the persistent split grid."""
     mla = cuda_lib
-    cfg = small(dtype, B=3, S=300, H=H, q_len=q_len)
-    inp = make_inputs(cfg, seed=80, lengths=torch.tensor([300, 129, max(q_len, 17)],
-                                                         dtype=torch.int32))
+    cfg = small(dtype, B=B, S=300, H=H, q_len=q_len)
+    lens = torch.tensor([300, 129, max(q_len, 17)] * (B // 3), dtype=torch.int32)
+    inp = make_inputs(cfg, seed=80, lengths=lens)
     d = mla.dims(cfg.batch, cfg.heads, cfg.s_max, mla.dtype_code(cache_storage(cfg)))
     qd = mla.query_dims(d, q_len)
     R = cfg.batch * q_len

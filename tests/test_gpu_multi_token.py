@@ -171,3 +171,21 @@ def test_captured_multi_token_step_from_host_memory(cuda_lib, dtype):
     torch.cuda.synchronize()
     np.testing.assert_array_equal(got, eager.double().cpu().numpy())
     assert int(step.status.item()) == 0
+
+
+def test_odd_token_count_persistent(cuda_lib):
+    """Three tokens per sequence (not paired) on 40 sequences: 120 query groups x
+    4 chunks run as the persistent split grid."""
+    import head_latent_attention_absorbed_gb300 as mla
+    cfg = small("bf16", 3, B=40, S=512)
+    d = mla.dims(cfg.batch, cfg.heads, cfg.s_max, mla.MLA_BF16)
+    assert mla.plan(mla.query_dims(d, 3), 4)[2]
+    g = torch.Generator().manual_seed(61)
+    lens = torch.randint(3, 513, (40,), generator=g, dtype=torch.int32)
+    lens[0], lens[1] = 3, 129
+    inp = make_inputs(cfg, seed=61, poison_tail=True, lengths=lens)
+    gpu = run_cuda(inp, 4)
+    assert gpu["status"] == 0
+    ref, bs = run_oracle(inp)
+    compare(gpu, ref, bs, "bf16")
+
