@@ -1285,9 +1285,12 @@ __global__ void __launch_bounds__(32)
 // merged through shared memory.  W grows with the chunk count (combine_warps),
 // so that many chunks are not read one group after another by a single warp.
 constexpr int kCombineMaxWarps = 8;
-// The warp states are merged in dynamic shared memory (W > 1 only), so that a
-// one-warp CTA needs none and fits beside a split CTA, launching early.
-__global__ void __launch_bounds__(32 * kCombineMaxWarps)
+// Each warp keeps kCombineGroup chunks' loads in flight (fewer registers than
+// the one-warp kernel's kCombineChunk, so that two 256-thread CTAs share an SM
+// and 128 chunks of 4 x 16 heads take one wave).  The warp states are merged in
+// dynamic shared memory.
+constexpr int kCombineGroup = 16;
+__global__ void __launch_bounds__(32 * kCombineMaxWarps, 2)
     combine_warps_kernel(const SplitParams p, float* o_c, float* lse_out) {
   extern __shared__ float4 s_acc[];   // [W][32], then s_m[W], s_sum[W]
   const int h = blockIdx.x, b = blockIdx.y;
@@ -1310,20 +1313,20 @@ __global__ void __launch_bounds__(32 * kCombineMaxWarps)
   const float4* po = reinterpret_cast<const float4*>(p.part_o + row0 * kDc) + col;
   float m = -INFINITY, sum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  for (int s0 = warp; s0 < nsplit; s0 += W * kCombineChunk) {
-    float ls[kCombineChunk];
-    float4 v[kCombineChunk];
+  for (int s0 = warp; s0 < nsplit; s0 += W * kCombineGroup) {
+    float ls[kCombineGroup];
+    float4 v[kCombineGroup];
 #pragma unroll
-    for (int u = 0; u < kCombineChunk; ++u) {
+    for (int u = 0; u < kCombineGroup; ++u) {
       const int sj = s0 + W * u;
       const bool ok = sj < nsplit;
       ls[u] = ok ? lse_bh[sj] : -INFINITY;
       v[u] = ok ? po[size_t(sj) * (kDc / 4)] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    if (s0 + W * kCombineChunk >= nsplit && threadIdx.x == 0) pdl_launch_dependents();
+    if (s0 + W * kCombineGroup >= nsplit && threadIdx.x == 0) pdl_launch_dependents();
     float cm = m;
 #pragma unroll
-    for (int u = 0; u < kCombineChunk; ++u) cm = fmaxf(cm, ls[u]);
+    for (int u = 0; u < kCombineGroup; ++u) cm = fmaxf(cm, ls[u]);
     // cm is finite: every chunk with rows has a finite lse, and s0 < nsplit.
     const float r = m == -INFINITY ? 0.f : expf(m - cm);
     sum *= r;
@@ -1332,7 +1335,7 @@ __global__ void __launch_bounds__(32 * kCombineMaxWarps)
     acc.z *= r;
     acc.w *= r;
 #pragma unroll
-    for (int u = 0; u < kCombineChunk; ++u) {
+    for (int u = 0; u < kCombineGroup; ++u) {
       const float w = s0 + W * u < nsplit ? expf(ls[u] - cm) : 0.f;
       sum += w;
       acc.x = fmaf(w, v[u].x, acc.x);
