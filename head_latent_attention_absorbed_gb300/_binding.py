@@ -13,10 +13,12 @@ from typing import Optional
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libmla_gb300.so")
+CHECK_LIB_PATH = os.path.join(PKG, "libmla_gb300_check.so")   # the checked build
 
 MLA_F32, MLA_BF16, MLA_FP8_E4M3 = 0, 1, 2
 MLA_DEV_LENGTH_OUT_OF_RANGE = 1
 MLA_DEV_PIPELINE_TIMEOUT = 2
+MLA_DEV_BOUNDS = 4
 STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_UNSUPPORTED",
           3: "MLA_ERR_WORKSPACE", 4: "MLA_ERR_CUDA"}
 EXPORTED = ("mla_absorb_q", "mla_decode_num_splits", "mla_decode_workspace_bytes",
@@ -28,7 +30,7 @@ EXPORTED = ("mla_absorb_q", "mla_decode_num_splits", "mla_decode_workspace_bytes
             "mla_absorb_q_materialized", "mla_ov_proj",
             "mla_status_string", "mla_last_error_message", "mla_test_set_split_hooks",
             "mla_set_launch_overlap", "mla_decode_plan", "mla_test_set_split_debug",
-            "mla_test_set_split_form")
+            "mla_test_set_split_form", "mla_built_with_checks", "mla_debug_bounds_word")
 
 
 class MlaDims(ctypes.Structure):
@@ -110,6 +112,10 @@ def load(path: Optional[str] = None):
     lib.mla_test_set_split_debug.restype = None
     lib.mla_test_set_split_form.argtypes = [I32]
     lib.mla_test_set_split_form.restype = None
+    lib.mla_built_with_checks.argtypes = []
+    lib.mla_built_with_checks.restype = I32
+    lib.mla_debug_bounds_word.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+    lib.mla_debug_bounds_word.restype = ctypes.c_int
     lib.mla_decode_plan.argtypes = [D, I32, ctypes.POINTER(I32), ctypes.POINTER(I32),
                                     ctypes.POINTER(I32)]
     lib.mla_decode_plan.restype = ctypes.c_int

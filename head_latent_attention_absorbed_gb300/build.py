@@ -19,6 +19,10 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libmla_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 BUILD_DIR = os.path.join(PKG, "_build")
+# The checked build (-DMLA_CHECK: index checks in the decode kernels that skip
+# an out-of-range access and raise MLA_DEV_BOUNDS), kept beside the default one.
+CHECK_LIB_PATH = os.path.join(PKG, "libmla_gb300_check.so")
+CHECK_BUILD_DIR = os.path.join(PKG, "_build_check")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-cudart", "shared",
@@ -47,16 +51,21 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
-    """Build (if stale) and return the path of the shared library."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(verbose: bool = False, force: bool = False, extra_flags=None, check: bool = False) -> str:
+    """Build (if stale) and return the path of the shared library; with
+    ``check`` the checked build (compiled with -DMLA_CHECK) instead."""
+    build_dir = CHECK_BUILD_DIR if check else BUILD_DIR
+    lib_path = CHECK_LIB_PATH if check else LIB_PATH
+    os.makedirs(build_dir, exist_ok=True)
     srcs = _sources()
     hdrs = _headers()
     flags = ARCH + NVCC_FLAGS + ["-I", INCLUDE, "-I", CSRC] + list(extra_flags or [])
+    if check:
+        flags.append("-DMLA_CHECK")
     objs = []
     jobs = []
     for s in srcs:
-        o = os.path.join(BUILD_DIR, os.path.basename(s)[:-3] + ".o")
+        o = os.path.join(build_dir, os.path.basename(s)[:-3] + ".o")
         objs.append(o)
         if force or _stale(o, [s] + hdrs):
             jobs.append([nvcc(), *flags, "-c", s, "-o", o])
@@ -73,9 +82,9 @@ def build(verbose: bool = False, force: bool = False, extra_flags=None) -> str:
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
             list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB_PATH, objs):
-        run([nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", LIB_PATH, *objs])
-    return LIB_PATH
+    if force or jobs or _stale(lib_path, objs):
+        run([nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", lib_path, *objs])
+    return lib_path
 
 
 if __name__ == "__main__":

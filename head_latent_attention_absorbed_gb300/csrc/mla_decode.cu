@@ -22,6 +22,27 @@
 namespace mla {
 namespace {
 
+// The checked build (compiled with -DMLA_CHECK): before an access whose index
+// it can compute, a kernel of this file tests that the index lies inside its
+// buffer; a failed test skips the access and ORs MLA_DEV_BOUNDS into the call's
+// status word (when it has one) and into g_bounds_word, which
+// mla_debug_bounds_word exposes.  In the default build the tests compile away.
+__device__ int32_t g_bounds_word;
+__device__ __forceinline__ bool bounds_ok(bool in_range, int32_t* status) {
+#ifdef MLA_CHECK
+  if (!in_range) {
+    atomicOr(&g_bounds_word, MLA_DEV_BOUNDS);
+    if (status) atomicOr(status, MLA_DEV_BOUNDS);
+  }
+  return in_range;
+#else
+  (void)status;
+  (void)in_range;
+  return true;
+#endif
+}
+#define MLA_IN_BOUNDS(cond) bounds_ok((cond), p.status)
+
 constexpr int kWarps = 4;
 constexpr int kChunkAlign = 8;   // chunk sizes are multiples of 8 rows
 constexpr int kThreads = kWarps * 32;
@@ -348,6 +369,9 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
   // and each 8-head softmax group masks the rows past its own token.
   const bool pair = kG == 32 && p.tpc == 2;
   constexpr bool persist = kPersist;
+  // Rows of the cache's [sequences * s_max, 576] view (index checks).
+  const long long cache_rows = static_cast<long long>(p.B / p.q_len) * p.s_max;
+  (void)cache_rows;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   auto bar = [&](int i) { return bars + 8 * i; };
 
@@ -366,8 +390,9 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
     prefetch_tmap(&tmap);
     for (int pos = 0; pos < kSlotsA; ++pos) {
       mbar_arrive_expect_tx(bar(BAR_FULLA + pos), kBoxBytes);
-      tma_load_2d(sbase + kOffA + pos * kBoxBytes, &tmap, 64 * pos, row,
-                  bar(BAR_FULLA + pos), keep);
+      if (MLA_IN_BOUNDS(row >= 0 && row < cache_rows))
+        tma_load_2d(sbase + kOffA + pos * kBoxBytes, &tmap, 64 * pos, row,
+                    bar(BAR_FULLA + pos), keep);
     }
   };
   const bool ring_a = warp == kWarpA && lane == 0;
@@ -544,10 +569,13 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
 #pragma unroll
     for (int i = 0; i < 9; ++i) {
       const int idx = tid + i * kSoftThreads;
+      // the query row (v', h) this load belongs to, for the index check
+      const int n = idx < kNA ? idx / (kDc / 4) : (idx - kNA) / (kDr / 4);
+      const size_t row = pair ? size_t(v + n / 16) * p.H + h0 + n % 16 : size_t(v) * p.H + h0 + n;
+      q4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (!MLA_IN_BOUNDS(row < size_t(p.B) * p.H)) continue;
       if (pair) {
         // column n: head h0 + n % 16 of query group v + n / 16
-        const int n = idx < kNA ? idx / (kDc / 4) : (idx - kNA) / (kDr / 4);
-        const size_t row = size_t(v + n / 16) * p.H + h0 + n % 16;
         q4[i] = idx < kNA ? reinterpret_cast<const float4*>(static_cast<const float*>(p.q_abs) +
                                                             row * kDc)[idx % (kDc / 4)]
                           : reinterpret_cast<const float4*>(static_cast<const float*>(p.q_pe) +
@@ -565,9 +593,12 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
       split_bf16(q4[i].x, q4[i].y, hi.x, lo.x);
       split_bf16(q4[i].z, q4[i].w, hi.y, lo.y);
       const int box = k >> 6, ch = (k & 63) >> 3, w = k & 7;
-      *reinterpret_cast<uint2*>(smem + kOffQ + box * kQBoxBytes + sw128(h, ch) + 2 * w) = hi;
-      *reinterpret_cast<uint2*>(smem + kOffQ + box * kQBoxBytes + sw128(h + kHeadGroup, ch) +
-                                2 * w) = lo;
+      const uint32_t o_hi = box * kQBoxBytes + sw128(h, ch) + 2 * w;
+      const uint32_t o_lo = box * kQBoxBytes + sw128(h + kHeadGroup, ch) + 2 * w;
+      if (MLA_IN_BOUNDS(o_hi + 8 <= 9u * kQBoxBytes && o_lo + 8 <= 9u * kQBoxBytes)) {
+        *reinterpret_cast<uint2*>(smem + kOffQ + o_hi) = hi;
+        *reinterpret_cast<uint2*>(smem + kOffQ + o_lo) = lo;
+      }
     }
     fence_proxy_async_smem();
   };
@@ -586,8 +617,9 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
           if (pos < kSlotsA) continue;   // issued before the CTA-wide barrier
           if (use > 0 && !wait_or_abort(bar(BAR_EMPTYA + sl), (use - 1) & 1, abort_flag, wait_ns)) break;
           mbar_arrive_expect_tx(bar(BAR_FULLA + sl), kBoxBytes);
-          tma_load_2d(sbase + kOffA + sl * kBoxBytes, &tmap, 64 * box_at(t, k), row,
-                      bar(BAR_FULLA + sl), keep);
+          if (MLA_IN_BOUNDS(row >= 0 && row < cache_rows))
+            tma_load_2d(sbase + kOffA + sl * kBoxBytes, &tmap, 64 * box_at(t, k), row,
+                        bar(BAR_FULLA + sl), keep);
           issued = pos + 1;
         }
       }
@@ -620,8 +652,9 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
               second = true;
             }
             mbar_arrive_expect_tx(bar(BAR_FULLX + k), kBoxBytes);
-            tma_load_2d(sbase + tail_box_off(k), &tmap, 64 * k, last_row, bar(BAR_FULLX + k),
-                        stream);
+            if (MLA_IN_BOUNDS(last_row >= 0 && last_row < cache_rows))
+              tma_load_2d(sbase + tail_box_off(k), &tmap, 64 * k, last_row, bar(BAR_FULLX + k),
+                          stream);
             armed_x |= 1u << k;
           }
           break;
@@ -650,8 +683,9 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
             mbar_arrive_expect_tx(bar(BAR_FULLX + x), 2 * kHalfBox);
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-              tma_load_2d(sbase + borrow_off(x) + h * kHalfBox, &tmap_half, 64 * (2 * mb + h), row,
-                          bar(BAR_FULLX + x), stream);
+              if (MLA_IN_BOUNDS(row >= 0 && row < cache_rows))
+                tma_load_2d(sbase + borrow_off(x) + h * kHalfBox, &tmap_half, 64 * (2 * mb + h),
+                            row, bar(BAR_FULLX + x), stream);
             armed_x |= 1u << x;
             continue;
           }
@@ -660,8 +694,9 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
           mbar_arrive_expect_tx(bar(BAR_FULLB + sl), 2 * kHalfBox);
 #pragma unroll
           for (int h = 0; h < 2; ++h)
-            tma_load_2d(sbase + kOffB + (2 * sl + h) * kHalfBox, &tmap_half, 64 * (2 * mb + h),
-                        row, bar(BAR_FULLB + sl), stream);
+            if (MLA_IN_BOUNDS(row >= 0 && row < cache_rows))
+              tma_load_2d(sbase + kOffB + (2 * sl + h) * kHalfBox, &tmap_half, 64 * (2 * mb + h),
+                          row, bar(BAR_FULLB + sl), stream);
           issued = pos + 1;
         }
       }
@@ -882,7 +917,9 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
           Lme = lane == h ? Ls : Lme;
           mme = lane == h ? mm[h] : mme;
         }
-        if (wq == 0 && lane < kHalfHeads)
+        const size_t n_part = size_t(p.B) * p.H * p.splits;   // rows of the partials
+        if (wq == 0 && lane < kHalfHeads &&
+            MLA_IN_BOUNDS(base + size_t(hw + lane) * p.splits < n_part))
           p.part_lse[base + size_t(hw + lane) * p.splits] =
               Lme > 0.f ? (mme + log2f(Lme)) * kLn2 : -INFINITY;
         uint32_t hi4[4][8], lo4[4][8];
@@ -895,10 +932,12 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
         float* orow = p.part_o + (base + size_t(hw) * p.splits) * kDc + 32 * wq + lane;
         const size_t head_stride = size_t(p.splits) * kDc;
 #pragma unroll
-        for (int h = 0; h < kHalfHeads; ++h, orow += head_stride)
+        for (int h = 0; h < kHalfHeads; ++h, orow += head_stride) {
+          if (!MLA_IN_BOUNDS(base + size_t(hw + h) * p.splits < n_part)) continue;
 #pragma unroll
           for (int mb = 0; mb < 4; ++mb)
             orow[128 * mb] = (__uint_as_float(hi4[mb][h]) + __uint_as_float(lo4[mb][h])) * inv[h];
+        }
       }
       if (!last) {
         // The O^T buffer may take a later item now.
@@ -1009,12 +1048,16 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
         // P^T (B operand of the PV MMA, K-major 128-byte swizzle, two 64-row
         // halves): row n < 16 is bf16(p) of head n, row 16 + n is
         // bf16(p - bf16(p)); the K index is the tile row.
-        uint8_t* pbuf = smem + kOffP + (t % kPBufs) * kPBytes + (row >> 6) * kPSub;
+        const uint32_t pofs = (t % kPBufs) * kPBytes + (row >> 6) * kPSub;
+        uint8_t* pbuf = smem + kOffP + pofs;
         const int ch = (row & 63) >> 3, w = row & 7;
 #pragma unroll
         for (int h = 0; h < kHalfHeads; ++h) {
           const __nv_bfloat16 hi = __float2bfloat16_rn(sc[h]);
           const __nv_bfloat16 lo = __float2bfloat16_rn(sc[h] - __bfloat162float(hi));
+          if (!MLA_IN_BOUNDS(pofs + sw128(kHeadGroup + hb + h, ch) + 2 * w + 2 <=
+                             uint32_t(kPBufs * kPBytes)))
+            continue;
           *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128(hb + h, ch) + 2 * w) = hi;
           *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128(kHeadGroup + hb + h, ch) + 2 * w) = lo;
         }
@@ -1037,7 +1080,9 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
             if (!tail_res(k >> 1)) wait_or_abort(bar(BAR_FULLX + k), 0, abort_flag, wait_ns);
             uint8_t* box = smem + tail_box_off(k) + zero_from * 128;
             for (int q = tid; q < nrow * 8; q += kSoftThreads)
-              *reinterpret_cast<uint4*>(box + q * 16) = make_uint4(0, 0, 0, 0);
+              if (MLA_IN_BOUNDS(zero_from >= 0 && tail_box_off(k) + zero_from * 128 + q * 16 + 16 <=
+                                                     tail_box_off(k) + kBoxBytes))
+                *reinterpret_cast<uint4*>(box + q * 16) = make_uint4(0, 0, 0, 0);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(BAR_ZEROX + k));
@@ -1055,8 +1100,9 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
           uint8_t* pr = smem + (bw ? borrow_off(x) : kOffB + 2 * sl * kHalfBox);
           for (int q = tid; q < 2 * nrow * 8; q += kSoftThreads) {
             const int h = q / (nrow * 8), rem = q % (nrow * 8);
-            *reinterpret_cast<uint4*>(pr + h * kHalfBox + (first + rem / 8) * 128 + (rem % 8) * 16) =
-                make_uint4(0, 0, 0, 0);
+            const int o = h * kHalfBox + (first + rem / 8) * 128 + (rem % 8) * 16;
+            if (MLA_IN_BOUNDS(o >= 0 && o + 16 <= 2 * kHalfBox))
+              *reinterpret_cast<uint4*>(pr + o) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -1082,8 +1128,9 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
           uint8_t* pr = smem + kOffB + 2 * sl * kHalfBox;
           for (int q = tid; q < 2 * nrow * 8; q += kSoftThreads) {
             const int h = q / (nrow * 8), rem = q % (nrow * 8);
-            *reinterpret_cast<uint4*>(pr + h * kHalfBox + (first + rem / 8) * 128 + (rem % 8) * 16) =
-                make_uint4(0, 0, 0, 0);
+            const int o = h * kHalfBox + (first + rem / 8) * 128 + (rem % 8) * 16;
+            if (MLA_IN_BOUNDS(o >= 0 && o + 16 <= 2 * kHalfBox))
+              *reinterpret_cast<uint4*>(pr + o) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -1228,7 +1275,8 @@ __global__ void __launch_bounds__(32)
   const int tid = blockIdx.z * 32 + threadIdx.x;   // float4 column of the 512
   const int len = clamp_length(p, b, false);   // a caller input, not the split's output
   pdl_wait();   // the partials come from the split kernel just before
-  const int nsplit = (len + p.chunk - 1) / p.chunk;
+  int nsplit = (len + p.chunk - 1) / p.chunk;
+  if (!MLA_IN_BOUNDS(nsplit <= p.splits)) nsplit = p.splits;   // partials past the workspace
   float* out = o_c + (size_t(b) * p.H + h) * kDc;
   if (nsplit == 0) {
     reinterpret_cast<float4*>(out)[tid] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -1298,7 +1346,8 @@ __global__ void __launch_bounds__(32 * kCombineMaxWarps, 2)
   const int col = blockIdx.z * 32 + lane;      // float4 column of the 512
   const int len = clamp_length(p, b, false);   // a caller input, not the split's output
   pdl_wait();   // the partials come from the split kernel just before
-  const int nsplit = (len + p.chunk - 1) / p.chunk;
+  int nsplit = (len + p.chunk - 1) / p.chunk;
+  if (!MLA_IN_BOUNDS(nsplit <= p.splits)) nsplit = p.splits;   // partials past the workspace
   float* out = o_c + (size_t(b) * p.H + h) * kDc;
   if (nsplit == 0) {
     if (warp == 0) {
@@ -1418,7 +1467,8 @@ __global__ void __launch_bounds__(128)
   // The next kernel (the next step's mla_absorb_q) may launch now and fetch its
   // weights; it waits for this grid before it reads or writes anything else.
   if (tid == 0) pdl_launch_dependents();
-  const int nsplit = (len + p.chunk - 1) / p.chunk;
+  int nsplit = (len + p.chunk - 1) / p.chunk;
+  if (!MLA_IN_BOUNDS(nsplit <= p.splits)) nsplit = p.splits;   // partials past the workspace
   float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
   float lse_v = -INFINITY;
   if (nsplit > 0) {
@@ -1677,6 +1727,29 @@ extern "C" int32_t mla_decode_num_splits(const mla_dims* dims, int32_t requested
   int splits = 0;
   chunk_rows(dims, requested, &splits);
   return splits;
+}
+
+extern "C" mla_status mla_debug_bounds_word(int32_t** word) {
+  if (!word) {
+    set_error("mla_debug_bounds_word: word is NULL");
+    return MLA_ERR_INVALID_ARG;
+  }
+  void* ptr = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&ptr, g_bounds_word);
+  if (e != cudaSuccess) {
+    set_error("mla_debug_bounds_word: cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
+    return MLA_ERR_CUDA;
+  }
+  *word = static_cast<int32_t*>(ptr);
+  return MLA_OK;
+}
+
+extern "C" int32_t mla_built_with_checks(void) {
+#ifdef MLA_CHECK
+  return 1;
+#else
+  return 0;
+#endif
 }
 
 extern "C" mla_status mla_decode_plan(const mla_dims* dims, int32_t requested, int32_t* splits,

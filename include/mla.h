@@ -93,6 +93,7 @@ typedef struct mla_dims {
 /* Bits a kernel ORs into the optional device status word (see mla_decode_attn). */
 #define MLA_DEV_LENGTH_OUT_OF_RANGE 1  /* some lengths[b] < 1 (< q_len) or > s_max */
 #define MLA_DEV_PIPELINE_TIMEOUT 2     /* a bounded wait in a kernel's pipeline gave up */
+#define MLA_DEV_BOUNDS 4               /* checked build: an index outside its buffer (skipped) */
 
 /*
  * mla_absorb_q -- absorbed query and rotated RoPE query for one decode step.
@@ -451,6 +452,25 @@ const char* mla_last_error_message(void);
  * of the pages: a measurement switch of this library.
  */
 void mla_set_launch_overlap(int32_t enable);
+
+/*
+ * The checked build.  Compiled with -DMLA_CHECK (the package's
+ * build(check=True) writes it beside the default library as
+ * libmla_gb300_check.so), the kernels of mla_decode_attn and of
+ * mla_decode_step's fused tail (the split kernels, the combines, the combine
+ * with W_UV) test each shared-memory and global index they can compute before
+ * the access: TMA rows of the cache, the query rows, the query and P tiles and
+ * the zeroed rows in shared memory, the partials and chunk counts.  A failed
+ * test skips the access, ORs MLA_DEV_BOUNDS into the call's dev_status (when
+ * given) and into the library's bounds word.  Nothing asserts or traps.  In the
+ * default build the tests compile away and the word is never written.
+ *
+ * mla_built_with_checks   1 in the checked build, 0 otherwise.
+ * mla_debug_bounds_word   the device address (current device) of the bounds
+ *                         word; the caller may zero it and read it back.
+ */
+int32_t mla_built_with_checks(void);
+mla_status mla_debug_bounds_word(int32_t** word);
 
 /*
  * mla_test_set_split_hooks -- test hooks of the bf16 split kernel; not for
