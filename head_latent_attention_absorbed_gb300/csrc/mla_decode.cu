@@ -115,7 +115,8 @@ struct TcPlan {
   static constexpr int kOffRed = kOffP + kPBufs * kPBytes;   // [2][kG heads][4 warps] tile maxima
   static constexpr int kOffLsum = kOffRed + 2 * kG * 4 * 4;
   static constexpr int kOffItems = kOffLsum + kG * 4 * 4;
-  static constexpr int kOffBar = kOffItems + kItems * static_cast<int>(sizeof(SplitItem));
+  static constexpr int kOffBar =
+      (kOffItems + kItems * static_cast<int>(sizeof(SplitItem)) + 127) / 128 * 128;
   static constexpr int BAR_FULLA = 0, BAR_EMPTYA = kSlotsA, BAR_FULLB = 2 * kSlotsA,
                        BAR_EMPTYB = BAR_FULLB + kSlotsB, BAR_ZEROB = BAR_EMPTYB + kSlotsB,
                        BAR_SFULL = BAR_ZEROB + kSlotsB, BAR_SFREE = BAR_SFULL + 2,
@@ -137,6 +138,9 @@ struct TcPlan {
   static constexpr uint32_t kOBufCols = 4 * kQN;
   static constexpr uint32_t kTmemCols = kG == 16 && !kPersist ? 256 : 512;
   static_assert(kOCol + kOBufs * kOBufCols <= kTmemCols, "tensor memory plan");
+  static_assert(kOffBar % 8 == 0 && kOffItems % 4 == 0 && kOffRed % 16 == 0 &&
+                    kOffLsum % 16 == 0 && kOffSlot % 16 == 0 && kOffAbort % 4 == 0,
+                "mbarriers need 8-byte alignment, the float4 reads of the maxima 16");
   static_assert(kSmem <= 232448, "shared memory plan exceeds 227 KB");
   static_assert(kSlotsA * kBoxBytes + 9 * kQBoxBytes >= 8 * kBoxBytes,
                 "the last tile's eight latent pairs fit in ring A and the query area");
