@@ -17,7 +17,8 @@ from ._binding import (EXPORTED, LIB_PATH, MLA_BF16, MLA_FP8_E4M3, MLA_DEV_LENGT
                        query_dims, wo_proj,
                        materialize_wkq, materialize_wov, absorb_q_materialized, ov_proj,
                        decode_attn_noalloc, decode_combine, decode_split, decode_step, dims,
-                       dtype_code, load, num_splits, out_proj, plan, set_launch_overlap,
+                       dtype_code, heads_per_cta, load, num_splits, out_proj, plan,
+                       set_launch_overlap, set_split_parts,
                        workspace_bytes)
 
 __all__ = [
@@ -28,7 +29,7 @@ __all__ = [
     "absorb_q_materialized", "ov_proj",
     "decode_attn_noalloc", "decode_split", "decode_combine", "decode_step", "dims",
     "dtype_code", "load", "num_splits", "out_proj", "workspace_bytes", "DecodeStep", "HostStep",
-    "cache_append", "wo_proj", "set_launch_overlap", "plan",
+    "cache_append", "wo_proj", "set_launch_overlap", "plan", "set_split_parts", "heads_per_cta",
 ]
 
 

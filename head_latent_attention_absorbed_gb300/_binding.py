@@ -30,7 +30,8 @@ EXPORTED = ("mla_absorb_q", "mla_decode_num_splits", "mla_decode_workspace_bytes
             "mla_absorb_q_materialized", "mla_ov_proj",
             "mla_status_string", "mla_last_error_message", "mla_test_set_split_hooks",
             "mla_set_launch_overlap", "mla_decode_plan", "mla_test_set_split_debug",
-            "mla_test_set_split_form", "mla_built_with_checks", "mla_debug_bounds_word")
+            "mla_test_set_split_form", "mla_built_with_checks", "mla_debug_bounds_word",
+            "mla_set_split_parts", "mla_decode_heads_per_cta")
 
 
 class MlaDims(ctypes.Structure):
@@ -112,6 +113,10 @@ def load(path: Optional[str] = None):
     lib.mla_test_set_split_debug.restype = None
     lib.mla_test_set_split_form.argtypes = [I32]
     lib.mla_test_set_split_form.restype = None
+    lib.mla_set_split_parts.argtypes = [I32]
+    lib.mla_set_split_parts.restype = ctypes.c_int
+    lib.mla_decode_heads_per_cta.argtypes = [D]
+    lib.mla_decode_heads_per_cta.restype = I32
     lib.mla_built_with_checks.argtypes = []
     lib.mla_built_with_checks.restype = I32
     lib.mla_debug_bounds_word.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
@@ -127,6 +132,17 @@ def load(path: Optional[str] = None):
 def set_launch_overlap(enable: bool) -> None:
     """Programmatic dependent launch on (default) or off for later launches."""
     load().mla_set_launch_overlap(1 if enable else 0)
+
+
+def set_split_parts(parts: int) -> None:
+    """0: the library's choice (one bf16 part of the query and P at multiples of
+    64 heads); 2: hi + lo parts everywhere."""
+    _check(load().mla_set_split_parts(int(parts)))
+
+
+def heads_per_cta(d: "MlaDims") -> int:
+    """Heads per split CTA under the current set_split_parts (64: one part)."""
+    return int(load().mla_decode_heads_per_cta(ctypes.byref(d)))
 
 
 def _check(code: int):

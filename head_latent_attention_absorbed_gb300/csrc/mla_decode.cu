@@ -85,18 +85,27 @@ constexpr int kMaxItems = 128;
 // Test hook (mla_test_set_split_form): 0 the planner chooses the split's form,
 // 1 persistent wherever the kernel allows it, 2 never persistent.
 std::atomic<int> g_split_form{0};
+// mla_set_split_parts: 0 the library's choice (one bf16 part of the query and P
+// with 64 heads per CTA where the head count is a multiple of 64), 2 always
+// hi + lo parts.
+std::atomic<int> g_split_parts{0};
 
-// The kernel's plan for kG heads per CTA (16 or 32; N = 2 kG query rows, the
-// heads' hi and lo parts).  kG = 32 halves, per head, the MMAs and the tile
-// reads (shared memory and L2); its query and accumulators need more room, so
-// ring A has four slots, P one buffer and O^T one buffer.  kPersist: the
-// persistent instance (16 heads per CTA) holds a table of work items and
-// double-buffers O^T in tensor memory, so that a CTA's next item accumulates
-// while the previous one's epilogue reads its result; the ordinary instance
-// has one item and none of that code.
+// The kernel's plan for kG heads per CTA.  With 16 or 32 heads the query and P
+// enter the tensor core as bf16 hi and lo parts (N = 2 kG query rows); with 64
+// as one bf16 part each (N = 64: bf16 operands, fp32 accumulation), which
+// halves the CTAs that read each row at 128 heads.  N = 64 halves, per head,
+// the MMAs and the tile reads (shared memory and L2) against N = 32; its query
+// and accumulators need more room, so ring A has four slots, P one buffer and
+// O^T one buffer.  kPersist: the persistent instance (16 heads per CTA) holds a
+// table of work items and double-buffers O^T in tensor memory, so that a CTA's
+// next item accumulates while the previous one's epilogue reads its result;
+// the ordinary instance has one item and none of that code.
 template <int kG, bool kPersist = false>
 struct TcPlan {
-  static constexpr int kSoftWarps = kG / 2;            // four warps per group of 8 heads
+  static constexpr int kParts = kG == 64 ? 1 : 2;      // bf16 parts of the query and of P
+  static constexpr int kQN = kParts * kG;              // query rows: [hi | lo] or the heads
+  static constexpr int kGroupHeads = 16 / kParts;      // heads per softmax group of four warps
+  static constexpr int kSoftWarps = kQN / 4;
   static constexpr int kSoftThreads = 32 * kSoftWarps;
   static constexpr int kThreads = kSoftThreads + 6 * 32;   // + ring A, ring B, 2 score, 2 PV
   static constexpr int kSlotsA = kG == 16 ? 6 : 4;
@@ -104,7 +113,6 @@ struct TcPlan {
   static constexpr int kPBufs = kG == 16 ? 2 : 1;
   static constexpr int kOBufs = kPersist ? 2 : 1;      // O^T accumulators in tensor memory
   static constexpr int kItems = kPersist ? kMaxItems : 1;
-  static constexpr int kQN = 2 * kG;                   // hi | lo query rows
   static constexpr int kQBoxBytes = kQN * 128;
   static constexpr int kPSub = kQN * 128;              // P^T: 64 tile rows of kQN rows
   static constexpr int kPBytes = 2 * kPSub;            // 128 tile rows
@@ -333,7 +341,8 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
   // The plan's sizes under the names the body uses (kHeadGroup: heads per CTA).
   using L = TcPlan<kG, kPersist>;
   static_assert(!kPersist || kG == 16, "the persistent instance takes 16 heads per CTA");
-  constexpr int kHeadGroup = kG, kHalfHeads = 8, kSoftWarps = L::kSoftWarps;
+  constexpr int kHeadGroup = kG, kGroupHeads = L::kGroupHeads, kSoftWarps = L::kSoftWarps;
+  constexpr int kParts = L::kParts;
   constexpr int kSoftThreads = L::kSoftThreads, kSlotsA = L::kSlotsA, kSlotsB = L::kSlotsB;
   constexpr int kPBufs = L::kPBufs, kQN = L::kQN, kQBoxBytes = L::kQBoxBytes, kPSub = L::kPSub;
   constexpr int kPBytes = L::kPBytes, kOffA = L::kOffA, kOffB = L::kOffB, kOffQ = L::kOffQ;
@@ -558,21 +567,24 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
                             : (k < 2 ? kOffQ : kOffB) + (k & 1) * kBoxBytes;
   };
 
-  // Query rows of the score MMA's B operand (K-major, 128-byte swizzle, one 4 KB
-  // box per 64 columns): row n < kG is bf16(q) of head n, row kG + n is
-  // bf16(q - bf16(q)).  q_abs[v, h0..h0+kG-1, :] and q_pe[v, h0.., :] are
-  // contiguous; each softmax thread loads nine float4 before converting them.
+  // Query rows of the score MMA's B operand (K-major, 128-byte swizzle, one box
+  // of kQN rows per 64 columns): with two parts row n < kG is bf16(q) of head n
+  // and row kG + n is bf16(q - bf16(q)); with one part row n is bf16(q) of head
+  // n.  q_abs[v, h0..h0+kG-1, :] and q_pe[v, h0.., :] are contiguous; each
+  // softmax thread loads nine float4 at a time before converting them.
   auto load_query = [&](int v, int h0) {
     const float4* qa = reinterpret_cast<const float4*>(static_cast<const float*>(p.q_abs) +
                                                        (size_t(v) * p.H + h0) * kDc);
     const float4* qp = reinterpret_cast<const float4*>(static_cast<const float*>(p.q_pe) +
                                                        (size_t(v) * p.H + h0) * kDr);
     constexpr int kNA = kHeadGroup * kDc / 4, kNQ = kNA + kHeadGroup * kDr / 4;
-    static_assert(kNQ == 9 * kSoftThreads, "nine float4 per softmax thread");
+    static_assert(kNQ % (9 * kSoftThreads) == 0, "nine float4 per softmax thread and pass");
+#pragma unroll 1
+    for (int pass = 0; pass < kNQ / (9 * kSoftThreads); ++pass) {
     float4 q4[9];
 #pragma unroll
     for (int i = 0; i < 9; ++i) {
-      const int idx = tid + i * kSoftThreads;
+      const int idx = tid + (9 * pass + i) * kSoftThreads;
       // the query row (v', h) this load belongs to, for the index check
       const int n = idx < kNA ? idx / (kDc / 4) : (idx - kNA) / (kDr / 4);
       const size_t row = pair ? size_t(v + n / 16) * p.H + h0 + n % 16 : size_t(v) * p.H + h0 + n;
@@ -590,7 +602,7 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
     }
 #pragma unroll
     for (int i = 0; i < 9; ++i) {
-      const int idx = tid + i * kSoftThreads;
+      const int idx = tid + (9 * pass + i) * kSoftThreads;
       const int h = idx < kNA ? idx / (kDc / 4) : (idx - kNA) / (kDr / 4);
       const int k = idx < kNA ? 4 * (idx % (kDc / 4)) : kDc + 4 * ((idx - kNA) % (kDr / 4));
       uint2 hi, lo;
@@ -599,10 +611,12 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
       const int box = k >> 6, ch = (k & 63) >> 3, w = k & 7;
       const uint32_t o_hi = box * kQBoxBytes + sw128(h, ch) + 2 * w;
       const uint32_t o_lo = box * kQBoxBytes + sw128(h + kHeadGroup, ch) + 2 * w;
-      if (MLA_IN_BOUNDS(o_hi + 8 <= 9u * kQBoxBytes && o_lo + 8 <= 9u * kQBoxBytes)) {
+      if (MLA_IN_BOUNDS(o_hi + 8 <= 9u * kQBoxBytes &&
+                        (kParts == 1 || o_lo + 8 <= 9u * kQBoxBytes))) {
         *reinterpret_cast<uint2*>(smem + kOffQ + o_hi) = hi;
-        *reinterpret_cast<uint2*>(smem + kOffQ + o_lo) = lo;
+        if (kParts == 2) *reinterpret_cast<uint2*>(smem + kOffQ + o_lo) = lo;
       }
+    }
     }
     fence_proxy_async_smem();
   };
@@ -877,12 +891,12 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
   } else if (warp < kSoftWarps) {
     // ------------------------------------------------------------ softmax warps
     const int gp = warp >> 2, wq = warp & 3;
-    const int hb = kHalfHeads * gp;                     // first head of this group
+    const int hb = kGroupHeads * gp;                     // first head of this group
     const int row = 32 * wq + lane;                     // tile row held by this thread
     const uint32_t lane_base = static_cast<uint32_t>(32 * wq) << 16;
-    float m[kHalfHeads], l[kHalfHeads];
+    float m[kGroupHeads], l[kGroupHeads];
 #pragma unroll
-    for (int h = 0; h < kHalfHeads; ++h) {
+    for (int h = 0; h < kGroupHeads; ++h) {
       m[h] = -INFINITY;
       l[h] = 0.f;
     }
@@ -891,12 +905,13 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
     auto finish_item = [&](int idx, int t_end, const float* mm, const float* ll, bool last) {
       const SplitItem it = items[idx];
       const uint32_t ocol = obuf_col(idx);
-      {
-        float tt[kHalfHeads];
 #pragma unroll
-        for (int h = 0; h < kHalfHeads; ++h) tt[h] = ll[h];
+      for (int e = 0; e < kGroupHeads; e += 8) {
+        float tt[8];
+#pragma unroll
+        for (int h = 0; h < 8; ++h) tt[h] = ll[e + h];
         const float ws = reduce8_heads<false>(tt, lane);
-        if (lane < 16 && (lane & 1) == 0) lsum[(hb + (lane >> 1)) * 4 + wq] = ws;
+        if (lane < 16 && (lane & 1) == 0) lsum[(hb + e + (lane >> 1)) * 4 + wq] = ws;
       }
       // O^T after the item's last PV: this thread's latent row is d = 128 mb + 32 wq + lane.
       wait_or_abort(bar(BAR_ODONE + (t_end & 1)), (t_end >> 1) & 1, abort_flag, wait_ns);
@@ -907,14 +922,14 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
         // Row (v, h, j) of the partials; heads h0 + hw + h are p.splits rows apart
         // (paired tokens: groups 2 and 3 belong to query group v + 1).
         const size_t base = size_t(it.part) + (pair ? size_t(gp >> 1) * p.H * p.splits : 0);
-        const int hw = pair ? kHalfHeads * (gp & 1) : hb;
+        const int hw = pair ? kGroupHeads * (gp & 1) : hb;
         // 1/L by the approximate reciprocal (within 2 ulp for the L > 0 reached
         // here, 1 <= L <= 2^8 x rows): a branch-free instruction, where eight
         // IEEE divisions in a row cost about 0.4 us of the CTA's critical path.
         // Lane h of the first warp of each group writes head h's log-sum-exp.
-        float inv[kHalfHeads], Lme = 0.f, mme = 0.f;
+        float inv[kGroupHeads], Lme = 0.f, mme = 0.f;
 #pragma unroll
-        for (int h = 0; h < kHalfHeads; ++h) {
+        for (int h = 0; h < kGroupHeads; ++h) {
           const float4 q4 = *reinterpret_cast<const float4*>(lsum + (hb + h) * 4);
           const float Ls = (q4.x + q4.y) + (q4.z + q4.w);
           inv[h] = Ls > 0.f ? __fdividef(1.f, Ls) : 0.f;
@@ -922,25 +937,31 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
           mme = lane == h ? mm[h] : mme;
         }
         const size_t n_part = size_t(p.B) * p.H * p.splits;   // rows of the partials
-        if (wq == 0 && lane < kHalfHeads &&
+        if (wq == 0 && lane < kGroupHeads &&
             MLA_IN_BOUNDS(base + size_t(hw + lane) * p.splits < n_part))
           p.part_lse[base + size_t(hw + lane) * p.splits] =
               Lme > 0.f ? (mme + log2f(Lme)) * kLn2 : -INFINITY;
-        uint32_t hi4[4][8], lo4[4][8];
+        // Two parts: columns hb.. (hi) and kG + hb.. (lo) of each O^T block, summed;
+        // one part: columns hb..hb+15 (heads hb..hb+7, then hb+8..hb+15).
+        uint32_t x4[4][8], y4[4][8];
 #pragma unroll
         for (int mb = 0; mb < 4; ++mb) {
-          tmem_ld8_nowait(tmem + lane_base + ocol + kQN * mb + hb, hi4[mb]);
-          tmem_ld8_nowait(tmem + lane_base + ocol + kQN * mb + kHeadGroup + hb, lo4[mb]);
+          tmem_ld8_nowait(tmem + lane_base + ocol + kQN * mb + hb, x4[mb]);
+          tmem_ld8_nowait(tmem + lane_base + ocol + kQN * mb + (kParts == 2 ? kHeadGroup : 8) + hb,
+                          y4[mb]);
         }
         tmem_wait_ld();
         float* orow = p.part_o + (base + size_t(hw) * p.splits) * kDc + 32 * wq + lane;
         const size_t head_stride = size_t(p.splits) * kDc;
 #pragma unroll
-        for (int h = 0; h < kHalfHeads; ++h, orow += head_stride) {
+        for (int h = 0; h < kGroupHeads; ++h, orow += head_stride) {
           if (!MLA_IN_BOUNDS(base + size_t(hw + h) * p.splits < n_part)) continue;
 #pragma unroll
           for (int mb = 0; mb < 4; ++mb)
-            orow[128 * mb] = (__uint_as_float(hi4[mb][h]) + __uint_as_float(lo4[mb][h])) * inv[h];
+            orow[128 * mb] = (kParts == 2 ? __uint_as_float(x4[mb][h]) + __uint_as_float(y4[mb][h])
+                              : h < 8     ? __uint_as_float(x4[mb][h & 7])
+                                          : __uint_as_float(y4[mb][h & 7])) *
+                             inv[h];
         }
       }
       if (!last) {
@@ -953,7 +974,7 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
     Cursor c{0, items[0].tiles};
     int qk = 0;                  // query changes so far
     int pend = -1, pend_t = 0;   // item whose partial is still to be written, its last tile
-    float mp[kHalfHeads], lp[kHalfHeads];
+    float mp[kGroupHeads], lp[kGroupHeads];
     for (int t = 0; t < T; ++t) {
       seek(c, t);
       const SplitItem it = items[c.i];
@@ -966,26 +987,31 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
                     kTileRows);
       if (kMulti && first_t && t > 0) {
 #pragma unroll
-        for (int h = 0; h < kHalfHeads; ++h) {
+        for (int h = 0; h < kGroupHeads; ++h) {
           m[h] = -INFINITY;
           l[h] = 0.f;
         }
       }
       wait_or_abort(bar(BAR_SFULL + sb), (t >> 1) & 1, abort_flag, wait_ns);
       tc_fence_after();
-      float sc[kHalfHeads], tt[kHalfHeads];
+      float sc[kGroupHeads], tt[kGroupHeads];
       {
-        uint32_t hi0[8], lo0[8], hi1[8], lo1[8];
-        tmem_ld8_nowait(tmem + lane_base + kQN * sb + hb, hi0);
-        tmem_ld8_nowait(tmem + lane_base + kQN * sb + kHeadGroup + hb, lo0);
-        tmem_ld8_nowait(tmem + lane_base + kS1Col + kQN * sb + hb, hi1);
-        tmem_ld8_nowait(tmem + lane_base + kS1Col + kQN * sb + kHeadGroup + hb, lo1);
+        // Two parts: S = hi + lo columns of each accumulator; one part: columns
+        // hb..hb+7 and hb+8..hb+15 of each accumulator are 16 heads.
+        constexpr int kY = kParts == 2 ? kHeadGroup : 8;
+        uint32_t x0[8], y0[8], x1[8], y1[8];
+        tmem_ld8_nowait(tmem + lane_base + kQN * sb + hb, x0);
+        tmem_ld8_nowait(tmem + lane_base + kQN * sb + kY + hb, y0);
+        tmem_ld8_nowait(tmem + lane_base + kS1Col + kQN * sb + hb, x1);
+        tmem_ld8_nowait(tmem + lane_base + kS1Col + kQN * sb + kY + hb, y1);
         tmem_wait_ld();
         const bool rv = row < valid;
 #pragma unroll
-        for (int h = 0; h < kHalfHeads; ++h) {
-          const float s0 = __uint_as_float(hi0[h]) + __uint_as_float(lo0[h]);
-          const float s1 = __uint_as_float(hi1[h]) + __uint_as_float(lo1[h]);
+        for (int h = 0; h < kGroupHeads; ++h) {
+          const float s0 = kParts == 2 ? __uint_as_float(x0[h]) + __uint_as_float(y0[h])
+                                       : __uint_as_float(h < 8 ? x0[h & 7] : y0[h & 7]);
+          const float s1 = kParts == 2 ? __uint_as_float(x1[h]) + __uint_as_float(y1[h])
+                                       : __uint_as_float(h < 8 ? x1[h & 7] : y1[h & 7]);
           sc[h] = rv ? (s0 + s1) * p.scale_log2 : -INFINITY;
           tt[h] = sc[h];
         }
@@ -994,13 +1020,16 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(BAR_SFREE + sb));
       float* rd = red + sb * kHeadGroup * 4;
-      const float wmax = reduce8_heads<true>(tt, lane);
-      if (lane < 16 && (lane & 1) == 0) rd[(hb + (lane >> 1)) * 4 + wq] = wmax;
+#pragma unroll
+      for (int e = 0; e < kGroupHeads; e += 8) {
+        const float wmax = reduce8_heads<true>(tt + e, lane);
+        if (lane < 16 && (lane & 1) == 0) rd[(hb + e + (lane >> 1)) * 4 + wq] = wmax;
+      }
       named_bar_sync(1, kSoftThreads);
       bool need = false;
-      float tmax[kHalfHeads];
+      float tmax[kGroupHeads];
 #pragma unroll
-      for (int h = 0; h < kHalfHeads; ++h) {
+      for (int h = 0; h < kGroupHeads; ++h) {
         const float4 q4 = *reinterpret_cast<const float4*>(rd + (hb + h) * 4);
         tmax[h] = fmaxf(fmaxf(q4.x, q4.y), fmaxf(q4.z, q4.w));
         need |= tmax[h] > m[h] + kRescaleLog2;
@@ -1009,9 +1038,9 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
         // Move this group's reference maxima; rescale its row sums and the O^T
         // columns it owns (in TMEM, after the previous PV finished).  The first
         // tile of an item starts from nothing (its first PV overwrites).
-        float alpha[kHalfHeads];
+        float alpha[kGroupHeads];
 #pragma unroll
-        for (int h = 0; h < kHalfHeads; ++h) {
+        for (int h = 0; h < kGroupHeads; ++h) {
           const float mn = fmaxf(m[h], tmax[h]);
           alpha[h] = m[h] == -INFINITY ? 0.f : ex2(m[h] - mn);
           m[h] = mn;
@@ -1025,13 +1054,16 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
           for (int mb = 0; mb < 4; ++mb) {
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-              const uint32_t col = ocol + kQN * mb + kHeadGroup * half + hb;
+              // two parts: hi (half 0) and lo (half 1) of 8 heads; one part: heads
+              // hb.. (half 0) and hb+8.. (half 1)
+              const uint32_t col = ocol + kQN * mb + (kParts == 2 ? kHeadGroup : 8) * half + hb;
+              const int a0 = kParts == 2 ? 0 : 8 * half;
               uint32_t r[8];
               float o[8];
               tmem_ld8_nowait(tmem + lane_base + col, r);
               tmem_wait_ld();
 #pragma unroll
-              for (int h = 0; h < kHalfHeads; ++h) o[h] = __uint_as_float(r[h]) * alpha[h];
+              for (int h = 0; h < 8; ++h) o[h] = __uint_as_float(r[h]) * alpha[a0 + h];
               tmem_st8(tmem + lane_base + col, o);
             }
           }
@@ -1039,7 +1071,7 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
         }
       }
 #pragma unroll
-      for (int h = 0; h < kHalfHeads; ++h) {
+      for (int h = 0; h < kGroupHeads; ++h) {
         const float mu = m[h] == -INFINITY ? 0.f : m[h];
         sc[h] = ex2(sc[h] - mu);
         l[h] += sc[h];
@@ -1050,20 +1082,22 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
                       wait_ns);
       {
         // P^T (B operand of the PV MMA, K-major 128-byte swizzle, two 64-row
-        // halves): row n < 16 is bf16(p) of head n, row 16 + n is
-        // bf16(p - bf16(p)); the K index is the tile row.
+        // halves): two parts: row n < kG is bf16(p) of head n, row kG + n is
+        // bf16(p - bf16(p)); one part: row n is bf16(p) of head n.  The K index
+        // is the tile row.
         const uint32_t pofs = (t % kPBufs) * kPBytes + (row >> 6) * kPSub;
         uint8_t* pbuf = smem + kOffP + pofs;
         const int ch = (row & 63) >> 3, w = row & 7;
 #pragma unroll
-        for (int h = 0; h < kHalfHeads; ++h) {
+        for (int h = 0; h < kGroupHeads; ++h) {
           const __nv_bfloat16 hi = __float2bfloat16_rn(sc[h]);
           const __nv_bfloat16 lo = __float2bfloat16_rn(sc[h] - __bfloat162float(hi));
-          if (!MLA_IN_BOUNDS(pofs + sw128(kHeadGroup + hb + h, ch) + 2 * w + 2 <=
-                             uint32_t(kPBufs * kPBytes)))
+          const int top = kParts == 2 ? kHeadGroup + hb + h : hb + h;   // highest row written
+          if (!MLA_IN_BOUNDS(pofs + sw128(top, ch) + 2 * w + 2 <= uint32_t(kPBufs * kPBytes)))
             continue;
           *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128(hb + h, ch) + 2 * w) = hi;
-          *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128(kHeadGroup + hb + h, ch) + 2 * w) = lo;
+          if (kParts == 2)
+            *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128(kHeadGroup + hb + h, ch) + 2 * w) = lo;
         }
       }
       fence_proxy_async_smem();
@@ -1160,7 +1194,7 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
         pend = c.i;
         pend_t = t;
 #pragma unroll
-        for (int h = 0; h < kHalfHeads; ++h) {
+        for (int h = 0; h < kGroupHeads; ++h) {
           mp[h] = m[h];
           lp[h] = l[h];
         }
@@ -1550,7 +1584,9 @@ __global__ void __launch_bounds__(128)
 // Heads per CTA of the decode kernel: 32 for a bf16 cache whose head count
 // allows it, else 16 (the FP8 kernel always takes 16).
 int tc_heads_per_cta(const mla_dims* d) {
-  return d->dtype == MLA_BF16 && d->heads % 32 == 0 ? 32 : kHeadGroup;
+  if (d->dtype != MLA_BF16) return kHeadGroup;
+  if (d->heads % 64 == 0 && g_split_parts.load() != 2) return 64;
+  return d->heads % 32 == 0 ? 32 : kHeadGroup;
 }
 
 // Whether the bf16 kernel pairs the tokens of a multi-token step: with fewer
@@ -1800,6 +1836,20 @@ static std::atomic<int> g_hook_stop_tiles{0};
 static std::atomic<int32_t*> g_hook_debug{nullptr};
 extern "C" void mla_test_set_split_form(int32_t form) { g_split_form.store(form); }
 
+extern "C" mla_status mla_set_split_parts(int32_t parts) {
+  if (parts != 0 && parts != 2) {
+    set_error("mla_set_split_parts: parts must be 0 (the library's choice) or 2 (hi + lo)");
+    return MLA_ERR_INVALID_ARG;
+  }
+  g_split_parts.store(parts);
+  return MLA_OK;
+}
+
+extern "C" int32_t mla_decode_heads_per_cta(const mla_dims* dims) {
+  if (check_dims(dims, "mla_decode_heads_per_cta") != MLA_OK) return 0;
+  return dims->dtype == MLA_F32 ? 1 : tc_heads_per_cta(dims);
+}
+
 extern "C" void mla_test_set_split_debug(int32_t* records) { g_hook_debug.store(records); }
 
 extern "C" void mla_test_set_split_hooks(uint64_t wait_ns, int32_t stop_after_tiles) {
@@ -1917,9 +1967,10 @@ static mla_status decode_split(const char* who, const mla_dims* dims, int q_len,
         return MLA_ERR_CUDA;
       }
     }
-    st = p.tpc == 2 || tc_heads_per_cta(dims) == 32
-             ? launch_split_tc<32, false>(tmap, tmap_half, p, dims->heads, s, who)
-             : p.persist ? launch_split_tc<16, true>(tmap, tmap_half, p, dims->heads, s, who)
+    const int per_cta = p.tpc == 2 ? 32 : tc_heads_per_cta(dims);
+    st = per_cta == 64   ? launch_split_tc<64, false>(tmap, tmap_half, p, dims->heads, s, who)
+         : per_cta == 32 ? launch_split_tc<32, false>(tmap, tmap_half, p, dims->heads, s, who)
+         : p.persist     ? launch_split_tc<16, true>(tmap, tmap_half, p, dims->heads, s, who)
                          : launch_split_tc<16, false>(tmap, tmap_half, p, dims->heads, s, who);
     if (st != MLA_OK) return st;
   } else {

@@ -454,6 +454,36 @@ const char* mla_last_error_message(void);
 void mla_set_launch_overlap(int32_t enable);
 
 /*
+ * mla_set_split_parts -- how the bf16 split kernel hands the fp32 absorbed
+ * query and the softmax weights P to the tensor core (bf16 operands, fp32
+ * accumulation in both forms).
+ *
+ *   0 (default)  the library's choice: where the head count is a multiple of
+ *                64, one bf16 part each (round to nearest), 64 heads per CTA;
+ *                otherwise two parts, as below.
+ *   2            two parts at every head count: bf16(x) and bf16(x - bf16(x)),
+ *                a rounding near 2^-17 relative (32 heads per CTA where the
+ *                head count is a multiple of 32, else 16).
+ *
+ * One part rounds each query element and weight to bf16 (2^-9 relative): on
+ * the V3 shape with N(0,1) rows and N(0,0.02^2) weights (Multi-Head Latent
+ * Attention, 3.1: 128 heads) o_c stays near 2e-3 relative L2 of the exact
+ * result, and the CTAs that read each cache row are halved.  Rows of large
+ * magnitude (scores spread over tens of units) want two parts.  Process-wide,
+ * read when a split is enqueued (a graph keeps the form of its capture).
+ * Returns MLA_OK, or MLA_ERR_INVALID_ARG for another value.
+ */
+mla_status mla_set_split_parts(int32_t parts);
+
+/*
+ * mla_decode_heads_per_cta -- heads each CTA of the split kernel takes for
+ * these dims under the current mla_set_split_parts: 64 (one bf16 part), 32 or
+ * 16 (two parts) for a bf16 cache, 16 for FP8 (four and three E4M3 parts), 1
+ * for fp32.  Returns 0 for invalid dims.
+ */
+int32_t mla_decode_heads_per_cta(const mla_dims* dims);
+
+/*
  * The checked build.  Compiled with -DMLA_CHECK (the package's
  * build(check=True) writes it beside the default library as
  * libmla_gb300_check.so), the kernels of mla_decode_attn and of

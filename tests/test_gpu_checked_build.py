@@ -46,24 +46,31 @@ def small(B, H, S, **kw):
                      hidden=2048, **kw)
 
 
-CASES = [
-    (small(3, 16, 300), [1, 129, 300], 0),
-    (small(3, 16, 300), [7, 255, 300], 3),
-    (small(2, 32, 300), [300, 137], 4),
-    (small(2, 128, 200), [200, 61], 2),
-    (small(24, 16, 1024), None, 8),       # persistent grid
-    (small(20, 48, 600), None, 4),        # persistent, head groups
+CASES = [   # (config, lengths, chunks requested, operand parts: 0 default, 2 hi + lo)
+    (small(3, 16, 300), [1, 129, 300], 0, 0),
+    (small(3, 16, 300), [7, 255, 300], 3, 0),
+    (small(2, 32, 300), [300, 137], 4, 0),
+    (small(2, 128, 200), [200, 61], 2, 0),   # 64 heads per CTA, one part
+    (small(2, 128, 200), [200, 61], 2, 2),   # 32 heads per CTA, hi + lo
+    (small(3, 64, 520), [520, 385, 1], 1, 0),
+    (small(24, 16, 1024), None, 8, 0),       # persistent grid
+    (small(20, 48, 600), None, 4, 0),        # persistent, head groups
 ]
 
 
 @pytest.mark.parametrize("case", range(len(CASES)))
 def test_small_cases_under_index_checks(checked, case):
+    from head_latent_attention_absorbed_gb300 import _binding
     lib, flags = checked
-    cfg, lengths, splits = CASES[case]
+    cfg, lengths, splits, parts = CASES[case]
     flags.zero_()
     lens = torch.tensor(lengths, dtype=torch.int32) if lengths else None
     inp = make_inputs(cfg, seed=90 + case, poison_tail=True, lengths=lens)
-    gpu = run_cuda(inp, num_splits=splits)
+    _binding.set_split_parts(parts)
+    try:
+        gpu = run_cuda(inp, num_splits=splits)
+    finally:
+        _binding.set_split_parts(0)
     torch.cuda.synchronize()
     assert int(flags.item()) == 0, "an index check failed"
     assert gpu["status"] == 0

@@ -20,7 +20,7 @@ from workloads import MlaConfig, make_inputs
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("H", [16, 32])
+@pytest.mark.parametrize("H", [16, 32, 64])
 def test_bounded_waits_run_out_and_report(cuda_lib, H):
     mla = cuda_lib
     lib = mla.load()

@@ -163,3 +163,24 @@ def test_multi_token_planning_counts_paired_ctas(lib):
     for dd, q in ((d, 3), (mla.dims(8, 16, 4096, mla.MLA_FP8_E4M3), 4),
                   (mla.dims(8, 32, 4096, mla.MLA_BF16), 4)):
         assert mla.multi_num_splits(dd, q, 0) == mla.num_splits(mla.query_dims(dd, q), 0)
+
+
+def test_split_parts_switch(lib):
+    """Heads per split CTA under mla_set_split_parts (host logic, no GPU): one
+    bf16 part and 64 heads per CTA at multiples of 64 heads by default, hi + lo
+    parts (32 or 16 heads) when asked; other values are refused."""
+    mla, so = lib
+    hp = lambda H, dt=mla.MLA_BF16: so.mla_decode_heads_per_cta(ctypes.byref(mla.dims(2, H, 256, dt)))
+    try:
+        assert [hp(H) for H in (16, 32, 48, 64, 128, 192)] == [16, 32, 16, 64, 64, 64]
+        assert hp(128, mla.MLA_FP8_E4M3) == 16 and hp(128, mla.MLA_F32) == 1
+        assert so.mla_set_split_parts(1) == 1 and so.mla_set_split_parts(-3) == 1
+        assert hp(128) == 64                               # a refused value changes nothing
+        assert so.mla_set_split_parts(2) == 0
+        assert [hp(H) for H in (16, 32, 48, 64, 128)] == [16, 32, 16, 32, 32]
+        # the planner counts the CTAs of the form in force
+        d = mla.dims(32, 128, 16384, mla.MLA_BF16)
+        assert mla.num_splits(d, 0) >= 1
+    finally:
+        so.mla_set_split_parts(0)
+    assert so.mla_decode_heads_per_cta(ctypes.byref(mla.dims(0, 16, 64, mla.MLA_BF16))) == 0
