@@ -212,29 +212,42 @@ __device__ void plan_items(const SplitParams& p, SplitItem* items, volatile int*
                            int lane) {
   const int groups = p.H / 16, ct = p.chunk / kTileRows;
   const long long G = gridDim.x, c = blockIdx.x;
+  // Lengths of the first 32 query groups, one load per lane, kept for both passes.
+  const int len_lane = lane < p.B ? clamp_length(p, lane, c == 0) : 0;
+  auto length_of = [&](int v0, bool report_it) {
+    const int v = v0 + lane;
+    return v0 == 0 ? len_lane : v < p.B ? clamp_length(p, v, report_it) : 0;
+  };
+  // Non-negative quotients; 32-bit division when both operands fit (the
+  // planner's tile counts always do in practice; 64-bit division is a long
+  // subroutine on the CTA's start-up path).
+  auto quot = [](long long a, long long b) {
+    return a <= 0x7fffffffll && b <= 0x7fffffffll
+               ? static_cast<long long>(static_cast<uint32_t>(a) / static_cast<uint32_t>(b))
+               : a / b;
+  };
   // Tiles of one head group: the sum over query groups of ceil(len / 128).
   long long tg = 0;
   for (int v0 = 0; v0 < p.B; v0 += 32) {
-    const int v = v0 + lane;
-    const int len = v < p.B ? clamp_length(p, v, c == 0) : 0;
+    const int len = length_of(v0, c == 0);
     int tot;
     warp_exclusive_scan((len + kTileRows - 1) / kTileRows, lane, &tot);
     tg += tot;
   }
-  const long long TT = groups * tg, lo = c * TT / G, hi = (c + 1) * TT / G;
+  const long long TT = groups * tg, lo = quot(c * TT, G), hi = quot((c + 1) * TT, G);
   int n = 0;
   long long base = 0;   // first tile of the current block of query groups
   for (int g = 0; g < groups && base < hi; ++g) {
     for (int v0 = 0; v0 < p.B && base < hi; v0 += 32) {
       const int v = v0 + lane;
-      const int len = v < p.B ? clamp_length(p, v, false) : 0;
+      const int len = length_of(v0, false);
       const int tiles = (len + kTileRows - 1) / kTileRows;
       int tot;
       const long long s = base + warp_exclusive_scan(tiles, lane, &tot);   // its first tile
       // chunks j of this query group whose first tile s + j ct is in [lo, hi)
       const int nch = (tiles + ct - 1) / ct;
-      long long jlo = lo > s ? (lo - s + ct - 1) / ct : 0;
-      long long jhi = hi > s ? (hi - s + ct - 1) / ct : 0;
+      long long jlo = lo > s ? quot(lo - s + ct - 1, ct) : 0;
+      long long jhi = hi > s ? quot(hi - s + ct - 1, ct) : 0;
       jlo = jlo < nch ? jlo : nch;
       jhi = jhi < nch ? jhi : nch;
       const int cnt = jhi > jlo ? static_cast<int>(jhi - jlo) : 0;
@@ -394,33 +407,105 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
   // another) before the CTA-wide barrier.  In a one-wave grid they need only the
   // chunk's first row and go out before the sequence length is known.
   const uint64_t keep = l2_evict_last_policy();   // read again by ring B
-  auto first_fills = [&](int row) {
-    for (int i = 0; i < kSlotsA; ++i) {
-      mbar_init(bar(BAR_FULLA + i), 1);
-      mbar_init(bar(BAR_EMPTYA + i), 1);
+  // Boxes [from, to) of the first fills; from == 0 also sets up ring A's barriers.
+  auto first_fills = [&](int row, int from = 0, int to = -1) {
+    if (to < 0) to = kSlotsA;
+    if (from == 0) {
+      for (int i = 0; i < kSlotsA; ++i) {
+        mbar_init(bar(BAR_FULLA + i), 1);
+        mbar_init(bar(BAR_EMPTYA + i), 1);
+      }
+      fence_mbarrier_init();
+      prefetch_tmap(&tmap);
     }
-    fence_mbarrier_init();
-    prefetch_tmap(&tmap);
-    for (int pos = 0; pos < kSlotsA; ++pos) {
+    for (int pos = from; pos < to; ++pos) {
       mbar_arrive_expect_tx(bar(BAR_FULLA + pos), kBoxBytes);
       if (MLA_IN_BOUNDS(row >= 0 && row < cache_rows))
         tma_load_2d(sbase + kOffA + pos * kBoxBytes, &tmap, 64 * pos, row,
                     bar(BAR_FULLA + pos), keep);
     }
   };
+  // Query rows of the score MMA's B operand (K-major, 128-byte swizzle, one box
+  // of kQN rows per 64 columns): with two parts row n < kG is bf16(q) of head n
+  // and row kG + n is bf16(q - bf16(q)); with one part row n is bf16(q) of head
+  // n.  q_abs[v, h0..h0+kG-1, :] and q_pe[v, h0.., :] are contiguous; each
+  // softmax thread loads nine float4 at a time before converting them.
+  // signal: arrive on named barrier 3 once the first pass's loads are issued.
+  auto load_query = [&](int v, int h0, bool signal = false) {
+    const float4* qa = reinterpret_cast<const float4*>(static_cast<const float*>(p.q_abs) +
+                                                       (size_t(v) * p.H + h0) * kDc);
+    const float4* qp = reinterpret_cast<const float4*>(static_cast<const float*>(p.q_pe) +
+                                                       (size_t(v) * p.H + h0) * kDr);
+    constexpr int kNA = kHeadGroup * kDc / 4, kNQ = kNA + kHeadGroup * kDr / 4;
+    static_assert(kNQ % (9 * kSoftThreads) == 0, "nine float4 per softmax thread and pass");
+#pragma unroll 1
+    for (int pass = 0; pass < kNQ / (9 * kSoftThreads); ++pass) {
+    float4 q4[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      const int idx = tid + (9 * pass + i) * kSoftThreads;
+      // the query row (v', h) this load belongs to, for the index check
+      const int n = idx < kNA ? idx / (kDc / 4) : (idx - kNA) / (kDr / 4);
+      const size_t row = pair ? size_t(v + n / 16) * p.H + h0 + n % 16 : size_t(v) * p.H + h0 + n;
+      q4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (!MLA_IN_BOUNDS(row < size_t(p.B) * p.H)) continue;
+      if (pair) {
+        // column n: head h0 + n % 16 of query group v + n / 16
+        q4[i] = idx < kNA ? reinterpret_cast<const float4*>(static_cast<const float*>(p.q_abs) +
+                                                            row * kDc)[idx % (kDc / 4)]
+                          : reinterpret_cast<const float4*>(static_cast<const float*>(p.q_pe) +
+                                                            row * kDr)[(idx - kNA) % (kDr / 4)];
+      } else {
+        q4[i] = idx < kNA ? qa[idx] : qp[idx - kNA];
+      }
+    }
+    if (signal && pass == 0) named_bar_arrive(3, kSoftThreads + 32);
+#pragma unroll
+    for (int i = 0; i < 9; ++i) {
+      const int idx = tid + (9 * pass + i) * kSoftThreads;
+      const int h = idx < kNA ? idx / (kDc / 4) : (idx - kNA) / (kDr / 4);
+      const int k = idx < kNA ? 4 * (idx % (kDc / 4)) : kDc + 4 * ((idx - kNA) % (kDr / 4));
+      uint2 hi, lo;
+      split_bf16(q4[i].x, q4[i].y, hi.x, lo.x);
+      split_bf16(q4[i].z, q4[i].w, hi.y, lo.y);
+      const int box = k >> 6, ch = (k & 63) >> 3, w = k & 7;
+      const uint32_t o_hi = box * kQBoxBytes + sw128(h, ch) + 2 * w;
+      const uint32_t o_lo = box * kQBoxBytes + sw128(h + kHeadGroup, ch) + 2 * w;
+      if (MLA_IN_BOUNDS(o_hi + 8 <= 9u * kQBoxBytes &&
+                        (kParts == 1 || o_lo + 8 <= 9u * kQBoxBytes))) {
+        *reinterpret_cast<uint2*>(smem + kOffQ + o_hi) = hi;
+        if (kParts == 2) *reinterpret_cast<uint2*>(smem + kOffQ + o_lo) = lo;
+      }
+    }
+    }
+    fence_proxy_async_smem();
+  };
   const bool ring_a = warp == kWarpA && lane == 0;
   int len_first = 0, len_pair = 0;   // paired tokens: rows of the earlier and later token
   int r0_one = 0;                    // one-item CTA: the chunk's first row in its sequence
+  int qv0 = 0, qh0 = 0;              // query group and first head of the CTA's first item
   if (persist) {
     if (warp == kWarpA) plan_items(p, items, counts, lane);
     __syncthreads();
     if (counts[0] == 0) return;   // no tile for this CTA
-    if (ring_a) first_fills(items[0].row0);
+    qv0 = items[0].qv;
+    qh0 = items[0].h0;
+    // Two boxes at once; the other first boxes once the softmax warps have
+    // issued the query's loads (named barrier 3), so that those do not queue
+    // behind every CTA's first-fill burst.
+    if (warp == kWarpA) {
+      if (lane == 0) first_fills(items[0].row0, 0, 2);
+      __syncwarp();
+      named_bar_sync(3, kSoftThreads + 32);
+      if (lane == 0) first_fills(items[0].row0, 2, kSlotsA);
+    }
   } else {
     const int g = blockIdx.x, j = blockIdx.y, b = pair ? 2 * blockIdx.z : blockIdx.z;
     const int r0 = j * p.chunk;
     r0_one = r0;
     const int row_base = cache_seq(p, b) * p.s_max + r0;
+    qv0 = b;
+    qh0 = g * (pair ? kHeadGroup / 2 : kHeadGroup);
     if (ring_a && p.fill_early) first_fills(row_base);
     // Launched after mla_absorb_q with programmatic serialization: everything up
     // to the query load (set-up, TMEM, the cache stream) overlaps that kernel.
@@ -447,7 +532,7 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
       m.t0 = 0;
       m.valid_last = r1 - (r0 + (nt - 1) * kTileRows);
       m.zero_from = len - (r0 + (nt - 1) * kTileRows);
-      m.h0 = g * (pair ? kHeadGroup / 2 : kHeadGroup);
+      m.h0 = qh0;
       m.part = (b * p.H + m.h0) * p.splits + j;
       m.qv = b;
       items[0] = m;
@@ -488,6 +573,16 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
   if (warp == kWarpA) {
     __syncwarp();
     tmem_alloc(smem_u32(slot_ptr), kTmemCols);
+  }
+  // The first item's query comes from the previous kernel of the stream
+  // (mla_absorb_q).  A persistent CTA loads it while the other roles set up, so
+  // that it is in place when the CTA-wide barrier below passes (its first boxes
+  // are in flight by then); a one-item CTA loads it after that barrier, so that
+  // under programmatic launch the set-up and ring B do not wait for the
+  // previous kernel, and its query loads do not join the first boxes' burst.
+  if (kPersist && warp < kSoftWarps) {
+    pdl_wait();
+    load_query(qv0, qh0, true);
   }
   tc_fence_before();
   __syncthreads();
@@ -567,59 +662,6 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
                             : (k < 2 ? kOffQ : kOffB) + (k & 1) * kBoxBytes;
   };
 
-  // Query rows of the score MMA's B operand (K-major, 128-byte swizzle, one box
-  // of kQN rows per 64 columns): with two parts row n < kG is bf16(q) of head n
-  // and row kG + n is bf16(q - bf16(q)); with one part row n is bf16(q) of head
-  // n.  q_abs[v, h0..h0+kG-1, :] and q_pe[v, h0.., :] are contiguous; each
-  // softmax thread loads nine float4 at a time before converting them.
-  auto load_query = [&](int v, int h0) {
-    const float4* qa = reinterpret_cast<const float4*>(static_cast<const float*>(p.q_abs) +
-                                                       (size_t(v) * p.H + h0) * kDc);
-    const float4* qp = reinterpret_cast<const float4*>(static_cast<const float*>(p.q_pe) +
-                                                       (size_t(v) * p.H + h0) * kDr);
-    constexpr int kNA = kHeadGroup * kDc / 4, kNQ = kNA + kHeadGroup * kDr / 4;
-    static_assert(kNQ % (9 * kSoftThreads) == 0, "nine float4 per softmax thread and pass");
-#pragma unroll 1
-    for (int pass = 0; pass < kNQ / (9 * kSoftThreads); ++pass) {
-    float4 q4[9];
-#pragma unroll
-    for (int i = 0; i < 9; ++i) {
-      const int idx = tid + (9 * pass + i) * kSoftThreads;
-      // the query row (v', h) this load belongs to, for the index check
-      const int n = idx < kNA ? idx / (kDc / 4) : (idx - kNA) / (kDr / 4);
-      const size_t row = pair ? size_t(v + n / 16) * p.H + h0 + n % 16 : size_t(v) * p.H + h0 + n;
-      q4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (!MLA_IN_BOUNDS(row < size_t(p.B) * p.H)) continue;
-      if (pair) {
-        // column n: head h0 + n % 16 of query group v + n / 16
-        q4[i] = idx < kNA ? reinterpret_cast<const float4*>(static_cast<const float*>(p.q_abs) +
-                                                            row * kDc)[idx % (kDc / 4)]
-                          : reinterpret_cast<const float4*>(static_cast<const float*>(p.q_pe) +
-                                                            row * kDr)[(idx - kNA) % (kDr / 4)];
-      } else {
-        q4[i] = idx < kNA ? qa[idx] : qp[idx - kNA];
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 9; ++i) {
-      const int idx = tid + (9 * pass + i) * kSoftThreads;
-      const int h = idx < kNA ? idx / (kDc / 4) : (idx - kNA) / (kDr / 4);
-      const int k = idx < kNA ? 4 * (idx % (kDc / 4)) : kDc + 4 * ((idx - kNA) % (kDr / 4));
-      uint2 hi, lo;
-      split_bf16(q4[i].x, q4[i].y, hi.x, lo.x);
-      split_bf16(q4[i].z, q4[i].w, hi.y, lo.y);
-      const int box = k >> 6, ch = (k & 63) >> 3, w = k & 7;
-      const uint32_t o_hi = box * kQBoxBytes + sw128(h, ch) + 2 * w;
-      const uint32_t o_lo = box * kQBoxBytes + sw128(h + kHeadGroup, ch) + 2 * w;
-      if (MLA_IN_BOUNDS(o_hi + 8 <= 9u * kQBoxBytes &&
-                        (kParts == 1 || o_lo + 8 <= 9u * kQBoxBytes))) {
-        *reinterpret_cast<uint2*>(smem + kOffQ + o_hi) = hi;
-        if (kParts == 2) *reinterpret_cast<uint2*>(smem + kOffQ + o_lo) = lo;
-      }
-    }
-    }
-    fence_proxy_async_smem();
-  };
 
   if (warp == kWarpA) {
     // ------------------------------------------------------------ ring A (HBM)
@@ -727,14 +769,14 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
           if (armed_x >> k & 1u) drain_phase(bar(BAR_FULLX + k), 0, wait_ns);
       }
     }
-  } else if (warp < kSoftWarps || warp == kWarpS0 || warp == kWarpS1) {
-    // The first item's query.  It comes from the previous kernel of the stream
-    // (mla_absorb_q).
+  } else if (!kPersist && (warp < kSoftWarps || warp == kWarpS0 || warp == kWarpS1)) {
+    // A one-item CTA's query (see above), then the softmax warps and the score
+    // issuers meet: query in place.
     if (warp < kSoftWarps) {
       pdl_wait();
-      load_query(items[0].qv, items[0].h0);
+      load_query(qv0, qh0);
     }
-    named_bar_sync(2, kSoftThreads + 64);   // softmax warps and score issuers: query in place
+    named_bar_sync(2, kSoftThreads + 64);
   }
 
   // One PV unit: O^T block u % 4 (of the O^T buffer at column ocol) += C^T (pair
