@@ -626,14 +626,21 @@ def workload_rooflines(mla, dev, stream, peak, bus):
         at, _ = graph_time(mla, stream, attn, n, 3, overlap=False)
         if int(status.item()) != 0:
             raise RuntimeError(f"device status {int(status.item())} on {name}")
+        splits, chunk, persistent = mla.plan(d, c.num_splits)
+        hpc = mla.heads_per_cta(d)
         entry = {"workload": name, "batch": B, "heads": H, "s_max": c.s_max,
-                 "kv_splits": mla.num_splits(d, c.num_splits), "bytes_per_launch": nbytes,
+                 "kv_splits": splits, "chunk_rows": chunk, "bytes_per_launch": nbytes,
+                 "split_form": ("persistent (one CTA per SM)" if persistent else
+                                "one CTA per (head group, chunk, sequence)"),
+                 "heads_per_cta": hpc,
+                 "operand_parts": "one bf16 part" if hpc == 64 else "bf16 hi + lo",
                  "launches_timed": n, "replays": 3, "clocks": clk}
         for key, us_list in (("split", sp), ("decode_attn", at)):
             us = statistics.median(us_list)
             gbs = nbytes / (us * 1e-6) / 1e9
             entry[key] = {"avg_launch_us": us, "achieved": gbs, "frac": gbs / peak,
                           "spread_us": [min(us_list), max(us_list)]}
+        entry["split"]["traffic"] = recorded_traffic(SPLIT_KERNEL[c.dtype], name)
         res.append(entry)
         del caches, ws, inp
         torch.cuda.empty_cache()
