@@ -593,7 +593,6 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
   const SplitItem fin = items[n_items - 1];   // the item of the CTA's last tile
   const int fin_item = n_items - 1;
   const int last_row = fin.row0 + (fin.tiles - 1) * kTileRows;
-  const int last_valid = fin.valid_last;
   const int zero_from = fin.zero_from;
   const bool zero_last = zero_from < kTileRows;
   const bool fin_first = T - 1 == fin.t0;     // the last tile is its item's first

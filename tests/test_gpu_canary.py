@@ -40,10 +40,12 @@ def small(dtype, B=3, S=300, H=16, hidden=2048, q_len=1):
 @pytest.mark.parametrize("dtype,H,q_len,B", [("bf16", 16, 1, 3), ("fp8", 16, 1, 3),
                                              ("f32", 16, 1, 3), ("bf16", 32, 1, 3),
                                              ("bf16", 16, 4, 3), ("fp8", 16, 2, 3),
-                                             ("bf16", 16, 1, 60), ("bf16", 16, 3, 20)])
+                                             ("bf16", 16, 1, 60), ("bf16", 16, 3, 20),
+                                             ("bf16", 128, 1, 3), ("bf16", 64, 3, 3)])
 @pytest.mark.parametrize("splits", [0, 3])
 def test_decode_calls_stay_in_bounds(cuda_lib, dtype, H, q_len, B, splits):
-    """B = 60 (three chunks) and 20 x 3 tokens run the persistent split grid."""
+    """B = 60 (three chunks) and 20 x 3 tokens run the persistent split grid; 64
+    and 128 heads the 64-head, one-part CTAs."""
     mla = cuda_lib
     cfg = small(dtype, B=B, S=300, H=H, q_len=q_len)
     lens = torch.tensor([300, 129, max(q_len, 17)] * (B // 3), dtype=torch.int32)

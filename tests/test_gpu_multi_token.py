@@ -113,14 +113,20 @@ def test_bench_shape_four_tokens(cuda_lib, cfg):
     compare(gpu, ref, bs, cfg.dtype)
 
 
-@pytest.mark.parametrize("H,q_len", [(32, 4), (32, 2), (128, 2), (48, 2), (48, 4)])
-def test_multi_token_head_groups(cuda_lib, H, q_len):
-    """Several 16-head groups with several tokens: the split CTAs of one chunk
-    share the cache stream across head groups and tokens (clusters of up to 8)."""
+@pytest.mark.parametrize("H,q_len,parts", [(32, 4, 0), (32, 2, 0), (128, 2, 0), (48, 2, 0),
+                                           (48, 4, 0), (64, 3, 0), (128, 3, 0), (128, 2, 2)])
+def test_multi_token_head_groups(cuda_lib, H, q_len, parts):
+    """Several head groups with several tokens: 32-head CTAs (hi + lo parts), paired
+    tokens at 48 heads, and at 64 and 128 heads the 64-head one-part CTAs (parts 0)
+    or the 32-head hi + lo ones (parts 2); each token masks its own later rows."""
     cfg = small("bf16", q_len, B=2, S=300, H=H)
     inp = make_inputs(cfg, seed=70 + H + q_len, poison_tail=True,
                       lengths=torch.tensor([130, 300], dtype=torch.int32))
-    gpu = run_cuda(inp, 0)
+    cuda_lib.set_split_parts(parts)
+    try:
+        gpu = run_cuda(inp, 0)
+    finally:
+        cuda_lib.set_split_parts(0)
     assert gpu["status"] == 0
     ref, bs = run_oracle(inp)
     compare(gpu, ref, bs, "bf16")
