@@ -128,7 +128,8 @@ struct TcPlan {
   static constexpr int BAR_FULLA = 0, BAR_EMPTYA = kSlotsA, BAR_FULLB = 2 * kSlotsA,
                        BAR_EMPTYB = BAR_FULLB + kSlotsB, BAR_ZEROB = BAR_EMPTYB + kSlotsB,
                        BAR_SFULL = BAR_ZEROB + kSlotsB, BAR_SFREE = BAR_SFULL + 2,
-                       BAR_PFULL = BAR_SFREE + 2, BAR_ODONE = BAR_PFULL + 2,
+                       BAR_PFULL = BAR_SFREE + 2, BAR_PFULL1 = BAR_PFULL + 2,
+                       BAR_P0FREE = BAR_PFULL1 + 2, BAR_ODONE = BAR_P0FREE + 2,
                        BAR_LASTA = BAR_ODONE + 2, BAR_FULLX = BAR_LASTA + 1,
                        BAR_ZEROX = BAR_FULLX + 8, BAR_ODONE2 = BAR_ZEROX + 8,
                        BAR_PVPREV = BAR_ODONE2 + 1, BAR_DONE = BAR_PVPREV + 1,
@@ -356,6 +357,9 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
   static_assert(!kPersist || kG == 16, "the persistent instance takes 16 heads per CTA");
   constexpr int kHeadGroup = kG, kGroupHeads = L::kGroupHeads, kSoftWarps = L::kSoftWarps;
   constexpr int kParts = L::kParts;
+  // One P buffer: the softmax writes each 64-row half of P as soon as the
+  // previous tile's PV is done with that half.
+  constexpr bool kHalfP = L::kPBufs == 1;
   constexpr int kSoftThreads = L::kSoftThreads, kSlotsA = L::kSlotsA, kSlotsB = L::kSlotsB;
   constexpr int kPBufs = L::kPBufs, kQN = L::kQN, kQBoxBytes = L::kQBoxBytes, kPSub = L::kPSub;
   constexpr int kPBytes = L::kPBytes, kOffA = L::kOffA, kOffB = L::kOffB, kOffQ = L::kOffQ;
@@ -367,7 +371,8 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
   constexpr uint32_t kOBufCols = L::kOBufCols;
   constexpr int BAR_FULLA = L::BAR_FULLA, BAR_EMPTYA = L::BAR_EMPTYA, BAR_FULLB = L::BAR_FULLB,
                 BAR_EMPTYB = L::BAR_EMPTYB, BAR_ZEROB = L::BAR_ZEROB, BAR_SFULL = L::BAR_SFULL,
-                BAR_SFREE = L::BAR_SFREE, BAR_PFULL = L::BAR_PFULL, BAR_ODONE = L::BAR_ODONE,
+                BAR_SFREE = L::BAR_SFREE, BAR_PFULL = L::BAR_PFULL, BAR_PFULL1 = L::BAR_PFULL1,
+                BAR_P0FREE = L::BAR_P0FREE, BAR_ODONE = L::BAR_ODONE,
                 BAR_LASTA = L::BAR_LASTA, BAR_FULLX = L::BAR_FULLX, BAR_ZEROX = L::BAR_ZEROX,
                 BAR_ODONE2 = L::BAR_ODONE2, BAR_PVPREV = L::BAR_PVPREV, BAR_DONE = L::BAR_DONE,
                 BAR_QFREE = L::BAR_QFREE, BAR_QREADY = L::BAR_QREADY, BAR_ODRAIN = L::BAR_ODRAIN;
@@ -549,7 +554,12 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(BAR_SFULL + i), 2);   // one commit per score issuer
       mbar_init(bar(BAR_SFREE + i), kSoftWarps);
-      mbar_init(bar(BAR_PFULL + i), kSoftWarps);
+      // With one P buffer, P is handed over per 64-row half: BAR_PFULL the rows
+      // 0-63 (or all of P with two buffers), BAR_PFULL1 the rows 64-127, and
+      // BAR_P0FREE: the previous PV has finished with rows 0-63.
+      mbar_init(bar(BAR_PFULL + i), kHalfP ? kSoftWarps / 2 : kSoftWarps);
+      mbar_init(bar(BAR_PFULL1 + i), kSoftWarps / 2);
+      mbar_init(bar(BAR_P0FREE + i), 2);   // one commit per PV issuer
       mbar_init(bar(BAR_ODONE + i), 2);   // one commit per PV issuer
       mbar_init(bar(BAR_ODRAIN + i), kSoftWarps);   // an O^T buffer's result has been read
     }
@@ -898,7 +908,8 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
         if (ok && T >= 2 && !wait_or_abort(bar(BAR_PVPREV), 0, abort_flag, wait_ns)) ok = false;
         if (ok && fin_first && !wait_drain(fin_item)) ok = false;
         if (ok && !wait_or_abort(bar(BAR_PFULL + (t & 1)), (t >> 1) & 1, abort_flag, wait_ns)) ok = false;
-        if (ok && pv_unit(t, 2 + i, fin_first, obuf_col(fin_item), false))
+        if (ok && pv_unit(t, 2 + i, fin_first, obuf_col(fin_item), false) &&
+            (!kHalfP || wait_or_abort(bar(BAR_PFULL1 + (t & 1)), (t >> 1) & 1, abort_flag, wait_ns)))
           pv_unit(t, 6 + i, fin_first, obuf_col(fin_item), false);
         umma_commit(bar(BAR_ODONE2));
       }
@@ -921,7 +932,18 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
         bool ok = true;
         const int step = t == T - 1 ? 4 : 2;
         const bool zmid = zero_mid(c, t);
-        for (int u = i; u < 8 && ok; u += step) ok = pv_unit(t, u, fresh, obuf_col(c.i), zmid);
+        for (int u = i; u < 8 && ok; u += step) {
+          if (kHalfP && u >= 4 && u - step < 4) {
+            // Rows 0-63 of P are free once this thread's MMAs so far have
+            // finished; rows 64-127 are needed from here on.
+            umma_commit(bar(BAR_P0FREE + (t & 1)));
+            if (!wait_or_abort(bar(BAR_PFULL1 + (t & 1)), (t >> 1) & 1, abort_flag, wait_ns)) {
+              ok = false;
+              break;
+            }
+          }
+          ok = pv_unit(t, u, fresh, obuf_col(c.i), zmid);
+        }
         if (!ok) break;
         umma_commit(bar(BAR_ODONE + (t & 1)));
         if (t == T - 2) umma_commit(bar(BAR_PVPREV));
@@ -1117,10 +1139,15 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
         sc[h] = ex2(sc[h] - mu);
         l[h] += sc[h];
       }
-      // P^T buffer sb was last read by the PV of tile t-2.
-      if (t >= kPBufs)
-        wait_or_abort(bar(BAR_ODONE + ((t - kPBufs) & 1)), ((t - kPBufs) >> 1) & 1, abort_flag,
-                      wait_ns);
+      // P^T buffer sb was last read by the PV of tile t - kPBufs (with one buffer,
+      // its rows 0-63 by that PV's first half).
+      if (t >= kPBufs) {
+        if (kHalfP && wq < 2)
+          wait_or_abort(bar(BAR_P0FREE + ((t - 1) & 1)), ((t - 1) >> 1) & 1, abort_flag, wait_ns);
+        else
+          wait_or_abort(bar(BAR_ODONE + ((t - kPBufs) & 1)), ((t - kPBufs) >> 1) & 1, abort_flag,
+                        wait_ns);
+      }
       {
         // P^T (B operand of the PV MMA, K-major 128-byte swizzle, two 64-row
         // halves): two parts: row n < kG is bf16(p) of head n, row kG + n is
@@ -1144,7 +1171,7 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(BAR_PFULL + sb));
+      if (lane == 0) mbar_arrive(bar((kHalfP && wq >= 2 ? BAR_PFULL1 : BAR_PFULL) + sb));
       if (t == T - 1 && zero_last) {
         // The last tile reaches past the sequence's end.  As each of its latent
         // box pairs lands in ring B, zero the rows past the end (they may hold
