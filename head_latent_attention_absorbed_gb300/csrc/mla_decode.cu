@@ -728,17 +728,9 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
           }
           break;
         }
-        // From tile 1 on, wait until the score MMAs of tile t are issued (its P
-        // follows soon); tile 0's pairs take the empty ring at once.
-        if (t > 0 && !(t == T - 1 && T >= 2)) {
-          const unsigned long long t0 = globaltimer_ns();
-          while ((s_issued[0] <= t || s_issued[1] <= t) && !*abort_flag)
-            if (globaltimer_ns() - t0 > wait_ns) {
-              abort_flag[1] = static_cast<int>(bars) - 8;   // no barrier: index -1
-              abort_flag[2] = (t & 0xFF) | (tid << 8);
-              *abort_flag = 1;
-            }
-        }
+        // A tile's pairs go out as soon as their ring slots are free (pacing them
+        // on the tile's score MMAs measured 1 % slower on the large caches); by
+        // then ring A, which runs ahead of the scores, has brought the rows to L2.
         // Unit u holds O^T block mb = u % 4 (ring slot mb) for row half u / 4.
         bool lasta = false;
         const int trow = row_of(c, t);
@@ -2019,7 +2011,10 @@ static mla_status decode_split(const char* who, const mla_dims* dims, int q_len,
     }
     // Two views of the cache [B * s_max rows, 576 columns]: 128-row boxes for
     // the score pass, 64-row boxes for the PV pass; 64 columns (128 bytes,
-    // 128-byte swizzle) per box in both.
+    // 128-byte swizzle) per box in both.  The score pass's L2 requests are
+    // promoted to 256 bytes (a row's next box comes with it from HBM); the PV
+    // pass re-reads rows already in L2 and asks for 128 bytes at a time
+    // (measured: 256-byte promotion there costs 1.5 % on the large caches).
     CUtensorMap tmap, tmap_half;
     const cuuint64_t gdim[2] = {cuuint64_t(kRow), cuuint64_t(dims->batch) * dims->s_max};
     const cuuint64_t gstride[1] = {cuuint64_t(kRow) * 2};
@@ -2029,7 +2024,9 @@ static mla_status decode_split(const char* who, const mla_dims* dims, int q_len,
       CUresult r = enc(v == 0 ? &tmap : &tmap_half, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
                        const_cast<void*>(cache), gdim, gstride, box, estride,
                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                       v == 0 ? CU_TENSOR_MAP_L2_PROMOTION_L2_256B
+                              : CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) {
         set_error("%s: cuTensorMapEncodeTiled failed (%d)", who, int(r));
         return MLA_ERR_CUDA;
