@@ -984,7 +984,14 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
         if (lane < 16 && (lane & 1) == 0) lsum[(hb + e + (lane >> 1)) * 4 + wq] = ws;
       }
       // O^T after the item's last PV: this thread's latent row is d = 128 mb + 32 wq + lane.
-      wait_or_abort(bar(BAR_ODONE + (t_end & 1)), (t_end >> 1) & 1, abort_flag, wait_ns);
+      // The CTA's last tile's PV is split: blocks 2 and 3 complete BAR_ODONE2 (score
+      // issuers), blocks 0 and 1 BAR_ODONE (PV issuers; block 0 usually waits for
+      // its re-read).  The one-item 16-head kernel stores blocks 2-3 first, then 0-1
+      // (bench workload: split 12.59 -> 12.28 us); with the other instances' register
+      // budgets the second pass of loads costs more than it saves.
+      constexpr bool kEarlyBlocks = kG == 16 && !kPersist;
+      if (!kEarlyBlocks || !last)
+        wait_or_abort(bar(BAR_ODONE + (t_end & 1)), (t_end >> 1) & 1, abort_flag, wait_ns);
       if (last) wait_or_abort(bar(BAR_ODONE2), 0, abort_flag, wait_ns);
       tc_fence_after();
       named_bar_sync(1, kSoftThreads);
@@ -1013,25 +1020,56 @@ __global__ void __launch_bounds__(TcPlan<kG, kPersist>::kThreads, 1)
               Lme > 0.f ? (mme + log2f(Lme)) * kLn2 : -INFINITY;
         // Two parts: columns hb.. (hi) and kG + hb.. (lo) of each O^T block, summed;
         // one part: columns hb..hb+15 (heads hb..hb+7, then hb+8..hb+15).
-        uint32_t x4[4][8], y4[4][8];
-#pragma unroll
-        for (int mb = 0; mb < 4; ++mb) {
-          tmem_ld8_nowait(tmem + lane_base + ocol + kQN * mb + hb, x4[mb]);
-          tmem_ld8_nowait(tmem + lane_base + ocol + kQN * mb + (kParts == 2 ? kHeadGroup : 8) + hb,
-                          y4[mb]);
-        }
-        tmem_wait_ld();
-        float* orow = p.part_o + (base + size_t(hw) * p.splits) * kDc + 32 * wq + lane;
         const size_t head_stride = size_t(p.splits) * kDc;
+        if (!kEarlyBlocks) {
+          uint32_t x4[4][8], y4[4][8];
 #pragma unroll
-        for (int h = 0; h < kGroupHeads; ++h, orow += head_stride) {
-          if (!MLA_IN_BOUNDS(base + size_t(hw + h) * p.splits < n_part)) continue;
+          for (int mb = 0; mb < 4; ++mb) {
+            tmem_ld8_nowait(tmem + lane_base + ocol + kQN * mb + hb, x4[mb]);
+            tmem_ld8_nowait(tmem + lane_base + ocol + kQN * mb + (kParts == 2 ? kHeadGroup : 8) + hb,
+                            y4[mb]);
+          }
+          tmem_wait_ld();
+          float* orow = p.part_o + (base + size_t(hw) * p.splits) * kDc + 32 * wq + lane;
 #pragma unroll
-          for (int mb = 0; mb < 4; ++mb)
-            orow[128 * mb] = (kParts == 2 ? __uint_as_float(x4[mb][h]) + __uint_as_float(y4[mb][h])
-                              : h < 8     ? __uint_as_float(x4[mb][h & 7])
-                                          : __uint_as_float(y4[mb][h & 7])) *
-                             inv[h];
+          for (int h = 0; h < kGroupHeads; ++h, orow += head_stride) {
+            if (!MLA_IN_BOUNDS(base + size_t(hw + h) * p.splits < n_part)) continue;
+#pragma unroll
+            for (int mb = 0; mb < 4; ++mb)
+              orow[128 * mb] = (kParts == 2 ? __uint_as_float(x4[mb][h]) + __uint_as_float(y4[mb][h])
+                                : h < 8     ? __uint_as_float(x4[mb][h & 7])
+                                            : __uint_as_float(y4[mb][h & 7])) *
+                               inv[h];
+          }
+        }
+        auto store_blocks = [&](int mb0) {   // O^T blocks mb0 and mb0 + 1
+          uint32_t x4[2][8], y4[2][8];
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            const uint32_t col = ocol + kQN * (mb0 + q) + hb;
+            tmem_ld8_nowait(tmem + lane_base + col, x4[q]);
+            tmem_ld8_nowait(tmem + lane_base + col + (kParts == 2 ? kHeadGroup : 8), y4[q]);
+          }
+          tmem_wait_ld();
+          float* orow = p.part_o + (base + size_t(hw) * p.splits) * kDc + 128 * mb0 + 32 * wq + lane;
+#pragma unroll
+          for (int h = 0; h < kGroupHeads; ++h, orow += head_stride) {
+            if (!MLA_IN_BOUNDS(base + size_t(hw + h) * p.splits < n_part)) continue;
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+              orow[128 * q] = (kParts == 2 ? __uint_as_float(x4[q][h]) + __uint_as_float(y4[q][h])
+                               : h < 8     ? __uint_as_float(x4[q][h & 7])
+                                           : __uint_as_float(y4[q][h & 7])) *
+                              inv[h];
+          }
+        };
+        if (kEarlyBlocks) {
+          store_blocks(2);
+          if (last) {
+            wait_or_abort(bar(BAR_ODONE + (t_end & 1)), (t_end >> 1) & 1, abort_flag, wait_ns);
+            tc_fence_after();
+          }
+          store_blocks(0);
         }
       }
       if (!last) {
