@@ -10,7 +10,7 @@ from __future__ import annotations
 
 from typing import Optional
 
-from ._binding import (EXPORTED, LIB_PATH, MLA_BF16, MLA_FP8_E4M3, MLA_DEV_LENGTH_OUT_OF_RANGE,
+from ._binding import (_check, _stream, step_call, EXPORTED, LIB_PATH, MLA_BF16, MLA_FP8_E4M3, MLA_DEV_LENGTH_OUT_OF_RANGE,
                        MLA_DEV_PIPELINE_TIMEOUT, MLA_F32, MlaDims, MlaError, absorb_q, cache_append,
                        decode_attn, decode_attn_multi, decode_step_multi, multi_num_splits,
                        multi_workspace_bytes,
@@ -115,10 +115,12 @@ class DecodeStep:
 
         Returns a ``HostStep``: pinned host tensors ``q_nope``, ``q_rope``,
         ``lengths``, ``positions`` (the step's inputs, filled by the caller) and
-        ``out`` (o, written by the step), and ``replay()``.  Every replay runs
-        mla_decode_step (mla_decode_step_multi for several tokens per sequence)
-        on the host tensors themselves: its kernels read the inputs and write o
-        over the host link, with no copies.
+        ``out`` (o, written by the step), ``replay()`` and ``launch()``.  Both
+        run mla_decode_step (mla_decode_step_multi for several tokens per
+        sequence) on the host tensors themselves: its kernels read the inputs
+        and write o over the host link, with no copies.  ``replay()`` replays
+        the captured graph; ``launch()`` makes the call directly with arguments
+        converted at capture, so that consecutive steps overlap.
         """
         return HostStep(self, cache, w_uk, w_uv)
 
@@ -181,5 +183,21 @@ class HostStep:
         with torch.cuda.graph(self._graph, stream=side):
             body()
 
+        # launch(): the same library call made directly, without the graph, its
+        # arguments checked and converted once here.  Consecutive launches let
+        # each step's first kernel overlap the previous step's last one
+        # (programmatic dependent launch), which separate graph replays cannot.
+        self._call = step_call(step.dims, step.q_len, h[0], h[1], w_uk, h[3], cache, h[2], w_uv,
+                               step.workspace, step.q_abs, step.q_pe, step.o_c, self.out,
+                               step.scale, step.rope_base, step.splits_requested, step.lse,
+                               step.status)
+
     def replay(self):
+        """The step as one replay of its CUDA graph."""
         self._graph.replay()
+
+    def launch(self, stream=None):
+        """The step as one direct mla_decode_step call (its kernels launched on
+        ``stream``, default the current one), on the same host buffers."""
+        fn, args = self._call
+        _check(fn(*args, _stream(stream)))

@@ -334,6 +334,26 @@ def decode_step_multi(d: MlaDims, q_len: int, q_nope, q_rope, w_uk, positions, c
                                         _ptr(out), _ptr(dev_status), _stream(stream)))
 
 
+def step_call(d: MlaDims, q_len: int, q_nope, q_rope, w_uk, positions, cache, lengths, w_uv,
+              workspace, q_abs, q_pe, o_c, out, softmax_scale: float, rope_base: float,
+              num_splits_requested: int, lse, dev_status):
+    """The checked arguments of mla_decode_step (q_len 1) or mla_decode_step_multi,
+    converted once: returns (function, arguments without the stream), for callers
+    that make the same call every step (HostStep.launch).  The tensors must stay
+    alive and in place while the arguments are used."""
+    _cuda_contig(w_uk, cache, w_uv, workspace, q_abs, q_pe, o_c, lse, dev_status)
+    _cuda_or_pinned(q_nope, q_rope, positions, lengths, out)
+    nbytes = workspace.numel() * workspace.element_size()
+    lib = load()
+    tail = (_ptr(q_nope), _ptr(q_rope), _ptr(w_uk), _ptr(positions), float(rope_base),
+            _ptr(cache), _ptr(lengths), float(softmax_scale), int(num_splits_requested),
+            _ptr(w_uv), _ptr(workspace), nbytes, _ptr(q_abs), _ptr(q_pe), _ptr(o_c), _ptr(lse),
+            _ptr(out), _ptr(dev_status))
+    if q_len == 1:
+        return lib.mla_decode_step, (ctypes.byref(d),) + tail
+    return lib.mla_decode_step_multi, (ctypes.byref(d), int(q_len)) + tail
+
+
 def out_proj(d: MlaDims, o_c, w_uv, out, stream=None) -> None:
     """o = W_UV . o_c per head."""
     _cuda_contig(o_c, w_uv, out)

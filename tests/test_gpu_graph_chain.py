@@ -12,7 +12,8 @@ inputs (its own cache, weights and queries, as the bench's rotating layer copies
 and its own o_c, lse and o, and every step is compared with the fp64 oracle.
 
 The same holds for the e2e path: several captured host-memory steps
-(DecodeStep.capture) replayed back to back at the bench's size.
+(DecodeStep.capture) replayed, or launched directly, back to back at the
+bench's size.
 """
 import numpy as np
 import pytest
@@ -138,6 +139,39 @@ def test_host_steps_back_to_back_at_bench_size(cuda_lib):
         assert_close(f"layer {k} o", hs.out.double().numpy()[bs], ref["o"], "bf16")
     ref, bs = run_oracle(layers[-1])
     assert_close("last o_c", step.o_c.double().cpu().numpy()[bs], ref["o_c"], "bf16")
+
+
+@pytest.mark.parametrize("cfg", [V2LITE_BF16_B8_S4096, V2LITE_FP8_B8_S4096], ids=lambda c: c.dtype)
+def test_host_steps_launched_directly(cuda_lib, cfg):
+    """HostStep.launch (the direct call, arguments converted at capture) computes
+    what replay computes, bit for bit, and back-to-back launches over four layers
+    (each step's absorb overlapping the previous step's tail) equal the oracle."""
+    mla = cuda_lib
+    layers = _layer_inputs(cfg, 4, 410)
+    step = mla.DecodeStep(cfg.batch, cfg.heads, cfg.s_max, cache_storage(cfg),
+                          rope_base=cfg.rope_base, softmax_scale=cfg.softmax_scale)
+    hosts = []
+    for x in layers:
+        hs = step.capture(x.cache.cuda(), x.w_uk.cuda(), x.w_uv.cuda())
+        hs.q_nope.copy_(x.q_nope)
+        hs.q_rope.copy_(x.q_rope)
+        hs.lengths.copy_(x.lengths)
+        hs.positions.copy_(x.positions)
+        hosts.append(hs)
+    hosts[0].replay()
+    torch.cuda.synchronize()
+    replayed = hosts[0].out.clone()
+    for hs in hosts:
+        hs.out.fill_(float("nan"))
+    for _ in range(2):
+        for hs in hosts:
+            hs.launch()
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    assert torch.equal(hosts[0].out, replayed)
+    for k, (hs, x) in enumerate(zip(hosts, layers)):
+        ref, bs = run_oracle(x)
+        assert_close(f"layer {k} o", hs.out.double().numpy()[bs], ref["o"], cfg.dtype)
 
 
 def test_plain_launches_equal_overlapped(cuda_lib):
