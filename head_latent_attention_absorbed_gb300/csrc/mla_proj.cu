@@ -15,6 +15,8 @@
 // fp32 accumulation.
 #include <math.h>
 
+#include <algorithm>
+
 #include "mla_common.cuh"
 #include "mla_split.cuh"
 #include "mla_wstream.cuh"
@@ -38,16 +40,36 @@ __device__ __forceinline__ float to_f<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
+// Pair `it` = (b, i) of head h: the inputs (position and the two values), then
+// the rotation.  The two halves are separate so that a caller can request the
+// inputs early and rotate later.
+struct RopeIn {
+  int32_t pos;
+  float x0, x1;
+};
+
+template <typename T>
+__device__ __forceinline__ RopeIn rope_load(const T* q_rope, const int32_t* positions, int H, int h,
+                                            int it) {
+  const int b = it / (kDr / 2), i = it % (kDr / 2);
+  const size_t off = (size_t(b) * H + h) * kDr + 2 * i;
+  return RopeIn{positions[b], to_f(q_rope[off]), to_f(q_rope[off + 1])};
+}
+
+__device__ __forceinline__ void rope_rotate(const RopeIn& in, const RopeTheta& th, float* q_pe,
+                                            int H, int h, int it) {
+  const int b = it / (kDr / 2), i = it % (kDr / 2);
+  float sn, cs;
+  sincosf(rope_angle(in.pos, th.turns[i]), &sn, &cs);
+  const size_t off = (size_t(b) * H + h) * kDr + 2 * i;
+  q_pe[off] = cs * in.x0 - sn * in.x1;
+  q_pe[off + 1] = sn * in.x0 + cs * in.x1;
+}
+
 template <typename T>
 __device__ __forceinline__ void rope_pair(const T* q_rope, const int32_t* positions,
                                           const RopeTheta& th, float* q_pe, int H, int h, int it) {
-  const int b = it / (kDr / 2), i = it % (kDr / 2);
-  float sn, cs;
-  sincosf(rope_angle(positions[b], th.turns[i]), &sn, &cs);
-  const size_t off = (size_t(b) * H + h) * kDr + 2 * i;
-  const float x0 = to_f(q_rope[off]), x1 = to_f(q_rope[off + 1]);
-  q_pe[off] = cs * x0 - sn * x1;
-  q_pe[off + 1] = sn * x0 + cs * x1;
+  rope_rotate(rope_load(q_rope, positions, H, h, it), th, q_pe, H, h, it);
 }
 
 // ---------------------------------------------------------------------- absorb, bf16
@@ -75,12 +97,38 @@ __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r
                : "r"(addr));
 }
 
-// kStage (queries in host memory): each 16-row tile of q_nope is first copied
-// into shared memory with coalesced 16-byte loads (8 per lane, whole 128-byte
-// lines over the host link) and the A fragments come from ldmatrix; otherwise
-// each lane loads its fragments directly (32 four-byte loads, which from
-// device memory cost one round trip less).
-template <bool kStage>
+// Within mla_decode_step: start the decode kernel's cache stream.  The pieces
+// of every chunk's first rows are spread over the grid's threads (thread `me`
+// of `nthreads`), the first piece of every chunk first.  Callers number their
+// threads CTA-fastest (thread t of CTA c is me = t * CTAs + c), so that
+// consecutive pieces go to different CTAs, hence SMs: each piece is one bulk
+// prefetch that the SM's copy unit turns into L2 requests, and a few SMs
+// holding all of them issue them one after another (measured on 8 sequences x
+// 4096 rows: its 1152 pieces on the first three CTAs of a 16-CTA grid made
+// the step 27 us slower).  The cache and lengths are inputs, not results of
+// the previous kernel, so this precedes the wait.
+__device__ __forceinline__ void issue_cache_prefetch(const CachePrefetch& pf, int me, int nthreads) {
+  if (!pf.cache) return;
+  const int nchunk = pf.B * pf.splits;
+  const int per_chunk = (pf.rows * pf.row_bytes + kPfPiece - 1) / kPfPiece;
+  for (int id = me; id < nchunk * per_chunk; id += nthreads) {
+    const int k = id / nchunk, c = id % nchunk;
+    const int b = c / pf.splits, r0 = (c % pf.splits) * pf.chunk;
+    const int len = min(max(pf.lengths[b], 0), pf.s_max);
+    const int rows = min(min(pf.chunk, len - r0), pf.rows);
+    if (rows <= 0) continue;
+    const long long first = (static_cast<long long>(b) * pf.s_max + r0) * pf.row_bytes;
+    const long long beg = first + static_cast<long long>(k) * kPfPiece;
+    const long long end = first + static_cast<long long>(rows) * pf.row_bytes;
+    if (beg >= end) continue;
+    const uint32_t size = static_cast<uint32_t>(min(static_cast<long long>(kPfPiece), end - beg));
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(pf.cache + beg), "r"(size)
+                 : "memory");
+  }
+}
+
+// Queries in device memory: each lane loads its A fragments directly (32
+// four-byte loads; the 32 CTAs of a head read its query rows from L2).
 __global__ void __launch_bounds__(32)
     absorb_bf16_kernel(const __nv_bfloat16* __restrict__ q_nope,
                        const __nv_bfloat16* __restrict__ q_rope,
@@ -88,7 +136,6 @@ __global__ void __launch_bounds__(32)
                        const RopeTheta th, float* __restrict__ q_abs, float* __restrict__ q_pe,
                        int B, int H, const CachePrefetch pf) {
   __shared__ __align__(128) uint8_t wt[kDn * 32];  // 128 k-rows x 16 bf16 columns
-  __shared__ __align__(16) uint8_t qs[kStage ? 16 * kQsRow : 16];  // one tile's 16 query rows
   const int h = blockIdx.x, cb = blockIdx.y, lane = threadIdx.x;
   pdl_launch_dependents();   // the decode kernel may start its set-up and cache stream now
   const int c0 = cb * 16;
@@ -101,76 +148,37 @@ __global__ void __launch_bounds__(32)
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
   }
   asm volatile("cp.async.commit_group;" ::: "memory");
-  if (pf.cache) {
-    // Within mla_decode_step: start the decode kernel's cache stream.  The
-    // pieces of every chunk's first rows are spread over all threads of the
-    // grid, the first piece of every chunk first.  The cache and lengths are
-    // inputs, not results of the previous kernel, so this precedes the wait.
-    const int nchunk = pf.B * pf.splits;
-    const int per_chunk = (pf.rows * pf.row_bytes + kPfPiece - 1) / kPfPiece;
-    const int nthreads = gridDim.x * gridDim.y * 32;
-    const int me = (blockIdx.y * gridDim.x + blockIdx.x) * 32 + lane;
-    for (int id = me; id < nchunk * per_chunk; id += nthreads) {
-      const int k = id / nchunk, c = id % nchunk;
-      const int b = c / pf.splits, r0 = (c % pf.splits) * pf.chunk;
-      const int len = min(max(pf.lengths[b], 0), pf.s_max);
-      const int rows = min(min(pf.chunk, len - r0), pf.rows);
-      if (rows <= 0) continue;
-      const long long first = (static_cast<long long>(b) * pf.s_max + r0) * pf.row_bytes;
-      const long long beg = first + static_cast<long long>(k) * kPfPiece;
-      const long long end = first + static_cast<long long>(rows) * pf.row_bytes;
-      if (beg >= end) continue;
-      const uint32_t size = static_cast<uint32_t>(min(static_cast<long long>(kPfPiece), end - beg));
-      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(pf.cache + beg), "r"(size)
-                   : "memory");
-    }
-  }
+  issue_cache_prefetch(pf, lane * (gridDim.x * gridDim.y) + blockIdx.y * gridDim.x + blockIdx.x,
+                       gridDim.x * gridDim.y * 32);
   pdl_wait();
-  for (int it = cb * 32 + lane; it < B * (kDr / 2); it += 32 * gridDim.y)
-    rope_pair(q_rope, pos, th, q_pe, H, h, it);
+  // This lane's first RoPE pair (a head has B * 32 pairs and 32 lanes per
+  // column block, so up to 32 sequences it is the lane's only one): its inputs
+  // are requested before the first query tile's, so that the two reads are in
+  // flight together instead of one after the other; the rotation follows the
+  // MMAs.
+  const int rope_it = cb * 32 + lane, rope_n = B * (kDr / 2), rope_step = 32 * gridDim.y;
+  RopeIn rope_first{0, 0.f, 0.f};
+  if (rope_it < rope_n) rope_first = rope_load(q_rope, pos, H, h, rope_it);
 
   const int gq = lane >> 2, cq = lane & 3;
-  const uint32_t wbase = smem_u32(wt), qbase = smem_u32(qs);
+  const uint32_t wbase = smem_u32(wt);
   for (int mt = 0; mt * 16 < B; ++mt) {
     const int bA = mt * 16 + gq, bB = bA + 8;
     uint32_t a[8][4];
-    if constexpr (kStage) {
-      // The tile's 16 query rows q_nope[b, h, :] (256 B each) into shared
-      // memory: load r of lane l is 16-byte chunk (l + 32 r) % 16 of row
-      // (l + 32 r) / 16 (rows past B read as zeros).
-      if (mt > 0) __syncwarp();   // the previous tile's rows have been read
+    const __nv_bfloat16* rA = q_nope + (size_t(bA) * H + h) * kDn + 2 * cq;
+    const __nv_bfloat16* rB = q_nope + (size_t(bB) * H + h) * kDn + 2 * cq;
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const int i = lane + 32 * r, row = i >> 4, ch = i & 15;
-        const int bq = mt * 16 + row;
-        const uint4 v = bq < B ? reinterpret_cast<const uint4*>(
-                                     q_nope + (size_t(bq) * H + h) * kDn)[ch]
-                               : make_uint4(0u, 0u, 0u, 0u);
-        *reinterpret_cast<uint4*>(qs + row * kQsRow + ch * 16) = v;
-      }
-    } else {
-      const __nv_bfloat16* rA = q_nope + (size_t(bA) * H + h) * kDn + 2 * cq;
-      const __nv_bfloat16* rB = q_nope + (size_t(bB) * H + h) * kDn + 2 * cq;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        a[ks][0] = bA < B ? *reinterpret_cast<const uint32_t*>(rA + 16 * ks) : 0u;
-        a[ks][1] = bB < B ? *reinterpret_cast<const uint32_t*>(rB + 16 * ks) : 0u;
-        a[ks][2] = bA < B ? *reinterpret_cast<const uint32_t*>(rA + 16 * ks + 8) : 0u;
-        a[ks][3] = bB < B ? *reinterpret_cast<const uint32_t*>(rB + 16 * ks + 8) : 0u;
-      }
+    for (int ks = 0; ks < 8; ++ks) {
+      a[ks][0] = bA < B ? *reinterpret_cast<const uint32_t*>(rA + 16 * ks) : 0u;
+      a[ks][1] = bB < B ? *reinterpret_cast<const uint32_t*>(rB + 16 * ks) : 0u;
+      a[ks][2] = bA < B ? *reinterpret_cast<const uint32_t*>(rA + 16 * ks + 8) : 0u;
+      a[ks][3] = bB < B ? *reinterpret_cast<const uint32_t*>(rB + 16 * ks + 8) : 0u;
     }
     if (mt == 0) asm volatile("cp.async.wait_all;" ::: "memory");
     __syncwarp();
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
     for (int ks = 0; ks < 8; ++ks) {
-      // A fragment of k in [16ks, 16ks+16): lanes 0-7 / 8-15 / 16-23 / 24-31
-      // address rows 0-7 / 8-15 / 0-7 / 8-15 at columns 16ks / 16ks / 16ks+8 /
-      // 16ks+8, the order of the mma's four A registers.
-      if constexpr (kStage)
-        ldsm_x4(qbase + ((lane & 7) + 8 * ((lane >> 3) & 1)) * kQsRow +
-                    (16 * ks + 8 * (lane >> 4)) * 2,
-                a[ks][0], a[ks][1], a[ks][2], a[ks][3]);
       // B fragments of n-blocks 0 and 1 for k in [16ks, 16ks+16): ldmatrix.trans
       // of the [k][n] slice (32-byte rows, 16-byte chunks swizzled by bit 2 of k).
       const int mi = lane >> 3;
@@ -192,6 +200,150 @@ __global__ void __launch_bounds__(32)
             make_float2(acc[nb][2], acc[nb][3]);
     }
   }
+  if (rope_it < rope_n) rope_rotate(rope_first, th, q_pe, H, h, rope_it);
+  for (int it = rope_it + rope_step; it < rope_n; it += rope_step)
+    rope_pair(q_rope, pos, th, q_pe, H, h, it);
+}
+
+// Queries in page-locked host memory, read over the host link: a head's
+// query rows are read by 16 / kWarps CTAs instead of 32 (the form above reads
+// them once per 16-column block).  grid (H, 16 / kWarps), 32 kWarps threads:
+// CTA (h, y) owns columns [32 kWarps y, 32 kWarps (y + 1)), warp w of them
+// the 32 columns at 32 w.  Before the wait, its W_UK[h] slice (128 rows x
+// 32 kWarps bf16) lands in shared memory as 16-column blocks in the layout
+// above.  After it, the first half of the warps copies up to 64 query rows at
+// a time into shared memory with whole-line 16-byte loads while the second
+// half rotates the head's RoPE pairs (shared over the head's CTAs; 32 lanes
+// over the 32 pairs of one row: one 128-byte line of q_rope); then each warp
+// computes its columns from those rows with ldmatrix fragments.
+constexpr int kHeadStageRows = 64;
+template <int kWarps>
+struct HeadPlan {
+  static constexpr int kThreads = 32 * kWarps;
+  static constexpr int kCols = 32 * kWarps;                    // columns per CTA
+  static constexpr int kCtasPerHead = kDc / kCols;
+  static constexpr size_t kWBytes = size_t(kCols / 16) * kDn * 32;
+  static constexpr size_t kSmem = kWBytes + size_t(kHeadStageRows) * kQsRow;
+  static_assert(kWarps >= 2 && kDc % kCols == 0, "whole column slices, two warp halves");
+};
+
+template <int kWarps>
+__global__ void __launch_bounds__(32 * kWarps)
+    absorb_bf16_head_kernel(const __nv_bfloat16* __restrict__ q_nope,
+                            const __nv_bfloat16* __restrict__ q_rope,
+                            const __nv_bfloat16* __restrict__ w_uk,
+                            const int32_t* __restrict__ pos, const RopeTheta th,
+                            float* __restrict__ q_abs, float* __restrict__ q_pe, int B, int H,
+                            const CachePrefetch pf) {
+  using P = HeadPlan<kWarps>;
+  constexpr int kHalf = P::kThreads / 2;
+  extern __shared__ __align__(128) uint8_t dsm[];
+  uint8_t* wt = dsm;                  // block i (columns c0 + 16i ..) at i * kDn * 32
+  uint8_t* qs = dsm + P::kWBytes;     // staged query rows, kQsRow bytes apart
+  const int h = blockIdx.x, y = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int c0 = y * P::kCols;
+  pdl_launch_dependents();   // the decode kernel may start its set-up and cache stream now
+  // The slice as 16-byte pieces: piece j is piece j % (kCols / 8) of k-row
+  // j / (kCols / 8), so consecutive threads read consecutive pieces of a row.
+  constexpr int kPieces = P::kCols / 8;
+  for (int j = tid; j < kDn * kPieces; j += P::kThreads) {
+    const int k = j / kPieces, piece = j % kPieces, blk = piece >> 1, ch = piece & 1;
+    const uint32_t dst =
+        smem_u32(wt + blk * (kDn * 32) + k * 32 + ((ch ^ ((k >> 2) & 1)) << 4));
+    const void* src = w_uk + (size_t(h) * kDn + k) * kDc + c0 + piece * 8;
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+  issue_cache_prefetch(pf, tid * (gridDim.x * gridDim.y) + blockIdx.y * gridDim.x + blockIdx.x,
+                       gridDim.x * gridDim.y * P::kThreads);
+  pdl_wait();
+
+  const int gq = lane >> 2, cq = lane & 3;
+  const uint32_t qbase = smem_u32(qs);
+  for (int g0 = 0; g0 < B; g0 += kHeadStageRows) {
+    const int tiles = (min(kHeadStageRows, B - g0) + 15) / 16;
+    if (g0 > 0) __syncthreads();   // every warp has read the previous rows
+    if (tid < kHalf) {
+      // Rows g0 .. of q_nope[., h, :] (256 B each), whole 16-row tiles (rows
+      // past B as zeros): load j is 16-byte chunk j % 16 of row j / 16.
+      for (int j = tid; j < tiles * 16 * 16; j += kHalf) {
+        const int row = j >> 4, ch = j & 15, b = g0 + row;
+        const uint4 v = b < B ? reinterpret_cast<const uint4*>(q_nope + (size_t(b) * H + h) * kDn)[ch]
+                              : make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4*>(qs + row * kQsRow + ch * 16) = v;
+      }
+    } else if (g0 == 0) {
+      for (int it = y * kHalf + tid - kHalf; it < B * (kDr / 2); it += kHalf * P::kCtasPerHead)
+        rope_pair(q_rope, pos, th, q_pe, H, h, it);
+    }
+    if (g0 == 0) asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();   // the rows and (first pass) every thread's W_UK pieces are in place
+    for (int mt = 0; mt < tiles; ++mt) {
+      const int bA = g0 + mt * 16 + gq, bB = bA + 8;
+      float acc[2][2][4] = {};
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        // A fragment of k in [16ks, 16ks+16): lanes 0-7 / 8-15 / 16-23 / 24-31
+        // address rows 0-7 / 8-15 / 0-7 / 8-15 of the tile at columns 16ks /
+        // 16ks / 16ks+8 / 16ks+8, the order of the mma's four A registers.
+        uint32_t a[4];
+        ldsm_x4(qbase + (16 * mt + (lane & 7) + 8 * ((lane >> 3) & 1)) * kQsRow +
+                    (16 * ks + 8 * (lane >> 4)) * 2,
+                a[0], a[1], a[2], a[3]);
+        const int mi = lane >> 3;
+        const int k = 16 * ks + ((mi & 1) << 3) + (lane & 7);
+        const int ch = mi >> 1;
+#pragma unroll
+        for (int blk = 0; blk < 2; ++blk) {
+          const uint32_t wbase = smem_u32(wt + (2 * warp + blk) * (kDn * 32));
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4_t(wbase + k * 32 + ((ch ^ ((k >> 2) & 1)) << 4), b0, b1, b2, b3);
+          mma_bf16(acc[blk][0], a, b0, b1);
+          mma_bf16(acc[blk][1], a, b2, b3);
+        }
+      }
+#pragma unroll
+      for (int blk = 0; blk < 2; ++blk)
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb) {
+          const int c = c0 + 32 * warp + 16 * blk + 8 * nb + 2 * cq;
+          if (bA < B)
+            *reinterpret_cast<float2*>(q_abs + (size_t(bA) * H + h) * kDc + c) =
+                make_float2(acc[blk][nb][0], acc[blk][nb][1]);
+          if (bB < B)
+            *reinterpret_cast<float2*>(q_abs + (size_t(bB) * H + h) * kDc + c) =
+                make_float2(acc[blk][nb][2], acc[blk][nb][3]);
+        }
+    }
+  }
+}
+
+template <int kWarps>
+mla_status launch_absorb_head(const char* who, bool early, cudaStream_t s,
+                              const __nv_bfloat16* qn, const __nv_bfloat16* qr,
+                              const __nv_bfloat16* wk, const int32_t* positions,
+                              const RopeTheta& th, float* qa, float* qp, int B, int H,
+                              const CachePrefetch& pf) {
+  using P = HeadPlan<kWarps>;
+  static DeviceFlags attr_done;
+  const int dev = current_device();
+  if (!attr_done.test(dev)) {
+    if (cudaFuncSetAttribute(absorb_bf16_head_kernel<kWarps>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(P::kSmem)) != cudaSuccess) {
+      set_error("%s: cannot reserve %zu bytes of shared memory", who, P::kSmem);
+      return MLA_ERR_CUDA;
+    }
+    attr_done.set(dev);
+  }
+  const dim3 grid(H, P::kCtasPerHead);
+  if (early)
+    launch_pdl(absorb_bf16_head_kernel<kWarps>, grid, dim3(P::kThreads), P::kSmem, s, qn, qr, wk,
+               positions, th, qa, qp, B, H, pf);
+  else
+    absorb_bf16_head_kernel<kWarps><<<grid, P::kThreads, P::kSmem, s>>>(qn, qr, wk, positions,
+                                                                         th, qa, qp, B, H, pf);
+  return MLA_OK;
 }
 
 // ---------------------------------------------------------------------- absorb, fp32
@@ -468,13 +620,11 @@ __global__ void __launch_bounds__(256) rope_q_kernel(const T* __restrict__ q_rop
 using namespace mla;
 
 // Dynamic shared memory (unused) of the early-launched absorb: with its static
-// shared memory (4 KB, or 8.25 KB when it stages the queries) and the 1 KB the
-// SM reserves per CTA, a CTA takes 48-49 KB, so at most four fit on an SM; the
-// total stays within the 48 KB a launch may use without opting in.
+// shared memory (4 KB) and the 1 KB the SM reserves per CTA, a CTA takes 48-49
+// KB, so at most four fit on an SM; the total stays within the 48 KB a launch
+// may use without opting in.
 constexpr size_t kAbsorbSpreadSmem = (44u << 10) - 16;
-constexpr size_t kAbsorbSpreadSmemStaged = 39u << 10;
-static_assert(kAbsorbSpreadSmem + kDn * 32 + 16 <= (48u << 10) &&
-                  kAbsorbSpreadSmemStaged + kDn * 32 + 16 * kQsRow <= (48u << 10),
+static_assert(kAbsorbSpreadSmem + kDn * 32 <= (48u << 10),
               "the early absorb's shared memory needs no opt-in");
 
 // Whether `p` is page-locked host memory (read by the kernels over the host link).
@@ -519,27 +669,40 @@ mla_status mla::absorb_q(const char* who, const mla_dims* dims, const void* q_no
   RopeTheta th;
   for (int i = 0; i < kDr / 2; ++i) th.turns[i] = pow(rope_base, -2.0 * i / kDr) / (2.0 * M_PI);
   if (dims->dtype != MLA_F32) {
-    // Queries in host memory: stage each tile with whole-line reads (measured on
-    // 8 sequences x 16 heads, one step per graph launch: 1.26 -> 1.29-1.31 TB/s
-    // end to end; from device memory the direct loads are faster).
-    const bool stage = host_resident(q_nope);
-    auto kern = stage ? absorb_bf16_kernel<true> : absorb_bf16_kernel<false>;
     const auto* qn = static_cast<const __nv_bfloat16*>(q_nope);
     const auto* qr = static_cast<const __nv_bfloat16*>(q_rope);
     const auto* wk = static_cast<const __nv_bfloat16*>(w_uk);
-    if (early)
+    auto* qa = static_cast<float*>(q_abs);
+    auto* qp = static_cast<float*>(q_pe);
+    if (host_resident(q_nope)) {
+      // Queries in host memory: read by fewer CTAs per head, about 64 CTAs in
+      // all (one per head from 64 heads up).  Measured end to end, one direct
+      // mla_decode_step call per step, against the 32-CTA-per-head form with
+      // staged loads: 8 x 4096 rows x 16 heads 23.5 -> 20.9 us (four CTAs per
+      // head; 21.0 with eight, 22.3 with one); 64 ragged sequences 120.2 ->
+      // 100.3 us (106 with eight or one); 32 x 16384 rows x 128 heads 448 ->
+      // 290 us (312 with four).
+      const int per_head = std::max(1, std::min(4, 64 / H));
+      st = per_head == 4   ? launch_absorb_head<4>(who, early, s, qn, qr, wk, positions, th, qa,
+                                                   qp, B, H, pf)
+           : per_head == 2 ? launch_absorb_head<8>(who, early, s, qn, qr, wk, positions, th, qa,
+                                                   qp, B, H, pf)
+                           : launch_absorb_head<16>(who, early, s, qn, qr, wk, positions, th, qa,
+                                                    qp, B, H, pf);
+      if (st != MLA_OK) return st;
+    } else if (early) {
       // Launched while the previous step's fused tail fills most SMs' register
       // files, the grid's small CTAs would all land on the few SMs left free
       // (measured on 8 sequences x 16 heads: 512 CTAs on 24 SMs, 22 per SM,
       // 3.3 us from the wait to the last exit).  Unused shared memory caps
       // them at four per SM, so the rest start on the SMs the tail leaves:
       // 128 SMs, 1.7 us, and the step 19.5 -> 18.5 us.
-      launch_pdl(kern, dim3(H, kDc / 16), dim3(32),
-                 stage ? kAbsorbSpreadSmemStaged : kAbsorbSpreadSmem, s, qn, qr, wk, positions,
-                 th, static_cast<float*>(q_abs), static_cast<float*>(q_pe), B, H, pf);
-    else
-      kern<<<dim3(H, kDc / 16), 32, 0, s>>>(qn, qr, wk, positions, th, static_cast<float*>(q_abs),
-                                           static_cast<float*>(q_pe), B, H, pf);
+      launch_pdl(absorb_bf16_kernel, dim3(H, kDc / 16), dim3(32), kAbsorbSpreadSmem, s, qn, qr,
+                 wk, positions, th, qa, qp, B, H, pf);
+    } else {
+      absorb_bf16_kernel<<<dim3(H, kDc / 16), 32, 0, s>>>(qn, qr, wk, positions, th, qa, qp, B,
+                                                          H, pf);
+    }
   } else {
     absorb_f32_kernel<<<dim3(H, B), 128, 0, s>>>(
         static_cast<const float*>(q_nope), static_cast<const float*>(q_rope),

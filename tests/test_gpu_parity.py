@@ -192,6 +192,42 @@ def test_captured_step_from_host_memory(cuda_lib, dtype):
 
 
 
+@pytest.mark.parametrize("dtype,B,H", [("bf16", 70, 16), ("bf16", 5, 128), ("fp8", 67, 32)])
+def test_host_memory_step_many_rows_and_heads(cuda_lib, dtype, B, H):
+    """The host-memory absorb (one CTA per head, up to 64 query rows per pass):
+    more than one pass of rows, a partial last 16-row tile, 128 heads.  A replay
+    equals the device-resident eager step bit for bit and matches the oracle."""
+    mla = cuda_lib
+    cfg = small(dtype=dtype, B=B, H=H, S=160)
+    g = torch.Generator().manual_seed(B + H)
+    lengths = torch.randint(1, 161, (B,), generator=g, dtype=torch.int32)
+    lengths[0] = 160
+    inp = make_inputs(cfg, seed=31, poison_tail=True, lengths=lengths)
+    step = mla.DecodeStep(cfg.batch, cfg.heads, cfg.s_max, cache_storage(cfg),
+                          rope_base=cfg.rope_base, softmax_scale=cfg.softmax_scale)
+    cache, w_uk, w_uv = inp.cache.cuda(), inp.w_uk.cuda(), inp.w_uv.cuda()
+    hs = step.capture(cache, w_uk, w_uv)
+    hs.q_nope.copy_(inp.q_nope)
+    hs.q_rope.copy_(inp.q_rope)
+    hs.lengths.copy_(inp.lengths)
+    hs.positions.copy_(inp.positions)
+    hs.out.fill_(float("nan"))
+    hs.launch()
+    torch.cuda.synchronize()
+    got = hs.out.double().numpy().copy()
+    q_abs = step.q_abs.double().cpu().numpy()
+    eager = step.run(inp.q_nope.cuda(), inp.q_rope.cuda(), cache, inp.lengths.cuda(),
+                     inp.positions.cuda(), w_uk, w_uv)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(q_abs, step.q_abs.double().cpu().numpy())
+    np.testing.assert_array_equal(got, eager.double().cpu().numpy())
+    assert int(step.status.item()) == 0
+    ref, bs = run_oracle(inp, batches=[0, 1, B // 2, B - 1])
+    from _parity import assert_close
+    assert_close("q_abs", q_abs[bs], ref["q_abs"], dtype)
+    assert_close("o", got[bs], ref["o"], dtype)
+
+
 def test_pageable_host_memory_is_refused(cuda_lib):
     """mla_decode_step accepts page-locked host buffers for its inputs and output
     but refuses pageable ones before anything is enqueued."""
