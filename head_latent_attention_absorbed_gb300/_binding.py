@@ -160,9 +160,16 @@ def _ptr(t) -> int:
 
 
 def _stream(stream) -> int:
+    """The raw cudaStream_t of ``stream``, default the current device's current
+    stream (read without building a torch.cuda.Stream object: that costs a few
+    microseconds per call, as much as a kernel launch)."""
     import torch
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return s.cuda_stream
+    if stream is not None:
+        return stream.cuda_stream
+    raw = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+    if raw is not None:
+        return raw(torch._C._cuda_getDevice())
+    return torch.cuda.current_stream().cuda_stream
 
 
 def dtype_code(torch_dtype) -> int:

@@ -2214,17 +2214,18 @@ constexpr long long kFusedTailMax = 256;
 // Bytes of the cache mla_decode_step asks L2 to fetch during its absorb kernel.
 constexpr long long kPrefetchBudget = 16ll << 20;
 
-// Whether the device can address `ptr` directly: device or managed memory, or
-// page-locked host memory (mapped into the device's address space).  Pageable
-// host memory is refused: a kernel touching it would fault.
-static bool device_addressable(const void* ptr) {
+// Whether the device can address `ptr` directly: 1 for device or managed
+// memory, 2 for page-locked host memory (mapped into the device's address
+// space), 0 otherwise.  Pageable host memory is refused: a kernel touching it
+// would fault.
+static int device_addressable(const void* ptr) {
   cudaPointerAttributes a;
   if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
     cudaGetLastError();
-    return false;
+    return 0;
   }
-  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return true;
-  return a.type == cudaMemoryTypeHost && a.devicePointer != nullptr;
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) return 1;
+  return a.type == cudaMemoryTypeHost && a.devicePointer != nullptr ? 2 : 0;
 }
 
 // The whole step for q_len tokens per sequence (mla_decode_step: q_len = 1).
@@ -2250,8 +2251,9 @@ static mla_status decode_step(const char* who, const mla_dims* dims, int q_len,
   // The per-step inputs and the output may live in page-locked host memory.
   const void* step_io[5] = {q_nope, q_rope, positions, lengths, out};
   const char* step_io_name[5] = {"q_nope", "q_rope", "positions", "lengths", "out"};
+  int kind[5] = {-1, -1, -1, -1, -1};
   for (int i = 0; i < 5; ++i) {
-    if (step_io[i] && !device_addressable(step_io[i])) {
+    if (step_io[i] && (kind[i] = device_addressable(step_io[i])) == 0) {
       set_error("%s: %s is not memory the device can address (pageable host memory?); use "
                 "device memory or page-locked host memory", who, step_io_name[i]);
       return MLA_ERR_INVALID_ARG;
@@ -2316,7 +2318,7 @@ static mla_status decode_step(const char* who, const mla_dims* dims, int q_len,
   // several waves the early decode CTAs crowd out the previous step's tail
   // (measured: 64 ragged sequences, step 103 -> 122 us with it).
   st = absorb_q(who, &qd, q_nope, q_rope, w_uk, positions, rope_base, q_abs, q_pe, stream, pf,
-                single_wave);
+                single_wave, kind[0] < 0 ? -1 : kind[0] == 2 ? 1 : 0);
   if (st != MLA_OK) return st;
   st = decode_split(who, dims, q_len, q_abs, q_pe, cache, lengths, softmax_scale, num_splits,
                     workspace, ws_bytes, dev_status, stream);

@@ -645,10 +645,22 @@ extern "C" mla_status mla_absorb_q(const mla_dims* dims, const void* q_nope, con
                   stream, none, false);
 }
 
+// theta_i / (2 pi) for `rope_base`, kept per thread for the last base seen
+// (a step's host work is a few microseconds; 32 fp64 powers are a visible part).
+static const RopeTheta& rope_theta(double rope_base) {
+  thread_local double base = 0.0;
+  thread_local RopeTheta th;
+  if (base != rope_base) {
+    for (int i = 0; i < kDr / 2; ++i) th.turns[i] = pow(rope_base, -2.0 * i / kDr) / (2.0 * M_PI);
+    base = rope_base;
+  }
+  return th;
+}
+
 mla_status mla::absorb_q(const char* who, const mla_dims* dims, const void* q_nope,
                          const void* q_rope, const void* w_uk, const int32_t* positions,
                          double rope_base, void* q_abs, void* q_pe, void* stream,
-                         const CachePrefetch& pf, bool early) {
+                         const CachePrefetch& pf, bool early, int q_host) {
   mla_status st = check_dims(dims, who);
   if (st != MLA_OK) return st;
   if (!q_nope || !q_rope || !w_uk || !positions || !q_abs || !q_pe) {
@@ -666,15 +678,14 @@ mla_status mla::absorb_q(const char* who, const mla_dims* dims, const void* q_no
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int B = dims->batch, H = dims->heads;
-  RopeTheta th;
-  for (int i = 0; i < kDr / 2; ++i) th.turns[i] = pow(rope_base, -2.0 * i / kDr) / (2.0 * M_PI);
+  const RopeTheta th = rope_theta(rope_base);
   if (dims->dtype != MLA_F32) {
     const auto* qn = static_cast<const __nv_bfloat16*>(q_nope);
     const auto* qr = static_cast<const __nv_bfloat16*>(q_rope);
     const auto* wk = static_cast<const __nv_bfloat16*>(w_uk);
     auto* qa = static_cast<float*>(q_abs);
     auto* qp = static_cast<float*>(q_pe);
-    if (host_resident(q_nope)) {
+    if (q_host < 0 ? host_resident(q_nope) : q_host == 1) {
       // Queries in host memory: read by fewer CTAs per head, about 64 CTAs in
       // all (one per head from 64 heads up).  Measured end to end, one direct
       // mla_decode_step call per step, against the 32-CTA-per-head form with

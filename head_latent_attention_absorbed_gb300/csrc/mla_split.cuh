@@ -65,9 +65,12 @@ mla_status launch_split_fp8(const SplitParams& p, const void* cache, cudaStream_
 
 // mla_absorb_q's work (named `who` in error messages), with the decode kernel's
 // first cache rows prefetched into L2 when pf.cache is set, and (bf16, `early`)
-// launched with programmatic stream serialization (mla_proj.cu).
+// launched with programmatic stream serialization (mla_proj.cu).  `q_host`:
+// whether q_nope is page-locked host memory, 1 or 0 when the caller knows it,
+// -1 to ask the runtime.
 mla_status absorb_q(const char* who, const mla_dims* dims, const void* q_nope, const void* q_rope,
                     const void* w_uk, const int32_t* positions, double rope_base, void* q_abs,
-                    void* q_pe, void* stream, const CachePrefetch& pf, bool early);
+                    void* q_pe, void* stream, const CachePrefetch& pf, bool early,
+                    int q_host = -1);
 
 }  // namespace mla
