@@ -40,36 +40,16 @@ __device__ __forceinline__ float to_f<float>(float v) { return v; }
 template <>
 __device__ __forceinline__ float to_f<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
-// Pair `it` = (b, i) of head h: the inputs (position and the two values), then
-// the rotation.  The two halves are separate so that a caller can request the
-// inputs early and rotate later.
-struct RopeIn {
-  int32_t pos;
-  float x0, x1;
-};
-
-template <typename T>
-__device__ __forceinline__ RopeIn rope_load(const T* q_rope, const int32_t* positions, int H, int h,
-                                            int it) {
-  const int b = it / (kDr / 2), i = it % (kDr / 2);
-  const size_t off = (size_t(b) * H + h) * kDr + 2 * i;
-  return RopeIn{positions[b], to_f(q_rope[off]), to_f(q_rope[off + 1])};
-}
-
-__device__ __forceinline__ void rope_rotate(const RopeIn& in, const RopeTheta& th, float* q_pe,
-                                            int H, int h, int it) {
-  const int b = it / (kDr / 2), i = it % (kDr / 2);
-  float sn, cs;
-  sincosf(rope_angle(in.pos, th.turns[i]), &sn, &cs);
-  const size_t off = (size_t(b) * H + h) * kDr + 2 * i;
-  q_pe[off] = cs * in.x0 - sn * in.x1;
-  q_pe[off + 1] = sn * in.x0 + cs * in.x1;
-}
-
 template <typename T>
 __device__ __forceinline__ void rope_pair(const T* q_rope, const int32_t* positions,
                                           const RopeTheta& th, float* q_pe, int H, int h, int it) {
-  rope_rotate(rope_load(q_rope, positions, H, h, it), th, q_pe, H, h, it);
+  const int b = it / (kDr / 2), i = it % (kDr / 2);
+  float sn, cs;
+  sincosf(rope_angle(positions[b], th.turns[i]), &sn, &cs);
+  const size_t off = (size_t(b) * H + h) * kDr + 2 * i;
+  const float x0 = to_f(q_rope[off]), x1 = to_f(q_rope[off + 1]);
+  q_pe[off] = cs * x0 - sn * x1;
+  q_pe[off + 1] = sn * x0 + cs * x1;
 }
 
 // ---------------------------------------------------------------------- absorb, bf16
@@ -151,14 +131,8 @@ __global__ void __launch_bounds__(32)
   issue_cache_prefetch(pf, lane * (gridDim.x * gridDim.y) + blockIdx.y * gridDim.x + blockIdx.x,
                        gridDim.x * gridDim.y * 32);
   pdl_wait();
-  // This lane's first RoPE pair (a head has B * 32 pairs and 32 lanes per
-  // column block, so up to 32 sequences it is the lane's only one): its inputs
-  // are requested before the first query tile's, so that the two reads are in
-  // flight together instead of one after the other; the rotation follows the
-  // MMAs.
-  const int rope_it = cb * 32 + lane, rope_n = B * (kDr / 2), rope_step = 32 * gridDim.y;
-  RopeIn rope_first{0, 0.f, 0.f};
-  if (rope_it < rope_n) rope_first = rope_load(q_rope, pos, H, h, rope_it);
+  for (int it = cb * 32 + lane; it < B * (kDr / 2); it += 32 * gridDim.y)
+    rope_pair(q_rope, pos, th, q_pe, H, h, it);
 
   const int gq = lane >> 2, cq = lane & 3;
   const uint32_t wbase = smem_u32(wt);
@@ -200,9 +174,6 @@ __global__ void __launch_bounds__(32)
             make_float2(acc[nb][2], acc[nb][3]);
     }
   }
-  if (rope_it < rope_n) rope_rotate(rope_first, th, q_pe, H, h, rope_it);
-  for (int it = rope_it + rope_step; it < rope_n; it += rope_step)
-    rope_pair(q_rope, pos, th, q_pe, H, h, it);
 }
 
 // Queries in page-locked host memory, read over the host link: a head's
