@@ -156,7 +156,8 @@ def test_separate_calls_multi_token(cuda_lib, dtype):
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
 def test_captured_multi_token_step_from_host_memory(cuda_lib, dtype):
     """DecodeStep.capture with four tokens: the kernels read the pinned host inputs
-    and write o in place; a replay equals the device-resident eager step bit for bit."""
+    and write o in place; a replay and a direct launch equal the device-resident
+    eager step bit for bit."""
     import numpy as np
     import head_latent_attention_absorbed_gb300 as mla
     cfg = small(dtype, 4)
@@ -172,10 +173,15 @@ def test_captured_multi_token_step_from_host_memory(cuda_lib, dtype):
     hs.replay()
     torch.cuda.synchronize()
     got = hs.out.double().numpy().copy()
+    hs.out.fill_(float("nan"))
+    hs.launch()                     # the same step as one direct call
+    torch.cuda.synchronize()
+    launched = hs.out.double().numpy().copy()
     eager = step.run(inp.q_nope.cuda(), inp.q_rope.cuda(), cache, inp.lengths.cuda(),
                      inp.positions.cuda(), w_uk, w_uv)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(got, eager.double().cpu().numpy())
+    np.testing.assert_array_equal(launched, got)
     assert int(step.status.item()) == 0
 
 
